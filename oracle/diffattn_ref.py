@@ -1,0 +1,226 @@
+"""Float64 CPU oracle for differential attention.
+
+TEST INFRASTRUCTURE ONLY. This module is imported by `tests/`, by `__graft_entry__.smoke()` and by
+`bench.py`'s CPU-baseline leg, and by nothing else: the library's product path never calls it and
+shares no code with it (no kernels, headers, helpers or constants). Inputs come from `synth/`.
+
+It is the plain definition of the operator written out in float64 with numpy, one step per
+equation, blocked over query rows only so that memory stays O(rows_per_block x N). No other
+blocking, fusion or reordering is done: every score is formed, every softmax row is normalised,
+the two maps are subtracted and the difference is multiplied by V, in that order.
+
+Sources (page title, section):
+  [P1] "Differential Transformer: Noise-Canceling Attention by Subtraction" -- "The mechanism",
+       "Making lambda learnable and stable".
+  [P3] "Differential Transformer: softmax can't say zero, so it subtracts" -- "The mechanism,
+       exactly" (DiffAttn equation and the quoted MultiheadDiffAttn.forward), "lambda,
+       re-parameterised", "The row no longer sums to one", "DIFF V2: what the authors changed".
+  [P5] "Differential Transformer V2" -- GQA pairing of the subtracted heads.
+
+Readings taken where the pages are silent or disagree (all listed in the design doc as well):
+  * the 1/sqrt(d) scale uses d = width of one query/key half (P1 `d**0.5`, P3 Q_i in R^{N x d});
+  * lambda is one float per head (P1 says per head, P3 says one per layer shared by every head; a
+    per-head array covers both); it is computed and used in full precision, no clipping;
+  * the per-head norm is an RMSNorm over all dv channels of the head, y = o / sqrt(mean(o^2) + eps)
+    * w, then times (1 - lambda_init) (P3 quotes `subln` then `* (1 - lambda_init)`); the
+    GroupNorm "+ lambda_init" form on the Japanese page is treated as garbled;
+  * causal prefill is top-left aligned with Nq = Nk (key j visible to query i iff j <= i); decode
+    attends to every cached key of its row;
+  * V2 pairs heads (2p, 2p+1), uses KV head floor(2p / (Hq/Hkv)), lambda = sigmoid(logit) per
+    token and pair, no per-head norm, and the default 1/sqrt(d) scale.
+
+Parity pins: every function here is pinned by `tests/test_oracle_pins.py` (worked examples printed
+on the pages, closed forms, library routines for special cases, brute force on tiny inputs).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+ROW_BLOCK = 256
+
+
+def _f64(x) -> np.ndarray:
+    """float64 copy of a numpy array or a (CPU) torch tensor, without importing torch."""
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().float().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------------------------
+# lambda  ([P1] "Making lambda learnable and stable"; [P3] "lambda, re-parameterised")
+# --------------------------------------------------------------------------------------------
+
+def lambda_init(layer: int) -> float:
+    """lambda_init(l) = 0.8 - 0.6 * exp(-0.3 * (l - 1)), with l the 1-indexed layer."""
+    return 0.8 - 0.6 * math.exp(-0.3 * (layer - 1))
+
+
+def lambda_full(lq1, lk1, lq2, lk2, layer: int) -> np.ndarray:
+    """lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init(layer), one value per row (head set).
+
+    Vectors are [n_sets, dim] (or [dim]); the dot products run over the last axis.
+    """
+    lq1, lk1, lq2, lk2 = (_f64(t) for t in (lq1, lk1, lq2, lk2))
+    dot1 = np.sum(lq1 * lk1, axis=-1)
+    dot2 = np.sum(lq2 * lk2, axis=-1)
+    return np.exp(dot1) - np.exp(dot2) + lambda_init(layer)
+
+
+# --------------------------------------------------------------------------------------------
+# the two maps and their difference  ([P3] "The mechanism, exactly"; [P1] "The mechanism")
+# --------------------------------------------------------------------------------------------
+
+def softmax_rows(S: np.ndarray) -> np.ndarray:
+    """Row-wise softmax exp(S - rowmax) / sum. -inf entries get weight 0."""
+    m = np.max(S, axis=-1, keepdims=True)
+    e = np.exp(S - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def scores(Q: np.ndarray, K: np.ndarray, row_ids: np.ndarray | None, causal: bool) -> np.ndarray:
+    """S = Q K^T / sqrt(d) with d = Q's width; causal sets S[i, j] = -inf for key j > query i.
+
+    `row_ids` are the absolute query positions of Q's rows (needed for the causal mask).
+    """
+    d = Q.shape[-1]
+    S = (Q @ K.T) / math.sqrt(d)
+    if causal:
+        cols = np.arange(K.shape[0])[None, :]
+        S = np.where(cols > row_ids[:, None], -np.inf, S)
+    return S
+
+
+def diff_weights(S1: np.ndarray, S2: np.ndarray, lam: float) -> np.ndarray:
+    """W = softmax(S1) - lam * softmax(S2): the signed weights of one differential head."""
+    return softmax_rows(S1) - lam * softmax_rows(S2)
+
+
+def diff_attn_head(q1, k1, q2, k2, v, lam: float, causal: bool, rows=None) -> np.ndarray:
+    """DiffAttn for one head: (softmax(Q1 K1^T/sqrt d) - lam softmax(Q2 K2^T/sqrt d)) V.
+
+    q1, q2 [Nq, d]; k1, k2 [Nk, d]; v [Nk, dv]. Returns the rows listed in `rows` (default all),
+    [len(rows), dv], computed ROW_BLOCK query rows at a time.
+    """
+    q1, k1, q2, k2, v = (_f64(t) for t in (q1, k1, q2, k2, v))
+    rows = np.arange(q1.shape[0]) if rows is None else np.asarray(rows)
+    out = np.empty((rows.shape[0], v.shape[1]), dtype=np.float64)
+    for s in range(0, rows.shape[0], ROW_BLOCK):
+        r = rows[s:s + ROW_BLOCK]
+        S1 = scores(q1[r], k1, r, causal)
+        S2 = scores(q2[r], k2, r, causal)
+        out[s:s + ROW_BLOCK] = diff_weights(S1, S2, lam) @ v
+    return out
+
+
+# --------------------------------------------------------------------------------------------
+# per-head norm and fixed rescale  ([P3] "The row no longer sums to one"; [P1] items 1-2)
+# --------------------------------------------------------------------------------------------
+
+def subln(O: np.ndarray, weight, eps: float) -> np.ndarray:
+    """RMSNorm over the last axis: O / sqrt(mean(O^2) + eps) * weight."""
+    O = _f64(O)
+    rms = np.sqrt(np.mean(O * O, axis=-1, keepdims=True) + eps)
+    w = 1.0 if weight is None else _f64(weight)
+    return O / rms * w
+
+
+def head_epilogue(O, weight, eps: float, lam_init: float, norm: bool, apply_scale: bool):
+    """subln (when `norm`) then multiply by (1 - lambda_init) (when `apply_scale`)."""
+    Y = subln(O, weight, eps) if norm else _f64(O)
+    if apply_scale:
+        Y = Y * (1.0 - lam_init)
+    return Y
+
+
+# --------------------------------------------------------------------------------------------
+# the three operator entry points
+# --------------------------------------------------------------------------------------------
+
+def diffattn_fwd(q, k, v, lam, lam_init: float, norm_weight=None, eps: float = 1e-5,
+                 norm: bool = True, apply_scale: bool = True, causal: bool = True, rows=None):
+    """Prefill over the layout q [B,N,H,2d] = [Q1|Q2], k [B,N,H,2d] = [K1|K2], v [B,N,H,dv].
+
+    lam: one value per head ([H]) or a scalar. Returns float64 [B, len(rows), H, dv].
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, N, H, two_d = q.shape
+    d = two_d // 2
+    lam = np.broadcast_to(_f64(lam), (H,))
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    out = np.empty((B, rows.shape[0], H, v.shape[-1]), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            O = diff_attn_head(q[b, :, h, :d], k[b, :, h, :d], q[b, :, h, d:], k[b, :, h, d:],
+                               v[b, :, h, :], float(lam[h]), causal, rows)
+            out[b, :, h, :] = head_epilogue(O, norm_weight, eps, lam_init, norm, apply_scale)
+    return out
+
+
+def diffattn_decode(q, k_cache, v_cache, seqlens, lam, lam_init: float, norm_weight=None,
+                    eps: float = 1e-5, norm: bool = True, apply_scale: bool = True):
+    """One query per sequence over its cached keys 0 .. seqlens[b]-1 (no mask inside that range).
+
+    q [B,H,2d], k_cache [B,L,H,2d], v_cache [B,L,H,dv], seqlens [B]. Returns float64 [B,H,dv].
+    """
+    q = _f64(q)
+    B, H, two_d = q.shape
+    d = two_d // 2
+    lam = np.broadcast_to(_f64(lam), (H,))
+    seqlens = np.asarray(_f64(seqlens)).astype(np.int64)
+    out = np.empty((B, H, v_cache.shape[-1]), dtype=np.float64)
+    for b in range(B):
+        L = int(seqlens[b])
+        kb = _f64(k_cache[b, :L])
+        vb = _f64(v_cache[b, :L])
+        for h in range(H):
+            O = diff_attn_head(q[b, h:h + 1, :d], kb[:, h, :d], q[b, h:h + 1, d:], kb[:, h, d:],
+                               vb[:, h, :], float(lam[h]), causal=False)
+            out[b, h, :] = head_epilogue(O, norm_weight, eps, lam_init, norm, apply_scale)[0]
+    return out
+
+
+def sigmoid(x):
+    x = _f64(x)
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def attention_head(q, k, v, causal: bool, rows=None) -> np.ndarray:
+    """Plain softmax attention softmax(q k^T / sqrt d) v for one head, blocked over rows."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    rows = np.arange(q.shape[0]) if rows is None else np.asarray(rows)
+    out = np.empty((rows.shape[0], v.shape[1]), dtype=np.float64)
+    for s in range(0, rows.shape[0], ROW_BLOCK):
+        r = rows[s:s + ROW_BLOCK]
+        out[s:s + ROW_BLOCK] = softmax_rows(scores(q[r], k, r, causal)) @ v
+    return out
+
+
+def v2_kv_head(p: int, Hq: int, Hkv: int) -> int:
+    """KV head shared by pair p: query heads of one GQA group are contiguous ([P5]), so query head
+    2p belongs to group floor(2p / (Hq / Hkv)); heads 2p and 2p+1 fall in the same group whenever
+    Hq / Hkv is even."""
+    return (2 * p) // (Hq // Hkv)
+
+
+def diffattn_v2_fwd(q, k, v, lam_logit, causal: bool = True, rows=None):
+    """DIFF V2 ([P3] "DIFF V2: what the authors changed"): attention over 2h query heads sharing
+    GQA KV heads, then out_p = attn[2p] - sigmoid(lam[t, p]) * attn[2p+1]; no norm, no lambda_init.
+
+    q [B,N,Hq,d], k, v [B,N,Hkv,d], lam_logit [B,N,Hq/2]. Returns float64 [B, len(rows), Hq/2, d].
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    P = Hq // 2
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    sig = sigmoid(lam_logit)
+    out = np.empty((B, rows.shape[0], P, v.shape[-1]), dtype=np.float64)
+    for b in range(B):
+        for p in range(P):
+            g = v2_kv_head(p, Hq, Hkv)
+            a1 = attention_head(q[b, :, 2 * p], k[b, :, g], v[b, :, g], causal, rows)
+            a2 = attention_head(q[b, :, 2 * p + 1], k[b, :, g], v[b, :, g], causal, rows)
+            out[b, :, p, :] = a1 - sig[b, rows, p][:, None] * a2
+    return out

@@ -1,0 +1,334 @@
+"""Pins for the float64 oracle (CPU only).
+
+Each pin ties an oracle function to something other than the oracle itself: a number printed on
+the pages (fixtures under tests/golden/, each citing its page and section), a closed form, a
+library routine that the method reduces to in a special case, or pure-Python brute force on tiny
+inputs. `test_planted_mistakes_are_caught` plants plausible mistakes in the oracle (on the CPU)
+and checks that at least one pin fails for each.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import diffattn_ref as ref
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _sdpa(q, k, v, causal):
+    """torch's scaled_dot_product_attention in float64 on the CPU (library routine)."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64))
+    return F.scaled_dot_product_attention(t(q)[None], t(k)[None], t(v)[None], is_causal=causal)[0].numpy()
+
+
+def _cummean(v):
+    return np.cumsum(v, axis=0) / np.arange(1, v.shape[0] + 1)[:, None]
+
+
+# ------------------------------------------------------------------------------------------
+# pins (plain functions so the planted-mistake test can run them against a mutated oracle)
+# ------------------------------------------------------------------------------------------
+
+def pin_lambda_init_table():
+    g = _golden("lambda_init_table.json")
+    for l, li, om in zip(g["layers"], g["lambda_init"], g["one_minus_init"]):
+        assert round(ref.lambda_init(l), 2) == pytest.approx(li, abs=1e-9), l
+        assert round(1.0 - ref.lambda_init(l), 2) == pytest.approx(om, abs=1e-9), l
+
+
+def pin_lambda_init_shape():
+    assert ref.lambda_init(1) == pytest.approx(0.2, abs=1e-15)
+    vals = [ref.lambda_init(l) for l in range(1, 60)]
+    assert all(b > a for a, b in zip(vals, vals[1:]))
+    assert vals[-1] == pytest.approx(0.8, abs=1e-6) and vals[-1] < 0.8
+
+
+def pin_lambda_closed_forms():
+    dim = 16
+    z = np.zeros((1, dim))
+    for l in (1, 5, 12):
+        assert ref.lambda_full(z, z, z, z, l)[0] == pytest.approx(ref.lambda_init(l), abs=1e-15)
+    # dot1 = ln 3 and dot2 = ln 2 -> lambda = 3 - 2 + lambda_init; swapping the sets -> 2 - 3.
+    a = np.zeros((1, dim)); a[0, 3] = math.log(3.0)
+    b = np.zeros((1, dim)); b[0, 3] = 1.0
+    c = np.zeros((1, dim)); c[0, 7] = 0.5
+    e = np.zeros((1, dim)); e[0, 7] = 2 * math.log(2.0)
+    li = ref.lambda_init(12)
+    assert ref.lambda_full(a, b, c, e, 12)[0] == pytest.approx(1.0 + li, abs=1e-12)
+    assert ref.lambda_full(c, e, a, b, 12)[0] == pytest.approx(-1.0 + li, abs=1e-12)
+
+
+def pin_lambda_spread():
+    g = _golden("lambda_spread.json")
+    rng = np.random.default_rng(12345)
+    n = 100_000
+    vecs = [rng.standard_normal((n, g["dim"])) * g["vector_std"] for _ in range(4)]
+    lam = ref.lambda_full(*vecs, layer=12)
+    assert np.std(lam) == pytest.approx(g["lambda_std"], abs=2e-3)
+    assert np.mean(lam) == pytest.approx(ref.lambda_init(12), abs=3e-3)
+
+
+def pin_softmax_floor():
+    g = _golden("softmax_floor.json")
+    d = 4
+    for n, Dp in zip(g["n"], g["D_half"]):
+        D = math.log(n - 1)
+        assert round(D, 2) == pytest.approx(Dp, abs=1e-9)
+        # One head, lambda = 0: query 0 sees key 0 at logit D and n-1 keys at logit 0.
+        q = np.zeros((1, d)); q[0, 0] = D * math.sqrt(d)
+        k = np.zeros((n, d)); k[0, 0] = 1.0
+        v = np.zeros((n, 2)); v[0, 0] = 1.0; v[1:, 1] = 1.0
+        o = ref.diff_attn_head(q, k, q, k, v, 0.0, causal=False)
+        assert o[0, 0] == pytest.approx(g["share_at_D_half"], abs=1e-12)
+        assert o[0, 1] == pytest.approx(1.0 - g["share_at_D_half"], abs=1e-12)
+
+
+def pin_toy_needle_table():
+    g = _golden("toy_needle_table.json")
+    lam, gap, sigma, seeds = g["lam"], g["gap"], g["sigma"], g["seeds"]
+
+    def draws(n, rho):
+        z1 = np.empty((seeds, n)); z2 = np.empty((seeds, n))
+        for s in range(seeds):
+            c, e = np.random.default_rng(s).standard_normal((2, n))
+            z1[s] = sigma * c
+            z1[s, 0] += gap
+            z2[s] = sigma * (rho * c + math.sqrt(1 - rho * rho) * e)
+        return z1, z2
+
+    def share(w):
+        return np.mean(np.abs(w[:, 0]) / np.abs(w).sum(axis=1))
+
+    for row in g["rho_sweep_n32"]:
+        z1, z2 = draws(32, row["rho"])
+        single = ref.diff_weights(z1, z2, 0.0)
+        diff = ref.diff_weights(z1, z2, lam)
+        assert round(share(single), 3) == pytest.approx(row["single"], abs=1e-9)
+        assert round(share(diff), 3) == pytest.approx(row["diff"], abs=1e-9)
+        assert round(np.mean(single[:, 0]), 3) == pytest.approx(row["w_single"], abs=1e-9)
+        assert round(np.mean(diff[:, 0]), 3) == pytest.approx(row["w_diff"], abs=1e-9)
+    for row in g["n_sweep_rho09"]:
+        z1, z2 = draws(row["n"], 0.9)
+        assert round(share(ref.diff_weights(z1, z2, 0.0)), 3) == pytest.approx(row["single"], abs=1e-9)
+        assert round(share(ref.diff_weights(z1, z2, lam)), 3) == pytest.approx(row["diff"], abs=1e-9)
+
+
+def pin_worked_example():
+    g = _golden("worked_example_rowsum.json")
+    n, d, lam = g["n"], g["d"], g["lam"]
+    torch.manual_seed(g["seed"])
+    q1, k1, q2, k2 = torch.randn(4, n, d)
+    _v = torch.randn(n, 2 * d)  # drawn to keep the generator sequence of the example
+    S1 = ref.scores(ref._f64(q1), ref._f64(k1), np.arange(n), causal=False)
+    S2 = ref.scores(ref._f64(q2), ref._f64(k2), np.arange(n), causal=False)
+    W = ref.diff_weights(S1, S2, lam)
+    assert f"{W.sum(axis=-1)[0]:.2f}" == g["printed_row_sum"]
+    assert int((W < 0).sum()) == g["printed_negative"] and W.size == g["printed_total"]
+
+
+def pin_row_sums():
+    rng = np.random.default_rng(3)
+    n, d = 37, 8
+    for lam in (0.0, 0.2, 0.8, 1.3):
+        for causal in (False, True):
+            S1 = ref.scores(rng.standard_normal((n, d)), rng.standard_normal((n, d)), np.arange(n), causal)
+            S2 = ref.scores(rng.standard_normal((n, d)), rng.standard_normal((n, d)), np.arange(n), causal)
+            W = ref.diff_weights(S1, S2, lam)
+            assert np.allclose(W.sum(-1), 1.0 - lam, atol=1e-12)
+            if causal:
+                assert np.all(W[np.triu_indices(n, 1)] == 0.0)
+
+
+def pin_lambda_zero_is_softmax_attention():
+    rng = np.random.default_rng(4)
+    for causal in (False, True):
+        n, d, dv = 29, 16, 32
+        q1, k1, q2, k2 = (rng.standard_normal((n, d)) for _ in range(4))
+        v = rng.standard_normal((n, dv))
+        o = ref.diff_attn_head(q1, k1, q2, k2, v, 0.0, causal)
+        assert np.allclose(o, _sdpa(q1, k1, v, causal), atol=1e-12, rtol=0)
+
+
+def pin_equal_maps_scale_attention():
+    rng = np.random.default_rng(5)
+    for causal in (False, True):
+        n, d, dv = 31, 8, 16
+        q, k = rng.standard_normal((n, d)), rng.standard_normal((n, d))
+        v = rng.standard_normal((n, dv))
+        lam = 0.71
+        o = ref.diff_attn_head(q, k, q, k, v, lam, causal)
+        assert np.allclose(o, (1 - lam) * _sdpa(q, k, v, causal), atol=1e-12, rtol=0)
+
+
+def pin_brute_force_tiny():
+    rng = np.random.default_rng(6)
+    n, d, dv, lam = 5, 3, 4, 0.6
+    q1, k1, q2, k2 = (rng.standard_normal((n, d)).tolist() for _ in range(4))
+    v = rng.standard_normal((n, dv)).tolist()
+    for causal in (False, True):
+        expect = []
+        for i in range(n):
+            keys = [j for j in range(n) if (not causal or j <= i)]
+            maps = []
+            for Q, K in ((q1, k1), (q2, k2)):
+                logits = [sum(Q[i][t] * K[j][t] for t in range(d)) / math.sqrt(d) for j in keys]
+                mx = max(logits)
+                ex = [math.exp(x - mx) for x in logits]
+                tot = sum(ex)
+                maps.append([x / tot for x in ex])
+            w = [maps[0][a] - lam * maps[1][a] for a in range(len(keys))]
+            expect.append([sum(w[a] * v[j][c] for a, j in enumerate(keys)) for c in range(dv)])
+        got = ref.diff_attn_head(np.array(q1), np.array(k1), np.array(q2), np.array(k2), np.array(v),
+                                 lam, causal)
+        assert np.allclose(got, np.array(expect), atol=1e-13, rtol=0)
+
+
+def pin_norm_and_scale():
+    rng = np.random.default_rng(7)
+    dv, eps = 256, 1e-5
+    O = rng.standard_normal((9, dv)) * np.array([1e-4, 1e-3, 3e-3, 1e-2, 0.1, 1, 3, 10, 100])[:, None]
+    w = rng.standard_normal(dv)
+    lib = F.rms_norm(torch.from_numpy(O), (dv,), torch.from_numpy(w), eps).numpy()
+    assert np.allclose(ref.subln(O, w, eps), lib, atol=1e-13, rtol=1e-12)
+    li = ref.lambda_init(12)
+    # constant row c: every channel becomes |c| / sqrt(c^2 + eps) * (1 - lambda_init), signed
+    for c in (1e-4, 3e-3, 0.5, -2.0):
+        Y = ref.head_epilogue(np.full((1, dv), c), None, eps, li, norm=True, apply_scale=True)
+        assert np.allclose(Y, np.sign(c) * abs(c) / math.sqrt(c * c + eps) * (1 - li), atol=1e-14, rtol=1e-12)
+    Y0 = ref.head_epilogue(np.zeros((1, dv)), None, eps, li, norm=True, apply_scale=True)
+    assert np.all(Y0 == 0.0)
+
+
+def pin_fwd_layout():
+    """q [B,N,H,2d] = [Q1|Q2]: with Q2 = K2 = 0 map 2 is uniform over the visible keys, so each
+    head's output is SDPA(Q1, K1, V) - lambda_h * running-mean(V), then RMSNorm and the scale."""
+    rng = np.random.default_rng(8)
+    B, N, H, d, dv, eps = 2, 19, 3, 4, 8, 1e-5
+    q = rng.standard_normal((B, N, H, 2 * d)); k = rng.standard_normal((B, N, H, 2 * d))
+    q[..., d:] = 0.0; k[..., d:] = 0.0
+    v = rng.standard_normal((B, N, H, dv))
+    lam = np.array([0.3, 0.55, 0.9])
+    w = rng.standard_normal(dv)
+    li = ref.lambda_init(7)
+    out = ref.diffattn_fwd(q, k, v, lam, li, norm_weight=w, eps=eps, causal=True)
+    for b in range(B):
+        for h in range(H):
+            O = _sdpa(q[b, :, h, :d], k[b, :, h, :d], v[b, :, h], True) - lam[h] * _cummean(v[b, :, h])
+            Y = F.rms_norm(torch.from_numpy(O), (dv,), torch.from_numpy(w), eps).numpy() * (1 - li)
+            assert np.allclose(out[b, :, h], Y, atol=1e-12, rtol=1e-10), (b, h)
+    rows = np.array([0, 5, 18])
+    sub = ref.diffattn_fwd(q, k, v, lam, li, norm_weight=w, eps=eps, causal=True, rows=rows)
+    assert np.array_equal(sub, out[:, rows])
+
+
+def pin_decode_is_last_prefill_row():
+    rng = np.random.default_rng(9)
+    B, L, H, d, dv = 3, 23, 2, 4, 8
+    kc = rng.standard_normal((B, L, H, 2 * d)); vc = rng.standard_normal((B, L, H, dv))
+    q = rng.standard_normal((B, H, 2 * d))
+    lam = np.array([0.4, 0.8]); li = ref.lambda_init(12); seqlens = np.array([23, 1, 11])
+    out = ref.diffattn_decode(q, kc, vc, seqlens, lam, li)
+    for b in range(B):
+        Lb = seqlens[b]
+        qp = rng.standard_normal((1, Lb, H, 2 * d)); qp[0, Lb - 1] = q[b]
+        full = ref.diffattn_fwd(qp, kc[b:b + 1, :Lb], vc[b:b + 1, :Lb], lam, li, causal=True,
+                                rows=np.array([Lb - 1]))
+        assert np.allclose(out[b], full[0, 0], atol=1e-12, rtol=1e-12), b
+
+
+def pin_v2():
+    rng = np.random.default_rng(10)
+    B, N, Hq, Hkv, d = 1, 17, 8, 2, 8
+    q = rng.standard_normal((B, N, Hq, d)); k = rng.standard_normal((B, N, Hkv, d))
+    v = rng.standard_normal((B, N, Hkv, d))
+    # Query heads of one GQA group are contiguous: Hq/Hkv = 4 query heads per KV head, so pairs
+    # 0 and 1 (heads 0..3) use KV head 0 and pairs 2 and 3 (heads 4..7) use KV head 1.
+    expected_group = {0: 0, 1: 0, 2: 1, 3: 1}
+    off = np.full((B, N, Hq // 2), -700.0)  # sigmoid -> 0: plain attention of head 2p
+    out = ref.diffattn_v2_fwd(q, k, v, off, causal=True)
+    for p, g in expected_group.items():
+        assert np.allclose(out[0, :, p], _sdpa(q[0, :, 2 * p], k[0, :, g], v[0, :, g], True), atol=1e-12)
+    q2 = q.copy(); q2[:, :, 1::2] = q2[:, :, 0::2]
+    logit = rng.standard_normal((B, N, Hq // 2))
+    out2 = ref.diffattn_v2_fwd(q2, k, v, logit, causal=False)
+    sig = 1 / (1 + np.exp(-logit))
+    for p, g in expected_group.items():
+        a = _sdpa(q2[0, :, 2 * p], k[0, :, g], v[0, :, g], False)
+        assert np.allclose(out2[0, :, p], (1 - sig[0, :, p])[:, None] * a, atol=1e-12)
+
+
+PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, pin_lambda_spread,
+        pin_softmax_floor, pin_toy_needle_table, pin_worked_example, pin_row_sums,
+        pin_lambda_zero_is_softmax_attention, pin_equal_maps_scale_attention, pin_brute_force_tiny,
+        pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin()
+
+
+# ------------------------------------------------------------------------------------------
+# planted mistakes: each must make at least one pin fail
+# ------------------------------------------------------------------------------------------
+
+def _mutants():
+    orig = {n: getattr(ref, n) for n in ("lambda_init", "lambda_full", "scores", "diff_weights",
+                                         "subln", "head_epilogue", "v2_kv_head", "softmax_rows")}
+
+    def scores_wrong_scale(Q, K, row_ids, causal):
+        return orig["scores"](Q, K, row_ids, causal) * math.sqrt(Q.shape[-1]) / math.sqrt(2 * Q.shape[-1])
+
+    def scores_transposed(Q, K, row_ids, causal):
+        S = (K @ Q.T) if Q.shape[0] == K.shape[0] else (Q @ K.T)
+        S = S / math.sqrt(Q.shape[-1])
+        if causal:
+            S = np.where(np.arange(K.shape[0])[None, :] > row_ids[:, None], -np.inf, S)
+        return S
+
+    def scores_mask_off_by_one(Q, K, row_ids, causal):
+        S = (Q @ K.T) / math.sqrt(Q.shape[-1])
+        if causal:
+            S = np.where(np.arange(K.shape[0])[None, :] >= row_ids[:, None], -np.inf, S)
+            S[:, 0] = np.where(row_ids == 0, 0.0, S[:, 0])
+        return S
+
+    return {
+        "lambda_init sign": ("lambda_init", lambda l: 0.8 - 0.6 * math.exp(0.3 * (l - 1))),
+        "lambda_init index base": ("lambda_init", lambda l: 0.8 - 0.6 * math.exp(-0.3 * l)),
+        "lambda_full plus": ("lambda_full", lambda a, b, c, d, layer: orig["lambda_full"](a, b, c, d, layer)
+                             + 2 * np.exp(np.sum(ref._f64(c) * ref._f64(d), axis=-1))),
+        "scale sqrt(2d)": ("scores", scores_wrong_scale),
+        "scores transposed": ("scores", scores_transposed),
+        "mask off by one": ("scores", scores_mask_off_by_one),
+        "diff plus": ("diff_weights", lambda S1, S2, lam: ref.softmax_rows(S1) + lam * ref.softmax_rows(S2)),
+        "softmax wrong axis": ("softmax_rows", lambda S: np.exp(S) / np.sum(np.exp(S), axis=0, keepdims=True)),
+        "norm without eps": ("subln", lambda O, w, eps: ref._f64(O) / np.sqrt(np.mean(ref._f64(O) ** 2, -1, keepdims=True)) * (1.0 if w is None else ref._f64(w))),
+        "scale 1+lambda_init": ("head_epilogue", lambda O, w, eps, li, norm, apply_scale:
+                                orig["head_epilogue"](O, w, eps, li, norm, False) * ((1 + li) if apply_scale else 1)),
+        "v2 wrong group": ("v2_kv_head", lambda p, Hq, Hkv: p // (Hq // Hkv)),
+    }
+
+
+@pytest.mark.parametrize("name", list(_mutants().keys()))
+def test_planted_mistakes_are_caught(name, monkeypatch):
+    attr, fn = _mutants()[name]
+    monkeypatch.setattr(ref, attr, fn)
+    failed = []
+    for pin in PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin()
+        except (AssertionError, FloatingPointError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"planted mistake '{name}' passed every pin"
