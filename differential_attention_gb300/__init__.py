@@ -1,0 +1,233 @@
+"""Differential attention on GB300 (sm_103a): Python binding of libdiffattn.so.
+
+Every function here has the name of the C entry point it calls (include/diffattn.h) and only
+marshals arguments: torch tensors supply device memory and the current CUDA stream, and all of the
+operator's arithmetic runs in the library's CUDA kernels. There is no CPU or PyTorch fallback; if
+the library has not been built, every call raises.
+
+Layouts (dense, row-major):
+    diffattn_fwd     q, k [B, N, H, 2d] ([Q1|Q2], [K1|K2]), v [B, N, H, 2d]  -> [B, N, H, 2d]
+    diffattn_decode  q [B, H, 2d], k_cache, v_cache [B, L, H, 2d]            -> [B, H, 2d]
+    diffattn_v2_fwd  q [B, N, Hq, d], k, v [B, N, Hkv, d], lam [B, N, Hq/2]  -> [B, N, Hq/2, d]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdiffattn.so")
+
+DIFFATTN_OK = 0
+DIFFATTN_BF16 = 0
+DIFFATTN_FP32 = 1
+DIFFATTN_CAUSAL = 1
+DIFFATTN_NORM = 2
+DIFFATTN_SCALE = 4
+DIFFATTN_CUDA_CORES = 8
+DIFFATTN_SINGLE_PASS = 16
+
+STATUS_NAMES = {0: "OK", -1: "ERR_ARG", -2: "ERR_SHAPE", -3: "ERR_DTYPE", -4: "ERR_ALIGN",
+                -5: "ERR_CUDA", -6: "ERR_TIMEOUT", -7: "ERR_UNSUPPORTED", -8: "ERR_WORKSPACE"}
+
+
+class DiffAttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+_SIGNATURES = {
+    "diffattn_version": (ctypes.c_int, []),
+    "diffattn_last_error_string": (ctypes.c_char_p, []),
+    "diffattn_device_status": (ctypes.c_int, [ctypes.c_void_p]),
+    "diffattn_lambda_init": (ctypes.c_float, [ctypes.c_int]),
+    "diffattn_lambda": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 3
+                        + [ctypes.c_void_p, ctypes.c_void_p]),
+    "diffattn_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_float, ctypes.c_void_p,
+                                                             ctypes.c_float] + [ctypes.c_int] * 7
+                     + [ctypes.c_void_p]),
+    "diffattn_decode_workspace_size": (ctypes.c_int, [ctypes.c_int] * 5
+                                       + [ctypes.POINTER(ctypes.c_size_t)]),
+    "diffattn_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.c_void_p,
+                                                               ctypes.c_float] + [ctypes.c_int] * 7
+                        + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_v2_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 7
+                        + [ctypes.c_void_p]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built with `build()`)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m differential_attention_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def build(force: bool = False) -> str:
+    from .build import build as _build
+    return _build(force=force)
+
+
+def _check(rc: int):
+    if rc != DIFFATTN_OK:
+        msg = lib().diffattn_last_error_string().decode(errors="replace")
+        raise DiffAttnError(rc, msg)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(name, t, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _code(dtype):
+    if dtype == torch.bfloat16:
+        return DIFFATTN_BF16
+    if dtype == torch.float32:
+        return DIFFATTN_FP32
+    raise ValueError(f"unsupported dtype {dtype}")
+
+
+def diffattn_version() -> int:
+    return lib().diffattn_version()
+
+
+def diffattn_device_status(stream=None) -> None:
+    """Synchronise `stream` and raise DiffAttnError if a kernel's bounded wait ran out."""
+    _check(lib().diffattn_device_status(_stream(stream)))
+
+
+def diffattn_lambda_init(layer: int) -> float:
+    return float(lib().diffattn_lambda_init(int(layer)))
+
+
+def diffattn_lambda(lq1, lk1, lq2, lk2, layer: int, out=None, stream=None):
+    """lambda = exp(lq1.lk1) - exp(lq2.lk2) + lambda_init(layer) per row of the [n_sets, dim]
+    fp32 vectors; returns a device fp32 tensor [n_sets]."""
+    for n, t in (("lq1", lq1), ("lk1", lk1), ("lq2", lq2), ("lk2", lk2)):
+        _dev(n, t, torch.float32)
+    if not (lq1.shape == lk1.shape == lq2.shape == lk2.shape) or lq1.dim() != 2:
+        raise ValueError("lambda vectors must all be [n_sets, dim]")
+    n_sets, dim = lq1.shape
+    if out is None:
+        out = torch.empty(n_sets, dtype=torch.float32, device=lq1.device)
+    _dev("out", out, torch.float32)
+    _check(lib().diffattn_lambda(_ptr(lq1), _ptr(lk1), _ptr(lq2), _ptr(lk2), dim, n_sets,
+                                 int(layer), _ptr(out), _stream(stream)))
+    return out
+
+
+def diffattn_fwd(q, k, v, lam, lambda_init: float = 0.0, norm_weight=None, eps: float = 1e-5,
+                 causal: bool = True, norm: bool = True, scale: bool = True,
+                 cuda_cores: bool = False, single_pass: bool = False, out=None, stream=None):
+    """Differential-attention prefill; see include/diffattn.h for the exact semantics."""
+    _dev("q", q)
+    B, N, H, two_d = q.shape
+    d, dv = two_d // 2, v.shape[-1]
+    _dev("k", k, q.dtype)
+    _dev("v", v, q.dtype)
+    if k.shape != q.shape or v.shape[:3] != (B, N, H):
+        raise ValueError("k must match q, and v must be [B, N, H, dv]")
+    _dev("lam", lam, torch.float32)
+    if lam.numel() != H:
+        raise ValueError("lam must hold one value per head")
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if out is None:
+        out = torch.empty((B, N, H, dv), dtype=q.dtype, device=q.device)
+    _dev("out", out, q.dtype)
+    flags = ((DIFFATTN_CAUSAL if causal else 0) | (DIFFATTN_NORM if norm else 0)
+             | (DIFFATTN_SCALE if scale else 0) | (DIFFATTN_CUDA_CORES if cuda_cores else 0)
+             | (DIFFATTN_SINGLE_PASS if single_pass else 0))
+    _check(lib().diffattn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lam), float(lambda_init),
+                              _ptr(norm_weight), float(eps), B, N, H, d, dv, flags,
+                              _code(q.dtype), _stream(stream)))
+    return out
+
+
+def diffattn_decode_workspace_size(B: int, Lmax: int, H: int, d: int = 128, dv: int = 256) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().diffattn_decode_workspace_size(B, Lmax, H, d, dv, ctypes.byref(n)))
+    return int(n.value)
+
+
+def diffattn_decode(q, k_cache, v_cache, lam, lambda_init: float = 0.0, seqlens=None,
+                    norm_weight=None, eps: float = 1e-5, norm: bool = True, scale: bool = True,
+                    workspace=None, out=None, stream=None):
+    """Split-KV decode of one query per sequence against its cache."""
+    _dev("q", q, torch.bfloat16)
+    B, H, two_d = q.shape
+    d = two_d // 2
+    _dev("k_cache", k_cache, torch.bfloat16)
+    _dev("v_cache", v_cache, torch.bfloat16)
+    Lmax, dv = k_cache.shape[1], v_cache.shape[-1]
+    if k_cache.shape != (B, Lmax, H, two_d) or v_cache.shape[:3] != (B, Lmax, H):
+        raise ValueError("caches must be [B, Lmax, H, 2d] and [B, Lmax, H, dv]")
+    _dev("lam", lam, torch.float32)
+    if seqlens is not None:
+        _dev("seqlens", seqlens, torch.int32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    need = diffattn_decode_workspace_size(B, Lmax, H, d, dv)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _dev("workspace", workspace)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    flags = (DIFFATTN_NORM if norm else 0) | (DIFFATTN_SCALE if scale else 0)
+    _check(lib().diffattn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(out),
+                                 _ptr(lam), float(lambda_init), _ptr(norm_weight), float(eps), B,
+                                 Lmax, H, d, dv, flags, DIFFATTN_BF16, _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def diffattn_v2_fwd(q, k, v, lam_logit, causal: bool = True, cuda_cores: bool = False,
+                    single_pass: bool = False, out=None, stream=None):
+    """DIFF V2 pair prefill: attn[2p] - sigmoid(lam_logit) * attn[2p+1] over shared GQA KV."""
+    _dev("q", q)
+    B, N, Hq, d = q.shape
+    _dev("k", k, q.dtype)
+    _dev("v", v, q.dtype)
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, N, Hkv, d]")
+    _dev("lam_logit", lam_logit, torch.float32)
+    if lam_logit.shape != (B, N, Hq // 2):
+        raise ValueError("lam_logit must be [B, N, Hq/2]")
+    if out is None:
+        out = torch.empty((B, N, Hq // 2, d), dtype=q.dtype, device=q.device)
+    _dev("out", out, q.dtype)
+    flags = ((DIFFATTN_CAUSAL if causal else 0) | (DIFFATTN_CUDA_CORES if cuda_cores else 0)
+             | (DIFFATTN_SINGLE_PASS if single_pass else 0))
+    _check(lib().diffattn_v2_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_logit), _ptr(out), B, N, Hq,
+                                 Hkv, d, flags, _code(q.dtype), _stream(stream)))
+    return out

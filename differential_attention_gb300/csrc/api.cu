@@ -1,0 +1,269 @@
+// api.cu -- the extern "C" entry points declared in include/diffattn.h: argument validation,
+// error reporting and dispatch to the kernels. No arithmetic of the operator happens here.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "diffattn.h"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string t_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return code;
+}
+
+int ok() {
+  t_err.clear();
+  return DIFFATTN_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(DIFFATTN_ERR_CUDA, "%s: %s (%d)", what, cudaGetErrorString(e), static_cast<int>(e));
+}
+
+// The kernels are built for sm_103a only.
+int check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3)
+    return fail(DIFFATTN_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                dev, major, minor);
+  return DIFFATTN_OK;
+}
+
+constexpr int kPrefillFlags =
+    DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE | DIFFATTN_CUDA_CORES | DIFFATTN_SINGLE_PASS;
+
+}  // namespace
+
+extern "C" {
+
+DIFFATTN_API int diffattn_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+DIFFATTN_API const char* diffattn_last_error_string(void) { return t_err.c_str(); }
+
+DIFFATTN_API int diffattn_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0, w = 0;
+  e = da::status_prefill_tc(&v);
+  if (e == cudaSuccess) e = da::status_prefill_exact(&w);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  v |= w;
+  if (v != 0) return fail(DIFFATTN_ERR_TIMEOUT, "a bounded wait inside a kernel ran out (status %d)", v);
+  return ok();
+}
+
+DIFFATTN_API float diffattn_lambda_init(int layer) {
+  if (layer < 1) return NAN;
+  return static_cast<float>(0.8 - 0.6 * std::exp(-0.3 * (layer - 1)));
+}
+
+DIFFATTN_API int diffattn_lambda(const float* lq1, const float* lk1, const float* lq2,
+                                 const float* lk2, int dim, int n_sets, int layer,
+                                 float* lambda_out, void* stream) {
+  if (!lq1 || !lk1 || !lq2 || !lk2 || !lambda_out)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_lambda: null pointer");
+  if (layer < 1) return fail(DIFFATTN_ERR_ARG, "diffattn_lambda: layer must be >= 1 (got %d)", layer);
+  if (dim < 1 || dim > 4096 || n_sets < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_lambda: need 1 <= dim <= 4096 and n_sets >= 1");
+  if (!aligned(lq1, 4) || !aligned(lk1, 4) || !aligned(lq2, 4) || !aligned(lk2, 4) ||
+      !aligned(lambda_out, 4))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_lambda: fp32 pointers must be 4-byte aligned");
+  int rc = check_device();
+  if (rc) return rc;
+  cudaError_t e = da::launch_lambda(lq1, lk1, lq2, lk2, dim, n_sets, diffattn_lambda_init(layer),
+                                    lambda_out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_lambda launch");
+  return ok();
+}
+
+static int run_prefill(da::Problem& p, int dtype, const char* name, cudaStream_t s) {
+  const bool simt = (p.flags & DIFFATTN_CUDA_CORES) || dtype == DIFFATTN_FP32;
+  if (simt) {
+    cudaError_t e = da::launch_prefill_simt(p, dtype == DIFFATTN_BF16, s);
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    return ok();
+  }
+  char err[256] = {0};
+  cudaError_t e = (p.flags & DIFFATTN_SINGLE_PASS) ? da::launch_prefill_tc(p, s, err, sizeof(err))
+                                                   : da::launch_prefill_exact(p, s, err, sizeof(err));
+  if (e == cudaErrorNotSupported)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: no tensor-core kernel for dqk=%d dv=%d", name, p.dqk, p.dv);
+  if (err[0]) return fail(DIFFATTN_ERR_CUDA, "%s: %s", name, err);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return ok();
+}
+
+DIFFATTN_API int diffattn_fwd(const void* q, const void* k, const void* v, void* out,
+                              const float* lambda, float lambda_init, const float* norm_weight,
+                              float eps, int B, int N, int H, int d, int dv, int flags, int dtype,
+                              void* stream) {
+  if (!q || !k || !v || !out || !lambda) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd: null pointer");
+  if (flags & ~kPrefillFlags) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd: unknown flag bits 0x%x", flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd: eps must be > 0 with DIFFATTN_NORM");
+  if (dtype != DIFFATTN_BF16 && dtype != DIFFATTN_FP32)
+    return fail(DIFFATTN_ERR_DTYPE, "diffattn_fwd: dtype must be DIFFATTN_BF16 or DIFFATTN_FP32");
+  if (B < 1 || N < 1 || H < 1) return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd: B, N, H must be >= 1");
+  if (!(d == 64 || d == 128) || dv != 2 * d)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd: need d in {64, 128} and dv = 2d (got d=%d dv=%d)", d, dv);
+  const long long tiles = (static_cast<long long>(N) + 127) / 128 * B * H;
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(N) * H > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd: problem too large for one launch");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_fwd: tensors must be 16-byte aligned");
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = N;
+  p.units = H;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_V1;
+  p.q_heads = H;
+  p.kv_heads = H;
+  p.q_cols = 2 * d;
+  p.k_cols = 2 * d;
+  p.group = 1;
+  p.lambda = lambda;
+  p.lam_logit = nullptr;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  return run_prefill(p, dtype, "diffattn_fwd", static_cast<cudaStream_t>(stream));
+}
+
+DIFFATTN_API int diffattn_decode_workspace_size(int B, int Lmax, int H, int d, int dv,
+                                                size_t* bytes) {
+  if (!bytes) return fail(DIFFATTN_ERR_ARG, "diffattn_decode_workspace_size: null pointer");
+  if (B < 1 || Lmax < 1 || H < 1 || d != 128 || dv != 256)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode_workspace_size: need B, Lmax, H >= 1, d = 128, dv = 256");
+  *bytes = da::decode_workspace_bytes(B, Lmax, H, dv);
+  return ok();
+}
+
+DIFFATTN_API int diffattn_decode(const void* q, const void* k_cache, const void* v_cache,
+                                 const int* seqlens, void* out, const float* lambda,
+                                 float lambda_init, const float* norm_weight, float eps, int B,
+                                 int Lmax, int H, int d, int dv, int flags, int dtype,
+                                 void* workspace, size_t ws_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !out || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_decode: null pointer");
+  if (flags & ~(DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_decode: unknown flag bits 0x%x", flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_decode: eps must be > 0 with DIFFATTN_NORM");
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "diffattn_decode: dtype must be DIFFATTN_BF16");
+  if (B < 1 || Lmax < 1 || H < 1 || B > 65535 || H > 65535)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode: need 1 <= B, H <= 65535 and Lmax >= 1");
+  if (d != 128 || dv != 256)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode: need d = 128 and dv = 256 (got d=%d dv=%d)", d, dv);
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || (seqlens && !aligned(seqlens, 4)) ||
+      (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_decode: tensors must be 16-byte aligned");
+  const size_t need = da::decode_workspace_bytes(B, Lmax, H, dv);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(DIFFATTN_ERR_WORKSPACE, "diffattn_decode: need a 256-byte aligned workspace of %zu bytes", need);
+  int rc = check_device();
+  if (rc) return rc;
+  da::DecodeArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.seqlens = seqlens;
+  a.out = out;
+  a.lambda = lambda;
+  a.lambda_init = lambda_init;
+  a.norm_w = norm_weight;
+  a.eps = eps;
+  a.flags = flags;
+  a.B = B;
+  a.Lmax = Lmax;
+  a.H = H;
+  a.d = d;
+  a.dv = dv;
+  a.ws = static_cast<float*>(workspace);
+  cudaError_t e = da::launch_decode(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_decode launch");
+  return ok();
+}
+
+DIFFATTN_API int diffattn_v2_fwd(const void* q, const void* k, const void* v,
+                                 const float* lam_logit, void* out, int B, int N, int Hq, int Hkv,
+                                 int d, int flags, int dtype, void* stream) {
+  if (!q || !k || !v || !lam_logit || !out) return fail(DIFFATTN_ERR_ARG, "diffattn_v2_fwd: null pointer");
+  constexpr int kV2Flags = DIFFATTN_CAUSAL | DIFFATTN_CUDA_CORES | DIFFATTN_SINGLE_PASS;
+  if (flags & ~kV2Flags) return fail(DIFFATTN_ERR_ARG, "diffattn_v2_fwd: unknown flag bits 0x%x", flags);
+  if (dtype != DIFFATTN_BF16 && dtype != DIFFATTN_FP32)
+    return fail(DIFFATTN_ERR_DTYPE, "diffattn_v2_fwd: dtype must be DIFFATTN_BF16 or DIFFATTN_FP32");
+  if (B < 1 || N < 1 || Hq < 2 || Hkv < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_fwd: B, N, Hkv must be >= 1 and Hq >= 2");
+  if (Hq % 2 != 0 || Hq % Hkv != 0 || (Hq / Hkv) % 2 != 0)
+    return fail(DIFFATTN_ERR_SHAPE,
+                "diffattn_v2_fwd: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even (a pair in one GQA group); "
+                "got Hq=%d Hkv=%d", Hq, Hkv);
+  if (!(d == 64 || d == 128)) return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_fwd: need d in {64, 128}");
+  const long long tiles = (static_cast<long long>(N) + 127) / 128 * B * (Hq / 2);
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(N) * Hq > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_fwd: problem too large for one launch");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lam_logit, 4))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_v2_fwd: tensors must be 16-byte aligned");
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = N;
+  p.units = Hq / 2;
+  p.dqk = d;
+  p.dv = d;
+  p.mode = da::MODE_V2;
+  p.q_heads = Hq;
+  p.kv_heads = Hkv;
+  p.q_cols = d;
+  p.k_cols = d;
+  p.group = Hq / Hkv;
+  p.lambda = nullptr;
+  p.lam_logit = lam_logit;
+  p.norm_w = nullptr;
+  p.eps = 0.f;
+  p.lambda_init = 0.f;
+  p.flags = flags & kV2Flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  return run_prefill(p, dtype, "diffattn_v2_fwd", static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

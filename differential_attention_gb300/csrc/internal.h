@@ -1,0 +1,84 @@
+// internal.h -- declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace da {
+
+enum Mode : int { MODE_V1 = 0, MODE_V2 = 1 };
+
+// One prefill problem, in the terms both prefill kernels (tensor-core and CUDA-core) use.
+// A "unit" is one differential head (V1) or one pair of query heads (V2); each unit has two maps
+// r = 0, 1 whose queries/keys are located by the helpers below.
+//   V1: q [B,N,H,2d], k [B,N,H,2d], v [B,N,H,dv]; map r uses columns [r*d, r*d + d) of head h.
+//   V2: q [B,N,Hq,d], k/v [B,N,Hkv,d]; map r uses query head 2p + r and KV head 2p / (Hq/Hkv).
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  int B, N;
+  int units;        // V1: H;  V2: Hq / 2
+  int dqk, dv;      // query/key width of one map, value width
+  int mode;
+  int q_heads;      // heads in the q tensor (V1: H, V2: Hq)
+  int kv_heads;     // heads in the k/v tensors (V1: H, V2: Hkv)
+  int q_cols;       // elements per (token, head) row of q (V1: 2d, V2: d)
+  int k_cols;       // same for k
+  int group;        // V2: Hq / Hkv (query heads per KV head); V1: 1
+  const float* lambda;     // V1: [H]
+  const float* lam_logit;  // V2: [B, N, Hq/2]
+  const float* norm_w;     // [dv] or null (weight 1)
+  float eps;
+  float lambda_init;
+  int flags;
+  float scale;             // 1 / sqrt(dqk)
+};
+
+__host__ __device__ inline int q_head_of(const Problem& p, int u, int r) {
+  return p.mode == MODE_V1 ? u : 2 * u + r;
+}
+__host__ __device__ inline int q_col_of(const Problem& p, int r) {
+  return p.mode == MODE_V1 ? r * p.dqk : 0;
+}
+__host__ __device__ inline int kv_head_of(const Problem& p, int u) {
+  return p.mode == MODE_V1 ? u : (2 * u) / p.group;
+}
+__host__ __device__ inline int k_col_of(const Problem& p, int r) {
+  return p.mode == MODE_V1 ? r * p.dqk : 0;
+}
+
+// Launchers. Each returns cudaSuccess or the launch error; `is_bf16` selects the storage type.
+cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                          int dim, int n_sets, float lambda_init, float* out, cudaStream_t s);
+cudaError_t launch_prefill_simt(const Problem& p, bool is_bf16, cudaStream_t s);
+// Tensor-core prefill (bf16). Returns cudaErrorNotSupported for shapes it does not cover.
+cudaError_t launch_prefill_tc(const Problem& p, cudaStream_t s, char* err, size_t err_len);
+
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int* seqlens;
+  void* out;
+  const float* lambda;
+  float lambda_init;
+  const float* norm_w;
+  float eps;
+  int flags;
+  int B, Lmax, H, d, dv;
+  float* ws;
+};
+int decode_splits(int B, int Lmax, int H, int* chunk_out);
+size_t decode_workspace_bytes(int B, int Lmax, int H, int dv);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// Two-pass tensor-core prefill (A1 - lambda A2 formed in fp32 before rounding).
+cudaError_t launch_prefill_exact(const Problem& p, cudaStream_t s, char* err, size_t err_len);
+
+// Read and clear the device status word of a tensor-core prefill translation unit.
+cudaError_t status_prefill_tc(int* v);
+cudaError_t status_prefill_exact(int* v);
+
+}  // namespace da

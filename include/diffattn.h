@@ -1,0 +1,173 @@
+/*
+ * diffattn.h -- C ABI of the GB300 (sm_103a) differential-attention library (libdiffattn.so).
+ *
+ * The operator (page "Differential Transformer: softmax can't say zero, so it subtracts",
+ * section "The mechanism, exactly", DiffAttn equation and the quoted MultiheadDiffAttn.forward):
+ *
+ *   DiffAttn = ( softmax(Q1 K1^T / sqrt(d)) - lambda * softmax(Q2 K2^T / sqrt(d)) ) V
+ *
+ * with V of width dv = 2d shared by both maps, followed per head by an RMSNorm over the dv
+ * channels and a fixed multiply by (1 - lambda_init) (same page, section "The row no longer sums
+ * to one"; page "Differential Transformer: Noise-Canceling Attention by Subtraction", section
+ * "Making lambda learnable and stable").
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named "device" are caller-owned CUDA device memory; the library never allocates
+ *     and never frees them. Host pointers are named "host".
+ *   - Tensors are dense row-major with the layout given at each call (last dimension contiguous,
+ *     no padding between rows). Every tensor pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (CUstream) passed as void*; NULL means the legacy default stream.
+ *     Calls are asynchronous on that stream: a return of DIFFATTN_OK means the work was enqueued.
+ *   - Every call returns 0 (DIFFATTN_OK) or a negative diffattn_status. Argument checks happen
+ *     before anything is enqueued; on error nothing is launched and diffattn_last_error_string()
+ *     (thread-local) describes the failure. Input values are not inspected: NaN/Inf propagate.
+ *   - Kernels never trap. Every wait inside a kernel is bounded; a wait that runs out sets a
+ *     device error flag and the kernel returns early, leaving the output undefined. Read the flag
+ *     with diffattn_device_status().
+ */
+#ifndef DIFFATTN_H_
+#define DIFFATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DIFFATTN_API __attribute__((visibility("default")))
+
+typedef enum {
+  DIFFATTN_OK = 0,
+  DIFFATTN_ERR_ARG = -1,         /* null pointer, bad scalar or flag */
+  DIFFATTN_ERR_SHAPE = -2,       /* unsupported or inconsistent sizes */
+  DIFFATTN_ERR_DTYPE = -3,       /* dtype not supported by this entry point */
+  DIFFATTN_ERR_ALIGN = -4,       /* a pointer is not 16-byte aligned */
+  DIFFATTN_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed (message has the code) */
+  DIFFATTN_ERR_TIMEOUT = -6,     /* a kernel's bounded wait ran out (see diffattn_device_status) */
+  DIFFATTN_ERR_UNSUPPORTED = -7, /* device is not sm_103 / sm_100 family */
+  DIFFATTN_ERR_WORKSPACE = -8    /* workspace missing or smaller than *_workspace_size */
+} diffattn_status;
+
+typedef enum { DIFFATTN_BF16 = 0, DIFFATTN_FP32 = 1 } diffattn_dtype;
+
+/* flags */
+#define DIFFATTN_CAUSAL 1 /* key j visible to query i iff j <= i (prefill, Nq = Nk, top-left) */
+#define DIFFATTN_NORM 2   /* per-head RMSNorm over the dv channels: o / sqrt(mean(o^2) + eps) * w */
+#define DIFFATTN_SCALE 4  /* multiply the (normed) head output by (1 - lambda_init) */
+#define DIFFATTN_CUDA_CORES 8 /* prefill only: take the CUDA-core path (fp32 math, exact row
+                                 statistics per map) instead of the tensor cores; for cross-checks */
+#define DIFFATTN_SINGLE_PASS 16 /* prefill only: one flash pass per map on the tensor cores, each
+   map's probabilities rounded to bf16 before the product with V (the numerics of running a flash
+   kernel once per map and subtracting). Fewer exponentials, but when the two maps are close its
+   error relative to the output grows like 2^-9 / |1 - lambda|. The default tensor-core path finds
+   each map's exact row statistics first and rounds A1 - lambda A2 once, after the subtraction. */
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+DIFFATTN_API int diffattn_version(void);
+
+/* Thread-local description of the last error returned on this thread ("" if none). The string is
+ * owned by the library and valid until the next call on the same thread. */
+DIFFATTN_API const char* diffattn_last_error_string(void);
+
+/* Synchronises `stream`, then reads and clears the device error flag that bounded waits set.
+ * Returns DIFFATTN_OK, DIFFATTN_ERR_TIMEOUT (a wait ran out since the last call), or
+ * DIFFATTN_ERR_CUDA. */
+DIFFATTN_API int diffattn_device_status(void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * lambda
+ * Page "Differential Transformer: softmax can't say zero, so it subtracts", section "lambda,
+ * re-parameterised": lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init, with
+ * lambda_init(l) = 0.8 - 0.6 * exp(-0.3 * (l - 1)) for the 1-indexed layer l (also page
+ * "Differential Transformer: Noise-Canceling Attention by Subtraction", section "Making lambda
+ * learnable and stable").
+ * ------------------------------------------------------------------------------------------ */
+
+/* lambda_init for 1-indexed layer `layer` (>= 1). Host function; returns NaN for layer < 1. */
+DIFFATTN_API float diffattn_lambda_init(int layer);
+
+/* lambda for `n_sets` independent sets of four vectors.
+ *   lq1, lk1, lq2, lk2 : device fp32 [n_sets, dim] each
+ *   lambda_out         : device fp32 [n_sets]
+ * The dot products and exponentials are taken in fp32. One set per layer (shared by every head)
+ * is the page's reading; pass n_sets = H for one lambda per head.
+ * Errors: ERR_ARG (null pointer, layer < 1), ERR_SHAPE (dim < 1 or > 4096, n_sets < 1). */
+DIFFATTN_API int diffattn_lambda(const float* lq1, const float* lk1, const float* lq2,
+                                 const float* lk2, int dim, int n_sets, int layer,
+                                 float* lambda_out, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Prefill: DiffAttn over N tokens (causal or full), then the per-head epilogue.
+ *   q      : device [B, N, H, 2d]  = [Q1 | Q2] per head
+ *   k      : device [B, N, H, 2d]  = [K1 | K2] per head
+ *   v      : device [B, N, H, dv]  (dv = 2d: one V shared by both maps)
+ *   out    : device [B, N, H, dv]  (same dtype as the inputs)
+ *   lambda : device fp32 [H]       (broadcast one value to all heads for one lambda per layer)
+ *   lambda_init : used only with DIFFATTN_SCALE
+ *   norm_weight : device fp32 [dv], or NULL for weight 1 (used only with DIFFATTN_NORM)
+ *   eps    : RMSNorm epsilon (> 0 with DIFFATTN_NORM)
+ *   flags  : DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE, optionally DIFFATTN_CUDA_CORES
+ *            or DIFFATTN_SINGLE_PASS
+ *   dtype  : DIFFATTN_BF16 (tensor-core path, fp32 accumulation and softmax) or DIFFATTN_FP32
+ *            (CUDA-core fp32 path)
+ * Supported: d in {64, 128}, dv = 2d, N >= 1, B, H >= 1. The 1/sqrt(d) scale uses d = width of
+ * one query/key half.
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_fwd(const void* q, const void* k, const void* v, void* out,
+                              const float* lambda, float lambda_init, const float* norm_weight,
+                              float eps, int B, int N, int H, int d, int dv, int flags, int dtype,
+                              void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Decode: one query per sequence against its KV cache, split over the cache length and merged.
+ * Page "Differential Transformer V2": V1 decoding with stock kernels loads the value cache twice;
+ * this call reads every cached K and V element once for both maps.
+ *   q       : device [B, H, 2d]          = [Q1 | Q2]
+ *   k_cache : device [B, Lmax, H, 2d]    = [K1 | K2]
+ *   v_cache : device [B, Lmax, H, dv]
+ *   seqlens : device int32 [B], 1 <= seqlens[b] <= Lmax (keys 0 .. seqlens[b]-1 are attended,
+ *             no mask inside that range), or NULL for Lmax everywhere. Values are not checked on
+ *             the host; an entry outside [1, Lmax] is clamped into it on the device.
+ *   out     : device [B, H, dv]
+ *   lambda  : device fp32 [H];  lambda_init, norm_weight, eps, flags: as for diffattn_fwd
+ *             (DIFFATTN_CAUSAL is ignored)
+ *   workspace, ws_bytes : device scratch of at least diffattn_decode_workspace_size() bytes,
+ *             256-byte aligned; contents need not be initialised. It must not be shared with a
+ *             call that can run at the same time.
+ * Supported: dtype DIFFATTN_BF16, d = 128, dv = 256.
+ * Errors: as diffattn_fwd, plus ERR_WORKSPACE.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_decode_workspace_size(int B, int Lmax, int H, int d, int dv,
+                                                size_t* bytes);
+DIFFATTN_API int diffattn_decode(const void* q, const void* k_cache, const void* v_cache,
+                                 const int* seqlens, void* out, const float* lambda,
+                                 float lambda_init, const float* norm_weight, float eps, int B,
+                                 int Lmax, int H, int d, int dv, int flags, int dtype,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * DIFF V2 prefill (page "Differential Transformer: softmax can't say zero, so it subtracts",
+ * section "DIFF V2: what the authors changed"; page "Differential Transformer V2"): softmax
+ * attention of 2h query heads over GQA KV heads, then out_p = attn[2p] - sigmoid(lam) * attn[2p+1]
+ * per token and pair; no per-head norm and no lambda_init.
+ *   q         : device [B, N, Hq, d]; pair p = query heads (2p, 2p+1)
+ *   k, v      : device [B, N, Hkv, d]; query heads of one GQA group are contiguous, so pair p
+ *               reads KV head floor(2p / (Hq / Hkv))
+ *   lam_logit : device fp32 [B, N, Hq/2], the value before the sigmoid
+ *   out       : device [B, N, Hq/2, d]
+ *   flags     : DIFFATTN_CAUSAL or 0, optionally DIFFATTN_CUDA_CORES or DIFFATTN_SINGLE_PASS
+ * Supported: dtype DIFFATTN_BF16, d in {64, 128}, Hq even, Hq % Hkv == 0 and (Hq / Hkv) even (the
+ * two heads of a pair must sit in one GQA group). The scale is 1/sqrt(d).
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_v2_fwd(const void* q, const void* k, const void* v,
+                                 const float* lam_logit, void* out, int B, int N, int Hq, int Hkv,
+                                 int d, int flags, int dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIFFATTN_H_ */

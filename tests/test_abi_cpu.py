@@ -1,0 +1,126 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol that include/diffattn.h
+declares, and rejects bad arguments with the documented status codes before touching a device.
+Pointers passed here are never dereferenced (validation is pure arithmetic on the host)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import differential_attention_gb300 as da
+from oracle import diffattn_ref as ref
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "diffattn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    da.build()
+    return da.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"DIFFATTN_API\s+[\w\s\*]+?\b(diffattn_\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_symbols())
+    for n in ("diffattn_lambda", "diffattn_fwd", "diffattn_decode", "diffattn_v2_fwd",
+              "diffattn_decode_workspace_size", "diffattn_last_error_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_only_declared_symbols_are_exported():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", da.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    ours = {s for s in exported if s.startswith("diffattn_")}
+    assert ours == set(declared_symbols())
+
+
+def test_version(L):
+    assert da.diffattn_version() >= 10000
+
+
+def test_lambda_init_host_function_matches_oracle(L):
+    for layer in (1, 2, 4, 8, 12, 16, 24, 28, 100):
+        assert da.diffattn_lambda_init(layer) == pytest.approx(ref.lambda_init(layer), rel=1e-6, abs=1e-7)
+    assert math.isnan(da.diffattn_lambda_init(0))
+
+
+FAKE = ctypes.c_void_p(0x10000)     # 16-byte aligned, never dereferenced
+ODD = ctypes.c_void_p(0x10008)      # 8-byte aligned only
+
+
+def _fwd(L, q=FAKE, k=FAKE, v=FAKE, out=FAKE, lam=FAKE, B=1, N=16, H=1, d=128, dv=256, flags=7,
+         dtype=0, eps=1e-5):
+    return L.diffattn_fwd(q, k, v, out, lam, 0.5, None, eps, B, N, H, d, dv, flags, dtype, None)
+
+
+def test_fwd_validation(L):
+    assert _fwd(L, q=None) == -1
+    assert _fwd(L, flags=64) == -1
+    assert _fwd(L, eps=0.0) == -1
+    assert _fwd(L, dtype=7) == -3
+    assert _fwd(L, N=0) == -2
+    assert _fwd(L, d=96, dv=192) == -2
+    assert _fwd(L, d=128, dv=128) == -2
+    assert _fwd(L, q=ODD) == -4
+    assert "aligned" in L.diffattn_last_error_string().decode()
+
+
+def test_decode_validation(L):
+    n = ctypes.c_size_t(0)
+    assert L.diffattn_decode_workspace_size(64, 32768, 12, 128, 256, ctypes.byref(n)) == 0
+    need = n.value
+    assert need > 0 and need % 16 == 0
+    assert L.diffattn_decode_workspace_size(1, 0, 1, 128, 256, ctypes.byref(n)) == -2
+    assert L.diffattn_decode_workspace_size(1, 10, 1, 64, 128, ctypes.byref(n)) == -2
+
+    def dec(ws=FAKE, ws_bytes=need, d=128, dv=256, dtype=0, q=FAKE, flags=6):
+        return L.diffattn_decode(q, FAKE, FAKE, None, FAKE, FAKE, 0.5, None, 1e-5, 64, 32768, 12,
+                                 d, dv, flags, dtype, ws, ws_bytes, None)
+
+    assert dec(q=None) == -1
+    assert dec(flags=16) == -1
+    assert dec(dtype=1) == -3
+    assert dec(d=64, dv=128) == -2
+    assert dec(ws=None) == -8
+    assert dec(ws_bytes=need - 1) == -8
+    assert dec(ws=ctypes.c_void_p(0x10010)) == -8  # not 256-byte aligned
+
+
+def test_v2_validation(L):
+    def v2(Hq=64, Hkv=8, d=128, dtype=0, flags=1, q=FAKE):
+        return L.diffattn_v2_fwd(q, FAKE, FAKE, FAKE, FAKE, 2, 64, Hq, Hkv, d, flags, dtype, None)
+
+    assert v2(q=None) == -1
+    assert v2(flags=2) == -1
+    assert v2(Hq=63) == -2
+    assert v2(Hq=64, Hkv=64) == -2   # Hq/Hkv = 1: a pair would straddle two GQA groups
+    assert v2(Hq=48, Hkv=16) == -2   # Hq/Hkv = 3
+    assert v2(Hq=64, Hkv=7) == -2
+    assert v2(d=96) == -2
+    assert v2(dtype=5) == -3
+
+
+def test_lambda_validation(L):
+    assert L.diffattn_lambda(None, FAKE, FAKE, FAKE, 128, 1, 12, FAKE, None) == -1
+    assert L.diffattn_lambda(FAKE, FAKE, FAKE, FAKE, 128, 1, 0, FAKE, None) == -1
+    assert L.diffattn_lambda(FAKE, FAKE, FAKE, FAKE, 0, 1, 12, FAKE, None) == -2
+    assert L.diffattn_lambda(FAKE, FAKE, FAKE, FAKE, 128, 0, 12, FAKE, None) == -2
+
+
+def test_binding_requires_cuda_tensors():
+    import torch
+    q = torch.zeros(1, 8, 1, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        da.diffattn_fwd(q, q, q, torch.zeros(1), 0.5)

@@ -1,0 +1,239 @@
+"""GPU parity: every entry point, called through the C ABI (Python ctypes binding), against the
+float64 oracle on identical seeded inputs. Small cases are compared on every output element;
+full-size workloads on sampled rows / sequences (same launch configuration as the bench)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import differential_attention_gb300 as da
+from oracle import diffattn_ref as ref
+from synth import (make_decode_inputs, make_lambda_vectors, make_prefill_inputs, make_tiny_inputs,
+                   make_v2_inputs)
+from tests.gpu_util import assert_bf16, assert_fp32, errors
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    da.build()
+    da.lib()
+    yield
+    da.diffattn_device_status()
+
+
+def _lam_for(inp, H):
+    lam = ref.lambda_full(*inp.lam_vectors, layer=inp.layer)  # one lambda per layer
+    return np.full(H, float(lam[0]))
+
+
+# ------------------------------------------------------------------------------------------
+# lambda
+# ------------------------------------------------------------------------------------------
+def test_lambda_kernel():
+    vecs = make_lambda_vectors(128, seed=3, n_sets=12)
+    for layer in (1, 12, 24):
+        got = da.diffattn_lambda(*(v.to(DEV) for v in vecs), layer=layer)
+        want = ref.lambda_full(*vecs, layer=layer)
+        assert np.allclose(got.cpu().numpy(), want, rtol=1e-5, atol=1e-6)
+
+
+# ------------------------------------------------------------------------------------------
+# tiny fp32 workload (CUDA-core path) and its invariant variants
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("variant", ["lam0.8", "lam0", "equal_maps"])
+def test_tiny_fp32(variant):
+    inp = make_tiny_inputs(seed=0)
+    q, k, v = inp.q.clone(), inp.k.clone(), inp.v
+    lam = 0.0 if variant == "lam0" else inp.lam_fixed
+    if variant == "equal_maps":
+        q[..., 64:] = q[..., :64]
+        k[..., 64:] = k[..., :64]
+    lam_t = torch.tensor([lam], dtype=torch.float32, device=DEV)
+    got = da.diffattn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), lam_t, 0.0, causal=False, norm=False,
+                          scale=False)
+    want = ref.diffattn_fwd(q, k, v, [lam], 0.0, norm=False, apply_scale=False, causal=False)
+    assert_fp32(got, want)
+
+
+# ------------------------------------------------------------------------------------------
+# bf16 prefill, tensor-core path, small shapes spanning several tiles and ragged tails
+# ------------------------------------------------------------------------------------------
+PREFILL_CASES = [
+    # (B, N, H, d, causal)
+    (1, 1, 1, 128, True),
+    (2, 77, 3, 128, True),
+    (1, 128, 2, 128, True),
+    (2, 300, 2, 128, True),
+    (1, 645, 2, 128, True),
+    (2, 300, 2, 128, False),
+    (1, 129, 1, 128, False),
+    (2, 200, 2, 64, True),
+    (1, 333, 3, 64, False),
+]
+
+
+@pytest.mark.parametrize("B,N,H,d,causal", PREFILL_CASES)
+def test_prefill_tc_small(B, N, H, d, causal):
+    inp = make_prefill_inputs(B, N, H, d, 2 * d, seed=11 + N, layer=12, causal=causal)
+    lam = _lam_for(inp, H)
+    li = ref.lambda_init(inp.layer)
+    w = torch.linspace(0.5, 1.5, 2 * d, dtype=torch.float32)
+    got = da.diffattn_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV),
+                          torch.tensor(lam, dtype=torch.float32, device=DEV), li,
+                          norm_weight=w.to(DEV), causal=causal)
+    want = ref.diffattn_fwd(inp.q, inp.k, inp.v, lam, li, norm_weight=w, causal=causal)
+    assert_bf16(got, want)
+    da.diffattn_device_status()
+
+
+@pytest.mark.parametrize("B,N,H,d,causal", [(2, 300, 2, 128, True), (1, 200, 2, 64, False)])
+def test_prefill_cuda_core_path_bf16(B, N, H, d, causal):
+    inp = make_prefill_inputs(B, N, H, d, 2 * d, seed=5, layer=12, causal=causal)
+    lam = _lam_for(inp, H)
+    li = ref.lambda_init(inp.layer)
+    got = da.diffattn_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV),
+                          torch.tensor(lam, dtype=torch.float32, device=DEV), li, causal=causal,
+                          cuda_cores=True)
+    want = ref.diffattn_fwd(inp.q, inp.k, inp.v, lam, li, causal=causal)
+    assert_bf16(got, want)
+
+
+def test_prefill_needle_rescale():
+    """A key whose logit against the last query is raised by ln(N-1): the running max jumps late
+    in the row, which exercises the rescale of the accumulator."""
+    inp = make_prefill_inputs(1, 1000, 2, 128, 256, seed=21, layer=24, needle=True)
+    lam = _lam_for(inp, 2)
+    li = ref.lambda_init(24)
+    got = da.diffattn_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV),
+                          torch.tensor(lam, dtype=torch.float32, device=DEV), li)
+    want = ref.diffattn_fwd(inp.q, inp.k, inp.v, lam, li)
+    assert_bf16(got, want)
+
+
+def test_prefill_large_logits_rescale():
+    """Logits of several units (inputs scaled by 4): the max moves by more than the rescale
+    threshold across tiles."""
+    g = torch.Generator().manual_seed(77)
+    B, N, H, d = 1, 700, 2, 128
+    q = (torch.randn(B, N, H, 2 * d, generator=g) * 1.5).to(torch.bfloat16)
+    k = (torch.randn(B, N, H, 2 * d, generator=g) * 1.5).to(torch.bfloat16)
+    v = torch.randn(B, N, H, 2 * d, generator=g).to(torch.bfloat16)
+    lam = np.array([0.3, 0.6])
+    got = da.diffattn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), torch.tensor(lam, dtype=torch.float32, device=DEV), 0.5)
+    want = ref.diffattn_fwd(q, k, v, lam, 0.5)
+    assert_bf16(got, want)
+
+
+@pytest.mark.parametrize("lam", [0.0, 0.5, 1.2])
+def test_prefill_lambda_values(lam):
+    inp = make_prefill_inputs(1, 256, 2, 128, 256, seed=31, layer=12)
+    li = ref.lambda_init(12)
+    lam_v = np.array([lam, lam])
+    got = da.diffattn_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV),
+                          torch.tensor(lam_v, dtype=torch.float32, device=DEV), li)
+    want = ref.diffattn_fwd(inp.q, inp.k, inp.v, lam_v, li)
+    assert_bf16(got, want)
+
+
+def test_prefill_no_norm_no_scale():
+    inp = make_prefill_inputs(1, 200, 2, 128, 256, seed=41, layer=3)
+    lam = _lam_for(inp, 2)
+    got = da.diffattn_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV),
+                          torch.tensor(lam, dtype=torch.float32, device=DEV), 0.3, norm=False,
+                          scale=False)
+    want = ref.diffattn_fwd(inp.q, inp.k, inp.v, lam, 0.3, norm=False, apply_scale=False)
+    assert_bf16(got, want, abs_tol=3e-2)
+
+
+def test_prefill_output_guard_band():
+    """Nothing is written outside the output tensor (guard bands on both sides stay intact)."""
+    inp = make_prefill_inputs(1, 150, 2, 128, 256, seed=51)
+    lam = _lam_for(inp, 2)
+    n = inp.q.numel()
+    buf = torch.full((n + 2 * 4096,), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = buf[4096:4096 + n].view(1, 150, 2, 256)
+    da.diffattn_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV),
+                    torch.tensor(lam, dtype=torch.float32, device=DEV), 0.5, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:4096] == 7.0) and torch.all(buf[4096 + n:] == 7.0)
+
+
+# ------------------------------------------------------------------------------------------
+# decode
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("B,L,H,ragged", [(3, 700, 2, True), (2, 1, 1, False), (2, 5000, 3, False),
+                                          (4, 3001, 2, True)])
+def test_decode_small(B, L, H, ragged):
+    inp = make_decode_inputs(B, L, H, 128, 256, seed=61 + L, ragged=ragged)
+    li = ref.lambda_init(inp.layer)
+    w = torch.linspace(0.8, 1.2, 256, dtype=torch.float32)
+    got = da.diffattn_decode(inp.q.to(DEV), inp.k_cache.to(DEV), inp.v_cache.to(DEV),
+                             inp.lam.to(DEV), li, seqlens=inp.seqlens.to(DEV),
+                             norm_weight=w.to(DEV))
+    want = ref.diffattn_decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, inp.lam, li,
+                               norm_weight=w)
+    assert_bf16(got, want)
+
+
+def test_decode_matches_prefill_last_row():
+    """Decode of query row L-1 over L cached keys equals row L-1 of the causal prefill."""
+    pin = make_prefill_inputs(1, 384, 2, 128, 256, seed=71)
+    lam = torch.tensor([0.4, 0.7], dtype=torch.float32, device=DEV)
+    q, k, v = pin.q.to(DEV), pin.k.to(DEV), pin.v.to(DEV)
+    pre = da.diffattn_fwd(q, k, v, lam, 0.5)
+    dec = da.diffattn_decode(q[:, -1].contiguous(), k, v, lam, 0.5)
+    max_abs, rel = errors(dec, pre[:, -1])
+    assert rel < 2e-2 and max_abs < 4e-2
+
+
+# ------------------------------------------------------------------------------------------
+# V2
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("B,N,Hq,Hkv,d,causal", [(2, 300, 8, 2, 128, True), (1, 129, 4, 2, 128, False),
+                                                 (1, 200, 8, 4, 64, True), (1, 1, 2, 1, 128, True)])
+def test_v2_small(B, N, Hq, Hkv, d, causal):
+    inp = make_v2_inputs(B, N, Hq, Hkv, d, seed=81 + N, causal=causal)
+    got = da.diffattn_v2_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.lam_logit.to(DEV),
+                             causal=causal)
+    want = ref.diffattn_v2_fwd(inp.q, inp.k, inp.v, inp.lam_logit, causal=causal)
+    assert_bf16(got, want)
+
+
+def test_v2_cuda_core_path():
+    inp = make_v2_inputs(1, 150, 8, 2, 128, seed=91)
+    got = da.diffattn_v2_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.lam_logit.to(DEV),
+                             cuda_cores=True)
+    want = ref.diffattn_v2_fwd(inp.q, inp.k, inp.v, inp.lam_logit)
+    assert_bf16(got, want)
+
+
+# ------------------------------------------------------------------------------------------
+# opt-in single-pass tensor-core path (bf16 probabilities per map): parity where the problem is
+# well conditioned (lambda away from 1); its error grows like 2^-9 / |1 - lambda|.
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("B,N,H,d,causal", [(2, 300, 2, 128, True), (1, 645, 2, 128, True),
+                                            (1, 200, 2, 64, False)])
+def test_prefill_single_pass(B, N, H, d, causal):
+    inp = make_prefill_inputs(B, N, H, d, 2 * d, seed=11 + N, layer=12, causal=causal)
+    lam = np.full(H, 0.6)
+    li = ref.lambda_init(12)
+    got = da.diffattn_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV),
+                          torch.tensor(lam, dtype=torch.float32, device=DEV), li, causal=causal,
+                          single_pass=True)
+    want = ref.diffattn_fwd(inp.q, inp.k, inp.v, lam, li, causal=causal)
+    assert_bf16(got, want)
+
+
+def test_v2_single_pass():
+    inp = make_v2_inputs(2, 300, 8, 2, 128, seed=93)
+    got = da.diffattn_v2_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.lam_logit.to(DEV),
+                             single_pass=True)
+    want = ref.diffattn_v2_fwd(inp.q, inp.k, inp.v, inp.lam_logit)
+    assert_bf16(got, want)
