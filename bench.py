@@ -1,0 +1,461 @@
+"""Benchmark of the differential-attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one pass of the prefill hot path on the 3B-layer workload (B 4, N 4096, 12 heads,
+d 128, dv 256, causal, bf16): the lambda kernel (exp reparameterisation) followed by the fused
+DiffAttn prefill with RMSNorm and (1 - lambda_init) epilogue. `value` is TFLOP/s counted at 1536
+MMA flops per causal query-key pair (4d for the two score maps + 4dv for the two value products),
+summed over ranks (weak scaling: every rank runs its own batch). The same JSON line carries the
+decode workload (B 64, cache 32768, 12 heads: HBM GB/s) and the V2 GQA workload as secondary
+objects, the roofline of the dominant kernel, the clocks seen during the timed region, an
+end-to-end number through host buffers, and the float64 oracle timed on the host cores.
+
+`--impl reference` times the float64 CPU oracle (the only reference implementation that exists
+for this method) on bounded samples of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PREFILL = dict(B=4, N=4096, H=12, d=128, dv=256, layer=12)
+DECODE = dict(B=64, L=32768, H=12, d=128, dv=256, layer=12)
+V2 = dict(B=2, N=8192, Hq=64, Hkv=8, d=128)
+FLOPS_PER_PAIR = 1536        # 4d + 4dv MMA flops per causal (query, key) pair, V1
+FLOPS_PER_PAIR_DEF = 1024    # 4d + 2dv: the definition (A1 - lambda A2) V
+V2_FLOPS_PER_PAIR = 8 * 128  # per (query, key) pair of one differential pair: 2 heads x (QK + PV)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def causal_pairs(N: int) -> int:
+    return N * (N + 1) // 2
+
+
+def prefill_flops(cfg=PREFILL, per_pair=FLOPS_PER_PAIR) -> float:
+    return float(cfg["B"] * cfg["H"] * causal_pairs(cfg["N"]) * per_pair)
+
+
+def decode_bytes(cfg=DECODE) -> float:
+    return float(cfg["B"] * cfg["L"] * cfg["H"] * (2 * cfg["d"] + cfg["dv"]) * 2)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "differential_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary: str, sha: str):
+    """dram bytes per launch from a committed ncu summary, or None if absent or stale."""
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != sha:
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for ln in (self.out or "").splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(loaded), "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU baseline: the float64 oracle on a bounded sample of the workload
+# ---------------------------------------------------------------------------------------------
+def oracle_sample(budget_s: float, seed: int = 0):
+    """Time the oracle on whole heads of the 3B-layer prefill (every causal row of a head, heads
+    and sequences in order) until `budget_s` of CPU time is used. Returns (TFLOP/s at 1536
+    flops/pair, cores, description, pairs, seconds)."""
+    import numpy as np
+    import torch
+    from oracle import diffattn_ref as ref
+    from synth import make_prefill_inputs
+
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    torch.set_num_threads(cores)
+    N, d, H = PREFILL["N"], PREFILL["d"], PREFILL["H"]
+    li = ref.lambda_init(PREFILL["layer"])
+    rows_done, pairs, t_used, heads = 0, 0, 0.0, 0
+    block = 256
+    for b in range(PREFILL["B"]):  # sequences of the workload, one at a time
+        if t_used >= budget_s:
+            break
+        inp = make_prefill_inputs(1, N, H, d, PREFILL["dv"], seed=seed + b, layer=PREFILL["layer"])
+        lam = float(ref.lambda_full(*inp.lam_vectors, layer=PREFILL["layer"])[0])
+        q, k, v = (ref._f64(t) for t in (inp.q, inp.k, inp.v))
+        for h in range(H):
+            if t_used >= budget_s:
+                break
+            qh, kh, vh = q[:, :, h:h + 1], k[:, :, h:h + 1], v[:, :, h:h + 1]
+            for hi in range(N, 0, -block):
+                if t_used >= budget_s:
+                    break
+                rows = np.arange(max(0, hi - block), hi)
+                t0 = time.perf_counter()
+                ref.diffattn_fwd(qh, kh, vh, [lam], li, rows=rows)
+                t_used += time.perf_counter() - t0
+                rows_done += rows.shape[0]
+                pairs += int(np.sum(rows + 1))
+            heads += 1
+    tflops = pairs * FLOPS_PER_PAIR / t_used / 1e12
+    desc = (f"oracle (numpy float64, {cores} threads) on {rows_done} causal query rows "
+            f"({heads} (sequence, head) pairs, longest rows first) of the 3B-layer prefill: "
+            f"{pairs} query-key pairs in {t_used:.1f} s")
+    return tflops, cores, desc, pairs, t_used
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    # each step times a bounded sample; the whole run stays within ~2 minutes
+    per_step = max(0.05, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(per_step * 0.25)
+    vals, times, pairs_total = [], [], 0
+    cores, desc = None, None
+    for _ in range(args.steps):
+        v, cores, desc, pairs, t = oracle_sample(per_step)
+        vals.append(v)
+        times.append(t)
+        pairs_total += pairs
+    value = pairs_total * FLOPS_PER_PAIR / sum(times) / 1e12
+    line = {
+        "impl": "reference", "metric": "DiffAttn fwd TFLOP/s (% dense BF16 TC peak); decode HBM GB/s (% peak)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "prefill_3b: B4 N4096 H12 d128 dv256 causal (bounded row sample per step)",
+                   "global_batch": PREFILL["B"], "seq_len": PREFILL["N"], "parallelism": "none (host cores)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {desc}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+# our path
+# ---------------------------------------------------------------------------------------------
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+    import differential_attention_gb300 as da
+    from synth import make_decode_inputs, make_lambda_vectors, make_prefill_inputs, make_v2_inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    da.build()
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+    peak_tf = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    line = {"metric": "DiffAttn fwd TFLOP/s (% dense BF16 TC peak); decode HBM GB/s (% peak)",
+            "value": None, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
+
+    # ======================= prefill: the step that `value` measures =======================
+    if args.only in ("all", "prefill"):
+        c = PREFILL
+        inp = make_prefill_inputs(c["B"], c["N"], c["H"], c["d"], c["dv"], seed=1000 + rank,
+                                  layer=c["layer"], device=dev)
+        lv = make_lambda_vectors(c["d"], seed=1001 + rank)
+        # one lambda per layer, shared by every head: the four vectors replicated per head
+        lv_h = tuple(t.to(dev).expand(c["H"], -1).contiguous() for t in lv)
+        lam_h = torch.empty(c["H"], dtype=torch.float32, device=dev)
+        lam_init = da.diffattn_lambda_init(c["layer"])
+        out = torch.empty((c["B"], c["N"], c["H"], c["dv"]), dtype=torch.bfloat16, device=dev)
+
+        for _ in range(args.warmup):
+            da.diffattn_lambda(*lv_h, layer=c["layer"], out=lam_h)
+            da.diffattn_fwd(inp.q, inp.k, inp.v, lam_h, lam_init, out=out)
+        da.diffattn_device_status()
+        kev = [(ev(), ev()) for _ in range(args.steps)]
+        with ClockSampler(dev.index) as clk:
+            barrier()
+            t_start, t_end = ev(), ev()
+            t_start.record(stream)
+            for i in range(args.steps):
+                da.diffattn_lambda(*lv_h, layer=c["layer"], out=lam_h)
+                kev[i][0].record(stream)
+                da.diffattn_fwd(inp.q, inp.k, inp.v, lam_h, lam_init, out=out)
+                kev[i][1].record(stream)
+            t_end.record(stream)
+            barrier()
+        da.diffattn_device_status()
+        total_ms = max_over_ranks(t_start.elapsed_time(t_end))
+        ms_per_step = total_ms / args.steps
+        kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+        flops = prefill_flops()
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        sha = source_sha(["prefill_exact.cu", "ptx.cuh"])
+        line.update({
+            "value": world * flops / (ms_per_step * 1e-3) / 1e12,
+            "ms_per_step": ms_per_step,
+            "config": {"workload": "prefill_3b: B4 N4096 H12 d128 dv256 causal, lambda (layer 12) + "
+                                   "DiffAttn + RMSNorm + (1 - lambda_init)",
+                       "global_batch": PREFILL["B"] * world, "seq_len": PREFILL["N"],
+                       "parallelism": f"replicas x{world} (independent batches, no collective)",
+                       "l2": "inputs larger than L2 (q, k, v = 302 MB per rank)",
+                       "flops_per_pair": FLOPS_PER_PAIR},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                         "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                         "traffic": profiled_traffic("prefill_exact_3b.md", sha),
+                         "kernel": "prefill_exact_kernel<128,256,false>", "kernel_ms": kernel_ms,
+                         "flops_per_launch": flops,
+                         "peak_source": f"bf16_tflops_sustained of {peak_src} (kernel run back to back)",
+                         "definition_count_tflops":
+                             flops / FLOPS_PER_PAIR * FLOPS_PER_PAIR_DEF / (kernel_ms * 1e-3) / 1e12},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+        })
+
+        # ---------------- end to end through host buffers ----------------
+        e2e_steps = max(3, min(20, args.steps))
+        hq, hk, hv = (t.cpu().pin_memory() for t in (inp.q, inp.k, inp.v))
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dq, dk, dvv = (torch.empty_like(t) for t in (inp.q, inp.k, inp.v))
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dvv.copy_(hv, non_blocking=True)
+            da.diffattn_lambda(*lv_h, layer=c["layer"], out=lam_h)
+            da.diffattn_fwd(dq, dk, dvv, lam_h, lam_init, out=out)
+            hout.copy_(out, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
+        line["e2e"] = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": 3 * inp.q.numel() * 2,
+                       "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": e2e_ms,
+                       "via": "pinned host -> device copies, diffattn_lambda + diffattn_fwd, "
+                              "device -> host copy of the output"}
+        del inp, out, hq, hk, hv, hout, dq, dk, dvv
+        torch.cuda.empty_cache()
+
+    # ======================= decode =======================
+    if args.only in ("all", "decode"):
+        dcfg = dict(DECODE, B=args.decode_batch)
+        dinp = make_decode_inputs(dcfg["B"], dcfg["L"], dcfg["H"], dcfg["d"], dcfg["dv"],
+                                  seed=2000 + rank, device=dev)
+        ws = torch.empty(da.diffattn_decode_workspace_size(dcfg["B"], dcfg["L"], dcfg["H"]),
+                         dtype=torch.uint8, device=dev)
+        dout = torch.empty((dcfg["B"], dcfg["H"], dcfg["dv"]), dtype=torch.bfloat16, device=dev)
+        li_dec = da.diffattn_lambda_init(dcfg["layer"])
+
+        def dec():
+            da.diffattn_decode(dinp.q, dinp.k_cache, dinp.v_cache, dinp.lam, li_dec, workspace=ws,
+                               out=dout)
+
+        for _ in range(args.warmup):
+            dec()
+        barrier()
+        dsteps = max(5, min(50, args.steps))
+        dev_ev = [(ev(), ev()) for _ in range(dsteps)]
+        for i in range(dsteps):
+            dev_ev[i][0].record(stream)
+            dec()
+            dev_ev[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        dms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+        dbytes = decode_bytes(dcfg)
+        dgbs = dbytes / (dms * 1e-3) / 1e9
+        dsha = source_sha(["decode.cu", "ptx.cuh"])
+        line["decode"] = {
+            "metric": "decode HBM GB/s", "value": world * dgbs, "unit": "GB/s", "ms_per_call": dms,
+            "workload": f"decode_32k: B{dcfg['B']}, one query per sequence, cache 32768, H12, "
+                        "d128, dv256, bf16 (cache 25.8 GB at B64, larger than L2)",
+            "roofline": {"bound": "hbm", "achieved": dgbs, "peak": hbm, "unit": "GB/s",
+                         "frac": dgbs / hbm, "traffic": profiled_traffic("decode_32k.md", dsha),
+                         "bytes_per_launch": dbytes,
+                         "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
+                         "timed": "diffattn_decode call (split kernel + combine kernel)"},
+            "gpu_launches": 2 * dsteps}
+        del dinp, ws, dout
+        torch.cuda.empty_cache()
+
+    # ======================= V2 =======================
+    if args.only in ("all", "v2"):
+        vc = V2
+        vinp = make_v2_inputs(vc["B"], vc["N"], vc["Hq"], vc["Hkv"], vc["d"], seed=3000 + rank,
+                              device=dev)
+        vout = torch.empty((vc["B"], vc["N"], vc["Hq"] // 2, vc["d"]), dtype=torch.bfloat16,
+                           device=dev)
+
+        def v2():
+            da.diffattn_v2_fwd(vinp.q, vinp.k, vinp.v, vinp.lam_logit, out=vout)
+
+        for _ in range(args.warmup):
+            v2()
+        barrier()
+        vsteps = max(5, min(30, args.steps))
+        v_ev = [(ev(), ev()) for _ in range(vsteps)]
+        for i in range(vsteps):
+            v_ev[i][0].record(stream)
+            v2()
+            v_ev[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        vms = statistics.mean(a.elapsed_time(b) for a, b in v_ev)
+        vflops = float(vc["B"] * (vc["Hq"] // 2) * causal_pairs(vc["N"]) * V2_FLOPS_PER_PAIR)
+        vtf = vflops / (vms * 1e-3) / 1e12
+        line["v2"] = {"metric": "V2 fwd TFLOP/s", "value": world * vtf, "unit": "TFLOP/s",
+                      "ms_per_call": vms,
+                      "workload": "v2_gqa: B2 N8192 Hq64 (32 pairs) Hkv8 d128 causal",
+                      "roofline": {"bound": "tensor", "achieved": vtf, "peak": peak_tf,
+                                   "unit": "TFLOP/s", "frac": vtf / peak_tf,
+                                   "flops_per_launch": vflops}}
+        del vinp, vout
+
+    # ======================= CPU baseline (rank 0, N = 1 only) =======================
+    line["cpu_baseline"] = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":
+        v, cores, desc, _, _ = oracle_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2"], default="all",
+                    help="profiling aid: run one workload (the JSON line then lacks the others)")
+    ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
+                    help="profiling aid: a smaller decode batch for captures that save device memory")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
