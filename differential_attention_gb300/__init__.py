@@ -67,7 +67,7 @@ def lib() -> ctypes.CDLL:
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is missing: build it with "
-                               "`python -m differential_attention_gb300.build`")
+                               "`python -m differential_attention_gb300.builder`")
         L = ctypes.CDLL(LIB_PATH)
         for name, (res, args) in _SIGNATURES.items():
             fn = getattr(L, name)
@@ -77,8 +77,9 @@ def lib() -> ctypes.CDLL:
 
 
 def build(force: bool = False) -> str:
-    from .build import build as _build
-    return _build(force=force)
+    """Compile libdiffattn.so for sm_103a if it is missing or stale (see builder.py)."""
+    from .builder import build_library
+    return build_library(force=force)
 
 
 def _check(rc: int):

@@ -1,6 +1,6 @@
 """Build libdiffattn.so in-tree for sm_103a with nvcc (one process per translation unit).
 
-    python -m differential_attention_gb300.build [--force] [--verbose] [--ptxas-info]
+    python -m differential_attention_gb300.builder [--force] [--verbose] [--ptxas-info]
 
 The shared library lands next to this file; objects go to `_build/`. Both are git-ignored.
 """
@@ -43,7 +43,7 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile every .cu source for sm_103a and link libdiffattn.so. Returns the library path."""
     deps = _deps()
     if not force and not ptxas_info and not _stale(LIB, deps):
@@ -88,4 +88,4 @@ if __name__ == "__main__":
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--ptxas-info", action="store_true")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=a.verbose, ptxas_info=a.ptxas_info))
+    print(build_library(force=a.force, verbose=a.verbose, ptxas_info=a.ptxas_info))
