@@ -56,6 +56,9 @@ _SIGNATURES = {
     "diffattn_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.c_void_p,
                                                                ctypes.c_float] + [ctypes.c_int] * 7
                         + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_decode_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 6
+                                + [ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
+                                + [ctypes.c_int] * 7 + [ctypes.c_void_p]),
     "diffattn_v2_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 7
                         + [ctypes.c_void_p]),
 }
@@ -208,6 +211,35 @@ def diffattn_decode(q, k_cache, v_cache, lam, lambda_init: float = 0.0, seqlens=
                                  _ptr(lam), float(lambda_init), _ptr(norm_weight), float(eps), B,
                                  Lmax, H, d, dv, flags, DIFFATTN_BF16, _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def diffattn_decode_noalloc(q, k_cache, v_cache, lam, lambda_init: float = 0.0, seqlens=None,
+                            norm_weight=None, eps: float = 1e-5, norm: bool = True,
+                            scale: bool = True, out=None, stream=None):
+    """diffattn_decode for callers that cannot allocate device memory where they decode: the
+    split partials go to a scratch array built into the library instead of a workspace. `out`
+    must be given by such a caller (otherwise one is allocated here for convenience)."""
+    _dev("q", q, torch.bfloat16)
+    B, H, two_d = q.shape
+    _dev("k_cache", k_cache, torch.bfloat16)
+    _dev("v_cache", v_cache, torch.bfloat16)
+    Lmax, dv = k_cache.shape[1], v_cache.shape[-1]
+    if k_cache.shape != (B, Lmax, H, two_d) or v_cache.shape[:3] != (B, Lmax, H):
+        raise ValueError("caches must be [B, Lmax, H, 2d] and [B, Lmax, H, dv]")
+    _dev("lam", lam, torch.float32)
+    if seqlens is not None:
+        _dev("seqlens", seqlens, torch.int32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    flags = (DIFFATTN_NORM if norm else 0) | (DIFFATTN_SCALE if scale else 0)
+    _check(lib().diffattn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
+                                         _ptr(out), _ptr(lam), float(lambda_init),
+                                         _ptr(norm_weight), float(eps), B, Lmax, H, two_d // 2,
+                                         dv, flags, DIFFATTN_BF16, _stream(stream)))
     return out
 
 

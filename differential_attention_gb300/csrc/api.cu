@@ -217,6 +217,58 @@ DIFFATTN_API int diffattn_decode(const void* q, const void* k_cache, const void*
   return ok();
 }
 
+DIFFATTN_API int diffattn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                         const int* seqlens, void* out, const float* lambda,
+                                         float lambda_init, const float* norm_weight, float eps,
+                                         int B, int Lmax, int H, int d, int dv, int flags,
+                                         int dtype, void* stream) {
+  static_assert(da::kNoAllocScratchBytes == DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES, "scratch size");
+  if (!q || !k_cache || !v_cache || !out || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_decode_noalloc: null pointer");
+  if (flags & ~(DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_decode_noalloc: unknown flag bits 0x%x", flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_decode_noalloc: eps must be > 0 with DIFFATTN_NORM");
+  if (dtype != DIFFATTN_BF16)
+    return fail(DIFFATTN_ERR_DTYPE, "diffattn_decode_noalloc: dtype must be DIFFATTN_BF16");
+  if (B < 1 || Lmax < 1 || H < 1 || B > 65535 || H > 65535)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode_noalloc: need 1 <= B, H <= 65535 and Lmax >= 1");
+  if (d != 128 || dv != 256)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode_noalloc: need d = 128 and dv = 256 (got d=%d dv=%d)", d, dv);
+  const long long units = static_cast<long long>(B) * H;
+  if (units > da::decode_noalloc_max_units())
+    return fail(DIFFATTN_ERR_SHAPE,
+                "diffattn_decode_noalloc: B*H = %lld exceeds the %lld (sequence, head) pairs whose "
+                "partials fit in the built-in %zu-byte scratch; use diffattn_decode with a workspace",
+                units, da::decode_noalloc_max_units(), da::kNoAllocScratchBytes);
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || (seqlens && !aligned(seqlens, 4)) ||
+      (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_decode_noalloc: tensors must be 16-byte aligned");
+  int rc = check_device();
+  if (rc) return rc;
+  da::DecodeArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.seqlens = seqlens;
+  a.out = out;
+  a.lambda = lambda;
+  a.lambda_init = lambda_init;
+  a.norm_w = norm_weight;
+  a.eps = eps;
+  a.flags = flags;
+  a.B = B;
+  a.Lmax = Lmax;
+  a.H = H;
+  a.d = d;
+  a.dv = dv;
+  a.ws = nullptr;
+  cudaError_t e = da::launch_decode_noalloc(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_decode_noalloc");
+  return ok();
+}
+
 DIFFATTN_API int diffattn_v2_fwd(const void* q, const void* k, const void* v,
                                  const float* lam_logit, void* out, int B, int N, int Hq, int Hkv,
                                  int d, int flags, int dtype, void* stream) {

@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -280,6 +281,100 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   DecCombineParams cp;
   cp.ws = a.ws;
+  cp.lambda = a.lambda;
+  cp.norm_w = a.norm_w;
+  cp.out = static_cast<__nv_bfloat16*>(a.out);
+  cp.lambda_init = a.lambda_init;
+  cp.eps = a.eps;
+  cp.flags = a.flags;
+  cp.H = a.H;
+  cp.splits = S;
+  decode_combine_kernel<<<dim3(a.H, a.B), kDecWidth, 0, st>>>(cp);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they decode: a plugin running
+// inside a host runtime that owns every device buffer and offers no allocator, or a decode loop
+// with a hard latency budget where cudaMalloc / cudaFree (which may synchronise the device) are
+// not allowed. For them the split partials go to a fixed scratch array that is part of this
+// library's device image: every GPU that loads the library holds kNoAllocScratchBytes of it
+// until the process exits.
+//
+// The array is shared by every call on a device and keeps the previous call's contents. Nothing
+// in it needs clearing: the split kernel writes every record (empty splits included) before the
+// combine kernel of the same call reads it. Two such calls that run at the same time on one
+// device (different streams, or graphs replayed concurrently) overwrite each other's partials:
+// the caller must keep them ordered.
+//
+// Host code may not use the array's name as a device address (on the host it names a host-side
+// stand-in). The device address is looked up once per device with cudaGetSymbolAddress, with that
+// device current, on the first call made on it; make that first call before any stream capture.
+// ---------------------------------------------------------------------------------------------
+static __device__ __align__(256) float g_decode_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+namespace {
+constexpr int kMaxDevices = 128;
+std::mutex g_scratch_mu;
+float* g_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+cudaError_t decode_scratch_address(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<float*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+long long decode_noalloc_max_units() {
+  return static_cast<long long>(kNoAllocScratchBytes / (kRec * sizeof(float)));
+}
+
+// Same kernels as launch_decode, with the split count lowered (if needed) so that the partials
+// of all B x H x splits records fit in the scratch array.
+cudaError_t launch_decode_noalloc(const DecodeArgs& a, cudaStream_t st) {
+  const long long units = static_cast<long long>(a.B) * a.H;
+  if (units > decode_noalloc_max_units()) return cudaErrorInvalidValue;
+  float* scratch = nullptr;
+  cudaError_t e = decode_scratch_address(&scratch);
+  if (e != cudaSuccess) return e;
+  int chunk = 0;
+  int S = decode_splits(a.B, a.Lmax, a.H, &chunk);
+  const long long fit = decode_noalloc_max_units() / units;
+  if (S > fit) {
+    const int step = kDecWarps * kG;
+    long long c = (a.Lmax + fit - 1) / fit;
+    c = (c + step - 1) / step * step;
+    chunk = static_cast<int>(c);
+    S = static_cast<int>((a.Lmax + c - 1) / c);
+  }
+  DecSplitParams sp;
+  sp.q = static_cast<const __nv_bfloat16*>(a.q);
+  sp.kc = static_cast<const __nv_bfloat16*>(a.k_cache);
+  sp.vc = static_cast<const __nv_bfloat16*>(a.v_cache);
+  sp.seqlens = a.seqlens;
+  sp.ws = scratch;
+  sp.Lmax = a.Lmax;
+  sp.H = a.H;
+  sp.splits = S;
+  sp.chunk = chunk;
+  sp.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.d));
+  decode_split_kernel<<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  DecCombineParams cp;
+  cp.ws = scratch;
   cp.lambda = a.lambda;
   cp.norm_w = a.norm_w;
   cp.out = static_cast<__nv_bfloat16*>(a.out);

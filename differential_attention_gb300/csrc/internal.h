@@ -74,6 +74,11 @@ int decode_splits(int B, int Lmax, int H, int* chunk_out);
 size_t decode_workspace_bytes(int B, int Lmax, int H, int dv);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
+// Decode whose split partials live in a fixed device array of this size (no workspace argument).
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(16) << 20;
+long long decode_noalloc_max_units();  // largest B * H whose partials fit (one split each)
+cudaError_t launch_decode_noalloc(const DecodeArgs& a, cudaStream_t s);
+
 // Two-pass tensor-core prefill (A1 - lambda A2 formed in fp32 before rounding).
 cudaError_t launch_prefill_exact(const Problem& p, cudaStream_t s, char* err, size_t err_len);
 

@@ -148,6 +148,30 @@ DIFFATTN_API int diffattn_decode(const void* q, const void* k_cache, const void*
                                  void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Decode that allocates nothing (the paper has no counterpart: this is a deployment aid).
+ * For callers that cannot allocate device memory where they decode -- a plugin inside a host
+ * runtime that owns every device buffer and hands out no allocator, or a latency-bound decode
+ * loop that may not call cudaMalloc / cudaFree because they can synchronise the device. The
+ * arguments and the result are those of diffattn_decode without workspace / ws_bytes; the split
+ * partials go to a scratch array built into the library (DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES,
+ * held on every GPU that loads the library until the process exits).
+ *   Limit: B * H <= DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES / 2064 (= 8128); larger calls return
+ *   DIFFATTN_ERR_SHAPE. The cache may be split into fewer slices than diffattn_decode uses, so
+ *   results agree with diffattn_decode to rounding, not bit for bit.
+ *   The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *   with that device current); make that first call before any stream capture.
+ *   All calls on a device share the array: calls that can run at the same time (other streams,
+ *   concurrent replays) race on it, so keep them ordered. No call depends on what an earlier call
+ *   left there. It calls no allocator (cudaMalloc, cudaFree or any library that allocates).
+ * ------------------------------------------------------------------------------------------ */
+#define DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
+DIFFATTN_API int diffattn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                         const int* seqlens, void* out, const float* lambda,
+                                         float lambda_init, const float* norm_weight, float eps,
+                                         int B, int Lmax, int H, int d, int dv, int flags,
+                                         int dtype, void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * DIFF V2 prefill (page "Differential Transformer: softmax can't say zero, so it subtracts",
  * section "DIFF V2: what the authors changed"; page "Differential Transformer V2"): softmax
  * attention of 2h query heads over GQA KV heads, then out_p = attn[2p] - sigmoid(lam) * attn[2p+1]
