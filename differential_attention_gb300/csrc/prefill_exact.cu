@@ -39,7 +39,7 @@ namespace exact {
 
 constexpr int BM = 128;
 constexpr int BN = 64;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 softmax
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -51,23 +51,23 @@ struct Cfg {
   static constexpr int kQMapBytes = BM * DQK * 2;          // one map's Q tile
   static constexpr int kKMapBytes = BN * DQK * 2;          // one map's K tile
   static constexpr int kQBytes = 2 * kQMapBytes;
-  static constexpr int kKBytes = (SHARED_K ? 1 : 2) * kKMapBytes;  // one K stage
-  static constexpr int kVBytes = BN * DV * 2;              // one V stage
-  static constexpr int NSK = (DQK == 128 && DV == 256) ? 3 : 4;
-  static constexpr int NSV = (DQK == 128 && DV == 256) ? 2 : 4;
+  static constexpr int kKBytes = (SHARED_K ? 1 : 2) * kKMapBytes;  // one K tile (both maps)
+  static constexpr int kVBytes = BN * DV * 2;              // one V tile
+  // One ring of slots holds K and V tiles in the order the MMA issuer consumes them.
+  static constexpr int kSlot = kKBytes > kVBytes ? kKBytes : kVBytes;
+  static constexpr int NSLOT = (kSlot >= 32768) ? 4 : 8;
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kQBytes;
-  static constexpr int kVOff = kKOff + NSK * kKBytes;
-  static constexpr int kEnd = kVOff + NSV * kVBytes;
+  static constexpr int kSlotOff = kQOff + kQBytes;
+  static constexpr int kEnd = kSlotOff + NSLOT * kSlot;
   static constexpr int kDynSmem = kEnd + 1024;
   static constexpr int kOCol = 256;
   static_assert(kOCol + DV <= kTmemCols, "TMEM budget");
-  static_assert(kDynSmem <= 232448 - 1024, "shared memory budget");
+  static_assert(kDynSmem + 8192 <= 232448, "shared memory budget (dynamic + static)");
 };
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t slot_full[8], slot_empty[8];
   uint64_t s_full[2], s_done[2];
   uint64_t o_full;
   uint64_t teardown;
@@ -76,6 +76,7 @@ struct Barriers {
 struct KParams {
   Problem p;
   int n_qt;
+  int group;        // (batch, unit) pairs whose K/V share L2 in one launch-order group
   float scale_log2;
 };
 
@@ -85,40 +86,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const KParams kp) {
   using C = Cfg<DQK, DV, SHARED_K>;
-  constexpr int NSK = C::NSK, NSV = C::NSV;
+  constexpr int NSLOT = C::NSLOT;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ float stats[2][4][BM];  // per-warpgroup partial row statistics
+  __shared__ float sumsq[2][BM];     // per-warpgroup partial RMSNorm sums of squares
 
   const Problem& P = kp.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sQ = smem_u32(smem + C::kQOff);
-  const uint32_t sK = smem_u32(smem + C::kKOff);
-  const uint32_t sV = smem_u32(smem + C::kVOff);
+  const uint32_t sSlot = smem_u32(smem + C::kSlotOff);
 
   // ---- work item: longest causal tiles first ----
   const int BU = P.B * P.units;
   const bool causal = (P.flags & 1) != 0;
+  // Launch order: (batch, unit) pairs are taken in groups whose K/V fit in L2 together; inside a
+  // group the query tiles go longest-first (causal) across the group's pairs.
   const int item = blockIdx.x;
-  const int qt = causal ? (kp.n_qt - 1 - item / BU) : (item / BU);
-  const int bu = item % BU;
+  const int g0 = (item / (kp.group * kp.n_qt)) * kp.group;
+  const int gsize = min(kp.group, BU - g0);
+  const int r_in = item - g0 * kp.n_qt;
+  const int qt = causal ? (kp.n_qt - 1 - r_in / gsize) : (r_in / gsize);
+  const int bu = g0 + r_in % gsize;
   const int b = bu / P.units, u = bu % P.units;
   const int n_kv_all = (P.N + BN - 1) / BN;
   const int n = causal ? min((qt * BM + BM + BN - 1) / BN, n_kv_all) : n_kv_all;
   const int T = 2 * n;  // tiles over both passes
+  // Ring order of the loads: K(0..n-1) for pass 1, then K(n+j), V(j) alternately for pass 2.
+  auto k_load = [n](int t) { return t < n ? t : 2 * t - n; };
+  auto v_load = [n](int jv) { return n + 2 * jv + 1; };
 
   auto bar = [](uint64_t& x) { return smem_u32(&x); };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(bars.q_full), 1);
-    for (int s = 0; s < 4; ++s) {
-      mbar_init(bar(bars.k_full[s]), 1);
-      mbar_init(bar(bars.k_empty[s]), 1);
-      mbar_init(bar(bars.v_full[s]), 1);
-      mbar_init(bar(bars.v_empty[s]), 1);
+    for (int s = 0; s < 8; ++s) {
+      mbar_init(bar(bars.slot_full[s]), 1);
+      mbar_init(bar(bars.slot_empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(bars.s_full[i]), 1);
@@ -155,34 +163,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < DQK / 64; ++c)
           tma_load_4d(sQ + r * C::kQMapBytes + c * C::kQChunk, &tm_q, bar(bars.q_full),
                       q_col_of(P, r) + 64 * c, q_head_of(P, u, r), qt * BM, b);
-      int k_issued = 0, v_issued = 0;
+      int issued = 0;  // loads issued into the ring
       bool ok = true;
+      auto acquire = [&](int idx, uint32_t bytes) -> int {
+        const int slot = idx % NSLOT;
+        if (!mbar_wait(bar(bars.slot_empty[slot]), ((idx / NSLOT) & 1) ^ 1, abrt)) return -1;
+        mbar_arrive_expect_tx(bar(bars.slot_full[slot]), bytes);
+        return slot;
+      };
       for (int t = 0; t < T && ok; ++t) {
         const int j = t < n ? t : t - n;
-        const int s = t % NSK;
-        if (!(ok = mbar_wait(bar(bars.k_empty[s]), ((t / NSK) & 1) ^ 1, abrt))) break;
-        mbar_arrive_expect_tx(bar(bars.k_full[s]), C::kKBytes);
+        const int ks = acquire(k_load(t), C::kKBytes);
+        if (!(ok = ks >= 0)) break;
         for (int r = 0; r < (SHARED_K ? 1 : 2); ++r)
           for (int c = 0; c < DQK / 64; ++c)
-            tma_load_4d(sK + s * C::kKBytes + r * C::kKMapBytes + c * C::kKChunk, &tm_k,
-                        bar(bars.k_full[s]), k_col_of(P, r) + 64 * c, kvh, j * BN, b);
-        k_issued = t + 1;
+            tma_load_4d(sSlot + ks * C::kSlot + r * C::kKMapBytes + c * C::kKChunk, &tm_k,
+                        bar(bars.slot_full[ks]), k_col_of(P, r) + 64 * c, kvh, j * BN, b);
+        issued = k_load(t) + 1;
         if (t >= n) {
-          const int jv = t - n, sv = jv % NSV;
-          if (!(ok = mbar_wait(bar(bars.v_empty[sv]), ((jv / NSV) & 1) ^ 1, abrt))) break;
-          mbar_arrive_expect_tx(bar(bars.v_full[sv]), C::kVBytes);
+          const int jv = t - n;
+          const int vs = acquire(v_load(jv), C::kVBytes);
+          if (!(ok = vs >= 0)) break;
           for (int c = 0; c < DV / 64; ++c)
-            tma_load_4d(sV + sv * C::kVBytes + c * C::kKChunk, &tm_v, bar(bars.v_full[sv]),
+            tma_load_4d(sSlot + vs * C::kSlot + c * C::kKChunk, &tm_v, bar(bars.slot_full[vs]),
                         64 * c, kvh, jv * BN, b);
-          v_issued = jv + 1;
+          issued = v_load(jv) + 1;
         }
       }
       // make sure no copy of ours is still landing in shared memory
       mbar_wait(bar(bars.q_full), 0, nullptr);
-      for (int t = max(0, k_issued - NSK); t < k_issued; ++t)
-        mbar_wait(bar(bars.k_full[t % NSK]), (t / NSK) & 1, nullptr);
-      for (int jv = max(0, v_issued - NSV); jv < v_issued; ++jv)
-        mbar_wait(bar(bars.v_full[jv % NSV]), (jv / NSV) & 1, nullptr);
+      for (int i = max(0, issued - NSLOT); i < issued; ++i)
+        mbar_wait(bar(bars.slot_full[i % NSLOT]), (i / NSLOT) & 1, nullptr);
     }
   } else if (warp == 1) {
     // ================================ MMA issuer ==================================
@@ -193,16 +204,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       for (int t = 0; ok && t <= T; ++t) {
         if (t < T) {
-          const int buf = t & 1, s = t % NSK;
+          const int buf = t & 1, ki = k_load(t), s = ki % NSLOT;
           // S buffer `buf` was last used by tile t-2: its scores must have been read (pass 1)
           // or replaced by D and handed over (pass 2; that D's product was issued already).
           if (t >= 2 && !(ok = mbar_wait(bar(bars.s_done[buf]), ((t - 2) >> 1) & 1, abrt))) break;
-          if (!(ok = mbar_wait(bar(bars.k_full[s]), (t / NSK) & 1, abrt))) break;
+          if (!(ok = mbar_wait(bar(bars.slot_full[s]), (ki / NSLOT) & 1, abrt))) break;
           tc_fence_after();
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const uint32_t d_s = tmem + buf * 128 + r * 64;
-            const uint32_t kbase = sK + s * C::kKBytes + (SHARED_K ? 0 : r * C::kKMapBytes);
+            const uint32_t kbase = sSlot + s * C::kSlot + (SHARED_K ? 0 : r * C::kKMapBytes);
 #pragma unroll
             for (int kk = 0; kk < DQK / 16; ++kk) {
               const uint64_t ad = umma_smem_desc(
@@ -212,22 +223,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16_ss(d_s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
             }
           }
-          tc_commit(bar(bars.k_empty[s]));
+          tc_commit(bar(bars.slot_empty[s]));
           tc_commit(bar(bars.s_full[buf]));
         }
         const int tp = t - 1;
         if (tp >= n) {
-          const int bp = tp & 1, jv = tp - n, sv = jv % NSV;
+          const int bp = tp & 1, jv = tp - n, vi = v_load(jv), sv = vi % NSLOT;
           if (!(ok = mbar_wait(bar(bars.s_done[bp]), (tp >> 1) & 1, abrt))) break;
-          if (!(ok = mbar_wait(bar(bars.v_full[sv]), (jv / NSV) & 1, abrt))) break;
+          if (!(ok = mbar_wait(bar(bars.slot_full[sv]), (vi / NSLOT) & 1, abrt))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             const uint32_t a_t = tmem + bp * 128 + kk * 8;  // D: 16 bf16 keys per 8 columns
-            const uint64_t bd = umma_smem_desc(sV + sv * C::kVBytes + kk * 2048, C::kKChunk, 1024);
+            const uint64_t bd = umma_smem_desc(sSlot + sv * C::kSlot + kk * 2048, C::kKChunk, 1024);
             mma_bf16_ts(tmem + C::kOCol, a_t, bd, idesc_o, (jv > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(bar(bars.v_empty[sv]));
+          tc_commit(bar(bars.slot_empty[sv]));
           if (tp == T - 1) tc_commit(bar(bars.o_full));
         }
       }
@@ -236,6 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ============================ softmax and epilogue ============================
+    // Two warpgroups: WG w owns the tiles t with t % 2 == w (and TMEM score buffer w), so one
+    // warpgroup turns S into statistics or D while the other waits for its next scores.
+    const int wg = (warp - kSoftmaxWarp0) >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int row = qt * BM + r;
     const uint32_t tl = static_cast<uint32_t>(32 * (warp & 3)) << 16;
@@ -243,11 +257,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lim = causal ? min(row + 1, P.N) : P.N;  // keys [0, lim) are visible
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
     float bias[2] = {0.f, 0.f}, lam = 0.f;
-    bool ok = true;
+    bool ok = true, merged = false;
 
-    for (int t = 0; t < T; ++t) {
+    // Merge the two warpgroups' partial row statistics (once, at the pass boundary).
+    auto merge = [&]() {
+      stats[wg][0][r] = m[0];
+      stats[wg][1][r] = l[0];
+      stats[wg][2][r] = m[1];
+      stats[wg][3][r] = l[1];
+      named_barrier_sync(1, 256);
+#pragma unroll
+      for (int mp = 0; mp < 2; ++mp) {
+        const float mo = stats[wg ^ 1][2 * mp][r], lo = stats[wg ^ 1][2 * mp + 1][r];
+        const float M = fmaxf(m[mp], mo);
+        const float L = (m[mp] == -INFINITY ? 0.f : l[mp] * ex2_approx(m[mp] - M)) +
+                        (mo == -INFINITY ? 0.f : lo * ex2_approx(mo - M));
+        bias[mp] = -(M + __log2f(L));
+      }
+      if (P.mode == MODE_V1) {
+        lam = P.lambda[u];
+      } else if (row < P.N) {
+        const float z = P.lam_logit[(static_cast<size_t>(b) * P.N + row) * P.units + u];
+        lam = 1.f / (1.f + expf(-z));
+      }
+      merged = true;
+    };
+
+    for (int t = wg; t < T; t += 2) {
       const int buf = t & 1;
       const bool pass2 = t >= n;
+      if (pass2 && !merged) merge();
       const int key0 = (pass2 ? t - n : t) * BN;
       ok = mbar_wait(bar(bars.s_full[buf]), (t >> 1) & 1, abrt);
       if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
@@ -280,24 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 4; i < BN; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(sr[mp][i]));
           const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
           const float mn = fmaxf(m[mp], mt);
-          const float nb = (mn == -INFINITY) ? 0.f : -mn;
+          if (mn == -INFINITY) continue;  // every key of this tile is masked for this row
+          const float nb = -mn;
           float la[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int i = 0; i < BN; ++i)
             la[i & 3] += ex2_approx(fmaf(__uint_as_float(sr[mp][i]), sl2, nb));
           l[mp] = l[mp] * ex2_approx(m[mp] + nb) + ((la[0] + la[1]) + (la[2] + la[3]));
           m[mp] = mn;
-        }
-        if (t == n - 1) {
-          // p / l = 2^(x - (m + log2 l)); lambda of this row
-          bias[0] = -(m[0] + __log2f(l[0]));
-          bias[1] = -(m[1] + __log2f(l[1]));
-          if (P.mode == MODE_V1) {
-            lam = P.lambda[u];
-          } else if (row < P.N) {
-            const float z = P.lam_logit[(static_cast<size_t>(b) * P.N + row) * P.units + u];
-            lam = 1.f / (1.f + expf(-z));
-          }
         }
       } else {
         // ---- pass 2: D = A1 - lambda A2 in fp32, rounded once to bf16 ----
@@ -316,34 +345,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(bars.s_done[buf]));
       }
     }
+    if (!merged) merge();
     if (ok) {
       ok = mbar_wait(bar(bars.o_full), 0, abrt);
       ok = !__any_sync(0xffffffffu, !ok);
     }
     tc_fence_after();
     // ------------------------------- epilogue -------------------------------------
-    if (ok) {
-      float scale = 1.f;
-      if (P.flags & 2) {
-        float ss = 0.f;
+    // WG w owns columns [w * DV/2, (w+1) * DV/2) of each row; the RMSNorm sum of squares is
+    // combined across the two warpgroups.
+    constexpr int HC = DV / 2;
+    const int c0 = wg * HC;
+    float ss = 0.f;
+    if (ok && (P.flags & 2)) {
 #pragma unroll 1
-        for (int c = 0; c < DV / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + tl + C::kOCol + 32 * c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ss = fmaf(__uint_as_float(o[i]), __uint_as_float(o[i]), ss);
-        }
-        scale = 1.f / sqrtf(ss / static_cast<float>(DV) + P.eps);
-      }
-      if (P.flags & 4) scale *= (1.f - P.lambda_init);
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P.out) +
-                           ((static_cast<size_t>(b) * P.N + row) * P.units + u) * DV;
-      const float* w = (P.flags & 2) ? P.norm_w : nullptr;
-#pragma unroll 1
-      for (int c = 0; c < DV / 32; ++c) {
+      for (int c = 0; c < HC / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem + tl + C::kOCol + 32 * c, o);
+        tmem_ld32(tmem + tl + C::kOCol + c0 + 32 * c, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ss = fmaf(__uint_as_float(o[i]), __uint_as_float(o[i]), ss);
+      }
+    }
+    float scale = 1.f;
+    if (P.flags & 2) {
+      sumsq[wg][r] = ss;
+      named_barrier_sync(1, 256);
+      scale = 1.f / sqrtf((ss + sumsq[wg ^ 1][r]) / static_cast<float>(DV) + P.eps);
+    }
+    if (P.flags & 4) scale *= (1.f - P.lambda_init);
+    if (ok) {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P.out) +
+                           ((static_cast<size_t>(b) * P.N + row) * P.units + u) * DV + c0;
+      const float* w = (P.flags & 2) && P.norm_w ? P.norm_w + c0 : nullptr;
+#pragma unroll 1
+      for (int c = 0; c < HC / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + tl + C::kOCol + c0 + 32 * c, o);
         tmem_wait_ld();
         if (row < P.N) {
 #pragma unroll
@@ -430,6 +468,13 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
   kp.p = p;
   kp.n_qt = (p.N + BM - 1) / BM;
   kp.scale_log2 = kLog2e * p.scale;
+  {
+    // K/V bytes one (batch, unit) pair streams; keep a group's K/V within ~64 MB of L2
+    const double kv_bytes = static_cast<double>(p.N) * (p.k_cols + DV) * 2.0;
+    long long g = static_cast<long long>((64.0 * 1024 * 1024) / (kv_bytes > 1 ? kv_bytes : 1));
+    const long long bu = static_cast<long long>(p.B) * p.units;
+    kp.group = static_cast<int>(g < 1 ? 1 : (g > bu ? bu : g));
+  }
   const long long items = static_cast<long long>(kp.n_qt) * p.B * p.units;
   if (items == 0) return cudaSuccess;
   kern<<<dim3(static_cast<unsigned>(items)), kThreads, C::kDynSmem, s>>>(mq, mk, mv, kp);

@@ -1,0 +1,102 @@
+"""GPU parity at the full workload sizes, in the launch configurations bench.py times.
+
+Inputs are drawn on the device (seeded CUDA generator); the kernels run on the whole problem;
+the float64 oracle then recomputes sampled outputs from the same inputs, copied to the host per
+head: the first rows, the last row, and seeded random rows of every head (all heads of the
+sampled sequences for decode). Tolerances are those of the small cases (tests/gpu_util.py).
+"""
+import numpy as np
+import pytest
+import torch
+
+import differential_attention_gb300 as da
+from oracle import diffattn_ref as ref
+from synth import make_decode_inputs, make_lambda_vectors, make_prefill_inputs, make_v2_inputs
+from tests.gpu_util import assert_bf16
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    da.build()
+    da.lib()
+    yield
+    torch.cuda.empty_cache()
+
+
+def _rows(N, n_first, n_rand, seed):
+    rng = np.random.default_rng(seed)
+    rand = rng.choice(np.arange(n_first, N - 1), size=min(n_rand, max(0, N - 1 - n_first)), replace=False)
+    return np.unique(np.concatenate([np.arange(min(n_first, N)), [N - 1], rand]))
+
+
+def _prefill_case(B, N, H, layer, seed, needle, n_first, n_rand):
+    inp = make_prefill_inputs(B, N, H, 128, 256, seed=seed, layer=layer, device=DEV, needle=needle)
+    lv = make_lambda_vectors(128, seed=seed + 1)
+    lv_h = tuple(t.to(DEV).expand(H, -1).contiguous() for t in lv)
+    lam_h = da.diffattn_lambda(*lv_h, layer=layer)
+    li = da.diffattn_lambda_init(layer)
+    out = da.diffattn_fwd(inp.q, inp.k, inp.v, lam_h, li)
+    da.diffattn_device_status()
+    lam = float(ref.lambda_full(*lv, layer=layer)[0])
+    rows = _rows(N, n_first, n_rand, seed)
+    got, want = [], []
+    for b in range(B):
+        for h in range(H):
+            q = inp.q[b:b + 1, :, h:h + 1].cpu()
+            k = inp.k[b:b + 1, :, h:h + 1].cpu()
+            v = inp.v[b:b + 1, :, h:h + 1].cpu()
+            want.append(ref.diffattn_fwd(q, k, v, [lam], ref.lambda_init(layer), rows=rows)[0, :, 0])
+            got.append(out[b, torch.as_tensor(rows, device=DEV), h].float().cpu().numpy())
+    return np.stack(got), np.stack(want), lam
+
+
+def test_prefill_3b_full():
+    """B4 N4096 H12 d128 dv256 causal, lambda from the layer-12 vectors, RMSNorm + scale."""
+    got, want, lam = _prefill_case(4, 4096, 12, 12, seed=1000, needle=False, n_first=64, n_rand=128)
+    assert_bf16(got, want)
+
+
+def test_prefill_64k_full_with_needle():
+    """B1 N65536 H12 causal, layer 24, one needle key per head raised by ln(N-1) against the last
+    query: the last row (needle row), the first rows and random rows of every head."""
+    got, want, lam = _prefill_case(1, 65536, 12, 24, seed=2024, needle=True, n_first=32, n_rand=64)
+    assert_bf16(got, want)
+
+
+def test_decode_32k_full():
+    """B64, cache 32768, H12: every head of 4 sampled sequences against the oracle."""
+    inp = make_decode_inputs(64, 32768, 12, 128, 256, seed=2000, device=DEV)
+    li = da.diffattn_lambda_init(12)
+    out = da.diffattn_decode(inp.q, inp.k_cache, inp.v_cache, inp.lam, li)
+    da.diffattn_device_status()
+    sample = [0, 17, 42, 63]
+    want = ref.diffattn_decode(inp.q[sample].cpu(), inp.k_cache[sample].cpu(), inp.v_cache[sample].cpu(),
+                               inp.seqlens[sample].cpu(), inp.lam.cpu(), ref.lambda_init(12))
+    assert_bf16(out[sample], want)
+    del inp
+    torch.cuda.empty_cache()
+
+
+def test_v2_gqa_full():
+    """B2 N8192, 32 pairs over 8 KV heads, causal: sampled rows of every pair."""
+    inp = make_v2_inputs(2, 8192, 64, 8, 128, seed=3000, device=DEV)
+    out = da.diffattn_v2_fwd(inp.q, inp.k, inp.v, inp.lam_logit)
+    da.diffattn_device_status()
+    rows = _rows(8192, 32, 64, 3000)
+    got, want = [], []
+    for b in range(2):
+        for p in range(32):
+            g = ref.v2_kv_head(p, 64, 8)
+            q = inp.q[b:b + 1, :, 2 * p:2 * p + 2].cpu()
+            k = inp.k[b:b + 1, :, g:g + 1].cpu()
+            v = inp.v[b:b + 1, :, g:g + 1].cpu()
+            lam = inp.lam_logit[b:b + 1, :, p:p + 1].cpu()
+            want.append(ref.diffattn_v2_fwd(q, k, v, lam, rows=rows)[0, :, 0])
+            got.append(out[b, torch.as_tensor(rows, device=DEV), p].float().cpu().numpy())
+    assert_bf16(np.stack(got), np.stack(want))
