@@ -13,17 +13,22 @@
 // error of about 2^-9 of each term, i.e. ~2^-9 / |1 - lambda| of the result. This kernel first
 // finds each map's exact row max and row sum (pass 1: QK^T only), then (pass 2) recomputes the
 // scores, forms D = 2^(s1 - b1) - lambda 2^(s2 - b2) with b = max + log2(sum) in fp32, rounds D
-// (already small) to bf16 and runs a single D V product. Both passes together issue the same
-// MMA work as the single-pass form (4d + 4dv flops per query-key pair).
+// (already small) to bf16 once and runs a single D V product. Both passes together issue the
+// same MMA work as the single-pass form (4d + 4dv flops per query-key pair).
 //
-// Structure: one CTA per 128-row query tile of one unit, 64-key tiles. TMA stages Q1|Q2 once and
-// a ring of K tiles (each K tile is streamed twice, once per pass) and V tiles (pass 2 only).
-// tcgen05.mma writes S1 and S2 (64 columns each, double-buffered) into tensor memory; four
-// softmax warps (one thread per query row) read them, and in pass 2 write D as packed bf16 over
-// the S1 columns; a second tcgen05.mma (A = D from tensor memory, B = V from shared memory)
-// accumulates O (128 x dv fp32, columns 256..) in tensor memory. Epilogue: RMSNorm and scale
-// straight out of tensor memory. Warp 0 = TMA producer, warp 1 = MMA issuer / TMEM owner,
-// warps 4-7 = softmax and epilogue. Every wait is bounded.
+// Structure: one CTA per 128-row query tile of one unit, 128-key tiles (a tcgen05.mma with
+// M = 128 has a fixed cost of ~95 cycles, so score MMAs use N = 128 and value MMAs N = dv).
+//   pass 1: S1, S2 (128 fp32 columns each) double-buffered over all 512 TMEM columns;
+//   pass 2: S1, S2 single-buffered in columns 0..255, O (128 x dv fp32) in columns 256..;
+//           D goes to shared memory (128B-swizzled K-major), so the next score MMA overlaps the
+//           D computation; the value MMA reads D and V from shared memory.
+// TMA stages Q1|Q2 once and a ring of K tiles (one load per map; each K tile is streamed twice,
+// once per pass) and V half tiles (pass 2 only), issued in exactly the order the MMA issuer
+// consumes them so that no load waits behind a slot of another kind. Two softmax warpgroups (one
+// thread per query row each) split every tile's 128 keys; their partial row statistics merge
+// once at the pass boundary. Epilogue: RMSNorm and scale straight out of tensor memory, the two
+// warpgroups taking half of the columns each. Warp 0 = TMA producer, warp 1 = MMA issuer and
+// TMEM owner, warps 4-11 = softmax and epilogue. Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -38,37 +43,42 @@ namespace da {
 namespace exact {
 
 constexpr int BM = 128;
-constexpr int BN = 64;
-constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 softmax
+constexpr int BN = 128;
+constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 softmax
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kSmemLimit = 232448;  // bytes of shared memory one CTA may use
 
 template <int DQK, int DV, bool SHARED_K>
 struct Cfg {
-  static constexpr int kQChunk = BM * 128;                 // 128 rows x 64 bf16
-  static constexpr int kKChunk = BN * 128;                 // 64 rows x 64 bf16
-  static constexpr int kQMapBytes = BM * DQK * 2;          // one map's Q tile
-  static constexpr int kKMapBytes = BN * DQK * 2;          // one map's K tile
+  static constexpr int kChunk = 128 * 128;              // 128 rows x 64 bf16 (one TMA box)
+  static constexpr int kQMapBytes = BM * DQK * 2;       // one map's Q tile
+  static constexpr int kKMapBytes = BN * DQK * 2;       // one map's K tile (one load)
   static constexpr int kQBytes = 2 * kQMapBytes;
-  static constexpr int kKBytes = (SHARED_K ? 1 : 2) * kKMapBytes;  // one K tile (both maps)
-  static constexpr int kVBytes = BN * DV * 2;              // one V tile
-  // One ring of slots holds K and V tiles in the order the MMA issuer consumes them.
-  static constexpr int kSlot = kKBytes > kVBytes ? kKBytes : kVBytes;
-  static constexpr int NSLOT = (kSlot >= 32768) ? 4 : 8;
+  static constexpr int kKLoads = SHARED_K ? 1 : 2;      // K loads per key tile
+  static constexpr int kVHalfChunk = (BN / 2) * 128;    // 64 keys x 64 bf16
+  static constexpr int kVHalfBytes = (BN / 2) * DV * 2; // half of a V tile (one load)
+  static constexpr int kDBytes = BM * BN * 2;           // D tile (bf16)
+  static constexpr int kSlot = kKMapBytes > kVHalfBytes ? kKMapBytes : kVHalfBytes;
+  static constexpr int kRingBudget = kSmemLimit - 2048 - 1024 - kQBytes - kDBytes;
+  static constexpr int NSLOT = (kRingBudget / kSlot) > 8 ? 8 : (kRingBudget / kSlot);
   static constexpr int kQOff = 0;
-  static constexpr int kSlotOff = kQOff + kQBytes;
+  static constexpr int kDOff = kQOff + kQBytes;
+  static constexpr int kSlotOff = kDOff + kDBytes;
   static constexpr int kEnd = kSlotOff + NSLOT * kSlot;
-  static constexpr int kDynSmem = kEnd + 1024;
+  static constexpr int kDynSmem = kEnd + 1024;          // + slack for 1024 B alignment
   static constexpr int kOCol = 256;
+  static_assert(NSLOT >= kKLoads + 2, "each load of a key tile needs its own slot");
   static_assert(kOCol + DV <= kTmemCols, "TMEM budget");
-  static_assert(kDynSmem + 8192 <= 232448, "shared memory budget (dynamic + static)");
+  static_assert(kDynSmem + 2048 <= kSmemLimit, "shared memory budget (dynamic + static)");
 };
 
 struct Barriers {
   uint64_t q_full;
   uint64_t slot_full[8], slot_empty[8];
-  uint64_t s_full[2], s_done[2];
+  uint64_t s_full[2], s_free[2];  // scores in TMEM buffer b ready / read by both warpgroups
+  uint64_t d_full, d_empty;       // D tile in shared memory written / consumed
   uint64_t o_full;
   uint64_t teardown;
 };
@@ -76,7 +86,7 @@ struct Barriers {
 struct KParams {
   Problem p;
   int n_qt;
-  int group;        // (batch, unit) pairs whose K/V share L2 in one launch-order group
+  int group;  // (batch, unit) pairs whose K/V share L2 in one launch-order group
   float scale_log2;
 };
 
@@ -91,21 +101,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ Barriers bars;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ float stats[2][4][BM];  // per-warpgroup partial row statistics
-  __shared__ float sumsq[2][BM];     // per-warpgroup partial RMSNorm sums of squares
 
   const Problem& P = kp.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sQ = smem_u32(smem + C::kQOff);
+  const uint32_t sD = smem_u32(smem + C::kDOff);
   const uint32_t sSlot = smem_u32(smem + C::kSlotOff);
+  // The D buffer doubles as scratch for the warpgroups' statistics merge (pass boundary) and
+  // the sums of squares (epilogue): D is not in use at either point.
+  float* scratch = reinterpret_cast<float*>(smem + C::kDOff);
 
-  // ---- work item: longest causal tiles first ----
-  const int BU = P.B * P.units;
-  const bool causal = (P.flags & 1) != 0;
   // Launch order: (batch, unit) pairs are taken in groups whose K/V fit in L2 together; inside a
   // group the query tiles go longest-first (causal) across the group's pairs.
+  const int BU = P.B * P.units;
+  const bool causal = (P.flags & 1) != 0;
   const int item = blockIdx.x;
   const int g0 = (item / (kp.group * kp.n_qt)) * kp.group;
   const int gsize = min(kp.group, BU - g0);
@@ -114,11 +125,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bu = g0 + r_in % gsize;
   const int b = bu / P.units, u = bu % P.units;
   const int n_kv_all = (P.N + BN - 1) / BN;
-  const int n = causal ? min((qt * BM + BM + BN - 1) / BN, n_kv_all) : n_kv_all;
+  const int n = causal ? min(qt + 1, n_kv_all) : n_kv_all;  // BM == BN
   const int T = 2 * n;  // tiles over both passes
-  // Ring order of the loads: K(0..n-1) for pass 1, then K(n+j), V(j) alternately for pass 2.
-  auto k_load = [n](int t) { return t < n ? t : 2 * t - n; };
-  auto v_load = [n](int jv) { return n + 2 * jv + 1; };
+
+  // Ring order of the loads = the order in which the MMA issuer consumes them. Iteration t of
+  // the issuer uses the K loads of tile t (one per map, or one shared K) and then, for t > n,
+  // the two V halves of pass-2 tile jv = t - 1 - n. base(t) = index of iteration t's first load.
+  constexpr int KL = C::kKLoads;
+  auto base = [n](int t) { return t * KL + 2 * max(0, t - n - 1); };
+  auto k_load = [&](int t, int r) { return base(t) + r; };
+  auto v_load = [&](int jv, int h) {
+    const int t = n + 1 + jv;
+    return base(t) + (t < T ? KL : 0) + h;
+  };
+  // TMEM score buffer of tile t and its use count on that buffer (barrier phase index).
+  auto sbuf = [n](int t) { return t < n ? (t & 1) : 0; };
+  auto suse = [n](int t) { return t < n ? (t >> 1) : ((n + 1) >> 1) + (t - n); };
 
   auto bar = [](uint64_t& x) { return smem_u32(&x); };
 
@@ -130,8 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(bars.s_full[i]), 1);
-      mbar_init(bar(bars.s_done[i]), 128);
+      mbar_init(bar(bars.s_free[i]), 256);
     }
+    mbar_init(bar(bars.d_full), 256);
+    mbar_init(bar(bars.d_empty), 1);
     mbar_init(bar(bars.o_full), 1);
     mbar_init(bar(bars.teardown), 1);
     abort_flag = 0;
@@ -161,33 +185,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(bar(bars.q_full), C::kQBytes);
       for (int r = 0; r < 2; ++r)
         for (int c = 0; c < DQK / 64; ++c)
-          tma_load_4d(sQ + r * C::kQMapBytes + c * C::kQChunk, &tm_q, bar(bars.q_full),
+          tma_load_4d(sQ + r * C::kQMapBytes + c * C::kChunk, &tm_q, bar(bars.q_full),
                       q_col_of(P, r) + 64 * c, q_head_of(P, u, r), qt * BM, b);
       int issued = 0;  // loads issued into the ring
-      bool ok = true;
       auto acquire = [&](int idx, uint32_t bytes) -> int {
         const int slot = idx % NSLOT;
         if (!mbar_wait(bar(bars.slot_empty[slot]), ((idx / NSLOT) & 1) ^ 1, abrt)) return -1;
         mbar_arrive_expect_tx(bar(bars.slot_full[slot]), bytes);
         return slot;
       };
-      for (int t = 0; t < T && ok; ++t) {
-        const int j = t < n ? t : t - n;
-        const int ks = acquire(k_load(t), C::kKBytes);
-        if (!(ok = ks >= 0)) break;
-        for (int r = 0; r < (SHARED_K ? 1 : 2); ++r)
-          for (int c = 0; c < DQK / 64; ++c)
-            tma_load_4d(sSlot + ks * C::kSlot + r * C::kKMapBytes + c * C::kKChunk, &tm_k,
-                        bar(bars.slot_full[ks]), k_col_of(P, r) + 64 * c, kvh, j * BN, b);
-        issued = k_load(t) + 1;
-        if (t >= n) {
-          const int jv = t - n;
-          const int vs = acquire(v_load(jv), C::kVBytes);
-          if (!(ok = vs >= 0)) break;
-          for (int c = 0; c < DV / 64; ++c)
-            tma_load_4d(sSlot + vs * C::kSlot + c * C::kKChunk, &tm_v, bar(bars.slot_full[vs]),
-                        64 * c, kvh, jv * BN, b);
-          issued = v_load(jv) + 1;
+      bool ok = true;
+      for (int t = 0; t <= T && ok; ++t) {
+        if (t < T) {
+          const int j = t < n ? t : t - n;
+          for (int r = 0; r < KL && ok; ++r) {
+            const int ks = acquire(k_load(t, r), C::kKMapBytes);
+            if (ks < 0) {
+              ok = false;
+              break;
+            }
+            for (int c = 0; c < DQK / 64; ++c)
+              tma_load_4d(sSlot + ks * C::kSlot + c * C::kChunk, &tm_k, bar(bars.slot_full[ks]),
+                          k_col_of(P, r) + 64 * c, kvh, j * BN, b);
+            issued = k_load(t, r) + 1;
+          }
+        }
+        if (ok && t >= n + 1) {
+          const int jv = t - n - 1;
+          for (int h = 0; h < 2 && ok; ++h) {
+            const int vs = acquire(v_load(jv, h), C::kVHalfBytes);
+            if (vs < 0) {
+              ok = false;
+              break;
+            }
+            for (int c = 0; c < DV / 64; ++c)
+              tma_load_4d(sSlot + vs * C::kSlot + c * C::kVHalfChunk, &tm_v,
+                          bar(bars.slot_full[vs]), 64 * c, kvh, jv * BN + 64 * h, b);
+            issued = v_load(jv, h) + 1;
+          }
         }
       }
       // make sure no copy of ours is still landing in shared memory
@@ -200,45 +235,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idesc_o = umma_idesc_bf16(BM, DV, 0, 1);
+      // Descriptors are built once; each k-step adds a constant offset.
+      const uint64_t dq0 = umma_smem_desc(sQ, 16, 1024);
+      const uint64_t dslot0 = umma_smem_desc(sSlot, 16, 1024);
+      const uint64_t dv0 = umma_smem_desc(sSlot, C::kVHalfChunk, 1024);  // V: MN-major, LBO = chunk
+      const uint64_t dd0 = umma_smem_desc(sD, 16, 1024);
       bool ok = mbar_wait(bar(bars.q_full), 0, abrt);
       tc_fence_after();
       for (int t = 0; ok && t <= T; ++t) {
         if (t < T) {
-          const int buf = t & 1, ki = k_load(t), s = ki % NSLOT;
-          // S buffer `buf` was last used by tile t-2: its scores must have been read (pass 1)
-          // or replaced by D and handed over (pass 2; that D's product was issued already).
-          if (t >= 2 && !(ok = mbar_wait(bar(bars.s_done[buf]), ((t - 2) >> 1) & 1, abrt))) break;
-          if (!(ok = mbar_wait(bar(bars.slot_full[s]), (ki / NSLOT) & 1, abrt))) break;
-          tc_fence_after();
+          const int buf = sbuf(t);
+          // The buffer's previous scores must have been read by both warpgroups: tile t-2 in
+          // pass 1 (two buffers), tile t-1 in pass 2 (one buffer; reading t-1 implies t-2).
+          const int prev = t < n ? t - 2 : t - 1;
+          if (prev >= 0 &&
+              !(ok = mbar_wait(bar(bars.s_free[sbuf(prev)]), suse(prev) & 1, abrt)))
+            break;
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const uint32_t d_s = tmem + buf * 128 + r * 64;
-            const uint32_t kbase = sSlot + s * C::kSlot + (SHARED_K ? 0 : r * C::kKMapBytes);
+            const int ki = k_load(t, SHARED_K ? 0 : r), s = ki % NSLOT;
+            if (r < KL) {
+              if (!(ok = mbar_wait(bar(bars.slot_full[s]), (ki / NSLOT) & 1, abrt))) break;
+              tc_fence_after();
+            }
+            const uint32_t d_s = tmem + buf * 256 + r * 128;
+            const uint64_t qd = desc_add(dq0, r * C::kQMapBytes);
+            const uint64_t kd = desc_add(dslot0, s * C::kSlot);
 #pragma unroll
             for (int kk = 0; kk < DQK / 16; ++kk) {
-              const uint64_t ad = umma_smem_desc(
-                  sQ + r * C::kQMapBytes + (kk >> 2) * C::kQChunk + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd =
-                  umma_smem_desc(kbase + (kk >> 2) * C::kKChunk + (kk & 3) * 32, 16, 1024);
-              mma_bf16_ss(d_s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+              const uint32_t off = (kk >> 2) * C::kChunk + (kk & 3) * 32;
+              mma_bf16_ss(d_s, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0 ? 1u : 0u);
             }
+            if (r == 1 || !SHARED_K) tc_commit(bar(bars.slot_empty[s]));
           }
-          tc_commit(bar(bars.slot_empty[s]));
+          if (!ok) break;
           tc_commit(bar(bars.s_full[buf]));
         }
         const int tp = t - 1;
         if (tp >= n) {
-          const int bp = tp & 1, jv = tp - n, vi = v_load(jv), sv = vi % NSLOT;
-          if (!(ok = mbar_wait(bar(bars.s_done[bp]), (tp >> 1) & 1, abrt))) break;
-          if (!(ok = mbar_wait(bar(bars.slot_full[sv]), (vi / NSLOT) & 1, abrt))) break;
-          tc_fence_after();
+          const int jv = tp - n;
+          if (!(ok = mbar_wait(bar(bars.d_full), jv & 1, abrt))) break;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t a_t = tmem + bp * 128 + kk * 8;  // D: 16 bf16 keys per 8 columns
-            const uint64_t bd = umma_smem_desc(sSlot + sv * C::kSlot + kk * 2048, C::kKChunk, 1024);
-            mma_bf16_ts(tmem + C::kOCol, a_t, bd, idesc_o, (jv > 0 || kk > 0) ? 1u : 0u);
+          for (int h = 0; h < 2; ++h) {
+            const int vi = v_load(jv, h), sv = vi % NSLOT;
+            if (!(ok = mbar_wait(bar(bars.slot_full[sv]), (vi / NSLOT) & 1, abrt))) break;
+            tc_fence_after();
+            const uint64_t vd = desc_add(dv0, sv * C::kSlot);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              // A = D (128 rows x 16 keys, K-major), B = V half (16 keys x dv, MN-major)
+              const int kk = 4 * h + k4;
+              const uint64_t ad = desc_add(dd0, (kk >> 2) * C::kChunk + (kk & 3) * 32);
+              mma_bf16_ss(tmem + C::kOCol, ad, desc_add(vd, k4 * 2048), idesc_o,
+                          (jv > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(bar(bars.slot_empty[sv]));
           }
-          tc_commit(bar(bars.slot_empty[sv]));
+          if (!ok) break;
+          tc_commit(bar(bars.d_empty));
           if (tp == T - 1) tc_commit(bar(bars.o_full));
         }
       }
@@ -247,8 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ============================ softmax and epilogue ============================
-    // Two warpgroups: WG w owns the tiles t with t % 2 == w (and TMEM score buffer w), so one
-    // warpgroup turns S into statistics or D while the other waits for its next scores.
+    // Warpgroup wg handles keys [64 wg, 64 wg + 64) of every tile (both maps) for its row.
     const int wg = (warp - kSoftmaxWarp0) >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int row = qt * BM + r;
@@ -259,16 +312,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     float bias[2] = {0.f, 0.f}, lam = 0.f;
     bool ok = true, merged = false;
 
-    // Merge the two warpgroups' partial row statistics (once, at the pass boundary).
+    // Merge the two warpgroups' partial row statistics (once, at the pass boundary). The D
+    // buffer is free then: no D has been written yet.
     auto merge = [&]() {
-      stats[wg][0][r] = m[0];
-      stats[wg][1][r] = l[0];
-      stats[wg][2][r] = m[1];
-      stats[wg][3][r] = l[1];
+      float* st = scratch + (wg * 4) * BM;
+      st[0 * BM + r] = m[0];
+      st[1 * BM + r] = l[0];
+      st[2 * BM + r] = m[1];
+      st[3 * BM + r] = l[1];
       named_barrier_sync(1, 256);
+      const float* so = scratch + ((wg ^ 1) * 4) * BM;
 #pragma unroll
       for (int mp = 0; mp < 2; ++mp) {
-        const float mo = stats[wg ^ 1][2 * mp][r], lo = stats[wg ^ 1][2 * mp + 1][r];
+        const float mo = so[(2 * mp) * BM + r], lo = so[(2 * mp + 1) * BM + r];
         const float M = fmaxf(m[mp], mo);
         const float L = (m[mp] == -INFINITY ? 0.f : l[mp] * ex2_approx(m[mp] - M)) +
                         (mo == -INFINITY ? 0.f : lo * ex2_approx(mo - M));
@@ -280,26 +336,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float z = P.lam_logit[(static_cast<size_t>(b) * P.N + row) * P.units + u];
         lam = 1.f / (1.f + expf(-z));
       }
+      named_barrier_sync(1, 256);  // both have read the scratch before D overwrites it
       merged = true;
     };
 
-    for (int t = wg; t < T; t += 2) {
-      const int buf = t & 1;
+    // This thread's 16-byte units of the D tile (row r, keys 64 wg .. 64 wg + 63): 128B-swizzled
+    // K-major layout, unit u of the row lands at (u ^ (r % 8)) within the row's 128 bytes.
+    const uint32_t d_row = sD + wg * C::kChunk + r * 128;
+
+    for (int t = 0; t < T; ++t) {
       const bool pass2 = t >= n;
       if (pass2 && !merged) merge();
-      const int key0 = (pass2 ? t - n : t) * BN;
-      ok = mbar_wait(bar(bars.s_full[buf]), (t >> 1) & 1, abrt);
-      if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+      const int buf = sbuf(t);
+      const int key0 = (pass2 ? t - n : t) * BN + 64 * wg;
+      ok = mbar_wait(bar(bars.s_full[buf]), suse(t) & 1, abrt);
+      if (__any_sync(0xffffffffu, !ok)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       uint32_t sr[2][64];
-      tmem_ld32(tmem + tl + buf * 128 + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0][0]));
-      tmem_ld32(tmem + tl + buf * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[0][32]));
-      tmem_ld32(tmem + tl + buf * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[1][0]));
-      tmem_ld32(tmem + tl + buf * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[1][32]));
+      const uint32_t sb = tmem + tl + buf * 256 + 64 * wg;
+      tmem_ld32(sb + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0][0]));
+      tmem_ld32(sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[0][32]));
+      tmem_ld32(sb + 128, *reinterpret_cast<uint32_t(*)[32]>(&sr[1][0]));
+      tmem_ld32(sb + 160, *reinterpret_cast<uint32_t(*)[32]>(&sr[1][32]));
       tmem_wait_ld();
-      if (key0 + BN > lim) {
+      tc_fence_before();
+      mbar_arrive(bar(bars.s_free[buf]));  // scores are in registers: the buffer is free
+      if (key0 + 64 > lim) {
 #pragma unroll
-        for (int i = 0; i < BN; ++i)
+        for (int i = 0; i < 64; ++i)
           if (key0 + i >= lim) {
             sr[0][i] = __float_as_uint(-INFINITY);
             sr[1][i] = __float_as_uint(-INFINITY);
@@ -308,28 +375,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (!pass2) {
         // ---- pass 1: exact row max and row sum of each map (online over key tiles) ----
-        tc_fence_before();
-        mbar_arrive(bar(bars.s_done[buf]));  // scores are in registers: the buffer is free
 #pragma unroll
         for (int mp = 0; mp < 2; ++mp) {
           float mx[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) mx[i] = __uint_as_float(sr[mp][i]);
 #pragma unroll
-          for (int i = 4; i < BN; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(sr[mp][i]));
+          for (int i = 4; i < 64; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(sr[mp][i]));
           const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
           const float mn = fmaxf(m[mp], mt);
           if (mn == -INFINITY) continue;  // every key of this tile is masked for this row
           const float nb = -mn;
           float la[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i < BN; ++i)
+          for (int i = 0; i < 64; ++i)
             la[i & 3] += ex2_approx(fmaf(__uint_as_float(sr[mp][i]), sl2, nb));
           l[mp] = l[mp] * ex2_approx(m[mp] + nb) + ((la[0] + la[1]) + (la[2] + la[3]));
           m[mp] = mn;
         }
       } else {
-        // ---- pass 2: D = A1 - lambda A2 in fp32, rounded once to bf16 ----
+        // ---- pass 2: D = A1 - lambda A2 in fp32, rounded once to bf16, into shared memory ----
+        const int jv = t - n;
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -339,10 +405,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float c1 = ex2_approx(fmaf(__uint_as_float(sr[1][2 * i + 1]), sl2, bias[1]));
           pk[i] = pack_bf16x2(fmaf(-lam, c0, a0), fmaf(-lam, c1, a1));
         }
-        tmem_st32(tmem + tl + buf * 128, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(bars.s_done[buf]));
+        // the previous D must have been consumed by its value MMA
+        if (jv > 0) {
+          ok = mbar_wait(bar(bars.d_empty), (jv - 1) & 1, abrt);
+          if (__any_sync(0xffffffffu, !ok)) {
+            ok = false;
+            break;
+          }
+        }
+#pragma unroll
+        for (int uu = 0; uu < 8; ++uu)
+          st_shared_v4(d_row + ((uu ^ (r & 7)) << 4), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2],
+                       pk[4 * uu + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(bars.d_full));
       }
     }
     if (!merged) merge();
@@ -352,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_after();
     // ------------------------------- epilogue -------------------------------------
-    // WG w owns columns [w * DV/2, (w+1) * DV/2) of each row; the RMSNorm sum of squares is
-    // combined across the two warpgroups.
+    // Warpgroup wg owns columns [wg * dv/2, (wg+1) * dv/2) of each row; the RMSNorm sum of
+    // squares is combined across the two warpgroups (scratch = D buffer, idle after o_full).
     constexpr int HC = DV / 2;
     const int c0 = wg * HC;
     float ss = 0.f;
@@ -369,9 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     float scale = 1.f;
     if (P.flags & 2) {
-      sumsq[wg][r] = ss;
+      scratch[wg * BM + r] = ss;
       named_barrier_sync(1, 256);
-      scale = 1.f / sqrtf((ss + sumsq[wg ^ 1][r]) / static_cast<float>(DV) + P.eps);
+      scale = 1.f / sqrtf((ss + scratch[(wg ^ 1) * BM + r]) / static_cast<float>(DV) + P.eps);
     }
     if (P.flags & 4) scale *= (1.f - P.lambda_init);
     if (ok) {
@@ -429,7 +505,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 4-D bf16 map over [B, N, heads, cols] with a 64-col x 1 x rows x 1 box, 128-byte swizzle,
+// 4-D bf16 map over [B, N, heads, cols] with a 64-col x 1 x box_rows x 1 box, 128-byte swizzle,
 // zero fill out of bounds.
 static bool make_map(CUtensorMap* m, const void* base, int cols, int heads, int N, int B,
                      int box_rows, char* err, size_t err_len) {
@@ -459,7 +535,7 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, p.q, p.q_cols, p.q_heads, p.N, p.B, BM, err, err_len) ||
       !make_map(&mk, p.k, p.k_cols, p.kv_heads, p.N, p.B, BN, err, err_len) ||
-      !make_map(&mv, p.v, DV, p.kv_heads, p.N, p.B, BN, err, err_len))
+      !make_map(&mv, p.v, DV, p.kv_heads, p.N, p.B, BN / 2, err, err_len))
     return cudaErrorInvalidValue;
   auto kern = prefill_exact_kernel<DQK, DV, SHARED_K>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);

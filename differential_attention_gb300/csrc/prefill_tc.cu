@@ -192,6 +192,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idesc_o = umma_idesc_bf16(BM, DV, 0, 1);
+      // Descriptors are built once; each k-step adds a constant offset.
+      const uint64_t dq0 = umma_smem_desc(sQ, 16, 1024);
+      const uint64_t dk0 = umma_smem_desc(sK, 16, 1024);
+      const uint64_t dv0 = umma_smem_desc(sV, C::kChunkBytes, 1024);
       bool ok = mbar_wait(bar(bars.q_full), 0, abrt);
       tc_fence_after();
       for (int j = 0; ok && j <= n_kv; ++j) {
@@ -203,9 +207,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-            const uint64_t ad = umma_smem_desc(sQ + off, 16, 1024);
-            const uint64_t bd = umma_smem_desc(sK + s * C::kKBytes + off, 16, 1024);
-            mma_bf16_ss(d_s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(d_s, desc_add(dq0, off), desc_add(dk0, s * C::kKBytes + off), idesc_s,
+                        kk > 0 ? 1u : 0u);
           }
           tc_commit(bar(bars.k_empty[s]));
           tc_commit(bar(bars.s_full[buf]));
@@ -218,8 +221,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             const uint32_t a_t = tmem + C::kSCol + bp * BN + kk * 8;  // 16 bf16 keys = 8 cols
-            const uint64_t bd = umma_smem_desc(sV + sp * C::kVBytes + kk * 2048, C::kChunkBytes, 1024);
-            mma_bf16_ts(tmem + C::kOCol, a_t, bd, idesc_o, (jp > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ts(tmem + C::kOCol, a_t, desc_add(dv0, sp * C::kVBytes + kk * 2048), idesc_o,
+                        (jp > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(bar(bars.v_empty[sp]));
           tc_commit(bar(bars.o_done));

@@ -265,6 +265,17 @@ __device__ __forceinline__ uint64_t umma_smem_desc(uint32_t saddr, uint32_t lbo_
   return d;
 }
 
+// Add a byte offset to the start-address field of a shared-memory descriptor. No carry can leave
+// the 14-bit field as long as every address stays below 256 KB (all of shared memory).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
 // c_format bits 4-5 (1 = f32), a_format bits 7-9 (1 = bf16), b_format bits 10-12 (1 = bf16),
 // a_major bit 15, b_major bit 16 (0 = K-major, 1 = MN-major), N>>3 at bits 17-22, M>>4 at 24-28.
