@@ -24,11 +24,11 @@
 //           D computation; the value MMA reads D and V from shared memory.
 // TMA stages Q1|Q2 once and a ring of K tiles (one load per map; each K tile is streamed twice,
 // once per pass) and V half tiles (pass 2 only), issued in exactly the order the MMA issuer
-// consumes them so that no load waits behind a slot of another kind. Two softmax warpgroups (one
+// consumes them so that no load waits behind a slot of another kind. Four softmax warpgroups (one
 // thread per query row each) split every tile's 128 keys; their partial row statistics merge
-// once at the pass boundary. Epilogue: RMSNorm and scale straight out of tensor memory, the two
-// warpgroups taking half of the columns each. Warp 0 = TMA producer, warp 1 = MMA issuer and
-// TMEM owner, warps 4-11 = softmax and epilogue. Every wait is bounded.
+// once at the pass boundary. Epilogue: RMSNorm and scale straight out of tensor memory, each
+// warpgroup taking a quarter of the columns. Warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
+// owner, warps 2-17 = softmax and epilogue. Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -44,8 +44,11 @@ namespace exact {
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 softmax
-constexpr int kSoftmaxWarp0 = 4;
+constexpr int kSoftmaxWarp0 = 2;  // warp 0 TMA, warp 1 MMA, warps 2..17 softmax
+constexpr int kNumWG = 4;         // softmax warpgroups; each takes 32 keys of every tile
+constexpr int kSoftmaxThreads = 128 * kNumWG;
+constexpr int kThreads = 32 * kSoftmaxWarp0 + kSoftmaxThreads;
+constexpr int KW = 128 / kNumWG;  // keys per warpgroup per tile
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kSmemLimit = 232448;  // bytes of shared memory one CTA may use
@@ -152,9 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(bars.s_full[i]), 1);
-      mbar_init(bar(bars.s_free[i]), 256);
+      mbar_init(bar(bars.s_free[i]), kSoftmaxThreads);
     }
-    mbar_init(bar(bars.d_full), 256);
+    mbar_init(bar(bars.d_full), kSoftmaxThreads);
     mbar_init(bar(bars.d_empty), 1);
     mbar_init(bar(bars.o_full), 1);
     mbar_init(bar(bars.teardown), 1);
@@ -301,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ============================ softmax and epilogue ============================
-    // Warpgroup wg handles keys [64 wg, 64 wg + 64) of every tile (both maps) for its row.
+    // Warpgroup wg (warps 2+4wg .. 5+4wg, which cover the four TMEM lane quarters) handles keys
+    // [32 wg, 32 wg + 32) of every tile, both maps, for its query row.
     const int wg = (warp - kSoftmaxWarp0) >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int row = qt * BM + r;
@@ -312,22 +316,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     float bias[2] = {0.f, 0.f}, lam = 0.f;
     bool ok = true, merged = false;
 
-    // Merge the two warpgroups' partial row statistics (once, at the pass boundary). The D
-    // buffer is free then: no D has been written yet.
+    // Merge the warpgroups' partial row statistics (once, at the pass boundary). The D buffer
+    // is free then: no D has been written yet.
     auto merge = [&]() {
       float* st = scratch + (wg * 4) * BM;
       st[0 * BM + r] = m[0];
       st[1 * BM + r] = l[0];
       st[2 * BM + r] = m[1];
       st[3 * BM + r] = l[1];
-      named_barrier_sync(1, 256);
-      const float* so = scratch + ((wg ^ 1) * 4) * BM;
+      named_barrier_sync(1, kSoftmaxThreads);
 #pragma unroll
       for (int mp = 0; mp < 2; ++mp) {
-        const float mo = so[(2 * mp) * BM + r], lo = so[(2 * mp + 1) * BM + r];
-        const float M = fmaxf(m[mp], mo);
-        const float L = (m[mp] == -INFINITY ? 0.f : l[mp] * ex2_approx(m[mp] - M)) +
-                        (mo == -INFINITY ? 0.f : lo * ex2_approx(mo - M));
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kNumWG; ++w) M = fmaxf(M, scratch[(w * 4 + 2 * mp) * BM + r]);
+        float L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNumWG; ++w) {
+          const float mw = scratch[(w * 4 + 2 * mp) * BM + r];
+          if (mw != -INFINITY) L += scratch[(w * 4 + 2 * mp + 1) * BM + r] * ex2_approx(mw - M);
+        }
         bias[mp] = -(M + __log2f(L));
       }
       if (P.mode == MODE_V1) {
@@ -336,37 +344,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float z = P.lam_logit[(static_cast<size_t>(b) * P.N + row) * P.units + u];
         lam = 1.f / (1.f + expf(-z));
       }
-      named_barrier_sync(1, 256);  // both have read the scratch before D overwrites it
+      named_barrier_sync(1, kSoftmaxThreads);  // all have read the scratch before D overwrites it
       merged = true;
     };
 
-    // This thread's 16-byte units of the D tile (row r, keys 64 wg .. 64 wg + 63): 128B-swizzled
-    // K-major layout, unit u of the row lands at (u ^ (r % 8)) within the row's 128 bytes.
-    const uint32_t d_row = sD + wg * C::kChunk + r * 128;
+    // This thread's part of the D tile: row r, keys 32 wg .. 32 wg + 31 = 16-byte units
+    // 4 (wg & 1) .. +3 of 64-key chunk wg / 2, in the 128B-swizzled K-major layout (unit u of a
+    // row lands at u ^ (r % 8) within the row's 128 bytes).
+    const uint32_t d_row = sD + (wg >> 1) * C::kChunk + r * 128;
+    const int u0 = (wg & 1) * 4;
 
     for (int t = 0; t < T; ++t) {
       const bool pass2 = t >= n;
       if (pass2 && !merged) merge();
       const int buf = sbuf(t);
-      const int key0 = (pass2 ? t - n : t) * BN + 64 * wg;
+      const int key0 = (pass2 ? t - n : t) * BN + KW * wg;
       ok = mbar_wait(bar(bars.s_full[buf]), suse(t) & 1, abrt);
       if (__any_sync(0xffffffffu, !ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sr[2][64];
-      const uint32_t sb = tmem + tl + buf * 256 + 64 * wg;
-      tmem_ld32(sb + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0][0]));
-      tmem_ld32(sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[0][32]));
-      tmem_ld32(sb + 128, *reinterpret_cast<uint32_t(*)[32]>(&sr[1][0]));
-      tmem_ld32(sb + 160, *reinterpret_cast<uint32_t(*)[32]>(&sr[1][32]));
+      uint32_t sr[2][KW];
+      const uint32_t sb = tmem + tl + buf * 256 + KW * wg;
+      tmem_ld32(sb, sr[0]);
+      tmem_ld32(sb + 128, sr[1]);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar(bars.s_free[buf]));  // scores are in registers: the buffer is free
-      if (key0 + 64 > lim) {
+      if (key0 + KW > lim) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
+        for (int i = 0; i < KW; ++i)
           if (key0 + i >= lim) {
             sr[0][i] = __float_as_uint(-INFINITY);
             sr[1][i] = __float_as_uint(-INFINITY);
@@ -377,33 +385,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- pass 1: exact row max and row sum of each map (online over key tiles) ----
 #pragma unroll
         for (int mp = 0; mp < 2; ++mp) {
-          float mx[4];
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) mx[i] = __uint_as_float(sr[mp][i]);
-#pragma unroll
-          for (int i = 4; i < 64; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(sr[mp][i]));
-          const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+          for (int i = 0; i < KW; i += 2)
+            mx[(i >> 1) & 3] = fmax3(mx[(i >> 1) & 3], __uint_as_float(sr[mp][i]),
+                                     __uint_as_float(sr[mp][i + 1]));
+          const float mt = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * sl2;
           const float mn = fmaxf(m[mp], mt);
           if (mn == -INFINITY) continue;  // every key of this tile is masked for this row
           const float nb = -mn;
-          float la[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint64_t scale2 = f2pack(sl2, sl2), off2 = f2pack(nb, nb);
+          uint64_t acc[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
-            la[i & 3] += ex2_approx(fmaf(__uint_as_float(sr[mp][i]), sl2, nb));
-          l[mp] = l[mp] * ex2_approx(m[mp] + nb) + ((la[0] + la[1]) + (la[2] + la[3]));
+          for (int i = 0; i < KW; i += 2) {
+            float x0, x1;
+            f2unpack(f2fma(f2pack(__uint_as_float(sr[mp][i]), __uint_as_float(sr[mp][i + 1])),
+                           scale2, off2),
+                     x0, x1);
+            acc[(i >> 1) & 1] = f2add(acc[(i >> 1) & 1], f2pack(ex2_approx(x0), ex2_approx(x1)));
+          }
+          float a0, a1, a2, a3;
+          f2unpack(acc[0], a0, a1);
+          f2unpack(acc[1], a2, a3);
+          l[mp] = l[mp] * ex2_approx(m[mp] + nb) + ((a0 + a1) + (a2 + a3));
           m[mp] = mn;
         }
       } else {
         // ---- pass 2: D = A1 - lambda A2 in fp32, rounded once to bf16, into shared memory ----
         const int jv = t - n;
-        uint32_t pk[32];
+        const uint64_t scale2 = f2pack(sl2, sl2), bias2 = f2pack(bias[0], bias[1]);
+        const uint64_t nlam2 = f2pack(-lam, -lam);
+        uint32_t pk[KW / 2];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float a0 = ex2_approx(fmaf(__uint_as_float(sr[0][2 * i]), sl2, bias[0]));
-          const float a1 = ex2_approx(fmaf(__uint_as_float(sr[0][2 * i + 1]), sl2, bias[0]));
-          const float c0 = ex2_approx(fmaf(__uint_as_float(sr[1][2 * i]), sl2, bias[1]));
-          const float c1 = ex2_approx(fmaf(__uint_as_float(sr[1][2 * i + 1]), sl2, bias[1]));
-          pk[i] = pack_bf16x2(fmaf(-lam, c0, a0), fmaf(-lam, c1, a1));
+        for (int i = 0; i < KW / 2; ++i) {
+          float x1a, x2a, x1b, x2b;  // (map 1, map 2) of keys 2i and 2i+1
+          f2unpack(f2fma(f2pack(__uint_as_float(sr[0][2 * i]), __uint_as_float(sr[1][2 * i])),
+                         scale2, bias2),
+                   x1a, x2a);
+          f2unpack(f2fma(f2pack(__uint_as_float(sr[0][2 * i + 1]),
+                                __uint_as_float(sr[1][2 * i + 1])),
+                         scale2, bias2),
+                   x1b, x2b);
+          float da, db;
+          f2unpack(f2fma(nlam2, f2pack(ex2_approx(x2a), ex2_approx(x2b)),
+                         f2pack(ex2_approx(x1a), ex2_approx(x1b))),
+                   da, db);
+          pk[i] = pack_bf16x2(da, db);
         }
         // the previous D must have been consumed by its value MMA
         if (jv > 0) {
@@ -414,9 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 #pragma unroll
-        for (int uu = 0; uu < 8; ++uu)
-          st_shared_v4(d_row + ((uu ^ (r & 7)) << 4), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2],
-                       pk[4 * uu + 3]);
+        for (int uu = 0; uu < KW / 8; ++uu)
+          st_shared_v4(d_row + (((u0 + uu) ^ (r & 7)) << 4), pk[4 * uu], pk[4 * uu + 1],
+                       pk[4 * uu + 2], pk[4 * uu + 3]);
         fence_proxy_async_smem();
         mbar_arrive(bar(bars.d_full));
       }
@@ -428,26 +455,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_after();
     // ------------------------------- epilogue -------------------------------------
-    // Warpgroup wg owns columns [wg * dv/2, (wg+1) * dv/2) of each row; the RMSNorm sum of
-    // squares is combined across the two warpgroups (scratch = D buffer, idle after o_full).
-    constexpr int HC = DV / 2;
+    // Warpgroup wg owns columns [wg * dv/4, (wg+1) * dv/4) of each row; the RMSNorm sum of
+    // squares is combined across the warpgroups (scratch = D buffer, idle after o_full).
+    constexpr int HC = DV / kNumWG;
+    constexpr int CW = HC >= 32 ? 32 : 16;
     const int c0 = wg * HC;
+    auto ld_o = [&](int c, uint32_t (&o)[CW]) {
+      if constexpr (CW == 32)
+        tmem_ld32(tmem + tl + C::kOCol + c0 + CW * c, o);
+      else
+        tmem_ld16(tmem + tl + C::kOCol + c0 + CW * c, o);
+      tmem_wait_ld();
+    };
     float ss = 0.f;
     if (ok && (P.flags & 2)) {
 #pragma unroll 1
-      for (int c = 0; c < HC / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tmem + tl + C::kOCol + c0 + 32 * c, o);
-        tmem_wait_ld();
+      for (int c = 0; c < HC / CW; ++c) {
+        uint32_t o[CW];
+        ld_o(c, o);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ss = fmaf(__uint_as_float(o[i]), __uint_as_float(o[i]), ss);
+        for (int i = 0; i < CW; ++i) ss = fmaf(__uint_as_float(o[i]), __uint_as_float(o[i]), ss);
       }
     }
     float scale = 1.f;
     if (P.flags & 2) {
       scratch[wg * BM + r] = ss;
-      named_barrier_sync(1, 256);
-      scale = 1.f / sqrtf((ss + scratch[(wg ^ 1) * BM + r]) / static_cast<float>(DV) + P.eps);
+      named_barrier_sync(1, kSoftmaxThreads);
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kNumWG; ++w) tot += scratch[w * BM + r];
+      scale = 1.f / sqrtf(tot / static_cast<float>(DV) + P.eps);
     }
     if (P.flags & 4) scale *= (1.f - P.lambda_init);
     if (ok) {
@@ -455,24 +492,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                            ((static_cast<size_t>(b) * P.N + row) * P.units + u) * DV + c0;
       const float* w = (P.flags & 2) && P.norm_w ? P.norm_w + c0 : nullptr;
 #pragma unroll 1
-      for (int c = 0; c < HC / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tmem + tl + C::kOCol + c0 + 32 * c, o);
-        tmem_wait_ld();
+      for (int c = 0; c < HC / CW; ++c) {
+        uint32_t o[CW];
+        ld_o(c, o);
         if (row < P.N) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
+          for (int g = 0; g < CW / 8; ++g) {
             uint4 pkt;
             uint32_t* pw = reinterpret_cast<uint32_t*>(&pkt);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int e = 8 * g + 2 * i;
-              const float w0 = w ? w[32 * c + e] : 1.f;
-              const float w1 = w ? w[32 * c + e + 1] : 1.f;
+              const float w0 = w ? w[CW * c + e] : 1.f;
+              const float w1 = w ? w[CW * c + e + 1] : 1.f;
               pw[i] = pack_bf16x2(__uint_as_float(o[e]) * scale * w0,
                                   __uint_as_float(o[e + 1]) * scale * w1);
             }
-            *reinterpret_cast<uint4*>(out + 32 * c + 8 * g) = pkt;
+            *reinterpret_cast<uint4*>(out + CW * c + 8 * g) = pkt;
           }
         }
       }
