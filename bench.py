@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 PREFILL = dict(B=4, N=4096, H=12, d=128, dv=256, layer=12)
 DECODE = dict(B=64, L=32768, H=12, d=128, dv=256, layer=12)
 V2 = dict(B=2, N=8192, Hq=64, Hkv=8, d=128)
+LONG = dict(B=1, N=65536, H=12, d=128, dv=256, layer=24)
 FLOPS_PER_PAIR = 1536        # 4d + 4dv MMA flops per causal (query, key) pair, V1
 FLOPS_PER_PAIR_DEF = 1024    # 4d + 2dv: the definition (A1 - lambda A2) V
 V2_FLOPS_PER_PAIR = 8 * 128  # per (query, key) pair of one differential pair: 2 heads x (QK + PV)
@@ -380,6 +381,44 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del dinp, ws, dout
         torch.cuda.empty_cache()
 
+    # ======================= long-context prefill =======================
+    if args.only in ("all", "long"):
+        c = LONG
+        inp = make_prefill_inputs(c["B"], c["N"], c["H"], c["d"], c["dv"], seed=4000 + rank,
+                                  layer=c["layer"], device=dev, needle=True)
+        lv = make_lambda_vectors(c["d"], seed=4001 + rank)
+        lv_h = tuple(t.to(dev).expand(c["H"], -1).contiguous() for t in lv)
+        lam_h = torch.empty(c["H"], dtype=torch.float32, device=dev)
+        li = da.diffattn_lambda_init(c["layer"])
+        out = torch.empty((c["B"], c["N"], c["H"], c["dv"]), dtype=torch.bfloat16, device=dev)
+
+        def lstep():
+            da.diffattn_lambda(*lv_h, layer=c["layer"], out=lam_h)
+            da.diffattn_fwd(inp.q, inp.k, inp.v, lam_h, li, out=out)
+
+        for _ in range(args.warmup):
+            lstep()
+        barrier()
+        lsteps = max(3, min(10, args.steps))
+        l_ev = [(ev(), ev()) for _ in range(lsteps)]
+        for i in range(lsteps):
+            l_ev[i][0].record(stream)
+            lstep()
+            l_ev[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        lms = statistics.mean(a.elapsed_time(b) for a, b in l_ev)
+        lflops = prefill_flops(c)
+        ltf = lflops / (lms * 1e-3) / 1e12
+        line["prefill_64k"] = {
+            "metric": "DiffAttn fwd TFLOP/s", "value": world * ltf, "unit": "TFLOP/s",
+            "ms_per_call": lms,
+            "workload": "prefill_64k: B1 N65536 H12 d128 dv256 causal, layer 24, one needle key per head",
+            "roofline": {"bound": "tensor", "achieved": ltf, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": ltf / peak_tf, "flops_per_launch": lflops}}
+        del inp, out
+        torch.cuda.empty_cache()
+
     # ======================= V2 =======================
     if args.only in ("all", "v2"):
         vc = V2
@@ -431,7 +470,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2", "long"], default="all",
                     help="profiling aid: run one workload (the JSON line then lacks the others)")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="profiling aid: a smaller decode batch for captures that save device memory")
