@@ -83,6 +83,28 @@ def profiled_traffic(summary: str, sha: str):
     return float(m_b.group(1))
 
 
+def dist_barrier():
+    """Synchronise the device, then all ranks (no-op in a single process)."""
+    import torch
+    import torch.distributed as dist
+    if torch.cuda.is_available() and torch.cuda.is_initialized():
+        torch.cuda.synchronize()
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def dist_max(x: float, device=None) -> float:
+    """Maximum of `x` over all ranks (the timing rule: the slowest rank sets the job's time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -233,16 +255,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
 
     def barrier():
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
+        dist_barrier()
 
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return dist_max(x, dev)
 
     def ev():
         return torch.cuda.Event(enable_timing=True)

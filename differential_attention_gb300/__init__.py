@@ -46,6 +46,7 @@ _SIGNATURES = {
     "diffattn_last_error_string": (ctypes.c_char_p, []),
     "diffattn_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "diffattn_lambda_init": (ctypes.c_float, [ctypes.c_int]),
+    "diffattn_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p]),
     "diffattn_lambda": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 3
                         + [ctypes.c_void_p, ctypes.c_void_p]),
     "diffattn_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_float, ctypes.c_void_p,
@@ -126,6 +127,12 @@ def diffattn_version() -> int:
 def diffattn_device_status(stream=None) -> None:
     """Synchronise `stream` and raise DiffAttnError if a kernel's bounded wait ran out."""
     _check(lib().diffattn_device_status(_stream(stream)))
+
+
+def diffattn_selftest_wait_timeout(limit_ms: int = 50, stream=None) -> None:
+    """Launch the diagnostic kernel whose bounded wait runs out after `limit_ms`; the next
+    diffattn_device_status() then raises DiffAttnError with ERR_TIMEOUT (once)."""
+    _check(lib().diffattn_selftest_wait_timeout(int(limit_ms), _stream(stream)))
 
 
 def diffattn_lambda_init(layer: int) -> float:

@@ -64,12 +64,23 @@ DIFFATTN_API const char* diffattn_last_error_string(void) { return t_err.c_str()
 DIFFATTN_API int diffattn_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  int v = 0, w = 0;
+  int v = 0, w = 0, x = 0;
   e = da::status_prefill_tc(&v);
   if (e == cudaSuccess) e = da::status_prefill_exact(&w);
+  if (e == cudaSuccess) e = da::status_simt(&x);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
-  v |= w;
+  v |= w | x;
   if (v != 0) return fail(DIFFATTN_ERR_TIMEOUT, "a bounded wait inside a kernel ran out (status %d)", v);
+  return ok();
+}
+
+DIFFATTN_API int diffattn_selftest_wait_timeout(int limit_ms, void* stream) {
+  if (limit_ms < 1 || limit_ms > 2000)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_selftest_wait_timeout: limit_ms must be in [1, 2000]");
+  int rc = check_device();
+  if (rc) return rc;
+  cudaError_t e = da::launch_wait_timeout(limit_ms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_selftest_wait_timeout launch");
   return ok();
 }
 

@@ -85,5 +85,10 @@ cudaError_t launch_prefill_exact(const Problem& p, cudaStream_t s, char* err, si
 // Read and clear the device status word of a tensor-core prefill translation unit.
 cudaError_t status_prefill_tc(int* v);
 cudaError_t status_prefill_exact(int* v);
+cudaError_t status_simt(int* v);
+
+// Diagnostics: one kernel whose bounded wait (on a barrier nothing arrives on) runs out after
+// limit_ms and sets the device status word of the CUDA-core translation unit.
+cudaError_t launch_wait_timeout(int limit_ms, cudaStream_t s);
 
 }  // namespace da

@@ -84,8 +84,9 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // wall-clock limit ran out or when `abort_flag` (CTA shared memory) became non-zero; the caller
 // then records the error and unwinds. Never traps, never spins forever.
 template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
+                                                volatile int* abort_flag,
+                                                unsigned long long limit_ns) {
   auto probe = [&]() {
     return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
   };
@@ -95,13 +96,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     if (probe()) return true;
     if ((it & 63u) == 0) {
       if (abort_flag != nullptr && *abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         flag_device_error(DEV_TIMEOUT);
         if (abort_flag != nullptr) *abort_flag = 1;
         return false;
       }
     }
   }
+}
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int* abort_flag) {
+  return mbar_wait_limit<kCluster>(bar, parity, abort_flag, kWaitLimitNs);
 }
 
 // Named barrier over `count` threads (a multiple of 32) of the CTA.

@@ -51,6 +51,27 @@ __global__ void lambda_kernel(const float* __restrict__ lq1, const float* __rest
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// diagnostics: a bounded wait that is certain to run out
+// ------------------------------------------------------------------------------------------
+__global__ void wait_timeout_kernel(unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // Nothing ever arrives on `bar`: the wait runs for limit_ns, flags DEV_TIMEOUT and returns.
+  if (threadIdx.x == 0) mbar_wait_limit(smem_u32(&bar), 0, nullptr, limit_ns);
+}
+
+cudaError_t launch_wait_timeout(int limit_ms, cudaStream_t s) {
+  wait_timeout_kernel<<<1, 32, 0, s>>>(static_cast<unsigned long long>(limit_ms) * 1000000ull);
+  return cudaGetLastError();
+}
+
+cudaError_t status_simt(int* v) { return read_clear_status(v); }
+
 cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                           int dim, int n_sets, float lambda_init, float* out, cudaStream_t s) {
   lambda_kernel<<<n_sets, 128, 0, s>>>(lq1, lk1, lq2, lk2, dim, lambda_init, out);

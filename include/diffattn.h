@@ -75,6 +75,13 @@ DIFFATTN_API const char* diffattn_last_error_string(void);
  * DIFFATTN_ERR_CUDA. */
 DIFFATTN_API int diffattn_device_status(void* stream);
 
+/* Diagnostics (not part of the method): launch one kernel whose bounded wait is certain to run
+ * out -- it waits on a barrier that nothing arrives on -- after `limit_ms` (1..2000). The kernel
+ * then sets the device status word and returns; it neither faults nor traps, and the context
+ * stays usable. The next diffattn_device_status() reports DIFFATTN_ERR_TIMEOUT (once). Use it to
+ * check that failure detection reaches the host. Errors: ERR_ARG, ERR_UNSUPPORTED, ERR_CUDA. */
+DIFFATTN_API int diffattn_selftest_wait_timeout(int limit_ms, void* stream);
+
 /* ------------------------------------------------------------------------------------------
  * lambda
  * Page "Differential Transformer: softmax can't say zero, so it subtracts", section "lambda,
