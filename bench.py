@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 PREFILL = dict(B=4, N=4096, H=12, d=128, dv=256, layer=12)
 DECODE = dict(B=64, L=32768, H=12, d=128, dv=256, layer=12)
 V2 = dict(B=2, N=8192, Hq=64, Hkv=8, d=128)
+V2_DECODE = dict(B=64, L=32768, Hq=64, Hkv=8, d=128)
 LONG = dict(B=1, N=65536, H=12, d=128, dv=256, layer=24)
 FLOPS_PER_PAIR = 1536        # 4d + 4dv MMA flops per causal (query, key) pair, V1
 FLOPS_PER_PAIR_DEF = 1024    # 4d + 2dv: the definition (A1 - lambda A2) V
@@ -51,6 +52,10 @@ def prefill_flops(cfg=PREFILL, per_pair=FLOPS_PER_PAIR) -> float:
 
 def decode_bytes(cfg=DECODE) -> float:
     return float(cfg["B"] * cfg["L"] * cfg["H"] * (2 * cfg["d"] + cfg["dv"]) * 2)
+
+
+def v2_decode_bytes(cfg=V2_DECODE) -> float:
+    return float(cfg["B"] * cfg["L"] * cfg["Hkv"] * 2 * cfg["d"] * 2)
 
 
 def load_peaks():
@@ -244,7 +249,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     import torch
     import torch.distributed as dist
     import differential_attention_gb300 as da
-    from synth import make_decode_inputs, make_lambda_vectors, make_prefill_inputs, make_v2_inputs
+    from synth import (make_decode_inputs, make_lambda_vectors, make_prefill_inputs,
+                       make_v2_decode_inputs, make_v2_inputs)
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -467,6 +473,49 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                    "unit": "TFLOP/s", "frac": vtf / peak_tf,
                                    "flops_per_launch": vflops}}
         del vinp, vout
+        torch.cuda.empty_cache()
+
+    # ======================= V2 decode =======================
+    if args.only in ("all", "v2_decode"):
+        c = dict(V2_DECODE, B=args.decode_batch)
+        vd = make_v2_decode_inputs(c["B"], c["L"], c["Hq"], c["Hkv"], c["d"], seed=5000 + rank,
+                                   device=dev)
+        ws = torch.empty(da.diffattn_v2_decode_workspace_size(c["B"], c["L"], c["Hq"], c["Hkv"],
+                                                              c["d"]), dtype=torch.uint8, device=dev)
+        vdout = torch.empty((c["B"], c["Hq"] // 2, c["d"]), dtype=torch.bfloat16, device=dev)
+
+        def v2dec():
+            da.diffattn_v2_decode(vd.q, vd.k_cache, vd.v_cache, vd.lam_logit, workspace=ws,
+                                  out=vdout)
+
+        for _ in range(args.warmup):
+            v2dec()
+        barrier()
+        n_steps = max(5, min(50, args.steps))
+        evs = [(ev(), ev()) for _ in range(n_steps)]
+        for i in range(n_steps):
+            evs[i][0].record(stream)
+            v2dec()
+            evs[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        nbytes = v2_decode_bytes(c)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        line["v2_decode"] = {
+            "metric": "V2 decode HBM GB/s", "value": world * gbs, "unit": "GB/s", "ms_per_call": ms,
+            "workload": f"v2_decode_32k: B{c['B']}, one query per sequence, cache 32768, Hq64 "
+                        "(32 pairs) over Hkv8, d128, bf16 (cache 8.6 GB at B64, larger than L2)",
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm,
+                         "traffic": profiled_traffic("v2_decode_32k.md",
+                                                     source_sha(["decode.cu", "ptx.cuh"])),
+                         "bytes_per_launch": nbytes,
+                         "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
+                         "timed": "diffattn_v2_decode call (split kernel + combine kernel)"},
+            "gpu_launches": 2 * n_steps}
+        del vd, ws, vdout
+        torch.cuda.empty_cache()
 
     # ======================= CPU baseline (rank 0, N = 1 only) =======================
     line["cpu_baseline"] = None
@@ -486,7 +535,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2", "long"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2", "v2_decode", "long"], default="all",
                     help="profiling aid: run one workload (the JSON line then lacks the others)")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="profiling aid: a smaller decode batch for captures that save device memory")

@@ -62,6 +62,10 @@ _SIGNATURES = {
                                 + [ctypes.c_int] * 7 + [ctypes.c_void_p]),
     "diffattn_v2_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 7
                         + [ctypes.c_void_p]),
+    "diffattn_v2_decode_workspace_size": (ctypes.c_int, [ctypes.c_int] * 5
+                                          + [ctypes.POINTER(ctypes.c_size_t)]),
+    "diffattn_v2_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int] * 7
+                           + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
 }
 
 
@@ -270,4 +274,40 @@ def diffattn_v2_fwd(q, k, v, lam_logit, causal: bool = True, cuda_cores: bool = 
              | (DIFFATTN_SINGLE_PASS if single_pass else 0))
     _check(lib().diffattn_v2_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_logit), _ptr(out), B, N, Hq,
                                  Hkv, d, flags, _code(q.dtype), _stream(stream)))
+    return out
+
+
+def diffattn_v2_decode_workspace_size(B: int, Lmax: int, Hq: int, Hkv: int, d: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().diffattn_v2_decode_workspace_size(B, Lmax, Hq, Hkv, d, ctypes.byref(n)))
+    return n.value
+
+
+def diffattn_v2_decode(q, k_cache, v_cache, lam_logit, seqlens=None, workspace=None, out=None,
+                       stream=None):
+    """DIFF V2 decode: one query token per sequence, attn[2p] - sigmoid(lam_logit) * attn[2p+1]
+    over the shared GQA cache; q [B, Hq, d], caches [B, Lmax, Hkv, d], lam_logit [B, Hq/2]."""
+    _dev("q", q, torch.bfloat16)
+    B, Hq, d = q.shape
+    _dev("k_cache", k_cache, torch.bfloat16)
+    _dev("v_cache", v_cache, torch.bfloat16)
+    Lmax, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if k_cache.shape != (B, Lmax, Hkv, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must both be [B, Lmax, Hkv, d]")
+    _dev("lam_logit", lam_logit, torch.float32)
+    if lam_logit.shape != (B, Hq // 2):
+        raise ValueError("lam_logit must be [B, Hq/2]")
+    if seqlens is not None:
+        _dev("seqlens", seqlens, torch.int32)
+    need = diffattn_v2_decode_workspace_size(B, Lmax, Hq, Hkv, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _dev("workspace", workspace)
+    if out is None:
+        out = torch.empty((B, Hq // 2, d), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    _check(lib().diffattn_v2_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
+                                    _ptr(lam_logit), _ptr(out), B, Lmax, Hq, Hkv, d, 0,
+                                    DIFFATTN_BF16, _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)))
     return out

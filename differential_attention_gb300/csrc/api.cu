@@ -330,3 +330,61 @@ DIFFATTN_API int diffattn_v2_fwd(const void* q, const void* k, const void* v,
 }
 
 }  // extern "C"
+
+namespace {
+int check_v2_decode_shape(const char* fn, int B, int Lmax, int Hq, int Hkv, int d) {
+  if (B < 1 || Lmax < 1 || Hq < 2 || Hkv < 1 || B > 65535 || Hkv > 65535)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need 1 <= B, Hkv <= 65535, Lmax >= 1 and Hq >= 2", fn);
+  if (Hq % Hkv != 0 || !(Hq / Hkv == 2 || Hq / Hkv == 4 || Hq / Hkv == 8))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need Hq / Hkv in {2, 4, 8} (got Hq=%d Hkv=%d)", fn, Hq, Hkv);
+  if (d != 128) return fail(DIFFATTN_ERR_SHAPE, "%s: need d = 128 (got %d)", fn, d);
+  if (static_cast<long long>(Hq / 2) > 65535)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: Hq / 2 must be <= 65535", fn);
+  return DIFFATTN_OK;
+}
+}  // namespace
+
+DIFFATTN_API int diffattn_v2_decode_workspace_size(int B, int Lmax, int Hq, int Hkv, int d,
+                                                   size_t* bytes) {
+  if (!bytes) return fail(DIFFATTN_ERR_ARG, "diffattn_v2_decode_workspace_size: null pointer");
+  int rc = check_v2_decode_shape("diffattn_v2_decode_workspace_size", B, Lmax, Hq, Hkv, d);
+  if (rc) return rc;
+  *bytes = da::v2_decode_workspace_bytes(B, Lmax, Hq, Hkv);
+  return ok();
+}
+
+DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const void* v_cache,
+                                    const int* seqlens, const float* lam_logit, void* out, int B,
+                                    int Lmax, int Hq, int Hkv, int d, int flags, int dtype,
+                                    void* workspace, size_t ws_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !lam_logit || !out)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_v2_decode: null pointer");
+  if (flags & ~DIFFATTN_CAUSAL) return fail(DIFFATTN_ERR_ARG, "diffattn_v2_decode: unknown flag bits 0x%x", flags);
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "diffattn_v2_decode: dtype must be DIFFATTN_BF16");
+  int rc = check_v2_decode_shape("diffattn_v2_decode", B, Lmax, Hq, Hkv, d);
+  if (rc) return rc;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(lam_logit, 4) || (seqlens && !aligned(seqlens, 4)))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_v2_decode: tensors must be 16-byte aligned");
+  const size_t need = da::v2_decode_workspace_bytes(B, Lmax, Hq, Hkv);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(DIFFATTN_ERR_WORKSPACE, "diffattn_v2_decode: need a 256-byte aligned workspace of %zu bytes", need);
+  rc = check_device();
+  if (rc) return rc;
+  da::V2DecodeArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.seqlens = seqlens;
+  a.lam_logit = lam_logit;
+  a.out = out;
+  a.B = B;
+  a.Lmax = Lmax;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.ws = static_cast<float*>(workspace);
+  cudaError_t e = da::launch_v2_decode(a, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_decode: unsupported group size");
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_decode launch");
+  return ok();
+}

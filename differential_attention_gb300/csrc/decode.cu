@@ -387,4 +387,313 @@ cudaError_t launch_decode_noalloc(const DecodeArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// =============================================================================================
+// DIFF V2 decode (page "Differential Transformer: softmax can't say zero, so it subtracts",
+// section "DIFF V2: what the authors changed"; page "Differential Transformer V2": the KV
+// cache is that of a baseline Transformer, so decoding reads it as a baseline would).
+//
+// One query token per sequence; the G = Hq / Hkv query heads of a GQA group share one KV head,
+// and query heads (2p, 2p+1) form differential pair p. Stage 1 (v2dec_split_kernel, grid
+// splits x Hkv x B): a CTA streams one slice of one KV head's cache once for all G query heads.
+// Each half-warp walks its own keys, kV2Keys at a time: lane t' (0..15) loads 16 bytes (8 dims)
+// of each K and V row, forms the G partial dot products, and a butterfly reduce-scatter over the
+// 16 lanes leaves head h's score in lanes 2h, 2h+1 (for G = 8), which keep that head's running
+// max and sum; the rescale factors and probabilities are broadcast back for the 8 x G fp32
+// output accumulators. Half-warps and warps are merged in shared memory; one record per
+// (b, kv head, split) holds, per query head, (m, l, o[d]). Stage 2 (v2dec_combine_kernel, grid
+// pairs x B): thread c merges the splits for channel c of both heads of its pair and writes
+// o_a / l_a - sigmoid(lam) * o_b / l_b.
+// =============================================================================================
+namespace {
+constexpr int kV2D = 128;          // head dim
+constexpr int kV2Keys = 4;         // keys per half-warp per step
+constexpr int kV2Warps = 8;
+
+// Sum each of the G values of v over the 16 lanes of the half-warp; afterwards lane t' holds the
+// total of value (t' >> sh) & (G - 1) for the shift sh = log2(16 / G) (lanes 2h, 2h+1 for G = 8).
+template <int G>
+__device__ __forceinline__ float reduce_scatter16(float (&v)[G], int lane) {
+  // rounds over lane bits 3, 2, ... while more than one value is left
+  int cnt = G;
+#pragma unroll
+  for (int bit = 8; bit >= 1; bit >>= 1) {
+    if (cnt > 1) {
+      const bool up = (lane & bit) != 0;
+      const int half = cnt >> 1;
+#pragma unroll
+      for (int i = 0; i < G / 2; ++i) {
+        if (i < half) {
+          const float send = up ? v[i] : v[i + half];
+          const float keep = up ? v[i + half] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+        }
+      }
+      cnt = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], bit);
+    }
+  }
+  return v[0];
+}
+
+template <int G>
+struct V2DecParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* kc;
+  const __nv_bfloat16* vc;
+  const int* seqlens;
+  float* ws;
+  int Lmax, Hq, Hkv, splits, chunk;
+  float scale_log2;
+};
+
+template <int G>
+__global__ void __launch_bounds__(kV2Warps * 32) v2dec_split_kernel(const V2DecParams<G> p) {
+  constexpr int kRec = G * (2 + kV2D);  // floats per record: per head m, l, o[128]
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hl = lane & 15, half = lane >> 4;
+  constexpr int kSh = (G == 8) ? 1 : (G == 4) ? 2 : 3;  // head of lane: (hl >> kSh) & (G-1)
+  const int my_head = (hl >> kSh) & (G - 1);
+  int L = p.seqlens ? p.seqlens[b] : p.Lmax;
+  L = L < 1 ? 1 : (L > p.Lmax ? p.Lmax : L);
+  const int k0 = s * p.chunk, k1 = min(k0 + p.chunk, L);
+
+  float qf[G][8];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const uint4 qu = *reinterpret_cast<const uint4*>(
+        p.q + (static_cast<size_t>(b) * p.Hq + g * G + h) * kV2D + 8 * hl);
+    bf16x8_to_f32(qu, qf[h]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qf[h][i] *= p.scale_log2;
+  }
+  float m = -INFINITY, l = 0.f;  // running stats of head my_head (this lane pair)
+  float o[G][8];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[h][i] = 0.f;
+
+  const size_t row = static_cast<size_t>(p.Hkv) * kV2D;  // elements between keys
+  const __nv_bfloat16* kb = p.kc + (static_cast<size_t>(b) * p.Lmax * p.Hkv + g) * kV2D + 8 * hl;
+  const __nv_bfloat16* vb = p.vc + (static_cast<size_t>(b) * p.Lmax * p.Hkv + g) * kV2D + 8 * hl;
+  constexpr int kStride = kV2Warps * 2 * kV2Keys;  // keys per CTA step
+  // The loop bound is warp-uniform so that every shuffle below has all 32 lanes; a half-warp
+  // whose keys all lie past k1 takes part with masked scores and leaves its state unchanged.
+  for (int jw = k0 + warp * 2 * kV2Keys; jw < k1; jw += kStride) {
+    const int j0 = jw + half * kV2Keys;
+    uint4 ku[kV2Keys], vu[kV2Keys];
+#pragma unroll
+    for (int e = 0; e < kV2Keys; ++e) {
+      const int j = min(j0 + e, k1 - 1);  // clamped in bounds; masked below
+      ku[e] = ldg_stream(kb + static_cast<size_t>(j) * row);
+      vu[e] = ldg_stream(vb + static_cast<size_t>(j) * row);
+    }
+    float sc[kV2Keys];
+#pragma unroll
+    for (int e = 0; e < kV2Keys; ++e) {
+      float kf[8];
+      bf16x8_to_f32(ku[e], kf);
+      float part[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float a = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a = fmaf(qf[h][i], kf[i], a);
+        part[h] = a;
+      }
+      const float r = reduce_scatter16<G>(part, hl);
+      sc[e] = (j0 + e < k1) ? r : -INFINITY;
+    }
+    float mx = sc[0];
+#pragma unroll
+    for (int e = 1; e < kV2Keys; ++e) mx = fmaxf(mx, sc[e]);
+    const float mn = fmaxf(m, mx);
+    const float ms = (mn == -INFINITY) ? 0.f : mn;  // no key seen yet: keep the state at zero
+    const float corr = ex2_approx(m - ms);
+    float pe[kV2Keys];
+    float ps = 0.f;
+#pragma unroll
+    for (int e = 0; e < kV2Keys; ++e) {
+      pe[e] = ex2_approx(sc[e] - ms);
+      ps += pe[e];
+    }
+    l = l * corr + ps;
+    m = mn;
+    // every head's correction and probabilities, broadcast to the whole half-warp
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float ch = __shfl_sync(0xffffffffu, corr, (lane & 16) | (h << kSh));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[h][i] *= ch;
+    }
+#pragma unroll
+    for (int e = 0; e < kV2Keys; ++e) {
+      float vf[8];
+      bf16x8_to_f32(vu[e], vf);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float ph = __shfl_sync(0xffffffffu, pe[e], (lane & 16) | (h << kSh));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[h][i] = fmaf(ph, vf[i], o[h][i]);
+      }
+    }
+  }
+
+  // merge the two half-warps of this warp in registers (lane t and t ^ 16 hold the same dims)
+  {
+    const float m_o = __shfl_xor_sync(0xffffffffu, m, 16);
+    const float l_o = __shfl_xor_sync(0xffffffffu, l, 16);
+    const float M = fmaxf(m, m_o);
+    const float Ms = (M == -INFINITY) ? 0.f : M;
+    const float f_me = ex2_approx(m - Ms), f_ot = ex2_approx(m_o - Ms);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const int src = h << kSh;
+      const float a = __shfl_sync(0xffffffffu, f_me, (lane & 16) | src);
+      const float c = __shfl_sync(0xffffffffu, f_ot, (lane & 16) | src);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[h][i] = o[h][i] * a + __shfl_xor_sync(0xffffffffu, o[h][i], 16) * c;
+    }
+    l = l * f_me + l_o * f_ot;
+    m = M;
+  }
+  // then the warps, in shared memory
+  __shared__ float s_o[kV2Warps][G][kV2D];
+  __shared__ float s_ml[kV2Warps][G][2];
+  if (half == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s_o[warp][h][8 * hl + i] = o[h][i];
+    if ((hl & ((1 << kSh) - 1)) == 0) {
+      s_ml[warp][my_head][0] = m;
+      s_ml[warp][my_head][1] = l;
+    }
+  }
+  __syncthreads();
+  float* rec = p.ws + ((static_cast<size_t>(b) * p.Hkv + g) * p.splits + s) * kRec;
+  for (int idx = threadIdx.x; idx < G * kV2D; idx += kV2Warps * 32) {
+    const int h = idx / kV2D, c = idx % kV2D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kV2Warps; ++w) M = fmaxf(M, s_ml[w][h][0]);
+    float oa = 0.f, la = 0.f;
+#pragma unroll
+    for (int w = 0; w < kV2Warps; ++w) {
+      const float mw = s_ml[w][h][0];
+      if (mw != -INFINITY) {
+        const float f = ex2_approx(mw - M);
+        la = fmaf(s_ml[w][h][1], f, la);
+        oa = fmaf(s_o[w][h][c], f, oa);
+      }
+    }
+    rec[h * (2 + kV2D) + 2 + c] = oa;
+    if (c == 0) {
+      rec[h * (2 + kV2D) + 0] = M;
+      rec[h * (2 + kV2D) + 1] = la;
+    }
+  }
+}
+
+struct V2CombineParams {
+  const float* ws;
+  const float* lam_logit;
+  __nv_bfloat16* out;
+  int Hq, Hkv, G, splits;
+};
+
+__global__ void __launch_bounds__(kV2D) v2dec_combine_kernel(const V2CombineParams p) {
+  const int pair = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
+  const int P = p.Hq / 2;
+  const int ha = 2 * pair, g = ha / p.G;
+  const int rec_len = p.G * (2 + kV2D);
+  const float* recs = p.ws + (static_cast<size_t>(b) * p.Hkv + g) * p.splits * rec_len;
+  float res[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int h = (ha + k) - g * p.G;
+    float M = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, recs[s * rec_len + h * (2 + kV2D)]);
+    float o = 0.f, l = 0.f;
+    for (int s = 0; s < p.splits; ++s) {
+      const float* r = recs + s * rec_len + h * (2 + kV2D);
+      if (r[0] != -INFINITY) {
+        const float f = ex2_approx(r[0] - M);
+        l = fmaf(r[1], f, l);
+        o = fmaf(r[2 + c], f, o);
+      }
+    }
+    res[k] = o / l;
+  }
+  const float z = p.lam_logit[static_cast<size_t>(b) * P + pair];
+  const float lam = 1.f / (1.f + expf(-z));
+  p.out[(static_cast<size_t>(b) * P + pair) * kV2D + c] = __float2bfloat16_rn(res[0] - lam * res[1]);
+}
+
+template <int G>
+cudaError_t launch_v2dec(const V2DecodeArgs& a, cudaStream_t st, int S, int chunk) {
+  V2DecParams<G> sp;
+  sp.q = static_cast<const __nv_bfloat16*>(a.q);
+  sp.kc = static_cast<const __nv_bfloat16*>(a.k_cache);
+  sp.vc = static_cast<const __nv_bfloat16*>(a.v_cache);
+  sp.seqlens = a.seqlens;
+  sp.ws = a.ws;
+  sp.Lmax = a.Lmax;
+  sp.Hq = a.Hq;
+  sp.Hkv = a.Hkv;
+  sp.splits = S;
+  sp.chunk = chunk;
+  sp.scale_log2 = kLog2e / sqrtf(static_cast<float>(kV2D));
+  v2dec_split_kernel<G><<<dim3(S, a.Hkv, a.B), kV2Warps * 32, 0, st>>>(sp);
+  return cudaGetLastError();
+}
+}  // namespace
+
+int v2_decode_splits(int B, int Lmax, int Hkv, int* chunk_out) {
+  const long long units = static_cast<long long>(B) * Hkv;
+  long long target = (16LL * 152 + units - 1) / units;
+  if (target < 1) target = 1;
+  const int step = kV2Warps * 2 * kV2Keys;
+  long long chunk = (Lmax + target - 1) / target;
+  if (chunk < 512) chunk = 512;
+  chunk = (chunk + step - 1) / step * step;
+  const int splits = static_cast<int>((Lmax + chunk - 1) / chunk);
+  if (chunk_out) *chunk_out = static_cast<int>(chunk);
+  return splits;
+}
+
+size_t v2_decode_workspace_bytes(int B, int Lmax, int Hq, int Hkv) {
+  const int S = v2_decode_splits(B, Lmax, Hkv, nullptr);
+  const int G = Hq / Hkv;
+  return static_cast<size_t>(B) * Hkv * S * G * (2 + kV2D) * sizeof(float);
+}
+
+cudaError_t launch_v2_decode(const V2DecodeArgs& a, cudaStream_t st) {
+  int chunk = 0;
+  const int S = v2_decode_splits(a.B, a.Lmax, a.Hkv, &chunk);
+  const int G = a.Hq / a.Hkv;
+  cudaError_t e;
+  if (G == 2)
+    e = launch_v2dec<2>(a, st, S, chunk);
+  else if (G == 4)
+    e = launch_v2dec<4>(a, st, S, chunk);
+  else if (G == 8)
+    e = launch_v2dec<8>(a, st, S, chunk);
+  else
+    return cudaErrorNotSupported;
+  if (e != cudaSuccess) return e;
+  V2CombineParams cp;
+  cp.ws = a.ws;
+  cp.lam_logit = a.lam_logit;
+  cp.out = static_cast<__nv_bfloat16*>(a.out);
+  cp.Hq = a.Hq;
+  cp.Hkv = a.Hkv;
+  cp.G = G;
+  cp.splits = S;
+  v2dec_combine_kernel<<<dim3(a.Hq / 2, a.B), kV2D, 0, st>>>(cp);
+  return cudaGetLastError();
+}
+
 }  // namespace da

@@ -74,6 +74,21 @@ int decode_splits(int B, int Lmax, int H, int* chunk_out);
 size_t decode_workspace_bytes(int B, int Lmax, int H, int dv);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
+// DIFF V2 decode: Hq query heads (pairs 2p, 2p+1) over an [B, Lmax, Hkv, 128] cache.
+struct V2DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int* seqlens;
+  const float* lam_logit;
+  void* out;
+  int B, Lmax, Hq, Hkv;
+  float* ws;
+};
+int v2_decode_splits(int B, int Lmax, int Hkv, int* chunk_out);
+size_t v2_decode_workspace_bytes(int B, int Lmax, int Hq, int Hkv);
+cudaError_t launch_v2_decode(const V2DecodeArgs& a, cudaStream_t s);
+
 // Decode whose split partials live in a fixed device array of this size (no workspace argument).
 constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(16) << 20;
 long long decode_noalloc_max_units();  // largest B * H whose partials fit (one split each)

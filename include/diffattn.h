@@ -197,6 +197,32 @@ DIFFATTN_API int diffattn_v2_fwd(const void* q, const void* k, const void* v,
                                  const float* lam_logit, void* out, int B, int N, int Hq, int Hkv,
                                  int d, int flags, int dtype, void* stream);
 
+/* ------------------------------------------------------------------------------------------
+ * DIFF V2 decode (page "Differential Transformer: softmax can't say zero, so it subtracts",
+ * section "DIFF V2: what the authors changed"; page "Differential Transformer V2": the KV cache
+ * is a baseline Transformer's, so decoding reads it as a baseline does). One query token per
+ * sequence: softmax attention of each of the Hq query heads over its GQA KV head's cached keys
+ * 0 .. seqlens[b]-1, then out_p = attn[2p] - sigmoid(lam_logit[b, p]) * attn[2p+1]. Every cached
+ * K and V element is read once for all Hq / Hkv query heads of its group.
+ *   q         : device [B, Hq, d]; pair p = query heads (2p, 2p+1)
+ *   k_cache, v_cache : device [B, Lmax, Hkv, d]; query head h reads KV head h / (Hq / Hkv)
+ *   seqlens   : device int32 [B] in [1, Lmax], or NULL for Lmax everywhere (clamped on the
+ *               device as for diffattn_decode)
+ *   lam_logit : device fp32 [B, Hq/2], the value before the sigmoid
+ *   out       : device [B, Hq/2, d]
+ *   flags     : 0 (DIFFATTN_CAUSAL is accepted and ignored)
+ *   workspace, ws_bytes : device scratch of at least diffattn_v2_decode_workspace_size() bytes,
+ *               256-byte aligned, not shared with a call that can run at the same time.
+ * Supported: dtype DIFFATTN_BF16, d = 128, Hq / Hkv in {2, 4, 8}. The scale is 1/sqrt(d).
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_v2_decode_workspace_size(int B, int Lmax, int Hq, int Hkv, int d,
+                                                   size_t* bytes);
+DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const void* v_cache,
+                                    const int* seqlens, const float* lam_logit, void* out, int B,
+                                    int Lmax, int Hq, int Hkv, int d, int flags, int dtype,
+                                    void* workspace, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -224,3 +224,30 @@ def diffattn_v2_fwd(q, k, v, lam_logit, causal: bool = True, rows=None):
             a2 = attention_head(q[b, :, 2 * p + 1], k[b, :, g], v[b, :, g], causal, rows)
             out[b, :, p, :] = a1 - sig[b, rows, p][:, None] * a2
     return out
+
+
+def diffattn_v2_decode(q, k_cache, v_cache, seqlens, lam_logit):
+    """DIFF V2 decode: one query token per sequence over its cached keys 0 .. seqlens[b]-1 (no
+    mask inside that range); out_p = attn[2p] - sigmoid(lam[b, p]) * attn[2p+1], the two query
+    heads of pair p sharing the GQA KV head floor(2p / (Hq / Hkv)) ([P3] "DIFF V2: what the
+    authors changed"; [P5] on V2 decoding over an unchanged KV cache).
+
+    q [B,Hq,d], k_cache, v_cache [B,L,Hkv,d], seqlens [B], lam_logit [B,Hq/2].
+    Returns float64 [B, Hq/2, d].
+    """
+    q = _f64(q)
+    B, Hq, d = q.shape
+    Hkv = k_cache.shape[2]
+    P = Hq // 2
+    seqlens = np.asarray(_f64(seqlens)).astype(np.int64)
+    sig = sigmoid(lam_logit)
+    out = np.empty((B, P, v_cache.shape[-1]), dtype=np.float64)
+    for b in range(B):
+        L = int(seqlens[b])
+        kb, vb = _f64(k_cache[b, :L]), _f64(v_cache[b, :L])
+        for p in range(P):
+            g = v2_kv_head(p, Hq, Hkv)
+            a1 = attention_head(q[b, 2 * p:2 * p + 1], kb[:, g], vb[:, g], causal=False)
+            a2 = attention_head(q[b, 2 * p + 1:2 * p + 2], kb[:, g], vb[:, g], causal=False)
+            out[b, p, :] = (a1 - sig[b, p] * a2)[0]
+    return out

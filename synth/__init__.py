@@ -11,5 +11,6 @@ from .workloads import (  # noqa: F401
     make_lambda_vectors,
     make_prefill_inputs,
     make_tiny_inputs,
+    make_v2_decode_inputs,
     make_v2_inputs,
 )

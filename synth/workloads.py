@@ -27,6 +27,7 @@ WORKLOADS = {
                         needle=True),
     "decode_32k": dict(B=64, L=32768, H=12, d=128, dv=256, dtype="bf16", layer=12, norm=True),
     "v2_gqa": dict(B=2, N=8192, Hq=64, Hkv=8, d=128, causal=True, dtype="bf16"),
+    "v2_decode_32k": dict(B=64, L=32768, Hq=64, Hkv=8, d=128, dtype="bf16"),
 }
 
 NORM_EPS = 1e-5
@@ -178,3 +179,33 @@ def make_v2_inputs(B: int, N: int, Hq: int, Hkv: int, d: int, seed: int, causal:
     v = _randn((B, N, Hkv, d), g, device, std).to(dtype)
     lam_logit = _randn((B, N, Hq // 2), g, device)
     return V2Inputs(q=q, k=k, v=v, lam_logit=lam_logit, causal=causal)
+
+
+@dataclass
+class V2DecodeInputs:
+    q: torch.Tensor          # [B, Hq, d]
+    k_cache: torch.Tensor    # [B, L, Hkv, d]
+    v_cache: torch.Tensor    # [B, L, Hkv, d]
+    seqlens: torch.Tensor    # [B] int32
+    lam_logit: torch.Tensor  # [B, Hq/2] fp32, sigmoid is applied by the operator
+
+
+def make_v2_decode_inputs(B: int, L: int, Hq: int, Hkv: int, d: int, seed: int, device="cpu",
+                          ragged: bool = False, dtype=torch.bfloat16) -> V2DecodeInputs:
+    """V2 decode inputs: cache ~ N(0, 1), q ~ N(0, 1)/sqrt(d), lambda logits ~ N(0, 1); the cache
+    is drawn one batch row at a time. With `ragged`, seqlens[b] ~ U{1..L}, else L everywhere."""
+    g = _gen(seed, device)
+    q = _randn((B, Hq, d), g, device, 1.0 / math.sqrt(d)).to(dtype)
+    k_cache = torch.empty((B, L, Hkv, d), dtype=dtype, device=device)
+    v_cache = torch.empty((B, L, Hkv, d), dtype=dtype, device=device)
+    for b in range(B):
+        k_cache[b].copy_(_randn((L, Hkv, d), g, device))
+        v_cache[b].copy_(_randn((L, Hkv, d), g, device))
+    gh = _gen(seed + 1, "cpu")
+    lam_logit = torch.randn((B, Hq // 2), generator=gh, dtype=torch.float32)
+    if ragged:
+        seqlens = torch.randint(1, L + 1, (B,), generator=gh, dtype=torch.int32)
+    else:
+        seqlens = torch.full((B,), L, dtype=torch.int32)
+    return V2DecodeInputs(q=q, k_cache=k_cache, v_cache=v_cache, seqlens=seqlens.to(device),
+                          lam_logit=lam_logit.to(device))

@@ -11,7 +11,8 @@ import torch
 
 import differential_attention_gb300 as da
 from oracle import diffattn_ref as ref
-from synth import make_decode_inputs, make_lambda_vectors, make_prefill_inputs, make_v2_inputs
+from synth import (make_decode_inputs, make_lambda_vectors, make_prefill_inputs, make_v2_decode_inputs,
+                   make_v2_inputs)
 from tests.gpu_util import assert_bf16
 
 pytestmark = pytest.mark.gpu
@@ -100,3 +101,17 @@ def test_v2_gqa_full():
             want.append(ref.diffattn_v2_fwd(q, k, v, lam, rows=rows)[0, :, 0])
             got.append(out[b, torch.as_tensor(rows, device=DEV), p].float().cpu().numpy())
     assert_bf16(np.stack(got), np.stack(want))
+
+
+def test_v2_decode_32k_full():
+    """B64, cache 32768, 64 query heads over 8 KV heads: all pairs of 3 sampled sequences."""
+    inp = make_v2_decode_inputs(64, 32768, 64, 8, 128, seed=4000, device=DEV)
+    out = da.diffattn_v2_decode(inp.q, inp.k_cache, inp.v_cache, inp.lam_logit)
+    da.diffattn_device_status()
+    sample = [0, 29, 63]
+    want = ref.diffattn_v2_decode(inp.q[sample].cpu(), inp.k_cache[sample].cpu(),
+                                  inp.v_cache[sample].cpu(), inp.seqlens[sample].cpu(),
+                                  inp.lam_logit[sample].cpu())
+    assert_bf16(out[sample], want)
+    del inp
+    torch.cuda.empty_cache()

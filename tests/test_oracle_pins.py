@@ -267,10 +267,27 @@ def pin_v2():
         assert np.allclose(out2[0, :, p], (1 - sig[0, :, p])[:, None] * a, atol=1e-12)
 
 
+def pin_v2_decode_is_last_prefill_row():
+    rng = np.random.default_rng(11)
+    B, L, Hq, Hkv, d = 3, 19, 8, 2, 8
+    kc = rng.standard_normal((B, L, Hkv, d)); vc = rng.standard_normal((B, L, Hkv, d))
+    q = rng.standard_normal((B, Hq, d)); logit = rng.standard_normal((B, Hq // 2))
+    seqlens = np.array([19, 1, 7])
+    out = ref.diffattn_v2_decode(q, kc, vc, seqlens, logit)
+    for b in range(B):
+        Lb = seqlens[b]
+        qp = rng.standard_normal((1, Lb, Hq, d)); qp[0, Lb - 1] = q[b]
+        lp = rng.standard_normal((1, Lb, Hq // 2)); lp[0, Lb - 1] = logit[b]
+        full = ref.diffattn_v2_fwd(qp, kc[b:b + 1, :Lb], vc[b:b + 1, :Lb], lp, causal=True,
+                                   rows=np.array([Lb - 1]))
+        assert np.allclose(out[b], full[0, 0], atol=1e-12, rtol=1e-12), b
+
+
 PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, pin_lambda_spread,
         pin_softmax_floor, pin_toy_needle_table, pin_worked_example, pin_row_sums,
         pin_lambda_zero_is_softmax_attention, pin_equal_maps_scale_attention, pin_brute_force_tiny,
-        pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2]
+        pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
+        pin_v2_decode_is_last_prefill_row]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])

@@ -10,7 +10,7 @@ import torch
 import differential_attention_gb300 as da
 from oracle import diffattn_ref as ref
 from synth import (make_decode_inputs, make_lambda_vectors, make_prefill_inputs, make_tiny_inputs,
-                   make_v2_inputs)
+                   make_v2_decode_inputs, make_v2_inputs)
 from tests.gpu_util import assert_bf16, assert_fp32, errors
 
 pytestmark = pytest.mark.gpu
@@ -212,6 +212,50 @@ def test_v2_cuda_core_path():
                              cuda_cores=True)
     want = ref.diffattn_v2_fwd(inp.q, inp.k, inp.v, inp.lam_logit)
     assert_bf16(got, want)
+
+
+# ------------------------------------------------------------------------------------------
+# V2 decode
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("B,L,Hq,Hkv,ragged", [(3, 700, 16, 2, False), (2, 1000, 16, 4, True),
+                                               (4, 513, 8, 4, True), (1, 1, 8, 1, False),
+                                               (5, 37, 4, 2, True)])
+def test_v2_decode_small(B, L, Hq, Hkv, ragged):
+    """Every group size (8, 4, 2 query heads per KV head), ragged lengths down to one key, and
+    lengths that leave the last split partly filled or some splits empty."""
+    inp = make_v2_decode_inputs(B, L, Hq, Hkv, 128, seed=101 + L, ragged=ragged)
+    got = da.diffattn_v2_decode(inp.q.to(DEV), inp.k_cache.to(DEV), inp.v_cache.to(DEV),
+                                inp.lam_logit.to(DEV), seqlens=inp.seqlens.to(DEV))
+    want = ref.diffattn_v2_decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, inp.lam_logit)
+    assert_bf16(got, want)
+
+
+def test_v2_decode_no_seqlens_means_full():
+    inp = make_v2_decode_inputs(2, 650, 16, 2, 128, seed=111)
+    got = da.diffattn_v2_decode(inp.q.to(DEV), inp.k_cache.to(DEV), inp.v_cache.to(DEV),
+                                inp.lam_logit.to(DEV))
+    want = ref.diffattn_v2_decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, inp.lam_logit)
+    assert_bf16(got, want)
+
+
+def test_v2_decode_matches_prefill_last_row():
+    """Decode of query row N-1 over N cached keys equals row N-1 of the causal V2 prefill."""
+    pin = make_v2_inputs(1, 384, 16, 2, 128, seed=113)
+    q, k, v = pin.q.to(DEV), pin.k.to(DEV), pin.v.to(DEV)
+    lam = pin.lam_logit.to(DEV)
+    pre = da.diffattn_v2_fwd(q, k, v, lam)
+    dec = da.diffattn_v2_decode(q[:, -1].contiguous(), k, v, lam[:, -1].contiguous())
+    max_abs, rel = errors(dec, pre[:, -1])
+    assert rel < 2e-2 and max_abs < 4e-2
+
+
+def test_v2_decode_rejects_bad_shapes():
+    q = torch.zeros((1, 6, 128), dtype=torch.bfloat16, device=DEV)
+    kc = torch.zeros((1, 8, 1, 128), dtype=torch.bfloat16, device=DEV)
+    lam = torch.zeros((1, 3), dtype=torch.float32, device=DEV)
+    with pytest.raises(da.DiffAttnError) as e:  # group of 6 query heads: not 2, 4 or 8
+        da.diffattn_v2_decode(q, kc, kc, lam)
+    assert e.value.status == -2  # DIFFATTN_ERR_SHAPE
 
 
 # ------------------------------------------------------------------------------------------
