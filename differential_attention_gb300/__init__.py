@@ -283,8 +283,8 @@ def diffattn_v2_decode_workspace_size(B: int, Lmax: int, Hq: int, Hkv: int, d: i
     return n.value
 
 
-def diffattn_v2_decode(q, k_cache, v_cache, lam_logit, seqlens=None, workspace=None, out=None,
-                       stream=None):
+def diffattn_v2_decode(q, k_cache, v_cache, lam_logit, seqlens=None, cuda_cores: bool = False,
+                       workspace=None, out=None, stream=None):
     """DIFF V2 decode: one query token per sequence, attn[2p] - sigmoid(lam_logit) * attn[2p+1]
     over the shared GQA cache; q [B, Hq, d], caches [B, Lmax, Hkv, d], lam_logit [B, Hq/2]."""
     _dev("q", q, torch.bfloat16)
@@ -307,7 +307,8 @@ def diffattn_v2_decode(q, k_cache, v_cache, lam_logit, seqlens=None, workspace=N
         out = torch.empty((B, Hq // 2, d), dtype=torch.bfloat16, device=q.device)
     _dev("out", out, torch.bfloat16)
     _check(lib().diffattn_v2_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
-                                    _ptr(lam_logit), _ptr(out), B, Lmax, Hq, Hkv, d, 0,
+                                    _ptr(lam_logit), _ptr(out), B, Lmax, Hq, Hkv, d,
+                                    DIFFATTN_CUDA_CORES if cuda_cores else 0,
                                     DIFFATTN_BF16, _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)))
     return out

@@ -64,12 +64,13 @@ DIFFATTN_API const char* diffattn_last_error_string(void) { return t_err.c_str()
 DIFFATTN_API int diffattn_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  int v = 0, w = 0, x = 0;
+  int v = 0, w = 0, x = 0, y = 0;
   e = da::status_prefill_tc(&v);
   if (e == cudaSuccess) e = da::status_prefill_exact(&w);
   if (e == cudaSuccess) e = da::status_simt(&x);
+  if (e == cudaSuccess) e = da::status_v2_decode_tc(&y);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
-  v |= w | x;
+  v |= w | x | y;
   if (v != 0) return fail(DIFFATTN_ERR_TIMEOUT, "a bounded wait inside a kernel ran out (status %d)", v);
   return ok();
 }
@@ -359,7 +360,8 @@ DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const vo
                                     void* workspace, size_t ws_bytes, void* stream) {
   if (!q || !k_cache || !v_cache || !lam_logit || !out)
     return fail(DIFFATTN_ERR_ARG, "diffattn_v2_decode: null pointer");
-  if (flags & ~DIFFATTN_CAUSAL) return fail(DIFFATTN_ERR_ARG, "diffattn_v2_decode: unknown flag bits 0x%x", flags);
+  if (flags & ~(DIFFATTN_CAUSAL | DIFFATTN_CUDA_CORES))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_v2_decode: unknown flag bits 0x%x", flags);
   if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "diffattn_v2_decode: dtype must be DIFFATTN_BF16");
   int rc = check_v2_decode_shape("diffattn_v2_decode", B, Lmax, Hq, Hkv, d);
   if (rc) return rc;
@@ -383,8 +385,12 @@ DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const vo
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.ws = static_cast<float*>(workspace);
-  cudaError_t e = da::launch_v2_decode(a, static_cast<cudaStream_t>(stream));
+  char err[256] = {0};
+  cudaError_t e = (flags & DIFFATTN_CUDA_CORES)
+                      ? da::launch_v2_decode(a, static_cast<cudaStream_t>(stream))
+                      : da::launch_v2_decode_tc(a, static_cast<cudaStream_t>(stream), err, sizeof(err));
   if (e == cudaErrorNotSupported) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_decode: unsupported group size");
+  if (e == cudaErrorInvalidValue && err[0]) return fail(DIFFATTN_ERR_CUDA, "diffattn_v2_decode: %s", err);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_decode launch");
   return ok();
 }

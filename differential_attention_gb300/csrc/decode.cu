@@ -665,9 +665,25 @@ int v2_decode_splits(int B, int Lmax, int Hkv, int* chunk_out) {
 }
 
 size_t v2_decode_workspace_bytes(int B, int Lmax, int Hq, int Hkv) {
-  const int S = v2_decode_splits(B, Lmax, Hkv, nullptr);
+  // room for the records of either split kernel (CUDA cores or tensor cores)
+  const int S1 = v2_decode_splits(B, Lmax, Hkv, nullptr);
+  const int S2 = v2_decode_tc_splits(B, Lmax, Hkv, nullptr);
+  const int S = S1 > S2 ? S1 : S2;
   const int G = Hq / Hkv;
   return static_cast<size_t>(B) * Hkv * S * G * (2 + kV2D) * sizeof(float);
+}
+
+cudaError_t launch_v2_combine(const V2DecodeArgs& a, int splits, cudaStream_t st) {
+  V2CombineParams cp;
+  cp.ws = a.ws;
+  cp.lam_logit = a.lam_logit;
+  cp.out = static_cast<__nv_bfloat16*>(a.out);
+  cp.Hq = a.Hq;
+  cp.Hkv = a.Hkv;
+  cp.G = a.Hq / a.Hkv;
+  cp.splits = splits;
+  v2dec_combine_kernel<<<dim3(a.Hq / 2, a.B), kV2D, 0, st>>>(cp);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_v2_decode(const V2DecodeArgs& a, cudaStream_t st) {
@@ -684,16 +700,7 @@ cudaError_t launch_v2_decode(const V2DecodeArgs& a, cudaStream_t st) {
   else
     return cudaErrorNotSupported;
   if (e != cudaSuccess) return e;
-  V2CombineParams cp;
-  cp.ws = a.ws;
-  cp.lam_logit = a.lam_logit;
-  cp.out = static_cast<__nv_bfloat16*>(a.out);
-  cp.Hq = a.Hq;
-  cp.Hkv = a.Hkv;
-  cp.G = G;
-  cp.splits = S;
-  v2dec_combine_kernel<<<dim3(a.Hq / 2, a.B), kV2D, 0, st>>>(cp);
-  return cudaGetLastError();
+  return launch_v2_combine(a, S, st);
 }
 
 }  // namespace da

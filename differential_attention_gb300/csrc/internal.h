@@ -85,9 +85,13 @@ struct V2DecodeArgs {
   int B, Lmax, Hq, Hkv;
   float* ws;
 };
-int v2_decode_splits(int B, int Lmax, int Hkv, int* chunk_out);
-size_t v2_decode_workspace_bytes(int B, int Lmax, int Hq, int Hkv);
-cudaError_t launch_v2_decode(const V2DecodeArgs& a, cudaStream_t s);
+int v2_decode_splits(int B, int Lmax, int Hkv, int* chunk_out);      // CUDA-core split kernel
+int v2_decode_tc_splits(int B, int Lmax, int Hkv, int* chunk_out);   // tensor-core split kernel
+size_t v2_decode_workspace_bytes(int B, int Lmax, int Hq, int Hkv);  // enough for either
+cudaError_t launch_v2_decode(const V2DecodeArgs& a, cudaStream_t s);  // CUDA cores
+cudaError_t launch_v2_decode_tc(const V2DecodeArgs& a, cudaStream_t s, char* err, size_t err_len);
+cudaError_t launch_v2_combine(const V2DecodeArgs& a, int splits, cudaStream_t s);
+cudaError_t status_v2_decode_tc(int* v);
 
 // Decode whose split partials live in a fixed device array of this size (no workspace argument).
 constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(16) << 20;

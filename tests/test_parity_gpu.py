@@ -230,6 +230,33 @@ def test_v2_decode_small(B, L, Hq, Hkv, ragged):
     assert_bf16(got, want)
 
 
+@pytest.mark.parametrize("B,L,Hq,Hkv,ragged", [(3, 700, 16, 2, False), (2, 1000, 16, 4, True),
+                                               (5, 37, 4, 2, True)])
+def test_v2_decode_cuda_core_path(B, L, Hq, Hkv, ragged):
+    inp = make_v2_decode_inputs(B, L, Hq, Hkv, 128, seed=121 + L, ragged=ragged)
+    got = da.diffattn_v2_decode(inp.q.to(DEV), inp.k_cache.to(DEV), inp.v_cache.to(DEV),
+                                inp.lam_logit.to(DEV), seqlens=inp.seqlens.to(DEV),
+                                cuda_cores=True)
+    want = ref.diffattn_v2_decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, inp.lam_logit)
+    assert_bf16(got, want)
+
+
+def test_v2_decode_ignores_cache_past_seqlen():
+    """Cache rows past seqlens[b] may hold anything (here NaN and Inf): the result must not see them."""
+    inp = make_v2_decode_inputs(3, 520, 16, 2, 128, seed=131)
+    seqlens = torch.tensor([200, 1, 389], dtype=torch.int32)
+    kc, vc = inp.k_cache.clone(), inp.v_cache.clone()
+    for b, L in enumerate(seqlens.tolist()):
+        kc[b, L:] = float("nan")
+        vc[b, L:] = float("inf")
+    want = ref.diffattn_v2_decode(inp.q, inp.k_cache, inp.v_cache, seqlens, inp.lam_logit)
+    for cc in (False, True):
+        got = da.diffattn_v2_decode(inp.q.to(DEV), kc.to(DEV), vc.to(DEV), inp.lam_logit.to(DEV),
+                                    seqlens=seqlens.to(DEV), cuda_cores=cc)
+        assert torch.isfinite(got).all()
+        assert_bf16(got, want)
+
+
 def test_v2_decode_no_seqlens_means_full():
     inp = make_v2_decode_inputs(2, 650, 16, 2, 128, seed=111)
     got = da.diffattn_v2_decode(inp.q.to(DEV), inp.k_cache.to(DEV), inp.v_cache.to(DEV),
