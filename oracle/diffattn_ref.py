@@ -251,3 +251,97 @@ def diffattn_v2_decode(q, k_cache, v_cache, seqlens, lam_logit):
             a2 = attention_head(q[b, 2 * p + 1:2 * p + 2], kb[:, g], vb[:, g], causal=False)
             out[b, p, :] = (a1 - sig[b, p] * a2)[0]
     return out
+
+
+# --------------------------------------------------------------------------------------------
+# backward of the V1 prefill: the gradients a training step needs  ([P3] "The mechanism,
+# exactly" gives the forward; its gradients follow by the chain rule, step by step in reverse)
+# --------------------------------------------------------------------------------------------
+
+def subln_bwd(O, weight, eps: float, dY):
+    """Gradients of Y = O / sqrt(mean(O^2) + eps) * w (over the last axis) given dY.
+
+    With r = (mean(O^2) + eps)^(-1/2) and Yhat = O r: dO = r (g - Yhat mean(g Yhat)), g = dY w;
+    dw = sum over rows of dY Yhat. Returns (dO, dw).
+    """
+    O, dY = _f64(O), _f64(dY)
+    r = 1.0 / np.sqrt(np.mean(O * O, axis=-1, keepdims=True) + eps)
+    Yhat = O * r
+    w = 1.0 if weight is None else _f64(weight)
+    g = dY * w
+    dO = r * (g - Yhat * np.mean(g * Yhat, axis=-1, keepdims=True))
+    dw = np.sum(dY * Yhat, axis=0)
+    return dO, dw
+
+
+def softmax_rows_bwd(A: np.ndarray, dA: np.ndarray) -> np.ndarray:
+    """dS for A = softmax(S) along rows: A * (dA - rowsum(dA * A)). Masked entries (A = 0) get 0."""
+    return A * (dA - np.sum(dA * A, axis=-1, keepdims=True))
+
+
+def diff_attn_head_bwd(q1, k1, q2, k2, v, lam: float, causal: bool, dO):
+    """Gradients of O = (softmax(S1) - lam softmax(S2)) V with S_m = Q_m K_m^T / sqrt(d).
+
+    Reverse order of the forward: dW = dO V^T and dV = W^T dO; dA1 = dW, dA2 = -lam dW and
+    dlam = -sum(A2 * dW); each softmax backward; then dQ_m = dS_m K_m / sqrt(d) and
+    dK_m = dS_m^T Q_m / sqrt(d). Returns (dq1, dk1, dq2, dk2, dv, dlam).
+    """
+    q1, k1, q2, k2, v, dO = (_f64(t) for t in (q1, k1, q2, k2, v, dO))
+    rows = np.arange(q1.shape[0])
+    c = 1.0 / math.sqrt(q1.shape[-1])
+    A1 = softmax_rows(scores(q1, k1, rows, causal))
+    A2 = softmax_rows(scores(q2, k2, rows, causal))
+    W = A1 - lam * A2
+    dW = dO @ v.T
+    dv = W.T @ dO
+    dlam = -float(np.sum(A2 * dW))
+    dS1 = softmax_rows_bwd(A1, dW)
+    dS2 = softmax_rows_bwd(A2, -lam * dW)
+    return (dS1 @ k1 * c, dS1.T @ q1 * c, dS2 @ k2 * c, dS2.T @ q2 * c, dv, dlam)
+
+
+def diffattn_bwd(q, k, v, lam, lam_init: float, dy, norm_weight=None, eps: float = 1e-5,
+                 norm: bool = True, apply_scale: bool = True, causal: bool = True, heads=None):
+    """Backward of `diffattn_fwd` for the upstream gradient dy [B,N,H,dv].
+
+    Returns dict(dq [B,N,H,2d] = [dQ1|dQ2], dk [B,N,H,2d] = [dK1|dK2], dv [B,N,H,dv],
+    dlam [H], dw [dv]) in float64; dw is the gradient of the per-channel norm weight (summed over
+    every row and head; zeros without the norm). `heads` restricts the work to a list of
+    (b, h) pairs (others stay zero) -- dlam and dw then sum over those pairs only.
+    """
+    q, k, v, dy = _f64(q), _f64(k), _f64(v), _f64(dy)
+    B, N, H, two_d = q.shape
+    d = two_d // 2
+    dvw = v.shape[-1]
+    lam = np.broadcast_to(_f64(lam), (H,))
+    s = (1.0 - lam_init) if apply_scale else 1.0
+    out = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v),
+               dlam=np.zeros(H), dw=np.zeros(dvw))
+    pairs = [(b, h) for b in range(B) for h in range(H)] if heads is None else heads
+    for b, h in pairs:
+        q1, q2 = q[b, :, h, :d], q[b, :, h, d:]
+        k1, k2 = k[b, :, h, :d], k[b, :, h, d:]
+        O = diff_attn_head(q1, k1, q2, k2, v[b, :, h, :], float(lam[h]), causal)
+        dYs = dy[b, :, h, :] * s
+        if norm:
+            dO, dwh = subln_bwd(O, norm_weight, eps, dYs)
+            out["dw"] += dwh
+        else:
+            dO = dYs
+        dq1, dk1, dq2, dk2, dvh, dl = diff_attn_head_bwd(q1, k1, q2, k2, v[b, :, h, :],
+                                                          float(lam[h]), causal, dO)
+        out["dq"][b, :, h, :d], out["dq"][b, :, h, d:] = dq1, dq2
+        out["dk"][b, :, h, :d], out["dk"][b, :, h, d:] = dk1, dk2
+        out["dv"][b, :, h, :] = dvh
+        out["dlam"][h] += dl
+    return out
+
+
+def lambda_full_bwd(lq1, lk1, lq2, lk2, dlam):
+    """Gradients of lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init w.r.t. the four
+    vectors ([n_sets, dim]) given dlam [n_sets]. Returns (dlq1, dlk1, dlq2, dlk2)."""
+    lq1, lk1, lq2, lk2 = (_f64(t) for t in (lq1, lk1, lq2, lk2))
+    g = _f64(dlam)[..., None]
+    e1 = np.exp(np.sum(lq1 * lk1, axis=-1, keepdims=True))
+    e2 = np.exp(np.sum(lq2 * lk2, axis=-1, keepdims=True))
+    return g * e1 * lk1, g * e1 * lq1, -g * e2 * lk2, -g * e2 * lq2

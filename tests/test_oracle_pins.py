@@ -283,11 +283,87 @@ def pin_v2_decode_is_last_prefill_row():
         assert np.allclose(out[b], full[0, 0], atol=1e-12, rtol=1e-12), b
 
 
+def _bwd_case(rng, B, N, H, d, dv):
+    q = rng.standard_normal((B, N, H, 2 * d))
+    k = rng.standard_normal((B, N, H, 2 * d))
+    v = rng.standard_normal((B, N, H, dv))
+    dy = rng.standard_normal((B, N, H, dv))
+    lam = rng.uniform(0.1, 1.1, H)
+    w = rng.uniform(0.5, 1.5, dv)
+    return q, k, v, dy, lam, w
+
+
+def pin_bwd_finite_differences():
+    """The backward against central differences of the (separately pinned) forward: for each
+    input, the directional derivative of L = sum(dy * fwd) along a random direction equals the
+    inner product of the returned gradient with that direction."""
+    rng = np.random.default_rng(7)
+    eps = 1e-6
+    for causal in (True, False):
+        for norm in (True, False):
+            q, k, v, dy, lam, w = _bwd_case(rng, 2, 7, 2, 3, 5)
+            li = 0.35
+            g = ref.diffattn_bwd(q, k, v, lam, li, dy, norm_weight=w, eps=1e-5, norm=norm,
+                                 causal=causal)
+            args = dict(q=q, k=k, v=v, lam=lam, w=w)
+
+            def L(a):
+                return float(np.sum(dy * ref.diffattn_fwd(a["q"], a["k"], a["v"], a["lam"], li,
+                                                          norm_weight=a["w"], eps=1e-5, norm=norm,
+                                                          causal=causal)))
+            for name, key in (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dlam", "lam"), ("dw", "w")):
+                D = rng.standard_normal(np.shape(args[key]))
+                hi, lo = dict(args), dict(args)
+                hi[key] = args[key] + eps * D
+                lo[key] = args[key] - eps * D
+                fd = (L(hi) - L(lo)) / (2 * eps)
+                an = float(np.sum(g[name] * D))
+                assert an == pytest.approx(fd, rel=1e-6, abs=1e-8), (name, causal, norm, an, fd)
+
+
+def pin_bwd_autograd():
+    """The backward against torch autograd (float64) of an independent torch expression of the
+    forward."""
+    rng = np.random.default_rng(11)
+    B, N, H, d, dv = 1, 9, 3, 4, 8
+    q, k, v, dy, lam, w = _bwd_case(rng, B, N, H, d, dv)
+    li, eps = 0.6, 1e-5
+    t = lambda a: torch.tensor(a, dtype=torch.float64, requires_grad=True)
+    tq, tk, tv, tl, tw = t(q), t(k), t(v), t(lam), t(w)
+    S1 = torch.einsum("bnhd,bmhd->bhnm", tq[..., :d], tk[..., :d]) / math.sqrt(d)
+    S2 = torch.einsum("bnhd,bmhd->bhnm", tq[..., d:], tk[..., d:]) / math.sqrt(d)
+    mask = torch.ones(N, N, dtype=torch.bool).tril()
+    S1, S2 = S1.masked_fill(~mask, float("-inf")), S2.masked_fill(~mask, float("-inf"))
+    Wt = torch.softmax(S1, -1) - tl[None, :, None, None] * torch.softmax(S2, -1)
+    O = torch.einsum("bhnm,bmhe->bnhe", Wt, tv)
+    Y = O * torch.rsqrt((O * O).mean(-1, keepdim=True) + eps) * tw * (1 - li)
+    (Y * torch.tensor(dy)).sum().backward()
+    g = ref.diffattn_bwd(q, k, v, lam, li, dy, norm_weight=w, eps=eps)
+    for name, tt in (("dq", tq), ("dk", tk), ("dv", tv), ("dlam", tl), ("dw", tw)):
+        assert np.allclose(g[name], tt.grad.numpy(), rtol=1e-10, atol=1e-12), name
+
+
+def pin_lambda_bwd():
+    """Gradients of the lambda re-parameterisation against central differences."""
+    rng = np.random.default_rng(5)
+    vecs = [rng.standard_normal((3, 8)) * 0.3 for _ in range(4)]
+    dl = rng.standard_normal(3)
+    grads = ref.lambda_full_bwd(*vecs, dl)
+    eps = 1e-6
+    for i in range(4):
+        D = rng.standard_normal(vecs[i].shape)
+        hi = [x + eps * D if j == i else x for j, x in enumerate(vecs)]
+        lo = [x - eps * D if j == i else x for j, x in enumerate(vecs)]
+        fd = (np.sum(dl * ref.lambda_full(*hi, 12)) - np.sum(dl * ref.lambda_full(*lo, 12))) / (2 * eps)
+        assert float(np.sum(grads[i] * D)) == pytest.approx(fd, rel=1e-6), i
+
+
 PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, pin_lambda_spread,
         pin_softmax_floor, pin_toy_needle_table, pin_worked_example, pin_row_sums,
         pin_lambda_zero_is_softmax_attention, pin_equal_maps_scale_attention, pin_brute_force_tiny,
         pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
-        pin_v2_decode_is_last_prefill_row]
+        pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
+        pin_lambda_bwd]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -301,7 +377,16 @@ def test_pin(pin):
 
 def _mutants():
     orig = {n: getattr(ref, n) for n in ("lambda_init", "lambda_full", "scores", "diff_weights",
-                                         "subln", "head_epilogue", "v2_kv_head", "softmax_rows")}
+                                         "subln", "head_epilogue", "v2_kv_head", "softmax_rows",
+                                         "diff_attn_head_bwd", "lambda_full_bwd")}
+
+    def bwd_dlam_sign(*a):
+        g = orig["diff_attn_head_bwd"](*a)
+        return g[:5] + (-g[5],)
+
+    def lambda_bwd_swapped(lq1, lk1, lq2, lk2, dlam):
+        g = orig["lambda_full_bwd"](lq1, lk1, lq2, lk2, dlam)
+        return g[1], g[0], g[2], g[3]
 
     def scores_wrong_scale(Q, K, row_ids, causal):
         return orig["scores"](Q, K, row_ids, causal) * math.sqrt(Q.shape[-1]) / math.sqrt(2 * Q.shape[-1])
@@ -334,6 +419,13 @@ def _mutants():
         "scale 1+lambda_init": ("head_epilogue", lambda O, w, eps, li, norm, apply_scale:
                                 orig["head_epilogue"](O, w, eps, li, norm, False) * ((1 + li) if apply_scale else 1)),
         "v2 wrong group": ("v2_kv_head", lambda p, Hq, Hkv: p // (Hq // Hkv)),
+        "softmax bwd without row term": ("softmax_rows_bwd", lambda A, dA: A * dA),
+        "norm bwd without projection": ("subln_bwd", lambda O, w, eps, dY: (
+            ref._f64(dY) * (1.0 if w is None else ref._f64(w))
+            / np.sqrt(np.mean(ref._f64(O) ** 2, -1, keepdims=True) + eps),
+            np.zeros(np.shape(O)[-1]))),
+        "dlam sign": ("diff_attn_head_bwd", bwd_dlam_sign),
+        "lambda bwd q/k swapped": ("lambda_full_bwd", lambda_bwd_swapped),
     }
 
 
