@@ -38,6 +38,12 @@ LONG = dict(B=1, N=65536, H=12, d=128, dv=256, layer=24)
 FLOPS_PER_PAIR = 1536        # 4d + 4dv MMA flops per causal (query, key) pair, V1
 FLOPS_PER_PAIR_DEF = 1024    # 4d + 2dv: the definition (A1 - lambda A2) V
 V2_FLOPS_PER_PAIR = 8 * 128  # per (query, key) pair of one differential pair: 2 heads x (QK + PV)
+# backward per causal pair: S1, S2 recomputed (4d), dW = dO V^T (2dv), dV (2dv), dK1+dK2 (4d),
+# dQ1+dQ2 (4d) = 2560, i.e. 2.5x the definition's forward count; the kernels issue 4352 (the
+# delta pass 2d + 2dv, and dW once per map)
+BWD_FLOPS_PER_PAIR = 4 * 128 + 2 * 256 + 2 * 256 + 4 * 128 + 4 * 128
+BWD_ISSUED_FLOPS_PER_PAIR = (2 * 128 + 2 * 256) + 2 * (2 * 128 + 2 * 256 + 2 * 128 + 2 * 128) \
+    + (4 * 128 + 2 * 256)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -249,7 +255,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     import torch
     import torch.distributed as dist
     import differential_attention_gb300 as da
-    from synth import (make_decode_inputs, make_lambda_vectors, make_prefill_inputs,
+    from synth import (make_decode_inputs, make_dout, make_lambda_vectors, make_prefill_inputs,
                        make_v2_decode_inputs, make_v2_inputs)
 
     dev = torch.device("cuda", local_rank)
@@ -475,6 +481,65 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del vinp, vout
         torch.cuda.empty_cache()
 
+    # ======================= training step: forward (saving statistics) + backward ==========
+    if args.only in ("all", "backward"):
+        c = PREFILL
+        inp = make_prefill_inputs(c["B"], c["N"], c["H"], c["d"], c["dv"], seed=7000 + rank,
+                                  layer=c["layer"], device=dev)
+        dy = make_dout(c["B"], c["N"], c["H"], c["dv"], seed=7007 + rank, device=dev)
+        lam = torch.linspace(0.5, 0.9, c["H"], dtype=torch.float32, device=dev)
+        li = da.diffattn_lambda_init(c["layer"])
+        w = torch.ones(c["dv"], dtype=torch.float32, device=dev)
+        ws = torch.empty(da.diffattn_bwd_workspace_size(c["B"], c["N"], c["H"], c["d"], c["dv"]),
+                         dtype=torch.uint8, device=dev)
+        saved = {}
+        grads = dict(dq=torch.empty_like(inp.q), dk=torch.empty_like(inp.k),
+                     dv=torch.empty_like(inp.v),
+                     dlam=torch.empty(c["H"], dtype=torch.float32, device=dev),
+                     dw=torch.empty(c["dv"], dtype=torch.float32, device=dev))
+
+        def fwd():
+            saved["out"], saved["o_pre"], saved["stats"] = da.diffattn_fwd_train(
+                inp.q, inp.k, inp.v, lam, li, norm_weight=w)
+
+        def bwd():
+            da.diffattn_bwd(inp.q, inp.k, inp.v, saved["o_pre"], saved["stats"], dy, lam, li,
+                            norm_weight=w, workspace=ws, grads=grads)
+
+        for _ in range(args.warmup):
+            fwd()
+            bwd()
+        barrier()
+        n_steps = max(3, min(20, args.steps))
+        ev_f = [(ev(), ev()) for _ in range(n_steps)]
+        ev_b = [(ev(), ev()) for _ in range(n_steps)]
+        for i in range(n_steps):
+            ev_f[i][0].record(stream)
+            fwd()
+            ev_f[i][1].record(stream)
+            ev_b[i][0].record(stream)
+            bwd()
+            ev_b[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        fms = statistics.mean(a.elapsed_time(b) for a, b in ev_f)
+        bms = statistics.mean(a.elapsed_time(b) for a, b in ev_b)
+        pairs = c["B"] * c["H"] * causal_pairs(c["N"])
+        bflops = float(pairs * BWD_FLOPS_PER_PAIR)
+        btf = bflops / (bms * 1e-3) / 1e12
+        line["backward"] = {
+            "metric": "DiffAttn bwd TFLOP/s", "value": world * btf, "unit": "TFLOP/s",
+            "ms_per_call": bms, "fwd_train_ms": fms,
+            "workload": "prefill_3b training step: B4 N4096 H12 d128 dv256 causal, norm + scale; "
+                        "forward with saved statistics, then every gradient",
+            "roofline": {"bound": "tensor", "achieved": btf, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": btf / peak_tf, "flops_per_launch": bflops,
+                         "flops_per_pair": BWD_FLOPS_PER_PAIR,
+                         "issued_flops_per_pair": BWD_ISSUED_FLOPS_PER_PAIR},
+            "gpu_launches": 5 * n_steps}
+        del inp, dy, saved, grads, ws
+        torch.cuda.empty_cache()
+
     # ======================= V2 decode =======================
     if args.only in ("all", "v2_decode"):
         c = dict(V2_DECODE, B=args.decode_batch)
@@ -535,7 +600,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2", "v2_decode", "long"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2", "v2_decode", "long", "backward"], default="all",
                     help="profiling aid: run one workload (the JSON line then lacks the others)")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="profiling aid: a smaller decode batch for captures that save device memory")

@@ -64,6 +64,15 @@ _SIGNATURES = {
                         + [ctypes.c_void_p]),
     "diffattn_v2_decode_workspace_size": (ctypes.c_int, [ctypes.c_int] * 5
                                           + [ctypes.POINTER(ctypes.c_size_t)]),
+    "diffattn_fwd_train": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_float, ctypes.c_void_p,
+                                                                   ctypes.c_float]
+                           + [ctypes.c_int] * 7 + [ctypes.c_void_p]),
+    "diffattn_bwd_workspace_size": (ctypes.c_int, [ctypes.c_int] * 5
+                                    + [ctypes.POINTER(ctypes.c_size_t)]),
+    "diffattn_bwd": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_float, ctypes.c_void_p,
+                                                             ctypes.c_float]
+                     + [ctypes.c_void_p] * 5 + [ctypes.c_int] * 7
+                     + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_v2_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int] * 7
                            + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
 }
@@ -312,3 +321,69 @@ def diffattn_v2_decode(q, k_cache, v_cache, lam_logit, seqlens=None, cuda_cores:
                                     DIFFATTN_BF16, _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
+
+
+def _train_flags(causal, norm, scale):
+    return ((DIFFATTN_CAUSAL if causal else 0) | (DIFFATTN_NORM if norm else 0)
+            | (DIFFATTN_SCALE if scale else 0))
+
+
+def diffattn_fwd_train(q, k, v, lam, lambda_init: float = 0.0, norm_weight=None, eps: float = 1e-5,
+                       causal: bool = True, norm: bool = True, scale: bool = True, stream=None):
+    """Forward for training: returns (out, o_pre, stats); o_pre is the head output before the
+    norm and scale, stats [B, H, 2, Npad] the per-row base-2 log-sum-exp of each map."""
+    _dev("q", q, torch.bfloat16)
+    B, N, H, two_d = q.shape
+    d = two_d // 2
+    _dev("k", k, torch.bfloat16)
+    _dev("v", v, torch.bfloat16)
+    dv = v.shape[-1]
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=q.device)
+    o_pre = torch.empty_like(out)
+    npad = (N + 127) // 128 * 128
+    stats = torch.empty((B, H, 2, npad), dtype=torch.float32, device=q.device)
+    _check(lib().diffattn_fwd_train(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(o_pre), _ptr(stats),
+                                    _ptr(lam), float(lambda_init), _ptr(norm_weight), float(eps),
+                                    B, N, H, d, dv, _train_flags(causal, norm, scale),
+                                    DIFFATTN_BF16, _stream(stream)))
+    return out, o_pre, stats
+
+
+def diffattn_bwd_workspace_size(B: int, N: int, H: int, d: int, dv: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().diffattn_bwd_workspace_size(B, N, H, d, dv, ctypes.byref(n)))
+    return n.value
+
+
+def diffattn_bwd(q, k, v, o_pre, stats, dout, lam, lambda_init: float = 0.0, norm_weight=None,
+                 eps: float = 1e-5, causal: bool = True, norm: bool = True, scale: bool = True,
+                 workspace=None, grads=None, stream=None):
+    """Backward of the V1 prefill. Returns dict(dq, dk, dv, dlam, dw) (dw None without a norm
+    weight tensor to differentiate)."""
+    _dev("q", q, torch.bfloat16)
+    B, N, H, two_d = q.shape
+    d = two_d // 2
+    dv = v.shape[-1]
+    for name, t in (("k", k), ("v", v), ("o_pre", o_pre), ("dout", dout)):
+        _dev(name, t, torch.bfloat16)
+    _dev("stats", stats, torch.float32)
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if workspace is None:
+        workspace = torch.empty(diffattn_bwd_workspace_size(B, N, H, d, dv), dtype=torch.uint8,
+                                device=q.device)
+    if grads is None:
+        grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                     dlam=torch.empty((H,), dtype=torch.float32, device=q.device),
+                     dw=torch.empty((dv,), dtype=torch.float32, device=q.device))
+    _check(lib().diffattn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o_pre), _ptr(stats), _ptr(dout),
+                              _ptr(lam), float(lambda_init), _ptr(norm_weight), float(eps),
+                              _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]),
+                              _ptr(grads["dlam"]), _ptr(grads.get("dw")), B, N, H, d, dv,
+                              _train_flags(causal, norm, scale), DIFFATTN_BF16, _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream)))
+    return grads

@@ -64,13 +64,14 @@ DIFFATTN_API const char* diffattn_last_error_string(void) { return t_err.c_str()
 DIFFATTN_API int diffattn_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  int v = 0, w = 0, x = 0, y = 0;
+  int v = 0, w = 0, x = 0, y = 0, z = 0;
   e = da::status_prefill_tc(&v);
   if (e == cudaSuccess) e = da::status_prefill_exact(&w);
   if (e == cudaSuccess) e = da::status_simt(&x);
   if (e == cudaSuccess) e = da::status_v2_decode_tc(&y);
+  if (e == cudaSuccess) e = da::status_backward(&z);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
-  v |= w | x | y;
+  v |= w | x | y | z;
   if (v != 0) return fail(DIFFATTN_ERR_TIMEOUT, "a bounded wait inside a kernel ran out (status %d)", v);
   return ok();
 }
@@ -392,5 +393,125 @@ DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const vo
   if (e == cudaErrorNotSupported) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_decode: unsupported group size");
   if (e == cudaErrorInvalidValue && err[0]) return fail(DIFFATTN_ERR_CUDA, "diffattn_v2_decode: %s", err);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_decode launch");
+  return ok();
+}
+
+namespace {
+int check_train_shape(const char* fn, int B, int N, int H, int d, int dv, int dtype) {
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);
+  if (B < 1 || N < 1 || H < 1) return fail(DIFFATTN_ERR_SHAPE, "%s: B, N, H must be >= 1", fn);
+  if (d != 128 || dv != 256)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need d = 128 and dv = 256 (got d=%d dv=%d)", fn, d, dv);
+  const long long tiles = (static_cast<long long>(N) + 127) / 128 * B * H;
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(N) * H > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: problem too large for one launch", fn);
+  return DIFFATTN_OK;
+}
+}  // namespace
+
+DIFFATTN_API int diffattn_fwd_train(const void* q, const void* k, const void* v, void* out,
+                                    void* o_pre, float* stats, const float* lambda,
+                                    float lambda_init, const float* norm_weight, float eps, int B,
+                                    int N, int H, int d, int dv, int flags, int dtype,
+                                    void* stream) {
+  if (!q || !k || !v || !out || !o_pre || !stats || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_train: null pointer");
+  constexpr int kTrainFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kTrainFlags) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_train: unknown flag bits 0x%x", flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_train: eps must be > 0 with DIFFATTN_NORM");
+  int rc = check_train_shape("diffattn_fwd_train", B, N, H, d, dv, dtype);
+  if (rc) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(o_pre, 16) || !aligned(stats, 16) || !aligned(lambda, 4) ||
+      (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_fwd_train: tensors must be 16-byte aligned");
+  rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = N;
+  p.units = H;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_V1;
+  p.q_heads = H;
+  p.kv_heads = H;
+  p.q_cols = 2 * d;
+  p.k_cols = 2 * d;
+  p.group = 1;
+  p.lambda = lambda;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  p.stats = stats;
+  p.o_pre = o_pre;
+  p.n_pad = (N + 127) / 128 * 128;
+  return run_prefill(p, dtype, "diffattn_fwd_train", static_cast<cudaStream_t>(stream));
+}
+
+DIFFATTN_API int diffattn_bwd_workspace_size(int B, int N, int H, int d, int dv, size_t* bytes) {
+  if (!bytes) return fail(DIFFATTN_ERR_ARG, "diffattn_bwd_workspace_size: null pointer");
+  int rc = check_train_shape("diffattn_bwd_workspace_size", B, N, H, d, dv, DIFFATTN_BF16);
+  if (rc) return rc;
+  *bytes = da::backward_workspace_bytes(B, N, H);
+  return ok();
+}
+
+DIFFATTN_API int diffattn_bwd(const void* q, const void* k, const void* v, const void* o_pre,
+                              const float* stats, const void* dout, const float* lambda,
+                              float lambda_init, const float* norm_weight, float eps, void* dq,
+                              void* dk, void* dv, float* dlambda, float* dnorm_weight, int B,
+                              int N, int H, int d, int dv_width, int flags, int dtype,
+                              void* workspace, size_t ws_bytes, void* stream) {
+  if (!q || !k || !v || !o_pre || !stats || !dout || !lambda || !dq || !dk || !dv || !dlambda)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_bwd: null pointer");
+  constexpr int kTrainFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kTrainFlags) return fail(DIFFATTN_ERR_ARG, "diffattn_bwd: unknown flag bits 0x%x", flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_bwd: eps must be > 0 with DIFFATTN_NORM");
+  int rc = check_train_shape("diffattn_bwd", B, N, H, d, dv_width, dtype);
+  if (rc) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o_pre, 16) ||
+      !aligned(stats, 16) || !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) ||
+      !aligned(dv, 16) || !aligned(lambda, 4) || !aligned(dlambda, 4) ||
+      (norm_weight && !aligned(norm_weight, 16)) || (dnorm_weight && !aligned(dnorm_weight, 4)))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_bwd: tensors must be 16-byte aligned");
+  const size_t need = da::backward_workspace_bytes(B, N, H);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(DIFFATTN_ERR_WORKSPACE, "diffattn_bwd: need a 256-byte aligned workspace of %zu bytes", need);
+  rc = check_device();
+  if (rc) return rc;
+  da::BackwardArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o_pre = o_pre;
+  a.stats = stats;
+  a.dout = dout;
+  a.lambda = lambda;
+  a.lambda_init = lambda_init;
+  a.norm_w = norm_weight;
+  a.eps = eps;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dlambda = dlambda;
+  a.dnorm_w = dnorm_weight;
+  a.B = B;
+  a.N = N;
+  a.H = H;
+  a.flags = flags;
+  a.workspace = workspace;
+  char err[256] = {0};
+  cudaError_t e = da::launch_backward(a, static_cast<cudaStream_t>(stream), err, sizeof(err));
+  if (err[0]) return fail(DIFFATTN_ERR_CUDA, "diffattn_bwd: %s", err);
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_bwd launch");
   return ok();
 }

@@ -1,0 +1,1196 @@
+// backward.cu -- gradients of the V1 prefill (page "Differential Transformer: softmax can't say
+// zero, so it subtracts", section "The mechanism, exactly" gives the forward; the backward is its
+// chain rule taken step by step in reverse).
+//
+// Per head, with c = 1/sqrt(d), A_m = softmax(c Q_m K_m^T) (causal), W = A1 - lam A2, O = W V and
+// Y = RMSNorm(O) * w * (1 - lambda_init):
+//   dO from dY through the norm;  dW = dO V^T;  dV = W^T dO;  dlam = -sum(A2 * dW)
+//   dS_m = coef_m * A_m * (dW - delta_m),  coef_1 = 1, coef_2 = -lam,
+//   delta_m[i] = sum_j A_m[i,j] dW[i,j] = dO_i . (A_m V)_i
+//   dQ_m = c dS_m K_m,  dK_m = c dS_m^T Q_m.
+// The forward for training saves, per row and map, b_m = log2 sum_j 2^(c log2(e) s_ij), so that
+// A_m = 2^(c log2(e) s - b_m) is recomputed exactly without a running max.
+//
+// Kernels, in launch order:
+//   bwd_pre_kernel    CUDA cores: norm backward -> dO (bf16), D = dO . O, norm-weight partials;
+//                     zeroes the fp32 dQ accumulator.
+//   bwd_delta_kernel  tcgen05, query-major: O2 = A2 V -> delta_2 = dO . O2,
+//                     delta_1 = D + lam delta_2 (because O = O1 - lam O2), and -sum delta_2 per CTA.
+//   bwd_dkdq_kernel   tcgen05, key-major, one map per CTA: S^T = K Q^T, dW^T = V dO^T,
+//                     dS^T in shared memory, dK += dS^T Q (TMEM), dQ partial = dS K (TMEM) added
+//                     to the fp32 accumulator with red.global.add.v4.f32.
+//   bwd_dv_kernel     tcgen05, key-major: S1^T, S2^T -> W^T in shared memory, dV += W^T dO.
+//   bwd_finish_kernel dQ fp32 -> bf16; dlam and norm-weight sums (fixed order: deterministic).
+// TMEM is 512 columns per SM; each tensor-core kernel fills it exactly:
+//   delta: S double-buffered (2 x 128) + O2 (256);  dkdq: S^T, dW^T, dK, dQ (4 x 128);
+//   dv: S1^T, S2^T (2 x 128) + dV (256).
+// Every wait is bounded (2 s); a timeout flags DEV_TIMEOUT in this file's status word and the
+// roles unwind without hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace da {
+namespace bwd {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kD = 128;    // width of one query/key half
+constexpr int kDV = 256;   // value width
+constexpr int kT = 128;    // rows per tile (queries or keys)
+constexpr int kBox = kT * 128;  // one 64-column box of a 128-row tile: 16 KB
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "barrier.red.and.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Launch order for L2 reuse: work units (a head, or a head and map) are taken in groups of
+// `group`; inside a group, tile rank 0 (the longest causal tile) of every unit first, then rank 1,
+// and so on. Returns the unit and the tile rank of item `idx`.
+__device__ __forceinline__ void grouped_item(int idx, int n_units, int n_tiles, int group,
+                                             int& unit, int& rank) {
+  const int g0 = (idx / (group * n_tiles)) * group;
+  const int gsize = min(group, n_units - g0);
+  const int r = idx - g0 * n_tiles;
+  rank = r / gsize;
+  unit = g0 + r % gsize;
+}
+
+struct Args {
+  const __nv_bfloat16* q;   // [B, N, H, 2d]
+  const __nv_bfloat16* k;   // [B, N, H, 2d]
+  const __nv_bfloat16* v;   // [B, N, H, dv]
+  const __nv_bfloat16* o_pre;  // [B, N, H, dv]
+  const __nv_bfloat16* dy;     // [B, N, H, dv]
+  const float* stats;          // [B, H, 2, Npad]
+  const float* lambda;         // [H]
+  const float* norm_w;         // [dv] or null
+  __nv_bfloat16* dq;           // [B, N, H, 2d]
+  __nv_bfloat16* dk;           // [B, N, H, 2d]
+  __nv_bfloat16* dv;           // [B, N, H, dv]
+  float* dlambda;              // [H]
+  float* dnorm_w;              // [dv] or null
+  // workspace
+  __nv_bfloat16* dO;           // [B, N, H, dv]
+  float* delta;                // [B, H, 2, Npad]: D (after pre) then delta_1; delta_2
+  float* dqacc;                // [B, N, H, 2d]
+  float* dw_part;              // [pre blocks, dv]
+  float* dl_part;              // [B, H, n_qt]
+  int B, N, H, Npad, n_t;
+  int pre_blocks;
+  int grp_delta, grp_dkdq, grp_dv;  // L2 groups (units per group) of the three tile kernels
+  float eps, scale_out;        // scale_out = (1 - lambda_init) with DIFFATTN_SCALE, else 1
+  bool norm, causal;
+  float c_log2;                // log2(e) / sqrt(d)
+  float c;                     // 1 / sqrt(d)
+};
+
+// =============================================================================================
+// bwd_pre_kernel: one warp per (b, n, h) row, lane = 8 channels. Without the norm dO = s dY;
+// with it (r = (mean(O^2) + eps)^-1/2, Yhat = O r, g = s dY w): dO = r (g - Yhat mean(g Yhat)),
+// dw += s dY Yhat. D = dO . O uses dO as rounded to bf16 (the value the MMAs see).
+// =============================================================================================
+constexpr int kPreWarps = 8;
+
+__global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(const Args a) {
+  __shared__ float sdw[kPreWarps][kDV];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(a.B) * a.N * a.H;
+  float wl[8], dwl[8];
+  float4 w0 = make_float4(1.f, 1.f, 1.f, 1.f), w1 = w0;
+  if (a.norm_w) {
+    w0 = reinterpret_cast<const float4*>(a.norm_w + 8 * lane)[0];
+    w1 = reinterpret_cast<const float4*>(a.norm_w + 8 * lane)[1];
+  }
+  wl[0] = w0.x; wl[1] = w0.y; wl[2] = w0.z; wl[3] = w0.w;
+  wl[4] = w1.x; wl[5] = w1.y; wl[6] = w1.z; wl[7] = w1.w;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) dwl[i] = 0.f;
+  const float s = a.scale_out;
+  for (long long r = static_cast<long long>(blockIdx.x) * kPreWarps + warp; r < rows;
+       r += static_cast<long long>(gridDim.x) * kPreWarps) {
+    const size_t off = static_cast<size_t>(r) * kDV + 8 * lane;
+    float o[8], dy[8], g[8];
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(a.o_pre + off), o);
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(a.dy + off), dy);
+    float dO[8];
+    if (a.norm) {
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(o[i], o[i], ss);
+      const float rs = rsqrtf(warp_sum(ss) / kDV + a.eps);
+      float gy = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        g[i] = s * dy[i] * wl[i];
+        gy = fmaf(g[i], o[i] * rs, gy);
+        dwl[i] = fmaf(s * dy[i], o[i] * rs, dwl[i]);
+      }
+      const float mg = warp_sum(gy) / kDV;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dO[i] = rs * (g[i] - o[i] * rs * mg);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dO[i] = s * dy[i];
+    }
+    uint4 pk;
+    pk.x = pack_bf16x2(dO[0], dO[1]);
+    pk.y = pack_bf16x2(dO[2], dO[3]);
+    pk.z = pack_bf16x2(dO[4], dO[5]);
+    pk.w = pack_bf16x2(dO[6], dO[7]);
+    *reinterpret_cast<uint4*>(a.dO + off) = pk;
+    float dr[8];
+    bf16x8_to_f32(pk, dr);
+    float Dp = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) Dp = fmaf(dr[i], o[i], Dp);
+    const float D = warp_sum(Dp);
+    const int h = static_cast<int>(r % a.H);
+    const long long bn = r / a.H;
+    const int n = static_cast<int>(bn % a.N), b = static_cast<int>(bn / a.N);
+    if (lane == 0) a.delta[(static_cast<size_t>(b) * a.H + h) * 2 * a.Npad + n] = D;
+    float4* zq = reinterpret_cast<float4*>(a.dqacc + static_cast<size_t>(r) * (2 * kD) + 8 * lane);
+    zq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    zq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sdw[warp][8 * lane + i] = dwl[i];
+  __syncthreads();
+  for (int cidx = threadIdx.x; cidx < kDV; cidx += blockDim.x) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kPreWarps; ++w) t += sdw[w][cidx];
+    a.dw_part[static_cast<size_t>(blockIdx.x) * kDV + cidx] = t;
+  }
+}
+
+// =============================================================================================
+// bwd_delta_kernel: one CTA per (query tile, b, h). Warp 0 TMA, warp 1 MMA + TMEM, warps 2-5:
+// thread r = query row r. S2 = Q2 K2^T (double-buffered TMEM), P2 = 2^(c' s - b2) to shared
+// memory (K-major), O2 += P2 V (TMEM). Then delta_2 = dO . O2, delta_1 = D + lam delta_2.
+// Loads stream through a ring of 32 KB slots in the order the MMA issuer uses them:
+// K2_0, then per tile t >= 1: K2_t, V_{t-1} keys 0-63, V_{t-1} keys 64-127; finally V_{n-1}.
+// =============================================================================================
+namespace dl {
+constexpr int kThreads = 192;
+constexpr int kSlot = 32 * 1024;
+constexpr int kNSlot = 5;
+constexpr int kQOff = 0;                         // Q2 tile, 32 KB
+constexpr int kPOff = kQOff + 2 * kBox;          // P buffer, 32 KB
+constexpr int kRingOff = kPOff + 2 * kBox;       // ring
+constexpr int kCtrlOff = kRingOff + kNSlot * kSlot;
+constexpr int kVHalfBox = 64 * 128;              // one 64-column box of 64 keys: 8 KB
+struct Ctrl {
+  uint64_t q_full, slot_full[kNSlot], slot_empty[kNSlot], s_full[2], s_free[2], p_full, p_empty,
+      o_full, teardown;
+  uint32_t tmem_slot;
+  int abort_flag;
+  float red[4];
+};
+constexpr int kDynSmem = kCtrlOff + static_cast<int>(sizeof(Ctrl));
+}  // namespace dl
+
+__global__ void __launch_bounds__(dl::kThreads, 1)
+    bwd_delta_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_vh, const Args a) {
+  using namespace dl;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Ctrl& cs = *reinterpret_cast<Ctrl*>(smem + kCtrlOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sQ = smem_u32(smem + kQOff), sP = smem_u32(smem + kPOff);
+  const uint32_t sRing = smem_u32(smem + kRingOff);
+  auto bar = [](uint64_t& x) { return smem_u32(&x); };
+  if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled layouts need 1 KB alignment
+    if (threadIdx.x == 0) flag_device_error(DEV_TIMEOUT);
+    return;
+  }
+
+  int bh, rank;
+  grouped_item(static_cast<int>(blockIdx.x), a.B * a.H, a.n_t, a.grp_delta, bh, rank);
+  const int qt = a.causal ? a.n_t - 1 - rank : rank;
+  const int b = bh / a.H, h = bh % a.H;
+  const int n = a.causal ? qt + 1 : a.n_t;  // key tiles
+  auto k_idx = [](int t) { return t + 2 * max(0, t - 1); };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(cs.q_full), 1);
+    for (int i = 0; i < kNSlot; ++i) {
+      mbar_init(bar(cs.slot_full[i]), 1);
+      mbar_init(bar(cs.slot_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(cs.s_full[i]), 1);
+      mbar_init(bar(cs.s_free[i]), 128);
+    }
+    mbar_init(bar(cs.p_full), 128);
+    mbar_init(bar(cs.p_empty), 1);
+    mbar_init(bar(cs.o_full), 1);
+    mbar_init(bar(cs.teardown), 1);
+    cs.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&cs.tmem_slot), 512);
+    tmem_relinquish();
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = cs.tmem_slot;
+  volatile int* abrt = &cs.abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_vh);
+      mbar_arrive_expect_tx(bar(cs.q_full), 2 * kBox);
+      for (int c = 0; c < 2; ++c)
+        tma_load_4d(sQ + c * kBox, &tm_q, bar(cs.q_full), kD + 64 * c, h, qt * kT, b);
+      int issued = 0;
+      bool ok = true;
+      auto acquire = [&](int idx, uint32_t bytes) -> int {
+        const int s = idx % kNSlot;
+        if (!mbar_wait(bar(cs.slot_empty[s]), ((idx / kNSlot) & 1) ^ 1, abrt)) return -1;
+        mbar_arrive_expect_tx(bar(cs.slot_full[s]), bytes);
+        return s;
+      };
+      for (int t = 0; t <= n && ok; ++t) {
+        int idx = k_idx(t);
+        if (t < n) {
+          const int s = acquire(idx, 2 * kBox);
+          if (s < 0) { ok = false; break; }
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(sRing + s * kSlot + c * kBox, &tm_k, bar(cs.slot_full[s]), kD + 64 * c, h,
+                        t * kT, b);
+          issued = ++idx;
+        }
+        if (t >= 1) {
+          for (int hf = 0; hf < 2 && ok; ++hf) {
+            const int s = acquire(idx, 4 * kVHalfBox);
+            if (s < 0) { ok = false; break; }
+            for (int c = 0; c < 4; ++c)
+              tma_load_4d(sRing + s * kSlot + c * kVHalfBox, &tm_vh, bar(cs.slot_full[s]), 64 * c,
+                          h, (t - 1) * kT + 64 * hf, b);
+            issued = ++idx;
+          }
+        }
+      }
+      mbar_wait(bar(cs.q_full), 0, nullptr);
+      for (int i = max(0, issued - kNSlot); i < issued; ++i)
+        mbar_wait(bar(cs.slot_full[i % kNSlot]), (i / kNSlot) & 1, nullptr);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = umma_idesc_bf16(kT, kT, 0, 0);
+      constexpr uint32_t idesc_o = umma_idesc_bf16(kT, kDV, 0, 1);
+      const uint64_t dq0 = umma_smem_desc(sQ, 16, 1024);
+      const uint64_t dr0 = umma_smem_desc(sRing, 16, 1024);
+      const uint64_t dvh0 = umma_smem_desc(sRing, kVHalfBox, 1024);
+      const uint64_t dp0 = umma_smem_desc(sP, 16, 1024);
+      bool ok = mbar_wait(bar(cs.q_full), 0, abrt);
+      tc_fence_after();
+      for (int t = 0; ok && t <= n; ++t) {
+        int idx = k_idx(t);
+        if (t < n) {
+          const int buf = t & 1;
+          if (t >= 2 && !(ok = mbar_wait(bar(cs.s_free[buf]), ((t >> 1) - 1) & 1, abrt))) break;
+          const int s = idx % kNSlot;
+          if (!(ok = mbar_wait(bar(cs.slot_full[s]), (idx / kNSlot) & 1, abrt))) break;
+          tc_fence_after();
+          const uint64_t kd = desc_add(dr0, s * kSlot);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+            mma_bf16_ss(tmem + buf * kT, desc_add(dq0, off), desc_add(kd, off), idesc_s,
+                        kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(cs.slot_empty[s]));
+          tc_commit(bar(cs.s_full[buf]));
+          ++idx;
+        }
+        if (t >= 1) {
+          const int jv = t - 1;
+          if (!(ok = mbar_wait(bar(cs.p_full), jv & 1, abrt))) break;
+          for (int hf = 0; hf < 2; ++hf) {
+            const int s = (idx + hf) % kNSlot;
+            if (!(ok = mbar_wait(bar(cs.slot_full[s]), ((idx + hf) / kNSlot) & 1, abrt))) break;
+            tc_fence_after();
+            const uint64_t vd = desc_add(dvh0, s * kSlot);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int kk = 4 * hf + k4;
+              mma_bf16_ss(tmem + 2 * kT, desc_add(dp0, (kk >> 2) * kBox + (kk & 3) * 32),
+                          desc_add(vd, k4 * 2048), idesc_o, (jv > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(bar(cs.slot_empty[s]));
+          }
+          if (!ok) break;
+          tc_commit(bar(cs.p_empty));
+          if (t == n) tc_commit(bar(cs.o_full));
+        }
+      }
+      tc_commit(bar(cs.teardown));
+      mbar_wait(bar(cs.teardown), 0, nullptr);
+    }
+  } else {
+    // ---- softmax rows: thread r = query row ----
+    const int q4 = warp & 3;
+    const int r = 32 * q4 + lane;
+    const int row = qt * kT + r;
+    const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+    const size_t st_base = static_cast<size_t>(b * a.H + h) * 2 * a.Npad;
+    const float b2 = row < a.N ? a.stats[st_base + a.Npad + row] : 0.f;
+    const int lim = a.causal ? min(row + 1, a.N) : a.N;  // keys [0, lim) visible
+    const uint32_t p_row = sP + r * 128;
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      const int buf = t & 1;
+      ok = ok && mbar_wait(bar(cs.s_full[buf]), (t >> 1) & 1, abrt);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + tl + buf * kT + 32 * c, sr[c]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(cs.s_free[buf]));
+      const int key0 = t * kT;
+      uint32_t pk[kT / 2];
+#pragma unroll
+      for (int i = 0; i < kT / 2; ++i) {
+        const float x0 = fmaf(__uint_as_float(sr[i >> 4][(2 * i) & 31]), a.c_log2, -b2);
+        const float x1 = fmaf(__uint_as_float(sr[i >> 4][(2 * i + 1) & 31]), a.c_log2, -b2);
+        const float p0 = (key0 + 2 * i < lim) ? ex2_approx(x0) : 0.f;
+        const float p1 = (key0 + 2 * i + 1 < lim) ? ex2_approx(x1) : 0.f;
+        pk[i] = pack_bf16x2(p0, p1);
+      }
+      if (t > 0) {
+        ok = mbar_wait(bar(cs.p_empty), (t - 1) & 1, abrt);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int blk = u >> 3, uu = u & 7;
+        st_shared_v4(p_row + blk * kBox + ((uu ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1],
+                     pk[4 * u + 2], pk[4 * u + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(cs.p_full));
+    }
+    if (ok) {
+      ok = mbar_wait(bar(cs.o_full), 0, abrt);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    float d2 = 0.f;
+    if (ok) {
+      tc_fence_after();
+      const __nv_bfloat16* dorow =
+          a.dO + ((static_cast<size_t>(b) * a.N + min(row, a.N - 1)) * a.H + h) * kDV;
+#pragma unroll 1
+      for (int c = 0; c < kDV / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + tl + 2 * kT + 32 * c, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float f[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(dorow + 32 * c + 8 * g), f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) d2 = fmaf(f[i], __uint_as_float(o[8 * g + i]), d2);
+        }
+      }
+      if (row < a.N) {
+        const float lam = a.lambda[h];
+        float* dl = a.delta + st_base;
+        dl[row] = dl[row] + lam * d2;  // D = dO . O = delta_1 - lam delta_2
+        dl[a.Npad + row] = d2;
+      } else {
+        d2 = 0.f;
+      }
+    }
+    const float ws = warp_sum(-d2);
+    if (lane == 0) cs.red[q4] = ws;
+    if (bar_and(1, 128, ok) && r == 0)
+      a.dl_part[static_cast<size_t>(bh) * a.n_t + qt] = cs.red[0] + cs.red[1] + cs.red[2] + cs.red[3];
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// =============================================================================================
+// bwd_dkdq_kernel: one CTA per (key tile j, b, h, map m); key-major. Warps 0 (TMA), 1 (MMA,
+// TMEM), 2-9: two warpgroups; thread r of warpgroup w owns key row r and query columns
+// [64 w, 64 w + 64) of each inner tile, and for the dQ readout query row r, d-columns
+// [64 w, 64 w + 64).
+// TMEM: S^T cols 0-127, dW^T 128-255, dK 256-383, dQ partial 384-511.
+// Shared memory: K_m,j (32 KB) and V_j (64 KB) stay; Q_m,i (32 KB + its b and delta rows) and
+// dO_i (64 KB) have one slot each; the dS^T tile (32 KB) is read K-major for dK and MN-major
+// for dQ. MMA issue order per inner tile t (keeps the Q slot, freed by dK_t, off the critical
+// path): dK_t | dW^T_{t+1} | S^T_{t+1} | dQ_t.
+// =============================================================================================
+namespace kq {
+constexpr int kThreads = 320;
+constexpr int kKOff = 0;
+constexpr int kVOff = kKOff + 2 * kBox;
+constexpr int kQOff = kVOff + 4 * kBox;
+constexpr int kDOOff = kQOff + 2 * kBox;
+constexpr int kDSOff = kDOOff + 4 * kBox;
+constexpr int kBDOff = kDSOff + 2 * kBox;   // b[128], delta[128]
+constexpr int kCtrlOff = kBDOff + 2 * kT * 4;
+struct Ctrl {
+  uint64_t kv_full, q_full, q_empty, do_full, do_empty, s_full, s_free, ds_full, ds_empty,
+      dq_full, dq_free, dk_full, teardown;
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+constexpr int kDynSmem = kCtrlOff + static_cast<int>(sizeof(Ctrl));
+}  // namespace kq
+
+__global__ void __launch_bounds__(kq::kThreads, 1)
+    bwd_dkdq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do, const Args a) {
+  using namespace kq;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Ctrl& cs = *reinterpret_cast<Ctrl*>(smem + kCtrlOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sK = smem_u32(smem + kKOff), sV = smem_u32(smem + kVOff);
+  const uint32_t sQ = smem_u32(smem + kQOff), sDO = smem_u32(smem + kDOOff);
+  const uint32_t sDS = smem_u32(smem + kDSOff), sBD = smem_u32(smem + kBDOff);
+  const float* bd = reinterpret_cast<const float*>(smem + kBDOff);
+  auto bar = [](uint64_t& x) { return smem_u32(&x); };
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) flag_device_error(DEV_TIMEOUT);
+    return;
+  }
+
+  int unit, j;
+  grouped_item(static_cast<int>(blockIdx.x), a.B * a.H * 2, a.n_t, a.grp_dkdq, unit, j);
+  const int m = unit & 1, bh = unit >> 1;  // both maps of a head run side by side (shared dO)
+  const int b = bh / a.H, h = bh % a.H;
+  const int i0 = a.causal ? j : 0;
+  const int T = a.n_t - i0;  // inner (query) tiles
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(cs.kv_full), 1);
+    mbar_init(bar(cs.q_full), 1);
+    mbar_init(bar(cs.q_empty), 1);
+    mbar_init(bar(cs.do_full), 1);
+    mbar_init(bar(cs.do_empty), 1);
+    mbar_init(bar(cs.s_full), 1);
+    mbar_init(bar(cs.s_free), 256);
+    mbar_init(bar(cs.ds_full), 256);
+    mbar_init(bar(cs.ds_empty), 1);
+    mbar_init(bar(cs.dq_full), 1);
+    mbar_init(bar(cs.dq_free), 256);
+    mbar_init(bar(cs.dk_full), 1);
+    mbar_init(bar(cs.teardown), 1);
+    cs.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&cs.tmem_slot), 512);
+    tmem_relinquish();
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = cs.tmem_slot;
+  volatile int* abrt = &cs.abort_flag;
+  const size_t st_base = static_cast<size_t>(b * a.H + h) * 2 * a.Npad + static_cast<size_t>(m) * a.Npad;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_do);
+      mbar_arrive_expect_tx(bar(cs.kv_full), 6 * kBox);
+      for (int c = 0; c < 2; ++c)
+        tma_load_4d(sK + c * kBox, &tm_k, bar(cs.kv_full), m * kD + 64 * c, h, j * kT, b);
+      for (int c = 0; c < 4; ++c)
+        tma_load_4d(sV + c * kBox, &tm_v, bar(cs.kv_full), 64 * c, h, j * kT, b);
+      bool ok = true;
+      int t = 0;
+      for (; t < T && ok; ++t) {
+        const int i = i0 + t;
+        if (!(ok = mbar_wait(bar(cs.do_empty), (t & 1) ^ 1, abrt))) break;
+        mbar_arrive_expect_tx(bar(cs.do_full), 4 * kBox);
+        for (int c = 0; c < 4; ++c)
+          tma_load_4d(sDO + c * kBox, &tm_do, bar(cs.do_full), 64 * c, h, i * kT, b);
+        if (!(ok = mbar_wait(bar(cs.q_empty), (t & 1) ^ 1, abrt))) break;
+        mbar_arrive_expect_tx(bar(cs.q_full), 2 * kBox + 2 * kT * 4);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sQ + c * kBox, &tm_q, bar(cs.q_full), m * kD + 64 * c, h, i * kT, b);
+        bulk_load(sBD, a.stats + st_base + static_cast<size_t>(i) * kT, kT * 4, bar(cs.q_full));
+        bulk_load(sBD + kT * 4, a.delta + st_base + static_cast<size_t>(i) * kT, kT * 4,
+                  bar(cs.q_full));
+      }
+      // nothing of ours may still be landing at exit
+      mbar_wait(bar(cs.kv_full), 0, nullptr);
+      if (t > 0) {
+        mbar_wait(bar(cs.do_full), (t - 1) & 1, nullptr);
+        mbar_wait(bar(cs.q_full), (t - 1) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_kk = umma_idesc_bf16(kT, kT, 0, 0);  // S^T, dW^T
+      constexpr uint32_t idesc_dk = umma_idesc_bf16(kT, kD, 0, 1);  // dS^T (K-major) x Q (MN)
+      constexpr uint32_t idesc_dq = umma_idesc_bf16(kT, kD, 1, 1);  // dS (MN) x K (MN)
+      const uint64_t dK0 = umma_smem_desc(sK, 16, 1024);
+      const uint64_t dKmn = umma_smem_desc(sK, kBox, 1024);
+      const uint64_t dV0 = umma_smem_desc(sV, 16, 1024);
+      const uint64_t dQ0 = umma_smem_desc(sQ, 16, 1024);
+      const uint64_t dQmn = umma_smem_desc(sQ, kBox, 1024);
+      const uint64_t dDO0 = umma_smem_desc(sDO, 16, 1024);
+      const uint64_t dDS0 = umma_smem_desc(sDS, 16, 1024);
+      const uint64_t dDSmn = umma_smem_desc(sDS, kBox, 1024);
+      auto issue_dw_s = [&](int t) -> bool {
+        if (!mbar_wait(bar(cs.do_full), t & 1, abrt)) return false;
+        if (t > 0 && !mbar_wait(bar(cs.s_free), (t - 1) & 1, abrt)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kDV / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          mma_bf16_ss(tmem + kT, desc_add(dV0, off), desc_add(dDO0, off), idesc_kk, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(cs.do_empty));
+        if (!mbar_wait(bar(cs.q_full), t & 1, abrt)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          mma_bf16_ss(tmem, desc_add(dK0, off), desc_add(dQ0, off), idesc_kk, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(cs.s_full));
+        return true;
+      };
+      bool ok = mbar_wait(bar(cs.kv_full), 0, abrt);
+      tc_fence_after();
+      if (ok && T > 0) ok = issue_dw_s(0);
+      for (int t = 0; ok && t < T; ++t) {
+        if (!(ok = mbar_wait(bar(cs.ds_full), t & 1, abrt))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)  // dK += dS^T Q  (K = queries)
+          mma_bf16_ss(tmem + 2 * kT, desc_add(dDS0, (kk >> 2) * kBox + (kk & 3) * 32),
+                      desc_add(dQmn, kk * 2048), idesc_dk, (t > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(cs.q_empty));
+        if (t + 1 < T && !(ok = issue_dw_s(t + 1))) break;
+        if (t > 0 && !(ok = mbar_wait(bar(cs.dq_free), (t - 1) & 1, abrt))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)  // dQ partial = dS K  (K = keys)
+          mma_bf16_ss(tmem + 3 * kT, desc_add(dDSmn, kk * 2048), desc_add(dKmn, kk * 2048),
+                      idesc_dq, kk > 0 ? 1u : 0u);
+        tc_commit(bar(cs.dq_full));
+        tc_commit(bar(cs.ds_empty));
+      }
+      tc_commit(bar(cs.dk_full));
+      tc_commit(bar(cs.teardown));
+      mbar_wait(bar(cs.teardown), 0, nullptr);
+    }
+  } else {
+    const int wg = (warp - 2) >> 2;      // 0, 1: query columns [64 wg, 64 wg + 64)
+    const int q4 = warp & 3;
+    const int r = 32 * q4 + lane;        // key row (and query row for the dQ readout)
+    const int key = j * kT + r;
+    const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+    const float lam = a.lambda[h];
+    const float coef = (m == 0 ? 1.f : -lam) * a.c;
+    const uint32_t ds_row = sDS + wg * kBox + r * 128;
+    bool ok = true;
+    auto dq_readout = [&](int t) -> bool {
+      bool g = mbar_wait(bar(cs.dq_full), t & 1, abrt);
+      g = __all_sync(0xffffffffu, g);
+      if (!g) return false;
+      tc_fence_after();
+      uint32_t o[2][32];
+      tmem_ld32(tmem + tl + 3 * kT + 64 * wg, o[0]);
+      tmem_ld32(tmem + tl + 3 * kT + 64 * wg + 32, o[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(cs.dq_free));
+      const int qrow = (i0 + t) * kT + r;
+      if (qrow < a.N) {
+        float* dst = a.dqacc + ((static_cast<size_t>(b) * a.N + qrow) * a.H + h) * (2 * kD) +
+                     m * kD + 64 * wg;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            red_add_v4(dst + 32 * hh + e, __uint_as_float(o[hh][e]), __uint_as_float(o[hh][e + 1]),
+                       __uint_as_float(o[hh][e + 2]), __uint_as_float(o[hh][e + 3]));
+      }
+      return true;
+    };
+    for (int t = 0; t < T; ++t) {
+      const int i = i0 + t;
+      ok = ok && mbar_wait(bar(cs.s_full), t & 1, abrt);
+      ok = ok && mbar_wait(bar(cs.q_full), t & 1, abrt);  // b and delta of this tile
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[2][32], wv[2][32];
+      tmem_ld32(tmem + tl + 64 * wg, sv[0]);
+      tmem_ld32(tmem + tl + 64 * wg + 32, sv[1]);
+      tmem_ld32(tmem + tl + kT + 64 * wg, wv[0]);
+      tmem_ld32(tmem + tl + kT + 64 * wg + 32, wv[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(cs.s_free));
+      uint32_t pk[32];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float dsv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = 64 * wg + 32 * hh + e + u;
+            const int qq = i * kT + col;
+            const bool valid = key < a.N && qq < a.N && (!a.causal || qq >= key);
+            const float p = ex2_approx(fmaf(__uint_as_float(sv[hh][e + u]), a.c_log2, -bd[col]));
+            dsv[u] = valid ? p * (__uint_as_float(wv[hh][e + u]) - bd[kT + col]) * coef : 0.f;
+          }
+          pk[16 * hh + (e >> 1)] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+      }
+      if (t > 0) {
+        ok = mbar_wait(bar(cs.ds_empty), (t - 1) & 1, abrt);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(ds_row + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                     pk[4 * u + 3]);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(cs.ds_full));
+      if (t > 0 && !(ok = dq_readout(t - 1))) break;
+    }
+    if (ok && T > 0) ok = dq_readout(T - 1);
+    if (ok) {
+      ok = mbar_wait(bar(cs.dk_full), 0, abrt);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      uint32_t o[2][32];
+      tmem_ld32(tmem + tl + 2 * kT + 64 * wg, o[0]);
+      tmem_ld32(tmem + tl + 2 * kT + 64 * wg + 32, o[1]);
+      tmem_wait_ld();
+      if (key < a.N) {
+        __nv_bfloat16* dst = a.dk + ((static_cast<size_t>(b) * a.N + key) * a.H + h) * (2 * kD) +
+                             m * kD + 64 * wg;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint4 pkt;
+            pkt.x = pack_bf16x2(__uint_as_float(o[hh][8 * g]), __uint_as_float(o[hh][8 * g + 1]));
+            pkt.y = pack_bf16x2(__uint_as_float(o[hh][8 * g + 2]), __uint_as_float(o[hh][8 * g + 3]));
+            pkt.z = pack_bf16x2(__uint_as_float(o[hh][8 * g + 4]), __uint_as_float(o[hh][8 * g + 5]));
+            pkt.w = pack_bf16x2(__uint_as_float(o[hh][8 * g + 6]), __uint_as_float(o[hh][8 * g + 7]));
+            *reinterpret_cast<uint4*>(dst + 32 * hh + 8 * g) = pkt;
+          }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// =============================================================================================
+// bwd_dv_kernel: one CTA per (key tile j, b, h); key-major. Warps 0 (TMA), 1 (MMA, TMEM), 2-9:
+// two warpgroups, thread r = key row, query columns [64 wg, 64 wg + 64).
+// TMEM: S1^T cols 0-127, S2^T 128-255, dV 256-511. Shared memory: K1_j, K2_j (64 KB) stay;
+// Q1_i | Q2_i (64 KB, with b1, b2) and dO_i (64 KB) one slot each; W^T tile 32 KB.
+// MMA order per inner tile: S_{t+1} (as soon as the Q slot refills) before dV_t.
+// =============================================================================================
+namespace vv {
+constexpr int kThreads = 320;
+constexpr int kKOff = 0;                    // K1 (2 boxes) then K2 (2 boxes)
+constexpr int kQOff = kKOff + 4 * kBox;     // Q1 then Q2
+constexpr int kDOOff = kQOff + 4 * kBox;
+constexpr int kWOff = kDOOff + 4 * kBox;
+constexpr int kBOff = kWOff + 2 * kBox;     // two buffers of b1[128], b2[128]
+constexpr int kCtrlOff = kBOff + 2 * 2 * kT * 4;
+struct Ctrl {
+  uint64_t kv_full, q_full, q_empty, do_full, do_empty, s_full, s_free, w_full, w_empty, dv_full,
+      teardown, b_empty[2];
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+constexpr int kDynSmem = kCtrlOff + static_cast<int>(sizeof(Ctrl));
+}  // namespace vv
+
+__global__ void __launch_bounds__(vv::kThreads, 1)
+    bwd_dv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_do, const Args a) {
+  using namespace vv;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Ctrl& cs = *reinterpret_cast<Ctrl*>(smem + kCtrlOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sK = smem_u32(smem + kKOff), sQ = smem_u32(smem + kQOff);
+  const uint32_t sDO = smem_u32(smem + kDOOff), sW = smem_u32(smem + kWOff);
+  const uint32_t sB = smem_u32(smem + kBOff);
+  const float* bbase = reinterpret_cast<const float*>(smem + kBOff);
+  auto bar = [](uint64_t& x) { return smem_u32(&x); };
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) flag_device_error(DEV_TIMEOUT);
+    return;
+  }
+
+  int bh, j;
+  grouped_item(static_cast<int>(blockIdx.x), a.B * a.H, a.n_t, a.grp_dv, bh, j);
+  const int b = bh / a.H, h = bh % a.H;
+  const int i0 = a.causal ? j : 0;
+  const int T = a.n_t - i0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(cs.kv_full), 1);
+    mbar_init(bar(cs.q_full), 1);
+    mbar_init(bar(cs.q_empty), 1);
+    mbar_init(bar(cs.do_full), 1);
+    mbar_init(bar(cs.do_empty), 1);
+    mbar_init(bar(cs.s_full), 1);
+    mbar_init(bar(cs.s_free), 256);
+    mbar_init(bar(cs.w_full), 256);
+    mbar_init(bar(cs.w_empty), 1);
+    mbar_init(bar(cs.dv_full), 1);
+    mbar_init(bar(cs.teardown), 1);
+    mbar_init(bar(cs.b_empty[0]), 256);
+    mbar_init(bar(cs.b_empty[1]), 256);
+    cs.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&cs.tmem_slot), 512);
+    tmem_relinquish();
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = cs.tmem_slot;
+  volatile int* abrt = &cs.abort_flag;
+  const size_t st_base = static_cast<size_t>(b * a.H + h) * 2 * a.Npad;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_do);
+      mbar_arrive_expect_tx(bar(cs.kv_full), 4 * kBox);
+      for (int c = 0; c < 4; ++c)
+        tma_load_4d(sK + c * kBox, &tm_k, bar(cs.kv_full), 64 * c, h, j * kT, b);
+      bool ok = true;
+      int t = 0;
+      for (; t < T && ok; ++t) {
+        const int i = i0 + t;
+        if (!(ok = mbar_wait(bar(cs.q_empty), (t & 1) ^ 1, abrt))) break;
+        if (!(ok = mbar_wait(bar(cs.b_empty[t & 1]), ((t >> 1) & 1) ^ 1, abrt))) break;
+        mbar_arrive_expect_tx(bar(cs.q_full), 4 * kBox + 2 * kT * 4);
+        for (int c = 0; c < 4; ++c)
+          tma_load_4d(sQ + c * kBox, &tm_q, bar(cs.q_full), 64 * c, h, i * kT, b);
+        const uint32_t sb = sB + (t & 1) * 2 * kT * 4;
+        bulk_load(sb, a.stats + st_base + static_cast<size_t>(i) * kT, kT * 4, bar(cs.q_full));
+        bulk_load(sb + kT * 4, a.stats + st_base + a.Npad + static_cast<size_t>(i) * kT, kT * 4,
+                  bar(cs.q_full));
+        if (!(ok = mbar_wait(bar(cs.do_empty), (t & 1) ^ 1, abrt))) break;
+        mbar_arrive_expect_tx(bar(cs.do_full), 4 * kBox);
+        for (int c = 0; c < 4; ++c)
+          tma_load_4d(sDO + c * kBox, &tm_do, bar(cs.do_full), 64 * c, h, i * kT, b);
+      }
+      mbar_wait(bar(cs.kv_full), 0, nullptr);
+      if (t > 0) {
+        mbar_wait(bar(cs.q_full), (t - 1) & 1, nullptr);
+        mbar_wait(bar(cs.do_full), (t - 1) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = umma_idesc_bf16(kT, kT, 0, 0);
+      constexpr uint32_t idesc_v = umma_idesc_bf16(kT, kDV, 0, 1);
+      const uint64_t dK0 = umma_smem_desc(sK, 16, 1024);
+      const uint64_t dQ0 = umma_smem_desc(sQ, 16, 1024);
+      const uint64_t dDOmn = umma_smem_desc(sDO, kBox, 1024);
+      const uint64_t dW0 = umma_smem_desc(sW, 16, 1024);
+      auto issue_s = [&](int t) -> bool {
+        if (!mbar_wait(bar(cs.q_full), t & 1, abrt)) return false;
+        if (t > 0 && !mbar_wait(bar(cs.s_free), (t - 1) & 1, abrt)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int mp = 0; mp < 2; ++mp)
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = mp * 2 * kBox + (kk >> 2) * kBox + (kk & 3) * 32;
+            mma_bf16_ss(tmem + mp * kT, desc_add(dK0, off), desc_add(dQ0, off), idesc_s,
+                        kk > 0 ? 1u : 0u);
+          }
+        tc_commit(bar(cs.q_empty));
+        tc_commit(bar(cs.s_full));
+        return true;
+      };
+      bool ok = mbar_wait(bar(cs.kv_full), 0, abrt);
+      tc_fence_after();
+      if (ok && T > 0) ok = issue_s(0);
+      for (int t = 0; ok && t < T; ++t) {
+        if (t + 1 < T && !(ok = issue_s(t + 1))) break;
+        if (!(ok = mbar_wait(bar(cs.w_full), t & 1, abrt))) break;
+        if (!(ok = mbar_wait(bar(cs.do_full), t & 1, abrt))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)  // dV += W^T dO  (K = queries)
+          mma_bf16_ss(tmem + 2 * kT, desc_add(dW0, (kk >> 2) * kBox + (kk & 3) * 32),
+                      desc_add(dDOmn, kk * 2048), idesc_v, (t > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(cs.w_empty));
+        tc_commit(bar(cs.do_empty));
+      }
+      tc_commit(bar(cs.dv_full));
+      tc_commit(bar(cs.teardown));
+      mbar_wait(bar(cs.teardown), 0, nullptr);
+    }
+  } else {
+    const int wg = (warp - 2) >> 2;
+    const int q4 = warp & 3;
+    const int r = 32 * q4 + lane;
+    const int key = j * kT + r;
+    const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+    const float lam = a.lambda[h];
+    const uint32_t w_row = sW + wg * kBox + r * 128;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int i = i0 + t;
+      ok = ok && mbar_wait(bar(cs.s_full), t & 1, abrt);
+      ok = ok && mbar_wait(bar(cs.q_full), t & 1, abrt);  // b1, b2 of this tile
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s1[2][32], s2[2][32];
+      tmem_ld32(tmem + tl + 64 * wg, s1[0]);
+      tmem_ld32(tmem + tl + 64 * wg + 32, s1[1]);
+      tmem_ld32(tmem + tl + kT + 64 * wg, s2[0]);
+      tmem_ld32(tmem + tl + kT + 64 * wg + 32, s2[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(cs.s_free));
+      const float* bb = bbase + (t & 1) * 2 * kT;
+      uint32_t pk[32];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float wv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = 64 * wg + 32 * hh + e + u;
+            const int qq = i * kT + col;
+            const bool valid = key < a.N && qq < a.N && (!a.causal || qq >= key);
+            const float p1 = ex2_approx(fmaf(__uint_as_float(s1[hh][e + u]), a.c_log2, -bb[col]));
+            const float p2 = ex2_approx(fmaf(__uint_as_float(s2[hh][e + u]), a.c_log2, -bb[kT + col]));
+            wv[u] = valid ? fmaf(-lam, p2, p1) : 0.f;
+          }
+          pk[16 * hh + (e >> 1)] = pack_bf16x2(wv[0], wv[1]);
+        }
+      }
+      mbar_arrive(bar(cs.b_empty[t & 1]));  // this buffer of b1, b2 may be refilled (tile t + 2)
+      if (t > 0) {
+        ok = mbar_wait(bar(cs.w_empty), (t - 1) & 1, abrt);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(w_row + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                     pk[4 * u + 3]);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(cs.w_full));
+    }
+    if (ok) {
+      ok = mbar_wait(bar(cs.dv_full), 0, abrt);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + tl + 2 * kT + 128 * wg + 32 * c, o);
+        tmem_wait_ld();
+        if (key < a.N) {
+          __nv_bfloat16* dst = a.dv + ((static_cast<size_t>(b) * a.N + key) * a.H + h) * kDV +
+                               128 * wg + 32 * c;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint4 pkt;
+            pkt.x = pack_bf16x2(__uint_as_float(o[8 * g]), __uint_as_float(o[8 * g + 1]));
+            pkt.y = pack_bf16x2(__uint_as_float(o[8 * g + 2]), __uint_as_float(o[8 * g + 3]));
+            pkt.z = pack_bf16x2(__uint_as_float(o[8 * g + 4]), __uint_as_float(o[8 * g + 5]));
+            pkt.w = pack_bf16x2(__uint_as_float(o[8 * g + 6]), __uint_as_float(o[8 * g + 7]));
+            *reinterpret_cast<uint4*>(dst + 8 * g) = pkt;
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// =============================================================================================
+// bwd_finish_kernel: blocks [0, nq) convert dQ (8 elements per thread); block nq sums dlam and
+// the norm-weight partials in a fixed order.
+// =============================================================================================
+__global__ void __launch_bounds__(256) bwd_finish_kernel(const Args a, long long n8, int nq) {
+  if (static_cast<int>(blockIdx.x) < nq) {
+    for (long long e = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; e < n8;
+         e += static_cast<long long>(nq) * 256) {
+      const float4* src = reinterpret_cast<const float4*>(a.dqacc) + 2 * e;
+      const float4 x = src[0], y = src[1];
+      uint4 pk;
+      pk.x = pack_bf16x2(x.x, x.y);
+      pk.y = pack_bf16x2(x.z, x.w);
+      pk.z = pack_bf16x2(y.x, y.y);
+      pk.w = pack_bf16x2(y.z, y.w);
+      reinterpret_cast<uint4*>(a.dq)[e] = pk;
+    }
+    return;
+  }
+  for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
+    float s = 0.f;
+    for (int b = 0; b < a.B; ++b)
+      for (int t = 0; t < a.n_t; ++t) s += a.dl_part[(static_cast<size_t>(b) * a.H + h) * a.n_t + t];
+    a.dlambda[h] = s;
+  }
+  if (a.dnorm_w) {
+    for (int c = threadIdx.x; c < kDV; c += blockDim.x) {
+      float s = 0.f;
+      for (int k = 0; k < a.pre_blocks; ++k) s += a.dw_part[static_cast<size_t>(k) * kDV + c];
+      a.dnorm_w[c] = a.norm ? s : 0.f;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult res;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &res) == cudaSuccess &&
+        res == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 4-D bf16 map over [B, N, H, cols], box 64 x 1 x rows x 1, 128-byte swizzle, zero fill.
+static bool make_map(CUtensorMap* m, const void* base, int cols, int H, int N, int B, int rows,
+                     char* err, size_t err_len) {
+  auto fn = encode_fn();
+  if (!fn) {
+    snprintf(err, err_len, "cuTensorMapEncodeTiled entry point unavailable");
+    return false;
+  }
+  cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * H * 2,
+                           (cuuint64_t)cols * H * 2 * (cuuint64_t)N};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(err, err_len, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  size_t dO, delta, dqacc, dw_part, dl_part, total;
+  int pre_blocks;
+};
+static WsLayout ws_layout(int B, int N, int H) {
+  WsLayout w;
+  const int Npad = (N + kT - 1) / kT * kT;
+  const int n_t = Npad / kT;
+  const long long rows = static_cast<long long>(B) * N * H;
+  long long blocks = (rows + kPreWarps - 1) / kPreWarps;
+  w.pre_blocks = static_cast<int>(blocks < 8 * 152 ? blocks : 8 * 152);
+  size_t off = 0;
+  w.dO = off;
+  off = align256(off + static_cast<size_t>(rows) * kDV * 2);
+  w.delta = off;
+  off = align256(off + static_cast<size_t>(B) * H * 2 * Npad * 4);
+  w.dqacc = off;
+  off = align256(off + static_cast<size_t>(rows) * 2 * kD * 4);
+  w.dw_part = off;
+  off = align256(off + static_cast<size_t>(w.pre_blocks) * kDV * 4);
+  w.dl_part = off;
+  off = align256(off + static_cast<size_t>(B) * H * n_t * 4);
+  w.total = off;
+  return w;
+}
+
+}  // namespace bwd
+
+size_t backward_workspace_bytes(int B, int N, int H) { return bwd::ws_layout(B, N, H).total; }
+
+cudaError_t status_backward(int* v) { return read_clear_status(v); }
+
+cudaError_t launch_backward(const BackwardArgs& x, cudaStream_t st, char* err, size_t err_len) {
+  using namespace bwd;
+  const WsLayout L = ws_layout(x.B, x.N, x.H);
+  uint8_t* ws = static_cast<uint8_t*>(x.workspace);
+  Args a{};
+  a.q = static_cast<const __nv_bfloat16*>(x.q);
+  a.k = static_cast<const __nv_bfloat16*>(x.k);
+  a.v = static_cast<const __nv_bfloat16*>(x.v);
+  a.o_pre = static_cast<const __nv_bfloat16*>(x.o_pre);
+  a.dy = static_cast<const __nv_bfloat16*>(x.dout);
+  a.stats = x.stats;
+  a.lambda = x.lambda;
+  a.norm_w = x.norm_w;
+  a.dq = static_cast<__nv_bfloat16*>(x.dq);
+  a.dk = static_cast<__nv_bfloat16*>(x.dk);
+  a.dv = static_cast<__nv_bfloat16*>(x.dv);
+  a.dlambda = x.dlambda;
+  a.dnorm_w = x.dnorm_w;
+  a.dO = reinterpret_cast<__nv_bfloat16*>(ws + L.dO);
+  a.delta = reinterpret_cast<float*>(ws + L.delta);
+  a.dqacc = reinterpret_cast<float*>(ws + L.dqacc);
+  a.dw_part = reinterpret_cast<float*>(ws + L.dw_part);
+  a.dl_part = reinterpret_cast<float*>(ws + L.dl_part);
+  a.B = x.B;
+  a.N = x.N;
+  a.H = x.H;
+  a.Npad = (x.N + kT - 1) / kT * kT;
+  a.n_t = a.Npad / kT;
+  a.pre_blocks = L.pre_blocks;
+  a.eps = x.eps;
+  a.scale_out = (x.flags & 4) ? (1.f - x.lambda_init) : 1.f;
+  a.norm = (x.flags & 2) != 0;
+  a.causal = (x.flags & 1) != 0;
+  a.c = 1.f / sqrtf(static_cast<float>(kD));
+  a.c_log2 = kLog2e * a.c;
+  {
+    // bytes each unit keeps re-reading (or, for dQ, accumulating) while its tiles run; a group
+    // keeps about 48 MB of them in the 126 MB L2
+    const double n = static_cast<double>(x.N);
+    auto grp = [&](double unit_bytes, int n_units) {
+      long long g = static_cast<long long>(48.0 * 1024 * 1024 / (unit_bytes > 1 ? unit_bytes : 1));
+      return static_cast<int>(g < 1 ? 1 : (g > n_units ? n_units : g));
+    };
+    a.grp_delta = grp(n * (kD + kDV) * 2, x.B * x.H);                 // K2, V
+    a.grp_dkdq = 2 * grp(2 * n * (kD * 2 + kDV * 2 + kD * 4), x.B * x.H);  // Q_m, dO, dQ_m; x2 maps
+    a.grp_dv = grp(n * (2 * kD + kDV) * 2, x.B * x.H);               // Q1|Q2, dO
+    if (a.grp_dkdq > 2 * x.B * x.H) a.grp_dkdq = 2 * x.B * x.H;
+  }
+
+  CUtensorMap mq, mk, mv, mvh, mdo;
+  if (!make_map(&mq, x.q, 2 * kD, x.H, x.N, x.B, kT, err, err_len) ||
+      !make_map(&mk, x.k, 2 * kD, x.H, x.N, x.B, kT, err, err_len) ||
+      !make_map(&mv, x.v, kDV, x.H, x.N, x.B, kT, err, err_len) ||
+      !make_map(&mvh, x.v, kDV, x.H, x.N, x.B, kT / 2, err, err_len) ||
+      !make_map(&mdo, a.dO, kDV, x.H, x.N, x.B, kT, err, err_len))
+    return cudaErrorInvalidValue;
+
+  bwd_pre_kernel<<<L.pre_blocks, kPreWarps * 32, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  const int items = a.n_t * x.B * x.H;
+  e = cudaFuncSetAttribute(bwd_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dl::kDynSmem);
+  if (e != cudaSuccess) return e;
+  bwd_delta_kernel<<<items, dl::kThreads, dl::kDynSmem, st>>>(mq, mk, mvh, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  e = cudaFuncSetAttribute(bwd_dkdq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kq::kDynSmem);
+  if (e != cudaSuccess) return e;
+  bwd_dkdq_kernel<<<2 * items, kq::kThreads, kq::kDynSmem, st>>>(mq, mk, mv, mdo, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  e = cudaFuncSetAttribute(bwd_dv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, vv::kDynSmem);
+  if (e != cudaSuccess) return e;
+  bwd_dv_kernel<<<items, vv::kThreads, vv::kDynSmem, st>>>(mq, mk, mdo, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  const long long n8 = static_cast<long long>(x.B) * x.N * x.H * 2 * kD / 8;
+  long long nq = (n8 + 255) / 256;
+  if (nq > 4 * 152) nq = 4 * 152;
+  bwd_finish_kernel<<<static_cast<int>(nq) + 1, 256, 0, st>>>(a, n8, static_cast<int>(nq));
+  return cudaGetLastError();
+}
+
+}  // namespace da

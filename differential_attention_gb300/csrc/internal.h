@@ -34,6 +34,11 @@ struct Problem {
   float lambda_init;
   int flags;
   float scale;             // 1 / sqrt(dqk)
+  // forward for training (V1, exact path): per row and map the base-2 log-sum-exp of the scaled
+  // scores, [B, H, 2, n_pad]; and the head output before the norm and scale, [B, N, H, dv]
+  float* stats;
+  void* o_pre;
+  int n_pad;
 };
 
 __host__ __device__ inline int q_head_of(const Problem& p, int u, int r) {
@@ -92,6 +97,30 @@ cudaError_t launch_v2_decode(const V2DecodeArgs& a, cudaStream_t s);  // CUDA co
 cudaError_t launch_v2_decode_tc(const V2DecodeArgs& a, cudaStream_t s, char* err, size_t err_len);
 cudaError_t launch_v2_combine(const V2DecodeArgs& a, int splits, cudaStream_t s);
 cudaError_t status_v2_decode_tc(int* v);
+
+// Backward of the V1 prefill (d = 128, dv = 256, bf16).
+struct BackwardArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o_pre;
+  const float* stats;
+  const void* dout;
+  const float* lambda;
+  float lambda_init;
+  const float* norm_w;
+  float eps;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dlambda;
+  float* dnorm_w;
+  int B, N, H, flags;
+  void* workspace;
+};
+size_t backward_workspace_bytes(int B, int N, int H);
+cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s, char* err, size_t err_len);
+cudaError_t status_backward(int* v);
 
 // Decode whose split partials live in a fixed device array of this size (no workspace argument).
 constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(16) << 20;

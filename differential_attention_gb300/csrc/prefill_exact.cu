@@ -510,7 +510,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             *reinterpret_cast<uint4*>(out + CW * c + 8 * g) = pkt;
           }
+          if (P.o_pre) {  // training: the head output before the norm and scale
+            __nv_bfloat16* op = static_cast<__nv_bfloat16*>(P.o_pre) +
+                                ((static_cast<size_t>(b) * P.N + row) * P.units + u) * DV + c0;
+#pragma unroll
+            for (int g = 0; g < CW / 8; ++g) {
+              uint4 pkt;
+              uint32_t* pw = reinterpret_cast<uint32_t*>(&pkt);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                pw[i] = pack_bf16x2(__uint_as_float(o[8 * g + 2 * i]),
+                                    __uint_as_float(o[8 * g + 2 * i + 1]));
+              *reinterpret_cast<uint4*>(op + CW * c + 8 * g) = pkt;
+            }
+          }
         }
+      }
+      if (P.stats && wg == 0 && row < P.N) {
+        float* st = P.stats + (static_cast<size_t>(b) * P.units + u) * 2 * P.n_pad + row;
+        st[0] = -bias[0];
+        st[P.n_pad] = -bias[1];
       }
     }
   }

@@ -223,6 +223,45 @@ DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const vo
                                     int Lmax, int Hq, int Hkv, int d, int flags, int dtype,
                                     void* workspace, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Training: forward that keeps what the backward needs, and the backward of the V1 prefill
+ * (page "Differential Transformer: softmax can't say zero, so it subtracts", section "The
+ * mechanism, exactly" defines the forward; the gradients are its chain rule).
+ *
+ * diffattn_fwd_train: diffattn_fwd (tensor-core exact path) plus two outputs:
+ *   o_pre : device bf16 [B, N, H, dv], the head output (A1 - lambda A2) V before the norm/scale
+ *   stats : device fp32 [B, H, 2, Npad], Npad = N rounded up to a multiple of 128: for each row
+ *           and map m, b_m = log2 sum_j 2^(log2(e) s_ij / sqrt(d)) over the visible keys, so that
+ *           A_m = 2^(log2(e) s / sqrt(d) - b_m). Entries past N are not written.
+ *   flags : DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE
+ * Supported: dtype DIFFATTN_BF16, d = 128, dv = 256.
+ *
+ * diffattn_bwd: given dout = dL/dout [B, N, H, dv] (bf16) and the tensors of a diffattn_fwd_train
+ * call with the same arguments, writes
+ *   dq, dk : device bf16 [B, N, H, 2d] = [dQ1 | dQ2], [dK1 | dK2]
+ *   dv     : device bf16 [B, N, H, dv]
+ *   dlambda: device fp32 [H], dL/dlambda[h] (summed over batch and rows; overwritten)
+ *   dnorm_weight : device fp32 [dv] or NULL, dL/dw of the norm weight (summed over every row and
+ *           head; zeros without DIFFATTN_NORM)
+ *   workspace, ws_bytes : at least diffattn_bwd_workspace_size() bytes, 256-byte aligned, not
+ *           shared with a call that can run at the same time (contents need not be initialised).
+ * lambda_init, norm_weight, eps and flags must be those of the forward. The result is
+ * deterministic except for the order of the fp32 additions that build dq.
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_fwd_train(const void* q, const void* k, const void* v, void* out,
+                                    void* o_pre, float* stats, const float* lambda,
+                                    float lambda_init, const float* norm_weight, float eps, int B,
+                                    int N, int H, int d, int dv, int flags, int dtype,
+                                    void* stream);
+DIFFATTN_API int diffattn_bwd_workspace_size(int B, int N, int H, int d, int dv, size_t* bytes);
+DIFFATTN_API int diffattn_bwd(const void* q, const void* k, const void* v, const void* o_pre,
+                              const float* stats, const void* dout, const float* lambda,
+                              float lambda_init, const float* norm_weight, float eps, void* dq,
+                              void* dk, void* dv, float* dlambda, float* dnorm_weight, int B,
+                              int N, int H, int d, int dv_width, int flags, int dtype,
+                              void* workspace, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

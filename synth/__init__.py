@@ -8,6 +8,7 @@ from .workloads import (  # noqa: F401
     WORKLOADS,
     bf16_round,
     make_decode_inputs,
+    make_dout,
     make_lambda_vectors,
     make_prefill_inputs,
     make_tiny_inputs,

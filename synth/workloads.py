@@ -209,3 +209,8 @@ def make_v2_decode_inputs(B: int, L: int, Hq: int, Hkv: int, d: int, seed: int, 
         seqlens = torch.full((B,), L, dtype=torch.int32)
     return V2DecodeInputs(q=q, k_cache=k_cache, v_cache=v_cache, seqlens=seqlens.to(device),
                           lam_logit=lam_logit.to(device))
+
+
+def make_dout(B: int, N: int, H: int, dv: int, seed: int, device="cpu", dtype=torch.bfloat16):
+    """Upstream gradient dL/dout for the backward: N(0, 1) per element."""
+    return _randn((B, N, H, dv), _gen(seed, device), device).to(dtype)

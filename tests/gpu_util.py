@@ -36,3 +36,29 @@ def assert_bf16(got, want, rel_tol=BF16_REL_L2, abs_tol=BF16_MAX_ABS):
     max_abs, rel = errors(got, want)
     assert rel <= rel_tol and max_abs <= abs_tol, f"rel L2 {rel:.3e} (<= {rel_tol}), max abs {max_abs:.3e} (<= {abs_tol})"
     return max_abs, rel
+
+
+# Gradients (backward of the bf16 prefill): P, dS, W and dO are rounded to bf16 before each
+# product (relative 2^-9 each) and every product accumulates in fp32, so a gradient carries a few
+# bf16 roundings of relative error: relative L2 <= 2e-2 per tensor, and no element off by more
+# than 5e-2 of the tensor's largest magnitude.
+GRAD_REL_L2 = 2e-2
+GRAD_MAX_REL = 5e-2
+
+
+# Where the exact gradient is identically zero (one visible key: the softmax is constant), the
+# kernel's dW - delta differs from 0 by the bf16 rounding of dO, so the bar is absolute.
+GRAD_ZERO_ABS = 1e-3
+
+
+def assert_grad(got, want, rel_tol=GRAD_REL_L2, max_rel=GRAD_MAX_REL, name=""):
+    g, w = to64(got), to64(want)
+    max_abs, rel = errors(g, w)
+    scale = float(np.max(np.abs(w))) if w.size else 0.0
+    if scale == 0.0:
+        assert max_abs <= GRAD_ZERO_ABS, f"{name}: exact gradient is 0, max abs {max_abs:.3e}"
+        return max_abs, rel
+    assert rel <= rel_tol and max_abs <= max_rel * max(scale, 1e-30), (
+        f"{name}: rel L2 {rel:.3e} (<= {rel_tol}), max abs {max_abs:.3e} "
+        f"(<= {max_rel} x {scale:.3e})")
+    return max_abs, rel

@@ -11,9 +11,9 @@ import torch
 
 import differential_attention_gb300 as da
 from oracle import diffattn_ref as ref
-from synth import (make_decode_inputs, make_lambda_vectors, make_prefill_inputs, make_v2_decode_inputs,
-                   make_v2_inputs)
-from tests.gpu_util import assert_bf16
+from synth import (make_decode_inputs, make_dout, make_lambda_vectors, make_prefill_inputs,
+                   make_v2_decode_inputs, make_v2_inputs)
+from tests.gpu_util import assert_bf16, assert_grad
 
 pytestmark = pytest.mark.gpu
 
@@ -114,4 +114,30 @@ def test_v2_decode_32k_full():
                                   inp.lam_logit[sample].cpu())
     assert_bf16(out[sample], want)
     del inp
+    torch.cuda.empty_cache()
+
+
+def test_bwd_3b_full():
+    """Backward at B4 N4096 H12 (the bench's training launch): every gradient of head 5 in all
+    four sequences (so dlambda[5] is complete) and of head 0 in sequence 1."""
+    B, N, H = 4, 4096, 12
+    inp = make_prefill_inputs(B, N, H, 128, 256, seed=6000, layer=12, device=DEV)
+    dy = make_dout(B, N, H, 256, seed=6007, device=DEV)
+    lam = torch.linspace(0.5, 0.9, H, dtype=torch.float32, device=DEV)
+    li = da.diffattn_lambda_init(12)
+    _, o_pre, stats = da.diffattn_fwd_train(inp.q, inp.k, inp.v, lam, li)
+    g = da.diffattn_bwd(inp.q, inp.k, inp.v, o_pre, stats, dy, lam, li)
+    da.diffattn_device_status()
+    lam_h = lam.cpu().numpy()
+    dl5 = 0.0
+    for b, h in [(0, 5), (1, 5), (2, 5), (3, 5), (1, 0)]:
+        sl = lambda t: t[b:b + 1, :, h:h + 1].cpu()
+        want = ref.diffattn_bwd(sl(inp.q), sl(inp.k), sl(inp.v), lam_h[h:h + 1], ref.lambda_init(12),
+                                sl(dy))
+        for name in ("dq", "dk", "dv"):
+            assert_grad(g[name][b:b + 1, :, h:h + 1], want[name], name=f"{name} b{b} h{h}")
+        if h == 5:
+            dl5 += want["dlam"][0]
+    assert_grad(g["dlam"][5:6], np.array([dl5]), rel_tol=1e-2, name="dlam[5]")
+    del inp, dy, o_pre, stats, g
     torch.cuda.empty_cache()
