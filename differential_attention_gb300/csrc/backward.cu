@@ -16,9 +16,9 @@
 //                     zeroes the fp32 dQ accumulator.
 //   bwd_delta_kernel  tcgen05, query-major: O2 = A2 V -> delta_2 = dO . O2,
 //                     delta_1 = D + lam delta_2 (because O = O1 - lam O2), and -sum delta_2 per CTA.
-//   bwd_dkdq_kernel   tcgen05, key-major, one map per CTA: S^T = K Q^T, dW^T = V dO^T,
-//                     dS^T in shared memory, dK += dS^T Q (TMEM), dQ partial = dS K (TMEM) added
-//                     to the fp32 accumulator with red.global.add.v4.f32.
+//   bwd_dkdq_kernel   tcgen05, key-major, one map per CTA: S = Q K^T, dW = dO V^T per inner
+//                     tile, dS in shared memory, dK += dS^T Q (TMEM), dQ partial = dS K (TMEM)
+//                     added to the fp32 accumulator with TMA tensor reductions.
 //   bwd_dv_kernel     tcgen05, key-major: S1^T, S2^T -> W^T in shared memory, dV += W^T dO.
 //   bwd_finish_kernel dQ fp32 -> bf16; dlam and norm-weight sums (fixed order: deterministic).
 // TMEM is 512 columns per SM; each tensor-core kernel fills it exactly:
@@ -56,6 +56,20 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                "f"(c), "f"(d)
                : "memory");
 }
+// Add a shared-memory tile into global memory through a tensor map (fp32 add in L2).
+__device__ __forceinline__ void tma_reduce_add_4d(const void* tmap, uint32_t smem_src, int c0,
+                                                  int c1, int c2, int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred) {
   uint32_t r;
   asm volatile(
@@ -73,6 +87,11 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
     f[2 * i] = __uint_as_float(w[i] << 16);
     f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
   }
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -465,18 +484,20 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
 }
 
 // =============================================================================================
-// bwd_dkdq_kernel: one CTA per (key tile j, b, h, map m); key-major. Warps 0 (TMA), 1 (MMA,
-// TMEM), 2-9: two warpgroups; thread r of warpgroup w owns key row r and query columns
-// [64 w, 64 w + 64) of each inner tile, and for the dQ readout query row r, d-columns
-// [64 w, 64 w + 64).
-// TMEM: S^T cols 0-127, dW^T 128-255, dK 256-383, dQ partial 384-511.
+// bwd_dkdq_kernel: one CTA per (key tile j, b, h, map m); key-major over the CTAs, but each
+// inner tile is computed query-major: S = Q K^T and dW = dO V^T have the 128 queries on the TMEM
+// lanes, so a query's b and delta are per-thread constants. Warps 0 (TMA), 1 (MMA, TMEM),
+// 2-9: two warpgroups, thread r = query row r, key columns [64 w, 64 w + 64); 10-13: the dQ
+// warpgroup (thread r = query row r, all 128 d-columns), which stages each tile's dQ in the dO
+// slot and adds it into the fp32 accumulator with TMA tensor reductions.
+// TMEM: S cols 0-127, dW 128-255, dK 256-383, dQ partial 384-511.
 // Shared memory: K_m,j (32 KB) and V_j (64 KB) stay; Q_m,i (32 KB + its b and delta rows) and
-// dO_i (64 KB) have one slot each; the dS^T tile (32 KB) is read K-major for dK and MN-major
-// for dQ. MMA issue order per inner tile t (keeps the Q slot, freed by dK_t, off the critical
-// path): dK_t | dW^T_{t+1} | S^T_{t+1} | dQ_t.
+// dO_i (64 KB) have one slot each; the dS tile (32 KB, [query][key]) is read MN-major as dS^T
+// for dK and K-major for dQ. MMA issue order per inner tile t (keeps the Q slot, freed by dK_t,
+// off the critical path): dK_t | dW_{t+1} | S_{t+1} | dQ_t.
 // =============================================================================================
 namespace kq {
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;  // TMA, MMA, 8 dS warps, 4 dQ warps
 constexpr int kKOff = 0;
 constexpr int kVOff = kKOff + 2 * kBox;
 constexpr int kQOff = kVOff + 4 * kBox;
@@ -497,7 +518,8 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
     bwd_dkdq_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_do, const Args a) {
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dqacc, const Args a) {
   using namespace kq;
   extern __shared__ __align__(1024) uint8_t smem[];
   Ctrl& cs = *reinterpret_cast<Ctrl*>(smem + kCtrlOff);
@@ -530,7 +552,7 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
     mbar_init(bar(cs.ds_full), 256);
     mbar_init(bar(cs.ds_empty), 1);
     mbar_init(bar(cs.dq_full), 1);
-    mbar_init(bar(cs.dq_free), 256);
+    mbar_init(bar(cs.dq_free), 128);
     mbar_init(bar(cs.dk_full), 1);
     mbar_init(bar(cs.teardown), 1);
     cs.abort_flag = 0;
@@ -584,9 +606,9 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_kk = umma_idesc_bf16(kT, kT, 0, 0);  // S^T, dW^T
-      constexpr uint32_t idesc_dk = umma_idesc_bf16(kT, kD, 0, 1);  // dS^T (K-major) x Q (MN)
-      constexpr uint32_t idesc_dq = umma_idesc_bf16(kT, kD, 1, 1);  // dS (MN) x K (MN)
+      constexpr uint32_t idesc_kk = umma_idesc_bf16(kT, kT, 0, 0);  // S, dW (queries x keys)
+      constexpr uint32_t idesc_dk = umma_idesc_bf16(kT, kD, 1, 1);  // dS^T (MN) x Q (MN)
+      constexpr uint32_t idesc_dq = umma_idesc_bf16(kT, kD, 0, 1);  // dS (K-major) x K (MN)
       const uint64_t dK0 = umma_smem_desc(sK, 16, 1024);
       const uint64_t dKmn = umma_smem_desc(sK, kBox, 1024);
       const uint64_t dV0 = umma_smem_desc(sV, 16, 1024);
@@ -602,15 +624,16 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kDV / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kT, desc_add(dV0, off), desc_add(dDO0, off), idesc_kk, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + kT, desc_add(dDO0, off), desc_add(dV0, off), idesc_kk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(bar(cs.do_empty));
+        // the dO slot next holds the staged dQ of tile t - 1; for t = 0 it is free right away
+        if (t == 0) tc_commit(bar(cs.do_empty));
         if (!mbar_wait(bar(cs.q_full), t & 1, abrt)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_bf16_ss(tmem, desc_add(dK0, off), desc_add(dQ0, off), idesc_kk, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem, desc_add(dQ0, off), desc_add(dK0, off), idesc_kk, kk > 0 ? 1u : 0u);
         }
         tc_commit(bar(cs.s_full));
         return true;
@@ -623,16 +646,16 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)  // dK += dS^T Q  (K = queries)
-          mma_bf16_ss(tmem + 2 * kT, desc_add(dDS0, (kk >> 2) * kBox + (kk & 3) * 32),
-                      desc_add(dQmn, kk * 2048), idesc_dk, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ss(tmem + 2 * kT, desc_add(dDSmn, kk * 2048), desc_add(dQmn, kk * 2048),
+                      idesc_dk, (t > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bar(cs.q_empty));
         if (t + 1 < T && !(ok = issue_dw_s(t + 1))) break;
         if (t > 0 && !(ok = mbar_wait(bar(cs.dq_free), (t - 1) & 1, abrt))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)  // dQ partial = dS K  (K = keys)
-          mma_bf16_ss(tmem + 3 * kT, desc_add(dDSmn, kk * 2048), desc_add(dKmn, kk * 2048),
-                      idesc_dq, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + 3 * kT, desc_add(dDS0, (kk >> 2) * kBox + (kk & 3) * 32),
+                      desc_add(dKmn, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
         tc_commit(bar(cs.dq_full));
         tc_commit(bar(cs.ds_empty));
       }
@@ -640,40 +663,19 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       tc_commit(bar(cs.teardown));
       mbar_wait(bar(cs.teardown), 0, nullptr);
     }
-  } else {
-    const int wg = (warp - 2) >> 2;      // 0, 1: query columns [64 wg, 64 wg + 64)
+  } else if (warp < 2 + 8) {
+    // ---- dS warpgroups: thread r = query row r of the inner tile, key columns
+    // [64 wg, 64 wg + 64); the row's b and delta are per-thread constants ----
+    const int wg = (warp - 2) >> 2;
     const int q4 = warp & 3;
-    const int r = 32 * q4 + lane;        // key row (and query row for the dQ readout)
-    const int key = j * kT + r;
+    const int r = 32 * q4 + lane;
+    const int key = j * kT + r;  // for the dK readout (TMEM lane = key row there)
     const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
     const float lam = a.lambda[h];
     const float coef = (m == 0 ? 1.f : -lam) * a.c;
+    const uint64_t c2 = f2pack(a.c_log2, a.c_log2), coef2 = f2pack(coef, coef);
     const uint32_t ds_row = sDS + wg * kBox + r * 128;
     bool ok = true;
-    auto dq_readout = [&](int t) -> bool {
-      bool g = mbar_wait(bar(cs.dq_full), t & 1, abrt);
-      g = __all_sync(0xffffffffu, g);
-      if (!g) return false;
-      tc_fence_after();
-      uint32_t o[2][32];
-      tmem_ld32(tmem + tl + 3 * kT + 64 * wg, o[0]);
-      tmem_ld32(tmem + tl + 3 * kT + 64 * wg + 32, o[1]);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(cs.dq_free));
-      const int qrow = (i0 + t) * kT + r;
-      if (qrow < a.N) {
-        float* dst = a.dqacc + ((static_cast<size_t>(b) * a.N + qrow) * a.H + h) * (2 * kD) +
-                     m * kD + 64 * wg;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            red_add_v4(dst + 32 * hh + e, __uint_as_float(o[hh][e]), __uint_as_float(o[hh][e + 1]),
-                       __uint_as_float(o[hh][e + 2]), __uint_as_float(o[hh][e + 3]));
-      }
-      return true;
-    };
     for (int t = 0; t < T; ++t) {
       const int i = i0 + t;
       ok = ok && mbar_wait(bar(cs.s_full), t & 1, abrt);
@@ -681,29 +683,37 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t sv[2][32], wv[2][32];
-      tmem_ld32(tmem + tl + 64 * wg, sv[0]);
-      tmem_ld32(tmem + tl + 64 * wg + 32, sv[1]);
-      tmem_ld32(tmem + tl + kT + 64 * wg, wv[0]);
-      tmem_ld32(tmem + tl + kT + 64 * wg + 32, wv[1]);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(cs.s_free));
+      const int qq = i * kT + r;
+      const float nb = -bd[r], nd = -bd[kT + r] * coef;
+      const uint64_t nb2 = f2pack(nb, nb), nd2 = f2pack(nd, nd);
+      // masks only where the tile reaches past N or crosses the diagonal
+      const bool edge = (j + 1) * kT > a.N || (i + 1) * kT > a.N || (a.causal && i == j);
       uint32_t pk[32];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sv[32], wv[32];
+        tmem_ld32(tmem + tl + 64 * wg + 32 * hh, sv);
+        tmem_ld32(tmem + tl + kT + 64 * wg + 32 * hh, wv);
+        tmem_wait_ld();
+        if (hh == 1) {
+          tc_fence_before();
+          mbar_arrive(bar(cs.s_free));  // S and dW are in registers
+        }
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float dsv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = 64 * wg + 32 * hh + e + u;
-            const int qq = i * kT + col;
-            const bool valid = key < a.N && qq < a.N && (!a.causal || qq >= key);
-            const float p = ex2_approx(fmaf(__uint_as_float(sv[hh][e + u]), a.c_log2, -bd[col]));
-            dsv[u] = valid ? p * (__uint_as_float(wv[hh][e + u]) - bd[kT + col]) * coef : 0.f;
+          float x0, x1;
+          f2unpack(f2fma(f2pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nb2), x0, x1);
+          const uint64_t g = f2fma(f2pack(__uint_as_float(wv[e]), __uint_as_float(wv[e + 1])), coef2, nd2);
+          float y0, y1;
+          f2unpack(f2mul(f2pack(ex2_approx(x0), ex2_approx(x1)), g), y0, y1);
+          if (edge) {
+            const int kk0 = j * kT + 64 * wg + 32 * hh + e;
+            const bool v0 = kk0 < a.N && qq < a.N && (!a.causal || qq >= kk0);
+            const bool v1 = kk0 + 1 < a.N && qq < a.N && (!a.causal || qq >= kk0 + 1);
+            y0 = v0 ? y0 : 0.f;
+            y1 = v1 ? y1 : 0.f;
           }
-          pk[16 * hh + (e >> 1)] = pack_bf16x2(dsv[0], dsv[1]);
+          pk[16 * hh + (e >> 1)] = pack_bf16x2(y0, y1);
         }
       }
       if (t > 0) {
@@ -717,9 +727,7 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
                      pk[4 * u + 3]);
       fence_proxy_async_smem();
       mbar_arrive(bar(cs.ds_full));
-      if (t > 0 && !(ok = dq_readout(t - 1))) break;
     }
-    if (ok && T > 0) ok = dq_readout(T - 1);
     if (ok) {
       ok = mbar_wait(bar(cs.dk_full), 0, abrt);
       ok = __all_sync(0xffffffffu, ok);
@@ -746,6 +754,50 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
           }
       }
     }
+  } else {
+    // ---- dQ warpgroup: thread r = query row r of the inner tile. Each tile's dQ partial goes
+    // from TMEM to the dO slot (free once the next tile's dW has read it), four 32-column
+    // 128B-swizzled boxes, and is added into the fp32 accumulator by TMA tensor reductions. The
+    // slot is handed back to the producer (do_empty) once the reductions have read it. ----
+    const int q4 = warp & 3;
+    const int r = 32 * q4 + lane;
+    const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      bool g = ok && mbar_wait(bar(cs.dq_full), t & 1, abrt);
+      g = __all_sync(0xffffffffu, g);
+      // thread 0 reaches this barrier only after the previous tile's reductions have read the
+      // slot (for the last tile nothing else orders the staging after them)
+      if (!(ok = bar_and(2, 128, g))) break;
+      {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + tl + 3 * kT + 32 * c, o);
+          tmem_wait_ld();
+          if (c == 3) {
+            tc_fence_before();
+            mbar_arrive(bar(cs.dq_free));
+          }
+          const uint32_t row = sDO + c * kBox + r * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            st_shared_v4(row + ((u ^ (r & 7)) << 4), o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+      }
+      if (!(ok = bar_and(2, 128, true))) break;
+      if (r == 0) {
+        const int i = i0 + t;
+        for (int c = 0; c < 4; ++c)
+          tma_reduce_add_4d(&tm_dqacc, sDO + c * kBox, m * kD + 32 * c, h, i * kT, b);
+        bulk_commit();
+        bulk_wait_read();
+        mbar_arrive(bar(cs.do_empty));  // the slot may take the next dO tile
+      }
+    }
+    if (r == 0) bulk_wait_all();
   }
 
   __syncwarp();
@@ -1075,6 +1127,30 @@ static bool make_map(CUtensorMap* m, const void* base, int cols, int H, int N, i
   return true;
 }
 
+// 4-D fp32 map over the dQ accumulator [B, N, H, 2d], box 32 x 1 x 128 x 1 (128-byte rows),
+// 128-byte swizzle: the target of the dK/dQ kernel's tensor reductions.
+static bool make_map_f32(CUtensorMap* m, void* base, int cols, int H, int N, int B, char* err,
+                         size_t err_len) {
+  auto fn = encode_fn();
+  if (!fn) {
+    snprintf(err, err_len, "cuTensorMapEncodeTiled entry point unavailable");
+    return false;
+  }
+  cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)cols * 4, (cuuint64_t)cols * H * 4,
+                           (cuuint64_t)cols * H * 4 * (cuuint64_t)N};
+  cuuint32_t box[4] = {32, 1, (cuuint32_t)kT, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(err, err_len, "cuTensorMapEncodeTiled (fp32) failed (CUresult %d)", static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
@@ -1158,8 +1234,9 @@ cudaError_t launch_backward(const BackwardArgs& x, cudaStream_t st, char* err, s
     if (a.grp_dkdq > 2 * x.B * x.H) a.grp_dkdq = 2 * x.B * x.H;
   }
 
-  CUtensorMap mq, mk, mv, mvh, mdo;
-  if (!make_map(&mq, x.q, 2 * kD, x.H, x.N, x.B, kT, err, err_len) ||
+  CUtensorMap mq, mk, mv, mvh, mdo, mdq;
+  if (!make_map_f32(&mdq, a.dqacc, 2 * kD, x.H, x.N, x.B, err, err_len) ||
+      !make_map(&mq, x.q, 2 * kD, x.H, x.N, x.B, kT, err, err_len) ||
       !make_map(&mk, x.k, 2 * kD, x.H, x.N, x.B, kT, err, err_len) ||
       !make_map(&mv, x.v, kDV, x.H, x.N, x.B, kT, err, err_len) ||
       !make_map(&mvh, x.v, kDV, x.H, x.N, x.B, kT / 2, err, err_len) ||
@@ -1178,7 +1255,7 @@ cudaError_t launch_backward(const BackwardArgs& x, cudaStream_t st, char* err, s
 
   e = cudaFuncSetAttribute(bwd_dkdq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kq::kDynSmem);
   if (e != cudaSuccess) return e;
-  bwd_dkdq_kernel<<<2 * items, kq::kThreads, kq::kDynSmem, st>>>(mq, mk, mv, mdo, a);
+  bwd_dkdq_kernel<<<2 * items, kq::kThreads, kq::kDynSmem, st>>>(mq, mk, mv, mdo, mdq, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   e = cudaFuncSetAttribute(bwd_dv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, vv::kDynSmem);
