@@ -285,16 +285,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         c = PREFILL
         inp = make_prefill_inputs(c["B"], c["N"], c["H"], c["d"], c["dv"], seed=1000 + rank,
                                   layer=c["layer"], device=dev)
-        lv = make_lambda_vectors(c["d"], seed=1001 + rank)
-        # one lambda per layer, shared by every head: the four vectors replicated per head
-        lv_h = tuple(t.to(dev).expand(c["H"], -1).contiguous() for t in lv)
-        lam_h = torch.empty(c["H"], dtype=torch.float32, device=dev)
-        lam_init = da.diffattn_lambda_init(c["layer"])
+        # one lambda per layer, shared by every head ([P3]), formed inside the prefill kernel
+        lv = tuple(t.to(dev).contiguous() for t in make_lambda_vectors(c["d"], seed=1001 + rank))
         out = torch.empty((c["B"], c["N"], c["H"], c["dv"]), dtype=torch.bfloat16, device=dev)
 
+        def step(q, k, v):
+            da.diffattn_fwd_fused_lambda(q, k, v, *lv, layer=c["layer"], out=out)
+
         for _ in range(args.warmup):
-            da.diffattn_lambda(*lv_h, layer=c["layer"], out=lam_h)
-            da.diffattn_fwd(inp.q, inp.k, inp.v, lam_h, lam_init, out=out)
+            step(inp.q, inp.k, inp.v)
         da.diffattn_device_status()
         kev = [(ev(), ev()) for _ in range(args.steps)]
         with ClockSampler(dev.index) as clk:
@@ -302,9 +301,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             t_start, t_end = ev(), ev()
             t_start.record(stream)
             for i in range(args.steps):
-                da.diffattn_lambda(*lv_h, layer=c["layer"], out=lam_h)
                 kev[i][0].record(stream)
-                da.diffattn_fwd(inp.q, inp.k, inp.v, lam_h, lam_init, out=out)
+                step(inp.q, inp.k, inp.v)
                 kev[i][1].record(stream)
             t_end.record(stream)
             barrier()
@@ -318,8 +316,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         line.update({
             "value": world * flops / (ms_per_step * 1e-3) / 1e12,
             "ms_per_step": ms_per_step,
-            "config": {"workload": "prefill_3b: B4 N4096 H12 d128 dv256 causal, lambda (layer 12) + "
-                                   "DiffAttn + RMSNorm + (1 - lambda_init)",
+            "config": {"workload": "prefill_3b: B4 N4096 H12 d128 dv256 causal, lambda (layer 12, "
+                                   "formed in the kernel) + DiffAttn + RMSNorm + (1 - lambda_init)",
                        "global_batch": PREFILL["B"] * world, "seq_len": PREFILL["N"],
                        "parallelism": f"replicas x{world} (independent batches, no collective)",
                        "l2": "inputs larger than L2 (q, k, v = 302 MB per rank)",
@@ -332,7 +330,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                          "peak_source": f"bf16_tflops_sustained of {peak_src} (kernel run back to back)",
                          "definition_count_tflops":
                              flops / FLOPS_PER_PAIR * FLOPS_PER_PAIR_DEF / (kernel_ms * 1e-3) / 1e12},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": args.steps,
             "clocks": clk.summary(),
         })
 
@@ -346,8 +344,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
             dvv.copy_(hv, non_blocking=True)
-            da.diffattn_lambda(*lv_h, layer=c["layer"], out=lam_h)
-            da.diffattn_fwd(dq, dk, dvv, lam_h, lam_init, out=out)
+            step(dq, dk, dvv)
             hout.copy_(out, non_blocking=True)
 
         e2e_step()
@@ -362,7 +359,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         line["e2e"] = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": 3 * inp.q.numel() * 2,
                        "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": e2e_ms,
-                       "via": "pinned host -> device copies, diffattn_lambda + diffattn_fwd, "
+                       "via": "pinned host -> device copies, diffattn_fwd_fused_lambda, "
                               "device -> host copy of the output"}
         del inp, out, hq, hk, hv, hout, dq, dk, dvv
         torch.cuda.empty_cache()
@@ -414,15 +411,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         c = LONG
         inp = make_prefill_inputs(c["B"], c["N"], c["H"], c["d"], c["dv"], seed=4000 + rank,
                                   layer=c["layer"], device=dev, needle=True)
-        lv = make_lambda_vectors(c["d"], seed=4001 + rank)
-        lv_h = tuple(t.to(dev).expand(c["H"], -1).contiguous() for t in lv)
-        lam_h = torch.empty(c["H"], dtype=torch.float32, device=dev)
-        li = da.diffattn_lambda_init(c["layer"])
+        lv = tuple(t.to(dev).contiguous() for t in make_lambda_vectors(c["d"], seed=4001 + rank))
         out = torch.empty((c["B"], c["N"], c["H"], c["dv"]), dtype=torch.bfloat16, device=dev)
 
         def lstep():
-            da.diffattn_lambda(*lv_h, layer=c["layer"], out=lam_h)
-            da.diffattn_fwd(inp.q, inp.k, inp.v, lam_h, li, out=out)
+            da.diffattn_fwd_fused_lambda(inp.q, inp.k, inp.v, *lv, layer=c["layer"], out=out)
 
         for _ in range(args.warmup):
             lstep()

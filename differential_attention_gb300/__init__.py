@@ -64,6 +64,9 @@ _SIGNATURES = {
                         + [ctypes.c_void_p]),
     "diffattn_v2_decode_workspace_size": (ctypes.c_int, [ctypes.c_int] * 5
                                           + [ctypes.POINTER(ctypes.c_size_t)]),
+    "diffattn_fwd_fused_lambda": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int] * 3
+                                  + [ctypes.c_void_p, ctypes.c_float] + [ctypes.c_int] * 7
+                                  + [ctypes.c_void_p]),
     "diffattn_fwd_train": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_float, ctypes.c_void_p,
                                                                    ctypes.c_float]
                            + [ctypes.c_int] * 7 + [ctypes.c_void_p]),
@@ -387,3 +390,32 @@ def diffattn_bwd(q, k, v, o_pre, stats, dout, lam, lambda_init: float = 0.0, nor
                               _train_flags(causal, norm, scale), DIFFATTN_BF16, _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream)))
     return grads
+
+
+def diffattn_fwd_fused_lambda(q, k, v, lq1, lk1, lq2, lk2, layer: int, norm_weight=None,
+                              eps: float = 1e-5, causal: bool = True, norm: bool = True,
+                              scale: bool = True, out=None, stream=None):
+    """Prefill with lambda formed in the kernel from the four re-parameterisation vectors
+    ([1, dim] for one lambda per layer, or [H, dim]) and the 1-indexed layer."""
+    _dev("q", q, torch.bfloat16)
+    B, N, H, two_d = q.shape
+    d = two_d // 2
+    _dev("k", k, torch.bfloat16)
+    _dev("v", v, torch.bfloat16)
+    dv = v.shape[-1]
+    vecs = [lq1, lk1, lq2, lk2]
+    for i, t in enumerate(vecs):
+        _dev(f"lambda vector {i}", t, torch.float32)
+    sets, dim = vecs[0].shape
+    if any(t.shape != (sets, dim) for t in vecs):
+        raise ValueError("the four lambda vectors must share one shape [sets, dim]")
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if out is None:
+        out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    _check(lib().diffattn_fwd_fused_lambda(_ptr(q), _ptr(k), _ptr(v), _ptr(out), *[_ptr(t) for t in vecs],
+                                           dim, sets, int(layer), _ptr(norm_weight), float(eps), B, N,
+                                           H, d, dv, _train_flags(causal, norm, scale), DIFFATTN_BF16,
+                                           _stream(stream)))
+    return out

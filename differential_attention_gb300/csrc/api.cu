@@ -515,3 +515,63 @@ DIFFATTN_API int diffattn_bwd(const void* q, const void* k, const void* v, const
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_bwd launch");
   return ok();
 }
+
+DIFFATTN_API int diffattn_fwd_fused_lambda(const void* q, const void* k, const void* v, void* out,
+                                           const float* lq1, const float* lk1, const float* lq2,
+                                           const float* lk2, int lambda_dim, int lambda_sets,
+                                           int layer, const float* norm_weight, float eps, int B,
+                                           int N, int H, int d, int dv, int flags, int dtype,
+                                           void* stream) {
+  if (!q || !k || !v || !out || !lq1 || !lk1 || !lq2 || !lk2)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_fused_lambda: null pointer");
+  constexpr int kFusedFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kFusedFlags)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_fused_lambda: unknown flag bits 0x%x", flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_fused_lambda: eps must be > 0 with DIFFATTN_NORM");
+  if (dtype != DIFFATTN_BF16)
+    return fail(DIFFATTN_ERR_DTYPE, "diffattn_fwd_fused_lambda: dtype must be DIFFATTN_BF16");
+  if (layer < 1) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_fused_lambda: layer must be >= 1");
+  if (lambda_dim < 1 || lambda_dim > 4096 || !(lambda_sets == 1 || lambda_sets == H))
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_fused_lambda: need 1 <= lambda_dim <= 4096 and lambda_sets in {1, H}");
+  if (B < 1 || N < 1 || H < 1) return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_fused_lambda: B, N, H must be >= 1");
+  if (!(d == 64 || d == 128) || dv != 2 * d)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_fused_lambda: need d in {64, 128} and dv = 2d");
+  const long long tiles = (static_cast<long long>(N) + 127) / 128 * B * H;
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(N) * H > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_fused_lambda: problem too large for one launch");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lq1, 4) || !aligned(lk1, 4) || !aligned(lq2, 4) || !aligned(lk2, 4) ||
+      (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_fwd_fused_lambda: tensors must be 16-byte aligned");
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = N;
+  p.units = H;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_V1;
+  p.q_heads = H;
+  p.kv_heads = H;
+  p.q_cols = 2 * d;
+  p.k_cols = 2 * d;
+  p.group = 1;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = diffattn_lambda_init(layer);
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  p.lam_vec[0] = lq1;
+  p.lam_vec[1] = lk1;
+  p.lam_vec[2] = lq2;
+  p.lam_vec[3] = lk2;
+  p.lam_dim = lambda_dim;
+  p.lam_sets = lambda_sets;
+  return run_prefill(p, dtype, "diffattn_fwd_fused_lambda", static_cast<cudaStream_t>(stream));
+}

@@ -39,7 +39,34 @@ struct Problem {
   float* stats;
   void* o_pre;
   int n_pad;
+  // lambda formed inside the kernel (V1, exact path) from the re-parameterisation vectors
+  // lq1, lk1, lq2, lk2 [lam_sets, lam_dim] (lam_sets 1: one lambda for every head); null: read
+  // `lambda`. lambda_init is then that of the layer.
+  const float* lam_vec[4];
+  int lam_dim, lam_sets;
 };
+
+// lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init for head u, from Problem::lam_vec.
+// Called by a whole warp (lanes split the dot products); every lane gets the value.
+__device__ inline float lambda_from_vectors_warp(const Problem& p, int u) {
+  const int lane = threadIdx.x & 31;
+  const int set = p.lam_sets == 1 ? 0 : u;
+  const float* a = p.lam_vec[0] + static_cast<size_t>(set) * p.lam_dim;
+  const float* b = p.lam_vec[1] + static_cast<size_t>(set) * p.lam_dim;
+  const float* c = p.lam_vec[2] + static_cast<size_t>(set) * p.lam_dim;
+  const float* d = p.lam_vec[3] + static_cast<size_t>(set) * p.lam_dim;
+  float d1 = 0.f, d2 = 0.f;
+  for (int i = lane; i < p.lam_dim; i += 32) {
+    d1 = fmaf(__ldg(a + i), __ldg(b + i), d1);
+    d2 = fmaf(__ldg(c + i), __ldg(d + i), d2);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+    d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+  }
+  return expf(d1) - expf(d2) + p.lambda_init;
+}
 
 __host__ __device__ inline int q_head_of(const Problem& p, int u, int r) {
   return p.mode == MODE_V1 ? u : 2 * u + r;

@@ -315,6 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
     float bias[2] = {0.f, 0.f}, lam = 0.f;
     bool ok = true, merged = false;
+    // lambda from its vectors: computed now, while the first tiles are still in flight
+    const float lam_fused =
+        (P.mode == MODE_V1 && P.lam_vec[0]) ? lambda_from_vectors_warp(P, u) : 0.f;
 
     // Merge the warpgroups' partial row statistics (once, at the pass boundary). The D buffer
     // is free then: no D has been written yet.
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bias[mp] = -(M + __log2f(L));
       }
       if (P.mode == MODE_V1) {
-        lam = P.lambda[u];
+        lam = P.lam_vec[0] ? lam_fused : P.lambda[u];
       } else if (row < P.N) {
         const float z = P.lam_logit[(static_cast<size_t>(b) * P.N + row) * P.units + u];
         lam = 1.f / (1.f + expf(-z));

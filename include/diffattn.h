@@ -224,6 +224,29 @@ DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const vo
                                     void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Prefill with lambda formed inside the kernel (pages "Differential Transformer: Noise-
+ * Canceling Attention by Subtraction", section "Making lambda learnable and stable", and
+ * "Differential Transformer: softmax can't say zero, so it subtracts", section "lambda,
+ * re-parameterised"): diffattn_fwd, but instead of lambda[H] it takes the four
+ * re-parameterisation vectors and the layer, and each CTA computes
+ *   lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init(layer),
+ *   lambda_init(layer) = 0.8 - 0.6 exp(-0.3 (layer - 1))   (layer 1-indexed)
+ * in fp32 before its subtraction pass, so a layer's step is one launch.
+ *   lq1, lk1, lq2, lk2 : device fp32 [lambda_sets, lambda_dim]; lambda_sets = 1 (one lambda for
+ *                        every head) or H (one per head); 1 <= lambda_dim <= 4096
+ *   layer              : >= 1; also sets the (1 - lambda_init) scale of DIFFATTN_SCALE
+ * Supported: dtype DIFFATTN_BF16 (tensor-core exact path), d in {64, 128}, dv = 2d; flags
+ * DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE.
+ * Errors: as diffattn_fwd.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_fwd_fused_lambda(const void* q, const void* k, const void* v, void* out,
+                                           const float* lq1, const float* lk1, const float* lq2,
+                                           const float* lk2, int lambda_dim, int lambda_sets,
+                                           int layer, const float* norm_weight, float eps, int B,
+                                           int N, int H, int d, int dv, int flags, int dtype,
+                                           void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * Training: forward that keeps what the backward needs, and the backward of the V1 prefill
  * (page "Differential Transformer: softmax can't say zero, so it subtracts", section "The
  * mechanism, exactly" defines the forward; the gradients are its chain rule).

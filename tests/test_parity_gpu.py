@@ -215,6 +215,26 @@ def test_v2_cuda_core_path():
 
 
 # ------------------------------------------------------------------------------------------
+# prefill with lambda formed in the kernel
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("sets,layer,N,causal", [(1, 12, 300, True), (3, 1, 200, False), (3, 24, 129, True)])
+def test_fwd_fused_lambda(sets, layer, N, causal):
+    """lambda from the re-parameterisation vectors inside the prefill equals the oracle's
+    lambda_full fed to its prefill (one lambda for every head, or one per head)."""
+    H = 3
+    inp = make_prefill_inputs(1, N, H, 128, 256, seed=141 + N, layer=layer, causal=causal)
+    vecs = make_lambda_vectors(128, seed=151 + sets, n_sets=sets, std=0.3)
+    w = torch.linspace(0.8, 1.2, 256, dtype=torch.float32)
+    got = da.diffattn_fwd_fused_lambda(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV),
+                                       *[t.to(DEV).contiguous() for t in vecs], layer=layer,
+                                       norm_weight=w.to(DEV), causal=causal)
+    lam = np.broadcast_to(ref.lambda_full(*vecs, layer=layer), (H,))
+    want = ref.diffattn_fwd(inp.q, inp.k, inp.v, lam, ref.lambda_init(layer), norm_weight=w,
+                            causal=causal)
+    assert_bf16(got, want)
+
+
+# ------------------------------------------------------------------------------------------
 # V2 decode
 # ------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("B,L,Hq,Hkv,ragged", [(3, 700, 16, 2, False), (2, 1000, 16, 4, True),
