@@ -345,3 +345,38 @@ def lambda_full_bwd(lq1, lk1, lq2, lk2, dlam):
     e1 = np.exp(np.sum(lq1 * lk1, axis=-1, keepdims=True))
     e2 = np.exp(np.sum(lq2 * lk2, axis=-1, keepdims=True))
     return g * e1 * lk1, g * e1 * lq1, -g * e2 * lk2, -g * e2 * lq2
+
+
+# --------------------------------------------------------------------------------------------
+# decode over a paged cache (a serving layout; the method is unchanged)
+# --------------------------------------------------------------------------------------------
+
+def paged_rows(block_table, seqlens, page_size: int, b: int) -> np.ndarray:
+    """Pool row of every key of sequence b: key j is row j % page_size of page
+    block_table[b, j // page_size], i.e. pool row block_table[b, j // page_size] * page_size +
+    j % page_size."""
+    L = int(np.asarray(_f64(seqlens)).astype(np.int64)[b])
+    table = np.asarray(_f64(block_table)).astype(np.int64)
+    j = np.arange(L)
+    return table[b, j // page_size] * page_size + j % page_size
+
+
+def diffattn_decode_paged(q, k_pool, v_pool, block_table, seqlens, lam, lam_init: float,
+                          norm_weight=None, eps: float = 1e-5, norm: bool = True,
+                          apply_scale: bool = True):
+    """`diffattn_decode` over a cache held in pages: k_pool [num_pages, page_size, H, 2d],
+    v_pool [num_pages, page_size, H, dv], block_table [B, max_pages], seqlens [B]. Each sequence's
+    keys are gathered from the pool in order, then decoded as a contiguous cache."""
+    num_pages, page_size, H, w = k_pool.shape
+    kp = _f64(k_pool).reshape(num_pages * page_size, H, w)
+    vp = _f64(v_pool).reshape(num_pages * page_size, H, v_pool.shape[-1])
+    B = q.shape[0]
+    sl = np.asarray(_f64(seqlens)).astype(np.int64)
+    L = int(sl.max())
+    kc = np.zeros((B, L, H, w))
+    vc = np.zeros((B, L, H, vp.shape[-1]))
+    for b in range(B):
+        rows = paged_rows(block_table, seqlens, page_size, b)
+        kc[b, :rows.size] = kp[rows]
+        vc[b, :rows.size] = vp[rows]
+    return diffattn_decode(q, kc, vc, sl, lam, lam_init, norm_weight, eps, norm, apply_scale)

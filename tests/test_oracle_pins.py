@@ -358,12 +358,36 @@ def pin_lambda_bwd():
         assert float(np.sum(grads[i] * D)) == pytest.approx(fd, rel=1e-6), i
 
 
+def pin_paged_decode():
+    """Paged decode equals contiguous decode when the pool is the contiguous cache cut into pages
+    (identity table), and is unchanged when the pool's pages are shuffled and the table follows."""
+    rng = np.random.default_rng(17)
+    B, L, H, d, dv, ps = 3, 20, 2, 4, 8, 6
+    max_pages = (L + ps - 1) // ps
+    q = rng.standard_normal((B, H, 2 * d))
+    kc = rng.standard_normal((B, max_pages * ps, H, 2 * d))
+    vc = rng.standard_normal((B, max_pages * ps, H, dv))
+    seqlens = np.array([20, 1, 13])
+    lam = np.array([0.3, 0.7])
+    want = ref.diffattn_decode(q, kc, vc, seqlens, lam, 0.4)
+    k_pool = kc.reshape(B * max_pages, ps, H, 2 * d)
+    v_pool = vc.reshape(B * max_pages, ps, H, dv)
+    table = np.arange(B * max_pages).reshape(B, max_pages)
+    got = ref.diffattn_decode_paged(q, k_pool, v_pool, table, seqlens, lam, 0.4)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    perm = rng.permutation(B * max_pages)          # new slot of each old page
+    k_sh = np.empty_like(k_pool); v_sh = np.empty_like(v_pool)
+    k_sh[perm], v_sh[perm] = k_pool, v_pool
+    got2 = ref.diffattn_decode_paged(q, k_sh, v_sh, perm[table], seqlens, lam, 0.4)
+    assert np.allclose(got2, want, rtol=1e-12, atol=1e-12)
+
+
 PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, pin_lambda_spread,
         pin_softmax_floor, pin_toy_needle_table, pin_worked_example, pin_row_sums,
         pin_lambda_zero_is_softmax_attention, pin_equal_maps_scale_attention, pin_brute_force_tiny,
         pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
-        pin_lambda_bwd]
+        pin_lambda_bwd, pin_paged_decode]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -426,6 +450,9 @@ def _mutants():
             np.zeros(np.shape(O)[-1]))),
         "dlam sign": ("diff_attn_head_bwd", bwd_dlam_sign),
         "lambda bwd q/k swapped": ("lambda_full_bwd", lambda_bwd_swapped),
+        "paged row: page and offset swapped": ("paged_rows", lambda table, sl, ps, b: (
+            np.asarray(ref._f64(table)).astype(np.int64)[b, np.arange(int(np.asarray(ref._f64(sl))[b])) % ps]
+            * ps + np.arange(int(np.asarray(ref._f64(sl))[b])) // ps)),
     }
 
 
@@ -438,6 +465,6 @@ def test_planted_mistakes_are_caught(name, monkeypatch):
         try:
             with np.errstate(all="ignore"):
                 pin()
-        except (AssertionError, FloatingPointError, ValueError):
+        except (AssertionError, FloatingPointError, ValueError, IndexError):
             failed.append(pin.__name__)
     assert failed, f"planted mistake '{name}' passed every pin"
