@@ -403,7 +403,42 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                          "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
                          "timed": "diffattn_decode call (split kernel + combine kernel)"},
             "gpu_launches": 2 * dsteps}
-        del dinp, ws, dout
+
+        # the same cache as a pool of 64-token pages, each sequence's pages scattered over it
+        ps = 64
+        mp = dcfg["L"] // ps
+        k_pool = dinp.k_cache.view(dcfg["B"] * mp, ps, dcfg["H"], 2 * dcfg["d"])
+        v_pool = dinp.v_cache.view(dcfg["B"] * mp, ps, dcfg["H"], dcfg["dv"])
+        gp = torch.Generator(device="cpu")
+        gp.manual_seed(2100 + rank)
+        table = torch.randperm(dcfg["B"] * mp, generator=gp).to(torch.int32).view(dcfg["B"], mp).to(dev)
+
+        def dec_paged():
+            da.diffattn_decode_paged(dinp.q, k_pool, v_pool, table, dinp.seqlens, dinp.lam, li_dec,
+                                     workspace=ws, out=dout)
+
+        for _ in range(args.warmup):
+            dec_paged()
+        barrier()
+        pev = [(ev(), ev()) for _ in range(dsteps)]
+        for i in range(dsteps):
+            pev[i][0].record(stream)
+            dec_paged()
+            pev[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        pms = statistics.mean(a.elapsed_time(b) for a, b in pev)
+        pgbs = dbytes / (pms * 1e-3) / 1e9
+        line["decode_paged"] = {
+            "metric": "decode HBM GB/s", "value": world * pgbs, "unit": "GB/s", "ms_per_call": pms,
+            "workload": f"decode_32k over a paged cache: B{dcfg['B']}, cache 32768 in 64-token pages "
+                        "placed in a random order in the pool, H12, d128, dv256, bf16",
+            "roofline": {"bound": "hbm", "achieved": pgbs, "peak": hbm, "unit": "GB/s",
+                         "frac": pgbs / hbm, "bytes_per_launch": dbytes,
+                         "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
+                         "timed": "diffattn_decode_paged call (split kernel + combine kernel)"},
+            "gpu_launches": 2 * dsteps}
+        del dinp, ws, dout, k_pool, v_pool, table
         torch.cuda.empty_cache()
 
     # ======================= long-context prefill =======================

@@ -30,7 +30,8 @@ DIFFATTN_CUDA_CORES = 8
 DIFFATTN_SINGLE_PASS = 16
 
 STATUS_NAMES = {0: "OK", -1: "ERR_ARG", -2: "ERR_SHAPE", -3: "ERR_DTYPE", -4: "ERR_ALIGN",
-                -5: "ERR_CUDA", -6: "ERR_TIMEOUT", -7: "ERR_UNSUPPORTED", -8: "ERR_WORKSPACE"}
+                -5: "ERR_CUDA", -6: "ERR_TIMEOUT", -7: "ERR_UNSUPPORTED", -8: "ERR_WORKSPACE",
+                -9: "ERR_INDEX"}
 
 
 class DiffAttnError(RuntimeError):
@@ -64,6 +65,10 @@ _SIGNATURES = {
                         + [ctypes.c_void_p]),
     "diffattn_v2_decode_workspace_size": (ctypes.c_int, [ctypes.c_int] * 5
                                           + [ctypes.POINTER(ctypes.c_size_t)]),
+    "diffattn_decode_paged": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_float, ctypes.c_void_p,
+                                                                      ctypes.c_float]
+                              + [ctypes.c_int] * 9 + [ctypes.c_void_p, ctypes.c_size_t,
+                                                      ctypes.c_void_p]),
     "diffattn_fwd_fused_lambda": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int] * 3
                                   + [ctypes.c_void_p, ctypes.c_float] + [ctypes.c_int] * 7
                                   + [ctypes.c_void_p]),
@@ -418,4 +423,39 @@ def diffattn_fwd_fused_lambda(q, k, v, lq1, lk1, lq2, lk2, layer: int, norm_weig
                                            dim, sets, int(layer), _ptr(norm_weight), float(eps), B, N,
                                            H, d, dv, _train_flags(causal, norm, scale), DIFFATTN_BF16,
                                            _stream(stream)))
+    return out
+
+
+def diffattn_decode_paged(q, k_pool, v_pool, block_table, seqlens, lam, lambda_init: float = 0.0,
+                          norm_weight=None, eps: float = 1e-5, norm: bool = True,
+                          scale: bool = True, workspace=None, out=None, stream=None):
+    """Decode over a paged cache: pools [num_pages, page_size, H, 2d] / [.., dv], block_table
+    [B, max_pages] int32, seqlens [B] int32."""
+    _dev("q", q, torch.bfloat16)
+    B, H, two_d = q.shape
+    d = two_d // 2
+    _dev("k_pool", k_pool, torch.bfloat16)
+    _dev("v_pool", v_pool, torch.bfloat16)
+    num_pages, page_size = k_pool.shape[0], k_pool.shape[1]
+    dv = v_pool.shape[-1]
+    if k_pool.shape != (num_pages, page_size, H, two_d) or v_pool.shape[:3] != (num_pages, page_size, H):
+        raise ValueError("pools must be [num_pages, page_size, H, 2d] and [num_pages, page_size, H, dv]")
+    _dev("block_table", block_table, torch.int32)
+    _dev("seqlens", seqlens, torch.int32)
+    max_pages = block_table.shape[1]
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if workspace is None:
+        workspace = torch.empty(diffattn_decode_workspace_size(B, max_pages * page_size, H, d, dv),
+                                dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    flags = (DIFFATTN_NORM if norm else 0) | (DIFFATTN_SCALE if scale else 0)
+    _check(lib().diffattn_decode_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                       _ptr(seqlens), _ptr(out), _ptr(lam), float(lambda_init),
+                                       _ptr(norm_weight), float(eps), B, H, d, dv, num_pages,
+                                       page_size, max_pages, flags, DIFFATTN_BF16, _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
     return out

@@ -55,6 +55,8 @@ constexpr int kPrefillFlags =
 
 }  // namespace
 
+constexpr int DEV_BAD_INDEX_BIT = 2;  // the kernels' DEV_BAD_INDEX status bit
+
 extern "C" {
 
 DIFFATTN_API int diffattn_version(void) { return 1 * 10000 + 0 * 100 + 0; }
@@ -70,8 +72,12 @@ DIFFATTN_API int diffattn_device_status(void* stream) {
   if (e == cudaSuccess) e = da::status_simt(&x);
   if (e == cudaSuccess) e = da::status_v2_decode_tc(&y);
   if (e == cudaSuccess) e = da::status_backward(&z);
+  int dd = 0;
+  if (e == cudaSuccess) e = da::status_decode(&dd);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
-  v |= w | x | y | z;
+  v |= w | x | y | z | dd;
+  if (v & DEV_BAD_INDEX_BIT)
+    return fail(DIFFATTN_ERR_INDEX, "a block-table entry was outside [0, num_pages) (status %d)", v);
   if (v != 0) return fail(DIFFATTN_ERR_TIMEOUT, "a bounded wait inside a kernel ran out (status %d)", v);
   return ok();
 }
@@ -574,4 +580,61 @@ DIFFATTN_API int diffattn_fwd_fused_lambda(const void* q, const void* k, const v
   p.lam_dim = lambda_dim;
   p.lam_sets = lambda_sets;
   return run_prefill(p, dtype, "diffattn_fwd_fused_lambda", static_cast<cudaStream_t>(stream));
+}
+
+DIFFATTN_API int diffattn_decode_paged(const void* q, const void* k_pool, const void* v_pool,
+                                       const int* block_table, const int* seqlens, void* out,
+                                       const float* lambda, float lambda_init,
+                                       const float* norm_weight, float eps, int B, int H, int d,
+                                       int dv, int num_pages, int page_size, int max_pages,
+                                       int flags, int dtype, void* workspace, size_t ws_bytes,
+                                       void* stream) {
+  if (!q || !k_pool || !v_pool || !block_table || !seqlens || !out || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_decode_paged: null pointer");
+  if (flags & ~(DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_decode_paged: unknown flag bits 0x%x", flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_decode_paged: eps must be > 0 with DIFFATTN_NORM");
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "diffattn_decode_paged: dtype must be DIFFATTN_BF16");
+  if (B < 1 || H < 1 || B > 65535 || H > 65535 || num_pages < 1 || page_size < 1 || max_pages < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode_paged: need 1 <= B, H <= 65535 and num_pages, page_size, max_pages >= 1");
+  const long long lmax = static_cast<long long>(max_pages) * page_size;
+  if (lmax > 0x7fffffffLL || static_cast<long long>(num_pages) * page_size > (1LL << 40))
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode_paged: max_pages * page_size too large");
+  if (d != 128 || dv != 256)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode_paged: need d = 128 and dv = 256 (got d=%d dv=%d)", d, dv);
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || !aligned(seqlens, 4) || !aligned(block_table, 4) ||
+      (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_decode_paged: tensors must be 16-byte aligned");
+  const int Lmax = static_cast<int>(lmax);
+  const size_t need = da::decode_workspace_bytes(B, Lmax, H, dv);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(DIFFATTN_ERR_WORKSPACE, "diffattn_decode_paged: need a 256-byte aligned workspace of %zu bytes", need);
+  int rc = check_device();
+  if (rc) return rc;
+  da::DecodeArgs a{};
+  a.q = q;
+  a.k_cache = k_pool;
+  a.v_cache = v_pool;
+  a.seqlens = seqlens;
+  a.out = out;
+  a.lambda = lambda;
+  a.lambda_init = lambda_init;
+  a.norm_w = norm_weight;
+  a.eps = eps;
+  a.flags = flags;
+  a.B = B;
+  a.Lmax = Lmax;
+  a.H = H;
+  a.d = d;
+  a.dv = dv;
+  a.ws = static_cast<float*>(workspace);
+  a.block_table = block_table;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  cudaError_t e = da::launch_decode(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_decode_paged launch");
+  return ok();
 }

@@ -77,8 +77,31 @@ struct DecSplitParams {
   float* ws;
   int Lmax, H, splits, chunk;
   float scale_log2;
+  const int* block_table;  // paged: [B, max_pages]
+  int page_size, max_pages, num_pages;
+  uint32_t ps_magic, ps_shift;  // j / page_size = (umulhi(j, magic) + j) >> shift, j < 2^31
 };
 
+// Row (key j of sequence b) of a contiguous [B, Lmax, H, w] cache, or of a paged pool
+// [num_pages, page_size, H, w] through the block table. A page id outside [0, num_pages) flags
+// DEV_BAD_INDEX and reads page 0 instead (the call's result is then invalid, nothing faults).
+template <bool kPaged>
+__device__ __forceinline__ size_t cache_row(const DecSplitParams& p, int b, int j) {
+  if constexpr (kPaged) {
+    const uint32_t uj = static_cast<uint32_t>(j);
+    const uint32_t pi = (__umulhi(uj, p.ps_magic) + uj) >> p.ps_shift;  // j / page_size
+    int pg = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + pi);
+    if (pg < 0 || pg >= p.num_pages) {
+      flag_device_error(DEV_BAD_INDEX);
+      pg = 0;
+    }
+    return static_cast<size_t>(pg) * p.page_size + (uj - pi * static_cast<uint32_t>(p.page_size));
+  } else {
+    return static_cast<size_t>(b) * p.Lmax + j;
+  }
+}
+
+template <bool kPaged>
 __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecSplitParams p) {
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -102,18 +125,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecSpli
   for (int i = 0; i < 8; ++i) o1[i] = o2[i] = 0.f;
 
   const size_t row_stride = static_cast<size_t>(p.H) * kDecWidth;  // elements between keys
-  const __nv_bfloat16* kbase =
-      p.kc + (static_cast<size_t>(b) * p.Lmax * p.H + h) * kDecWidth + 8 * lane;
-  const __nv_bfloat16* vbase =
-      p.vc + (static_cast<size_t>(b) * p.Lmax * p.H + h) * kDecWidth + 8 * lane;
+  const __nv_bfloat16* kbase = p.kc + static_cast<size_t>(h) * kDecWidth + 8 * lane;
+  const __nv_bfloat16* vbase = p.vc + static_cast<size_t>(h) * kDecWidth + 8 * lane;
 
   for (int g0 = k0 + warp * kG; g0 < k1; g0 += kDecWarps * kG) {
     uint4 ku[kG], vu[kG];
 #pragma unroll
     for (int e = 0; e < kG; ++e) {
       const int j = min(g0 + e, k1 - 1);  // clamp keeps the load in bounds; masked below
-      ku[e] = ldg_stream(kbase + static_cast<size_t>(j) * row_stride);
-      vu[e] = ldg_stream(vbase + static_cast<size_t>(j) * row_stride);
+      const size_t row = cache_row<kPaged>(p, b, j) * row_stride;
+      ku[e] = ldg_stream(kbase + row);
+      vu[e] = ldg_stream(vbase + row);
     }
     float sc[kG];
 #pragma unroll
@@ -262,6 +284,8 @@ __global__ void __launch_bounds__(kDecWidth) decode_combine_kernel(const DecComb
   p.out[(static_cast<size_t>(b) * p.H + h) * kDecWidth + c] = __float2bfloat16_rn(y);
 }
 
+cudaError_t status_decode(int* v) { return read_clear_status(v); }
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   int chunk = 0;
   const int S = decode_splits(a.B, a.Lmax, a.H, &chunk);
@@ -276,7 +300,24 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   sp.splits = S;
   sp.chunk = chunk;
   sp.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.d));
-  decode_split_kernel<<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
+  sp.block_table = a.block_table;
+  sp.page_size = a.page_size;
+  sp.max_pages = a.max_pages;
+  sp.num_pages = a.num_pages;
+  sp.ps_magic = sp.ps_shift = 0;
+  if (a.block_table) {
+    // division by the invariant page size (Granlund and Montgomery, "Division by invariant
+    // integers using multiplication", 1994): l = ceil(log2 d), m = 2^32 (2^l - d) / d + 1
+    uint32_t l = 0;
+    while ((1ull << l) < static_cast<unsigned long long>(a.page_size)) ++l;
+    const unsigned long long d = static_cast<unsigned long long>(a.page_size);
+    sp.ps_magic = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+    sp.ps_shift = l;
+  }
+  if (a.block_table)
+    decode_split_kernel<true><<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
+  else
+    decode_split_kernel<false><<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   DecCombineParams cp;
@@ -370,7 +411,8 @@ cudaError_t launch_decode_noalloc(const DecodeArgs& a, cudaStream_t st) {
   sp.splits = S;
   sp.chunk = chunk;
   sp.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.d));
-  decode_split_kernel<<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
+  sp.block_table = nullptr;
+  decode_split_kernel<false><<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   DecCombineParams cp;

@@ -101,10 +101,16 @@ struct DecodeArgs {
   int flags;
   int B, Lmax, H, d, dv;
   float* ws;
+  // paged cache (block_table non-null): k_cache / v_cache are pools [num_pages, page_size, H, *]
+  // and key j of sequence b lives in page block_table[b * max_pages + j / page_size];
+  // Lmax = max_pages * page_size
+  const int* block_table;
+  int page_size, max_pages, num_pages;
 };
 int decode_splits(int B, int Lmax, int H, int* chunk_out);
 size_t decode_workspace_bytes(int B, int Lmax, int H, int dv);
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);  // contiguous or paged
+cudaError_t status_decode(int* v);
 
 // DIFF V2 decode: Hq query heads (pairs 2p, 2p+1) over an [B, Lmax, Hkv, 128] cache.
 struct V2DecodeArgs {

@@ -9,7 +9,7 @@
 namespace da {
 
 // Error codes a kernel can leave in the device status word.
-enum : int { DEV_OK = 0, DEV_TIMEOUT = 1 };
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
 
 // Device status word of this translation unit: a kernel whose bounded wait ran out ORs an
 // error code into it; the host reads and clears it (read_clear_status). Internal linkage keeps

@@ -46,7 +46,8 @@ typedef enum {
   DIFFATTN_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed (message has the code) */
   DIFFATTN_ERR_TIMEOUT = -6,     /* a kernel's bounded wait ran out (see diffattn_device_status) */
   DIFFATTN_ERR_UNSUPPORTED = -7, /* device is not sm_103 / sm_100 family */
-  DIFFATTN_ERR_WORKSPACE = -8    /* workspace missing or smaller than *_workspace_size */
+  DIFFATTN_ERR_WORKSPACE = -8,   /* workspace missing or smaller than *_workspace_size */
+  DIFFATTN_ERR_INDEX = -9        /* a device-side index (a block-table entry) was out of range */
 } diffattn_status;
 
 typedef enum { DIFFATTN_BF16 = 0, DIFFATTN_FP32 = 1 } diffattn_dtype;
@@ -70,9 +71,10 @@ DIFFATTN_API int diffattn_version(void);
  * owned by the library and valid until the next call on the same thread. */
 DIFFATTN_API const char* diffattn_last_error_string(void);
 
-/* Synchronises `stream`, then reads and clears the device error flag that bounded waits set.
- * Returns DIFFATTN_OK, DIFFATTN_ERR_TIMEOUT (a wait ran out since the last call), or
- * DIFFATTN_ERR_CUDA. */
+/* Synchronises `stream`, then reads and clears the device error flags that kernels set.
+ * Returns DIFFATTN_OK, DIFFATTN_ERR_TIMEOUT (a bounded wait ran out since the last call),
+ * DIFFATTN_ERR_INDEX (a paged decode met a block-table entry outside [0, num_pages): that access
+ * read page 0 instead and the call's output is invalid), or DIFFATTN_ERR_CUDA. */
 DIFFATTN_API int diffattn_device_status(void* stream);
 
 /* Diagnostics (not part of the method): launch one kernel whose bounded wait is certain to run
@@ -193,6 +195,28 @@ DIFFATTN_API int diffattn_decode_noalloc(const void* q, const void* k_cache, con
  * two heads of a pair must sit in one GQA group). The scale is 1/sqrt(d).
  * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_CUDA.
  * ------------------------------------------------------------------------------------------ */
+/* ------------------------------------------------------------------------------------------
+ * Decode over a paged KV cache: diffattn_decode with the cache held in fixed-size pages of a
+ * shared pool (the pages give no cache layout; this is the usual serving layout, and the method
+ * is unchanged: key j of sequence b is row j % page_size of page block_table[b][j / page_size]).
+ *   k_pool : device [num_pages, page_size, H, 2d] = [K1 | K2]
+ *   v_pool : device [num_pages, page_size, H, dv]
+ *   block_table : device int32 [B, max_pages]; entries for keys < seqlens[b] must be in
+ *            [0, num_pages) (checked on the device: see DIFFATTN_ERR_INDEX); the rest are not read
+ *   seqlens : device int32 [B], required, in [1, max_pages * page_size] (clamped on the device)
+ *   other arguments and the workspace: as diffattn_decode, with
+ *   diffattn_decode_workspace_size(B, max_pages * page_size, H, d, dv)
+ * Supported: dtype DIFFATTN_BF16, d = 128, dv = 256, page_size >= 1.
+ * Errors: as diffattn_decode.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_decode_paged(const void* q, const void* k_pool, const void* v_pool,
+                                       const int* block_table, const int* seqlens, void* out,
+                                       const float* lambda, float lambda_init,
+                                       const float* norm_weight, float eps, int B, int H, int d,
+                                       int dv, int num_pages, int page_size, int max_pages,
+                                       int flags, int dtype, void* workspace, size_t ws_bytes,
+                                       void* stream);
+
 DIFFATTN_API int diffattn_v2_fwd(const void* q, const void* k, const void* v,
                                  const float* lam_logit, void* out, int B, int N, int Hq, int Hkv,
                                  int d, int flags, int dtype, void* stream);

@@ -14,4 +14,5 @@ from .workloads import (  # noqa: F401
     make_tiny_inputs,
     make_v2_decode_inputs,
     make_v2_inputs,
+    page_cache,
 )

@@ -214,3 +214,23 @@ def make_v2_decode_inputs(B: int, L: int, Hq: int, Hkv: int, d: int, seed: int, 
 def make_dout(B: int, N: int, H: int, dv: int, seed: int, device="cpu", dtype=torch.bfloat16):
     """Upstream gradient dL/dout for the backward: N(0, 1) per element."""
     return _randn((B, N, H, dv), _gen(seed, device), device).to(dtype)
+
+
+def page_cache(k_cache: torch.Tensor, v_cache: torch.Tensor, page_size: int, seed: int,
+               spare_pages: int = 0):
+    """Cut a contiguous cache [B, L, H, *] (L a multiple of page_size) into pages, place them in a
+    pool in a seeded random order (with `spare_pages` unused pages of noise), and return
+    (k_pool, v_pool, block_table int32 [B, L / page_size])."""
+    B, L, H, wk = k_cache.shape
+    wv = v_cache.shape[-1]
+    mp = L // page_size
+    n = B * mp + spare_pages
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    slot = torch.randperm(n, generator=g)[:B * mp]  # pool slot of logical page (b, p)
+    k_pool = torch.randn((n, page_size, H, wk), generator=g).to(k_cache.dtype).to(k_cache.device)
+    v_pool = torch.randn((n, page_size, H, wv), generator=g).to(v_cache.dtype).to(v_cache.device)
+    slot_d = slot.to(k_cache.device)
+    k_pool[slot_d] = k_cache.reshape(B * mp, page_size, H, wk)
+    v_pool[slot_d] = v_cache.reshape(B * mp, page_size, H, wv)
+    return k_pool, v_pool, slot.reshape(B, mp).to(torch.int32).to(k_cache.device)

@@ -10,7 +10,7 @@ import torch
 import differential_attention_gb300 as da
 from oracle import diffattn_ref as ref
 from synth import (make_decode_inputs, make_lambda_vectors, make_prefill_inputs, make_tiny_inputs,
-                   make_v2_decode_inputs, make_v2_inputs)
+                   make_v2_decode_inputs, make_v2_inputs, page_cache)
 from tests.gpu_util import assert_bf16, assert_fp32, errors
 
 pytestmark = pytest.mark.gpu
@@ -191,6 +191,40 @@ def test_decode_matches_prefill_last_row():
     dec = da.diffattn_decode(q[:, -1].contiguous(), k, v, lam, 0.5)
     max_abs, rel = errors(dec, pre[:, -1])
     assert rel < 2e-2 and max_abs < 4e-2
+
+
+# ------------------------------------------------------------------------------------------
+# decode over a paged cache
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("B,L,H,ps", [(3, 640, 2, 16), (2, 300, 2, 100), (2, 256, 1, 128), (3, 50, 2, 1)])
+def test_decode_paged(B, L, H, ps):
+    """Ragged sequences in a shuffled pool with spare pages, against the oracle; and the same
+    numbers as the contiguous decode of the same cache (same splits, same order: bit-equal)."""
+    inp = make_decode_inputs(B, L, H, 128, 256, seed=161 + L, ragged=True)
+    li = ref.lambda_init(inp.layer)
+    k_pool, v_pool, table = page_cache(inp.k_cache, inp.v_cache, ps, seed=171 + ps, spare_pages=3)
+    got = da.diffattn_decode_paged(inp.q.to(DEV), k_pool.to(DEV), v_pool.to(DEV), table.to(DEV),
+                                   inp.seqlens.to(DEV), inp.lam.to(DEV), li)
+    want = ref.diffattn_decode_paged(inp.q, k_pool, v_pool, table, inp.seqlens, inp.lam, li)
+    assert_bf16(got, want)
+    flat = da.diffattn_decode(inp.q.to(DEV), inp.k_cache.to(DEV), inp.v_cache.to(DEV),
+                              inp.lam.to(DEV), li, seqlens=inp.seqlens.to(DEV))
+    assert torch.equal(got, flat)
+    da.diffattn_device_status()
+
+
+def test_decode_paged_bad_page_is_reported():
+    """A block-table entry outside the pool is caught by the kernel's own bounds check: the
+    access is redirected to page 0, nothing faults, and the host sees DIFFATTN_ERR_INDEX."""
+    inp = make_decode_inputs(1, 64, 1, 128, 256, seed=181)
+    k_pool, v_pool, table = page_cache(inp.k_cache, inp.v_cache, 16, seed=182)
+    table[0, 2] = k_pool.shape[0] + 5
+    da.diffattn_decode_paged(inp.q.to(DEV), k_pool.to(DEV), v_pool.to(DEV), table.to(DEV),
+                             inp.seqlens.to(DEV), inp.lam.to(DEV), 0.5)
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_device_status()
+    assert e.value.status == -9  # DIFFATTN_ERR_INDEX
+    da.diffattn_device_status()  # cleared: a later call reports OK
 
 
 # ------------------------------------------------------------------------------------------
