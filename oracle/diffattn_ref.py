@@ -380,3 +380,28 @@ def diffattn_decode_paged(q, k_pool, v_pool, block_table, seqlens, lam, lam_init
         kc[b, :rows.size] = kp[rows]
         vc[b, :rows.size] = vp[rows]
     return diffattn_decode(q, kc, vc, sl, lam, lam_init, norm_weight, eps, norm, apply_scale)
+
+
+# --------------------------------------------------------------------------------------------
+# variable-length prefill (packed sequences; the operator per sequence is unchanged)
+# --------------------------------------------------------------------------------------------
+
+def varlen_segments(cu_seqlens) -> list:
+    """(start, end) rows of each packed sequence from the offsets cu_seqlens [B + 1]."""
+    cu = np.asarray(_f64(cu_seqlens)).astype(np.int64)
+    return [(int(cu[i]), int(cu[i + 1])) for i in range(cu.size - 1)]
+
+
+def diffattn_fwd_varlen(q, k, v, cu_seqlens, lam, lam_init: float, norm_weight=None,
+                        eps: float = 1e-5, norm: bool = True, apply_scale: bool = True,
+                        causal: bool = True):
+    """`diffattn_fwd` applied to each sequence of a packed batch on its own: q, k [total, H, 2d],
+    v [total, H, dv]; sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1. Returns float64
+    [total, H, dv]; rows in no sequence are 0."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    out = np.zeros((q.shape[0], q.shape[1], v.shape[-1]))
+    for s0, s1 in varlen_segments(cu_seqlens):
+        if s1 > s0:
+            out[s0:s1] = diffattn_fwd(q[None, s0:s1], k[None, s0:s1], v[None, s0:s1], lam, lam_init,
+                                      norm_weight, eps, norm, apply_scale, causal)[0]
+    return out

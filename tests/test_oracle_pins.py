@@ -382,12 +382,35 @@ def pin_paged_decode():
     assert np.allclose(got2, want, rtol=1e-12, atol=1e-12)
 
 
+def pin_varlen():
+    """Packed sequences: with equal lengths the result is the batched prefill's; and each sequence
+    sees only itself (changing another sequence's tokens leaves its rows unchanged)."""
+    rng = np.random.default_rng(19)
+    B, N, H, d, dv = 3, 7, 2, 4, 8
+    q = rng.standard_normal((B, N, H, 2 * d)); k = rng.standard_normal((B, N, H, 2 * d))
+    v = rng.standard_normal((B, N, H, dv)); lam = np.array([0.2, 0.9])
+    cu = np.arange(B + 1) * N
+    got = ref.diffattn_fwd_varlen(q.reshape(B * N, H, 2 * d), k.reshape(B * N, H, 2 * d),
+                                  v.reshape(B * N, H, dv), cu, lam, 0.3)
+    want = ref.diffattn_fwd(q, k, v, lam, 0.3).reshape(B * N, H, dv)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    cu2 = np.array([0, 5, 5, 12, 20])
+    T = 21
+    q2, k2, v2 = (rng.standard_normal((T, H, w)) for w in (2 * d, 2 * d, dv))
+    a = ref.diffattn_fwd_varlen(q2, k2, v2, cu2, lam, 0.3)
+    k3 = k2.copy(); k3[5:12] += rng.standard_normal(k3[5:12].shape); v3 = v2.copy(); v3[12:20] -= 2.0
+    b = ref.diffattn_fwd_varlen(q2, k3, v3, cu2, lam, 0.3)
+    assert np.allclose(a[0:5], b[0:5]) and not np.allclose(a[5:12], b[5:12])
+    assert np.allclose(a[5:12], ref.diffattn_fwd(q2[None, 5:12], k2[None, 5:12], v2[None, 5:12], lam, 0.3)[0])
+    assert np.all(a[20] == 0)
+
+
 PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, pin_lambda_spread,
         pin_softmax_floor, pin_toy_needle_table, pin_worked_example, pin_row_sums,
         pin_lambda_zero_is_softmax_attention, pin_equal_maps_scale_attention, pin_brute_force_tiny,
         pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
-        pin_lambda_bwd, pin_paged_decode]
+        pin_lambda_bwd, pin_paged_decode, pin_varlen]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -450,6 +473,7 @@ def _mutants():
             np.zeros(np.shape(O)[-1]))),
         "dlam sign": ("diff_attn_head_bwd", bwd_dlam_sign),
         "lambda bwd q/k swapped": ("lambda_full_bwd", lambda_bwd_swapped),
+        "varlen: one sequence": ("varlen_segments", lambda cu: [(0, int(np.asarray(cu)[-1]))]),
         "paged row: page and offset swapped": ("paged_rows", lambda table, sl, ps, b: (
             np.asarray(ref._f64(table)).astype(np.int64)[b, np.arange(int(np.asarray(ref._f64(sl))[b])) % ps]
             * ps + np.arange(int(np.asarray(ref._f64(sl))[b])) // ps)),
