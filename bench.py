@@ -26,6 +26,7 @@ import statistics
 import subprocess
 import sys
 import time
+import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -62,6 +63,18 @@ def decode_bytes(cfg=DECODE) -> float:
 
 def v2_decode_bytes(cfg=V2_DECODE) -> float:
     return float(cfg["B"] * cfg["L"] * cfg["Hkv"] * 2 * cfg["d"] * 2)
+
+
+def varlen_lengths():
+    """A seeded mix of 16 sequence lengths from 1 to 4096 tokens (16,384 in total): the packed
+    stand-in for a batch of documents of different lengths."""
+    rng = np.random.default_rng(12)
+    lens = np.maximum(1, np.round(rng.pareto(1.2, 16) * 300)).astype(int)
+    lens = np.minimum(lens, 4096)
+    lens[0], lens[-1] = 4096, 1
+    rest = 16384 - lens.sum()
+    lens[1] = max(1, lens[1] + rest)
+    return [int(x) for x in np.minimum(lens, 4096)]
 
 
 def load_peaks():
@@ -509,6 +522,47 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del vinp, vout
         torch.cuda.empty_cache()
 
+    # ======================= variable-length prefill (packed sequences) =======================
+    if args.only in ("all", "varlen"):
+        c = PREFILL
+        lens = varlen_lengths()
+        total = int(sum(lens))
+        inp = make_prefill_inputs(1, total, c["H"], c["d"], c["dv"], seed=8000 + rank,
+                                  layer=c["layer"], device=dev)
+        cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=dev)
+        lam = torch.full((c["H"],), 0.6, dtype=torch.float32, device=dev)
+        li = da.diffattn_lambda_init(c["layer"])
+        out = torch.empty((total, c["H"], c["dv"]), dtype=torch.bfloat16, device=dev)
+        q, k, v = inp.q[0], inp.k[0], inp.v[0]
+
+        def vstep():
+            da.diffattn_fwd_varlen(q, k, v, cu, lam, li, max_seqlen=max(lens), out=out)
+
+        for _ in range(args.warmup):
+            vstep()
+        barrier()
+        n_steps = max(5, min(50, args.steps))
+        evs = [(ev(), ev()) for _ in range(n_steps)]
+        for i in range(n_steps):
+            evs[i][0].record(stream)
+            vstep()
+            evs[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        vflops = float(sum(c["H"] * causal_pairs(n) * FLOPS_PER_PAIR for n in lens))
+        vtf = vflops / (ms * 1e-3) / 1e12
+        line["varlen"] = {
+            "metric": "DiffAttn fwd TFLOP/s", "value": world * vtf, "unit": "TFLOP/s",
+            "ms_per_call": ms,
+            "workload": f"prefill_3b shapes over {len(lens)} packed sequences of mixed length "
+                        f"(seeded, {min(lens)}..{max(lens)} tokens, {total} in total), causal, H12",
+            "roofline": {"bound": "tensor", "achieved": vtf, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": vtf / peak_tf, "flops_per_launch": vflops},
+            "gpu_launches": n_steps}
+        del inp, out, q, k, v
+        torch.cuda.empty_cache()
+
     # ======================= training step: forward (saving statistics) + backward ==========
     if args.only in ("all", "backward"):
         c = PREFILL
@@ -628,7 +682,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2", "v2_decode", "long", "backward"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2", "v2_decode", "long", "backward", "varlen"], default="all",
                     help="profiling aid: run one workload (the JSON line then lacks the others)")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="profiling aid: a smaller decode batch for captures that save device memory")

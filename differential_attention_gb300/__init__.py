@@ -69,6 +69,9 @@ _SIGNATURES = {
                                                                       ctypes.c_float]
                               + [ctypes.c_int] * 9 + [ctypes.c_void_p, ctypes.c_size_t,
                                                       ctypes.c_void_p]),
+    "diffattn_fwd_varlen": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 2
+                            + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
+                            + [ctypes.c_int] * 6 + [ctypes.c_void_p]),
     "diffattn_fwd_fused_lambda": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int] * 3
                                   + [ctypes.c_void_p, ctypes.c_float] + [ctypes.c_int] * 7
                                   + [ctypes.c_void_p]),
@@ -458,4 +461,34 @@ def diffattn_decode_paged(q, k_pool, v_pool, block_table, seqlens, lam, lambda_i
                                        _ptr(norm_weight), float(eps), B, H, d, dv, num_pages,
                                        page_size, max_pages, flags, DIFFATTN_BF16, _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def diffattn_fwd_varlen(q, k, v, cu_seqlens, lam, lambda_init: float = 0.0, max_seqlen=None,
+                        norm_weight=None, eps: float = 1e-5, causal: bool = True, norm: bool = True,
+                        scale: bool = True, out=None, stream=None):
+    """Prefill over packed sequences: q, k [total, H, 2d], v [total, H, dv], cu_seqlens int32
+    [B + 1] on the device. `max_seqlen` (the longest sequence) is read from cu_seqlens if not
+    given (one device-to-host copy)."""
+    _dev("q", q, torch.bfloat16)
+    total, H, two_d = q.shape
+    d = two_d // 2
+    _dev("k", k, torch.bfloat16)
+    _dev("v", v, torch.bfloat16)
+    dv = v.shape[-1]
+    _dev("cu_seqlens", cu_seqlens, torch.int32)
+    B = cu_seqlens.numel() - 1
+    if max_seqlen is None:
+        max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if B > 0 else 1
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if out is None:
+        out = torch.zeros((total, H, dv), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    _check(lib().diffattn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(cu_seqlens),
+                                     max(1, int(max_seqlen)), total, _ptr(lam), float(lambda_init),
+                                     _ptr(norm_weight), float(eps), B, H, d, dv,
+                                     _train_flags(causal, norm, scale), DIFFATTN_BF16,
+                                     _stream(stream)))
     return out

@@ -638,3 +638,54 @@ DIFFATTN_API int diffattn_decode_paged(const void* q, const void* k_pool, const 
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_decode_paged launch");
   return ok();
 }
+
+DIFFATTN_API int diffattn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
+                                     const int* cu_seqlens, int max_seqlen, int total,
+                                     const float* lambda, float lambda_init,
+                                     const float* norm_weight, float eps, int B, int H, int d,
+                                     int dv, int flags, int dtype, void* stream) {
+  if (!q || !k || !v || !out || !cu_seqlens || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_varlen: null pointer");
+  constexpr int kVarFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kVarFlags) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_varlen: unknown flag bits 0x%x", flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_varlen: eps must be > 0 with DIFFATTN_NORM");
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "diffattn_fwd_varlen: dtype must be DIFFATTN_BF16");
+  if (B < 1 || H < 1 || max_seqlen < 1 || total < 1 || max_seqlen > total)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_varlen: need B, H >= 1 and 1 <= max_seqlen <= total");
+  if (!(d == 64 || d == 128) || dv != 2 * d)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_varlen: need d in {64, 128} and dv = 2d");
+  const long long tiles = (static_cast<long long>(max_seqlen) + 127) / 128 * B * H;
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(total) * H > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_varlen: problem too large for one launch");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || !aligned(cu_seqlens, 4) || (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_fwd_varlen: tensors must be 16-byte aligned");
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = max_seqlen;
+  p.units = H;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_V1;
+  p.q_heads = H;
+  p.kv_heads = H;
+  p.q_cols = 2 * d;
+  p.k_cols = 2 * d;
+  p.group = 1;
+  p.lambda = lambda;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  p.cu_seqlens = cu_seqlens;
+  p.total = total;
+  return run_prefill(p, dtype, "diffattn_fwd_varlen", static_cast<cudaStream_t>(stream));
+}

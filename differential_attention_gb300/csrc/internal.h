@@ -44,6 +44,11 @@ struct Problem {
   // `lambda`. lambda_init is then that of the layer.
   const float* lam_vec[4];
   int lam_dim, lam_sets;
+  // variable-length prefill (V1, exact path): sequences packed along the token axis of
+  // q/k/v/out [total, H, *]; sequence b holds rows cu_seqlens[b] .. cu_seqlens[b+1]-1. N is then
+  // the longest sequence (it sizes the grid) and `total` the packed length.
+  const int* cu_seqlens;
+  int total;
 };
 
 // lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init for head u, from Problem::lam_vec.

@@ -127,7 +127,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qt = causal ? (kp.n_qt - 1 - r_in / gsize) : (r_in / gsize);
   const int bu = g0 + r_in % gsize;
   const int b = bu / P.units, u = bu % P.units;
-  const int n_kv_all = (P.N + BN - 1) / BN;
+  // this sequence's rows: [seq0, seq0 + SN) of the (packed) token axis; TMA batch coordinate tb
+  int seq0 = 0, SN = P.N, tb = b;
+  if (P.cu_seqlens) {
+    seq0 = P.cu_seqlens[b];
+    SN = P.cu_seqlens[b + 1] - seq0;
+    tb = 0;
+    // offsets are device data: a sequence outside [0, total) or longer than the stated maximum
+    // is reported (DEV_BAD_INDEX) and skipped, so no store leaves the output
+    if (seq0 < 0 || SN < 0 || SN > P.N || seq0 > P.total - SN) {
+      if (threadIdx.x == 0 && qt == 0) flag_device_error(DEV_BAD_INDEX);
+      return;
+    }
+    if (qt * BM >= SN) return;  // a tile past this sequence's end: nothing to do (uniform)
+  }
+  const int n_kv_all = (SN + BN - 1) / BN;
   const int n = causal ? min(qt + 1, n_kv_all) : n_kv_all;  // BM == BN
   const int T = 2 * n;  // tiles over both passes
 
@@ -189,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r < 2; ++r)
         for (int c = 0; c < DQK / 64; ++c)
           tma_load_4d(sQ + r * C::kQMapBytes + c * C::kChunk, &tm_q, bar(bars.q_full),
-                      q_col_of(P, r) + 64 * c, q_head_of(P, u, r), qt * BM, b);
+                      q_col_of(P, r) + 64 * c, q_head_of(P, u, r), seq0 + qt * BM, tb);
       int issued = 0;  // loads issued into the ring
       auto acquire = [&](int idx, uint32_t bytes) -> int {
         const int slot = idx % NSLOT;
@@ -209,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int c = 0; c < DQK / 64; ++c)
               tma_load_4d(sSlot + ks * C::kSlot + c * C::kChunk, &tm_k, bar(bars.slot_full[ks]),
-                          k_col_of(P, r) + 64 * c, kvh, j * BN, b);
+                          k_col_of(P, r) + 64 * c, kvh, seq0 + j * BN, tb);
             issued = k_load(t, r) + 1;
           }
         }
@@ -223,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int c = 0; c < DV / 64; ++c)
               tma_load_4d(sSlot + vs * C::kSlot + c * C::kVHalfChunk, &tm_v,
-                          bar(bars.slot_full[vs]), 64 * c, kvh, jv * BN + 64 * h, b);
+                          bar(bars.slot_full[vs]), 64 * c, kvh, seq0 + jv * BN + 64 * h, tb);
             issued = v_load(jv, h) + 1;
           }
         }
@@ -311,7 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = qt * BM + r;
     const uint32_t tl = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const float sl2 = kp.scale_log2;
-    const int lim = causal ? min(row + 1, P.N) : P.N;  // keys [0, lim) are visible
+    const int lim = causal ? min(row + 1, SN) : SN;  // keys [0, lim) are visible
+    // output row on the token axis: packed (seq0 + row) or batched (b * N + row)
+    const size_t orow = P.cu_seqlens ? static_cast<size_t>(seq0) + row
+                                     : static_cast<size_t>(b) * P.N + row;
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
     float bias[2] = {0.f, 0.f}, lam = 0.f;
     bool ok = true, merged = false;
@@ -492,13 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (P.flags & 4) scale *= (1.f - P.lambda_init);
     if (ok) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P.out) +
-                           ((static_cast<size_t>(b) * P.N + row) * P.units + u) * DV + c0;
+                           (orow * P.units + u) * DV + c0;
       const float* w = (P.flags & 2) && P.norm_w ? P.norm_w + c0 : nullptr;
 #pragma unroll 1
       for (int c = 0; c < HC / CW; ++c) {
         uint32_t o[CW];
         ld_o(c, o);
-        if (row < P.N) {
+        if (row < SN) {
 #pragma unroll
           for (int g = 0; g < CW / 8; ++g) {
             uint4 pkt;
@@ -515,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (P.o_pre) {  // training: the head output before the norm and scale
             __nv_bfloat16* op = static_cast<__nv_bfloat16*>(P.o_pre) +
-                                ((static_cast<size_t>(b) * P.N + row) * P.units + u) * DV + c0;
+                                (orow * P.units + u) * DV + c0;
 #pragma unroll
             for (int g = 0; g < CW / 8; ++g) {
               uint4 pkt;
@@ -591,9 +608,11 @@ template <int DQK, int DV, bool SHARED_K>
 static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
   using C = Cfg<DQK, DV, SHARED_K>;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, p.q_cols, p.q_heads, p.N, p.B, BM, err, err_len) ||
-      !make_map(&mk, p.k, p.k_cols, p.kv_heads, p.N, p.B, BN, err, err_len) ||
-      !make_map(&mv, p.v, DV, p.kv_heads, p.N, p.B, BN / 2, err, err_len))
+  // packed sequences: one batch row of `total` tokens; otherwise [B, N]
+  const int mN = p.cu_seqlens ? p.total : p.N, mB = p.cu_seqlens ? 1 : p.B;
+  if (!make_map(&mq, p.q, p.q_cols, p.q_heads, mN, mB, BM, err, err_len) ||
+      !make_map(&mk, p.k, p.k_cols, p.kv_heads, mN, mB, BN, err, err_len) ||
+      !make_map(&mv, p.v, DV, p.kv_heads, mN, mB, BN / 2, err, err_len))
     return cudaErrorInvalidValue;
   auto kern = prefill_exact_kernel<DQK, DV, SHARED_K>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);

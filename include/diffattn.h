@@ -73,8 +73,9 @@ DIFFATTN_API const char* diffattn_last_error_string(void);
 
 /* Synchronises `stream`, then reads and clears the device error flags that kernels set.
  * Returns DIFFATTN_OK, DIFFATTN_ERR_TIMEOUT (a bounded wait ran out since the last call),
- * DIFFATTN_ERR_INDEX (a paged decode met a block-table entry outside [0, num_pages): that access
- * read page 0 instead and the call's output is invalid), or DIFFATTN_ERR_CUDA. */
+ * DIFFATTN_ERR_INDEX (device-side offsets were out of range: a paged decode met a block-table
+ * entry outside [0, num_pages), and read page 0 instead; or a varlen prefill met a sequence
+ * outside [0, total), and skipped it; that call's output is invalid), or DIFFATTN_ERR_CUDA. */
 DIFFATTN_API int diffattn_device_status(void* stream);
 
 /* Diagnostics (not part of the method): launch one kernel whose bounded wait is certain to run
@@ -246,6 +247,27 @@ DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const vo
                                     const int* seqlens, const float* lam_logit, void* out, int B,
                                     int Lmax, int Hq, int Hkv, int d, int flags, int dtype,
                                     void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Variable-length prefill: diffattn_fwd over sequences of different lengths packed along the
+ * token axis (no padding), each attending only to itself (causally with DIFFATTN_CAUSAL). The
+ * pages give no batching scheme; the operator per sequence is that of diffattn_fwd.
+ *   q, k   : device [total, H, 2d];  v, out : device [total, H, dv]
+ *   cu_seqlens : device int32 [B + 1], cu_seqlens[0] = 0, non-decreasing, cu_seqlens[B] <= total;
+ *            sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (empty sequences allowed).
+ *            Checked on the device: a sequence outside [0, total) or longer than max_seqlen is
+ *            skipped and reported by diffattn_device_status() as DIFFATTN_ERR_INDEX.
+ *   max_seqlen : the longest sequence (sizes the grid)
+ *   lambda, lambda_init, norm_weight, eps, flags : as diffattn_fwd
+ * Rows of `out` that belong to no sequence are not written.
+ * Supported: dtype DIFFATTN_BF16 (tensor-core exact path), d in {64, 128}, dv = 2d.
+ * Errors: as diffattn_fwd.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
+                                     const int* cu_seqlens, int max_seqlen, int total,
+                                     const float* lambda, float lambda_init,
+                                     const float* norm_weight, float eps, int B, int H, int d,
+                                     int dv, int flags, int dtype, void* stream);
 
 /* ------------------------------------------------------------------------------------------
  * Prefill with lambda formed inside the kernel (pages "Differential Transformer: Noise-

@@ -194,6 +194,48 @@ def test_decode_matches_prefill_last_row():
 
 
 # ------------------------------------------------------------------------------------------
+# variable-length prefill
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("lens,causal", [([300, 1, 129, 0, 640], True), ([128, 256], False),
+                                         ([5, 77, 200], True)])
+def test_fwd_varlen(lens, causal):
+    """Packed sequences of mixed lengths (one key, empty, ragged tails, several tiles) against
+    the oracle, and each equal to the fixed-length prefill of that sequence alone."""
+    H = 2
+    total = sum(lens) + 3  # three trailing rows in no sequence
+    inp = make_prefill_inputs(1, total, H, 128, 256, seed=191 + len(lens), causal=causal)
+    q, k, v = inp.q[0], inp.k[0], inp.v[0]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    lam = torch.tensor([0.4, 0.8], dtype=torch.float32)
+    li = ref.lambda_init(12)
+    w = torch.linspace(0.8, 1.2, 256, dtype=torch.float32)
+    got = da.diffattn_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cu.to(DEV), lam.to(DEV), li,
+                                 norm_weight=w.to(DEV), causal=causal)
+    want = ref.diffattn_fwd_varlen(q, k, v, cu, lam.numpy(), li, norm_weight=w, causal=causal)
+    assert_bf16(got[:sum(lens)], want[:sum(lens)])
+    assert torch.count_nonzero(got[sum(lens):]) == 0  # rows in no sequence stay as they were
+    i = min(2, len(lens) - 1)
+    s0, n = int(cu[i]), lens[i]
+    one = da.diffattn_fwd(q[None, s0:s0 + n].contiguous().to(DEV), k[None, s0:s0 + n].contiguous().to(DEV),
+                          v[None, s0:s0 + n].contiguous().to(DEV), lam.to(DEV), li,
+                          norm_weight=w.to(DEV), causal=causal)
+    assert torch.equal(got[s0:s0 + n], one[0])
+
+
+def test_fwd_varlen_bad_offsets_are_reported():
+    """A sequence past the packed length is caught by the kernel's own check: skipped, nothing
+    faults, and the host sees DIFFATTN_ERR_INDEX."""
+    inp = make_prefill_inputs(1, 256, 1, 128, 256, seed=197)
+    cu = torch.tensor([0, 128, 400], dtype=torch.int32, device=DEV)  # 400 > total
+    da.diffattn_fwd_varlen(inp.q[0].to(DEV), inp.k[0].to(DEV), inp.v[0].to(DEV), cu,
+                           torch.tensor([0.5], device=DEV), 0.5, max_seqlen=256)
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_device_status()
+    assert e.value.status == -9  # DIFFATTN_ERR_INDEX
+    da.diffattn_device_status()
+
+
+# ------------------------------------------------------------------------------------------
 # decode over a paged cache
 # ------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("B,L,H,ps", [(3, 640, 2, 16), (2, 300, 2, 100), (2, 256, 1, 128), (3, 50, 2, 1)])
