@@ -617,7 +617,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "roofline": {"bound": "tensor", "achieved": btf, "peak": peak_tf, "unit": "TFLOP/s",
                          "frac": btf / peak_tf, "flops_per_launch": bflops,
                          "flops_per_pair": BWD_FLOPS_PER_PAIR,
-                         "issued_flops_per_pair": BWD_ISSUED_FLOPS_PER_PAIR},
+                         "issued_flops_per_pair": BWD_ISSUED_FLOPS_PER_PAIR,
+                         "traffic": profiled_traffic("backward_dkdq_3b.md",
+                                                     source_sha(["backward.cu", "ptx.cuh"])),
+                         "traffic_kernel": "bwd_dkdq_kernel (the largest of the five)"},
             "gpu_launches": 5 * n_steps}
         del inp, dy, saved, grads, ws
         torch.cuda.empty_cache()
@@ -656,7 +659,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                          "frac": gbs / hbm,
                          "traffic": profiled_traffic("v2_decode_32k.md",
-                                                     source_sha(["decode.cu", "ptx.cuh"])),
+                                                     source_sha(["decode_v2_tc.cu", "ptx.cuh"])),
                          "bytes_per_launch": nbytes,
                          "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
                          "timed": "diffattn_v2_decode call (split kernel + combine kernel)"},
