@@ -269,7 +269,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     import torch.distributed as dist
     import differential_attention_gb300 as da
     from synth import (make_decode_inputs, make_dout, make_lambda_vectors, make_prefill_inputs,
-                       make_v2_decode_inputs, make_v2_inputs)
+                       make_v2_decode_inputs, make_v2_inputs, to_fp8_e4m3)
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -522,6 +522,50 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del vinp, vout
         torch.cuda.empty_cache()
 
+    # ======================= prefill with fp8 scores =======================
+    if args.only in ("all", "fp8"):
+        c = PREFILL
+        inp = make_prefill_inputs(c["B"], c["N"], c["H"], c["d"], c["dv"], seed=9000 + rank,
+                                  layer=c["layer"], device=dev)
+        q8, qs = to_fp8_e4m3(inp.q)
+        k8, ks = to_fp8_e4m3(inp.k)
+        lam = torch.full((c["H"],), 0.6, dtype=torch.float32, device=dev)
+        li = da.diffattn_lambda_init(c["layer"])
+        out = torch.empty((c["B"], c["N"], c["H"], c["dv"]), dtype=torch.bfloat16, device=dev)
+
+        def f8step():
+            da.diffattn_fwd_fp8(q8, k8, inp.v, lam, qs, ks, li, out=out)
+
+        for _ in range(args.warmup):
+            f8step()
+        barrier()
+        n_steps = max(5, min(200, args.steps))
+        evs = [(ev(), ev()) for _ in range(n_steps)]
+        for i in range(n_steps):
+            evs[i][0].record(stream)
+            f8step()
+            evs[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        f8flops = prefill_flops()
+        f8tf = f8flops / (ms * 1e-3) / 1e12
+        # 1024 of the 1536 flops per pair are score products on the fp8 tensor cores (twice the
+        # bf16 rate by the nominal ratio), 512 the bf16 product with V: blended peak 1.5x bf16
+        blend = 1.5 * peak_tf
+        line["prefill_fp8"] = {
+            "metric": "DiffAttn fwd TFLOP/s", "value": world * f8tf, "unit": "TFLOP/s",
+            "ms_per_call": ms,
+            "workload": "prefill_3b (B4 N4096 H12 d128 dv256 causal) with fp8 e4m3 q and k "
+                        "(per-tensor absmax scale), bf16 v and output",
+            "roofline": {"bound": "tensor", "achieved": f8tf, "peak": blend, "unit": "TFLOP/s",
+                         "frac": f8tf / blend, "flops_per_launch": f8flops,
+                         "peak_source": "1.5 x bf16_tflops_sustained: scores at the fp8 rate "
+                                        "(2x bf16, nominal ratio), the V product at the bf16 rate"},
+            "gpu_launches": n_steps}
+        del inp, q8, k8, out
+        torch.cuda.empty_cache()
+
     # ======================= variable-length prefill (packed sequences) =======================
     if args.only in ("all", "varlen"):
         c = PREFILL
@@ -685,7 +729,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2", "v2_decode", "long", "backward", "varlen"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2", "v2_decode", "long", "backward", "varlen", "fp8"], default="all",
                     help="profiling aid: run one workload (the JSON line then lacks the others)")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="profiling aid: a smaller decode batch for captures that save device memory")

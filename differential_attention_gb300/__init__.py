@@ -69,6 +69,9 @@ _SIGNATURES = {
                                                                       ctypes.c_float]
                               + [ctypes.c_int] * 9 + [ctypes.c_void_p, ctypes.c_size_t,
                                                       ctypes.c_void_p]),
+    "diffattn_fwd_fp8": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_float] * 2
+                         + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
+                         + [ctypes.c_int] * 6 + [ctypes.c_void_p]),
     "diffattn_fwd_varlen": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 2
                             + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
                             + [ctypes.c_int] * 6 + [ctypes.c_void_p]),
@@ -491,4 +494,28 @@ def diffattn_fwd_varlen(q, k, v, cu_seqlens, lam, lambda_init: float = 0.0, max_
                                      _ptr(norm_weight), float(eps), B, H, d, dv,
                                      _train_flags(causal, norm, scale), DIFFATTN_BF16,
                                      _stream(stream)))
+    return out
+
+
+def diffattn_fwd_fp8(q8, k8, v, lam, q_descale: float, k_descale: float, lambda_init: float = 0.0,
+                     norm_weight=None, eps: float = 1e-5, causal: bool = True, norm: bool = True,
+                     scale: bool = True, out=None, stream=None):
+    """Prefill with fp8 e4m3 q and k (real values q8 * q_descale, k8 * k_descale) and bf16 v:
+    the score products run on the fp8 tensor cores."""
+    _dev("q8", q8, torch.float8_e4m3fn)
+    B, N, H, two_d = q8.shape
+    d = two_d // 2
+    _dev("k8", k8, torch.float8_e4m3fn)
+    _dev("v", v, torch.bfloat16)
+    dv = v.shape[-1]
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if out is None:
+        out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=v.device)
+    _dev("out", out, torch.bfloat16)
+    _check(lib().diffattn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v), _ptr(out), float(q_descale),
+                                  float(k_descale), _ptr(lam), float(lambda_init),
+                                  _ptr(norm_weight), float(eps), B, N, H, d, dv,
+                                  _train_flags(causal, norm, scale), _stream(stream)))
     return out

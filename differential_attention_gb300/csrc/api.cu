@@ -689,3 +689,51 @@ DIFFATTN_API int diffattn_fwd_varlen(const void* q, const void* k, const void* v
   p.total = total;
   return run_prefill(p, dtype, "diffattn_fwd_varlen", static_cast<cudaStream_t>(stream));
 }
+
+DIFFATTN_API int diffattn_fwd_fp8(const void* q, const void* k, const void* v, void* out,
+                                  float q_descale, float k_descale, const float* lambda,
+                                  float lambda_init, const float* norm_weight, float eps, int B,
+                                  int N, int H, int d, int dv, int flags, void* stream) {
+  if (!q || !k || !v || !out || !lambda) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_fp8: null pointer");
+  constexpr int kF8Flags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kF8Flags) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_fp8: unknown flag bits 0x%x", flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_fp8: eps must be > 0 with DIFFATTN_NORM");
+  if (!(q_descale > 0.f) || !(k_descale > 0.f) || !std::isfinite(q_descale) || !std::isfinite(k_descale))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_fp8: descale factors must be finite and > 0");
+  if (B < 1 || N < 1 || H < 1) return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_fp8: B, N, H must be >= 1");
+  if (d != 128 || dv != 256)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_fp8: need d = 128 and dv = 256 (got d=%d dv=%d)", d, dv);
+  const long long tiles = (static_cast<long long>(N) + 127) / 128 * B * H;
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(N) * H > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_fp8: problem too large for one launch");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_fwd_fp8: tensors must be 16-byte aligned");
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = N;
+  p.units = H;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_V1;
+  p.q_heads = H;
+  p.kv_heads = H;
+  p.q_cols = 2 * d;
+  p.k_cols = 2 * d;
+  p.group = 1;
+  p.lambda = lambda;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = q_descale * k_descale / std::sqrt(static_cast<float>(d));
+  p.qk_fp8 = true;
+  return run_prefill(p, DIFFATTN_BF16, "diffattn_fwd_fp8", static_cast<cudaStream_t>(stream));
+}

@@ -49,6 +49,9 @@ struct Problem {
   // the longest sequence (it sizes the grid) and `total` the packed length.
   const int* cu_seqlens;
   int total;
+  // q and k in fp8 e4m3 (V1, exact path): the score products run as kind::f8f6f4; `scale`
+  // then also carries the per-tensor dequantisation factors
+  bool qk_fp8;
 };
 
 // lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init for head u, from Problem::lam_vec.

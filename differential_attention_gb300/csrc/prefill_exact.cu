@@ -53,17 +53,24 @@ constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kSmemLimit = 232448;  // bytes of shared memory one CTA may use
 
-template <int DQK, int DV, bool SHARED_K>
+// QK8: q and k hold fp8 e4m3 (v stays bf16); the score products run as kind::f8f6f4.
+template <int DQK, int DV, bool SHARED_K, bool QK8 = false>
 struct Cfg {
-  static constexpr int kChunk = 128 * 128;              // 128 rows x 64 bf16 (one TMA box)
-  static constexpr int kQMapBytes = BM * DQK * 2;       // one map's Q tile
-  static constexpr int kKMapBytes = BN * DQK * 2;       // one map's K tile (one load)
+  static constexpr int kChunk = 128 * 128;              // 128 rows x 128 bytes (one TMA box)
+  static constexpr int kQKElt = QK8 ? 1 : 2;            // bytes per q/k element
+  static constexpr int kQKBoxCols = 128 / kQKElt;       // q/k elements per 128-byte box row
+  static constexpr int kQKBoxes = DQK * kQKElt / 128;   // boxes per map's Q or K tile
+  static constexpr int kQKSteps = DQK * kQKElt / 32;    // score MMA k-steps (32 bytes each)
+  static constexpr int kQMapBytes = BM * DQK * kQKElt;  // one map's Q tile
+  static constexpr int kKMapBytes = BN * DQK * kQKElt;  // one map's K tile
   static constexpr int kQBytes = 2 * kQMapBytes;
-  static constexpr int kKLoads = SHARED_K ? 1 : 2;      // K loads per key tile
+  // K loads per key tile: one per map, or one for both (shared K in V2; both fp8 maps in a slot)
+  static constexpr int kKLoads = (SHARED_K || QK8) ? 1 : 2;
+  static constexpr int kKLoadBytes = QK8 ? 2 * kKMapBytes : kKMapBytes;
   static constexpr int kVHalfChunk = (BN / 2) * 128;    // 64 keys x 64 bf16
   static constexpr int kVHalfBytes = (BN / 2) * DV * 2; // half of a V tile (one load)
   static constexpr int kDBytes = BM * BN * 2;           // D tile (bf16)
-  static constexpr int kSlot = kKMapBytes > kVHalfBytes ? kKMapBytes : kVHalfBytes;
+  static constexpr int kSlot = kKLoadBytes > kVHalfBytes ? kKLoadBytes : kVHalfBytes;
   static constexpr int kRingBudget = kSmemLimit - 2048 - 1024 - kQBytes - kDBytes;
   static constexpr int NSLOT = (kRingBudget / kSlot) > 8 ? 8 : (kRingBudget / kSlot);
   static constexpr int kQOff = 0;
@@ -93,12 +100,12 @@ struct KParams {
   float scale_log2;
 };
 
-template <int DQK, int DV, bool SHARED_K>
+template <int DQK, int DV, bool SHARED_K, bool QK8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_exact_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const KParams kp) {
-  using C = Cfg<DQK, DV, SHARED_K>;
+  using C = Cfg<DQK, DV, SHARED_K, QK8>;
   constexpr int NSLOT = C::NSLOT;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
@@ -201,9 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kvh = kv_head_of(P, u);
       mbar_arrive_expect_tx(bar(bars.q_full), C::kQBytes);
       for (int r = 0; r < 2; ++r)
-        for (int c = 0; c < DQK / 64; ++c)
+        for (int c = 0; c < C::kQKBoxes; ++c)
           tma_load_4d(sQ + r * C::kQMapBytes + c * C::kChunk, &tm_q, bar(bars.q_full),
-                      q_col_of(P, r) + 64 * c, q_head_of(P, u, r), seq0 + qt * BM, tb);
+                      q_col_of(P, r) + C::kQKBoxCols * c, q_head_of(P, u, r), seq0 + qt * BM, tb);
       int issued = 0;  // loads issued into the ring
       auto acquire = [&](int idx, uint32_t bytes) -> int {
         const int slot = idx % NSLOT;
@@ -216,14 +223,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < T) {
           const int j = t < n ? t : t - n;
           for (int r = 0; r < KL && ok; ++r) {
-            const int ks = acquire(k_load(t, r), C::kKMapBytes);
+            const int ks = acquire(k_load(t, r), C::kKLoadBytes);
             if (ks < 0) {
               ok = false;
               break;
             }
-            for (int c = 0; c < DQK / 64; ++c)
-              tma_load_4d(sSlot + ks * C::kSlot + c * C::kChunk, &tm_k, bar(bars.slot_full[ks]),
-                          k_col_of(P, r) + 64 * c, kvh, seq0 + j * BN, tb);
+            for (int mp = QK8 ? 0 : r; mp <= (QK8 ? 1 : r); ++mp)  // maps in this load
+              for (int c = 0; c < C::kQKBoxes; ++c)
+                tma_load_4d(sSlot + ks * C::kSlot + (QK8 ? mp * C::kKMapBytes : 0) + c * C::kChunk,
+                            &tm_k, bar(bars.slot_full[ks]), k_col_of(P, mp) + C::kQKBoxCols * c,
+                            kvh, seq0 + j * BN, tb);
             issued = k_load(t, r) + 1;
           }
         }
@@ -250,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ================================ MMA issuer ==================================
     if (lane == 0) {
-      constexpr uint32_t idesc_s = umma_idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t idesc_s = QK8 ? umma_idesc_e4m3(BM, BN) : umma_idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idesc_o = umma_idesc_bf16(BM, DV, 0, 1);
       // Descriptors are built once; each k-step adds a constant offset.
       const uint64_t dq0 = umma_smem_desc(sQ, 16, 1024);
@@ -270,20 +279,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const int ki = k_load(t, SHARED_K ? 0 : r), s = ki % NSLOT;
+            const int ki = k_load(t, (SHARED_K || QK8) ? 0 : r), s = ki % NSLOT;
             if (r < KL) {
               if (!(ok = mbar_wait(bar(bars.slot_full[s]), (ki / NSLOT) & 1, abrt))) break;
               tc_fence_after();
             }
             const uint32_t d_s = tmem + buf * 256 + r * 128;
             const uint64_t qd = desc_add(dq0, r * C::kQMapBytes);
-            const uint64_t kd = desc_add(dslot0, s * C::kSlot);
+            const uint64_t kd = desc_add(dslot0, s * C::kSlot + (QK8 ? r * C::kKMapBytes : 0));
 #pragma unroll
-            for (int kk = 0; kk < DQK / 16; ++kk) {
+            for (int kk = 0; kk < C::kQKSteps; ++kk) {
               const uint32_t off = (kk >> 2) * C::kChunk + (kk & 3) * 32;
-              mma_bf16_ss(d_s, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0 ? 1u : 0u);
+              if constexpr (QK8)
+                mma_e4m3_ss(d_s, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0 ? 1u : 0u);
+              else
+                mma_bf16_ss(d_s, desc_add(qd, off), desc_add(kd, off), idesc_s, kk > 0 ? 1u : 0u);
             }
-            if (r == 1 || !SHARED_K) tc_commit(bar(bars.slot_empty[s]));
+            if (r == 1 || (!SHARED_K && !QK8)) tc_commit(bar(bars.slot_empty[s]));
           }
           if (!ok) break;
           tc_commit(bar(bars.s_full[buf]));
@@ -583,18 +595,19 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 // 4-D bf16 map over [B, N, heads, cols] with a 64-col x 1 x box_rows x 1 box, 128-byte swizzle,
 // zero fill out of bounds.
 static bool make_map(CUtensorMap* m, const void* base, int cols, int heads, int N, int B,
-                     int box_rows, char* err, size_t err_len) {
+                     int box_rows, char* err, size_t err_len, int elt = 2) {
   auto fn = get_encode_fn();
   if (!fn) {
     snprintf(err, err_len, "cuTensorMapEncodeTiled entry point unavailable");
     return false;
   }
   cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)heads, (cuuint64_t)N, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * heads * 2,
-                           (cuuint64_t)cols * heads * 2 * (cuuint64_t)N};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)cols * elt, (cuuint64_t)cols * heads * elt,
+                           (cuuint64_t)cols * heads * elt * (cuuint64_t)N};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / elt), 1, (cuuint32_t)box_rows, 1};  // 128-byte rows
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(m, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                  const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -604,17 +617,17 @@ static bool make_map(CUtensorMap* m, const void* base, int cols, int heads, int 
   return true;
 }
 
-template <int DQK, int DV, bool SHARED_K>
+template <int DQK, int DV, bool SHARED_K, bool QK8 = false>
 static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
-  using C = Cfg<DQK, DV, SHARED_K>;
+  using C = Cfg<DQK, DV, SHARED_K, QK8>;
   CUtensorMap mq, mk, mv;
   // packed sequences: one batch row of `total` tokens; otherwise [B, N]
   const int mN = p.cu_seqlens ? p.total : p.N, mB = p.cu_seqlens ? 1 : p.B;
-  if (!make_map(&mq, p.q, p.q_cols, p.q_heads, mN, mB, BM, err, err_len) ||
-      !make_map(&mk, p.k, p.k_cols, p.kv_heads, mN, mB, BN, err, err_len) ||
+  if (!make_map(&mq, p.q, p.q_cols, p.q_heads, mN, mB, BM, err, err_len, C::kQKElt) ||
+      !make_map(&mk, p.k, p.k_cols, p.kv_heads, mN, mB, BN, err, err_len, C::kQKElt) ||
       !make_map(&mv, p.v, DV, p.kv_heads, mN, mB, BN / 2, err, err_len))
     return cudaErrorInvalidValue;
-  auto kern = prefill_exact_kernel<DQK, DV, SHARED_K>;
+  auto kern = prefill_exact_kernel<DQK, DV, SHARED_K, QK8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   KParams kp;
@@ -623,7 +636,7 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
   kp.scale_log2 = kLog2e * p.scale;
   {
     // K/V bytes one (batch, unit) pair streams; keep a group's K/V within ~64 MB of L2
-    const double kv_bytes = static_cast<double>(p.N) * (p.k_cols + DV) * 2.0;
+    const double kv_bytes = static_cast<double>(p.N) * (p.k_cols * C::kQKElt + DV * 2.0);
     long long g = static_cast<long long>((64.0 * 1024 * 1024) / (kv_bytes > 1 ? kv_bytes : 1));
     const long long bu = static_cast<long long>(p.B) * p.units;
     kp.group = static_cast<int>(g < 1 ? 1 : (g > bu ? bu : g));
@@ -640,6 +653,10 @@ cudaError_t status_prefill_exact(int* v) { return read_clear_status(v); }
 
 cudaError_t launch_prefill_exact(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
   if (p.mode == MODE_V1) {
+    if (p.qk_fp8) {
+      if (p.dqk == 128 && p.dv == 256) return exact::launch_cfg<128, 256, false, true>(p, s, err, err_len);
+      return cudaErrorNotSupported;
+    }
     if (p.dqk == 128 && p.dv == 256) return exact::launch_cfg<128, 256, false>(p, s, err, err_len);
     if (p.dqk == 64 && p.dv == 128) return exact::launch_cfg<64, 128, false>(p, s, err, err_len);
   } else {

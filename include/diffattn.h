@@ -270,6 +270,25 @@ DIFFATTN_API int diffattn_fwd_varlen(const void* q, const void* k, const void* v
                                      int dv, int flags, int dtype, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Prefill with fp8 scores (page "Differential Transformer: softmax can't say zero, so it
+ * subtracts", on the attention logits quantized to low bit widths: DIFF's logits are several
+ * times smaller relative to their spread, so low-bit score products cost it little).
+ * diffattn_fwd where q and k hold fp8 e4m3 values with one dequantisation factor each:
+ *   q, k : device fp8 e4m3 [B, N, H, 2d] = [Q1 | Q2], [K1 | K2]; the real values are
+ *          q * q_descale and k * k_descale (per tensor, finite, > 0)
+ *   v, out : device bf16 as for diffattn_fwd
+ * The score products Q_m K_m^T run on the fp8 tensor cores (tcgen05 kind::f8f6f4, fp32
+ * accumulation); the two softmaxes, the subtraction, the product with V (bf16), the norm and the
+ * scale are those of diffattn_fwd.
+ * Supported: d = 128, dv = 256; flags DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE.
+ * Errors: as diffattn_fwd.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_fwd_fp8(const void* q, const void* k, const void* v, void* out,
+                                  float q_descale, float k_descale, const float* lambda,
+                                  float lambda_init, const float* norm_weight, float eps, int B,
+                                  int N, int H, int d, int dv, int flags, void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * Prefill with lambda formed inside the kernel (pages "Differential Transformer: Noise-
  * Canceling Attention by Subtraction", section "Making lambda learnable and stable", and
  * "Differential Transformer: softmax can't say zero, so it subtracts", section "lambda,

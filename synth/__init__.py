@@ -15,4 +15,5 @@ from .workloads import (  # noqa: F401
     make_v2_decode_inputs,
     make_v2_inputs,
     page_cache,
+    to_fp8_e4m3,
 )

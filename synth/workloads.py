@@ -234,3 +234,11 @@ def page_cache(k_cache: torch.Tensor, v_cache: torch.Tensor, page_size: int, see
     k_pool[slot_d] = k_cache.reshape(B * mp, page_size, H, wk)
     v_pool[slot_d] = v_cache.reshape(B * mp, page_size, H, wv)
     return k_pool, v_pool, slot.reshape(B, mp).to(torch.int32).to(k_cache.device)
+
+
+def to_fp8_e4m3(x: torch.Tensor):
+    """Per-tensor absmax cast to fp8 e4m3: returns (x8, descale) with x ~= x8 * descale (the
+    largest magnitude maps to 448, the format's largest finite value)."""
+    amax = float(x.float().abs().max())
+    descale = amax / 448.0 if amax > 0 else 1.0
+    return (x.float() / descale).to(torch.float8_e4m3fn), descale

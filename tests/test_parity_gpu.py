@@ -10,7 +10,7 @@ import torch
 import differential_attention_gb300 as da
 from oracle import diffattn_ref as ref
 from synth import (make_decode_inputs, make_lambda_vectors, make_prefill_inputs, make_tiny_inputs,
-                   make_v2_decode_inputs, make_v2_inputs, page_cache)
+                   make_v2_decode_inputs, make_v2_inputs, page_cache, to_fp8_e4m3)
 from tests.gpu_util import assert_bf16, assert_fp32, errors
 
 pytestmark = pytest.mark.gpu
@@ -191,6 +191,27 @@ def test_decode_matches_prefill_last_row():
     dec = da.diffattn_decode(q[:, -1].contiguous(), k, v, lam, 0.5)
     max_abs, rel = errors(dec, pre[:, -1])
     assert rel < 2e-2 and max_abs < 4e-2
+
+
+# ------------------------------------------------------------------------------------------
+# fp8 scores
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("B,N,H,causal", [(1, 300, 2, True), (2, 129, 1, False), (1, 640, 1, True)])
+def test_fwd_fp8(B, N, H, causal):
+    """fp8 e4m3 q and k: the oracle runs on exactly the dequantised fp8 values, so the bar is the
+    bf16 prefill's."""
+    inp = make_prefill_inputs(B, N, H, 128, 256, seed=211 + N, causal=causal)
+    q8, qs = to_fp8_e4m3(inp.q)
+    k8, ks = to_fp8_e4m3(inp.k)
+    lam = np.linspace(0.3, 0.8, H)
+    li = ref.lambda_init(12)
+    w = torch.linspace(0.8, 1.2, 256, dtype=torch.float32)
+    got = da.diffattn_fwd_fp8(q8.to(DEV), k8.to(DEV), inp.v.to(DEV),
+                              torch.tensor(lam, dtype=torch.float32, device=DEV), qs, ks, li,
+                              norm_weight=w.to(DEV), causal=causal)
+    want = ref.diffattn_fwd(q8.float() * qs, k8.float() * ks, inp.v, lam, li, norm_weight=w,
+                            causal=causal)
+    assert_bf16(got, want)
 
 
 # ------------------------------------------------------------------------------------------
