@@ -69,6 +69,9 @@ _SIGNATURES = {
                                                                       ctypes.c_float]
                               + [ctypes.c_int] * 9 + [ctypes.c_void_p, ctypes.c_size_t,
                                                       ctypes.c_void_p]),
+    "diffattn_fwd_strided": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.POINTER(ctypes.c_longlong)]
+                             + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
+                             + [ctypes.c_int] * 7 + [ctypes.c_void_p]),
     "diffattn_fwd_fp8": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_float] * 2
                          + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
                          + [ctypes.c_int] * 6 + [ctypes.c_void_p]),
@@ -518,4 +521,38 @@ def diffattn_fwd_fp8(q8, k8, v, lam, q_descale: float, k_descale: float, lambda_
                                   float(k_descale), _ptr(lam), float(lambda_init),
                                   _ptr(norm_weight), float(eps), B, N, H, d, dv,
                                   _train_flags(causal, norm, scale), _stream(stream)))
+    return out
+
+
+def _strided(name, t, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != 4 or t.stride(-1) != 1:
+        raise ValueError(f"{name} must be 4-D [B, N, H, width] with a contiguous last dimension")
+    return list(t.stride()[:3])
+
+
+def diffattn_fwd_strided(q, k, v, lam, lambda_init: float = 0.0, norm_weight=None,
+                         eps: float = 1e-5, causal: bool = True, norm: bool = True,
+                         scale: bool = True, cuda_cores: bool = False, out=None, stream=None):
+    """diffattn_fwd over strided views (e.g. q, k, v = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+    of a fused [B, N, 3, H, 2d] projection); `out` may be a strided view too."""
+    B, N, H, two_d = q.shape
+    d = two_d // 2
+    dv = v.shape[-1]
+    st = _strided("q", q) + _strided("k", k, q.dtype) + _strided("v", v, q.dtype)
+    if out is None:
+        out = torch.empty((B, N, H, dv), dtype=q.dtype, device=q.device)
+    st += _strided("out", out, q.dtype)
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    arr = (ctypes.c_longlong * 12)(*st)
+    flags = ((DIFFATTN_CAUSAL if causal else 0) | (DIFFATTN_NORM if norm else 0)
+             | (DIFFATTN_SCALE if scale else 0) | (DIFFATTN_CUDA_CORES if cuda_cores else 0))
+    _check(lib().diffattn_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(out), arr, _ptr(lam),
+                                      float(lambda_init), _ptr(norm_weight), float(eps), B, N, H,
+                                      d, dv, flags, _code(q.dtype), _stream(stream)))
     return out

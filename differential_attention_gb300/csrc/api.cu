@@ -117,7 +117,10 @@ DIFFATTN_API int diffattn_lambda(const float* lq1, const float* lk1, const float
 }
 
 static int run_prefill(da::Problem& p, int dtype, const char* name, cudaStream_t s) {
+  da::fill_dense_strides(p);
   const bool simt = (p.flags & DIFFATTN_CUDA_CORES) || dtype == DIFFATTN_FP32;
+  if ((p.flags & DIFFATTN_SINGLE_PASS) && !simt && !da::dense_strides(p))
+    return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: DIFFATTN_SINGLE_PASS needs dense tensors", name);
   if (simt) {
     cudaError_t e = da::launch_prefill_simt(p, dtype == DIFFATTN_BF16, s);
     if (e != cudaSuccess) return cuda_fail(e, name);
@@ -736,4 +739,63 @@ DIFFATTN_API int diffattn_fwd_fp8(const void* q, const void* k, const void* v, v
   p.scale = q_descale * k_descale / std::sqrt(static_cast<float>(d));
   p.qk_fp8 = true;
   return run_prefill(p, DIFFATTN_BF16, "diffattn_fwd_fp8", static_cast<cudaStream_t>(stream));
+}
+
+DIFFATTN_API int diffattn_fwd_strided(const void* q, const void* k, const void* v, void* out,
+                                      const long long* strides, const float* lambda,
+                                      float lambda_init, const float* norm_weight, float eps,
+                                      int B, int N, int H, int d, int dv, int flags, int dtype,
+                                      void* stream) {
+  if (!strides) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_strided: null strides");
+  if (!q || !k || !v || !out || !lambda) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_strided: null pointer");
+  if (flags & ~kPrefillFlags) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_strided: unknown flag bits 0x%x", flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_strided: eps must be > 0 with DIFFATTN_NORM");
+  if (dtype != DIFFATTN_BF16 && dtype != DIFFATTN_FP32)
+    return fail(DIFFATTN_ERR_DTYPE, "diffattn_fwd_strided: dtype must be DIFFATTN_BF16 or DIFFATTN_FP32");
+  if (B < 1 || N < 1 || H < 1) return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_strided: B, N, H must be >= 1");
+  if (!(d == 64 || d == 128) || dv != 2 * d)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_strided: need d in {64, 128} and dv = 2d");
+  const long long tiles = (static_cast<long long>(N) + 127) / 128 * B * H;
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(N) * H > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_strided: problem too large for one launch");
+  // strides: positive, and multiples of 16 bytes (the tensor-map rule) for bf16
+  const long long align_elems = dtype == DIFFATTN_BF16 ? 8 : 4;
+  for (int i = 0; i < 12; ++i)
+    if (strides[i] < 1 || strides[i] % align_elems != 0 || strides[i] > (1LL << 36))
+      return fail(DIFFATTN_ERR_ALIGN, "diffattn_fwd_strided: stride %d (%lld) must be a positive multiple of 16 bytes", i, strides[i]);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_fwd_strided: tensors must be 16-byte aligned");
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = N;
+  p.units = H;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_V1;
+  p.q_heads = H;
+  p.kv_heads = H;
+  p.q_cols = 2 * d;
+  p.k_cols = 2 * d;
+  p.group = 1;
+  p.lambda = lambda;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  for (int i = 0; i < 3; ++i) {
+    p.qs[i] = strides[i];
+    p.ks[i] = strides[3 + i];
+    p.vs[i] = strides[6 + i];
+    p.os[i] = strides[9 + i];
+  }
+  return run_prefill(p, dtype, "diffattn_fwd_strided", static_cast<cudaStream_t>(stream));
 }

@@ -52,7 +52,36 @@ struct Problem {
   // q and k in fp8 e4m3 (V1, exact path): the score products run as kind::f8f6f4; `scale`
   // then also carries the per-tensor dequantisation factors
   bool qk_fp8;
+  // element strides (batch, token, head) of q, k, v and out; the last dimension is contiguous.
+  // All zero: the dense layout (filled in by fill_dense_strides).
+  long long qs[3], ks[3], vs[3], os[3];
 };
+
+__host__ inline void fill_dense_strides(Problem& p) {
+  if (p.qs[2] != 0) return;
+  auto dense = [&](long long (&s)[3], int heads, int cols) {
+    s[2] = cols;
+    s[1] = static_cast<long long>(heads) * cols;
+    s[0] = s[1] * p.N;
+  };
+  dense(p.qs, p.q_heads, p.q_cols);
+  dense(p.ks, p.kv_heads, p.k_cols);
+  dense(p.vs, p.kv_heads, p.dv);
+  dense(p.os, p.units, p.dv);
+}
+__host__ inline bool dense_strides(const Problem& p) {
+  Problem d = p;
+  d.qs[2] = 0;
+  fill_dense_strides(d);
+  for (int i = 0; i < 3; ++i)
+    if (d.qs[i] != p.qs[i] || d.ks[i] != p.ks[i] || d.vs[i] != p.vs[i] || d.os[i] != p.os[i])
+      return false;
+  return true;
+}
+__host__ __device__ inline size_t elem_off(const long long (&s)[3], long long b, long long n,
+                                           long long h) {
+  return static_cast<size_t>(b * s[0] + n * s[1] + h * s[2]);
+}
 
 // lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init for head u, from Problem::lam_vec.
 // Called by a whole warp (lanes split the dot products); every lane gets the value.

@@ -338,9 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const float sl2 = kp.scale_log2;
     const int lim = causal ? min(row + 1, SN) : SN;  // keys [0, lim) are visible
-    // output row on the token axis: packed (seq0 + row) or batched (b * N + row)
+    // output row on the token axis: packed (seq0 + row) or batched (b * N + row); `oaddr` is
+    // the row's element offset in the (possibly strided) output
     const size_t orow = P.cu_seqlens ? static_cast<size_t>(seq0) + row
                                      : static_cast<size_t>(b) * P.N + row;
+    const size_t oaddr = P.cu_seqlens ? elem_off(P.os, 0, seq0 + row, u) : elem_off(P.os, b, row, u);
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
     float bias[2] = {0.f, 0.f}, lam = 0.f;
     bool ok = true, merged = false;
@@ -521,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (P.flags & 4) scale *= (1.f - P.lambda_init);
     if (ok) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P.out) +
-                           (orow * P.units + u) * DV + c0;
+                           oaddr + c0;
       const float* w = (P.flags & 2) && P.norm_w ? P.norm_w + c0 : nullptr;
 #pragma unroll 1
       for (int c = 0; c < HC / CW; ++c) {
@@ -595,15 +597,17 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 // 4-D bf16 map over [B, N, heads, cols] with a 64-col x 1 x box_rows x 1 box, 128-byte swizzle,
 // zero fill out of bounds.
 static bool make_map(CUtensorMap* m, const void* base, int cols, int heads, int N, int B,
-                     int box_rows, char* err, size_t err_len, int elt = 2) {
+                     const long long (&st)[3], int box_rows, char* err, size_t err_len,
+                     int elt = 2) {
   auto fn = get_encode_fn();
   if (!fn) {
     snprintf(err, err_len, "cuTensorMapEncodeTiled entry point unavailable");
     return false;
   }
   cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)heads, (cuuint64_t)N, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)cols * elt, (cuuint64_t)cols * heads * elt,
-                           (cuuint64_t)cols * heads * elt * (cuuint64_t)N};
+  // element strides (batch, token, head) -> byte strides of dims 1..3 (head, token, batch)
+  cuuint64_t strides[3] = {(cuuint64_t)st[2] * elt, (cuuint64_t)st[1] * elt,
+                           (cuuint64_t)st[0] * elt};
   cuuint32_t box[4] = {(cuuint32_t)(128 / elt), 1, (cuuint32_t)box_rows, 1};  // 128-byte rows
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
@@ -623,9 +627,9 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
   CUtensorMap mq, mk, mv;
   // packed sequences: one batch row of `total` tokens; otherwise [B, N]
   const int mN = p.cu_seqlens ? p.total : p.N, mB = p.cu_seqlens ? 1 : p.B;
-  if (!make_map(&mq, p.q, p.q_cols, p.q_heads, mN, mB, BM, err, err_len, C::kQKElt) ||
-      !make_map(&mk, p.k, p.k_cols, p.kv_heads, mN, mB, BN, err, err_len, C::kQKElt) ||
-      !make_map(&mv, p.v, DV, p.kv_heads, mN, mB, BN / 2, err, err_len))
+  if (!make_map(&mq, p.q, p.q_cols, p.q_heads, mN, mB, p.qs, BM, err, err_len, C::kQKElt) ||
+      !make_map(&mk, p.k, p.k_cols, p.kv_heads, mN, mB, p.ks, BN, err, err_len, C::kQKElt) ||
+      !make_map(&mv, p.v, DV, p.kv_heads, mN, mB, p.vs, BN / 2, err, err_len))
     return cudaErrorInvalidValue;
   auto kern = prefill_exact_kernel<DQK, DV, SHARED_K, QK8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);

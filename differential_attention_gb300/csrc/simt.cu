@@ -128,8 +128,7 @@ __global__ void __launch_bounds__(kSimtRows * 32)
   const T* v = static_cast<const T*>(p.v);
   const int d = p.dqk, dv = p.dv;
   for (int r = 0; r < 2; ++r) {
-    const size_t qo = (static_cast<size_t>(b) * p.N + i) * p.q_heads + q_head_of(p, u, r);
-    const T* qr = q + qo * p.q_cols + q_col_of(p, r);
+    const T* qr = q + elem_off(p.qs, b, i, q_head_of(p, u, r)) + q_col_of(p, r);
     for (int c = lane; c < d; c += 32) sq[warp][r][c] = ldf(qr + c);
   }
   __syncwarp();
@@ -137,8 +136,7 @@ __global__ void __launch_bounds__(kSimtRows * 32)
   const int kvh = kv_head_of(p, u);
   const int kend = (p.flags & 1) ? (i + 1) : p.N;
   auto krow = [&](int j, int r) {
-    const size_t ko = (static_cast<size_t>(b) * p.N + j) * p.kv_heads + kvh;
-    return k + ko * p.k_cols + k_col_of(p, r);
+    return k + elem_off(p.ks, b, j, kvh) + k_col_of(p, r);
   };
   auto score = [&](int j, int r) {
     const T* kr = krow(j, r);
@@ -190,8 +188,7 @@ __global__ void __launch_bounds__(kSimtRows * 32)
     const int cnt = min(32, kend - j0);
     for (int jj = 0; jj < cnt; ++jj) {
       const float wj = __shfl_sync(0xffffffffu, w, jj);
-      const size_t vo = (static_cast<size_t>(b) * p.N + j0 + jj) * p.kv_heads + kvh;
-      const T* vr = v + vo * dv;
+      const T* vr = v + elem_off(p.vs, b, j0 + jj, kvh);
 #pragma unroll
       for (int c = 0; c < kMaxC; ++c)
         if (c < ncol) acc[c] = fmaf(wj, ldf(vr + lane + 32 * c), acc[c]);
@@ -212,7 +209,7 @@ __global__ void __launch_bounds__(kSimtRows * 32)
   }
   const float sc = (p.flags & 4) ? (1.f - p.lambda_init) : 1.f;
   T* out = static_cast<T*>(p.out);
-  const size_t oo = ((static_cast<size_t>(b) * p.N + i) * p.units + u) * dv;
+  const size_t oo = elem_off(p.os, b, i, u);
 #pragma unroll
   for (int c = 0; c < kMaxC; ++c)
     if (c < ncol) out[oo + lane + 32 * c] = from_f<T>(acc[c] * sc);

@@ -249,6 +249,24 @@ DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const vo
                                     void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Prefill over strided tensors: diffattn_fwd where q, k, v and out may be views, e.g. slices of
+ * one fused projection output [B, N, 3, H, 2d]. The last dimension of each tensor is
+ * contiguous; the others are given as element strides:
+ *   strides : host int64 [12] = {q: batch, token, head,  k: batch, token, head,
+ *                                v: batch, token, head,  out: batch, token, head}
+ *             each a positive multiple of 16 bytes (8 bf16 or 4 fp32 elements)
+ * Other arguments as diffattn_fwd. DIFFATTN_SINGLE_PASS needs the dense layout (ERR_UNSUPPORTED
+ * otherwise); the default tensor-core path and the CUDA-core path take any strides. Elements of
+ * `out` outside the addressed rows and columns are not written.
+ * Errors: as diffattn_fwd.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_fwd_strided(const void* q, const void* k, const void* v, void* out,
+                                      const long long* strides, const float* lambda,
+                                      float lambda_init, const float* norm_weight, float eps,
+                                      int B, int N, int H, int d, int dv, int flags, int dtype,
+                                      void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * Variable-length prefill: diffattn_fwd over sequences of different lengths packed along the
  * token axis (no padding), each attending only to itself (causally with DIFFATTN_CAUSAL). The
  * pages give no batching scheme; the operator per sequence is that of diffattn_fwd.

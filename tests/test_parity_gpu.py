@@ -194,6 +194,31 @@ def test_decode_matches_prefill_last_row():
 
 
 # ------------------------------------------------------------------------------------------
+# strided views (a fused QKV projection)
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype,cuda_cores", [("bf16", False), ("bf16", True), ("fp32", False)])
+def test_fwd_strided_fused_qkv(dtype, cuda_cores):
+    """q, k, v as slices of one [B, N, 3, H, 256] tensor and out as the first half of a
+    [B, N, H, 512] buffer: the same result as the dense layout, the rest of the buffer untouched."""
+    B, N, H = 2, 300, 2
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    inp = make_prefill_inputs(B, N, H, 128, 256, seed=221, dtype=tdt)
+    qkv = torch.stack([inp.q, inp.k, inp.v], dim=2).to(DEV)  # [B, N, 3, H, 256]
+    buf = torch.zeros((B, N, H, 512), dtype=tdt, device=DEV)
+    lam = np.array([0.4, 0.8])
+    li = ref.lambda_init(12)
+    got = da.diffattn_fwd_strided(qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2],
+                                  torch.tensor(lam, dtype=torch.float32, device=DEV), li,
+                                  cuda_cores=cuda_cores, out=buf[..., :256])
+    want = ref.diffattn_fwd(inp.q, inp.k, inp.v, lam, li)
+    if dtype == "bf16":
+        assert_bf16(got, want)
+    else:
+        assert_fp32(got, want)
+    assert torch.count_nonzero(buf[..., 256:]) == 0
+
+
+# ------------------------------------------------------------------------------------------
 # fp8 scores
 # ------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("B,N,H,causal", [(1, 300, 2, True), (2, 129, 1, False), (1, 640, 1, True)])
