@@ -69,6 +69,11 @@ _SIGNATURES = {
                                                                       ctypes.c_float]
                               + [ctypes.c_int] * 9 + [ctypes.c_void_p, ctypes.c_size_t,
                                                       ctypes.c_void_p]),
+    "diffattn_fwd_host_workspace_size": (ctypes.c_int, [ctypes.c_int] * 5
+                                         + [ctypes.POINTER(ctypes.c_size_t)]),
+    "diffattn_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int] * 3
+                          + [ctypes.c_void_p, ctypes.c_float] + [ctypes.c_int] * 6
+                          + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_fwd_strided": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.POINTER(ctypes.c_longlong)]
                              + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
                              + [ctypes.c_int] * 7 + [ctypes.c_void_p]),
@@ -555,4 +560,37 @@ def diffattn_fwd_strided(q, k, v, lam, lambda_init: float = 0.0, norm_weight=Non
     _check(lib().diffattn_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(out), arr, _ptr(lam),
                                       float(lambda_init), _ptr(norm_weight), float(eps), B, N, H,
                                       d, dv, flags, _code(q.dtype), _stream(stream)))
+    return out
+
+
+def diffattn_fwd_host_workspace_size(B: int, N: int, H: int, d: int, dv: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().diffattn_fwd_host_workspace_size(B, N, H, d, dv, ctypes.byref(n)))
+    return n.value
+
+
+def diffattn_fwd_host(q, k, v, out, lq1, lk1, lq2, lk2, layer: int, norm_weight=None,
+                      eps: float = 1e-5, causal: bool = True, norm: bool = True, scale: bool = True,
+                      workspace=None, stream=None):
+    """The layer's forward with q, k, v and out in page-locked host memory; copies in and out are
+    pipelined against the prefill of other chunks. Returns `out` (filled when the stream is done)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a contiguous bf16 host tensor")
+    B, N, H, two_d = q.shape
+    d = two_d // 2
+    dv = v.shape[-1]
+    vecs = [lq1, lk1, lq2, lk2]
+    for i, t in enumerate(vecs):
+        _dev(f"lambda vector {i}", t, torch.float32)
+    sets, dim = vecs[0].shape
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if workspace is None:
+        workspace = torch.empty(diffattn_fwd_host_workspace_size(B, N, H, d, dv), dtype=torch.uint8,
+                                device=lq1.device)
+    _check(lib().diffattn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), *[_ptr(t) for t in vecs],
+                                   dim, sets, int(layer), _ptr(norm_weight), float(eps), B, N, H, d,
+                                   dv, _train_flags(causal, norm, scale), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)))
     return out

@@ -799,3 +799,101 @@ DIFFATTN_API int diffattn_fwd_strided(const void* q, const void* k, const void* 
   }
   return run_prefill(p, dtype, "diffattn_fwd_strided", static_cast<cudaStream_t>(stream));
 }
+
+namespace {
+// one chunk of diffattn_fwd_host: the fused-lambda exact prefill on device slot buffers
+cudaError_t host_chunk_prefill(const da::HostPipeArgs& a, const void* q, const void* k,
+                               const void* v, void* out, int nb, cudaStream_t s, void* ctx) {
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = nb;
+  p.N = a.N;
+  p.units = a.H;
+  p.dqk = a.d;
+  p.dv = a.dv;
+  p.mode = da::MODE_V1;
+  p.q_heads = a.H;
+  p.kv_heads = a.H;
+  p.q_cols = 2 * a.d;
+  p.k_cols = 2 * a.d;
+  p.group = 1;
+  p.norm_w = a.norm_w;
+  p.eps = a.eps;
+  p.lambda_init = diffattn_lambda_init(a.layer);
+  p.flags = a.flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(a.d));
+  for (int i = 0; i < 4; ++i) p.lam_vec[i] = a.lam_vec[i];
+  p.lam_dim = a.lam_dim;
+  p.lam_sets = a.lam_sets;
+  da::fill_dense_strides(p);
+  char* err = static_cast<char*>(ctx);
+  return da::launch_prefill_exact(p, s, err, 256);
+}
+}  // namespace
+
+DIFFATTN_API int diffattn_fwd_host_workspace_size(int B, int N, int H, int d, int dv, size_t* bytes) {
+  if (!bytes) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_host_workspace_size: null pointer");
+  if (B < 1 || N < 1 || H < 1 || !(d == 64 || d == 128) || dv != 2 * d)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_host_workspace_size: need B, N, H >= 1, d in {64, 128}, dv = 2d");
+  *bytes = da::host_workspace_bytes(B, N, H, d, dv);
+  return ok();
+}
+
+DIFFATTN_API int diffattn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                                   void* out_host, const float* lq1, const float* lk1,
+                                   const float* lq2, const float* lk2, int lambda_dim,
+                                   int lambda_sets, int layer, const float* norm_weight,
+                                   float eps, int B, int N, int H, int d, int dv, int flags,
+                                   void* workspace, size_t ws_bytes, void* stream) {
+  if (!q_host || !k_host || !v_host || !out_host || !lq1 || !lk1 || !lq2 || !lk2)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_host: null pointer");
+  constexpr int kHostFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kHostFlags) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_host: unknown flag bits 0x%x", flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_host: eps must be > 0 with DIFFATTN_NORM");
+  if (layer < 1) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_host: layer must be >= 1");
+  if (lambda_dim < 1 || lambda_dim > 4096 || !(lambda_sets == 1 || lambda_sets == H))
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_host: need 1 <= lambda_dim <= 4096 and lambda_sets in {1, H}");
+  if (B < 1 || N < 1 || H < 1) return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_host: B, N, H must be >= 1");
+  if (!(d == 64 || d == 128) || dv != 2 * d)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_host: need d in {64, 128} and dv = 2d");
+  if (static_cast<long long>(N) * H > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_fwd_host: problem too large for one launch");
+  if (!aligned(lq1, 4) || !aligned(lk1, 4) || !aligned(lq2, 4) || !aligned(lk2, 4) ||
+      (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_fwd_host: tensors must be aligned");
+  const size_t need = da::host_workspace_bytes(B, N, H, d, dv);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(DIFFATTN_ERR_WORKSPACE, "diffattn_fwd_host: need a 256-byte aligned workspace of %zu bytes", need);
+  int rc = check_device();
+  if (rc) return rc;
+  da::HostPipeArgs a{};
+  a.q = q_host;
+  a.k = k_host;
+  a.v = v_host;
+  a.out = out_host;
+  a.B = B;
+  a.N = N;
+  a.H = H;
+  a.d = d;
+  a.dv = dv;
+  a.workspace = workspace;
+  a.lam_vec[0] = lq1;
+  a.lam_vec[1] = lk1;
+  a.lam_vec[2] = lq2;
+  a.lam_vec[3] = lk2;
+  a.lam_dim = lambda_dim;
+  a.lam_sets = lambda_sets;
+  a.layer = layer;
+  a.norm_w = norm_weight;
+  a.eps = eps;
+  a.flags = flags;
+  char err[256] = {0};
+  cudaError_t e = da::launch_host_pipeline(a, static_cast<cudaStream_t>(stream), host_chunk_prefill, err);
+  if (err[0]) return fail(DIFFATTN_ERR_CUDA, "diffattn_fwd_host: %s", err);
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_fwd_host");
+  return ok();
+}

@@ -1,0 +1,128 @@
+// host_pipeline.cu -- prefill straight from host buffers, copies overlapped with compute.
+//
+// diffattn_fwd_host takes q, k, v and out in (pinned) host memory. The batch is cut into chunks
+// of whole sequences; two chunk slots in the caller's device workspace are used in turn. Per chunk:
+//   copy stream : wait until the slot's previous chunk has been computed, copy q, k, v in
+//   caller stream: wait for the copies, run the prefill on the chunk (lambda formed in the kernel)
+//   out stream  : wait for the prefill, copy the chunk's output back
+// so chunk c + 1 is copied in while chunk c computes and chunk c - 1 is copied out. The caller's
+// stream finally waits for the last copy out, so the call is asynchronous on that stream like
+// every other entry point. Streams and events are created once per device and reused.
+#include <mutex>
+
+#include "internal.h"
+
+namespace da {
+namespace {
+
+struct DevicePipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t copied[2], computed[2], drained[2], done;
+};
+
+constexpr int kMaxDevices = 64;
+DevicePipe g_pipes[kMaxDevices];
+std::mutex g_pipe_mutex;
+
+cudaError_t get_pipe(DevicePipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_pipe_mutex);
+  DevicePipe& p = g_pipes[dev];
+  if (!p.ready) {
+    if ((e = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    for (int i = 0; i < 2; ++i) {
+      if ((e = cudaEventCreateWithFlags(&p.copied[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+      if ((e = cudaEventCreateWithFlags(&p.computed[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+      if ((e = cudaEventCreateWithFlags(&p.drained[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    if ((e = cudaEventCreateWithFlags(&p.done, cudaEventDisableTiming)) != cudaSuccess) return e;
+    p.ready = true;
+  }
+  *out = &p;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+int host_chunk_sequences(int B, int N, int H) {
+  // smallest chunk that still fills every SM about twice with CTAs (128-row tiles x heads)
+  const long long per_seq = static_cast<long long>((N + 127) / 128) * H;
+  long long cb = (2LL * 152 + per_seq - 1) / (per_seq > 0 ? per_seq : 1);
+  if (cb < 1) cb = 1;
+  if (cb > B) cb = B;
+  return static_cast<int>(cb);
+}
+
+size_t host_workspace_bytes(int B, int N, int H, int d, int dv) {
+  const int cb = host_chunk_sequences(B, N, H);
+  const size_t rows = static_cast<size_t>(cb) * N * H;
+  const size_t slot = rows * (2 * d + 2 * d + dv + dv) * 2;  // q, k, v, out (bf16)
+  return 2 * ((slot + 255) & ~static_cast<size_t>(255));
+}
+
+// `run` launches the prefill of one chunk (B = cb sequences) on `stream` with device pointers.
+cudaError_t launch_host_pipeline(const HostPipeArgs& a, cudaStream_t stream,
+                                 cudaError_t (*run)(const HostPipeArgs&, const void*, const void*,
+                                                    const void*, void*, int, cudaStream_t, void*),
+                                 void* ctx) {
+  DevicePipe* pp = nullptr;
+  cudaError_t e = get_pipe(&pp);
+  if (e != cudaSuccess) return e;
+  DevicePipe& p = *pp;
+  // one call at a time enqueues on this device's shared copy streams and events
+  std::lock_guard<std::mutex> lock(g_pipe_mutex);
+  const int cb = host_chunk_sequences(a.B, a.N, a.H);
+  const size_t seq_q = static_cast<size_t>(a.N) * a.H * 2 * a.d * 2;  // bytes of one sequence
+  const size_t seq_v = static_cast<size_t>(a.N) * a.H * a.dv * 2;
+  const size_t slot_bytes = host_workspace_bytes(a.B, a.N, a.H, a.d, a.dv) / 2;
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  const char* qh = static_cast<const char*>(a.q);
+  const char* kh = static_cast<const char*>(a.k);
+  const char* vh = static_cast<const char*>(a.v);
+  char* oh = static_cast<char*>(a.out);
+
+  // the slots' previous users are from an earlier call on this device: start after the caller's
+  // earlier work (the copy streams are non-blocking)
+  if ((e = cudaEventRecord(p.done, stream)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(p.in, p.done, 0)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(p.out, p.done, 0)) != cudaSuccess) return e;
+
+  const int chunks = (a.B + cb - 1) / cb;
+  for (int c = 0; c < chunks; ++c) {
+    const int s = c & 1;
+    const int b0 = c * cb, nb = (a.B - b0) < cb ? (a.B - b0) : cb;
+    uint8_t* slot = ws + s * slot_bytes;
+    uint8_t* dq = slot;
+    uint8_t* dk = dq + cb * seq_q;
+    uint8_t* dvv = dk + cb * seq_q;
+    uint8_t* dout = dvv + cb * seq_v;
+    // inputs of chunk c may overwrite the slot once chunk c - 2 has been computed
+    if (c >= 2 && (e = cudaStreamWaitEvent(p.in, p.computed[s], 0)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(dq, qh + b0 * seq_q, nb * seq_q, cudaMemcpyHostToDevice, p.in)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(dk, kh + b0 * seq_q, nb * seq_q, cudaMemcpyHostToDevice, p.in)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(dvv, vh + b0 * seq_v, nb * seq_v, cudaMemcpyHostToDevice, p.in)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(p.copied[s], p.in)) != cudaSuccess) return e;
+    // compute: its inputs are in, and the slot's output buffer has been drained (chunk c - 2)
+    if ((e = cudaStreamWaitEvent(stream, p.copied[s], 0)) != cudaSuccess) return e;
+    if (c >= 2 && (e = cudaStreamWaitEvent(stream, p.drained[s], 0)) != cudaSuccess) return e;
+    if ((e = run(a, dq, dk, dvv, dout, nb, stream, ctx)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(p.computed[s], stream)) != cudaSuccess) return e;
+    // copy the chunk's output back
+    if ((e = cudaStreamWaitEvent(p.out, p.computed[s], 0)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(oh + b0 * seq_v, dout, nb * seq_v, cudaMemcpyDeviceToHost, p.out)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(p.drained[s], p.out)) != cudaSuccess) return e;
+  }
+  // the caller's stream completes with the last copy out; the input stream is joined too so that
+  // a later call cannot start copying into a slot this call still reads
+  if ((e = cudaEventRecord(p.done, p.out)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(stream, p.done, 0)) != cudaSuccess) return e;
+  if ((e = cudaEventRecord(p.done, p.in)) != cudaSuccess) return e;
+  return cudaStreamWaitEvent(stream, p.done, 0);
+}
+
+}  // namespace da

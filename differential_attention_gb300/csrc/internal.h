@@ -168,6 +168,27 @@ cudaError_t launch_v2_decode_tc(const V2DecodeArgs& a, cudaStream_t s, char* err
 cudaError_t launch_v2_combine(const V2DecodeArgs& a, int splits, cudaStream_t s);
 cudaError_t status_v2_decode_tc(int* v);
 
+// Prefill from host buffers with the copies pipelined against compute (host_pipeline.cu).
+struct HostPipeArgs {
+  const void* q;  // host [B, N, H, 2d]
+  const void* k;  // host [B, N, H, 2d]
+  const void* v;  // host [B, N, H, dv]
+  void* out;      // host [B, N, H, dv]
+  int B, N, H, d, dv;
+  void* workspace;  // device, host_workspace_bytes()
+  const float* lam_vec[4];
+  int lam_dim, lam_sets, layer;
+  const float* norm_w;
+  float eps;
+  int flags;
+};
+int host_chunk_sequences(int B, int N, int H);
+size_t host_workspace_bytes(int B, int N, int H, int d, int dv);
+cudaError_t launch_host_pipeline(const HostPipeArgs& a, cudaStream_t stream,
+                                 cudaError_t (*run)(const HostPipeArgs&, const void*, const void*,
+                                                    const void*, void*, int, cudaStream_t, void*),
+                                 void* ctx);
+
 // Backward of the V1 prefill (d = 128, dv = 256, bf16).
 struct BackwardArgs {
   const void* q;

@@ -249,6 +249,32 @@ DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const vo
                                     void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Prefill straight from host memory (not part of the method; the serving path around it): the
+ * layer's forward of diffattn_fwd_fused_lambda with q, k, v and out in host memory. The batch is
+ * cut into chunks of whole sequences that pass through two slots of `workspace` in turn; the
+ * copies in and out run on two library-owned streams and overlap the prefill of the previous or
+ * next chunk, which runs on `stream`.
+ *   q_host, k_host : host [B, N, H, 2d] bf16;  v_host, out_host : host [B, N, H, dv] bf16.
+ *                    Page-locked (cudaHostAlloc / cudaHostRegister) memory is needed for the
+ *                    copies to overlap; all four must stay valid until `stream` completes.
+ *   lq1 .. lk2, lambda_dim, lambda_sets, layer, norm_weight, eps, flags :
+ *                    device data and meaning as diffattn_fwd_fused_lambda
+ *   workspace, ws_bytes : device, >= diffattn_fwd_host_workspace_size(), 256-byte aligned, not
+ *                    shared with a call that can run at the same time
+ * The call returns once everything is enqueued; `stream` then completes after the last output
+ * copy. Calls on one device serialise on the library's copy streams.
+ * Supported: d in {64, 128}, dv = 2d. Errors: as diffattn_fwd_fused_lambda, plus ERR_WORKSPACE.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_fwd_host_workspace_size(int B, int N, int H, int d, int dv,
+                                                  size_t* bytes);
+DIFFATTN_API int diffattn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                                   void* out_host, const float* lq1, const float* lk1,
+                                   const float* lq2, const float* lk2, int lambda_dim,
+                                   int lambda_sets, int layer, const float* norm_weight,
+                                   float eps, int B, int N, int H, int d, int dv, int flags,
+                                   void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * Prefill over strided tensors: diffattn_fwd where q, k, v and out may be views, e.g. slices of
  * one fused projection output [B, N, 3, H, 2d]. The last dimension of each tensor is
  * contiguous; the others are given as element strides:
