@@ -469,3 +469,53 @@ def test_v2_single_pass():
                              single_pass=True)
     want = ref.diffattn_v2_fwd(inp.q, inp.k, inp.v, inp.lam_logit)
     assert_bf16(got, want)
+
+
+# ------------------------------------------------------------------------------------------
+# CUDA graphs: every entry point only enqueues kernels (no allocation, no synchronisation), so
+# a decode step or a layer's prefill can be captured once and replayed
+# ------------------------------------------------------------------------------------------
+def test_cuda_graph_capture_and_replay():
+    inp = make_prefill_inputs(2, 300, 2, 128, 256, seed=241)
+    vecs = [t.to(DEV).contiguous() for t in inp.lam_vectors]
+    q, k, v = inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV)
+    dinp = make_decode_inputs(3, 700, 2, 128, 256, seed=242, ragged=True)
+    dq, dk, dv = dinp.q.to(DEV), dinp.k_cache.to(DEV), dinp.v_cache.to(DEV)
+    dl, ds = dinp.lam.to(DEV), dinp.seqlens.to(DEV)
+    v2 = make_v2_decode_inputs(2, 500, 16, 2, 128, seed=243, ragged=True)
+    v2q, v2k, v2v = v2.q.to(DEV), v2.k_cache.to(DEV), v2.v_cache.to(DEV)
+    v2l, v2s = v2.lam_logit.to(DEV), v2.seqlens.to(DEV)
+    li = da.diffattn_lambda_init(12)
+    out_p = torch.empty((2, 300, 2, 256), dtype=torch.bfloat16, device=DEV)
+    out_d = torch.empty((3, 2, 256), dtype=torch.bfloat16, device=DEV)
+    out_v = torch.empty((2, 8, 128), dtype=torch.bfloat16, device=DEV)
+    ws_d = torch.empty(da.diffattn_decode_workspace_size(3, 700, 2), dtype=torch.uint8, device=DEV)
+    ws_v = torch.empty(da.diffattn_v2_decode_workspace_size(2, 500, 16, 2, 128), dtype=torch.uint8,
+                       device=DEV)
+
+    def step(stream=None):
+        da.diffattn_fwd_fused_lambda(q, k, v, *vecs, layer=12, out=out_p, stream=stream)
+        da.diffattn_decode(dq, dk, dv, dl, li, seqlens=ds, workspace=ws_d, out=out_d, stream=stream)
+        da.diffattn_v2_decode(v2q, v2k, v2v, v2l, seqlens=v2s, workspace=ws_v, out=out_v,
+                              stream=stream)
+
+    step()  # eager reference (also loads the kernels before capture)
+    torch.cuda.synchronize()
+    want = [t.clone() for t in (out_p, out_d, out_v)]
+    for t in (out_p, out_d, out_v):
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step(stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        for t in (out_p, out_d, out_v):
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for got, w in zip((out_p, out_d, out_v), want):
+            assert torch.equal(got, w)
+    da.diffattn_device_status()
