@@ -124,3 +124,110 @@ def test_binding_requires_cuda_tensors():
     q = torch.zeros(1, 8, 1, 256, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         da.diffattn_fwd(q, q, q, torch.zeros(1), 0.5)
+
+
+def test_v2_decode_validation(L):
+    n = ctypes.c_size_t(0)
+    assert L.diffattn_v2_decode_workspace_size(64, 32768, 64, 8, 128, ctypes.byref(n)) == 0
+    need = n.value
+    assert L.diffattn_v2_decode_workspace_size(1, 16, 6, 1, 128, ctypes.byref(n)) == -2  # group 6
+
+    def v2d(q=FAKE, Hq=64, Hkv=8, d=128, dtype=0, flags=0, ws=FAKE, ws_bytes=need):
+        return L.diffattn_v2_decode(q, FAKE, FAKE, None, FAKE, FAKE, 64, 32768, Hq, Hkv, d, flags,
+                                    dtype, ws, ws_bytes, None)
+
+    assert v2d(q=None) == -1
+    assert v2d(flags=2) == -1
+    assert v2d(Hq=24, Hkv=8) == -2
+    assert v2d(d=64) == -2
+    assert v2d(dtype=1) == -3
+    assert v2d(q=ODD) == -4
+    assert v2d(ws_bytes=need - 1) == -8
+
+
+def test_training_validation(L):
+    def train(q=FAKE, stats=FAKE, d=128, dv=256, flags=7, dtype=0):
+        return L.diffattn_fwd_train(q, FAKE, FAKE, FAKE, FAKE, stats, FAKE, 0.5, None, 1e-5, 1, 16,
+                                    1, d, dv, flags, dtype, None)
+
+    assert train(q=None) == -1
+    assert train(flags=8) == -1          # DIFFATTN_CUDA_CORES has no training path
+    assert train(d=64, dv=128) == -2
+    assert train(dtype=1) == -3
+    assert train(stats=ODD) == -4
+    n = ctypes.c_size_t(0)
+    assert L.diffattn_bwd_workspace_size(4, 4096, 12, 128, 256, ctypes.byref(n)) == 0
+    need = n.value
+
+    def bwd(q=FAKE, dlam=FAKE, ws=FAKE, ws_bytes=need, N=4096):
+        return L.diffattn_bwd(q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.5, None, 1e-5, FAKE, FAKE,
+                              FAKE, dlam, None, 4, N, 12, 128, 256, 7, 0, ws, ws_bytes, None)
+
+    assert bwd(q=None) == -1
+    assert bwd(dlam=None) == -1
+    assert bwd(N=0) == -2
+    assert bwd(q=ODD) == -4
+    assert bwd(ws_bytes=need - 1) == -8
+
+
+def test_fused_lambda_varlen_fp8_strided_validation(L):
+    def fused(layer=12, dim=128, sets=1, H=2, flags=7):
+        return L.diffattn_fwd_fused_lambda(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dim, sets,
+                                           layer, None, 1e-5, 1, 16, H, 128, 256, flags, 0, None)
+
+    assert fused(layer=0) == -1
+    assert fused(dim=0) == -2
+    assert fused(sets=3, H=2) == -2      # one lambda set per head, or one for all
+    assert fused(flags=8) == -1
+
+    def varlen(maxlen=16, total=32, cu=FAKE):
+        return L.diffattn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, cu, maxlen, total, FAKE, 0.5, None,
+                                     1e-5, 2, 1, 128, 256, 7, 0, None)
+
+    assert varlen(cu=None) == -1
+    assert varlen(maxlen=64, total=32) == -2
+    assert varlen(cu=ctypes.c_void_p(0x10002)) == -4
+
+    def fp8(qd=1.0, d=128):
+        return L.diffattn_fwd_fp8(FAKE, FAKE, FAKE, FAKE, qd, 1.0, FAKE, 0.5, None, 1e-5, 1, 16, 1,
+                                  d, 2 * d, 7, None)
+
+    assert fp8(qd=0.0) == -1
+    assert fp8(qd=float("inf")) == -1
+    assert fp8(d=64) == -2
+
+    def strided(st):
+        arr = (ctypes.c_longlong * 12)(*st)
+        return L.diffattn_fwd_strided(FAKE, FAKE, FAKE, FAKE, arr, FAKE, 0.5, None, 1e-5, 1, 16, 1,
+                                      128, 256, 7, 0, None)
+
+    dense = [16 * 256, 256, 256] * 4
+    assert strided([s if i != 4 else 260 for i, s in enumerate(dense)]) == -4  # not 16-byte
+    assert strided([s if i != 0 else 0 for i, s in enumerate(dense)]) == -4
+    assert L.diffattn_fwd_strided(FAKE, FAKE, FAKE, FAKE, None, FAKE, 0.5, None, 1e-5, 1, 16, 1, 128,
+                                  256, 7, 0, None) == -1
+
+
+def test_paged_and_host_validation(L):
+    n = ctypes.c_size_t(0)
+    assert L.diffattn_decode_workspace_size(2, 64 * 16, 2, 128, 256, ctypes.byref(n)) == 0
+    need = n.value
+
+    def paged(table=FAKE, ps=16, mp=64, npages=200, ws_bytes=need):
+        return L.diffattn_decode_paged(FAKE, FAKE, FAKE, table, FAKE, FAKE, FAKE, 0.5, None, 1e-5, 2,
+                                       2, 128, 256, npages, ps, mp, 6, 0, FAKE, ws_bytes, None)
+
+    assert paged(table=None) == -1
+    assert paged(ps=0) == -2
+    assert paged(table=ctypes.c_void_p(0x10002)) == -4
+    assert paged(ws_bytes=need - 1) == -8
+    assert L.diffattn_fwd_host_workspace_size(4, 4096, 12, 128, 256, ctypes.byref(n)) == 0
+    hneed = n.value
+
+    def host(q=FAKE, layer=12, ws_bytes=hneed):
+        return L.diffattn_fwd_host(q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 1, layer, None,
+                                   1e-5, 4, 4096, 12, 128, 256, 7, FAKE, ws_bytes, None)
+
+    assert host(q=None) == -1
+    assert host(layer=0) == -1
+    assert host(ws_bytes=hneed - 1) == -8
