@@ -19,7 +19,8 @@
 //   bwd_dkdq_kernel   tcgen05, key-major, one map per CTA: S = Q K^T, dW = dO V^T per inner
 //                     tile, dS in shared memory, dK += dS^T Q (TMEM), dQ partial = dS K (TMEM)
 //                     added to the fp32 accumulator with TMA tensor reductions.
-//   bwd_dv_kernel     tcgen05, key-major: S1^T, S2^T -> W^T in shared memory, dV += W^T dO.
+//   bwd_dv_kernel     tcgen05, key-major: S1, S2 per inner tile -> W in shared memory,
+//                     dV += W^T dO.
 //   bwd_finish_kernel dQ fp32 -> bf16; dlam and norm-weight sums (fixed order: deterministic).
 // TMEM is 512 columns per SM; each tensor-core kernel fills it exactly:
 //   delta: S double-buffered (2 x 128) + O2 (256);  dkdq: S^T, dW^T, dK, dQ (4 x 128);
@@ -810,10 +811,12 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
 }
 
 // =============================================================================================
-// bwd_dv_kernel: one CTA per (key tile j, b, h); key-major. Warps 0 (TMA), 1 (MMA, TMEM), 2-9:
-// two warpgroups, thread r = key row, query columns [64 wg, 64 wg + 64).
-// TMEM: S1^T cols 0-127, S2^T 128-255, dV 256-511. Shared memory: K1_j, K2_j (64 KB) stay;
-// Q1_i | Q2_i (64 KB, with b1, b2) and dO_i (64 KB) one slot each; W^T tile 32 KB.
+// bwd_dv_kernel: one CTA per (key tile j, b, h); key-major over the CTAs, each inner tile
+// query-major like the dK/dQ kernel. Warps 0 (TMA), 1 (MMA, TMEM), 2-9: two warpgroups, thread
+// r = query row r, key columns [64 wg, 64 wg + 64).
+// TMEM: S1 cols 0-127, S2 128-255, dV 256-511. Shared memory: K1_j, K2_j (64 KB) stay;
+// Q1_i | Q2_i (64 KB, with b1, b2) and dO_i (64 KB) one slot each; the W tile ([query][key],
+// 32 KB), read MN-major as W^T for dV.
 // MMA order per inner tile: S_{t+1} (as soon as the Q slot refills) before dV_t.
 // =============================================================================================
 namespace vv {
@@ -920,12 +923,12 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = umma_idesc_bf16(kT, kT, 0, 0);
-      constexpr uint32_t idesc_v = umma_idesc_bf16(kT, kDV, 0, 1);
+      constexpr uint32_t idesc_s = umma_idesc_bf16(kT, kT, 0, 0);   // S_m = Q_m K_m^T
+      constexpr uint32_t idesc_v = umma_idesc_bf16(kT, kDV, 1, 1);  // W^T (MN) x dO (MN)
       const uint64_t dK0 = umma_smem_desc(sK, 16, 1024);
       const uint64_t dQ0 = umma_smem_desc(sQ, 16, 1024);
       const uint64_t dDOmn = umma_smem_desc(sDO, kBox, 1024);
-      const uint64_t dW0 = umma_smem_desc(sW, 16, 1024);
+      const uint64_t dWmn = umma_smem_desc(sW, kBox, 1024);
       auto issue_s = [&](int t) -> bool {
         if (!mbar_wait(bar(cs.q_full), t & 1, abrt)) return false;
         if (t > 0 && !mbar_wait(bar(cs.s_free), (t - 1) & 1, abrt)) return false;
@@ -935,7 +938,7 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = mp * 2 * kBox + (kk >> 2) * kBox + (kk & 3) * 32;
-            mma_bf16_ss(tmem + mp * kT, desc_add(dK0, off), desc_add(dQ0, off), idesc_s,
+            mma_bf16_ss(tmem + mp * kT, desc_add(dQ0, off), desc_add(dK0, off), idesc_s,
                         kk > 0 ? 1u : 0u);
           }
         tc_commit(bar(cs.q_empty));
@@ -952,8 +955,8 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)  // dV += W^T dO  (K = queries)
-          mma_bf16_ss(tmem + 2 * kT, desc_add(dW0, (kk >> 2) * kBox + (kk & 3) * 32),
-                      desc_add(dDOmn, kk * 2048), idesc_v, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ss(tmem + 2 * kT, desc_add(dWmn, kk * 2048), desc_add(dDOmn, kk * 2048),
+                      idesc_v, (t > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bar(cs.w_empty));
         tc_commit(bar(cs.do_empty));
       }
@@ -962,12 +965,15 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
       mbar_wait(bar(cs.teardown), 0, nullptr);
     }
   } else {
+    // thread r = query row r of the inner tile (key columns [64 wg, 64 wg + 64)): the row's b1
+    // and b2 are per-thread constants; for the dV readout, TMEM lane r = key row r
     const int wg = (warp - 2) >> 2;
     const int q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const int key = j * kT + r;
     const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
     const float lam = a.lambda[h];
+    const uint64_t c2 = f2pack(a.c_log2, a.c_log2), nlam2 = f2pack(-lam, -lam);
     const uint32_t w_row = sW + wg * kBox + r * 128;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
@@ -977,34 +983,42 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s1[2][32], s2[2][32];
-      tmem_ld32(tmem + tl + 64 * wg, s1[0]);
-      tmem_ld32(tmem + tl + 64 * wg + 32, s1[1]);
-      tmem_ld32(tmem + tl + kT + 64 * wg, s2[0]);
-      tmem_ld32(tmem + tl + kT + 64 * wg + 32, s2[1]);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(cs.s_free));
       const float* bb = bbase + (t & 1) * 2 * kT;
+      const float nb1 = -bb[r], nb2 = -bb[kT + r];
+      mbar_arrive(bar(cs.b_empty[t & 1]));  // this buffer of b1, b2 may be refilled (tile t + 2)
+      const uint64_t nb1_2 = f2pack(nb1, nb1), nb2_2 = f2pack(nb2, nb2);
+      const int qq = i * kT + r;
+      const bool edge = (j + 1) * kT > a.N || (i + 1) * kT > a.N || (a.causal && i == j);
       uint32_t pk[32];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
+        uint32_t s1[32], s2[32];
+        tmem_ld32(tmem + tl + 64 * wg + 32 * hh, s1);
+        tmem_ld32(tmem + tl + kT + 64 * wg + 32 * hh, s2);
+        tmem_wait_ld();
+        if (hh == 1) {
+          tc_fence_before();
+          mbar_arrive(bar(cs.s_free));  // both score tiles are in registers
+        }
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float wv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = 64 * wg + 32 * hh + e + u;
-            const int qq = i * kT + col;
-            const bool valid = key < a.N && qq < a.N && (!a.causal || qq >= key);
-            const float p1 = ex2_approx(fmaf(__uint_as_float(s1[hh][e + u]), a.c_log2, -bb[col]));
-            const float p2 = ex2_approx(fmaf(__uint_as_float(s2[hh][e + u]), a.c_log2, -bb[kT + col]));
-            wv[u] = valid ? fmaf(-lam, p2, p1) : 0.f;
+          float x0, x1, y0, y1;
+          f2unpack(f2fma(f2pack(__uint_as_float(s1[e]), __uint_as_float(s1[e + 1])), c2, nb1_2), x0, x1);
+          f2unpack(f2fma(f2pack(__uint_as_float(s2[e]), __uint_as_float(s2[e + 1])), c2, nb2_2), y0, y1);
+          float w0, w1;
+          f2unpack(f2fma(f2pack(ex2_approx(y0), ex2_approx(y1)), nlam2,
+                         f2pack(ex2_approx(x0), ex2_approx(x1))),
+                   w0, w1);
+          if (edge) {
+            const int kk0 = j * kT + 64 * wg + 32 * hh + e;
+            const bool v0 = kk0 < a.N && qq < a.N && (!a.causal || qq >= kk0);
+            const bool v1 = kk0 + 1 < a.N && qq < a.N && (!a.causal || qq >= kk0 + 1);
+            w0 = v0 ? w0 : 0.f;
+            w1 = v1 ? w1 : 0.f;
           }
-          pk[16 * hh + (e >> 1)] = pack_bf16x2(wv[0], wv[1]);
+          pk[16 * hh + (e >> 1)] = pack_bf16x2(w0, w1);
         }
       }
-      mbar_arrive(bar(cs.b_empty[t & 1]));  // this buffer of b1, b2 may be refilled (tile t + 2)
       if (t > 0) {
         ok = mbar_wait(bar(cs.w_empty), (t - 1) & 1, abrt);
         ok = __all_sync(0xffffffffu, ok);
