@@ -36,6 +36,8 @@ DECODE = dict(B=64, L=32768, H=12, d=128, dv=256, layer=12)
 V2 = dict(B=2, N=8192, Hq=64, Hkv=8, d=128)
 V2_DECODE = dict(B=64, L=32768, Hq=64, Hkv=8, d=128)
 LONG = dict(B=1, N=65536, H=12, d=128, dv=256, layer=24)
+PREFILL_WORKLOAD = ("prefill_3b: B4 N4096 H12 d128 dv256 causal, lambda (layer 12, formed in the "
+                    "kernel) + DiffAttn + RMSNorm + (1 - lambda_init)")
 FLOPS_PER_PAIR = 1536        # 4d + 4dv MMA flops per causal (query, key) pair, V1
 FLOPS_PER_PAIR_DEF = 1024    # 4d + 2dv: the definition (A1 - lambda A2) V
 V2_FLOPS_PER_PAIR = 8 * 128  # per (query, key) pair of one differential pair: 2 heads x (QK + PV)
@@ -252,8 +254,9 @@ def run_reference(args, rank: int, world: int):
         "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "prefill_3b: B4 N4096 H12 d128 dv256 causal (bounded row sample per step)",
-                   "global_batch": PREFILL["B"], "seq_len": PREFILL["N"], "parallelism": "none (host cores)"},
+        "config": {"workload": PREFILL_WORKLOAD, "global_batch": PREFILL["B"],
+                   "seq_len": PREFILL["N"], "parallelism": "none (host cores)",
+                   "flops_per_pair": FLOPS_PER_PAIR},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"per step: {desc}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -329,8 +332,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         line.update({
             "value": world * flops / (ms_per_step * 1e-3) / 1e12,
             "ms_per_step": ms_per_step,
-            "config": {"workload": "prefill_3b: B4 N4096 H12 d128 dv256 causal, lambda (layer 12, "
-                                   "formed in the kernel) + DiffAttn + RMSNorm + (1 - lambda_init)",
+            "config": {"workload": PREFILL_WORKLOAD,
                        "global_batch": PREFILL["B"] * world, "seq_len": PREFILL["N"],
                        "parallelism": f"replicas x{world} (independent batches, no collective)",
                        "l2": "inputs larger than L2 (q, k, v = 302 MB per rank)",
