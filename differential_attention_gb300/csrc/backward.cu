@@ -28,7 +28,6 @@
 // Every wait is bounded (2 s); a timeout flags DEV_TIMEOUT in this file's status word and the
 // roles unwind without hanging.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include <cstdio>
 
@@ -1105,64 +1104,25 @@ __global__ void __launch_bounds__(256) bwd_finish_kernel(const Args a, long long
 // ---------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult res;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &res) == cudaSuccess &&
-        res == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // 4-D bf16 map over [B, N, H, cols], box 64 x 1 x rows x 1, 128-byte swizzle, zero fill.
 static bool make_map(CUtensorMap* m, const void* base, int cols, int H, int N, int B, int rows,
                      char* err, size_t err_len) {
-  auto fn = encode_fn();
-  if (!fn) {
-    snprintf(err, err_len, "cuTensorMapEncodeTiled entry point unavailable");
-    return false;
-  }
   cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * H * 2,
                            (cuuint64_t)cols * H * 2 * (cuuint64_t)N};
   cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    snprintf(err, err_len, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
-    return false;
-  }
-  return true;
+  return encode_tmap_4d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, dims, strides, box, err, err_len);
 }
 
 // 4-D fp32 map over the dQ accumulator [B, N, H, 2d], box 32 x 1 x 128 x 1 (128-byte rows),
 // 128-byte swizzle: the target of the dK/dQ kernel's tensor reductions.
 static bool make_map_f32(CUtensorMap* m, void* base, int cols, int H, int N, int B, char* err,
                          size_t err_len) {
-  auto fn = encode_fn();
-  if (!fn) {
-    snprintf(err, err_len, "cuTensorMapEncodeTiled entry point unavailable");
-    return false;
-  }
   cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)cols * 4, (cuuint64_t)cols * H * 4,
                            (cuuint64_t)cols * H * 4 * (cuuint64_t)N};
   cuuint32_t box[4] = {32, 1, (cuuint32_t)kT, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    snprintf(err, err_len, "cuTensorMapEncodeTiled (fp32) failed (CUresult %d)", static_cast<int>(r));
-    return false;
-  }
-  return true;
+  return encode_tmap_4d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, dims, strides, box, err, err_len);
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }

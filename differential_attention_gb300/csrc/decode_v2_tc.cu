@@ -24,7 +24,6 @@
 // shared memory before the product, so cache contents beyond seqlens[b] are never used.
 // Every wait is bounded; a timeout flags DEV_TIMEOUT and all roles unwind without hanging.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include <cstdio>
 
@@ -416,40 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* q = nullptr;
-    cudaDriverEntryPointQueryResult res;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault,
-                                         &res) == cudaSuccess &&
-        res == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(q);
-  }
-  return fn;
-}
-
 // 4-D bf16 map over a row-major [d3][d2][d1][128] tensor, box 64 x box1 x box2 x 1, 128-byte
 // swizzle, zero fill out of bounds.
 static bool make_map(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uint64_t d3,
                      uint32_t box1, uint32_t box2, char* err, size_t err_len) {
-  auto fn = encode_fn();
-  if (!fn) {
-    snprintf(err, err_len, "cuTensorMapEncodeTiled entry point unavailable");
-    return false;
-  }
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), d1, d2, d3};
   cuuint64_t strides[3] = {kD * 2ull, kD * 2ull * d1, kD * 2ull * d1 * d2};
   cuuint32_t box[4] = {64, box1, box2, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    snprintf(err, err_len, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
-    return false;
-  }
-  return true;
+  return encode_tmap_4d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, dims, strides, box, err, err_len);
 }
 
 static int sm_count() {

@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace da {
@@ -82,6 +83,12 @@ __host__ __device__ inline size_t elem_off(const long long (&s)[3], long long b,
                                            long long h) {
   return static_cast<size_t>(b * s[0] + n * s[1] + h * s[2]);
 }
+
+// TMA tensor map of 4 dimensions with 128-byte swizzle, 256-byte L2 promotion and zero fill out
+// of bounds (tmap.cu); dims innermost first, byte strides of dims 1..3.
+bool encode_tmap_4d(CUtensorMap* m, CUtensorMapDataType type, const void* base,
+                    const cuuint64_t (&dims)[4], const cuuint64_t (&byte_strides)[3],
+                    const cuuint32_t (&box)[4], char* err, size_t err_len);
 
 // lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init for head u, from Problem::lam_vec.
 // Called by a whole warp (lanes split the dot products); every lane gets the value.

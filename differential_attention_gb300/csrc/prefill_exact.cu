@@ -30,7 +30,6 @@
 // warpgroup taking a quarter of the columns. Warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
 // owner, warps 2-17 = softmax and epilogue. Every wait is bounded.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -581,44 +580,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // 4-D bf16 map over [B, N, heads, cols] with a 64-col x 1 x box_rows x 1 box, 128-byte swizzle,
 // zero fill out of bounds.
 static bool make_map(CUtensorMap* m, const void* base, int cols, int heads, int N, int B,
                      const long long (&st)[3], int box_rows, char* err, size_t err_len,
                      int elt = 2) {
-  auto fn = get_encode_fn();
-  if (!fn) {
-    snprintf(err, err_len, "cuTensorMapEncodeTiled entry point unavailable");
-    return false;
-  }
   cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)heads, (cuuint64_t)N, (cuuint64_t)B};
   // element strides (batch, token, head) -> byte strides of dims 1..3 (head, token, batch)
   cuuint64_t strides[3] = {(cuuint64_t)st[2] * elt, (cuuint64_t)st[1] * elt,
                            (cuuint64_t)st[0] * elt};
   cuuint32_t box[4] = {(cuuint32_t)(128 / elt), 1, (cuuint32_t)box_rows, 1};  // 128-byte rows
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                  const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    snprintf(err, err_len, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
-    return false;
-  }
-  return true;
+  const CUtensorMapDataType type = elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return encode_tmap_4d(m, type, base, dims, strides, box, err, err_len);
 }
 
 template <int DQK, int DV, bool SHARED_K, bool QK8 = false>

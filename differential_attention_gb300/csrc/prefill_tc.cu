@@ -23,7 +23,6 @@
 // lane quarter each warp may access). Every mbarrier wait is bounded (ptx.cuh); on a timeout the
 // kernel flags the device status word and unwinds without trapping.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -436,41 +435,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // 4-D bf16 map over [B, N, heads, cols] (cols innermost) with a 64-col x 1 x 128-row x 1 box,
 // 128-byte swizzle, zero fill out of bounds.
 static bool make_map(CUtensorMap* m, const void* base, int cols, int heads, int N, int B,
                      char* err, size_t err_len) {
-  auto fn = get_encode_fn();
-  if (!fn) {
-    snprintf(err, err_len, "cuTensorMapEncodeTiled entry point unavailable");
-    return false;
-  }
   cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)heads, (cuuint64_t)N, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * heads * 2,
                            (cuuint64_t)cols * heads * 2 * (cuuint64_t)N};
   cuuint32_t box[4] = {64, 1, 128, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    snprintf(err, err_len, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
-    return false;
-  }
-  return true;
+  return encode_tmap_4d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, dims, strides, box, err, err_len);
 }
 
 template <int DQK, int DV, int NS>
