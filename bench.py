@@ -707,6 +707,49 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                          "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
                          "timed": "diffattn_v2_decode call (split kernel + combine kernel)"},
             "gpu_launches": 2 * n_steps}
+
+        # the same cache as pools of pages placed in a random order: 64-token pages (one TMA box
+        # per 64 keys) and 16-token pages (the smallest box the tensor-core kernel takes)
+        paged = {}
+        for ps in (64, 16):
+            mp = c["L"] // ps
+            k_pool = vd.k_cache.view(c["B"] * mp, ps, c["Hkv"], c["d"])
+            v_pool = vd.v_cache.view(c["B"] * mp, ps, c["Hkv"], c["d"])
+            gp = torch.Generator(device="cpu")
+            gp.manual_seed(5100 + ps + rank)
+            table = torch.randperm(c["B"] * mp, generator=gp).to(torch.int32).view(c["B"], mp).to(dev)
+
+            def v2dec_paged():
+                da.diffattn_v2_decode_paged(vd.q, k_pool, v_pool, table, vd.seqlens, vd.lam_logit,
+                                            workspace=ws, out=vdout)
+
+            for _ in range(args.warmup):
+                v2dec_paged()
+            barrier()
+            evs = [(ev(), ev()) for _ in range(n_steps)]
+            for i in range(n_steps):
+                evs[i][0].record(stream)
+                v2dec_paged()
+                evs[i][1].record(stream)
+            barrier()
+            da.diffattn_device_status()
+            pms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+            pgbs = nbytes / (pms * 1e-3) / 1e9
+            paged[f"page_{ps}"] = {"value": world * pgbs, "ms_per_call": pms, "frac": pgbs / hbm}
+            del k_pool, v_pool, table
+        line["v2_decode_paged"] = {
+            "metric": "V2 decode HBM GB/s", "unit": "GB/s",
+            "value": paged["page_64"]["value"], "ms_per_call": paged["page_64"]["ms_per_call"],
+            "workload": f"v2_decode_32k over a paged cache: B{c['B']}, cache 32768 in pages placed "
+                        "in a random order in the pool, Hq64 over Hkv8, d128, bf16",
+            "page_sizes": paged,
+            "roofline": {"bound": "hbm", "achieved": paged["page_64"]["value"] / world, "peak": hbm,
+                         "unit": "GB/s", "frac": paged["page_64"]["frac"],
+                         "bytes_per_launch": nbytes,
+                         "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
+                         "timed": "diffattn_v2_decode_paged call, 64-token pages (split kernel + "
+                                  "combine kernel)"},
+            "gpu_launches": 2 * n_steps * len(paged)}
         del vd, ws, vdout
         torch.cuda.empty_cache()
 

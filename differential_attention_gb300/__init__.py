@@ -97,6 +97,8 @@ _SIGNATURES = {
                      + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_v2_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int] * 7
                            + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_v2_decode_paged": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 9
+                                 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
 }
 
 
@@ -342,6 +344,42 @@ def diffattn_v2_decode(q, k_cache, v_cache, lam_logit, seqlens=None, cuda_cores:
                                     DIFFATTN_CUDA_CORES if cuda_cores else 0,
                                     DIFFATTN_BF16, _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def diffattn_v2_decode_paged(q, k_pool, v_pool, block_table, seqlens, lam_logit,
+                             cuda_cores: bool = False, workspace=None, out=None, stream=None):
+    """DIFF V2 decode over a paged cache: pools [num_pages, page_size, Hkv, d], block_table
+    [B, max_pages] int32, seqlens [B] int32; q [B, Hq, d], lam_logit [B, Hq/2]."""
+    _dev("q", q, torch.bfloat16)
+    B, Hq, d = q.shape
+    _dev("k_pool", k_pool, torch.bfloat16)
+    _dev("v_pool", v_pool, torch.bfloat16)
+    num_pages, page_size, Hkv = k_pool.shape[0], k_pool.shape[1], k_pool.shape[2]
+    if k_pool.shape != (num_pages, page_size, Hkv, d) or v_pool.shape != k_pool.shape:
+        raise ValueError("pools must both be [num_pages, page_size, Hkv, d]")
+    _dev("block_table", block_table, torch.int32)
+    _dev("seqlens", seqlens, torch.int32)
+    if block_table.dim() != 2 or block_table.shape[0] != B or seqlens.shape != (B,):
+        raise ValueError("block_table must be [B, max_pages] and seqlens [B]")
+    max_pages = block_table.shape[1]
+    _dev("lam_logit", lam_logit, torch.float32)
+    if lam_logit.shape != (B, Hq // 2):
+        raise ValueError("lam_logit must be [B, Hq/2]")
+    if workspace is None:
+        need = diffattn_v2_decode_workspace_size(B, max_pages * page_size, Hq, Hkv, d)
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _dev("workspace", workspace)
+    if out is None:
+        out = torch.empty((B, Hq // 2, d), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    _check(lib().diffattn_v2_decode_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                          _ptr(seqlens), _ptr(lam_logit), _ptr(out), B, Hq, Hkv,
+                                          d, num_pages, page_size, max_pages,
+                                          DIFFATTN_CUDA_CORES if cuda_cores else 0, DIFFATTN_BF16,
+                                          _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(),
+                                          _stream(stream)))
     return out
 
 

@@ -405,6 +405,60 @@ DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const vo
   return ok();
 }
 
+DIFFATTN_API int diffattn_v2_decode_paged(const void* q, const void* k_pool, const void* v_pool,
+                                          const int* block_table, const int* seqlens,
+                                          const float* lam_logit, void* out, int B, int Hq,
+                                          int Hkv, int d, int num_pages, int page_size,
+                                          int max_pages, int flags, int dtype, void* workspace,
+                                          size_t ws_bytes, void* stream) {
+  if (!q || !k_pool || !v_pool || !block_table || !seqlens || !lam_logit || !out)
+    return fail(DIFFATTN_ERR_ARG, "diffattn_v2_decode_paged: null pointer");
+  if (flags & ~(DIFFATTN_CAUSAL | DIFFATTN_CUDA_CORES))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_v2_decode_paged: unknown flag bits 0x%x", flags);
+  if (dtype != DIFFATTN_BF16)
+    return fail(DIFFATTN_ERR_DTYPE, "diffattn_v2_decode_paged: dtype must be DIFFATTN_BF16");
+  if (num_pages < 1 || page_size < 1 || max_pages < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_decode_paged: need num_pages, page_size, max_pages >= 1");
+  const long long lmax = static_cast<long long>(max_pages) * page_size;
+  if (lmax > (1LL << 30) || static_cast<long long>(num_pages) * page_size > 0x7fffffffLL)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_decode_paged: need max_pages * page_size <= 2^30 and num_pages * page_size < 2^31");
+  const int Lmax = static_cast<int>(lmax);
+  int rc = check_v2_decode_shape("diffattn_v2_decode_paged", B, Lmax, Hq, Hkv, d);
+  if (rc) return rc;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(lam_logit, 4) || !aligned(seqlens, 4) || !aligned(block_table, 4))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_v2_decode_paged: tensors must be 16-byte aligned");
+  const size_t need = da::v2_decode_workspace_bytes(B, Lmax, Hq, Hkv);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(DIFFATTN_ERR_WORKSPACE, "diffattn_v2_decode_paged: need a 256-byte aligned workspace of %zu bytes", need);
+  rc = check_device();
+  if (rc) return rc;
+  da::V2DecodeArgs a{};
+  a.q = q;
+  a.k_cache = k_pool;
+  a.v_cache = v_pool;
+  a.seqlens = seqlens;
+  a.lam_logit = lam_logit;
+  a.out = out;
+  a.B = B;
+  a.Lmax = Lmax;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.ws = static_cast<float*>(workspace);
+  a.block_table = block_table;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  char err[256] = {0};
+  cudaError_t e = (flags & DIFFATTN_CUDA_CORES)
+                      ? da::launch_v2_decode(a, static_cast<cudaStream_t>(stream))
+                      : da::launch_v2_decode_tc(a, static_cast<cudaStream_t>(stream), err, sizeof(err));
+  if (e == cudaErrorNotSupported) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_decode_paged: unsupported shape");
+  if (e == cudaErrorInvalidValue && err[0]) return fail(DIFFATTN_ERR_CUDA, "diffattn_v2_decode_paged: %s", err);
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_decode_paged launch");
+  return ok();
+}
+
 namespace {
 int check_train_shape(const char* fn, int B, int N, int H, int d, int dv, int dtype) {
   if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);

@@ -82,23 +82,30 @@ struct DecSplitParams {
   uint32_t ps_magic, ps_shift;  // j / page_size = (umulhi(j, magic) + j) >> shift, j < 2^31
 };
 
-// Row (key j of sequence b) of a contiguous [B, Lmax, H, w] cache, or of a paged pool
-// [num_pages, page_size, H, w] through the block table. A page id outside [0, num_pages) flags
-// DEV_BAD_INDEX and reads page 0 instead (the call's result is then invalid, nothing faults).
+// Pool row of key j of sequence b in a paged cache [num_pages, page_size, heads, w]. A page id
+// outside [0, num_pages) flags DEV_BAD_INDEX and reads page 0 instead (the call's result is then
+// invalid, nothing faults).
+__device__ __forceinline__ size_t paged_row(const int* table, int max_pages, int page_size,
+                                            int num_pages, uint32_t magic, uint32_t shift, int b,
+                                            int j) {
+  const uint32_t uj = static_cast<uint32_t>(j);
+  const uint32_t pi = (__umulhi(uj, magic) + uj) >> shift;  // j / page_size
+  int pg = __ldg(table + static_cast<size_t>(b) * max_pages + pi);
+  if (pg < 0 || pg >= num_pages) {
+    flag_device_error(DEV_BAD_INDEX);
+    pg = 0;
+  }
+  return static_cast<size_t>(pg) * page_size + (uj - pi * static_cast<uint32_t>(page_size));
+}
+
+// Row (key j of sequence b) of a contiguous [B, Lmax, H, w] cache, or of a paged pool.
 template <bool kPaged>
 __device__ __forceinline__ size_t cache_row(const DecSplitParams& p, int b, int j) {
-  if constexpr (kPaged) {
-    const uint32_t uj = static_cast<uint32_t>(j);
-    const uint32_t pi = (__umulhi(uj, p.ps_magic) + uj) >> p.ps_shift;  // j / page_size
-    int pg = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + pi);
-    if (pg < 0 || pg >= p.num_pages) {
-      flag_device_error(DEV_BAD_INDEX);
-      pg = 0;
-    }
-    return static_cast<size_t>(pg) * p.page_size + (uj - pi * static_cast<uint32_t>(p.page_size));
-  } else {
+  if constexpr (kPaged)
+    return paged_row(p.block_table, p.max_pages, p.page_size, p.num_pages, p.ps_magic, p.ps_shift,
+                     b, j);
+  else
     return static_cast<size_t>(b) * p.Lmax + j;
-  }
 }
 
 template <bool kPaged>
@@ -286,6 +293,16 @@ __global__ void __launch_bounds__(kDecWidth) decode_combine_kernel(const DecComb
 
 cudaError_t status_decode(int* v) { return read_clear_status(v); }
 
+void page_magic(int page_size, uint32_t* magic, uint32_t* shift) {
+  // division by the invariant page size d (Granlund and Montgomery, "Division by invariant
+  // integers using multiplication", 1994): l = ceil(log2 d), m = 2^32 (2^l - d) / d + 1
+  uint32_t l = 0;
+  while ((1ull << l) < static_cast<unsigned long long>(page_size)) ++l;
+  const unsigned long long d = static_cast<unsigned long long>(page_size);
+  *magic = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+  *shift = l;
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   int chunk = 0;
   const int S = decode_splits(a.B, a.Lmax, a.H, &chunk);
@@ -305,15 +322,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   sp.max_pages = a.max_pages;
   sp.num_pages = a.num_pages;
   sp.ps_magic = sp.ps_shift = 0;
-  if (a.block_table) {
-    // division by the invariant page size (Granlund and Montgomery, "Division by invariant
-    // integers using multiplication", 1994): l = ceil(log2 d), m = 2^32 (2^l - d) / d + 1
-    uint32_t l = 0;
-    while ((1ull << l) < static_cast<unsigned long long>(a.page_size)) ++l;
-    const unsigned long long d = static_cast<unsigned long long>(a.page_size);
-    sp.ps_magic = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
-    sp.ps_shift = l;
-  }
+  if (a.block_table) page_magic(a.page_size, &sp.ps_magic, &sp.ps_shift);
   if (a.block_table)
     decode_split_kernel<true><<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
   else
@@ -487,9 +496,12 @@ struct V2DecParams {
   float* ws;
   int Lmax, Hq, Hkv, splits, chunk;
   float scale_log2;
+  const int* block_table;  // paged: [B, max_pages]
+  int page_size, max_pages, num_pages;
+  uint32_t ps_magic, ps_shift;
 };
 
-template <int G>
+template <int G, bool kPaged>
 __global__ void __launch_bounds__(kV2Warps * 32) v2dec_split_kernel(const V2DecParams<G> p) {
   constexpr int kRec = G * (2 + kV2D);  // floats per record: per head m, l, o[128]
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -518,8 +530,15 @@ __global__ void __launch_bounds__(kV2Warps * 32) v2dec_split_kernel(const V2DecP
     for (int i = 0; i < 8; ++i) o[h][i] = 0.f;
 
   const size_t row = static_cast<size_t>(p.Hkv) * kV2D;  // elements between keys
-  const __nv_bfloat16* kb = p.kc + (static_cast<size_t>(b) * p.Lmax * p.Hkv + g) * kV2D + 8 * hl;
-  const __nv_bfloat16* vb = p.vc + (static_cast<size_t>(b) * p.Lmax * p.Hkv + g) * kV2D + 8 * hl;
+  const __nv_bfloat16* kb = p.kc + static_cast<size_t>(g) * kV2D + 8 * hl;
+  const __nv_bfloat16* vb = p.vc + static_cast<size_t>(g) * kV2D + 8 * hl;
+  auto rowof = [&](int j) -> size_t {
+    if constexpr (kPaged)
+      return paged_row(p.block_table, p.max_pages, p.page_size, p.num_pages, p.ps_magic,
+                       p.ps_shift, b, j);
+    else
+      return static_cast<size_t>(b) * p.Lmax + j;
+  };
   constexpr int kStride = kV2Warps * 2 * kV2Keys;  // keys per CTA step
   // The loop bound is warp-uniform so that every shuffle below has all 32 lanes; a half-warp
   // whose keys all lie past k1 takes part with masked scores and leaves its state unchanged.
@@ -529,8 +548,9 @@ __global__ void __launch_bounds__(kV2Warps * 32) v2dec_split_kernel(const V2DecP
 #pragma unroll
     for (int e = 0; e < kV2Keys; ++e) {
       const int j = min(j0 + e, k1 - 1);  // clamped in bounds; masked below
-      ku[e] = ldg_stream(kb + static_cast<size_t>(j) * row);
-      vu[e] = ldg_stream(vb + static_cast<size_t>(j) * row);
+      const size_t rj = rowof(j) * row;
+      ku[e] = ldg_stream(kb + rj);
+      vu[e] = ldg_stream(vb + rj);
     }
     float sc[kV2Keys];
 #pragma unroll
@@ -688,7 +708,17 @@ cudaError_t launch_v2dec(const V2DecodeArgs& a, cudaStream_t st, int S, int chun
   sp.splits = S;
   sp.chunk = chunk;
   sp.scale_log2 = kLog2e / sqrtf(static_cast<float>(kV2D));
-  v2dec_split_kernel<G><<<dim3(S, a.Hkv, a.B), kV2Warps * 32, 0, st>>>(sp);
+  sp.block_table = a.block_table;
+  sp.page_size = a.page_size;
+  sp.max_pages = a.max_pages;
+  sp.num_pages = a.num_pages;
+  sp.ps_magic = sp.ps_shift = 0;
+  if (a.block_table) {
+    page_magic(a.page_size, &sp.ps_magic, &sp.ps_shift);
+    v2dec_split_kernel<G, true><<<dim3(S, a.Hkv, a.B), kV2Warps * 32, 0, st>>>(sp);
+  } else {
+    v2dec_split_kernel<G, false><<<dim3(S, a.Hkv, a.B), kV2Warps * 32, 0, st>>>(sp);
+  }
   return cudaGetLastError();
 }
 }  // namespace

@@ -14,6 +14,8 @@
 // Work: one item = (sequence b, KV head g, split s of the cache); a persistent grid of one CTA
 // per SM takes items round-robin. Warp roles:
 //   warp 0     TMA producer: Q of each item (G rows), then K and V tiles into a 3-stage ring
+//              (for a paged cache with pages smaller than a tile: Q only)
+//   warps 6-13 paged cache with pages smaller than a tile: gather K and V rows into the ring
 //   warp 1     TMEM owner and MMA issuer: S_t, then O_{t-1} (so S_{t+1} overlaps softmax_t)
 //   warps 2-5  softmax: thread r owns key r of the tile for S and dim r of the head for O;
 //              per-head running max (exact, no lazy rescale), probabilities to P^T in bf16,
@@ -22,6 +24,12 @@
 //              (m, l, o[128]) in the layout the split-merge kernel of decode.cu reads.
 // Keys past the item's end inside the last tile get probability 0; their V rows are zeroed in
 // shared memory before the product, so cache contents beyond seqlens[b] are never used.
+// Paged cache, page size a multiple of 128: a tile lies in one page and is one TMA box per
+// 64-dim half, as for a contiguous cache. Other page sizes: TMA's cost per box makes one box per
+// page slow for small pages, so gather warps copy the tile themselves: each looks up the pool
+// rows of its 32 keys through the block table, then copies the rows with 16-byte cp.async into
+// the same 128-byte-swizzled layout TMA would write.
+// A page id outside the pool reads page 0 and, where the key is in use, flags DEV_BAD_INDEX.
 // Every wait is bounded; a timeout flags DEV_TIMEOUT and all roles unwind without hanging.
 #include <cuda.h>
 
@@ -48,8 +56,11 @@ constexpr int kQOff = kVOff + kStages * kKV;
 constexpr int kPOff = kQOff + 2 * kQSlot;
 constexpr int kSmemUsed = kPOff + 2 * kPBuf;
 constexpr int kDynSmem = kSmemUsed + 1024;  // + alignment slack
-constexpr int kThreads = 192;
+constexpr int kThreads = 448;
 constexpr int kSoftmaxThreads = 128;
+constexpr int kGatherWarp0 = 6;            // warps 6-13 gather K, V from a paged cache:
+constexpr int kGatherWarps = 4;            // two teams of four warps, tiles taken in turn
+constexpr int kGatherTeams = 2;
 constexpr uint32_t kTmemCols = 64;         // S[2] at cols 0, 16; O[2] at cols 32, 48
 constexpr int kRecStride = 2 + kD;         // floats per query head in a record
 static_assert(kDynSmem <= 227 * 1024, "shared memory budget");
@@ -66,6 +77,13 @@ struct Params {
   float* ws;
   int B, Lmax, Hq, Hkv, splits, chunk, n_items;
   float scale_log2;
+  const int* block_table;  // paged: [B, max_pages]; null for a contiguous cache
+  int page_size, max_pages, num_pages, box_rows;
+  int gather;                       // paged, page size not a multiple of 128: warp 0 gathers
+  const uint8_t* kpool;             // gather: pool bases and the bytes between keys (Hkv * 256)
+  const uint8_t* vpool;
+  size_t key_bytes;
+  uint32_t ps_magic, ps_shift;      // j / page_size = (umulhi(j, magic) + j) >> shift
 };
 
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
@@ -118,6 +136,22 @@ __device__ __forceinline__ Item item_of(const Params& p, int i) {
   return it;
 }
 
+// Pool row of key j of item `it` (paged cache). An entry past the block table's end reads page
+// 0; so does one outside the pool, which flags DEV_BAD_INDEX when the key is in use.
+__device__ __forceinline__ int page_row(const Params& p, const Item& it, int j) {
+  const uint32_t uj = static_cast<uint32_t>(j);
+  const uint32_t pi = (__umulhi(uj, p.ps_magic) + uj) >> p.ps_shift;
+  int pg = 0;
+  if (pi < static_cast<uint32_t>(p.max_pages)) {
+    pg = __ldg(p.block_table + static_cast<size_t>(it.b) * p.max_pages + pi);
+    if (pg < 0 || pg >= p.num_pages) {
+      if (j < it.k1) flag_device_error(DEV_BAD_INDEX);
+      pg = 0;
+    }
+  }
+  return pg * p.page_size + static_cast<int>(uj - pi * static_cast<uint32_t>(p.page_size));
+}
+
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
     v2dec_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -140,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(bars.k_full[i]), 1);
-      mbar_init(bar(bars.v_full[i]), 1);
+      mbar_init(bar(bars.k_full[i]), p.gather ? kGatherWarps : 1);
+      mbar_init(bar(bars.v_full[i]), p.gather ? kGatherWarps : 1);
       mbar_init(bar(bars.kv_empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -178,7 +212,81 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_slot;
   volatile int* abrt = &abort_flag;
 
-  if (warp == 0) {
+  if (warp == 0 && p.gather) {
+    // ======================= Q producer (the gather warps load K, V) =======================
+    if (lane == 0) {
+      int qi = 0;
+      for (int i = blockIdx.x; i < p.n_items; i += gridDim.x) {
+        const Item it = item_of(p, i);
+        if (it.nt == 0) continue;
+        const int qs = qi & 1;
+        if (!mbar_wait(bar(bars.q_empty[qs]), ((qi >> 1) & 1) ^ 1, abrt)) break;
+        mbar_arrive_expect_tx(bar(bars.q_full[qs]), 2 * G * 128);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sQ + qs * kQSlot + c * (kN * 128), &tm_q, bar(bars.q_full[qs]), 64 * c,
+                      it.g * G, it.b, 0);
+        ++qi;
+      }
+      for (int j = max(0, qi - 2); j < qi; ++j)
+        mbar_wait(bar(bars.q_full[j & 1]), (j >> 1) & 1, nullptr);
+    }
+  } else if (warp >= kGatherWarp0) {
+    // ====================== gathering producers (paged cache only) =======================
+    // Tiles alternate between the two teams, so two tiles are in flight. Warp w of a team
+    // copies keys 32w .. 32w + 31 of its tiles: lane l looks up the pool row of key 32w + l, then
+    // each instruction copies two keys' 256-byte head rows (lanes 0-15 one key, lanes 16-31 the
+    // next, 16 bytes a lane). A warp waits for its own copies, fences them for the tensor cores'
+    // proxy and arrives on the tile's barrier (four arrivals complete it).
+    if (p.gather) {
+      const int gw = (warp - kGatherWarp0) % kGatherWarps;
+      const int team = (warp - kGatherWarp0) / kGatherWarps;
+      int n = 0;
+      bool ok = true;
+      const int kh = lane >> 4;
+      const uint32_t ch = lane & 15;
+      const uint32_t cdst = (ch >> 3) * kChunk, jc = ch & 7;
+      for (int i = blockIdx.x; ok && i < p.n_items; i += gridDim.x) {
+        const Item it = item_of(p, i);
+        if (it.nt == 0) continue;
+        const uint8_t* kg = p.kpool + static_cast<size_t>(it.g) * (2 * kD) + ch * 16;
+        const uint8_t* vg = p.vpool + static_cast<size_t>(it.g) * (2 * kD) + ch * 16;
+        for (int t = 0; t < it.nt; ++t, ++n) {
+          if (n % kGatherTeams != team) continue;  // the other team's tile
+          const int st = n % kStages;
+          const int row = page_row(p, it, it.k0 + t * kTile + 32 * gw + lane);
+          // every lane waits: with lane 0 waiting alone and the others parked at a shuffle, the
+          // warp resumed late enough to halve the throughput
+          const bool w = mbar_wait(bar(bars.kv_empty[st]), ((n / kStages) & 1) ^ 1, abrt);
+          if (!(ok = __all_sync(0xffffffffu, w))) break;
+          const uint32_t dk = sK + st * kKV + cdst, dv = sV + st * kKV + cdst;
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {
+            const int rl = 2 * kk + kh, r = 32 * gw + rl;
+            const int rr = __shfl_sync(0xffffffffu, row, rl);
+            cp_async16(dk + r * 128 + ((jc ^ (r & 7)) << 4),
+                       kg + static_cast<size_t>(rr) * p.key_bytes);
+          }
+          cp_async_commit();
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {
+            const int rl = 2 * kk + kh, r = 32 * gw + rl;
+            const int rr = __shfl_sync(0xffffffffu, row, rl);
+            cp_async16(dv + r * 128 + ((jc ^ (r & 7)) << 4),
+                       vg + static_cast<size_t>(rr) * p.key_bytes);
+          }
+          cp_async_commit();
+          cp_async_wait<0>();  // our part of the tile has landed: hand it over
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bar(bars.k_full[st]));
+            mbar_arrive(bar(bars.v_full[st]));
+          }
+        }
+      }
+      cp_async_wait<0>();  // nothing of ours may still be landing when the CTA exits
+    }
+  } else if (warp == 0) {
     // ================================ TMA producer ================================
     if (lane == 0) {
       int n = 0, qi = 0;
@@ -195,16 +303,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++qi;
         for (int t = 0; t < it.nt; ++t, ++n) {
           const int st = n % kStages;
-          if (!(ok = mbar_wait(bar(bars.kv_empty[st]), ((n / kStages) & 1) ^ 1, abrt))) break;
           const int key = it.k0 + t * kTile;
+          // paged, page size a multiple of 128: the tile is rows row0 .. row0 + 127 of one page
+          const int row0 = p.block_table ? page_row(p, it, key) : 0;
+          if (!(ok = mbar_wait(bar(bars.kv_empty[st]), ((n / kStages) & 1) ^ 1, abrt))) break;
           mbar_arrive_expect_tx(bar(bars.k_full[st]), kKV);
-          for (int c = 0; c < 2; ++c)
-            tma_load_4d(sK + st * kKV + c * kChunk, &tm_k, bar(bars.k_full[st]), 64 * c, it.g,
-                        key, it.b);
-          mbar_arrive_expect_tx(bar(bars.v_full[st]), kKV);
-          for (int c = 0; c < 2; ++c)
-            tma_load_4d(sV + st * kKV + c * kChunk, &tm_v, bar(bars.v_full[st]), 64 * c, it.g,
-                        key, it.b);
+          if (p.block_table) {
+            for (int c = 0; c < 2; ++c)
+              tma_load_4d(sK + st * kKV + c * kChunk, &tm_k, bar(bars.k_full[st]), 64 * c, it.g,
+                          row0, 0);
+            mbar_arrive_expect_tx(bar(bars.v_full[st]), kKV);
+            for (int c = 0; c < 2; ++c)
+              tma_load_4d(sV + st * kKV + c * kChunk, &tm_v, bar(bars.v_full[st]), 64 * c, it.g,
+                          row0, 0);
+          } else {
+            for (int c = 0; c < 2; ++c)
+              tma_load_4d(sK + st * kKV + c * kChunk, &tm_k, bar(bars.k_full[st]), 64 * c, it.g,
+                          key, it.b);
+            mbar_arrive_expect_tx(bar(bars.v_full[st]), kKV);
+            for (int c = 0; c < 2; ++c)
+              tma_load_4d(sV + st * kKV + c * kChunk, &tm_v, bar(bars.v_full[st]), 64 * c, it.g,
+                          key, it.b);
+          }
         }
       }
       // no copy of ours may still be landing when the CTA exits
@@ -272,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar(bars.teardown), 0, nullptr);
     }
   } else {
-    // ============================ softmax and output ==============================
+    // ============================ softmax and output (warps 2-5) =================
     const int q4 = warp & 3;  // TMEM lane quarter this warp may access
     const int r = 32 * q4 + lane;
     const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
@@ -437,9 +557,15 @@ template <int G>
 static cudaError_t launch_g(const V2DecodeArgs& a, int splits, int chunk, cudaStream_t st,
                             char* err, size_t err_len) {
   CUtensorMap mq, mk, mv;
+  const bool paged = a.block_table != nullptr;
+  const bool gather = paged && a.page_size % kTile != 0;
+  // paged: the pools as one [num_pages * page_size, Hkv, 128] cache (the maps are not used when
+  // warp 0 gathers)
+  const uint64_t rows = paged ? static_cast<uint64_t>(a.num_pages) * a.page_size : a.Lmax;
+  const uint32_t box_rows = gather ? 1u : kTile;
   if (!make_map(&mq, a.q, a.Hq, a.B, 1, G, 1, err, err_len) ||
-      !make_map(&mk, a.k_cache, a.Hkv, a.Lmax, a.B, 1, kTile, err, err_len) ||
-      !make_map(&mv, a.v_cache, a.Hkv, a.Lmax, a.B, 1, kTile, err, err_len))
+      !make_map(&mk, a.k_cache, a.Hkv, rows, paged ? 1 : a.B, 1, box_rows, err, err_len) ||
+      !make_map(&mv, a.v_cache, a.Hkv, rows, paged ? 1 : a.B, 1, box_rows, err, err_len))
     return cudaErrorInvalidValue;
   auto kern = v2dec_tc_kernel<G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
@@ -455,6 +581,17 @@ static cudaError_t launch_g(const V2DecodeArgs& a, int splits, int chunk, cudaSt
   p.chunk = chunk;
   p.n_items = a.B * a.Hkv * splits;
   p.scale_log2 = kLog2e / sqrtf(static_cast<float>(kD));
+  p.block_table = a.block_table;
+  p.page_size = a.page_size;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
+  p.box_rows = static_cast<int>(box_rows);
+  p.gather = gather ? 1 : 0;
+  p.kpool = static_cast<const uint8_t*>(a.k_cache);
+  p.vpool = static_cast<const uint8_t*>(a.v_cache);
+  p.key_bytes = static_cast<size_t>(a.Hkv) * kD * 2;
+  p.ps_magic = p.ps_shift = 0;
+  if (paged) page_magic(a.page_size, &p.ps_magic, &p.ps_shift);
   const int grid = min(p.n_items, sm_count());
   kern<<<grid, kThreads, kDynSmem, st>>>(mq, mk, mv, p);
   return cudaGetLastError();
@@ -481,6 +618,8 @@ cudaError_t launch_v2_decode_tc(const V2DecodeArgs& a, cudaStream_t st, char* er
   int chunk = 0;
   const int S = v2_decode_tc_splits(a.B, a.Lmax, a.Hkv, &chunk);
   const int G = a.Hq / a.Hkv;
+  if (a.block_table && static_cast<long long>(a.num_pages) * a.page_size > 0x7fffffffLL)
+    return cudaErrorNotSupported;
   cudaError_t e;
   if (G == 8)
     e = v2tc::launch_g<8>(a, S, chunk, st, err, err_len);

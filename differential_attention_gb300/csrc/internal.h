@@ -166,7 +166,14 @@ struct V2DecodeArgs {
   void* out;
   int B, Lmax, Hq, Hkv;
   float* ws;
+  // paged cache (block_table non-null): pools [num_pages, page_size, Hkv, 128], key j of sequence
+  // b in page block_table[b * max_pages + j / page_size]; Lmax = max_pages * page_size
+  const int* block_table;
+  int page_size, max_pages, num_pages;
 };
+// j / page_size = (umulhi(j, magic) + j) >> shift for 0 <= j < 2^31 (division by an invariant
+// integer, Granlund and Montgomery 1994)
+void page_magic(int page_size, uint32_t* magic, uint32_t* shift);
 int v2_decode_splits(int B, int Lmax, int Hkv, int* chunk_out);      // CUDA-core split kernel
 int v2_decode_tc_splits(int B, int Lmax, int Hkv, int* chunk_out);   // tensor-core split kernel
 size_t v2_decode_workspace_bytes(int B, int Lmax, int Hq, int Hkv);  // enough for either

@@ -235,7 +235,8 @@ DIFFATTN_API int diffattn_v2_fwd(const void* q, const void* k, const void* v,
  *               device as for diffattn_decode)
  *   lam_logit : device fp32 [B, Hq/2], the value before the sigmoid
  *   out       : device [B, Hq/2, d]
- *   flags     : 0 (DIFFATTN_CAUSAL is accepted and ignored)
+ *   flags     : 0 runs the tensor-core kernel; DIFFATTN_CUDA_CORES the CUDA-core one (same
+ *               result up to rounding order); DIFFATTN_CAUSAL is accepted and ignored
  *   workspace, ws_bytes : device scratch of at least diffattn_v2_decode_workspace_size() bytes,
  *               256-byte aligned, not shared with a call that can run at the same time.
  * Supported: dtype DIFFATTN_BF16, d = 128, Hq / Hkv in {2, 4, 8}. The scale is 1/sqrt(d).
@@ -247,6 +248,29 @@ DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const vo
                                     const int* seqlens, const float* lam_logit, void* out, int B,
                                     int Lmax, int Hq, int Hkv, int d, int flags, int dtype,
                                     void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * DIFF V2 decode over a paged KV cache: the result of diffattn_v2_decode where key j of
+ * sequence b sits at row j % page_size of page block_table[b * max_pages + j / page_size].
+ *   k_pool, v_pool : device [num_pages, page_size, Hkv, d]
+ *   block_table    : device int32 [B, max_pages]; only entries for keys < seqlens[b] are used
+ *   seqlens        : device int32 [B] (required), clamped to [1, max_pages * page_size]
+ *   q, lam_logit, out, flags : as for diffattn_v2_decode
+ *   workspace, ws_bytes : at least diffattn_v2_decode_workspace_size(B, max_pages * page_size,
+ *                    Hq, Hkv, d) bytes, 256-byte aligned.
+ * Any page size >= 1 (multiples of 128 read each tile of 128 keys as TMA boxes, others gather
+ * the keys' rows one by one). A used block-table entry outside [0, num_pages) reads page 0
+ * instead and makes the next diffattn_device_status() report DIFFATTN_ERR_INDEX; that call's
+ * output is then invalid.
+ * Errors: ERR_ARG, ERR_SHAPE (max_pages * page_size > 2^30 or num_pages * page_size >= 2^31),
+ * ERR_DTYPE, ERR_ALIGN, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_v2_decode_paged(const void* q, const void* k_pool, const void* v_pool,
+                                          const int* block_table, const int* seqlens,
+                                          const float* lam_logit, void* out, int B, int Hq,
+                                          int Hkv, int d, int num_pages, int page_size,
+                                          int max_pages, int flags, int dtype, void* workspace,
+                                          size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------
  * Prefill straight from host memory (not part of the method; the serving path around it): the

@@ -382,6 +382,25 @@ def diffattn_decode_paged(q, k_pool, v_pool, block_table, seqlens, lam, lam_init
     return diffattn_decode(q, kc, vc, sl, lam, lam_init, norm_weight, eps, norm, apply_scale)
 
 
+def diffattn_v2_decode_paged(q, k_pool, v_pool, block_table, seqlens, lam_logit):
+    """`diffattn_v2_decode` over a cache held in pages: k_pool, v_pool [num_pages, page_size,
+    Hkv, d], block_table [B, max_pages], seqlens [B]. Each sequence's keys are gathered from the
+    pool in order, then decoded as a contiguous cache."""
+    num_pages, page_size, Hkv, w = k_pool.shape
+    kp = _f64(k_pool).reshape(num_pages * page_size, Hkv, w)
+    vp = _f64(v_pool).reshape(num_pages * page_size, Hkv, v_pool.shape[-1])
+    B = q.shape[0]
+    sl = np.asarray(_f64(seqlens)).astype(np.int64)
+    L = int(sl.max())
+    kc = np.zeros((B, L, Hkv, w))
+    vc = np.zeros((B, L, Hkv, vp.shape[-1]))
+    for b in range(B):
+        rows = paged_rows(block_table, seqlens, page_size, b)
+        kc[b, :rows.size] = kp[rows]
+        vc[b, :rows.size] = vp[rows]
+    return diffattn_v2_decode(q, kc, vc, sl, lam_logit)
+
+
 # --------------------------------------------------------------------------------------------
 # variable-length prefill (packed sequences; the operator per sequence is unchanged)
 # --------------------------------------------------------------------------------------------

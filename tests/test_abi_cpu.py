@@ -145,6 +145,28 @@ def test_v2_decode_validation(L):
     assert v2d(ws_bytes=need - 1) == -8
 
 
+def test_v2_decode_paged_validation(L):
+    n = ctypes.c_size_t(0)
+    assert L.diffattn_v2_decode_workspace_size(8, 64 * 256, 16, 2, 128, ctypes.byref(n)) == 0
+    need = n.value
+
+    def v2p(table=FAKE, seqlens=FAKE, num_pages=100, page_size=64, max_pages=256, Hq=16,
+            flags=0, dtype=0, ws_bytes=need):
+        return L.diffattn_v2_decode_paged(FAKE, FAKE, FAKE, table, seqlens, FAKE, FAKE, 8, Hq, 2,
+                                          128, num_pages, page_size, max_pages, flags, dtype, FAKE,
+                                          ws_bytes, None)
+
+    assert v2p(table=None) == -1
+    assert v2p(seqlens=None) == -1  # required for a paged cache
+    assert v2p(flags=2) == -1
+    assert v2p(page_size=0) == -2
+    assert v2p(max_pages=1 << 20, page_size=4096) == -2  # 2^32 keys
+    assert v2p(num_pages=1 << 20, page_size=4096) == -2  # pool rows past 2^31
+    assert v2p(Hq=12) == -2  # group of 6
+    assert v2p(dtype=1) == -3
+    assert v2p(ws_bytes=need - 1) == -8
+
+
 def test_training_validation(L):
     def train(q=FAKE, stats=FAKE, d=128, dv=256, flags=7, dtype=0):
         return L.diffattn_fwd_train(q, FAKE, FAKE, FAKE, FAKE, stats, FAKE, 0.5, None, 1e-5, 1, 16,

@@ -382,6 +382,32 @@ def pin_paged_decode():
     assert np.allclose(got2, want, rtol=1e-12, atol=1e-12)
 
 
+def pin_v2_paged_decode():
+    """Paged V2 decode equals contiguous V2 decode over the same keys: identity table, then a
+    shuffled pool with the table following it; table entries past a sequence's pages are unused."""
+    rng = np.random.default_rng(23)
+    B, Hq, Hkv, d, ps = 3, 8, 2, 4, 4
+    max_pages = 5
+    q = rng.standard_normal((B, Hq, d))
+    kc = rng.standard_normal((B, max_pages * ps, Hkv, d))
+    vc = rng.standard_normal((B, max_pages * ps, Hkv, d))
+    seqlens = np.array([17, 3, 20])
+    lam = rng.standard_normal((B, Hq // 2))
+    want = ref.diffattn_v2_decode(q, kc, vc, seqlens, lam)
+    k_pool = kc.reshape(B * max_pages, ps, Hkv, d)
+    v_pool = vc.reshape(B * max_pages, ps, Hkv, d)
+    table = np.arange(B * max_pages).reshape(B, max_pages)
+    got = ref.diffattn_v2_decode_paged(q, k_pool, v_pool, table, seqlens, lam)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    perm = rng.permutation(B * max_pages)
+    k_sh = np.empty_like(k_pool); v_sh = np.empty_like(v_pool)
+    k_sh[perm], v_sh[perm] = k_pool, v_pool
+    t2 = perm[table]
+    t2[1, 1:] = -1                                   # sequence 1 holds 3 keys: one page
+    got2 = ref.diffattn_v2_decode_paged(q, k_sh, v_sh, t2, seqlens, lam)
+    assert np.allclose(got2, want, rtol=1e-12, atol=1e-12)
+
+
 def pin_varlen():
     """Packed sequences: with equal lengths the result is the batched prefill's; and each sequence
     sees only itself (changing another sequence's tokens leaves its rows unchanged)."""
@@ -410,7 +436,7 @@ PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, p
         pin_lambda_zero_is_softmax_attention, pin_equal_maps_scale_attention, pin_brute_force_tiny,
         pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
-        pin_lambda_bwd, pin_paged_decode, pin_varlen]
+        pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])

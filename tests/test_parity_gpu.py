@@ -446,6 +446,52 @@ def test_v2_decode_rejects_bad_shapes():
     assert e.value.status == -2  # DIFFATTN_ERR_SHAPE
 
 
+@pytest.mark.parametrize("ps,cuda_cores", [(16, False), (64, False), (128, False), (256, False),
+                                           (48, False), (1, False), (16, True), (256, True)])
+def test_v2_decode_paged(ps, cuda_cores):
+    """Ragged sequences in a shuffled pool with spare pages: against the oracle, and bit-equal to
+    the contiguous decode of the same cache (same kernel, same splits). Page sizes that are not a
+    multiple of 128 take the gathering producer, multiples of 128 the TMA one."""
+    B, L, Hq, Hkv = 3, 768, 16, 2
+    inp = make_v2_decode_inputs(B, L, Hq, Hkv, 128, seed=141 + ps, ragged=True)
+    k_pool, v_pool, table = page_cache(inp.k_cache, inp.v_cache, ps, seed=151 + ps, spare_pages=2)
+    got = da.diffattn_v2_decode_paged(inp.q.to(DEV), k_pool.to(DEV), v_pool.to(DEV),
+                                      table.to(DEV), inp.seqlens.to(DEV), inp.lam_logit.to(DEV),
+                                      cuda_cores=cuda_cores)
+    want = ref.diffattn_v2_decode_paged(inp.q, k_pool, v_pool, table, inp.seqlens, inp.lam_logit)
+    assert_bf16(got, want)
+    flat = da.diffattn_v2_decode(inp.q.to(DEV), inp.k_cache.to(DEV), inp.v_cache.to(DEV),
+                                 inp.lam_logit.to(DEV), seqlens=inp.seqlens.to(DEV),
+                                 cuda_cores=cuda_cores)
+    assert torch.equal(got, flat)
+    da.diffattn_device_status()
+
+
+@pytest.mark.parametrize("cuda_cores", [False, True])
+def test_v2_decode_paged_unused_entries_and_bad_page(cuda_cores):
+    """Block-table entries past a sequence's pages are never read (-1 there is fine); an entry
+    outside the pool for a page in use reads page 0, nothing faults, and the host sees
+    DIFFATTN_ERR_INDEX."""
+    inp = make_v2_decode_inputs(2, 512, 8, 2, 128, seed=191)
+    seqlens = torch.tensor([100, 300], dtype=torch.int32)
+    k_pool, v_pool, table = page_cache(inp.k_cache, inp.v_cache, 32, seed=192)
+    table[0, 4:] = -1  # sequence 0 holds 100 keys: pages 0..3
+    table[1, 10:] = -1
+    args = (inp.q.to(DEV), k_pool.to(DEV), v_pool.to(DEV))
+    got = da.diffattn_v2_decode_paged(*args, table.to(DEV), seqlens.to(DEV),
+                                      inp.lam_logit.to(DEV), cuda_cores=cuda_cores)
+    da.diffattn_device_status()  # OK: no used entry is bad
+    want = ref.diffattn_v2_decode(inp.q, inp.k_cache, inp.v_cache, seqlens, inp.lam_logit)
+    assert_bf16(got, want)
+    table[1, 3] = k_pool.shape[0] + 7
+    da.diffattn_v2_decode_paged(*args, table.to(DEV), seqlens.to(DEV), inp.lam_logit.to(DEV),
+                                cuda_cores=cuda_cores)
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_device_status()
+    assert e.value.status == -9  # DIFFATTN_ERR_INDEX
+    da.diffattn_device_status()
+
+
 # ------------------------------------------------------------------------------------------
 # opt-in single-pass tensor-core path (bf16 probabilities per map): parity where the problem is
 # well conditioned (lambda away from 1); its error grows like 2^-9 / |1 - lambda|.
