@@ -606,6 +606,46 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del inp, out, q, k, v
         torch.cuda.empty_cache()
 
+        # the last 1024-token chunk of each prefill_3b prompt against its 4096 keys (queries and
+        # keys with offsets of their own)
+        Lq, Lk = 1024, c["N"]
+        kin = make_prefill_inputs(c["B"], Lk, c["H"], c["d"], c["dv"], seed=8100 + rank,
+                                  layer=c["layer"], device=dev)
+        k, v = kin.k.reshape(-1, c["H"], 2 * c["d"]), kin.v.reshape(-1, c["H"], c["dv"])
+        q = kin.q[:, Lk - Lq:].reshape(-1, c["H"], 2 * c["d"]).contiguous()
+        cu_q = torch.arange(c["B"] + 1, dtype=torch.int32, device=dev) * Lq
+        cu_k = torch.arange(c["B"] + 1, dtype=torch.int32, device=dev) * Lk
+        out = torch.empty((c["B"] * Lq, c["H"], c["dv"]), dtype=torch.bfloat16, device=dev)
+
+        def cstep():
+            da.diffattn_fwd_varlen_qk(q, k, v, cu_q, cu_k, lam, li, max_seqlen_q=Lq,
+                                      max_seqlen_k=Lk, out=out)
+
+        for _ in range(args.warmup):
+            cstep()
+        barrier()
+        evs = [(ev(), ev()) for _ in range(n_steps)]
+        for i in range(n_steps):
+            evs[i][0].record(stream)
+            cstep()
+            evs[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        pairs = Lq * (Lk - Lq) + Lq * (Lq + 1) // 2  # query at position p sees p + 1 keys
+        cflops = float(c["B"] * c["H"] * pairs * FLOPS_PER_PAIR)
+        ctf = cflops / (ms * 1e-3) / 1e12
+        line["varlen_qk"] = {
+            "metric": "DiffAttn fwd TFLOP/s", "value": world * ctf, "unit": "TFLOP/s",
+            "ms_per_call": ms,
+            "workload": f"prefill_3b prompts computed as a last chunk: B{c['B']}, {Lq} queries "
+                        f"against {Lk} keys each, causal, H12, d128, dv256",
+            "roofline": {"bound": "tensor", "achieved": ctf, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": ctf / peak_tf, "flops_per_launch": cflops},
+            "gpu_launches": n_steps}
+        del kin, out, q, k, v
+        torch.cuda.empty_cache()
+
     # ======================= training step: forward (saving statistics) + backward ==========
     if args.only in ("all", "backward"):
         c = PREFILL

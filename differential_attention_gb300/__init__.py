@@ -83,6 +83,9 @@ _SIGNATURES = {
     "diffattn_fwd_varlen": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 2
                             + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
                             + [ctypes.c_int] * 6 + [ctypes.c_void_p]),
+    "diffattn_fwd_varlen_qk": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int] * 4
+                               + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
+                               + [ctypes.c_int] * 6 + [ctypes.c_void_p]),
     "diffattn_fwd_fused_lambda": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int] * 3
                                   + [ctypes.c_void_p, ctypes.c_float] + [ctypes.c_int] * 7
                                   + [ctypes.c_void_p]),
@@ -540,6 +543,45 @@ def diffattn_fwd_varlen(q, k, v, cu_seqlens, lam, lambda_init: float = 0.0, max_
                                      _ptr(norm_weight), float(eps), B, H, d, dv,
                                      _train_flags(causal, norm, scale), DIFFATTN_BF16,
                                      _stream(stream)))
+    return out
+
+
+def diffattn_fwd_varlen_qk(q, k, v, cu_seqlens_q, cu_seqlens_k, lam, lambda_init: float = 0.0,
+                           max_seqlen_q=None, max_seqlen_k=None, norm_weight=None,
+                           eps: float = 1e-5, causal: bool = True, norm: bool = True,
+                           scale: bool = True, out=None, stream=None):
+    """Packed prefill where each sequence's Lq queries (q, out [total_q, H, *]) are the last Lq of
+    its Lk keys (k, v [total_k, H, *]); cu_seqlens_q and cu_seqlens_k are int32 [B + 1] on the
+    device. Missing maxima are read from the offsets (one device-to-host copy each)."""
+    _dev("q", q, torch.bfloat16)
+    total_q, H, two_d = q.shape
+    d = two_d // 2
+    _dev("k", k, torch.bfloat16)
+    _dev("v", v, torch.bfloat16)
+    total_k, dv = k.shape[0], v.shape[-1]
+    if k.shape != (total_k, H, two_d) or v.shape[:2] != (total_k, H):
+        raise ValueError("k must be [total_k, H, 2d] and v [total_k, H, dv]")
+    _dev("cu_seqlens_q", cu_seqlens_q, torch.int32)
+    _dev("cu_seqlens_k", cu_seqlens_k, torch.int32)
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B + 1 entries")
+    if max_seqlen_q is None:
+        max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B > 0 else 1
+    if max_seqlen_k is None:
+        max_seqlen_k = int((cu_seqlens_k[1:] - cu_seqlens_k[:-1]).max().item()) if B > 0 else 1
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if out is None:
+        out = torch.zeros((total_q, H, dv), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    _check(lib().diffattn_fwd_varlen_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(cu_seqlens_q),
+                                        _ptr(cu_seqlens_k), max(1, int(max_seqlen_q)),
+                                        max(1, int(max_seqlen_k)), total_q, total_k, _ptr(lam),
+                                        float(lambda_init), _ptr(norm_weight), float(eps), B, H, d,
+                                        dv, _train_flags(causal, norm, scale), DIFFATTN_BF16,
+                                        _stream(stream)))
     return out
 
 

@@ -747,6 +747,65 @@ DIFFATTN_API int diffattn_fwd_varlen(const void* q, const void* k, const void* v
   return run_prefill(p, dtype, "diffattn_fwd_varlen", static_cast<cudaStream_t>(stream));
 }
 
+DIFFATTN_API int diffattn_fwd_varlen_qk(const void* q, const void* k, const void* v, void* out,
+                                        const int* cu_seqlens_q, const int* cu_seqlens_k,
+                                        int max_seqlen_q, int max_seqlen_k, int total_q,
+                                        int total_k, const float* lambda, float lambda_init,
+                                        const float* norm_weight, float eps, int B, int H, int d,
+                                        int dv, int flags, int dtype, void* stream) {
+  const char* fn = "diffattn_fwd_varlen_qk";
+  if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  constexpr int kVarFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kVarFlags) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "%s: eps must be > 0 with DIFFATTN_NORM", fn);
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);
+  if (B < 1 || H < 1 || max_seqlen_q < 1 || total_q < 1 || max_seqlen_q > total_q ||
+      max_seqlen_k < max_seqlen_q || total_k < total_q || max_seqlen_k > total_k)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need B, H >= 1, 1 <= max_seqlen_q <= total_q, "
+                "max_seqlen_q <= max_seqlen_k <= total_k and total_q <= total_k", fn);
+  if (!(d == 64 || d == 128) || dv != 2 * d)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need d in {64, 128} and dv = 2d", fn);
+  const long long tiles = (static_cast<long long>(max_seqlen_q) + 127) / 128 * B * H;
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(total_k) * H > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: problem too large for one launch", fn);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) ||
+      (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = max_seqlen_q;
+  p.units = H;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_V1;
+  p.q_heads = H;
+  p.kv_heads = H;
+  p.q_cols = 2 * d;
+  p.k_cols = 2 * d;
+  p.group = 1;
+  p.lambda = lambda;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  p.cu_seqlens = cu_seqlens_q;
+  p.total = total_q;
+  p.cu_seqlens_k = cu_seqlens_k;
+  p.total_k = total_k;
+  p.max_seqlen_k = max_seqlen_k;
+  return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
+}
+
 DIFFATTN_API int diffattn_fwd_fp8(const void* q, const void* k, const void* v, void* out,
                                   float q_descale, float k_descale, const float* lambda,
                                   float lambda_init, const float* norm_weight, float eps, int B,

@@ -133,22 +133,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qt = causal ? (kp.n_qt - 1 - r_in / gsize) : (r_in / gsize);
   const int bu = g0 + r_in % gsize;
   const int b = bu / P.units, u = bu % P.units;
-  // this sequence's rows: [seq0, seq0 + SN) of the (packed) token axis; TMA batch coordinate tb
+  // this sequence's query rows: [seq0, seq0 + SN) of the (packed) token axis, its key rows
+  // [kseq0, kseq0 + SNk); TMA batch coordinate tb. With keys of their own (cu_seqlens_k) the
+  // queries are the sequence's last SN positions: query row i sees keys [0, qoff + i], with
+  // qoff = SNk - SN.
   int seq0 = 0, SN = P.N, tb = b;
+  int kseq0 = 0, SNk = P.N;
   if (P.cu_seqlens) {
     seq0 = P.cu_seqlens[b];
     SN = P.cu_seqlens[b + 1] - seq0;
     tb = 0;
-    // offsets are device data: a sequence outside [0, total) or longer than the stated maximum
-    // is reported (DEV_BAD_INDEX) and skipped, so no store leaves the output
-    if (seq0 < 0 || SN < 0 || SN > P.N || seq0 > P.total - SN) {
+    kseq0 = seq0;
+    SNk = SN;
+    if (P.cu_seqlens_k) {
+      kseq0 = P.cu_seqlens_k[b];
+      SNk = P.cu_seqlens_k[b + 1] - kseq0;
+    }
+    // offsets are device data: a sequence outside [0, total) or longer than the stated maximum,
+    // or with fewer keys than queries, is reported (DEV_BAD_INDEX) and skipped, so no store
+    // leaves the output
+    const int ktot = P.cu_seqlens_k ? P.total_k : P.total;
+    if (seq0 < 0 || SN < 0 || SN > P.N || seq0 > P.total - SN || kseq0 < 0 || SNk < SN ||
+        kseq0 > ktot - SNk) {
       if (threadIdx.x == 0 && qt == 0) flag_device_error(DEV_BAD_INDEX);
       return;
     }
     if (qt * BM >= SN) return;  // a tile past this sequence's end: nothing to do (uniform)
   }
-  const int n_kv_all = (SN + BN - 1) / BN;
-  const int n = causal ? min(qt + 1, n_kv_all) : n_kv_all;  // BM == BN
+  const int qoff = SNk - SN;
+  const int n_kv_all = (SNk + BN - 1) / BN;
+  // causal: the tile's last query row sees keys up to qoff + (qt + 1) BM - 1
+  const int n = causal ? min((qoff + (qt + 1) * BM + BN - 1) / BN, n_kv_all) : n_kv_all;
   const int T = 2 * n;  // tiles over both passes
 
   // Ring order of the loads = the order in which the MMA issuer consumes them. Iteration t of
@@ -231,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int c = 0; c < C::kQKBoxes; ++c)
                 tma_load_4d(sSlot + ks * C::kSlot + (QK8 ? mp * C::kKMapBytes : 0) + c * C::kChunk,
                             &tm_k, bar(bars.slot_full[ks]), k_col_of(P, mp) + C::kQKBoxCols * c,
-                            kvh, seq0 + j * BN, tb);
+                            kvh, kseq0 + j * BN, tb);
             issued = k_load(t, r) + 1;
           }
         }
@@ -245,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int c = 0; c < DV / 64; ++c)
               tma_load_4d(sSlot + vs * C::kSlot + c * C::kVHalfChunk, &tm_v,
-                          bar(bars.slot_full[vs]), 64 * c, kvh, seq0 + jv * BN + 64 * h, tb);
+                          bar(bars.slot_full[vs]), 64 * c, kvh, kseq0 + jv * BN + 64 * h, tb);
             issued = v_load(jv, h) + 1;
           }
         }
@@ -336,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = qt * BM + r;
     const uint32_t tl = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const float sl2 = kp.scale_log2;
-    const int lim = causal ? min(row + 1, SN) : SN;  // keys [0, lim) are visible
+    const int lim = causal ? min(qoff + row + 1, SNk) : SNk;  // keys [0, lim) are visible
     // output row on the token axis: packed (seq0 + row) or batched (b * N + row); `oaddr` is
     // the row's element offset in the (possibly strided) output
     const size_t orow = P.cu_seqlens ? static_cast<size_t>(seq0) + row
@@ -600,9 +615,10 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
   CUtensorMap mq, mk, mv;
   // packed sequences: one batch row of `total` tokens; otherwise [B, N]
   const int mN = p.cu_seqlens ? p.total : p.N, mB = p.cu_seqlens ? 1 : p.B;
+  const int mNk = p.cu_seqlens_k ? p.total_k : mN;  // keys with offsets of their own
   if (!make_map(&mq, p.q, p.q_cols, p.q_heads, mN, mB, p.qs, BM, err, err_len, C::kQKElt) ||
-      !make_map(&mk, p.k, p.k_cols, p.kv_heads, mN, mB, p.ks, BN, err, err_len, C::kQKElt) ||
-      !make_map(&mv, p.v, DV, p.kv_heads, mN, mB, p.vs, BN / 2, err, err_len))
+      !make_map(&mk, p.k, p.k_cols, p.kv_heads, mNk, mB, p.ks, BN, err, err_len, C::kQKElt) ||
+      !make_map(&mv, p.v, DV, p.kv_heads, mNk, mB, p.vs, BN / 2, err, err_len))
     return cudaErrorInvalidValue;
   auto kern = prefill_exact_kernel<DQK, DV, SHARED_K, QK8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
@@ -613,7 +629,8 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
   kp.scale_log2 = kLog2e * p.scale;
   {
     // K/V bytes one (batch, unit) pair streams; keep a group's K/V within ~64 MB of L2
-    const double kv_bytes = static_cast<double>(p.N) * (p.k_cols * C::kQKElt + DV * 2.0);
+    const int nk = p.cu_seqlens_k ? p.max_seqlen_k : p.N;
+    const double kv_bytes = static_cast<double>(nk) * (p.k_cols * C::kQKElt + DV * 2.0);
     long long g = static_cast<long long>((64.0 * 1024 * 1024) / (kv_bytes > 1 ? kv_bytes : 1));
     const long long bu = static_cast<long long>(p.B) * p.units;
     kp.group = static_cast<int>(g < 1 ? 1 : (g > bu ? bu : g));

@@ -338,6 +338,34 @@ DIFFATTN_API int diffattn_fwd_varlen(const void* q, const void* k, const void* v
                                      int dv, int flags, int dtype, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Variable-length prefill with queries and keys of their own lengths: sequence b has Lk keys
+ * (rows cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 of k and v) and Lq <= Lk queries (rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q and out), which are its last Lq positions. With
+ * DIFFATTN_CAUSAL, query i of the sequence sees keys 0 .. Lk - Lq + i (the causal mask aligned
+ * at the end). This covers a prompt computed in chunks against the keys cached so far, and
+ * several new tokens at once over a cache. With Lq = Lk it is diffattn_fwd_varlen; with Lq = 1
+ * the decode of the sequence's last query. The pages give no batching scheme; the operator per
+ * query row is that of diffattn_fwd (P3 "The mechanism, exactly").
+ *   q      : device [total_q, H, 2d];  out : device [total_q, H, dv]
+ *   k      : device [total_k, H, 2d];  v   : device [total_k, H, dv]
+ *   cu_seqlens_q, cu_seqlens_k : device int32 [B + 1] each, non-decreasing from 0. Checked on
+ *            the device: a sequence outside its tensor, with Lq > max_seqlen_q, or with Lk < Lq is
+ *            skipped and reported by diffattn_device_status() as DIFFATTN_ERR_INDEX.
+ *   max_seqlen_q, max_seqlen_k : the longest query and key runs (max_seqlen_q sizes the grid)
+ *   lambda, lambda_init, norm_weight, eps, flags : as diffattn_fwd
+ * Rows of `out` that belong to no sequence are not written.
+ * Supported: dtype DIFFATTN_BF16 (tensor-core exact path), d in {64, 128}, dv = 2d.
+ * Errors: ERR_ARG, ERR_SHAPE (also max_seqlen_q > max_seqlen_k or total_q > total_k), ERR_DTYPE,
+ * ERR_ALIGN, ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_fwd_varlen_qk(const void* q, const void* k, const void* v, void* out,
+                                        const int* cu_seqlens_q, const int* cu_seqlens_k,
+                                        int max_seqlen_q, int max_seqlen_k, int total_q,
+                                        int total_k, const float* lambda, float lambda_init,
+                                        const float* norm_weight, float eps, int B, int H, int d,
+                                        int dv, int flags, int dtype, void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * Prefill with fp8 scores (page "Differential Transformer: softmax can't say zero, so it
  * subtracts", on the attention logits quantized to low bit widths: DIFF's logits are several
  * times smaller relative to their spread, so low-bit score products cost it little).

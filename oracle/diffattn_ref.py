@@ -424,3 +424,40 @@ def diffattn_fwd_varlen(q, k, v, cu_seqlens, lam, lam_init: float, norm_weight=N
             out[s0:s1] = diffattn_fwd(q[None, s0:s1], k[None, s0:s1], v[None, s0:s1], lam, lam_init,
                                       norm_weight, eps, norm, apply_scale, causal)[0]
     return out
+
+
+# --------------------------------------------------------------------------------------------
+# queries and keys of their own lengths (a prompt in chunks, several new tokens over a cache);
+# the operator per query row is unchanged ([P3] "The mechanism, exactly")
+# --------------------------------------------------------------------------------------------
+
+def query_positions(Lq: int, Lk: int) -> np.ndarray:
+    """Positions of a sequence's Lq queries among its Lk keys: they are the last Lq."""
+    return np.arange(Lq) + (Lk - Lq)
+
+
+def diffattn_fwd_varlen_qk(q, k, v, cu_seqlens_q, cu_seqlens_k, lam, lam_init: float,
+                           norm_weight=None, eps: float = 1e-5, norm: bool = True,
+                           apply_scale: bool = True, causal: bool = True):
+    """Packed prefill where sequence b has keys k, v rows cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1
+    and queries q rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1, its last Lq positions; the query
+    at position p sees keys 0 .. p (causal) or all Lk keys. q, k [*, H, 2d] = [Q1|Q2], [K1|K2];
+    v [*, H, dv]. Returns float64 [total_q, H, dv]; rows in no sequence are 0."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    H, two_d = q.shape[1], q.shape[2]
+    d = two_d // 2
+    lam = np.broadcast_to(_f64(lam), (H,))
+    out = np.zeros((q.shape[0], H, v.shape[-1]))
+    for (q0, q1), (k0, k1) in zip(varlen_segments(cu_seqlens_q), varlen_segments(cu_seqlens_k)):
+        if q1 == q0:
+            continue
+        pos = query_positions(q1 - q0, k1 - k0)
+        for h in range(H):
+            for s in range(0, q1 - q0, ROW_BLOCK):
+                r = slice(q0 + s, min(q1, q0 + s + ROW_BLOCK))
+                p = pos[s:s + ROW_BLOCK]
+                S1 = scores(q[r, h, :d], k[k0:k1, h, :d], p, causal)
+                S2 = scores(q[r, h, d:], k[k0:k1, h, d:], p, causal)
+                O = diff_weights(S1, S2, float(lam[h])) @ v[k0:k1, h, :]
+                out[r, h, :] = head_epilogue(O, norm_weight, eps, lam_init, norm, apply_scale)
+    return out

@@ -206,6 +206,14 @@ def test_fused_lambda_varlen_fp8_strided_validation(L):
         return L.diffattn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, cu, maxlen, total, FAKE, 0.5, None,
                                      1e-5, 2, 1, 128, 256, 7, 0, None)
 
+    def varlen_qk(mq=16, mk=32, tq=32, tk=64, cu=FAKE):
+        return L.diffattn_fwd_varlen_qk(FAKE, FAKE, FAKE, FAKE, cu, FAKE, mq, mk, tq, tk, FAKE,
+                                        0.5, None, 1e-5, 2, 2, 128, 256, 7, 0, None)
+    assert varlen_qk(cu=None) == -1
+    assert varlen_qk(mq=64, mk=32) == -2   # more queries than keys
+    assert varlen_qk(tq=64, tk=32) == -2
+    assert varlen_qk(mk=128, tk=64) == -2
+    assert varlen_qk(cu=ctypes.c_void_p(0x10002)) == -4
     assert varlen(cu=None) == -1
     assert varlen(maxlen=64, total=32) == -2
     assert varlen(cu=ctypes.c_void_p(0x10002)) == -4

@@ -431,12 +431,42 @@ def pin_varlen():
     assert np.all(a[20] == 0)
 
 
+def pin_varlen_qk():
+    """Queries as the last Lq of Lk positions: they equal those rows of the full prefill (the
+    earlier queries do not matter), Lq = Lk is the packed prefill, and Lq = 1 is the decode of
+    the last position over all Lk keys."""
+    rng = np.random.default_rng(29)
+    H, d, dv = 2, 4, 8
+    Lks, Lqs = [9, 5, 12, 7], [4, 5, 1, 0]
+    lam = np.array([0.35, 0.8])
+    k = rng.standard_normal((sum(Lks), H, 2 * d)); v = rng.standard_normal((sum(Lks), H, dv))
+    qf = rng.standard_normal((sum(Lks), H, 2 * d))          # a query for every key position
+    cu_k = np.concatenate([[0], np.cumsum(Lks)])
+    # the last Lq query rows of each sequence, packed
+    q = np.concatenate([qf[cu_k[i + 1] - Lqs[i]:cu_k[i + 1]] for i in range(4)])
+    cu_q = np.concatenate([[0], np.cumsum(Lqs)])
+    got = ref.diffattn_fwd_varlen_qk(q, k, v, cu_q, cu_k, lam, 0.3)
+    full = ref.diffattn_fwd_varlen(qf, k, v, cu_k, lam, 0.3)
+    want = np.concatenate([full[cu_k[i + 1] - Lqs[i]:cu_k[i + 1]] for i in range(4)])
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    # Lq = 1 (sequence 2): the decode of its last position over its 12 keys
+    s0 = cu_k[2]
+    dec = ref.diffattn_decode(q[None, cu_q[2], :, :], k[None, s0:s0 + 12], v[None, s0:s0 + 12],
+                              np.array([12]), lam, 0.3)
+    assert np.allclose(got[cu_q[2]], dec[0], rtol=1e-12, atol=1e-12)
+    # non-causal: every query row sees all of its sequence's keys, whatever its position
+    nc = ref.diffattn_fwd_varlen_qk(q, k, v, cu_q, cu_k, lam, 0.3, causal=False)
+    full_nc = ref.diffattn_fwd_varlen(qf, k, v, cu_k, lam, 0.3, causal=False)
+    want_nc = np.concatenate([full_nc[cu_k[i + 1] - Lqs[i]:cu_k[i + 1]] for i in range(4)])
+    assert np.allclose(nc, want_nc, rtol=1e-12, atol=1e-12)
+
+
 PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, pin_lambda_spread,
         pin_softmax_floor, pin_toy_needle_table, pin_worked_example, pin_row_sums,
         pin_lambda_zero_is_softmax_attention, pin_equal_maps_scale_attention, pin_brute_force_tiny,
         pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
-        pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen]
+        pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen, pin_varlen_qk]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -500,6 +530,7 @@ def _mutants():
         "dlam sign": ("diff_attn_head_bwd", bwd_dlam_sign),
         "lambda bwd q/k swapped": ("lambda_full_bwd", lambda_bwd_swapped),
         "varlen: one sequence": ("varlen_segments", lambda cu: [(0, int(np.asarray(cu)[-1]))]),
+        "queries at the first positions": ("query_positions", lambda Lq, Lk: np.arange(Lq)),
         "paged row: page and offset swapped": ("paged_rows", lambda table, sl, ps, b: (
             np.asarray(ref._f64(table)).astype(np.int64)[b, np.arange(int(np.asarray(ref._f64(sl))[b])) % ps]
             * ps + np.arange(int(np.asarray(ref._f64(sl))[b])) // ps)),

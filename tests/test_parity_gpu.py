@@ -300,6 +300,76 @@ def test_fwd_varlen_bad_offsets_are_reported():
     da.diffattn_device_status()
 
 
+@pytest.mark.parametrize("lens_q,lens_k,causal", [
+    ([300, 1, 100, 0, 640], [300, 700, 357, 90, 640], True),   # Lq = Lk, decode-like, ragged
+    ([128, 77], [1000, 77], True),                              # a chunk far into a long prefix
+    ([50, 200], [260, 200], False)])
+def test_fwd_varlen_qk(lens_q, lens_k, causal):
+    """Queries as the last Lq of each sequence's Lk keys, against the oracle; keys past a
+    sequence's prefix and packed rows of other sequences are never seen."""
+    H = 2
+    tq, tk = sum(lens_q) + 2, sum(lens_k) + 5
+    gen = make_prefill_inputs(1, tk, H, 128, 256, seed=211 + len(lens_q), causal=causal)
+    k, v = gen.k[0], gen.v[0]
+    q = make_prefill_inputs(1, tq, H, 128, 256, seed=213 + len(lens_q)).q[0]
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lens_q)]), dtype=torch.int32)
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lens_k)]), dtype=torch.int32)
+    lam = torch.tensor([0.4, 0.8], dtype=torch.float32)
+    li = ref.lambda_init(12)
+    got = da.diffattn_fwd_varlen_qk(q.to(DEV), k.to(DEV), v.to(DEV), cu_q.to(DEV), cu_k.to(DEV),
+                                    lam.to(DEV), li, causal=causal)
+    want = ref.diffattn_fwd_varlen_qk(q, k, v, cu_q, cu_k, lam.numpy(), li, causal=causal)
+    n = sum(lens_q)
+    assert_bf16(got[:n], want[:n])
+    assert torch.count_nonzero(got[n:]) == 0
+    da.diffattn_device_status()
+
+
+def test_fwd_varlen_qk_chunked_prompt():
+    """A prompt of 1000 tokens computed as three chunks (300, 450, 250 queries against the keys
+    so far) gives the full causal prefill's rows; a chunk with Lq = Lk is bit-equal to
+    diffattn_fwd_varlen."""
+    H, N = 2, 1000
+    inp = make_prefill_inputs(1, N, H, 128, 256, seed=217)
+    q, k, v = inp.q[0], inp.k[0], inp.v[0]
+    lam = torch.tensor([0.5, 0.7], dtype=torch.float32, device=DEV)
+    li = ref.lambda_init(12)
+    full = ref.diffattn_fwd(inp.q, inp.k, inp.v, lam.cpu().numpy(), li)[0]
+    cuts = [0, 300, 750, 1000]
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        cu_q = torch.tensor([0, b - a], dtype=torch.int32, device=DEV)
+        cu_k = torch.tensor([0, b], dtype=torch.int32, device=DEV)
+        got = da.diffattn_fwd_varlen_qk(q[a:b].contiguous().to(DEV), k[:b].contiguous().to(DEV),
+                                        v[:b].contiguous().to(DEV), cu_q, cu_k, lam, li)
+        assert_bf16(got, full[a:b])
+    cu = torch.tensor([0, 300], dtype=torch.int32, device=DEV)
+    same = da.diffattn_fwd_varlen_qk(q[:300].contiguous().to(DEV), k[:300].contiguous().to(DEV),
+                                     v[:300].contiguous().to(DEV), cu, cu, lam, li)
+    plain = da.diffattn_fwd_varlen(q[:300].contiguous().to(DEV), k[:300].contiguous().to(DEV),
+                                   v[:300].contiguous().to(DEV), cu, lam, li)
+    assert torch.equal(same, plain)
+
+
+def test_fwd_varlen_qk_fewer_keys_than_queries_is_reported():
+    """A sequence with Lk < Lq is skipped and reported as DIFFATTN_ERR_INDEX; the others are
+    computed."""
+    inp = make_prefill_inputs(1, 512, 1, 128, 256, seed=219)
+    q, k, v = inp.q[0].to(DEV), inp.k[0].to(DEV), inp.v[0].to(DEV)
+    cu_q = torch.tensor([0, 100, 300], dtype=torch.int32, device=DEV)
+    cu_k = torch.tensor([0, 200, 350], dtype=torch.int32, device=DEV)  # sequence 1: 150 < 200
+    lam = torch.tensor([0.5], device=DEV)
+    out = da.diffattn_fwd_varlen_qk(q[:300], k[:350], v[:350], cu_q, cu_k, lam, 0.5,
+                                    max_seqlen_q=200, max_seqlen_k=200)
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_device_status()
+    assert e.value.status == -9  # DIFFATTN_ERR_INDEX
+    da.diffattn_device_status()
+    assert torch.count_nonzero(out[100:300]) == 0
+    want = ref.diffattn_fwd_varlen_qk(inp.q[0][:100], inp.k[0][:200], inp.v[0][:200],
+                                      np.array([0, 100]), np.array([0, 200]), np.array([0.5]), 0.5)
+    assert_bf16(out[:100], want)
+
+
 # ------------------------------------------------------------------------------------------
 # decode over a paged cache
 # ------------------------------------------------------------------------------------------
