@@ -86,6 +86,8 @@ _SIGNATURES = {
     "diffattn_fwd_varlen_qk": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int] * 4
                                + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
                                + [ctypes.c_int] * 6 + [ctypes.c_void_p]),
+    "diffattn_v2_fwd_varlen": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 10
+                               + [ctypes.c_void_p]),
     "diffattn_fwd_fused_lambda": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int] * 3
                                   + [ctypes.c_void_p, ctypes.c_float] + [ctypes.c_int] * 7
                                   + [ctypes.c_void_p]),
@@ -581,6 +583,44 @@ def diffattn_fwd_varlen_qk(q, k, v, cu_seqlens_q, cu_seqlens_k, lam, lambda_init
                                         max(1, int(max_seqlen_k)), total_q, total_k, _ptr(lam),
                                         float(lambda_init), _ptr(norm_weight), float(eps), B, H, d,
                                         dv, _train_flags(causal, norm, scale), DIFFATTN_BF16,
+                                        _stream(stream)))
+    return out
+
+
+def diffattn_v2_fwd_varlen(q, k, v, lam_logit, cu_seqlens_q, cu_seqlens_k=None, max_seqlen_q=None,
+                           max_seqlen_k=None, causal: bool = True, out=None, stream=None):
+    """DIFF V2 over packed sequences: q [total_q, Hq, d], k, v [total_k, Hkv, d], lam_logit
+    [total_q, Hq/2]; cu_seqlens_k None means the keys share the queries' offsets."""
+    _dev("q", q, torch.bfloat16)
+    total_q, Hq, d = q.shape
+    _dev("k", k, torch.bfloat16)
+    _dev("v", v, torch.bfloat16)
+    total_k, Hkv = k.shape[0], k.shape[1]
+    if k.shape != (total_k, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must both be [total_k, Hkv, d]")
+    _dev("lam_logit", lam_logit, torch.float32)
+    if lam_logit.shape != (total_q, Hq // 2):
+        raise ValueError("lam_logit must be [total_q, Hq/2]")
+    _dev("cu_seqlens_q", cu_seqlens_q, torch.int32)
+    B = cu_seqlens_q.numel() - 1
+    if max_seqlen_q is None:
+        max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B > 0 else 1
+    if cu_seqlens_k is not None:
+        _dev("cu_seqlens_k", cu_seqlens_k, torch.int32)
+        if cu_seqlens_k.numel() != B + 1:
+            raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B + 1 entries")
+        if max_seqlen_k is None:
+            max_seqlen_k = int((cu_seqlens_k[1:] - cu_seqlens_k[:-1]).max().item()) if B > 0 else 1
+    else:
+        max_seqlen_k = max_seqlen_q
+    if out is None:
+        out = torch.zeros((total_q, Hq // 2, d), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    _check(lib().diffattn_v2_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_logit), _ptr(out),
+                                        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                        max(1, int(max_seqlen_q)), max(1, int(max_seqlen_k)),
+                                        total_q, total_k, B, Hq, Hkv, d,
+                                        DIFFATTN_CAUSAL if causal else 0, DIFFATTN_BF16,
                                         _stream(stream)))
     return out
 

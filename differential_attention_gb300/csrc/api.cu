@@ -806,6 +806,64 @@ DIFFATTN_API int diffattn_fwd_varlen_qk(const void* q, const void* k, const void
   return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
 }
 
+DIFFATTN_API int diffattn_v2_fwd_varlen(const void* q, const void* k, const void* v,
+                                        const float* lam_logit, void* out,
+                                        const int* cu_seqlens_q, const int* cu_seqlens_k,
+                                        int max_seqlen_q, int max_seqlen_k, int total_q,
+                                        int total_k, int B, int Hq, int Hkv, int d, int flags,
+                                        int dtype, void* stream) {
+  const char* fn = "diffattn_v2_fwd_varlen";
+  if (!q || !k || !v || !lam_logit || !out || !cu_seqlens_q)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (flags & ~DIFFATTN_CAUSAL) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);
+  if (!cu_seqlens_k) {  // the keys share the query offsets
+    max_seqlen_k = max_seqlen_q;
+    total_k = total_q;
+  }
+  if (B < 1 || Hq < 2 || Hkv < 1 || max_seqlen_q < 1 || total_q < 1 || max_seqlen_q > total_q ||
+      max_seqlen_k < max_seqlen_q || total_k < total_q || max_seqlen_k > total_k)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need B, Hkv >= 1, Hq >= 2, 1 <= max_seqlen_q <= total_q, "
+                "max_seqlen_q <= max_seqlen_k <= total_k and total_q <= total_k", fn);
+  if (Hq % 2 != 0 || Hq % Hkv != 0 || (Hq / Hkv) % 2 != 0)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even (got Hq=%d Hkv=%d)",
+                fn, Hq, Hkv);
+  if (!(d == 64 || d == 128)) return fail(DIFFATTN_ERR_SHAPE, "%s: need d in {64, 128}", fn);
+  const long long tiles = (static_cast<long long>(max_seqlen_q) + 127) / 128 * B * (Hq / 2);
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(total_k) * Hq > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: problem too large for one launch", fn);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lam_logit, 4) || !aligned(cu_seqlens_q, 4) || (cu_seqlens_k && !aligned(cu_seqlens_k, 4)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = max_seqlen_q;
+  p.units = Hq / 2;
+  p.dqk = d;
+  p.dv = d;
+  p.mode = da::MODE_V2;
+  p.q_heads = Hq;
+  p.kv_heads = Hkv;
+  p.q_cols = d;
+  p.k_cols = d;
+  p.group = Hq / Hkv;
+  p.lam_logit = lam_logit;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  p.cu_seqlens = cu_seqlens_q;
+  p.total = total_q;
+  p.cu_seqlens_k = cu_seqlens_k;
+  p.total_k = total_k;
+  p.max_seqlen_k = max_seqlen_k;
+  return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
+}
+
 DIFFATTN_API int diffattn_fwd_fp8(const void* q, const void* k, const void* v, void* out,
                                   float q_descale, float k_descale, const float* lambda,
                                   float lambda_init, const float* norm_weight, float eps, int B,

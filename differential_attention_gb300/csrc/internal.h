@@ -50,17 +50,18 @@ struct Problem {
   // the longest sequence (it sizes the grid) and `total` the packed length.
   const int* cu_seqlens;
   int total;
-  // keys with offsets of their own (null: the keys share cu_seqlens): sequence b's keys are rows
-  // cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 of k/v [total_k, H, *], and its Lq queries are the
-  // last Lq of its Lk >= Lq positions (causal: query i sees keys 0 .. Lk - Lq + i)
-  const int* cu_seqlens_k;
-  int total_k, max_seqlen_k;
   // q and k in fp8 e4m3 (V1, exact path): the score products run as kind::f8f6f4; `scale`
   // then also carries the per-tensor dequantisation factors
   bool qk_fp8;
   // element strides (batch, token, head) of q, k, v and out; the last dimension is contiguous.
   // All zero: the dense layout (filled in by fill_dense_strides).
   long long qs[3], ks[3], vs[3], os[3];
+  // keys with offsets of their own (null: the keys share cu_seqlens): sequence b's keys are rows
+  // cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 of k/v [total_k, H, *], and its Lq queries are the
+  // last Lq of its Lk >= Lq positions (causal: query i sees keys 0 .. Lk - Lq + i). Last in the
+  // struct, so that adding them moved no other field of the kernels' parameters.
+  const int* cu_seqlens_k;
+  int total_k, max_seqlen_k;
 };
 
 __host__ inline void fill_dense_strides(Problem& p) {

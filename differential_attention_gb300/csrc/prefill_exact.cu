@@ -99,7 +99,11 @@ struct KParams {
   float scale_log2;
 };
 
-template <int DQK, int DV, bool SHARED_K, bool QK8>
+// SHARED_K: the V2 operator (both maps read one K tile); without it, V1 (launch_prefill_exact
+// picks the instantiation by mode). KOFF: keys with offsets of their own (cu_seqlens_k). A
+// separate instantiation: the extra live values made the default variants spill at their
+// 96-register budget.
+template <int DQK, int DV, bool SHARED_K, bool QK8, bool KOFF>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_exact_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -138,32 +142,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   // queries are the sequence's last SN positions: query row i sees keys [0, qoff + i], with
   // qoff = SNk - SN.
   int seq0 = 0, SN = P.N, tb = b;
-  int kseq0 = 0, SNk = P.N;
   if (P.cu_seqlens) {
     seq0 = P.cu_seqlens[b];
     SN = P.cu_seqlens[b + 1] - seq0;
     tb = 0;
-    kseq0 = seq0;
-    SNk = SN;
-    if (P.cu_seqlens_k) {
-      kseq0 = P.cu_seqlens_k[b];
-      SNk = P.cu_seqlens_k[b + 1] - kseq0;
-    }
-    // offsets are device data: a sequence outside [0, total) or longer than the stated maximum,
-    // or with fewer keys than queries, is reported (DEV_BAD_INDEX) and skipped, so no store
-    // leaves the output
-    const int ktot = P.cu_seqlens_k ? P.total_k : P.total;
-    if (seq0 < 0 || SN < 0 || SN > P.N || seq0 > P.total - SN || kseq0 < 0 || SNk < SN ||
-        kseq0 > ktot - SNk) {
+    // offsets are device data: a sequence outside [0, total) or longer than the stated maximum
+    // is reported (DEV_BAD_INDEX) and skipped, so no store leaves the output
+    if (seq0 < 0 || SN < 0 || SN > P.N || seq0 > P.total - SN) {
       if (threadIdx.x == 0 && qt == 0) flag_device_error(DEV_BAD_INDEX);
       return;
     }
     if (qt * BM >= SN) return;  // a tile past this sequence's end: nothing to do (uniform)
   }
-  const int qoff = SNk - SN;
+  int kseq0 = seq0, SNk = SN;
+  if constexpr (KOFF) {
+    kseq0 = P.cu_seqlens_k[b];
+    SNk = P.cu_seqlens_k[b + 1] - kseq0;
+    // keys outside k, or fewer keys than queries: reported and skipped like the query offsets
+    if (kseq0 < 0 || SNk < SN || kseq0 > P.total_k - SNk) {
+      if (threadIdx.x == 0 && qt == 0) flag_device_error(DEV_BAD_INDEX);
+      return;
+    }
+  }
+  const int qoff = KOFF ? SNk - SN : 0;
   const int n_kv_all = (SNk + BN - 1) / BN;
   // causal: the tile's last query row sees keys up to qoff + (qt + 1) BM - 1
-  const int n = causal ? min((qoff + (qt + 1) * BM + BN - 1) / BN, n_kv_all) : n_kv_all;
+  const int n = !causal ? n_kv_all
+                        : KOFF ? min((qoff + (qt + 1) * BM + BN - 1) / BN, n_kv_all)
+                               : min(qt + 1, n_kv_all);  // BM == BN
   const int T = 2 * n;  // tiles over both passes
 
   // Ring order of the loads = the order in which the MMA issuer consumes them. Iteration t of
@@ -388,8 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (P.mode == MODE_V1) {
         lam = P.lam_vec[0] ? lam_fused : P.lambda[u];
-      } else if (row < P.N) {
-        const float z = P.lam_logit[(static_cast<size_t>(b) * P.N + row) * P.units + u];
+      } else if (row < (SHARED_K ? SN : P.N)) {
+        // V2: the sigmoid of this token's logit for pair u (packed sequences: token seq0 + row;
+        // the select exists only in the V2 instantiations, as changes here shifted the V1 code)
+        size_t t = static_cast<size_t>(b) * P.N + row;
+        if constexpr (SHARED_K) {
+          if (P.cu_seqlens) t = orow;
+        }
+        const float z = P.lam_logit[t * P.units + u];
         lam = 1.f / (1.f + expf(-z));
       }
       named_barrier_sync(1, kSoftmaxThreads);  // all have read the scratch before D overwrites it
@@ -609,7 +621,7 @@ static bool make_map(CUtensorMap* m, const void* base, int cols, int heads, int 
   return encode_tmap_4d(m, type, base, dims, strides, box, err, err_len);
 }
 
-template <int DQK, int DV, bool SHARED_K, bool QK8 = false>
+template <int DQK, int DV, bool SHARED_K, bool QK8 = false, bool KOFF = false>
 static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
   using C = Cfg<DQK, DV, SHARED_K, QK8>;
   CUtensorMap mq, mk, mv;
@@ -620,7 +632,7 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
       !make_map(&mk, p.k, p.k_cols, p.kv_heads, mNk, mB, p.ks, BN, err, err_len, C::kQKElt) ||
       !make_map(&mv, p.v, DV, p.kv_heads, mNk, mB, p.vs, BN / 2, err, err_len))
     return cudaErrorInvalidValue;
-  auto kern = prefill_exact_kernel<DQK, DV, SHARED_K, QK8>;
+  auto kern = prefill_exact_kernel<DQK, DV, SHARED_K, QK8, KOFF>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   KParams kp;
@@ -651,11 +663,21 @@ cudaError_t launch_prefill_exact(const Problem& p, cudaStream_t s, char* err, si
       if (p.dqk == 128 && p.dv == 256) return exact::launch_cfg<128, 256, false, true>(p, s, err, err_len);
       return cudaErrorNotSupported;
     }
-    if (p.dqk == 128 && p.dv == 256) return exact::launch_cfg<128, 256, false>(p, s, err, err_len);
-    if (p.dqk == 64 && p.dv == 128) return exact::launch_cfg<64, 128, false>(p, s, err, err_len);
+    const bool koff = p.cu_seqlens && p.cu_seqlens_k;
+    if (p.dqk == 128 && p.dv == 256)
+      return koff ? exact::launch_cfg<128, 256, false, false, true>(p, s, err, err_len)
+                  : exact::launch_cfg<128, 256, false>(p, s, err, err_len);
+    if (p.dqk == 64 && p.dv == 128)
+      return koff ? exact::launch_cfg<64, 128, false, false, true>(p, s, err, err_len)
+                  : exact::launch_cfg<64, 128, false>(p, s, err, err_len);
   } else {
-    if (p.dqk == 128 && p.dv == 128) return exact::launch_cfg<128, 128, true>(p, s, err, err_len);
-    if (p.dqk == 64 && p.dv == 64) return exact::launch_cfg<64, 64, true>(p, s, err, err_len);
+    const bool koff = p.cu_seqlens && p.cu_seqlens_k;
+    if (p.dqk == 128 && p.dv == 128)
+      return koff ? exact::launch_cfg<128, 128, true, false, true>(p, s, err, err_len)
+                  : exact::launch_cfg<128, 128, true>(p, s, err, err_len);
+    if (p.dqk == 64 && p.dv == 64)
+      return koff ? exact::launch_cfg<64, 64, true, false, true>(p, s, err, err_len)
+                  : exact::launch_cfg<64, 64, true>(p, s, err, err_len);
   }
   return cudaErrorNotSupported;
 }

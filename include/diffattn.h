@@ -366,6 +366,29 @@ DIFFATTN_API int diffattn_fwd_varlen_qk(const void* q, const void* k, const void
                                         int dv, int flags, int dtype, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * DIFF V2 over packed sequences (page "Differential Transformer: softmax can't say zero, so it
+ * subtracts", section "DIFF V2: what the authors changed"): diffattn_v2_fwd per sequence, the
+ * sequences packed along the token axis, optionally with keys of their own lengths as for
+ * diffattn_fwd_varlen_qk (a sequence's Lq queries are its last Lq of Lk positions).
+ *   q : device [total_q, Hq, d];  k, v : device [total_k, Hkv, d]
+ *   lam_logit : device fp32 [total_q, Hq/2] (per token and pair, before the sigmoid)
+ *   out : device [total_q, Hq/2, d]
+ *   cu_seqlens_q : device int32 [B + 1];  cu_seqlens_k : device int32 [B + 1], or NULL for keys
+ *            at the queries' offsets (max_seqlen_k and total_k are then ignored). Checked on the
+ *            device as for diffattn_fwd_varlen_qk (DIFFATTN_ERR_INDEX).
+ *   flags : DIFFATTN_CAUSAL or 0
+ * Rows of `out` that belong to no sequence are not written. Supported: dtype DIFFATTN_BF16
+ * (tensor-core exact path), d in {64, 128}, Hq/Hkv even.
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_v2_fwd_varlen(const void* q, const void* k, const void* v,
+                                        const float* lam_logit, void* out,
+                                        const int* cu_seqlens_q, const int* cu_seqlens_k,
+                                        int max_seqlen_q, int max_seqlen_k, int total_q,
+                                        int total_k, int B, int Hq, int Hkv, int d, int flags,
+                                        int dtype, void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * Prefill with fp8 scores (page "Differential Transformer: softmax can't say zero, so it
  * subtracts", on the attention logits quantized to low bit widths: DIFF's logits are several
  * times smaller relative to their spread, so low-bit score products cost it little).

@@ -461,3 +461,31 @@ def diffattn_fwd_varlen_qk(q, k, v, cu_seqlens_q, cu_seqlens_k, lam, lam_init: f
                 O = diff_weights(S1, S2, float(lam[h])) @ v[k0:k1, h, :]
                 out[r, h, :] = head_epilogue(O, norm_weight, eps, lam_init, norm, apply_scale)
     return out
+
+
+def diffattn_v2_fwd_varlen(q, k, v, lam_logit, cu_seqlens_q, cu_seqlens_k=None,
+                           causal: bool = True):
+    """`diffattn_v2_fwd` per packed sequence: q [total_q, Hq, d], k, v [total_k, Hkv, d],
+    lam_logit [total_q, Hq/2]; sequence b's queries are rows cu_seqlens_q[b] .. of q, its keys
+    rows cu_seqlens_k[b] .. of k and v (cu_seqlens_q when None), the queries being its last Lq
+    positions. Returns float64 [total_q, Hq/2, d]; rows in no sequence are 0."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    sig = sigmoid(lam_logit)
+    out = np.zeros((q.shape[0], Hq // 2, v.shape[-1]))
+    cu_k = cu_seqlens_q if cu_seqlens_k is None else cu_seqlens_k
+    for (q0, q1), (k0, k1) in zip(varlen_segments(cu_seqlens_q), varlen_segments(cu_k)):
+        if q1 == q0:
+            continue
+        pos = query_positions(q1 - q0, k1 - k0)
+        for p in range(Hq // 2):
+            g = v2_kv_head(p, Hq, Hkv)
+            kg, vg = k[k0:k1, g], v[k0:k1, g]
+            for s in range(0, q1 - q0, ROW_BLOCK):
+                r = slice(q0 + s, min(q1, q0 + s + ROW_BLOCK))
+                ps = pos[s:s + ROW_BLOCK]
+                a1 = softmax_rows(scores(q[r, 2 * p], kg, ps, causal)) @ vg
+                a2 = softmax_rows(scores(q[r, 2 * p + 1], kg, ps, causal)) @ vg
+                out[r, p, :] = a1 - sig[r, p][:, None] * a2
+    return out

@@ -214,6 +214,12 @@ def test_fused_lambda_varlen_fp8_strided_validation(L):
     assert varlen_qk(tq=64, tk=32) == -2
     assert varlen_qk(mk=128, tk=64) == -2
     assert varlen_qk(cu=ctypes.c_void_p(0x10002)) == -4
+    def v2var(cu=FAKE, Hq=8, Hkv=2, flags=1):
+        return L.diffattn_v2_fwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, cu, None, 16, 16, 32, 32, 2,
+                                        Hq, Hkv, 128, flags, 0, None)
+    assert v2var(cu=None) == -1
+    assert v2var(flags=4) == -1            # only DIFFATTN_CAUSAL
+    assert v2var(Hq=6, Hkv=2) == -2        # a pair split across GQA groups
     assert varlen(cu=None) == -1
     assert varlen(maxlen=64, total=32) == -2
     assert varlen(cu=ctypes.c_void_p(0x10002)) == -4

@@ -461,12 +461,36 @@ def pin_varlen_qk():
     assert np.allclose(nc, want_nc, rtol=1e-12, atol=1e-12)
 
 
+def pin_v2_varlen():
+    """V2 over packed sequences: with shared offsets each sequence equals the batched V2 prefill
+    of that sequence alone; with keys of their own, the queries equal the last rows of the full
+    sequence's V2 prefill."""
+    rng = np.random.default_rng(31)
+    Hq, Hkv, d = 8, 2, 4
+    lens = [6, 1, 9]
+    T = sum(lens)
+    q = rng.standard_normal((T, Hq, d)); k = rng.standard_normal((T, Hkv, d))
+    v = rng.standard_normal((T, Hkv, d)); lam = rng.standard_normal((T, Hq // 2))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    got = ref.diffattn_v2_fwd_varlen(q, k, v, lam, cu)
+    for i in range(3):
+        a, b = cu[i], cu[i + 1]
+        one = ref.diffattn_v2_fwd(q[None, a:b], k[None, a:b], v[None, a:b], lam[None, a:b])[0]
+        assert np.allclose(got[a:b], one, rtol=1e-12, atol=1e-12)
+    # sequence 2 (9 positions) with only its last 4 queries
+    a, b = cu[2], cu[3]
+    cu_q, cu_k = np.array([0, 4]), np.array([0, 9])
+    part = ref.diffattn_v2_fwd_varlen(q[b - 4:b], k[a:b], v[a:b], lam[b - 4:b], cu_q, cu_k)
+    assert np.allclose(part, got[b - 4:b], rtol=1e-12, atol=1e-12)
+
+
 PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, pin_lambda_spread,
         pin_softmax_floor, pin_toy_needle_table, pin_worked_example, pin_row_sums,
         pin_lambda_zero_is_softmax_attention, pin_equal_maps_scale_attention, pin_brute_force_tiny,
         pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
-        pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen, pin_varlen_qk]
+        pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen, pin_varlen_qk,
+        pin_v2_varlen]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])

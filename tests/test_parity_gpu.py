@@ -370,6 +370,37 @@ def test_fwd_varlen_qk_fewer_keys_than_queries_is_reported():
     assert_bf16(out[:100], want)
 
 
+@pytest.mark.parametrize("lens_q,lens_k,causal", [([300, 1, 129, 0, 200], None, True),
+                                                   ([100, 64], [700, 64], True),
+                                                   ([50, 130], [50, 300], False)])
+def test_v2_fwd_varlen(lens_q, lens_k, causal):
+    """V2 over packed sequences (shared offsets, and keys of their own) against the oracle."""
+    Hq, Hkv, d = 8, 2, 128
+    tq = sum(lens_q) + 2
+    tk = tq if lens_k is None else sum(lens_k) + 3
+    g = torch.Generator().manual_seed(223 + len(lens_q))
+    q = (torch.randn((tq, Hq, d), generator=g) / d ** 0.5).to(torch.bfloat16)
+    k = (torch.randn((tk, Hkv, d), generator=g) / d ** 0.5).to(torch.bfloat16)
+    v = (torch.randn((tk, Hkv, d), generator=g) / d ** 0.5).to(torch.bfloat16)
+    lam = torch.randn((tq, Hq // 2), generator=g, dtype=torch.float32)
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lens_q)]), dtype=torch.int32)
+    cu_k = None if lens_k is None else torch.tensor(np.concatenate([[0], np.cumsum(lens_k)]),
+                                                    dtype=torch.int32)
+    got = da.diffattn_v2_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), lam.to(DEV), cu_q.to(DEV),
+                                    None if cu_k is None else cu_k.to(DEV), causal=causal)
+    want = ref.diffattn_v2_fwd_varlen(q, k, v, lam, cu_q, cu_k, causal=causal)
+    n = sum(lens_q)
+    assert_bf16(got[:n], want[:n])
+    assert torch.count_nonzero(got[n:]) == 0
+    if lens_k is None:  # sequence 2 alone through the batched V2 prefill: the same numbers
+        a, b = int(cu_q[2]), int(cu_q[3])
+        one = da.diffattn_v2_fwd(q[None, a:b].contiguous().to(DEV), k[None, a:b].contiguous().to(DEV),
+                                 v[None, a:b].contiguous().to(DEV), lam[None, a:b].contiguous().to(DEV),
+                                 causal=causal)
+        assert torch.equal(got[a:b], one[0])
+    da.diffattn_device_status()
+
+
 # ------------------------------------------------------------------------------------------
 # decode over a paged cache
 # ------------------------------------------------------------------------------------------
