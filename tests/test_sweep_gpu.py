@@ -140,3 +140,37 @@ def test_sweep_backward(case):
                             norm=norm, apply_scale=scale, causal=causal)
     for name in ("dq", "dk", "dv"):
         assert_grad(g[name], want[name], name=name)
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_sweep_packed_chunks(case):
+    """Packed sequences whose queries are the last Lq of Lk positions (V1 and V2), random
+    lengths including Lq = 0, Lq = 1 and Lq = Lk."""
+    rng = np.random.default_rng(1500 + case)
+    B = int(rng.integers(1, 5))
+    lens_k = [int(rng.integers(1, 600)) for _ in range(B)]
+    lens_q = [int(rng.choice([0, 1, lk, int(rng.integers(0, lk + 1))])) for lk in lens_k]
+    lens_q[0] = max(1, lens_q[0])
+    causal = bool(rng.integers(0, 2))
+    tq, tk = sum(lens_q), sum(lens_k)
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lens_q)]), dtype=torch.int32)
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lens_k)]), dtype=torch.int32)
+    H = int(rng.integers(1, 3))
+    kv = make_prefill_inputs(1, tk, H, 128, 256, seed=1500 + case, causal=causal)
+    q = make_prefill_inputs(1, tq, H, 128, 256, seed=1550 + case).q[0]
+    lam = rng.uniform(0.0, 1.1, H)
+    li = ref.lambda_init(12)
+    got = da.diffattn_fwd_varlen_qk(q.to(DEV), kv.k[0].to(DEV), kv.v[0].to(DEV), cu_q.to(DEV),
+                                    cu_k.to(DEV), torch.tensor(lam, dtype=torch.float32, device=DEV),
+                                    li, causal=causal)
+    assert_bf16(got, ref.diffattn_fwd_varlen_qk(q, kv.k[0], kv.v[0], cu_q, cu_k, lam, li,
+                                                causal=causal))
+    Hkv = int(rng.integers(1, 3))
+    Hq = Hkv * int(rng.choice([2, 4]))
+    v2 = make_v2_inputs(1, tk, Hq, Hkv, 128, seed=1570 + case, causal=causal)
+    v2q = make_v2_inputs(1, tq, Hq, Hkv, 128, seed=1590 + case)
+    got2 = da.diffattn_v2_fwd_varlen(v2q.q[0].to(DEV), v2.k[0].to(DEV), v2.v[0].to(DEV),
+                                     v2q.lam_logit[0].to(DEV), cu_q.to(DEV), cu_k.to(DEV),
+                                     causal=causal)
+    assert_bf16(got2, ref.diffattn_v2_fwd_varlen(v2q.q[0], v2.k[0], v2.v[0], v2q.lam_logit[0],
+                                                 cu_q, cu_k, causal=causal))
