@@ -643,7 +643,45 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "roofline": {"bound": "tensor", "achieved": ctf, "peak": peak_tf, "unit": "TFLOP/s",
                          "frac": ctf / peak_tf, "flops_per_launch": cflops},
             "gpu_launches": n_steps}
-        del kin, out, q, k, v
+
+        # the same chunk with the prompts' keys in a pool of 256-token pages in a random order
+        ps = 256
+        mp = Lk // ps
+        k_pool = kin.k.reshape(c["B"] * mp, ps, c["H"], 2 * c["d"])
+        v_pool = kin.v.reshape(c["B"] * mp, ps, c["H"], c["dv"])
+        gp = torch.Generator(device="cpu")
+        gp.manual_seed(8200 + rank)
+        table = torch.randperm(c["B"] * mp, generator=gp).to(torch.int32).view(c["B"], mp).to(dev)
+        # the pool's pages in table order hold the prompts' keys: page table[b, i] <- (b, i)
+        k_pool = k_pool[torch.argsort(table.flatten())].contiguous()
+        v_pool = v_pool[torch.argsort(table.flatten())].contiguous()
+        sk = torch.full((c["B"],), Lk, dtype=torch.int32, device=dev)
+
+        def pstep():
+            da.diffattn_fwd_paged(q, k_pool, v_pool, cu_q, sk, table, lam, li, max_seqlen_q=Lq,
+                                  max_seqlen_k=Lk, out=out)
+
+        for _ in range(args.warmup):
+            pstep()
+        barrier()
+        evs = [(ev(), ev()) for _ in range(n_steps)]
+        for i in range(n_steps):
+            evs[i][0].record(stream)
+            pstep()
+            evs[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        ptf = cflops / (ms * 1e-3) / 1e12
+        line["paged_prefill"] = {
+            "metric": "DiffAttn fwd TFLOP/s", "value": world * ptf, "unit": "TFLOP/s",
+            "ms_per_call": ms,
+            "workload": f"the varlen_qk chunk with the keys in {ps}-token pages placed in a random "
+                        "order in the pool",
+            "roofline": {"bound": "tensor", "achieved": ptf, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": ptf / peak_tf, "flops_per_launch": cflops},
+            "gpu_launches": n_steps}
+        del kin, out, q, k, v, k_pool, v_pool, table
         torch.cuda.empty_cache()
 
     # ======================= training step: forward (saving statistics) + backward ==========

@@ -88,6 +88,11 @@ _SIGNATURES = {
                                + [ctypes.c_int] * 6 + [ctypes.c_void_p]),
     "diffattn_v2_fwd_varlen": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 10
                                + [ctypes.c_void_p]),
+    "diffattn_fwd_paged": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 6
+                           + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
+                           + [ctypes.c_int] * 6 + [ctypes.c_void_p]),
+    "diffattn_v2_fwd_paged": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int] * 12
+                              + [ctypes.c_void_p]),
     "diffattn_fwd_fused_lambda": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int] * 3
                                   + [ctypes.c_void_p, ctypes.c_float] + [ctypes.c_int] * 7
                                   + [ctypes.c_void_p]),
@@ -622,6 +627,80 @@ def diffattn_v2_fwd_varlen(q, k, v, lam_logit, cu_seqlens_q, cu_seqlens_k=None, 
                                         total_q, total_k, B, Hq, Hkv, d,
                                         DIFFATTN_CAUSAL if causal else 0, DIFFATTN_BF16,
                                         _stream(stream)))
+    return out
+
+
+def _paged_args(q, k_pool, v_pool, cu_seqlens_q, seqlens_k, block_table, max_seqlen_q,
+                max_seqlen_k):
+    _dev("k_pool", k_pool, torch.bfloat16)
+    _dev("v_pool", v_pool, torch.bfloat16)
+    _dev("cu_seqlens_q", cu_seqlens_q, torch.int32)
+    _dev("seqlens_k", seqlens_k, torch.int32)
+    _dev("block_table", block_table, torch.int32)
+    B = cu_seqlens_q.numel() - 1
+    if seqlens_k.shape != (B,) or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("seqlens_k must be [B] and block_table [B, max_pages]")
+    if max_seqlen_q is None:
+        max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B > 0 else 1
+    if max_seqlen_k is None:
+        max_seqlen_k = int(seqlens_k.max().item()) if B > 0 else 1
+    return B, max(1, int(max_seqlen_q)), max(1, int(max_seqlen_k))
+
+
+def diffattn_fwd_paged(q, k_pool, v_pool, cu_seqlens_q, seqlens_k, block_table, lam,
+                       lambda_init: float = 0.0, max_seqlen_q=None, max_seqlen_k=None,
+                       norm_weight=None, eps: float = 1e-5, causal: bool = True,
+                       norm: bool = True, scale: bool = True, out=None, stream=None):
+    """Packed queries q [total_q, H, 2d] against keys in a page pool: k_pool [num_pages,
+    page_size, H, 2d], v_pool [.., H, dv]; sequence b has seqlens_k[b] keys through
+    block_table[b] and its queries are the last of those positions."""
+    _dev("q", q, torch.bfloat16)
+    total_q, H, two_d = q.shape
+    d = two_d // 2
+    B, mq, mk = _paged_args(q, k_pool, v_pool, cu_seqlens_q, seqlens_k, block_table,
+                            max_seqlen_q, max_seqlen_k)
+    num_pages, page_size, dv = k_pool.shape[0], k_pool.shape[1], v_pool.shape[-1]
+    if k_pool.shape != (num_pages, page_size, H, two_d) or v_pool.shape[:3] != (num_pages, page_size, H):
+        raise ValueError("pools must be [num_pages, page_size, H, 2d] and [num_pages, page_size, H, dv]")
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if out is None:
+        out = torch.zeros((total_q, H, dv), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    _check(lib().diffattn_fwd_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(out),
+                                    _ptr(cu_seqlens_q), _ptr(seqlens_k), _ptr(block_table), mq, mk,
+                                    total_q, num_pages, page_size, block_table.shape[1], _ptr(lam),
+                                    float(lambda_init), _ptr(norm_weight), float(eps), B, H, d, dv,
+                                    _train_flags(causal, norm, scale), DIFFATTN_BF16,
+                                    _stream(stream)))
+    return out
+
+
+def diffattn_v2_fwd_paged(q, k_pool, v_pool, lam_logit, cu_seqlens_q, seqlens_k, block_table,
+                          max_seqlen_q=None, max_seqlen_k=None, causal: bool = True, out=None,
+                          stream=None):
+    """DIFF V2 with packed queries q [total_q, Hq, d] against keys in a page pool: k_pool,
+    v_pool [num_pages, page_size, Hkv, d]; lam_logit [total_q, Hq/2]."""
+    _dev("q", q, torch.bfloat16)
+    total_q, Hq, d = q.shape
+    B, mq, mk = _paged_args(q, k_pool, v_pool, cu_seqlens_q, seqlens_k, block_table,
+                            max_seqlen_q, max_seqlen_k)
+    num_pages, page_size, Hkv = k_pool.shape[0], k_pool.shape[1], k_pool.shape[2]
+    if k_pool.shape != (num_pages, page_size, Hkv, d) or v_pool.shape != k_pool.shape:
+        raise ValueError("pools must both be [num_pages, page_size, Hkv, d]")
+    _dev("lam_logit", lam_logit, torch.float32)
+    if lam_logit.shape != (total_q, Hq // 2):
+        raise ValueError("lam_logit must be [total_q, Hq/2]")
+    if out is None:
+        out = torch.zeros((total_q, Hq // 2, d), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    _check(lib().diffattn_v2_fwd_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(lam_logit),
+                                       _ptr(out), _ptr(cu_seqlens_q), _ptr(seqlens_k),
+                                       _ptr(block_table), mq, mk, total_q, num_pages, page_size,
+                                       block_table.shape[1], B, Hq, Hkv, d,
+                                       DIFFATTN_CAUSAL if causal else 0, DIFFATTN_BF16,
+                                       _stream(stream)))
     return out
 
 

@@ -864,6 +864,146 @@ DIFFATTN_API int diffattn_v2_fwd_varlen(const void* q, const void* k, const void
   return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// shape rules shared by the two paged prefills
+int check_paged_prefill(const char* fn, int B, int max_seqlen_q, int max_seqlen_k, int total_q,
+                        int num_pages, int page_size, int max_pages) {
+  if (B < 1 || max_seqlen_q < 1 || total_q < 1 || max_seqlen_q > total_q ||
+      max_seqlen_k < max_seqlen_q || num_pages < 1 || max_pages < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need B >= 1, 1 <= max_seqlen_q <= total_q, "
+                "max_seqlen_q <= max_seqlen_k, num_pages >= 1 and max_pages >= 1", fn);
+  if (page_size < 128 || page_size % 128 != 0)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: page_size must be a multiple of 128 (got %d)", fn, page_size);
+  if (static_cast<long long>(num_pages) * page_size > 0x7fffffffLL ||
+      static_cast<long long>(max_pages) * page_size > (1LL << 30) ||
+      static_cast<long long>(max_seqlen_k) > static_cast<long long>(max_pages) * page_size)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need num_pages * page_size < 2^31 and "
+                "max_seqlen_k <= max_pages * page_size <= 2^30", fn);
+  return DIFFATTN_OK;
+}
+}  // namespace
+
+DIFFATTN_API int diffattn_fwd_paged(const void* q, const void* k_pool, const void* v_pool,
+                                    void* out, const int* cu_seqlens_q, const int* seqlens_k,
+                                    const int* block_table, int max_seqlen_q, int max_seqlen_k,
+                                    int total_q, int num_pages, int page_size, int max_pages,
+                                    const float* lambda, float lambda_init,
+                                    const float* norm_weight, float eps, int B, int H, int d,
+                                    int dv, int flags, int dtype, void* stream) {
+  const char* fn = "diffattn_fwd_paged";
+  if (!q || !k_pool || !v_pool || !out || !cu_seqlens_q || !seqlens_k || !block_table || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  constexpr int kFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kFlags) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "%s: eps must be > 0 with DIFFATTN_NORM", fn);
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);
+  int rc = check_paged_prefill(fn, B, max_seqlen_q, max_seqlen_k, total_q, num_pages, page_size,
+                               max_pages);
+  if (rc) return rc;
+  if (H < 1) return fail(DIFFATTN_ERR_SHAPE, "%s: H must be >= 1", fn);
+  if (d != 128 || dv != 256)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need d = 128 and dv = 256 (got d=%d dv=%d)", fn, d, dv);
+  const long long tiles = (static_cast<long long>(max_seqlen_q) + 127) / 128 * B * H;
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(num_pages) * page_size * H > (1LL << 34))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: problem too large for one launch", fn);
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || !aligned(cu_seqlens_q, 4) || !aligned(seqlens_k, 4) ||
+      !aligned(block_table, 4) || (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k_pool;
+  p.v = v_pool;
+  p.out = out;
+  p.B = B;
+  p.N = max_seqlen_q;
+  p.units = H;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_V1;
+  p.q_heads = H;
+  p.kv_heads = H;
+  p.q_cols = 2 * d;
+  p.k_cols = 2 * d;
+  p.group = 1;
+  p.lambda = lambda;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  p.cu_seqlens = cu_seqlens_q;
+  p.total = total_q;
+  p.max_seqlen_k = max_seqlen_k;
+  p.seqlens_k = seqlens_k;
+  p.block_table = block_table;
+  p.page_size = page_size;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
+}
+
+DIFFATTN_API int diffattn_v2_fwd_paged(const void* q, const void* k_pool, const void* v_pool,
+                                       const float* lam_logit, void* out,
+                                       const int* cu_seqlens_q, const int* seqlens_k,
+                                       const int* block_table, int max_seqlen_q, int max_seqlen_k,
+                                       int total_q, int num_pages, int page_size, int max_pages,
+                                       int B, int Hq, int Hkv, int d, int flags, int dtype,
+                                       void* stream) {
+  const char* fn = "diffattn_v2_fwd_paged";
+  if (!q || !k_pool || !v_pool || !lam_logit || !out || !cu_seqlens_q || !seqlens_k || !block_table)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (flags & ~DIFFATTN_CAUSAL) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);
+  int rc = check_paged_prefill(fn, B, max_seqlen_q, max_seqlen_k, total_q, num_pages, page_size,
+                               max_pages);
+  if (rc) return rc;
+  if (Hq < 2 || Hkv < 1 || Hq % 2 != 0 || Hq % Hkv != 0 || (Hq / Hkv) % 2 != 0)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even (got Hq=%d Hkv=%d)",
+                fn, Hq, Hkv);
+  if (d != 128) return fail(DIFFATTN_ERR_SHAPE, "%s: need d = 128 (got %d)", fn, d);
+  const long long tiles = (static_cast<long long>(max_seqlen_q) + 127) / 128 * B * (Hq / 2);
+  if (tiles * 2 > 0x7fffffffLL)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: problem too large for one launch", fn);
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(lam_logit, 4) || !aligned(cu_seqlens_q, 4) || !aligned(seqlens_k, 4) ||
+      !aligned(block_table, 4))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k_pool;
+  p.v = v_pool;
+  p.out = out;
+  p.B = B;
+  p.N = max_seqlen_q;
+  p.units = Hq / 2;
+  p.dqk = d;
+  p.dv = d;
+  p.mode = da::MODE_V2;
+  p.q_heads = Hq;
+  p.kv_heads = Hkv;
+  p.q_cols = d;
+  p.k_cols = d;
+  p.group = Hq / Hkv;
+  p.lam_logit = lam_logit;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  p.cu_seqlens = cu_seqlens_q;
+  p.total = total_q;
+  p.max_seqlen_k = max_seqlen_k;
+  p.seqlens_k = seqlens_k;
+  p.block_table = block_table;
+  p.page_size = page_size;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
+}
+
 DIFFATTN_API int diffattn_fwd_fp8(const void* q, const void* k, const void* v, void* out,
                                   float q_descale, float k_descale, const float* lambda,
                                   float lambda_init, const float* norm_weight, float eps, int B,

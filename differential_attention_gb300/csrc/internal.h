@@ -62,6 +62,12 @@ struct Problem {
   // struct, so that adding them moved no other field of the kernels' parameters.
   const int* cu_seqlens_k;
   int total_k, max_seqlen_k;
+  // paged keys (with cu_seqlens for the queries): sequence b has seqlens_k[b] keys, key r at row
+  // r % page_size of page block_table[b * max_pages + r / page_size] of the pools k/v
+  // [num_pages, page_size, H, *]; its queries are the last of those positions, as above
+  const int* seqlens_k;
+  const int* block_table;
+  int page_size, max_pages, num_pages;
 };
 
 __host__ inline void fill_dense_strides(Problem& p) {

@@ -99,11 +99,18 @@ struct KParams {
   float scale_log2;
 };
 
+// Where a sequence's keys are (KMODE).
+enum : int {
+  kKeysShared = 0,  // at the queries' rows (batched, or packed with cu_seqlens)
+  kKeysOffset = 1,  // packed with offsets of their own (cu_seqlens_k)
+  kKeysPaged = 2,   // in a page pool through a block table (page size a multiple of 128)
+};
+
 // SHARED_K: the V2 operator (both maps read one K tile); without it, V1 (launch_prefill_exact
-// picks the instantiation by mode). KOFF: keys with offsets of their own (cu_seqlens_k). A
-// separate instantiation: the extra live values made the default variants spill at their
-// 96-register budget.
-template <int DQK, int DV, bool SHARED_K, bool QK8, bool KOFF>
+// picks the instantiation by mode). KMODE: where the keys are. The key modes are instantiations
+// of their own: their extra live values made the default variants spill at their 96-register
+// budget.
+template <int DQK, int DV, bool SHARED_K, bool QK8, int KMODE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_exact_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -155,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (qt * BM >= SN) return;  // a tile past this sequence's end: nothing to do (uniform)
   }
   int kseq0 = seq0, SNk = SN;
-  if constexpr (KOFF) {
+  if constexpr (KMODE == kKeysOffset) {
     kseq0 = P.cu_seqlens_k[b];
     SNk = P.cu_seqlens_k[b + 1] - kseq0;
     // keys outside k, or fewer keys than queries: reported and skipped like the query offsets
@@ -163,12 +170,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (threadIdx.x == 0 && qt == 0) flag_device_error(DEV_BAD_INDEX);
       return;
     }
+  } else if constexpr (KMODE == kKeysPaged) {
+    kseq0 = 0;
+    SNk = P.seqlens_k[b];
+    if (SNk < SN || SNk > P.max_pages * P.page_size) {
+      if (threadIdx.x == 0 && qt == 0) flag_device_error(DEV_BAD_INDEX);
+      return;
+    }
   }
-  const int qoff = KOFF ? SNk - SN : 0;
+  const int qoff = KMODE != kKeysShared ? SNk - SN : 0;
   const int n_kv_all = (SNk + BN - 1) / BN;
   // causal: the tile's last query row sees keys up to qoff + (qt + 1) BM - 1
   const int n = !causal ? n_kv_all
-                        : KOFF ? min((qoff + (qt + 1) * BM + BN - 1) / BN, n_kv_all)
+                        : KMODE != kKeysShared ? min((qoff + (qt + 1) * BM + BN - 1) / BN, n_kv_all)
                                : min(qt + 1, n_kv_all);  // BM == BN
   const int T = 2 * n;  // tiles over both passes
 
@@ -238,10 +252,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(bar(bars.slot_full[slot]), bytes);
         return slot;
       };
+      // token-axis row of the sequence's key r: packed or batched rows, or (paged) the pool row
+      // through the block table. A page id outside the pool reads page 0 and, where the key is
+      // in use, flags DEV_BAD_INDEX; tiles start at multiples of 64 keys, inside one page.
+      auto key_row = [&](int r) -> int {
+        if constexpr (KMODE == kKeysPaged) {
+          const int pi = r / P.page_size;
+          int pg = 0;
+          if (pi < P.max_pages) {
+            pg = P.block_table[static_cast<size_t>(b) * P.max_pages + pi];
+            if (pg < 0 || pg >= P.num_pages) {
+              if (r < SNk) flag_device_error(DEV_BAD_INDEX);
+              pg = 0;
+            }
+          }
+          return pg * P.page_size + (r - pi * P.page_size);
+        } else {
+          return kseq0 + r;
+        }
+      };
       bool ok = true;
       for (int t = 0; t <= T && ok; ++t) {
         if (t < T) {
           const int j = t < n ? t : t - n;
+          const int krow = key_row(j * BN);  // (paged: the table read overlaps the slot wait)
           for (int r = 0; r < KL && ok; ++r) {
             const int ks = acquire(k_load(t, r), C::kKLoadBytes);
             if (ks < 0) {
@@ -252,13 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int c = 0; c < C::kQKBoxes; ++c)
                 tma_load_4d(sSlot + ks * C::kSlot + (QK8 ? mp * C::kKMapBytes : 0) + c * C::kChunk,
                             &tm_k, bar(bars.slot_full[ks]), k_col_of(P, mp) + C::kQKBoxCols * c,
-                            kvh, kseq0 + j * BN, tb);
+                            kvh, krow, tb);
             issued = k_load(t, r) + 1;
           }
         }
         if (ok && t >= n + 1) {
           const int jv = t - n - 1;
           for (int h = 0; h < 2 && ok; ++h) {
+            const int vrow = key_row(jv * BN + 64 * h);
             const int vs = acquire(v_load(jv, h), C::kVHalfBytes);
             if (vs < 0) {
               ok = false;
@@ -266,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int c = 0; c < DV / 64; ++c)
               tma_load_4d(sSlot + vs * C::kSlot + c * C::kVHalfChunk, &tm_v,
-                          bar(bars.slot_full[vs]), 64 * c, kvh, kseq0 + jv * BN + 64 * h, tb);
+                          bar(bars.slot_full[vs]), 64 * c, kvh, vrow, tb);
             issued = v_load(jv, h) + 1;
           }
         }
@@ -621,18 +656,21 @@ static bool make_map(CUtensorMap* m, const void* base, int cols, int heads, int 
   return encode_tmap_4d(m, type, base, dims, strides, box, err, err_len);
 }
 
-template <int DQK, int DV, bool SHARED_K, bool QK8 = false, bool KOFF = false>
+template <int DQK, int DV, bool SHARED_K, bool QK8 = false, int KMODE = kKeysShared>
 static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
   using C = Cfg<DQK, DV, SHARED_K, QK8>;
   CUtensorMap mq, mk, mv;
   // packed sequences: one batch row of `total` tokens; otherwise [B, N]
   const int mN = p.cu_seqlens ? p.total : p.N, mB = p.cu_seqlens ? 1 : p.B;
-  const int mNk = p.cu_seqlens_k ? p.total_k : mN;  // keys with offsets of their own
+  // keys with offsets of their own, or the page pools as one [num_pages * page_size] axis
+  const int mNk = KMODE == kKeysPaged    ? p.num_pages * p.page_size
+                  : KMODE == kKeysOffset ? p.total_k
+                                         : mN;
   if (!make_map(&mq, p.q, p.q_cols, p.q_heads, mN, mB, p.qs, BM, err, err_len, C::kQKElt) ||
       !make_map(&mk, p.k, p.k_cols, p.kv_heads, mNk, mB, p.ks, BN, err, err_len, C::kQKElt) ||
       !make_map(&mv, p.v, DV, p.kv_heads, mNk, mB, p.vs, BN / 2, err, err_len))
     return cudaErrorInvalidValue;
-  auto kern = prefill_exact_kernel<DQK, DV, SHARED_K, QK8, KOFF>;
+  auto kern = prefill_exact_kernel<DQK, DV, SHARED_K, QK8, KMODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   KParams kp;
@@ -641,7 +679,7 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
   kp.scale_log2 = kLog2e * p.scale;
   {
     // K/V bytes one (batch, unit) pair streams; keep a group's K/V within ~64 MB of L2
-    const int nk = p.cu_seqlens_k ? p.max_seqlen_k : p.N;
+    const int nk = (p.cu_seqlens_k || p.block_table) ? p.max_seqlen_k : p.N;
     const double kv_bytes = static_cast<double>(nk) * (p.k_cols * C::kQKElt + DV * 2.0);
     long long g = static_cast<long long>((64.0 * 1024 * 1024) / (kv_bytes > 1 ? kv_bytes : 1));
     const long long bu = static_cast<long long>(p.B) * p.units;
@@ -664,19 +702,23 @@ cudaError_t launch_prefill_exact(const Problem& p, cudaStream_t s, char* err, si
       return cudaErrorNotSupported;
     }
     const bool koff = p.cu_seqlens && p.cu_seqlens_k;
+    const bool paged = p.cu_seqlens && p.block_table;
     if (p.dqk == 128 && p.dv == 256)
-      return koff ? exact::launch_cfg<128, 256, false, false, true>(p, s, err, err_len)
-                  : exact::launch_cfg<128, 256, false>(p, s, err, err_len);
-    if (p.dqk == 64 && p.dv == 128)
-      return koff ? exact::launch_cfg<64, 128, false, false, true>(p, s, err, err_len)
+      return paged  ? exact::launch_cfg<128, 256, false, false, exact::kKeysPaged>(p, s, err, err_len)
+             : koff ? exact::launch_cfg<128, 256, false, false, exact::kKeysOffset>(p, s, err, err_len)
+                    : exact::launch_cfg<128, 256, false>(p, s, err, err_len);
+    if (p.dqk == 64 && p.dv == 128 && !paged)
+      return koff ? exact::launch_cfg<64, 128, false, false, exact::kKeysOffset>(p, s, err, err_len)
                   : exact::launch_cfg<64, 128, false>(p, s, err, err_len);
   } else {
     const bool koff = p.cu_seqlens && p.cu_seqlens_k;
+    const bool paged = p.cu_seqlens && p.block_table;
     if (p.dqk == 128 && p.dv == 128)
-      return koff ? exact::launch_cfg<128, 128, true, false, true>(p, s, err, err_len)
-                  : exact::launch_cfg<128, 128, true>(p, s, err, err_len);
-    if (p.dqk == 64 && p.dv == 64)
-      return koff ? exact::launch_cfg<64, 64, true, false, true>(p, s, err, err_len)
+      return paged  ? exact::launch_cfg<128, 128, true, false, exact::kKeysPaged>(p, s, err, err_len)
+             : koff ? exact::launch_cfg<128, 128, true, false, exact::kKeysOffset>(p, s, err, err_len)
+                    : exact::launch_cfg<128, 128, true>(p, s, err, err_len);
+    if (p.dqk == 64 && p.dv == 64 && !paged)
+      return koff ? exact::launch_cfg<64, 64, true, false, exact::kKeysOffset>(p, s, err, err_len)
                   : exact::launch_cfg<64, 64, true>(p, s, err, err_len);
   }
   return cudaErrorNotSupported;

@@ -389,6 +389,41 @@ DIFFATTN_API int diffattn_v2_fwd_varlen(const void* q, const void* k, const void
                                         int dtype, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Prefill over a paged KV cache: diffattn_fwd_varlen_qk (V1) and diffattn_v2_fwd_varlen (V2)
+ * with each sequence's keys in pages of a pool, as a serving engine holds them: a prompt chunk,
+ * or several new tokens, against the keys cached so far. The pages give no cache layout; the
+ * operator per query row is unchanged.
+ *   q, out : packed queries as for diffattn_fwd_varlen_qk / diffattn_v2_fwd_varlen
+ *            (cu_seqlens_q, device int32 [B + 1]); sequence b's Lq queries are the last Lq of
+ *            its Lk = seqlens_k[b] key positions
+ *   k_pool, v_pool : device [num_pages, page_size, H, 2d] and [.., H, dv] (V1), or
+ *            [num_pages, page_size, Hkv, d] both (V2)
+ *   seqlens_k   : device int32 [B]; block_table : device int32 [B, max_pages]: key r of
+ *            sequence b is row r % page_size of page block_table[b * max_pages + r / page_size]
+ *   max_seqlen_q, max_seqlen_k : the longest query run (sizes the grid) and key run
+ *   page_size   : a multiple of 128 (a tile of 128 keys lies in one page)
+ * Checked on the device: a sequence with Lk < Lq or Lk > max_pages * page_size is skipped, and a
+ * used block-table entry outside [0, num_pages) reads page 0; both are reported by
+ * diffattn_device_status() as DIFFATTN_ERR_INDEX. Entries past a sequence's keys are not read.
+ * Other arguments as the packed calls. Supported: dtype DIFFATTN_BF16, d = 128 (V1: dv = 256).
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_fwd_paged(const void* q, const void* k_pool, const void* v_pool,
+                                    void* out, const int* cu_seqlens_q, const int* seqlens_k,
+                                    const int* block_table, int max_seqlen_q, int max_seqlen_k,
+                                    int total_q, int num_pages, int page_size, int max_pages,
+                                    const float* lambda, float lambda_init,
+                                    const float* norm_weight, float eps, int B, int H, int d,
+                                    int dv, int flags, int dtype, void* stream);
+DIFFATTN_API int diffattn_v2_fwd_paged(const void* q, const void* k_pool, const void* v_pool,
+                                       const float* lam_logit, void* out,
+                                       const int* cu_seqlens_q, const int* seqlens_k,
+                                       const int* block_table, int max_seqlen_q, int max_seqlen_k,
+                                       int total_q, int num_pages, int page_size, int max_pages,
+                                       int B, int Hq, int Hkv, int d, int flags, int dtype,
+                                       void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * Prefill with fp8 scores (page "Differential Transformer: softmax can't say zero, so it
  * subtracts", on the attention logits quantized to low bit widths: DIFF's logits are several
  * times smaller relative to their spread, so low-bit score products cost it little).

@@ -489,3 +489,35 @@ def diffattn_v2_fwd_varlen(q, k, v, lam_logit, cu_seqlens_q, cu_seqlens_k=None,
                 a2 = softmax_rows(scores(q[r, 2 * p + 1], kg, ps, causal)) @ vg
                 out[r, p, :] = a1 - sig[r, p][:, None] * a2
     return out
+
+
+def gather_pages(pool, block_table, seqlens_k):
+    """Each sequence's keys read from a page pool [num_pages, page_size, ...] in order, packed one
+    sequence after another: returns (rows [sum(seqlens_k), ...], offsets [B + 1])."""
+    num_pages, page_size = pool.shape[0], pool.shape[1]
+    flat = _f64(pool).reshape((num_pages * page_size,) + tuple(pool.shape[2:]))
+    B = int(np.asarray(_f64(seqlens_k)).size)
+    rows = [paged_rows(block_table, seqlens_k, page_size, b) for b in range(B)]
+    cu = np.concatenate([[0], np.cumsum([r.size for r in rows])]).astype(np.int64)
+    idx = np.concatenate(rows).astype(np.int64) if B else np.zeros(0, dtype=np.int64)
+    return flat[idx], cu
+
+
+def diffattn_fwd_paged(q, k_pool, v_pool, cu_seqlens_q, seqlens_k, block_table, lam,
+                       lam_init: float, norm_weight=None, eps: float = 1e-5, norm: bool = True,
+                       apply_scale: bool = True, causal: bool = True):
+    """`diffattn_fwd_varlen_qk` with each sequence's keys read from page pools k_pool
+    [num_pages, page_size, H, 2d], v_pool [.., H, dv] through block_table [B, max_pages]."""
+    k, cu_k = gather_pages(k_pool, block_table, seqlens_k)
+    v, _ = gather_pages(v_pool, block_table, seqlens_k)
+    return diffattn_fwd_varlen_qk(q, k, v, cu_seqlens_q, cu_k, lam, lam_init, norm_weight, eps,
+                                  norm, apply_scale, causal)
+
+
+def diffattn_v2_fwd_paged(q, k_pool, v_pool, lam_logit, cu_seqlens_q, seqlens_k, block_table,
+                          causal: bool = True):
+    """`diffattn_v2_fwd_varlen` with each sequence's keys read from page pools k_pool, v_pool
+    [num_pages, page_size, Hkv, d] through block_table [B, max_pages]."""
+    k, cu_k = gather_pages(k_pool, block_table, seqlens_k)
+    v, _ = gather_pages(v_pool, block_table, seqlens_k)
+    return diffattn_v2_fwd_varlen(q, k, v, lam_logit, cu_seqlens_q, cu_k, causal)

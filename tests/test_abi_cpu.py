@@ -214,6 +214,15 @@ def test_fused_lambda_varlen_fp8_strided_validation(L):
     assert varlen_qk(tq=64, tk=32) == -2
     assert varlen_qk(mk=128, tk=64) == -2
     assert varlen_qk(cu=ctypes.c_void_p(0x10002)) == -4
+    def paged(ps=128, mq=16, mk=300, tq=32, pages=8, maxp=4, d=128):
+        return L.diffattn_fwd_paged(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, mq, mk, tq, pages,
+                                    ps, maxp, FAKE, 0.5, None, 1e-5, 2, 2, d, 2 * d, 7, 0, None)
+    assert paged(ps=64) == -2              # a tile of 128 keys must lie in one page
+    assert paged(mk=8, mq=16) == -2        # fewer keys than queries
+    assert paged(mk=600) == -2             # more keys than the table can name (4 x 128)
+    assert paged(d=64) == -2
+    assert L.diffattn_v2_fwd_paged(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 16, 32, 32, 8,
+                                   128, 4, 2, 8, 2, 128, 1, 0, None) == -1
     def v2var(cu=FAKE, Hq=8, Hkv=2, flags=1):
         return L.diffattn_v2_fwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, cu, None, 16, 16, 32, 32, 2,
                                         Hq, Hkv, 128, flags, 0, None)

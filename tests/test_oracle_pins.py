@@ -484,13 +484,45 @@ def pin_v2_varlen():
     assert np.allclose(part, got[b - 4:b], rtol=1e-12, atol=1e-12)
 
 
+def pin_paged_prefill():
+    """Prefill over pages: with the pool holding each sequence's keys in order (identity table)
+    it is the packed prefill over those keys, and shuffling the pool's pages with the table
+    following them changes nothing; V2 likewise."""
+    rng = np.random.default_rng(37)
+    H, d, dv, ps = 2, 4, 8, 3
+    Lk, Lq = [7, 3], [2, 3]
+    mp = 3
+    kc = rng.standard_normal((2, mp * ps, H, 2 * d)); vc = rng.standard_normal((2, mp * ps, H, dv))
+    q = rng.standard_normal((sum(Lq), H, 2 * d)); lam = np.array([0.4, 0.9])
+    cu_q = np.concatenate([[0], np.cumsum(Lq)])
+    k_pool = kc.reshape(2 * mp, ps, H, 2 * d); v_pool = vc.reshape(2 * mp, ps, H, dv)
+    table = np.arange(2 * mp).reshape(2, mp)
+    got = ref.diffattn_fwd_paged(q, k_pool, v_pool, cu_q, np.array(Lk), table, lam, 0.2)
+    kp = np.concatenate([kc[0, :7], kc[1, :3]]); vp = np.concatenate([vc[0, :7], vc[1, :3]])
+    want = ref.diffattn_fwd_varlen_qk(q, kp, vp, cu_q, np.array([0, 7, 10]), lam, 0.2)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    perm = rng.permutation(2 * mp)
+    k_sh = np.empty_like(k_pool); v_sh = np.empty_like(v_pool)
+    k_sh[perm], v_sh[perm] = k_pool, v_pool
+    got2 = ref.diffattn_fwd_paged(q, k_sh, v_sh, cu_q, np.array(Lk), perm[table], lam, 0.2)
+    assert np.allclose(got2, want, rtol=1e-12, atol=1e-12)
+    Hq, Hkv = 4, 2
+    q2 = rng.standard_normal((sum(Lq), Hq, d)); lg = rng.standard_normal((sum(Lq), Hq // 2))
+    k2 = rng.standard_normal((2 * mp, ps, Hkv, d)); v2 = rng.standard_normal((2 * mp, ps, Hkv, d))
+    a = ref.diffattn_v2_fwd_paged(q2, k2, v2, lg, cu_q, np.array(Lk), table)
+    flat_k, flat_v = k2.reshape(2 * mp * ps, Hkv, d), v2.reshape(2 * mp * ps, Hkv, d)
+    rows = np.concatenate([np.arange(7), mp * ps + np.arange(3)])
+    b = ref.diffattn_v2_fwd_varlen(q2, flat_k[rows], flat_v[rows], lg, cu_q, np.array([0, 7, 10]))
+    assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
 PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, pin_lambda_spread,
         pin_softmax_floor, pin_toy_needle_table, pin_worked_example, pin_row_sums,
         pin_lambda_zero_is_softmax_attention, pin_equal_maps_scale_attention, pin_brute_force_tiny,
         pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
         pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen, pin_varlen_qk,
-        pin_v2_varlen]
+        pin_v2_varlen, pin_paged_prefill]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])

@@ -401,6 +401,61 @@ def test_v2_fwd_varlen(lens_q, lens_k, causal):
     da.diffattn_device_status()
 
 
+@pytest.mark.parametrize("ps,lens_q,lens_k", [(128, [300, 1, 64], [700, 200, 64]),
+                                              (256, [128, 500], [1000, 500])])
+def test_fwd_paged(ps, lens_q, lens_k):
+    """Packed queries against keys in a shuffled page pool with spare pages: against the oracle,
+    and bit-equal to the packed prefill over the same keys laid out contiguously."""
+    B, H = len(lens_q), 2
+    mp = (max(lens_k) + ps - 1) // ps
+    kin = make_prefill_inputs(B, mp * ps, H, 128, 256, seed=241 + ps)
+    k_pool, v_pool, table = page_cache(kin.k, kin.v, ps, seed=243 + ps, spare_pages=3)
+    q = make_prefill_inputs(1, sum(lens_q), H, 128, 256, seed=245 + ps).q[0]
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lens_q)]), dtype=torch.int32)
+    sk = torch.tensor(lens_k, dtype=torch.int32)
+    lam = torch.tensor([0.45, 0.8], dtype=torch.float32)
+    li = ref.lambda_init(12)
+    got = da.diffattn_fwd_paged(q.to(DEV), k_pool.to(DEV), v_pool.to(DEV), cu_q.to(DEV),
+                                sk.to(DEV), table.to(DEV), lam.to(DEV), li)
+    want = ref.diffattn_fwd_paged(q, k_pool, v_pool, cu_q, sk, table, lam.numpy(), li)
+    assert_bf16(got, want)
+    kp = torch.cat([kin.k[b, :lens_k[b]] for b in range(B)])
+    vp = torch.cat([kin.v[b, :lens_k[b]] for b in range(B)])
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lens_k)]), dtype=torch.int32)
+    flat = da.diffattn_fwd_varlen_qk(q.to(DEV), kp.to(DEV), vp.to(DEV), cu_q.to(DEV),
+                                     cu_k.to(DEV), lam.to(DEV), li)
+    assert torch.equal(got, flat)
+    da.diffattn_device_status()
+
+
+def test_v2_fwd_paged_and_bad_page():
+    """V2 against keys in pages, against the oracle; unused table entries (-1) are never read,
+    and a used entry outside the pool is reported as DIFFATTN_ERR_INDEX."""
+    ps, Hq, Hkv = 128, 8, 2
+    lens_q, lens_k = [200, 5], [600, 130]
+    mp = 5
+    g = torch.Generator().manual_seed(251)
+    kc = (torch.randn((2, mp * ps, Hkv, 128), generator=g) / 128 ** 0.5).to(torch.bfloat16)
+    vc = (torch.randn((2, mp * ps, Hkv, 128), generator=g) / 128 ** 0.5).to(torch.bfloat16)
+    k_pool, v_pool, table = page_cache(kc, vc, ps, seed=252, spare_pages=1)
+    table[1, 2:] = -1  # sequence 1 holds 130 keys: pages 0 and 1
+    q = (torch.randn((sum(lens_q), Hq, 128), generator=g) / 128 ** 0.5).to(torch.bfloat16)
+    lg = torch.randn((sum(lens_q), Hq // 2), generator=g, dtype=torch.float32)
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lens_q)]), dtype=torch.int32)
+    sk = torch.tensor(lens_k, dtype=torch.int32)
+    args = (q.to(DEV), k_pool.to(DEV), v_pool.to(DEV), lg.to(DEV), cu_q.to(DEV), sk.to(DEV))
+    got = da.diffattn_v2_fwd_paged(*args, table.to(DEV))
+    da.diffattn_device_status()  # OK: no used entry is bad
+    want = ref.diffattn_v2_fwd_paged(q, k_pool, v_pool, lg, cu_q, sk, table)
+    assert_bf16(got, want)
+    table[0, 3] = k_pool.shape[0] + 4
+    da.diffattn_v2_fwd_paged(*args, table.to(DEV))
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_device_status()
+    assert e.value.status == -9  # DIFFATTN_ERR_INDEX
+    da.diffattn_device_status()
+
+
 # ------------------------------------------------------------------------------------------
 # decode over a paged cache
 # ------------------------------------------------------------------------------------------
