@@ -174,3 +174,41 @@ def test_sweep_packed_chunks(case):
                                      causal=causal)
     assert_bf16(got2, ref.diffattn_v2_fwd_varlen(v2q.q[0], v2.k[0], v2.v[0], v2q.lam_logit[0],
                                                  cu_q, cu_k, causal=causal))
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_sweep_paged_prefill(case):
+    """Packed queries against keys in a shuffled page pool (V1 and V2), random lengths and page
+    sizes of 128 or 256 tokens."""
+    rng = np.random.default_rng(1600 + case)
+    B = int(rng.integers(1, 4))
+    ps = int(rng.choice([128, 256]))
+    lens_k = [int(rng.integers(1, 700)) for _ in range(B)]
+    lens_q = [max(1, int(rng.integers(0, lk + 1))) for lk in lens_k]
+    causal = bool(rng.integers(0, 2))
+    mp = (max(lens_k) + ps - 1) // ps + int(rng.integers(0, 2))
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lens_q)]), dtype=torch.int32)
+    sk = torch.tensor(lens_k, dtype=torch.int32)
+    H = int(rng.integers(1, 3))
+    kin = make_prefill_inputs(B, mp * ps, H, 128, 256, seed=1600 + case)
+    k_pool, v_pool, table = page_cache(kin.k, kin.v, ps, seed=1610 + case, spare_pages=2)
+    q = make_prefill_inputs(1, sum(lens_q), H, 128, 256, seed=1620 + case).q[0]
+    lam = rng.uniform(0.0, 1.1, H)
+    li = ref.lambda_init(12)
+    got = da.diffattn_fwd_paged(q.to(DEV), k_pool.to(DEV), v_pool.to(DEV), cu_q.to(DEV),
+                                sk.to(DEV), table.to(DEV),
+                                torch.tensor(lam, dtype=torch.float32, device=DEV), li,
+                                causal=causal)
+    assert_bf16(got, ref.diffattn_fwd_paged(q, k_pool, v_pool, cu_q, sk, table, lam, li,
+                                            causal=causal))
+    Hkv = int(rng.integers(1, 3))
+    Hq = Hkv * int(rng.choice([2, 4]))
+    g = torch.Generator().manual_seed(1630 + case)
+    kc = (torch.randn((B, mp * ps, Hkv, 128), generator=g) / 128 ** 0.5).to(torch.bfloat16)
+    vc = (torch.randn((B, mp * ps, Hkv, 128), generator=g) / 128 ** 0.5).to(torch.bfloat16)
+    k2, v2, t2 = page_cache(kc, vc, ps, seed=1640 + case, spare_pages=1)
+    q2 = (torch.randn((sum(lens_q), Hq, 128), generator=g) / 128 ** 0.5).to(torch.bfloat16)
+    lg = torch.randn((sum(lens_q), Hq // 2), generator=g, dtype=torch.float32)
+    got2 = da.diffattn_v2_fwd_paged(q2.to(DEV), k2.to(DEV), v2.to(DEV), lg.to(DEV), cu_q.to(DEV),
+                                    sk.to(DEV), t2.to(DEV), causal=causal)
+    assert_bf16(got2, ref.diffattn_v2_fwd_paged(q2, k2, v2, lg, cu_q, sk, t2, causal=causal))
