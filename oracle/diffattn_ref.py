@@ -17,15 +17,17 @@ Sources (page title, section):
        re-parameterised", "The row no longer sums to one", "DIFF V2: what the authors changed".
   [P5] "Differential Transformer V2" -- GQA pairing of the subtracted heads.
 
-Readings taken where the pages are silent or disagree (all listed in the design doc as well):
+Readings taken where the pages are silent or disagree:
   * the 1/sqrt(d) scale uses d = width of one query/key half (P1 `d**0.5`, P3 Q_i in R^{N x d});
   * lambda is one float per head (P1 says per head, P3 says one per layer shared by every head; a
     per-head array covers both); it is computed and used in full precision, no clipping;
   * the per-head norm is an RMSNorm over all dv channels of the head, y = o / sqrt(mean(o^2) + eps)
     * w, then times (1 - lambda_init) (P3 quotes `subln` then `* (1 - lambda_init)`); the
     GroupNorm "+ lambda_init" form on the Japanese page is treated as garbled;
-  * causal prefill is top-left aligned with Nq = Nk (key j visible to query i iff j <= i); decode
-    attends to every cached key of its row;
+  * causal prefill with Nq = Nk: key j is visible to query i iff j <= i; when a sequence's Lq
+    queries are the last of its Lk key positions (the packed and paged forms), the query at
+    position p sees keys 0 .. p, so the mask is aligned at the end; decode attends to every
+    cached key of its row;
   * V2 pairs heads (2p, 2p+1), uses KV head floor(2p / (Hq/Hkv)), lambda = sigmoid(logit) per
     token and pair, no per-head norm, and the default 1/sqrt(d) scale.
 
