@@ -746,6 +746,52 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del inp, dy, saved, grads, ws
         torch.cuda.empty_cache()
 
+        # the backward over the packed-sequence workload (16 sequences of mixed length)
+        lens = varlen_lengths()
+        total = int(sum(lens))
+        pin = make_prefill_inputs(1, total, c["H"], c["d"], c["dv"], seed=7100 + rank,
+                                  layer=c["layer"], device=dev)
+        q, k, v = pin.q[0], pin.k[0], pin.v[0]
+        dyp = make_dout(1, total, c["H"], c["dv"], seed=7107 + rank, device=dev)[0]
+        cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=dev)
+        mx = max(lens)
+        _, o_pre, stats = da.diffattn_fwd_train_varlen(q, k, v, cu, lam, li, max_seqlen=mx,
+                                                       norm_weight=w)
+        ws = torch.empty(da.diffattn_bwd_varlen_workspace_size(len(lens), mx, total, c["H"],
+                                                               c["d"], c["dv"]),
+                         dtype=torch.uint8, device=dev)
+        grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                     dlam=torch.empty(c["H"], dtype=torch.float32, device=dev),
+                     dw=torch.empty(c["dv"], dtype=torch.float32, device=dev))
+
+        def bwd_packed():
+            da.diffattn_bwd_varlen(q, k, v, o_pre, stats, dyp, cu, lam, li, max_seqlen=mx,
+                                   norm_weight=w, workspace=ws, grads=grads)
+
+        for _ in range(args.warmup):
+            bwd_packed()
+        barrier()
+        evs = [(ev(), ev()) for _ in range(n_steps)]
+        for i in range(n_steps):
+            evs[i][0].record(stream)
+            bwd_packed()
+            evs[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        vflops = float(sum(c["H"] * causal_pairs(n) * BWD_FLOPS_PER_PAIR for n in lens))
+        vtf = vflops / (ms * 1e-3) / 1e12
+        line["backward_varlen"] = {
+            "metric": "DiffAttn bwd TFLOP/s", "value": world * vtf, "unit": "TFLOP/s",
+            "ms_per_call": ms,
+            "workload": f"backward over {len(lens)} packed sequences of mixed length ({min(lens)}.."
+                        f"{max(lens)} tokens, {total} in total), causal, H12, norm + scale",
+            "roofline": {"bound": "tensor", "achieved": vtf, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": vtf / peak_tf, "flops_per_launch": vflops},
+            "gpu_launches": 5 * n_steps}
+        del pin, q, k, v, dyp, o_pre, stats, ws, grads
+        torch.cuda.empty_cache()
+
     # ======================= V2 decode =======================
     if args.only in ("all", "v2_decode"):
         c = dict(V2_DECODE, B=args.decode_batch)

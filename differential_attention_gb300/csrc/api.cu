@@ -472,23 +472,27 @@ int check_train_shape(const char* fn, int B, int N, int H, int d, int dv, int dt
 }
 }  // namespace
 
-DIFFATTN_API int diffattn_fwd_train(const void* q, const void* k, const void* v, void* out,
-                                    void* o_pre, float* stats, const float* lambda,
-                                    float lambda_init, const float* norm_weight, float eps, int B,
-                                    int N, int H, int d, int dv, int flags, int dtype,
-                                    void* stream) {
+namespace {
+// the training forward, batched (cu null: [B, N, H, *]) or packed (cu [B + 1], N the longest
+// sequence, `total` rows)
+int fwd_train_impl(const char* fn, const void* q, const void* k, const void* v, void* out,
+                   void* o_pre, float* stats, const float* lambda, float lambda_init,
+                   const float* norm_weight, float eps, int B, int N, int H, int d, int dv,
+                   int flags, int dtype, const int* cu, int total, void* stream) {
   if (!q || !k || !v || !out || !o_pre || !stats || !lambda)
-    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_train: null pointer");
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
   constexpr int kTrainFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
-  if (flags & ~kTrainFlags) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_train: unknown flag bits 0x%x", flags);
+  if (flags & ~kTrainFlags) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
   if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
-    return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_train: eps must be > 0 with DIFFATTN_NORM");
-  int rc = check_train_shape("diffattn_fwd_train", B, N, H, d, dv, dtype);
+    return fail(DIFFATTN_ERR_ARG, "%s: eps must be > 0 with DIFFATTN_NORM", fn);
+  int rc = check_train_shape(fn, B, N, H, d, dv, dtype);
   if (rc) return rc;
+  if (cu && (total < N || static_cast<long long>(total) * H > (1LL << 30)))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need max_seqlen <= total and total * H <= 2^30", fn);
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
       !aligned(o_pre, 16) || !aligned(stats, 16) || !aligned(lambda, 4) ||
-      (norm_weight && !aligned(norm_weight, 16)))
-    return fail(DIFFATTN_ERR_ALIGN, "diffattn_fwd_train: tensors must be 16-byte aligned");
+      (norm_weight && !aligned(norm_weight, 16)) || (cu && !aligned(cu, 4)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
   rc = check_device();
   if (rc) return rc;
   da::Problem p{};
@@ -516,39 +520,68 @@ DIFFATTN_API int diffattn_fwd_train(const void* q, const void* k, const void* v,
   p.stats = stats;
   p.o_pre = o_pre;
   p.n_pad = (N + 127) / 128 * 128;
-  return run_prefill(p, dtype, "diffattn_fwd_train", static_cast<cudaStream_t>(stream));
+  p.cu_seqlens = cu;
+  p.total = total;
+  return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+DIFFATTN_API int diffattn_fwd_train(const void* q, const void* k, const void* v, void* out,
+                                    void* o_pre, float* stats, const float* lambda,
+                                    float lambda_init, const float* norm_weight, float eps, int B,
+                                    int N, int H, int d, int dv, int flags, int dtype,
+                                    void* stream) {
+  return fwd_train_impl("diffattn_fwd_train", q, k, v, out, o_pre, stats, lambda, lambda_init,
+                        norm_weight, eps, B, N, H, d, dv, flags, dtype, nullptr, 0, stream);
+}
+
+DIFFATTN_API int diffattn_fwd_train_varlen(const void* q, const void* k, const void* v,
+                                           void* out, void* o_pre, float* stats,
+                                           const int* cu_seqlens, int max_seqlen, int total,
+                                           const float* lambda, float lambda_init,
+                                           const float* norm_weight, float eps, int B, int H,
+                                           int d, int dv, int flags, int dtype, void* stream) {
+  if (!cu_seqlens) return fail(DIFFATTN_ERR_ARG, "diffattn_fwd_train_varlen: null pointer");
+  return fwd_train_impl("diffattn_fwd_train_varlen", q, k, v, out, o_pre, stats, lambda,
+                        lambda_init, norm_weight, eps, B, max_seqlen, H, d, dv, flags, dtype,
+                        cu_seqlens, total, stream);
 }
 
 DIFFATTN_API int diffattn_bwd_workspace_size(int B, int N, int H, int d, int dv, size_t* bytes) {
   if (!bytes) return fail(DIFFATTN_ERR_ARG, "diffattn_bwd_workspace_size: null pointer");
   int rc = check_train_shape("diffattn_bwd_workspace_size", B, N, H, d, dv, DIFFATTN_BF16);
   if (rc) return rc;
-  *bytes = da::backward_workspace_bytes(B, N, H);
+  *bytes = da::backward_workspace_bytes(B, N, H, static_cast<long long>(B) * N);
   return ok();
 }
 
-DIFFATTN_API int diffattn_bwd(const void* q, const void* k, const void* v, const void* o_pre,
-                              const float* stats, const void* dout, const float* lambda,
-                              float lambda_init, const float* norm_weight, float eps, void* dq,
-                              void* dk, void* dv, float* dlambda, float* dnorm_weight, int B,
-                              int N, int H, int d, int dv_width, int flags, int dtype,
-                              void* workspace, size_t ws_bytes, void* stream) {
+namespace {
+// the backward, batched (cu null) or packed (cu [B + 1], N the longest sequence, `total` rows)
+int bwd_impl(const char* fn, const void* q, const void* k, const void* v, const void* o_pre,
+             const float* stats, const void* dout, const float* lambda, float lambda_init,
+             const float* norm_weight, float eps, void* dq, void* dk, void* dv, float* dlambda,
+             float* dnorm_weight, int B, int N, int H, int d, int dv_width, int flags, int dtype,
+             const int* cu, int total, void* workspace, size_t ws_bytes, void* stream) {
   if (!q || !k || !v || !o_pre || !stats || !dout || !lambda || !dq || !dk || !dv || !dlambda)
-    return fail(DIFFATTN_ERR_ARG, "diffattn_bwd: null pointer");
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
   constexpr int kTrainFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
-  if (flags & ~kTrainFlags) return fail(DIFFATTN_ERR_ARG, "diffattn_bwd: unknown flag bits 0x%x", flags);
+  if (flags & ~kTrainFlags) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
   if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
-    return fail(DIFFATTN_ERR_ARG, "diffattn_bwd: eps must be > 0 with DIFFATTN_NORM");
-  int rc = check_train_shape("diffattn_bwd", B, N, H, d, dv_width, dtype);
+    return fail(DIFFATTN_ERR_ARG, "%s: eps must be > 0 with DIFFATTN_NORM", fn);
+  int rc = check_train_shape(fn, B, N, H, d, dv_width, dtype);
   if (rc) return rc;
+  if (cu && (total < N || static_cast<long long>(total) * H > (1LL << 30)))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need max_seqlen <= total and total * H <= 2^30", fn);
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o_pre, 16) ||
       !aligned(stats, 16) || !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) ||
       !aligned(dv, 16) || !aligned(lambda, 4) || !aligned(dlambda, 4) ||
-      (norm_weight && !aligned(norm_weight, 16)) || (dnorm_weight && !aligned(dnorm_weight, 4)))
-    return fail(DIFFATTN_ERR_ALIGN, "diffattn_bwd: tensors must be 16-byte aligned");
-  const size_t need = da::backward_workspace_bytes(B, N, H);
+      (norm_weight && !aligned(norm_weight, 16)) || (dnorm_weight && !aligned(dnorm_weight, 4)) ||
+      (cu && !aligned(cu, 4)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  const long long rows = cu ? total : static_cast<long long>(B) * N;
+  const size_t need = da::backward_workspace_bytes(B, N, H, rows);
   if (!workspace || ws_bytes < need || !aligned(workspace, 256))
-    return fail(DIFFATTN_ERR_WORKSPACE, "diffattn_bwd: need a 256-byte aligned workspace of %zu bytes", need);
+    return fail(DIFFATTN_ERR_WORKSPACE, "%s: need a 256-byte aligned workspace of %zu bytes", fn, need);
   rc = check_device();
   if (rc) return rc;
   da::BackwardArgs a{};
@@ -572,11 +605,51 @@ DIFFATTN_API int diffattn_bwd(const void* q, const void* k, const void* v, const
   a.H = H;
   a.flags = flags;
   a.workspace = workspace;
+  a.cu_seqlens = cu;
+  a.total = total;
   char err[256] = {0};
   cudaError_t e = da::launch_backward(a, static_cast<cudaStream_t>(stream), err, sizeof(err));
-  if (err[0]) return fail(DIFFATTN_ERR_CUDA, "diffattn_bwd: %s", err);
-  if (e != cudaSuccess) return cuda_fail(e, "diffattn_bwd launch");
+  if (err[0]) return fail(DIFFATTN_ERR_CUDA, "%s: %s", fn, err);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
   return ok();
+}
+}  // namespace
+
+DIFFATTN_API int diffattn_bwd(const void* q, const void* k, const void* v, const void* o_pre,
+                              const float* stats, const void* dout, const float* lambda,
+                              float lambda_init, const float* norm_weight, float eps, void* dq,
+                              void* dk, void* dv, float* dlambda, float* dnorm_weight, int B,
+                              int N, int H, int d, int dv_width, int flags, int dtype,
+                              void* workspace, size_t ws_bytes, void* stream) {
+  return bwd_impl("diffattn_bwd", q, k, v, o_pre, stats, dout, lambda, lambda_init, norm_weight,
+                  eps, dq, dk, dv, dlambda, dnorm_weight, B, N, H, d, dv_width, flags, dtype,
+                  nullptr, 0, workspace, ws_bytes, stream);
+}
+
+DIFFATTN_API int diffattn_bwd_varlen_workspace_size(int B, int max_seqlen, int total, int H,
+                                                   int d, int dv, size_t* bytes) {
+  if (!bytes) return fail(DIFFATTN_ERR_ARG, "diffattn_bwd_varlen_workspace_size: null pointer");
+  int rc = check_train_shape("diffattn_bwd_varlen_workspace_size", B, max_seqlen, H, d, dv,
+                             DIFFATTN_BF16);
+  if (rc) return rc;
+  if (total < max_seqlen)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_bwd_varlen_workspace_size: need max_seqlen <= total");
+  *bytes = da::backward_workspace_bytes(B, max_seqlen, H, total);
+  return ok();
+}
+
+DIFFATTN_API int diffattn_bwd_varlen(const void* q, const void* k, const void* v,
+                                     const void* o_pre, const float* stats, const void* dout,
+                                     const int* cu_seqlens, int max_seqlen, int total,
+                                     const float* lambda, float lambda_init,
+                                     const float* norm_weight, float eps, void* dq, void* dk,
+                                     void* dv, float* dlambda, float* dnorm_weight, int B, int H,
+                                     int d, int dv_width, int flags, int dtype, void* workspace,
+                                     size_t ws_bytes, void* stream) {
+  if (!cu_seqlens) return fail(DIFFATTN_ERR_ARG, "diffattn_bwd_varlen: null pointer");
+  return bwd_impl("diffattn_bwd_varlen", q, k, v, o_pre, stats, dout, lambda, lambda_init,
+                  norm_weight, eps, dq, dk, dv, dlambda, dnorm_weight, B, max_seqlen, H, d,
+                  dv_width, flags, dtype, cu_seqlens, total, workspace, ws_bytes, stream);
 }
 
 DIFFATTN_API int diffattn_fwd_fused_lambda(const void* q, const void* k, const void* v, void* out,

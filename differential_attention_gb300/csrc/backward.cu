@@ -138,7 +138,34 @@ struct Args {
   bool norm, causal;
   float c_log2;                // log2(e) / sqrt(d)
   float c;                     // 1 / sqrt(d)
+  // packed sequences (null: batched): sequence b is rows cu[b] .. cu[b+1]-1 of [total, H, *];
+  // N is then the longest sequence, and stats, delta, dl_part keep their per-sequence layout
+  const int* cu;
+  int total;
 };
+
+// Rows of sequence b: [s0, s0 + len) of the token axis (batched: b N .. b N + N - 1), and the
+// TMA coordinates (row, batch) of its first row. False for offsets outside the packed tensor
+// or longer than N: the caller reports DEV_BAD_INDEX and skips the sequence. A tile that reaches
+// past the sequence's end reads (and, for dQ, adds zeros into) the next sequence's rows, which
+// every mask treats as past the end.
+struct SeqRows {
+  int s0, len, trow, tb;
+};
+__device__ __forceinline__ bool seq_rows(const Args& a, int b, SeqRows& s) {
+  if (!a.cu) {
+    s.s0 = b * a.N;
+    s.len = a.N;
+    s.trow = 0;
+    s.tb = b;
+    return true;
+  }
+  s.s0 = a.cu[b];
+  s.len = a.cu[b + 1] - s.s0;
+  s.trow = s.s0;
+  s.tb = 0;
+  return s.s0 >= 0 && s.len >= 0 && s.len <= a.N && s.s0 <= a.total - s.len;
+}
 
 // =============================================================================================
 // bwd_pre_kernel: one warp per (b, n, h) row, lane = 8 channels. Without the norm dO = s dY;
@@ -150,7 +177,9 @@ constexpr int kPreWarps = 8;
 __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(const Args a) {
   __shared__ float sdw[kPreWarps][kDV];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long rows = static_cast<long long>(a.B) * a.N * a.H;
+  // packed: rows past the last sequence belong to none and are skipped
+  const long long rows = a.cu ? static_cast<long long>(min(max(a.cu[a.B], 0), a.total)) * a.H
+                              : static_cast<long long>(a.B) * a.N * a.H;
   float wl[8], dwl[8];
   float4 w0 = make_float4(1.f, 1.f, 1.f, 1.f), w1 = w0;
   if (a.norm_w) {
@@ -202,8 +231,20 @@ __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(const Args a) {
     const float D = warp_sum(Dp);
     const int h = static_cast<int>(r % a.H);
     const long long bn = r / a.H;
-    const int n = static_cast<int>(bn % a.N), b = static_cast<int>(bn / a.N);
-    if (lane == 0) a.delta[(static_cast<size_t>(b) * a.H + h) * 2 * a.Npad + n] = D;
+    int n, b;
+    if (a.cu) {  // the sequence holding token bn: the last b with cu[b] <= bn
+      int lo = 0, hi = a.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.cu[mid] <= bn) lo = mid; else hi = mid - 1;
+      }
+      b = lo;
+      n = static_cast<int>(bn - a.cu[b]);
+    } else {
+      n = static_cast<int>(bn % a.N);
+      b = static_cast<int>(bn / a.N);
+    }
+    if (lane == 0 && n < a.Npad) a.delta[(static_cast<size_t>(b) * a.H + h) * 2 * a.Npad + n] = D;
     float4* zq = reinterpret_cast<float4*>(a.dqacc + static_cast<size_t>(r) * (2 * kD) + 8 * lane);
     zq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     zq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -265,7 +306,17 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
   grouped_item(static_cast<int>(blockIdx.x), a.B * a.H, a.n_t, a.grp_delta, bh, rank);
   const int qt = a.causal ? a.n_t - 1 - rank : rank;
   const int b = bh / a.H, h = bh % a.H;
-  const int n = a.causal ? qt + 1 : a.n_t;  // key tiles
+  SeqRows sq;
+  const bool seq_ok = seq_rows(a, b, sq);
+  const int nts = (sq.len + kT - 1) / kT;  // this sequence's tiles
+  if (!seq_ok || qt >= nts) {  // nothing to do (packed): this tile's share of dlambda is 0
+    if (threadIdx.x == 0) {
+      if (!seq_ok && qt == 0) flag_device_error(DEV_BAD_INDEX);
+      a.dl_part[static_cast<size_t>(bh) * a.n_t + qt] = 0.f;
+    }
+    return;
+  }
+  const int n = a.causal ? qt + 1 : nts;  // key tiles
   auto k_idx = [](int t) { return t + 2 * max(0, t - 1); };
 
   if (threadIdx.x == 0) {
@@ -303,7 +354,8 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
       prefetch_tmap(&tm_vh);
       mbar_arrive_expect_tx(bar(cs.q_full), 2 * kBox);
       for (int c = 0; c < 2; ++c)
-        tma_load_4d(sQ + c * kBox, &tm_q, bar(cs.q_full), kD + 64 * c, h, qt * kT, b);
+        tma_load_4d(sQ + c * kBox, &tm_q, bar(cs.q_full), kD + 64 * c, h, sq.trow + qt * kT,
+                    sq.tb);
       int issued = 0;
       bool ok = true;
       auto acquire = [&](int idx, uint32_t bytes) -> int {
@@ -319,7 +371,7 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
           if (s < 0) { ok = false; break; }
           for (int c = 0; c < 2; ++c)
             tma_load_4d(sRing + s * kSlot + c * kBox, &tm_k, bar(cs.slot_full[s]), kD + 64 * c, h,
-                        t * kT, b);
+                        sq.trow + t * kT, sq.tb);
           issued = ++idx;
         }
         if (t >= 1) {
@@ -328,7 +380,7 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
             if (s < 0) { ok = false; break; }
             for (int c = 0; c < 4; ++c)
               tma_load_4d(sRing + s * kSlot + c * kVHalfBox, &tm_vh, bar(cs.slot_full[s]), 64 * c,
-                          h, (t - 1) * kT + 64 * hf, b);
+                          h, sq.trow + (t - 1) * kT + 64 * hf, sq.tb);
             issued = ++idx;
           }
         }
@@ -397,8 +449,8 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
     const int row = qt * kT + r;
     const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
     const size_t st_base = static_cast<size_t>(b * a.H + h) * 2 * a.Npad;
-    const float b2 = row < a.N ? a.stats[st_base + a.Npad + row] : 0.f;
-    const int lim = a.causal ? min(row + 1, a.N) : a.N;  // keys [0, lim) visible
+    const float b2 = row < sq.len ? a.stats[st_base + a.Npad + row] : 0.f;
+    const int lim = a.causal ? min(row + 1, sq.len) : sq.len;  // keys [0, lim) visible
     const uint32_t p_row = sP + r * 128;
     bool ok = true;
     for (int t = 0; t < n; ++t) {
@@ -445,7 +497,7 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
     if (ok) {
       tc_fence_after();
       const __nv_bfloat16* dorow =
-          a.dO + ((static_cast<size_t>(b) * a.N + min(row, a.N - 1)) * a.H + h) * kDV;
+          a.dO + ((static_cast<size_t>(sq.s0) + min(row, sq.len - 1)) * a.H + h) * kDV;
 #pragma unroll 1
       for (int c = 0; c < kDV / 32; ++c) {
         uint32_t o[32];
@@ -459,7 +511,7 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
           for (int i = 0; i < 8; ++i) d2 = fmaf(f[i], __uint_as_float(o[8 * g + i]), d2);
         }
       }
-      if (row < a.N) {
+      if (row < sq.len) {
         const float lam = a.lambda[h];
         float* dl = a.delta + st_base;
         dl[row] = dl[row] + lam * d2;  // D = dO . O = delta_1 - lam delta_2
@@ -538,8 +590,15 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
   grouped_item(static_cast<int>(blockIdx.x), a.B * a.H * 2, a.n_t, a.grp_dkdq, unit, j);
   const int m = unit & 1, bh = unit >> 1;  // both maps of a head run side by side (shared dO)
   const int b = bh / a.H, h = bh % a.H;
+  SeqRows sq;
+  const bool seq_ok = seq_rows(a, b, sq);
+  const int nts = (sq.len + kT - 1) / kT;  // this sequence's tiles
+  if (!seq_ok || j >= nts) {  // (packed) no keys of this sequence in this tile
+    if (!seq_ok && j == 0 && m == 0 && threadIdx.x == 0) flag_device_error(DEV_BAD_INDEX);
+    return;
+  }
   const int i0 = a.causal ? j : 0;
-  const int T = a.n_t - i0;  // inner (query) tiles
+  const int T = nts - i0;  // inner (query) tiles
 
   if (threadIdx.x == 0) {
     mbar_init(bar(cs.kv_full), 1);
@@ -578,9 +637,10 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       prefetch_tmap(&tm_do);
       mbar_arrive_expect_tx(bar(cs.kv_full), 6 * kBox);
       for (int c = 0; c < 2; ++c)
-        tma_load_4d(sK + c * kBox, &tm_k, bar(cs.kv_full), m * kD + 64 * c, h, j * kT, b);
+        tma_load_4d(sK + c * kBox, &tm_k, bar(cs.kv_full), m * kD + 64 * c, h, sq.trow + j * kT,
+                    sq.tb);
       for (int c = 0; c < 4; ++c)
-        tma_load_4d(sV + c * kBox, &tm_v, bar(cs.kv_full), 64 * c, h, j * kT, b);
+        tma_load_4d(sV + c * kBox, &tm_v, bar(cs.kv_full), 64 * c, h, sq.trow + j * kT, sq.tb);
       bool ok = true;
       int t = 0;
       for (; t < T && ok; ++t) {
@@ -588,11 +648,12 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
         if (!(ok = mbar_wait(bar(cs.do_empty), (t & 1) ^ 1, abrt))) break;
         mbar_arrive_expect_tx(bar(cs.do_full), 4 * kBox);
         for (int c = 0; c < 4; ++c)
-          tma_load_4d(sDO + c * kBox, &tm_do, bar(cs.do_full), 64 * c, h, i * kT, b);
+          tma_load_4d(sDO + c * kBox, &tm_do, bar(cs.do_full), 64 * c, h, sq.trow + i * kT, sq.tb);
         if (!(ok = mbar_wait(bar(cs.q_empty), (t & 1) ^ 1, abrt))) break;
         mbar_arrive_expect_tx(bar(cs.q_full), 2 * kBox + 2 * kT * 4);
         for (int c = 0; c < 2; ++c)
-          tma_load_4d(sQ + c * kBox, &tm_q, bar(cs.q_full), m * kD + 64 * c, h, i * kT, b);
+          tma_load_4d(sQ + c * kBox, &tm_q, bar(cs.q_full), m * kD + 64 * c, h, sq.trow + i * kT,
+                      sq.tb);
         bulk_load(sBD, a.stats + st_base + static_cast<size_t>(i) * kT, kT * 4, bar(cs.q_full));
         bulk_load(sBD + kT * 4, a.delta + st_base + static_cast<size_t>(i) * kT, kT * 4,
                   bar(cs.q_full));
@@ -687,7 +748,7 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       const float nb = -bd[r], nd = -bd[kT + r] * coef;
       const uint64_t nb2 = f2pack(nb, nb), nd2 = f2pack(nd, nd);
       // masks only where the tile reaches past N or crosses the diagonal
-      const bool edge = (j + 1) * kT > a.N || (i + 1) * kT > a.N || (a.causal && i == j);
+      const bool edge = (j + 1) * kT > sq.len || (i + 1) * kT > sq.len || (a.causal && i == j);
       uint32_t pk[32];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -708,8 +769,8 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
           f2unpack(f2mul(f2pack(ex2_approx(x0), ex2_approx(x1)), g), y0, y1);
           if (edge) {
             const int kk0 = j * kT + 64 * wg + 32 * hh + e;
-            const bool v0 = kk0 < a.N && qq < a.N && (!a.causal || qq >= kk0);
-            const bool v1 = kk0 + 1 < a.N && qq < a.N && (!a.causal || qq >= kk0 + 1);
+            const bool v0 = kk0 < sq.len && qq < sq.len && (!a.causal || qq >= kk0);
+            const bool v1 = kk0 + 1 < sq.len && qq < sq.len && (!a.causal || qq >= kk0 + 1);
             y0 = v0 ? y0 : 0.f;
             y1 = v1 ? y1 : 0.f;
           }
@@ -738,8 +799,8 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       tmem_ld32(tmem + tl + 2 * kT + 64 * wg, o[0]);
       tmem_ld32(tmem + tl + 2 * kT + 64 * wg + 32, o[1]);
       tmem_wait_ld();
-      if (key < a.N) {
-        __nv_bfloat16* dst = a.dk + ((static_cast<size_t>(b) * a.N + key) * a.H + h) * (2 * kD) +
+      if (key < sq.len) {
+        __nv_bfloat16* dst = a.dk + ((static_cast<size_t>(sq.s0) + key) * a.H + h) * (2 * kD) +
                              m * kD + 64 * wg;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh)
@@ -791,7 +852,8 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       if (r == 0) {
         const int i = i0 + t;
         for (int c = 0; c < 4; ++c)
-          tma_reduce_add_4d(&tm_dqacc, sDO + c * kBox, m * kD + 32 * c, h, i * kT, b);
+          tma_reduce_add_4d(&tm_dqacc, sDO + c * kBox, m * kD + 32 * c, h, sq.trow + i * kT,
+                            sq.tb);
         bulk_commit();
         bulk_wait_read();
         mbar_arrive(bar(cs.do_empty));  // the slot may take the next dO tile
@@ -856,8 +918,15 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
   int bh, j;
   grouped_item(static_cast<int>(blockIdx.x), a.B * a.H, a.n_t, a.grp_dv, bh, j);
   const int b = bh / a.H, h = bh % a.H;
+  SeqRows sq;
+  const bool seq_ok = seq_rows(a, b, sq);
+  const int nts = (sq.len + kT - 1) / kT;  // this sequence's tiles
+  if (!seq_ok || j >= nts) {  // (packed) no keys of this sequence in this tile
+    if (!seq_ok && j == 0 && threadIdx.x == 0) flag_device_error(DEV_BAD_INDEX);
+    return;
+  }
   const int i0 = a.causal ? j : 0;
-  const int T = a.n_t - i0;
+  const int T = nts - i0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(cs.kv_full), 1);
@@ -895,7 +964,7 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
       prefetch_tmap(&tm_do);
       mbar_arrive_expect_tx(bar(cs.kv_full), 4 * kBox);
       for (int c = 0; c < 4; ++c)
-        tma_load_4d(sK + c * kBox, &tm_k, bar(cs.kv_full), 64 * c, h, j * kT, b);
+        tma_load_4d(sK + c * kBox, &tm_k, bar(cs.kv_full), 64 * c, h, sq.trow + j * kT, sq.tb);
       bool ok = true;
       int t = 0;
       for (; t < T && ok; ++t) {
@@ -904,7 +973,7 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
         if (!(ok = mbar_wait(bar(cs.b_empty[t & 1]), ((t >> 1) & 1) ^ 1, abrt))) break;
         mbar_arrive_expect_tx(bar(cs.q_full), 4 * kBox + 2 * kT * 4);
         for (int c = 0; c < 4; ++c)
-          tma_load_4d(sQ + c * kBox, &tm_q, bar(cs.q_full), 64 * c, h, i * kT, b);
+          tma_load_4d(sQ + c * kBox, &tm_q, bar(cs.q_full), 64 * c, h, sq.trow + i * kT, sq.tb);
         const uint32_t sb = sB + (t & 1) * 2 * kT * 4;
         bulk_load(sb, a.stats + st_base + static_cast<size_t>(i) * kT, kT * 4, bar(cs.q_full));
         bulk_load(sb + kT * 4, a.stats + st_base + a.Npad + static_cast<size_t>(i) * kT, kT * 4,
@@ -912,7 +981,7 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
         if (!(ok = mbar_wait(bar(cs.do_empty), (t & 1) ^ 1, abrt))) break;
         mbar_arrive_expect_tx(bar(cs.do_full), 4 * kBox);
         for (int c = 0; c < 4; ++c)
-          tma_load_4d(sDO + c * kBox, &tm_do, bar(cs.do_full), 64 * c, h, i * kT, b);
+          tma_load_4d(sDO + c * kBox, &tm_do, bar(cs.do_full), 64 * c, h, sq.trow + i * kT, sq.tb);
       }
       mbar_wait(bar(cs.kv_full), 0, nullptr);
       if (t > 0) {
@@ -987,7 +1056,7 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
       mbar_arrive(bar(cs.b_empty[t & 1]));  // this buffer of b1, b2 may be refilled (tile t + 2)
       const uint64_t nb1_2 = f2pack(nb1, nb1), nb2_2 = f2pack(nb2, nb2);
       const int qq = i * kT + r;
-      const bool edge = (j + 1) * kT > a.N || (i + 1) * kT > a.N || (a.causal && i == j);
+      const bool edge = (j + 1) * kT > sq.len || (i + 1) * kT > sq.len || (a.causal && i == j);
       uint32_t pk[32];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -1010,8 +1079,8 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
                    w0, w1);
           if (edge) {
             const int kk0 = j * kT + 64 * wg + 32 * hh + e;
-            const bool v0 = kk0 < a.N && qq < a.N && (!a.causal || qq >= kk0);
-            const bool v1 = kk0 + 1 < a.N && qq < a.N && (!a.causal || qq >= kk0 + 1);
+            const bool v0 = kk0 < sq.len && qq < sq.len && (!a.causal || qq >= kk0);
+            const bool v1 = kk0 + 1 < sq.len && qq < sq.len && (!a.causal || qq >= kk0 + 1);
             w0 = v0 ? w0 : 0.f;
             w1 = v1 ? w1 : 0.f;
           }
@@ -1041,8 +1110,8 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
         uint32_t o[32];
         tmem_ld32(tmem + tl + 2 * kT + 128 * wg + 32 * c, o);
         tmem_wait_ld();
-        if (key < a.N) {
-          __nv_bfloat16* dst = a.dv + ((static_cast<size_t>(b) * a.N + key) * a.H + h) * kDV +
+        if (key < sq.len) {
+          __nv_bfloat16* dst = a.dv + ((static_cast<size_t>(sq.s0) + key) * a.H + h) * kDV +
                                128 * wg + 32 * c;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -1073,6 +1142,8 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
 // =============================================================================================
 __global__ void __launch_bounds__(256) bwd_finish_kernel(const Args a, long long n8, int nq) {
   if (static_cast<int>(blockIdx.x) < nq) {
+    // packed: rows past the last sequence belong to none and are not written
+    if (a.cu) n8 = min(n8, static_cast<long long>(min(max(a.cu[a.B], 0), a.total)) * a.H * 2 * kD / 8);
     for (long long e = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; e < n8;
          e += static_cast<long long>(nq) * 256) {
       const float4* src = reinterpret_cast<const float4*>(a.dqacc) + 2 * e;
@@ -1131,11 +1202,12 @@ struct WsLayout {
   size_t dO, delta, dqacc, dw_part, dl_part, total;
   int pre_blocks;
 };
-static WsLayout ws_layout(int B, int N, int H) {
+// tokens: B N (batched) or the packed length
+static WsLayout ws_layout(int B, int N, int H, long long tokens) {
   WsLayout w;
   const int Npad = (N + kT - 1) / kT * kT;
   const int n_t = Npad / kT;
-  const long long rows = static_cast<long long>(B) * N * H;
+  const long long rows = tokens * H;
   long long blocks = (rows + kPreWarps - 1) / kPreWarps;
   w.pre_blocks = static_cast<int>(blocks < 8 * 152 ? blocks : 8 * 152);
   size_t off = 0;
@@ -1155,13 +1227,17 @@ static WsLayout ws_layout(int B, int N, int H) {
 
 }  // namespace bwd
 
-size_t backward_workspace_bytes(int B, int N, int H) { return bwd::ws_layout(B, N, H).total; }
+size_t backward_workspace_bytes(int B, int N, int H, long long rows) {
+  return bwd::ws_layout(B, N, H, rows).total;
+}
 
 cudaError_t status_backward(int* v) { return read_clear_status(v); }
 
 cudaError_t launch_backward(const BackwardArgs& x, cudaStream_t st, char* err, size_t err_len) {
   using namespace bwd;
-  const WsLayout L = ws_layout(x.B, x.N, x.H);
+  const bool packed = x.cu_seqlens != nullptr;
+  const long long tokens = packed ? x.total : static_cast<long long>(x.B) * x.N;
+  const WsLayout L = ws_layout(x.B, x.N, x.H, tokens);
   uint8_t* ws = static_cast<uint8_t*>(x.workspace);
   Args a{};
   a.q = static_cast<const __nv_bfloat16*>(x.q);
@@ -1194,6 +1270,8 @@ cudaError_t launch_backward(const BackwardArgs& x, cudaStream_t st, char* err, s
   a.causal = (x.flags & 1) != 0;
   a.c = 1.f / sqrtf(static_cast<float>(kD));
   a.c_log2 = kLog2e * a.c;
+  a.cu = x.cu_seqlens;
+  a.total = x.total;
   {
     // bytes each unit keeps re-reading (or, for dQ, accumulating) while its tiles run; a group
     // keeps about 48 MB of them in the 126 MB L2
@@ -1208,13 +1286,15 @@ cudaError_t launch_backward(const BackwardArgs& x, cudaStream_t st, char* err, s
     if (a.grp_dkdq > 2 * x.B * x.H) a.grp_dkdq = 2 * x.B * x.H;
   }
 
+  // packed: the token axis as one batch row of `total`
+  const int mN = packed ? x.total : x.N, mB = packed ? 1 : x.B;
   CUtensorMap mq, mk, mv, mvh, mdo, mdq;
-  if (!make_map_f32(&mdq, a.dqacc, 2 * kD, x.H, x.N, x.B, err, err_len) ||
-      !make_map(&mq, x.q, 2 * kD, x.H, x.N, x.B, kT, err, err_len) ||
-      !make_map(&mk, x.k, 2 * kD, x.H, x.N, x.B, kT, err, err_len) ||
-      !make_map(&mv, x.v, kDV, x.H, x.N, x.B, kT, err, err_len) ||
-      !make_map(&mvh, x.v, kDV, x.H, x.N, x.B, kT / 2, err, err_len) ||
-      !make_map(&mdo, a.dO, kDV, x.H, x.N, x.B, kT, err, err_len))
+  if (!make_map_f32(&mdq, a.dqacc, 2 * kD, x.H, mN, mB, err, err_len) ||
+      !make_map(&mq, x.q, 2 * kD, x.H, mN, mB, kT, err, err_len) ||
+      !make_map(&mk, x.k, 2 * kD, x.H, mN, mB, kT, err, err_len) ||
+      !make_map(&mv, x.v, kDV, x.H, mN, mB, kT, err, err_len) ||
+      !make_map(&mvh, x.v, kDV, x.H, mN, mB, kT / 2, err, err_len) ||
+      !make_map(&mdo, a.dO, kDV, x.H, mN, mB, kT, err, err_len))
     return cudaErrorInvalidValue;
 
   bwd_pre_kernel<<<L.pre_blocks, kPreWarps * 32, 0, st>>>(a);
@@ -1237,7 +1317,7 @@ cudaError_t launch_backward(const BackwardArgs& x, cudaStream_t st, char* err, s
   bwd_dv_kernel<<<items, vv::kThreads, vv::kDynSmem, st>>>(mq, mk, mdo, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  const long long n8 = static_cast<long long>(x.B) * x.N * x.H * 2 * kD / 8;
+  const long long n8 = tokens * x.H * 2 * kD / 8;
   long long nq = (n8 + 255) / 256;
   if (nq > 4 * 152) nq = 4 * 152;
   bwd_finish_kernel<<<static_cast<int>(nq) + 1, 256, 0, st>>>(a, n8, static_cast<int>(nq));

@@ -234,8 +234,13 @@ struct BackwardArgs {
   float* dnorm_w;
   int B, N, H, flags;
   void* workspace;
+  // packed sequences (null: batched [B, N, H, *]): rows cu_seqlens[b] .. cu_seqlens[b+1]-1 of
+  // [total, H, *]; N is then the longest sequence
+  const int* cu_seqlens;
+  int total;
 };
-size_t backward_workspace_bytes(int B, int N, int H);
+// rows: B N (batched) or `total` (packed); N the (longest) sequence length
+size_t backward_workspace_bytes(int B, int N, int H, long long rows);
 cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s, char* err, size_t err_len);
 cudaError_t status_backward(int* v);
 

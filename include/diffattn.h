@@ -504,6 +504,39 @@ DIFFATTN_API int diffattn_bwd(const void* q, const void* k, const void* v, const
                               int N, int H, int d, int dv_width, int flags, int dtype,
                               void* workspace, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Training over packed sequences: diffattn_fwd_train and diffattn_bwd for sequences of
+ * different lengths packed along the token axis, each attending only to itself, as
+ * diffattn_fwd_varlen does for the forward.
+ *   q, k : device [total, H, 2d];  v, out, o_pre, dout : device [total, H, dv];
+ *   dq, dk : device [total, H, 2d];  dv : device [total, H, dv]
+ *   cu_seqlens : device int32 [B + 1], non-decreasing from 0: sequence b is rows
+ *            cu_seqlens[b] .. cu_seqlens[b+1]-1. Checked on the device: a sequence outside
+ *            [0, total) or longer than max_seqlen is skipped and reported by
+ *            diffattn_device_status() as DIFFATTN_ERR_INDEX.
+ *   stats : device fp32 [B, H, 2, Npad], Npad = max_seqlen rounded up to a multiple of 128;
+ *            row i of sequence b at index i (entries past the sequence's length mean nothing)
+ *   workspace, ws_bytes : at least diffattn_bwd_varlen_workspace_size() bytes
+ * Rows that belong to no sequence are not written. dlambda and dnorm_weight sum over every
+ * sequence. Other arguments, support and errors as diffattn_fwd_train and diffattn_bwd.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_fwd_train_varlen(const void* q, const void* k, const void* v,
+                                           void* out, void* o_pre, float* stats,
+                                           const int* cu_seqlens, int max_seqlen, int total,
+                                           const float* lambda, float lambda_init,
+                                           const float* norm_weight, float eps, int B, int H,
+                                           int d, int dv, int flags, int dtype, void* stream);
+DIFFATTN_API int diffattn_bwd_varlen_workspace_size(int B, int max_seqlen, int total, int H,
+                                                   int d, int dv, size_t* bytes);
+DIFFATTN_API int diffattn_bwd_varlen(const void* q, const void* k, const void* v,
+                                     const void* o_pre, const float* stats, const void* dout,
+                                     const int* cu_seqlens, int max_seqlen, int total,
+                                     const float* lambda, float lambda_init,
+                                     const float* norm_weight, float eps, void* dq, void* dk,
+                                     void* dv, float* dlambda, float* dnorm_weight, int B, int H,
+                                     int d, int dv_width, int flags, int dtype, void* workspace,
+                                     size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

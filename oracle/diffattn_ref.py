@@ -523,3 +523,25 @@ def diffattn_v2_fwd_paged(q, k_pool, v_pool, lam_logit, cu_seqlens_q, seqlens_k,
     k, cu_k = gather_pages(k_pool, block_table, seqlens_k)
     v, _ = gather_pages(v_pool, block_table, seqlens_k)
     return diffattn_v2_fwd_varlen(q, k, v, lam_logit, cu_seqlens_q, cu_k, causal)
+
+
+def diffattn_bwd_varlen(q, k, v, cu_seqlens, lam, lam_init: float, dy, norm_weight=None,
+                        eps: float = 1e-5, norm: bool = True, apply_scale: bool = True,
+                        causal: bool = True):
+    """`diffattn_bwd` over packed sequences (q, k [total, H, 2d], v, dy [total, H, dv]): each
+    sequence's gradients are those of its own forward; dlam and dw sum over the sequences. Rows in
+    no sequence get zero gradients."""
+    q, k, v, dy = _f64(q), _f64(k), _f64(v), _f64(dy)
+    H = q.shape[1]
+    out = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v),
+               dlam=np.zeros(H), dw=np.zeros(v.shape[-1]))
+    for s0, s1 in varlen_segments(cu_seqlens):
+        if s1 == s0:
+            continue
+        g = diffattn_bwd(q[None, s0:s1], k[None, s0:s1], v[None, s0:s1], lam, lam_init,
+                         dy[None, s0:s1], norm_weight, eps, norm, apply_scale, causal)
+        for name in ("dq", "dk", "dv"):
+            out[name][s0:s1] = g[name][0]
+        out["dlam"] += g["dlam"]
+        out["dw"] += g["dw"]
+    return out

@@ -167,6 +167,19 @@ def test_v2_decode_paged_validation(L):
     assert v2p(ws_bytes=need - 1) == -8
 
 
+def test_training_varlen_validation(L):
+    n = ctypes.c_size_t(0)
+    assert L.diffattn_bwd_varlen_workspace_size(2, 300, 200, 2, 128, 256, ctypes.byref(n)) == -2
+    assert L.diffattn_bwd_varlen_workspace_size(2, 300, 600, 2, 128, 256, ctypes.byref(n)) == 0
+    assert L.diffattn_fwd_train_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 16, 32, FAKE, 0.5,
+                                       None, 1e-5, 2, 2, 128, 256, 7, 0, None) == -1
+    assert L.diffattn_fwd_train_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 32, FAKE, 0.5,
+                                       None, 1e-5, 2, 2, 128, 256, 7, 0, None) == -2
+    assert L.diffattn_bwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 32, FAKE, 0.5, None,
+                                 1e-5, FAKE, FAKE, FAKE, FAKE, None, 2, 2, 128, 256, 7, 0, FAKE,
+                                 0, None) == -8
+
+
 def test_training_validation(L):
     def train(q=FAKE, stats=FAKE, d=128, dv=256, flags=7, dtype=0):
         return L.diffattn_fwd_train(q, FAKE, FAKE, FAKE, FAKE, stats, FAKE, 0.5, None, 1e-5, 1, 16,

@@ -137,3 +137,62 @@ def test_bwd_lambda_zero_and_equal_maps():
     want = ref.diffattn_bwd(inp.q, inp.k, inp.v, np.zeros(H), li, dy, norm_weight=w)
     for name in ("dq", "dk", "dv"):
         assert_grad(g[name], want[name], name=name)
+
+
+@pytest.mark.parametrize("lens,causal,norm", [([300, 0, 129, 5, 640], True, True),
+                                              ([128, 257], False, True),
+                                              ([200, 2, 77], True, False)])
+def test_train_varlen(lens, causal, norm):
+    """Training over packed sequences: the forward equals the packed prefill (bit-equal) and every
+    gradient matches the oracle's per-sequence backward; rows in no sequence stay zero."""
+    H = 2
+    total = sum(lens) + 3
+    inp, dy, lam, w = _case(1, total, H, 401 + len(lens), causal)
+    q, k, v, dyp = inp.q[0], inp.k[0], inp.v[0], dy[0]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    li = ref.lambda_init(LAYER)
+    lam_t = torch.tensor(lam, dtype=torch.float32, device=DEV)
+    wd = w.to(DEV) if norm else None
+    qd, kd, vd, cud = q.to(DEV), k.to(DEV), v.to(DEV), cu.to(DEV)
+    out, o_pre, stats = da.diffattn_fwd_train_varlen(qd, kd, vd, cud, lam_t, li, norm_weight=wd,
+                                                     causal=causal, norm=norm)
+    plain = da.diffattn_fwd_varlen(qd, kd, vd, cud, lam_t, li, norm_weight=wd, causal=causal,
+                                   norm=norm)
+    n = sum(lens)
+    assert torch.equal(out[:n], plain[:n])
+    g = da.diffattn_bwd_varlen(qd, kd, vd, o_pre, stats, dyp.to(DEV), cud, lam_t, li,
+                               norm_weight=wd, causal=causal, norm=norm)
+    want = ref.diffattn_bwd_varlen(q, k, v, cu, lam, li, dyp, norm_weight=w if norm else None,
+                                   norm=norm, causal=causal)
+    for name in ("dq", "dk", "dv"):
+        assert_grad(g[name][:n], want[name][:n], name=name)
+        assert torch.count_nonzero(g[name][n:]) == 0
+    terms = np.zeros(H)
+    for s0, s1 in zip(cu[:-1].tolist(), cu[1:].tolist()):
+        if s1 > s0:
+            one = type(inp)(**{**inp.__dict__, "q": inp.q[:, s0:s1], "k": inp.k[:, s0:s1],
+                               "v": inp.v[:, s0:s1]})
+            terms += _dlam_term_scale(one, dy[:, s0:s1], lam, li, w if norm else None, norm,
+                                      True, causal)
+    _assert_dlam(g["dlam"], want["dlam"], terms)
+    if norm:
+        assert_grad(g["dw"], want["dw"], rel_tol=1e-2, name="dw")
+    da.diffattn_device_status()
+
+
+def test_train_varlen_bad_offsets_are_reported():
+    """A sequence running past the packed length (and longer than max_seqlen) is skipped by the
+    forward and every backward kernel, and reported."""
+    inp, dy, lam, w = _case(1, 256, 1, 451, True)
+    cu = torch.tensor([0, 128, 400], dtype=torch.int32, device=DEV)  # 400 > total
+    lam_t = torch.tensor(lam[:1], dtype=torch.float32, device=DEV)
+    q, k, v = inp.q[0].to(DEV), inp.k[0].to(DEV), inp.v[0].to(DEV)
+    out, o_pre, stats = da.diffattn_fwd_train_varlen(q, k, v, cu, lam_t, 0.5, max_seqlen=256)
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_device_status()
+    assert e.value.status == -9
+    da.diffattn_bwd_varlen(q, k, v, o_pre, stats, dy[0].to(DEV), cu, lam_t, 0.5, max_seqlen=256)
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_device_status()
+    assert e.value.status == -9
+    da.diffattn_device_status()

@@ -516,13 +516,32 @@ def pin_paged_prefill():
     assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
 
 
+def pin_bwd_varlen():
+    """Packed backward: with equal lengths it is the batched backward; the per-sequence dlam
+    partial sums add up to the whole."""
+    rng = np.random.default_rng(41)
+    B, N, H, d, dv = 2, 5, 2, 4, 8
+    q = rng.standard_normal((B, N, H, 2 * d)); k = rng.standard_normal((B, N, H, 2 * d))
+    v = rng.standard_normal((B, N, H, dv)); dy = rng.standard_normal((B, N, H, dv))
+    lam = np.array([0.3, 0.7]); w = rng.uniform(0.5, 1.5, dv)
+    want = ref.diffattn_bwd(q, k, v, lam, 0.2, dy, norm_weight=w)
+    cu = np.array([0, N, 2 * N])
+    got = ref.diffattn_bwd_varlen(q.reshape(B * N, H, -1), k.reshape(B * N, H, -1),
+                                  v.reshape(B * N, H, -1), cu, lam, 0.2, dy.reshape(B * N, H, -1),
+                                  norm_weight=w)
+    for name in ("dq", "dk", "dv"):
+        assert np.allclose(got[name], want[name].reshape(B * N, H, -1), rtol=1e-12, atol=1e-12)
+    assert np.allclose(got["dlam"], want["dlam"], rtol=1e-12, atol=1e-12)
+    assert np.allclose(got["dw"], want["dw"], rtol=1e-12, atol=1e-12)
+
+
 PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, pin_lambda_spread,
         pin_softmax_floor, pin_toy_needle_table, pin_worked_example, pin_row_sums,
         pin_lambda_zero_is_softmax_attention, pin_equal_maps_scale_attention, pin_brute_force_tiny,
         pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
         pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen, pin_varlen_qk,
-        pin_v2_varlen, pin_paged_prefill]
+        pin_v2_varlen, pin_paged_prefill, pin_bwd_varlen]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
