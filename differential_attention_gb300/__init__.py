@@ -50,6 +50,8 @@ _SIGNATURES = {
     "diffattn_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p]),
     "diffattn_lambda": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 3
                         + [ctypes.c_void_p, ctypes.c_void_p]),
+    "diffattn_lambda_bwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 3
+                            + [ctypes.c_void_p] * 5),
     "diffattn_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_float, ctypes.c_void_p,
                                                              ctypes.c_float] + [ctypes.c_int] * 7
                      + [ctypes.c_void_p]),
@@ -210,6 +212,24 @@ def diffattn_lambda(lq1, lk1, lq2, lk2, layer: int, out=None, stream=None):
     _check(lib().diffattn_lambda(_ptr(lq1), _ptr(lk1), _ptr(lq2), _ptr(lk2), dim, n_sets,
                                  int(layer), _ptr(out), _stream(stream)))
     return out
+
+
+def diffattn_lambda_bwd(lq1, lk1, lq2, lk2, dlam, stream=None):
+    """Gradients of lambda with respect to its [n_sets, dim] vectors given dlam (fp32,
+    [n_sets * per_set]: each set sums per_set consecutive entries, e.g. the per-head dlambda of
+    diffattn_bwd for one lambda per layer). Returns (dlq1, dlk1, dlq2, dlk2)."""
+    for n, t in (("lq1", lq1), ("lk1", lk1), ("lq2", lq2), ("lk2", lk2), ("dlam", dlam)):
+        _dev(n, t, torch.float32)
+    if not (lq1.shape == lk1.shape == lq2.shape == lk2.shape) or lq1.dim() != 2:
+        raise ValueError("lambda vectors must all be [n_sets, dim]")
+    n_sets, dim = lq1.shape
+    if dlam.numel() % n_sets != 0:
+        raise ValueError("dlam must hold a whole number of entries per set")
+    grads = tuple(torch.empty_like(lq1) for _ in range(4))
+    _check(lib().diffattn_lambda_bwd(_ptr(lq1), _ptr(lk1), _ptr(lq2), _ptr(lk2), _ptr(dlam), dim,
+                                     n_sets, dlam.numel() // n_sets, *(_ptr(g) for g in grads),
+                                     _stream(stream)))
+    return grads
 
 
 def diffattn_fwd(q, k, v, lam, lambda_init: float = 0.0, norm_weight=None, eps: float = 1e-5,

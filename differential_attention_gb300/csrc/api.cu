@@ -116,6 +116,30 @@ DIFFATTN_API int diffattn_lambda(const float* lq1, const float* lk1, const float
   return ok();
 }
 
+DIFFATTN_API int diffattn_lambda_bwd(const float* lq1, const float* lk1, const float* lq2,
+                                     const float* lk2, const float* dlambda, int dim, int n_sets,
+                                     int per_set, float* dlq1, float* dlk1, float* dlq2,
+                                     float* dlk2, void* stream) {
+  const char* fn = "diffattn_lambda_bwd";
+  if (!lq1 || !lk1 || !lq2 || !lk2 || !dlambda || !dlq1 || !dlk1 || !dlq2 || !dlk2)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (dim < 1 || dim > 4096 || n_sets < 1 || per_set < 1 ||
+      static_cast<long long>(n_sets) * per_set > (1LL << 24))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need 1 <= dim <= 4096, n_sets >= 1 and per_set >= 1", fn);
+  for (const void* ptr : {static_cast<const void*>(lq1), static_cast<const void*>(lk1),
+                          static_cast<const void*>(lq2), static_cast<const void*>(lk2),
+                          static_cast<const void*>(dlambda), static_cast<const void*>(dlq1),
+                          static_cast<const void*>(dlk1), static_cast<const void*>(dlq2),
+                          static_cast<const void*>(dlk2)})
+    if (!aligned(ptr, 4)) return fail(DIFFATTN_ERR_ALIGN, "%s: fp32 pointers must be 4-byte aligned", fn);
+  int rc = check_device();
+  if (rc) return rc;
+  cudaError_t e = da::launch_lambda_bwd(lq1, lk1, lq2, lk2, dlambda, dim, n_sets, per_set, dlq1,
+                                        dlk1, dlq2, dlk2, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_lambda_bwd launch");
+  return ok();
+}
+
 static int run_prefill(da::Problem& p, int dtype, const char* name, cudaStream_t s) {
   da::fill_dense_strides(p);
   const bool simt = (p.flags & DIFFATTN_CUDA_CORES) || dtype == DIFFATTN_FP32;

@@ -140,6 +140,10 @@ __host__ __device__ inline int k_col_of(const Problem& p, int r) {
 // Launchers. Each returns cudaSuccess or the launch error; `is_bf16` selects the storage type.
 cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                           int dim, int n_sets, float lambda_init, float* out, cudaStream_t s);
+cudaError_t launch_lambda_bwd(const float* lq1, const float* lk1, const float* lq2,
+                              const float* lk2, const float* dlam, int dim, int n_sets,
+                              int per_set, float* dlq1, float* dlk1, float* dlq2, float* dlk2,
+                              cudaStream_t s);
 cudaError_t launch_prefill_simt(const Problem& p, bool is_bf16, cudaStream_t s);
 // Tensor-core prefill (bf16). Returns cudaErrorNotSupported for shapes it does not cover.
 cudaError_t launch_prefill_tc(const Problem& p, cudaStream_t s, char* err, size_t err_len);

@@ -20,10 +20,11 @@ namespace da {
 // ------------------------------------------------------------------------------------------
 // lambda
 // ------------------------------------------------------------------------------------------
-__global__ void lambda_kernel(const float* __restrict__ lq1, const float* __restrict__ lk1,
-                              const float* __restrict__ lq2, const float* __restrict__ lk2,
-                              int dim, float lambda_init, float* __restrict__ out) {
-  const int set = blockIdx.x;
+// (lq1 . lk1, lq2 . lk2) of set `set`, reduced over the block; every thread gets both.
+__device__ __forceinline__ float2 lambda_dots(const float* __restrict__ lq1,
+                                              const float* __restrict__ lk1,
+                                              const float* __restrict__ lq2,
+                                              const float* __restrict__ lk2, int dim, int set) {
   const size_t base = static_cast<size_t>(set) * dim;
   float d1 = 0.f, d2 = 0.f;
   for (int i = threadIdx.x; i < dim; i += blockDim.x) {
@@ -41,13 +42,40 @@ __global__ void lambda_kernel(const float* __restrict__ lq1, const float* __rest
     red[1][w] = d2;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float a = 0.f, b = 0.f;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
-      a += red[0][i];
-      b += red[1][i];
-    }
-    out[set] = expf(a) - expf(b) + lambda_init;
+  float a = 0.f, b = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {  // the same fixed order in every thread
+    a += red[0][i];
+    b += red[1][i];
+  }
+  return make_float2(a, b);
+}
+
+__global__ void lambda_kernel(const float* __restrict__ lq1, const float* __restrict__ lk1,
+                              const float* __restrict__ lq2, const float* __restrict__ lk2,
+                              int dim, float lambda_init, float* __restrict__ out) {
+  const float2 d = lambda_dots(lq1, lk1, lq2, lk2, dim, blockIdx.x);
+  if (threadIdx.x == 0) out[blockIdx.x] = expf(d.x) - expf(d.y) + lambda_init;
+}
+
+// Gradients of lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init with respect to the four
+// vectors of each set, given g = the sum of dlambda over the set's `per_set` consecutive entries:
+// dlq1 = g e1 lk1, dlk1 = g e1 lq1, dlq2 = -g e2 lk2, dlk2 = -g e2 lq2 (e_m = exp(lq_m . lk_m)).
+__global__ void lambda_bwd_kernel(const float* __restrict__ lq1, const float* __restrict__ lk1,
+                                  const float* __restrict__ lq2, const float* __restrict__ lk2,
+                                  const float* __restrict__ dlam, int dim, int per_set,
+                                  float* __restrict__ dlq1, float* __restrict__ dlk1,
+                                  float* __restrict__ dlq2, float* __restrict__ dlk2) {
+  const int set = blockIdx.x;
+  const float2 d = lambda_dots(lq1, lk1, lq2, lk2, dim, set);
+  float g = 0.f;
+  for (int i = 0; i < per_set; ++i) g += dlam[static_cast<size_t>(set) * per_set + i];
+  const float g1 = g * expf(d.x), g2 = -g * expf(d.y);
+  const size_t base = static_cast<size_t>(set) * dim;
+  for (int i = threadIdx.x; i < dim; i += blockDim.x) {
+    dlq1[base + i] = g1 * lk1[base + i];
+    dlk1[base + i] = g1 * lq1[base + i];
+    dlq2[base + i] = g2 * lk2[base + i];
+    dlk2[base + i] = g2 * lq2[base + i];
   }
 }
 
@@ -75,6 +103,15 @@ cudaError_t status_simt(int* v) { return read_clear_status(v); }
 cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                           int dim, int n_sets, float lambda_init, float* out, cudaStream_t s) {
   lambda_kernel<<<n_sets, 128, 0, s>>>(lq1, lk1, lq2, lk2, dim, lambda_init, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lambda_bwd(const float* lq1, const float* lk1, const float* lq2,
+                              const float* lk2, const float* dlam, int dim, int n_sets,
+                              int per_set, float* dlq1, float* dlk1, float* dlq2, float* dlk2,
+                              cudaStream_t s) {
+  lambda_bwd_kernel<<<n_sets, 128, 0, s>>>(lq1, lk1, lq2, lk2, dlam, dim, per_set, dlq1, dlk1,
+                                           dlq2, dlk2);
   return cudaGetLastError();
 }
 

@@ -107,6 +107,20 @@ DIFFATTN_API int diffattn_lambda(const float* lq1, const float* lk1, const float
                                  const float* lk2, int dim, int n_sets, int layer,
                                  float* lambda_out, void* stream);
 
+/* Gradients of lambda with respect to its four vectors (training; the chain rule through the
+ * re-parameterisation): for set s, g = dlambda[s * per_set] + ... + dlambda[s * per_set +
+ * per_set - 1], e_m = exp(lq_m . lk_m), and
+ *   dlq1 = g e1 lk1,  dlk1 = g e1 lq1,  dlq2 = -g e2 lk2,  dlk2 = -g e2 lq2.
+ * per_set = H sums the per-head dlambda of diffattn_bwd into one lambda per layer; per_set = 1
+ * with n_sets = H is one lambda per head.
+ *   lq1 .. lk2 : device fp32 [n_sets, dim];  dlambda : device fp32 [n_sets * per_set]
+ *   dlq1 .. dlk2 : device fp32 [n_sets, dim] (overwritten)
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_CUDA. */
+DIFFATTN_API int diffattn_lambda_bwd(const float* lq1, const float* lk1, const float* lq2,
+                                     const float* lk2, const float* dlambda, int dim, int n_sets,
+                                     int per_set, float* dlq1, float* dlk1, float* dlq2,
+                                     float* dlk2, void* stream);
+
 /* ------------------------------------------------------------------------------------------
  * Prefill: DiffAttn over N tokens (causal or full), then the per-head epilogue.
  *   q      : device [B, N, H, 2d]  = [Q1 | Q2] per head

@@ -167,6 +167,15 @@ def test_v2_decode_paged_validation(L):
     assert v2p(ws_bytes=need - 1) == -8
 
 
+def test_lambda_bwd_validation(L):
+    args = [FAKE] * 5
+    assert L.diffattn_lambda_bwd(*args, 128, 1, 12, FAKE, FAKE, FAKE, None, None) == -1
+    assert L.diffattn_lambda_bwd(*args, 0, 1, 12, FAKE, FAKE, FAKE, FAKE, None) == -2
+    assert L.diffattn_lambda_bwd(*args, 128, 1, 0, FAKE, FAKE, FAKE, FAKE, None) == -2
+    assert L.diffattn_lambda_bwd(ctypes.c_void_p(0x10002), *args[1:], 128, 1, 12, FAKE, FAKE,
+                                 FAKE, FAKE, None) == -4
+
+
 def test_training_varlen_validation(L):
     n = ctypes.c_size_t(0)
     assert L.diffattn_bwd_varlen_workspace_size(2, 300, 200, 2, 128, 256, ctypes.byref(n)) == -2

@@ -196,3 +196,17 @@ def test_train_varlen_bad_offsets_are_reported():
         da.diffattn_device_status()
     assert e.value.status == -9
     da.diffattn_device_status()
+
+
+
+@pytest.mark.parametrize("n_sets,per_set", [(1, 12), (4, 1)])
+def test_lambda_bwd(n_sets, per_set):
+    """The vectors' gradients from dlambda against the oracle's chain rule (one lambda per layer
+    fed by every head's dlambda, and one per head)."""
+    g = torch.Generator().manual_seed(461 + n_sets)
+    vecs = [torch.randn((n_sets, 128), generator=g) * 0.1 for _ in range(4)]
+    dl = torch.randn((n_sets * per_set,), generator=g)
+    got = da.diffattn_lambda_bwd(*(t.to(DEV) for t in vecs), dl.to(DEV))
+    want = ref.lambda_full_bwd(*vecs, dl.numpy().reshape(n_sets, per_set).sum(axis=1))
+    for a, b in zip(got, want):
+        np.testing.assert_allclose(a.double().cpu().numpy(), b, rtol=1e-5, atol=1e-6)
