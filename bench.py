@@ -832,6 +832,38 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                          "timed": "diffattn_v2_decode call (split kernel + combine kernel)"},
             "gpu_launches": 2 * n_steps}
 
+        # fp8 e4m3 q and K cache (per-tensor scales), V bf16: 3/4 of the bytes for every key
+        q8, qds = to_fp8_e4m3(vd.q)
+        k8, kds = to_fp8_e4m3(vd.k_cache)
+
+        def v2dec8():
+            da.diffattn_v2_decode_fp8(q8, k8, vd.v_cache, vd.lam_logit, qds, kds, workspace=ws,
+                                      out=vdout)
+
+        for _ in range(args.warmup):
+            v2dec8()
+        barrier()
+        evs = [(ev(), ev()) for _ in range(n_steps)]
+        for i in range(n_steps):
+            evs[i][0].record(stream)
+            v2dec8()
+            evs[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        ms8 = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        nbytes8 = nbytes * 3 / 4
+        gbs8 = nbytes8 / (ms8 * 1e-3) / 1e9
+        line["v2_decode_fp8"] = {
+            "metric": "V2 decode HBM GB/s", "value": world * gbs8, "unit": "GB/s",
+            "ms_per_call": ms8, "speedup_vs_bf16_cache": ms / ms8,
+            "workload": f"v2_decode_32k with fp8 e4m3 q and K cache (per-tensor scales), bf16 V",
+            "roofline": {"bound": "hbm", "achieved": gbs8, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs8 / hbm, "bytes_per_launch": nbytes8,
+                         "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
+                         "timed": "diffattn_v2_decode_fp8 call (split kernel + combine kernel)"},
+            "gpu_launches": 2 * n_steps}
+        del q8, k8
+
         # the same cache as pools of pages placed in a random order: 64-token pages (one TMA box
         # per 64 keys) and 16-token pages (the smallest box the tensor-core kernel takes)
         paged = {}

@@ -119,6 +119,9 @@ _SIGNATURES = {
                             + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_v2_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int] * 7
                            + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_v2_decode_fp8": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float] * 2
+                               + [ctypes.c_int] * 6
+                               + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_v2_decode_paged": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 9
                                  + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
 }
@@ -384,6 +387,37 @@ def diffattn_v2_decode(q, k_cache, v_cache, lam_logit, seqlens=None, cuda_cores:
                                     DIFFATTN_CUDA_CORES if cuda_cores else 0,
                                     DIFFATTN_BF16, _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def diffattn_v2_decode_fp8(q8, k_cache8, v_cache, lam_logit, q_descale: float, k_descale: float,
+                           seqlens=None, workspace=None, out=None, stream=None):
+    """DIFF V2 decode with fp8 e4m3 q [B, Hq, d] and K cache [B, Lmax, Hkv, d] (real values
+    q8 * q_descale, k8 * k_descale) and a bf16 V cache."""
+    _dev("q8", q8, torch.float8_e4m3fn)
+    B, Hq, d = q8.shape
+    _dev("k_cache8", k_cache8, torch.float8_e4m3fn)
+    _dev("v_cache", v_cache, torch.bfloat16)
+    Lmax, Hkv = k_cache8.shape[1], k_cache8.shape[2]
+    if k_cache8.shape != (B, Lmax, Hkv, d) or v_cache.shape != k_cache8.shape:
+        raise ValueError("caches must both be [B, Lmax, Hkv, d]")
+    _dev("lam_logit", lam_logit, torch.float32)
+    if lam_logit.shape != (B, Hq // 2):
+        raise ValueError("lam_logit must be [B, Hq/2]")
+    if seqlens is not None:
+        _dev("seqlens", seqlens, torch.int32)
+    if workspace is None:
+        workspace = torch.empty(diffattn_v2_decode_workspace_size(B, Lmax, Hq, Hkv, d),
+                                dtype=torch.uint8, device=q8.device)
+    _dev("workspace", workspace)
+    if out is None:
+        out = torch.empty((B, Hq // 2, d), dtype=torch.bfloat16, device=q8.device)
+    _dev("out", out, torch.bfloat16)
+    _check(lib().diffattn_v2_decode_fp8(_ptr(q8), _ptr(k_cache8), _ptr(v_cache), _ptr(seqlens),
+                                        _ptr(lam_logit), _ptr(out), float(q_descale),
+                                        float(k_descale), B, Lmax, Hq, Hkv, d, 0, _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream(stream)))
     return out
 
 

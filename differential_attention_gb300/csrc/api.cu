@@ -483,6 +483,49 @@ DIFFATTN_API int diffattn_v2_decode_paged(const void* q, const void* k_pool, con
   return ok();
 }
 
+DIFFATTN_API int diffattn_v2_decode_fp8(const void* q8, const void* k_cache8, const void* v_cache,
+                                        const int* seqlens, const float* lam_logit, void* out,
+                                        float q_descale, float k_descale, int B, int Lmax, int Hq,
+                                        int Hkv, int d, int flags, void* workspace,
+                                        size_t ws_bytes, void* stream) {
+  const char* fn = "diffattn_v2_decode_fp8";
+  if (!q8 || !k_cache8 || !v_cache || !lam_logit || !out)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (flags & ~DIFFATTN_CAUSAL) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if (!(q_descale > 0.f) || !(k_descale > 0.f) || !std::isfinite(q_descale * k_descale))
+    return fail(DIFFATTN_ERR_ARG, "%s: descales must be finite and > 0", fn);
+  int rc = check_v2_decode_shape(fn, B, Lmax, Hq, Hkv, d);
+  if (rc) return rc;
+  if (!aligned(q8, 16) || !aligned(k_cache8, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(lam_logit, 4) || (seqlens && !aligned(seqlens, 4)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  const size_t need = da::v2_decode_workspace_bytes(B, Lmax, Hq, Hkv);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(DIFFATTN_ERR_WORKSPACE, "%s: need a 256-byte aligned workspace of %zu bytes", fn, need);
+  rc = check_device();
+  if (rc) return rc;
+  da::V2DecodeArgs a{};
+  a.q = q8;
+  a.k_cache = k_cache8;
+  a.v_cache = v_cache;
+  a.seqlens = seqlens;
+  a.lam_logit = lam_logit;
+  a.out = out;
+  a.B = B;
+  a.Lmax = Lmax;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.ws = static_cast<float*>(workspace);
+  a.k8 = true;
+  a.qk_descale = q_descale * k_descale;
+  char err[256] = {0};
+  cudaError_t e = da::launch_v2_decode_tc(a, static_cast<cudaStream_t>(stream), err, sizeof(err));
+  if (e == cudaErrorNotSupported) return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: unsupported shape", fn);
+  if (e == cudaErrorInvalidValue && err[0]) return fail(DIFFATTN_ERR_CUDA, "%s: %s", fn, err);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
 namespace {
 int check_train_shape(const char* fn, int B, int N, int H, int d, int dv, int dtype) {
   if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);

@@ -152,7 +152,10 @@ __device__ __forceinline__ int page_row(const Params& p, const Item& it, int j) 
   return pg * p.page_size + static_cast<int>(uj - pi * static_cast<uint32_t>(p.page_size));
 }
 
-template <int G>
+// K8: q and the K cache in fp8 e4m3 (scales folded into scale_log2). A K row or a Q row of 128
+// elements is then one 128-byte swizzle atom: one TMA box a tile (the first 16 KB of the tile's
+// 32 KB stage) and four kind::f8f6f4 k-steps for the scores; V and the output product are bf16.
+template <int G, bool K8>
 __global__ void __launch_bounds__(kThreads, 1)
     v2dec_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -221,8 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it.nt == 0) continue;
         const int qs = qi & 1;
         if (!mbar_wait(bar(bars.q_empty[qs]), ((qi >> 1) & 1) ^ 1, abrt)) break;
-        mbar_arrive_expect_tx(bar(bars.q_full[qs]), 2 * G * 128);
-        for (int c = 0; c < 2; ++c)
+        mbar_arrive_expect_tx(bar(bars.q_full[qs]), (K8 ? 1 : 2) * G * 128);
+        for (int c = 0; c < (K8 ? 1 : 2); ++c)
           tma_load_4d(sQ + qs * kQSlot + c * (kN * 128), &tm_q, bar(bars.q_full[qs]), 64 * c,
                       it.g * G, it.b, 0);
         ++qi;
@@ -296,8 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it.nt == 0) continue;
         const int qs = qi & 1;
         if (!(ok = mbar_wait(bar(bars.q_empty[qs]), ((qi >> 1) & 1) ^ 1, abrt))) break;
-        mbar_arrive_expect_tx(bar(bars.q_full[qs]), 2 * G * 128);
-        for (int c = 0; c < 2; ++c)
+        mbar_arrive_expect_tx(bar(bars.q_full[qs]), (K8 ? 1 : 2) * G * 128);
+        for (int c = 0; c < (K8 ? 1 : 2); ++c)
           tma_load_4d(sQ + qs * kQSlot + c * (kN * 128), &tm_q, bar(bars.q_full[qs]), 64 * c,
                       it.g * G, it.b, 0);
         ++qi;
@@ -307,9 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // paged, page size a multiple of 128: the tile is rows row0 .. row0 + 127 of one page
           const int row0 = p.block_table ? page_row(p, it, key) : 0;
           if (!(ok = mbar_wait(bar(bars.kv_empty[st]), ((n / kStages) & 1) ^ 1, abrt))) break;
-          mbar_arrive_expect_tx(bar(bars.k_full[st]), kKV);
+          mbar_arrive_expect_tx(bar(bars.k_full[st]), K8 ? kChunk : kKV);
           if (p.block_table) {
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < (K8 ? 1 : 2); ++c)
               tma_load_4d(sK + st * kKV + c * kChunk, &tm_k, bar(bars.k_full[st]), 64 * c, it.g,
                           row0, 0);
             mbar_arrive_expect_tx(bar(bars.v_full[st]), kKV);
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_4d(sV + st * kKV + c * kChunk, &tm_v, bar(bars.v_full[st]), 64 * c, it.g,
                           row0, 0);
           } else {
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < (K8 ? 1 : 2); ++c)
               tma_load_4d(sK + st * kKV + c * kChunk, &tm_k, bar(bars.k_full[st]), 64 * c, it.g,
                           key, it.b);
             mbar_arrive_expect_tx(bar(bars.v_full[st]), kKV);
@@ -338,7 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ================================ MMA issuer ==================================
     if (lane == 0) {
-      constexpr uint32_t idesc_s = umma_idesc_bf16(kTile, kN, 0, 0);  // A = K, B = Q: K-major
+      constexpr uint32_t idesc_s = K8 ? umma_idesc_e4m3(kTile, kN)   // A = K, B = Q: K-major
+                                      : umma_idesc_bf16(kTile, kN, 0, 0);
       constexpr uint32_t idesc_o = umma_idesc_bf16(kD, kN, 1, 0);     // A = V^T MN-major
       const uint64_t dk0 = umma_smem_desc(sK, 16, 1024);
       const uint64_t dv0 = umma_smem_desc(sV, kChunk, 1024);  // LBO = stride of 64-dim boxes
@@ -359,11 +363,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = mbar_wait(bar(bars.k_full[st]), (nn / kStages) & 1, abrt))) break;
             tc_fence_after();
             const uint64_t kd = desc_add(dk0, st * kKV), qd = desc_add(dq0, qs * kQSlot);
+            if constexpr (K8) {
 #pragma unroll
-            for (int k = 0; k < kD / 16; ++k) {
-              mma_bf16_ss(tmem + sb * kN, desc_add(kd, (k >> 2) * kChunk + (k & 3) * 32),
-                          desc_add(qd, (k >> 2) * (kN * 128) + (k & 3) * 32), idesc_s,
-                          k > 0 ? 1u : 0u);
+              for (int k = 0; k < 4; ++k)  // 32 fp8 elements (32 bytes) a k-step
+                mma_e4m3_ss(tmem + sb * kN, desc_add(kd, k * 32), desc_add(qd, k * 32), idesc_s,
+                            k > 0 ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int k = 0; k < kD / 16; ++k) {
+                mma_bf16_ss(tmem + sb * kN, desc_add(kd, (k >> 2) * kChunk + (k & 3) * 32),
+                            desc_add(qd, (k >> 2) * (kN * 128) + (k & 3) * 32), idesc_s,
+                            k > 0 ? 1u : 0u);
+              }
             }
             tc_commit(bar(bars.s_full[sb]));
             if (t == it.nt - 1) tc_commit(bar(bars.q_empty[qs]));
@@ -545,6 +556,15 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2,
   return encode_tmap_4d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, dims, strides, box, err, err_len);
 }
 
+// The same map over fp8 (one byte an element): box 128 x box1 x box2 x 1, 128-byte rows.
+static bool make_map8(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uint64_t d3,
+                      uint32_t box1, uint32_t box2, char* err, size_t err_len) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), d1, d2, d3};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kD), kD * 1ull * d1, kD * 1ull * d1 * d2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(kD), box1, box2, 1};
+  return encode_tmap_4d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, dims, strides, box, err, err_len);
+}
+
 static int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -553,7 +573,7 @@ static int sm_count() {
   return n;
 }
 
-template <int G>
+template <int G, bool K8>
 static cudaError_t launch_g(const V2DecodeArgs& a, int splits, int chunk, cudaStream_t st,
                             char* err, size_t err_len) {
   CUtensorMap mq, mk, mv;
@@ -563,11 +583,14 @@ static cudaError_t launch_g(const V2DecodeArgs& a, int splits, int chunk, cudaSt
   // warp 0 gathers)
   const uint64_t rows = paged ? static_cast<uint64_t>(a.num_pages) * a.page_size : a.Lmax;
   const uint32_t box_rows = gather ? 1u : kTile;
-  if (!make_map(&mq, a.q, a.Hq, a.B, 1, G, 1, err, err_len) ||
-      !make_map(&mk, a.k_cache, a.Hkv, rows, paged ? 1 : a.B, 1, box_rows, err, err_len) ||
-      !make_map(&mv, a.v_cache, a.Hkv, rows, paged ? 1 : a.B, 1, box_rows, err, err_len))
+  const bool qk_ok =
+      K8 ? make_map8(&mq, a.q, a.Hq, a.B, 1, G, 1, err, err_len) &&
+               make_map8(&mk, a.k_cache, a.Hkv, rows, paged ? 1 : a.B, 1, box_rows, err, err_len)
+         : make_map(&mq, a.q, a.Hq, a.B, 1, G, 1, err, err_len) &&
+               make_map(&mk, a.k_cache, a.Hkv, rows, paged ? 1 : a.B, 1, box_rows, err, err_len);
+  if (!qk_ok || !make_map(&mv, a.v_cache, a.Hkv, rows, paged ? 1 : a.B, 1, box_rows, err, err_len))
     return cudaErrorInvalidValue;
-  auto kern = v2dec_tc_kernel<G>;
+  auto kern = v2dec_tc_kernel<G, K8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
   if (e != cudaSuccess) return e;
   Params p;
@@ -580,7 +603,7 @@ static cudaError_t launch_g(const V2DecodeArgs& a, int splits, int chunk, cudaSt
   p.splits = splits;
   p.chunk = chunk;
   p.n_items = a.B * a.Hkv * splits;
-  p.scale_log2 = kLog2e / sqrtf(static_cast<float>(kD));
+  p.scale_log2 = kLog2e / sqrtf(static_cast<float>(kD)) * (K8 ? a.qk_descale : 1.f);
   p.block_table = a.block_table;
   p.page_size = a.page_size;
   p.max_pages = a.max_pages;
@@ -620,13 +643,18 @@ cudaError_t launch_v2_decode_tc(const V2DecodeArgs& a, cudaStream_t st, char* er
   const int G = a.Hq / a.Hkv;
   if (a.block_table && static_cast<long long>(a.num_pages) * a.page_size > 0x7fffffffLL)
     return cudaErrorNotSupported;
+  // fp8 K rows are gathered by no warp: pages of fp8 K must be whole tiles
+  if (a.k8 && a.block_table && a.page_size % v2tc::kTile != 0) return cudaErrorNotSupported;
   cudaError_t e;
   if (G == 8)
-    e = v2tc::launch_g<8>(a, S, chunk, st, err, err_len);
+    e = a.k8 ? v2tc::launch_g<8, true>(a, S, chunk, st, err, err_len)
+             : v2tc::launch_g<8, false>(a, S, chunk, st, err, err_len);
   else if (G == 4)
-    e = v2tc::launch_g<4>(a, S, chunk, st, err, err_len);
+    e = a.k8 ? v2tc::launch_g<4, true>(a, S, chunk, st, err, err_len)
+             : v2tc::launch_g<4, false>(a, S, chunk, st, err, err_len);
   else if (G == 2)
-    e = v2tc::launch_g<2>(a, S, chunk, st, err, err_len);
+    e = a.k8 ? v2tc::launch_g<2, true>(a, S, chunk, st, err, err_len)
+             : v2tc::launch_g<2, false>(a, S, chunk, st, err, err_len);
   else
     return cudaErrorNotSupported;
   if (e != cudaSuccess) return e;

@@ -186,6 +186,9 @@ struct V2DecodeArgs {
   // b in page block_table[b * max_pages + j / page_size]; Lmax = max_pages * page_size
   const int* block_table;
   int page_size, max_pages, num_pages;
+  // q and k_cache in fp8 e4m3: scores times qk_descale (the product of the two scales)
+  bool k8;
+  float qk_descale;
 };
 // j / page_size = (umulhi(j, magic) + j) >> shift for 0 <= j < 2^31 (division by an invariant
 // integer, Granlund and Montgomery 1994)

@@ -263,6 +263,21 @@ DIFFATTN_API int diffattn_v2_decode(const void* q, const void* k_cache, const vo
                                     int Lmax, int Hq, int Hkv, int d, int flags, int dtype,
                                     void* workspace, size_t ws_bytes, void* stream);
 
+/* DIFF V2 decode with q and the K cache in fp8 e4m3 (page "Differential Transformer: softmax
+ * can't say zero, so it subtracts", on quantized attention logits): the scores come from
+ * fp8 x fp8 tensor-core products, scaled by q_descale * k_descale / sqrt(d); V stays bf16. A
+ * cached key then costs 3/4 of the bf16 cache's bytes.
+ *   q8 : device e4m3 [B, Hq, d] (q ~ q8 * q_descale);  k_cache8 : device e4m3 [B, Lmax, Hkv, d]
+ *   (k ~ k_cache8 * k_descale);  v_cache : device bf16 [B, Lmax, Hkv, d]
+ *   q_descale, k_descale : per-tensor scales, finite and > 0
+ * Other arguments (the workspace included) as diffattn_v2_decode; flags: 0 or DIFFATTN_CAUSAL
+ * (ignored). Errors: ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA. */
+DIFFATTN_API int diffattn_v2_decode_fp8(const void* q8, const void* k_cache8, const void* v_cache,
+                                        const int* seqlens, const float* lam_logit, void* out,
+                                        float q_descale, float k_descale, int B, int Lmax, int Hq,
+                                        int Hkv, int d, int flags, void* workspace,
+                                        size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------------------------
  * DIFF V2 decode over a paged KV cache: the result of diffattn_v2_decode where key j of
  * sequence b sits at row j % page_size of page block_table[b * max_pages + j / page_size].

@@ -176,6 +176,20 @@ def test_lambda_bwd_validation(L):
                                  FAKE, FAKE, None) == -4
 
 
+def test_v2_decode_fp8_validation(L):
+    n = ctypes.c_size_t(0)
+    assert L.diffattn_v2_decode_workspace_size(4, 1024, 16, 2, 128, ctypes.byref(n)) == 0
+
+    def dec(qd=0.5, kd=0.5, Hq=16, ws=n.value, flags=0):
+        return L.diffattn_v2_decode_fp8(FAKE, FAKE, FAKE, None, FAKE, FAKE, qd, kd, 4, 1024, Hq, 2,
+                                        128, flags, FAKE, ws, None)
+    assert dec(qd=0.0) == -1
+    assert dec(kd=float("inf")) == -1
+    assert dec(flags=8) == -1          # no CUDA-core form
+    assert dec(Hq=12) == -2
+    assert dec(ws=n.value - 1) == -8
+
+
 def test_training_varlen_validation(L):
     n = ctypes.c_size_t(0)
     assert L.diffattn_bwd_varlen_workspace_size(2, 300, 200, 2, 128, 256, ctypes.byref(n)) == -2

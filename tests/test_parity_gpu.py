@@ -558,6 +558,28 @@ def test_v2_decode_cuda_core_path(B, L, Hq, Hkv, ragged):
     assert_bf16(got, want)
 
 
+@pytest.mark.parametrize("B,L,Hq,Hkv,ragged", [(3, 700, 16, 2, True), (2, 1000, 16, 4, False),
+                                               (2, 300, 8, 4, True)])
+def test_v2_decode_fp8(B, L, Hq, Hkv, ragged):
+    """fp8 q and K cache against the oracle on the same (dequantized) values, every group size;
+    cache rows past seqlens hold NaN (K) and Inf (V) and must not reach the result."""
+    inp = make_v2_decode_inputs(B, L, Hq, Hkv, 128, seed=261 + L, ragged=ragged)
+    q8, qs = to_fp8_e4m3(inp.q)
+    k8, ks = to_fp8_e4m3(inp.k_cache)
+    vc = inp.v_cache.clone()
+    k8 = k8.clone()
+    for b, n in enumerate(inp.seqlens.tolist()):
+        k8[b, n:] = float("nan")
+        vc[b, n:] = float("inf")
+    got = da.diffattn_v2_decode_fp8(q8.to(DEV), k8.to(DEV), vc.to(DEV), inp.lam_logit.to(DEV), qs,
+                                    ks, seqlens=inp.seqlens.to(DEV))
+    want = ref.diffattn_v2_decode(q8.float() * qs, k8.float() * ks, inp.v_cache, inp.seqlens,
+                                  inp.lam_logit)
+    assert torch.isfinite(got).all()
+    assert_bf16(got, want)
+    da.diffattn_device_status()
+
+
 def test_v2_decode_ignores_cache_past_seqlen():
     """Cache rows past seqlens[b] may hold anything (here NaN and Inf): the result must not see them."""
     inp = make_v2_decode_inputs(3, 520, 16, 2, 128, seed=131)
