@@ -30,6 +30,11 @@ Readings taken where the pages are silent or disagree:
     cached key of its row;
   * V2 pairs heads (2p, 2p+1), uses KV head floor(2p / (Hq/Hkv)), lambda = sigmoid(logit) per
     token and pair, no per-head norm, and the default 1/sqrt(d) scale.
+  * grouped differential attention (the pages give only "3 or 4 signal heads per noise head"):
+    Hs signal heads and Hn noise heads, Hs a multiple of Hn; signal head h keeps its own Q1, K1,
+    V, lambda and norm, and subtracts the map of noise head floor(h / (Hs/Hn)), the noise heads
+    split in contiguous groups as the query heads of a GQA group are. With Hn = Hs it is the
+    ungrouped operator.
 
 Parity pins: every function here is pinned by `tests/test_oracle_pins.py` (worked examples printed
 on the pages, closed forms, library routines for special cases, brute force on tiny inputs).
@@ -544,4 +549,68 @@ def diffattn_bwd_varlen(q, k, v, cu_seqlens, lam, lam_init: float, dy, norm_weig
             out[name][s0:s1] = g[name][0]
         out["dlam"] += g["dlam"]
         out["dw"] += g["dw"]
+    return out
+
+
+# --------------------------------------------------------------------------------------------
+# grouped differential attention: several signal heads subtract one shared noise head
+# ([P3] "What other people found": the Grouped Differential Attention result, 3 or 4 signal
+# heads per noise head against 1:1)
+# --------------------------------------------------------------------------------------------
+
+def gda_noise_head(h: int, n_signal: int, n_noise: int) -> int:
+    """Noise head whose map signal head h subtracts: signal heads are split into n_noise
+    contiguous groups of G = n_signal / n_noise, as the query heads of a GQA group are, so head h
+    takes noise head floor(h / G)."""
+    return h // (n_signal // n_noise)
+
+
+def diffattn_gda_fwd(q, k, v, lam, lam_init: float, n_signal: int, norm_weight=None,
+                     eps: float = 1e-5, norm: bool = True, apply_scale: bool = True,
+                     causal: bool = True, rows=None):
+    """Grouped prefill: signal head h computes (softmax(Q1_h K1_h^T/sqrt d) - lam[h]
+    softmax(Q2_g K2_g^T/sqrt d)) V_h with g = gda_noise_head(h), then the per-head norm and the
+    (1 - lambda_init) scale of the ungrouped operator.
+
+    q, k [B, N, Hs + Hn, d]: heads 0 .. Hs-1 hold the signal heads' Q1 (K1), heads Hs .. Hs+Hn-1
+    the noise heads' Q2 (K2). v [B, N, Hs, dv]. lam [Hs] or a scalar.
+    Returns float64 [B, len(rows), Hs, dv].
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, N, heads, d = q.shape
+    Hs = n_signal
+    Hn = heads - Hs
+    lam = np.broadcast_to(_f64(lam), (Hs,))
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    out = np.empty((B, rows.shape[0], Hs, v.shape[-1]), dtype=np.float64)
+    for b in range(B):
+        for h in range(Hs):
+            g = Hs + gda_noise_head(h, Hs, Hn)
+            O = diff_attn_head(q[b, :, h], k[b, :, h], q[b, :, g], k[b, :, g], v[b, :, h],
+                               float(lam[h]), causal, rows)
+            out[b, :, h, :] = head_epilogue(O, norm_weight, eps, lam_init, norm, apply_scale)
+    return out
+
+
+def diffattn_gda_decode(q, k_cache, v_cache, seqlens, lam, lam_init: float, n_signal: int,
+                        norm_weight=None, eps: float = 1e-5, norm: bool = True,
+                        apply_scale: bool = True):
+    """Grouped decode: one query per sequence over its cached keys 0 .. seqlens[b]-1 (no mask
+    inside that range). q [B, Hs + Hn, d], k_cache [B, L, Hs + Hn, d] (signal heads first, as in
+    `diffattn_gda_fwd`), v_cache [B, L, Hs, dv]. Returns float64 [B, Hs, dv]."""
+    q = _f64(q)
+    B, heads, d = q.shape
+    Hs = n_signal
+    Hn = heads - Hs
+    lam = np.broadcast_to(_f64(lam), (Hs,))
+    seqlens = np.asarray(_f64(seqlens)).astype(np.int64)
+    out = np.empty((B, Hs, v_cache.shape[-1]), dtype=np.float64)
+    for b in range(B):
+        L = int(seqlens[b])
+        kb, vb = _f64(k_cache[b, :L]), _f64(v_cache[b, :L])
+        for h in range(Hs):
+            g = Hs + gda_noise_head(h, Hs, Hn)
+            O = diff_attn_head(q[b, h:h + 1], kb[:, h], q[b, g:g + 1], kb[:, g], vb[:, h],
+                               float(lam[h]), causal=False)
+            out[b, h, :] = head_epilogue(O, norm_weight, eps, lam_init, norm, apply_scale)[0]
     return out

@@ -535,13 +535,54 @@ def pin_bwd_varlen():
     assert np.allclose(got["dw"], want["dw"], rtol=1e-12, atol=1e-12)
 
 
+def pin_gda():
+    """Grouped prefill: with one noise head per signal head it is the ungrouped operator; with G
+    signal heads per noise head it is the ungrouped operator whose Q2, K2 of head h are copies of
+    noise head floor(h / G) (repetition over contiguous groups); a noise head reaches exactly the
+    signal heads of its own group."""
+    rng = np.random.default_rng(43)
+    B, N, d, dv, li = 2, 9, 4, 8, 0.35
+    w = rng.uniform(0.5, 1.5, dv)
+    for Hs, Hn in ((3, 3), (6, 2), (4, 1)):
+        G = Hs // Hn
+        q = rng.standard_normal((B, N, Hs + Hn, d)); k = rng.standard_normal((B, N, Hs + Hn, d))
+        v = rng.standard_normal((B, N, Hs, dv)); lam = rng.uniform(0.1, 0.9, Hs)
+        rep = np.repeat(np.arange(Hs, Hs + Hn), G)            # noise head of each signal head
+        q_v1 = np.concatenate([q[:, :, :Hs], q[:, :, rep]], axis=-1)
+        k_v1 = np.concatenate([k[:, :, :Hs], k[:, :, rep]], axis=-1)
+        for causal in (False, True):
+            want = ref.diffattn_fwd(q_v1, k_v1, v, lam, li, norm_weight=w, causal=causal)
+            got = ref.diffattn_gda_fwd(q, k, v, lam, li, Hs, norm_weight=w, causal=causal)
+            assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+        if Hn > 1:
+            base = ref.diffattn_gda_fwd(q, k, v, lam, li, Hs, norm=False, apply_scale=False)
+            q2 = q.copy(); q2[:, :, Hs + 1] += 1.0               # move noise head 1 only
+            moved = ref.diffattn_gda_fwd(q2, k, v, lam, li, Hs, norm=False, apply_scale=False)
+            same = np.all(np.isclose(moved, base, rtol=0, atol=0), axis=(0, 1, 3))
+            assert same.tolist() == [h // G != 1 for h in range(Hs)]
+
+
+def pin_gda_decode_is_last_prefill_row():
+    """Grouped decode equals the last row of a causal grouped prefill over the same keys."""
+    rng = np.random.default_rng(47)
+    B, L, Hs, Hn, d, dv = 2, 11, 4, 2, 4, 8
+    q = rng.standard_normal((B, L, Hs + Hn, d)); k = rng.standard_normal((B, L, Hs + Hn, d))
+    v = rng.standard_normal((B, L, Hs, dv)); lam = rng.uniform(0.1, 0.9, Hs)
+    full = ref.diffattn_gda_fwd(q, k, v, lam, 0.4, Hs, causal=True)
+    got = ref.diffattn_gda_decode(q[:, -1], k, v, np.array([L, L]), lam, 0.4, Hs)
+    assert np.allclose(got, full[:, -1], rtol=1e-12, atol=1e-12)
+    short = ref.diffattn_gda_decode(q[:, 5], k, v, np.array([6, 6]), lam, 0.4, Hs)
+    assert np.allclose(short, full[:, 5], rtol=1e-12, atol=1e-12)
+
+
 PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, pin_lambda_spread,
         pin_softmax_floor, pin_toy_needle_table, pin_worked_example, pin_row_sums,
         pin_lambda_zero_is_softmax_attention, pin_equal_maps_scale_attention, pin_brute_force_tiny,
         pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
         pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen, pin_varlen_qk,
-        pin_v2_varlen, pin_paged_prefill, pin_bwd_varlen]
+        pin_v2_varlen, pin_paged_prefill, pin_bwd_varlen, pin_gda,
+        pin_gda_decode_is_last_prefill_row]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -556,7 +597,8 @@ def test_pin(pin):
 def _mutants():
     orig = {n: getattr(ref, n) for n in ("lambda_init", "lambda_full", "scores", "diff_weights",
                                          "subln", "head_epilogue", "v2_kv_head", "softmax_rows",
-                                         "diff_attn_head_bwd", "lambda_full_bwd")}
+                                         "diff_attn_head_bwd", "lambda_full_bwd",
+                                         "gda_noise_head")}
 
     def bwd_dlam_sign(*a):
         g = orig["diff_attn_head_bwd"](*a)
@@ -605,6 +647,7 @@ def _mutants():
         "dlam sign": ("diff_attn_head_bwd", bwd_dlam_sign),
         "lambda bwd q/k swapped": ("lambda_full_bwd", lambda_bwd_swapped),
         "varlen: one sequence": ("varlen_segments", lambda cu: [(0, int(np.asarray(cu)[-1]))]),
+        "gda noise heads interleaved": ("gda_noise_head", lambda h, hs, hn: h % hn),
         "queries at the first positions": ("query_positions", lambda Lq, Lk: np.arange(Lq)),
         "paged row: page and offset swapped": ("paged_rows", lambda table, sl, ps, b: (
             np.asarray(ref._f64(table)).astype(np.int64)[b, np.arange(int(np.asarray(ref._f64(sl))[b])) % ps]
