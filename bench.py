@@ -35,6 +35,8 @@ PREFILL = dict(B=4, N=4096, H=12, d=128, dv=256, layer=12)
 DECODE = dict(B=64, L=32768, H=12, d=128, dv=256, layer=12)
 V2 = dict(B=2, N=8192, Hq=64, Hkv=8, d=128)
 V2_DECODE = dict(B=64, L=32768, Hq=64, Hkv=8, d=128)
+GDA = dict(B=4, N=4096, Hs=12, Hn=3, d=128, dv=256, layer=12)       # 4 signal heads per noise head
+GDA_DECODE = dict(B=64, L=32768, Hs=12, Hn=3, d=128, dv=256, layer=12)
 LONG = dict(B=1, N=65536, H=12, d=128, dv=256, layer=24)
 PREFILL_WORKLOAD = ("prefill_3b: B4 N4096 H12 d128 dv256 causal, lambda (layer 12, formed in the "
                     "kernel) + DiffAttn + RMSNorm + (1 - lambda_init)")
@@ -61,6 +63,11 @@ def prefill_flops(cfg=PREFILL, per_pair=FLOPS_PER_PAIR) -> float:
 
 def decode_bytes(cfg=DECODE) -> float:
     return float(cfg["B"] * cfg["L"] * cfg["H"] * (2 * cfg["d"] + cfg["dv"]) * 2)
+
+
+def gda_decode_bytes(cfg=GDA_DECODE) -> float:
+    # each cached row once: K of the signal and noise heads, V of the signal heads
+    return float(cfg["B"] * cfg["L"] * ((cfg["Hs"] + cfg["Hn"]) * cfg["d"] + cfg["Hs"] * cfg["dv"]) * 2)
 
 
 def v2_decode_bytes(cfg=V2_DECODE) -> float:
@@ -271,8 +278,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     import torch
     import torch.distributed as dist
     import differential_attention_gb300 as da
-    from synth import (make_decode_inputs, make_dout, make_lambda_vectors, make_prefill_inputs,
-                       make_v2_decode_inputs, make_v2_inputs, to_fp8_e4m3)
+    from synth import (make_decode_inputs, make_dout, make_gda_decode_inputs, make_gda_inputs,
+                       make_lambda_vectors, make_prefill_inputs, make_v2_decode_inputs,
+                       make_v2_inputs, to_fp8_e4m3)
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -909,6 +917,82 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del vd, ws, vdout
         torch.cuda.empty_cache()
 
+    # ======================= grouped: signal heads sharing noise heads =======================
+    if args.only in ("all", "gda"):
+        gc = GDA
+        ginp = make_gda_inputs(gc["B"], gc["N"], gc["Hs"], gc["Hn"], gc["d"], gc["dv"],
+                               seed=5000 + rank, device=dev)
+        gout = torch.empty((gc["B"], gc["N"], gc["Hs"], gc["dv"]), dtype=torch.bfloat16, device=dev)
+        li_g = da.diffattn_lambda_init(gc["layer"])
+
+        def gda():
+            da.diffattn_gda_fwd(ginp.q, ginp.k, ginp.v, ginp.lam, gc["Hs"], li_g, out=gout)
+
+        for _ in range(args.warmup):
+            gda()
+        barrier()
+        gsteps = max(5, min(50, args.steps))
+        g_ev = [(ev(), ev()) for _ in range(gsteps)]
+        for i in range(gsteps):
+            g_ev[i][0].record(stream)
+            gda()
+            g_ev[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        gms = statistics.mean(a.elapsed_time(b) for a, b in g_ev)
+        gflops = float(gc["B"] * gc["Hs"] * causal_pairs(gc["N"]) * FLOPS_PER_PAIR)
+        gtf = gflops / (gms * 1e-3) / 1e12
+        line["gda_prefill"] = {
+            "metric": "DiffAttn fwd TFLOP/s", "value": world * gtf, "unit": "TFLOP/s",
+            "ms_per_call": gms,
+            "workload": "gda_prefill_3b: B4 N4096, 12 signal heads over 3 noise heads (4 per noise "
+                        "head), d128 dv256 causal, RMSNorm + scale",
+            "roofline": {"bound": "tensor", "achieved": gtf, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": gtf / peak_tf, "flops_per_launch": gflops,
+                         "flops_per_pair": FLOPS_PER_PAIR,
+                         "note": "MMA flops issued: each signal head's CTA recomputes its noise map"},
+            "gpu_launches": gsteps}
+        del ginp, gout
+        torch.cuda.empty_cache()
+
+        gd = dict(GDA_DECODE, B=args.decode_batch)
+        gdi = make_gda_decode_inputs(gd["B"], gd["L"], gd["Hs"], gd["Hn"], gd["d"], gd["dv"],
+                                     seed=5100 + rank, device=dev)
+        gws = torch.empty(da.diffattn_decode_workspace_size(gd["B"], gd["L"], gd["Hs"]),
+                          dtype=torch.uint8, device=dev)
+        gdout = torch.empty((gd["B"], gd["Hs"], gd["dv"]), dtype=torch.bfloat16, device=dev)
+
+        def gdec():
+            da.diffattn_gda_decode(gdi.q, gdi.k_cache, gdi.v_cache, gdi.lam, gd["Hs"], li_g,
+                                   workspace=gws, out=gdout)
+
+        for _ in range(args.warmup):
+            gdec()
+        barrier()
+        gdsteps = max(5, min(50, args.steps))
+        gd_ev = [(ev(), ev()) for _ in range(gdsteps)]
+        for i in range(gdsteps):
+            gd_ev[i][0].record(stream)
+            gdec()
+            gd_ev[i][1].record(stream)
+        barrier()
+        da.diffattn_device_status()
+        gdms = statistics.mean(a.elapsed_time(b) for a, b in gd_ev)
+        gdbytes = gda_decode_bytes(gd)
+        gdgbs = gdbytes / (gdms * 1e-3) / 1e9
+        line["gda_decode"] = {
+            "metric": "decode HBM GB/s", "value": world * gdgbs, "unit": "GB/s", "ms_per_call": gdms,
+            "workload": f"gda_decode_32k: B{gd['B']}, one query per sequence, cache 32768, 12 "
+                        "signal heads over 3 noise heads, d128, dv256, bf16 (cache 20.9 GB at B64)",
+            "roofline": {"bound": "hbm", "achieved": gdgbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gdgbs / hbm, "bytes_per_launch": gdbytes,
+                         "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
+                         "timed": "diffattn_gda_decode call (split kernel + combine kernel); a "
+                                  "noise head's K rows serve its 4 signal heads, repeats from L2"},
+            "gpu_launches": 2 * gdsteps}
+        del gdi, gws, gdout
+        torch.cuda.empty_cache()
+
     # ======================= CPU baseline (rank 0, N = 1 only) =======================
     line["cpu_baseline"] = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":
@@ -927,7 +1011,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2", "v2_decode", "long", "backward", "varlen", "fp8"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "v2", "v2_decode", "long", "backward", "varlen", "fp8", "gda"], default="all",
                     help="profiling aid: run one workload (the JSON line then lacks the others)")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
                     help="profiling aid: a smaller decode batch for captures that save device memory")

@@ -124,6 +124,13 @@ _SIGNATURES = {
                                + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_v2_decode_paged": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 9
                                  + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_gda_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_float, ctypes.c_void_p,
+                                                                 ctypes.c_float] + [ctypes.c_int] * 8
+                         + [ctypes.c_void_p]),
+    "diffattn_gda_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.c_void_p,
+                                                                    ctypes.c_float]
+                            + [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_size_t,
+                                                     ctypes.c_void_p]),
 }
 
 
@@ -934,4 +941,71 @@ def diffattn_fwd_host(q, k, v, out, lq1, lk1, lq2, lk2, layer: int, norm_weight=
                                    dim, sets, int(layer), _ptr(norm_weight), float(eps), B, N, H, d,
                                    dv, _train_flags(causal, norm, scale), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def diffattn_gda_fwd(q, k, v, lam, n_signal: int, lambda_init: float = 0.0, norm_weight=None,
+                     eps: float = 1e-5, causal: bool = True, norm: bool = True, scale: bool = True,
+                     cuda_cores: bool = False, single_pass: bool = False, out=None, stream=None):
+    """Grouped differential-attention prefill: q, k [B, N, n_signal + n_noise, d] (signal heads'
+    Q1/K1 first, then the noise heads' Q2/K2), v [B, N, n_signal, dv], lam [n_signal]; signal
+    head h subtracts noise head h // (n_signal / n_noise). See include/diffattn.h."""
+    _dev("q", q)
+    B, N, heads, d = q.shape
+    n_noise = heads - int(n_signal)
+    dv = v.shape[-1]
+    _dev("k", k, q.dtype)
+    _dev("v", v, q.dtype)
+    if k.shape != q.shape or v.shape[:3] != (B, N, n_signal):
+        raise ValueError("k must match q, and v must be [B, N, n_signal, dv]")
+    _dev("lam", lam, torch.float32)
+    if lam.numel() != n_signal:
+        raise ValueError("lam must hold one value per signal head")
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if out is None:
+        out = torch.empty((B, N, n_signal, dv), dtype=q.dtype, device=q.device)
+    _dev("out", out, q.dtype)
+    flags = ((DIFFATTN_CAUSAL if causal else 0) | (DIFFATTN_NORM if norm else 0)
+             | (DIFFATTN_SCALE if scale else 0) | (DIFFATTN_CUDA_CORES if cuda_cores else 0)
+             | (DIFFATTN_SINGLE_PASS if single_pass else 0))
+    _check(lib().diffattn_gda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lam),
+                                  float(lambda_init), _ptr(norm_weight), float(eps), B, N,
+                                  int(n_signal), n_noise, d, dv, flags, _code(q.dtype),
+                                  _stream(stream)))
+    return out
+
+
+def diffattn_gda_decode(q, k_cache, v_cache, lam, n_signal: int, lambda_init: float = 0.0,
+                        seqlens=None, norm_weight=None, eps: float = 1e-5, norm: bool = True,
+                        scale: bool = True, workspace=None, out=None, stream=None):
+    """Grouped decode: q [B, n_signal + n_noise, d], k_cache [B, Lmax, n_signal + n_noise, d],
+    v_cache [B, Lmax, n_signal, dv], lam [n_signal]; returns [B, n_signal, dv]."""
+    _dev("q", q, torch.bfloat16)
+    B, heads, d = q.shape
+    n_noise = heads - int(n_signal)
+    _dev("k_cache", k_cache, torch.bfloat16)
+    _dev("v_cache", v_cache, torch.bfloat16)
+    Lmax, dv = k_cache.shape[1], v_cache.shape[-1]
+    if k_cache.shape != (B, Lmax, heads, d) or v_cache.shape[:3] != (B, Lmax, n_signal):
+        raise ValueError("caches must be [B, Lmax, n_signal + n_noise, d] and "
+                         "[B, Lmax, n_signal, dv]")
+    _dev("lam", lam, torch.float32)
+    if seqlens is not None:
+        _dev("seqlens", seqlens, torch.int32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    need = diffattn_decode_workspace_size(B, Lmax, int(n_signal), d, dv)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _dev("workspace", workspace)
+    if out is None:
+        out = torch.empty((B, n_signal, dv), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    flags = (DIFFATTN_NORM if norm else 0) | (DIFFATTN_SCALE if scale else 0)
+    _check(lib().diffattn_gda_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
+                                     _ptr(out), _ptr(lam), float(lambda_init), _ptr(norm_weight),
+                                     float(eps), B, Lmax, int(n_signal), n_noise, d, dv, flags,
+                                     DIFFATTN_BF16, _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)))
     return out

@@ -1348,3 +1348,113 @@ DIFFATTN_API int diffattn_fwd_host(const void* q_host, const void* k_host, const
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_fwd_host");
   return ok();
 }
+
+// ---------------------------------------------------------------------------------------------
+// grouped differential attention: n_signal heads, each subtracting the map of one of n_noise
+// shared noise heads (contiguous groups of G = n_signal / n_noise)
+// ---------------------------------------------------------------------------------------------
+static int check_groups(const char* fn, int n_signal, int n_noise) {
+  if (n_signal < 1 || n_noise < 1 || n_signal % n_noise != 0 || n_signal > 65535)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need n_signal a multiple of n_noise >= 1 (got %d, %d)", fn,
+                n_signal, n_noise);
+  return 0;
+}
+
+DIFFATTN_API int diffattn_gda_fwd(const void* q, const void* k, const void* v, void* out,
+                                  const float* lambda, float lambda_init, const float* norm_weight,
+                                  float eps, int B, int N, int n_signal, int n_noise, int d, int dv,
+                                  int flags, int dtype, void* stream) {
+  const char* fn = "diffattn_gda_fwd";
+  if (!q || !k || !v || !out || !lambda) return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (flags & ~kPrefillFlags) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "%s: eps must be > 0 with DIFFATTN_NORM", fn);
+  if (dtype != DIFFATTN_BF16 && dtype != DIFFATTN_FP32)
+    return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16 or DIFFATTN_FP32", fn);
+  if (B < 1 || N < 1) return fail(DIFFATTN_ERR_SHAPE, "%s: B, N must be >= 1", fn);
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  if (!(d == 64 || d == 128) || dv != 2 * d)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need d in {64, 128} and dv = 2d (got d=%d dv=%d)", fn, d, dv);
+  const int heads = n_signal + n_noise;
+  const long long tiles = (static_cast<long long>(N) + 127) / 128 * B * n_signal;
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(N) * heads > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: problem too large for one launch", fn);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = N;
+  p.units = n_signal;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_GDA;
+  p.q_heads = heads;
+  p.kv_heads = heads;
+  p.q_cols = d;
+  p.k_cols = d;
+  p.group = n_signal / n_noise;
+  p.lambda = lambda;
+  p.lam_logit = nullptr;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
+}
+
+DIFFATTN_API int diffattn_gda_decode(const void* q, const void* k_cache, const void* v_cache,
+                                     const int* seqlens, void* out, const float* lambda,
+                                     float lambda_init, const float* norm_weight, float eps, int B,
+                                     int Lmax, int n_signal, int n_noise, int d, int dv, int flags,
+                                     int dtype, void* workspace, size_t ws_bytes, void* stream) {
+  const char* fn = "diffattn_gda_decode";
+  if (!q || !k_cache || !v_cache || !out || !lambda) return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (flags & ~(DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE))
+    return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "%s: eps must be > 0 with DIFFATTN_NORM", fn);
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);
+  if (B < 1 || Lmax < 1 || B > 65535)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need 1 <= B <= 65535 and Lmax >= 1", fn);
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  if (d != 128 || dv != 256)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need d = 128 and dv = 256 (got d=%d dv=%d)", fn, d, dv);
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || (seqlens && !aligned(seqlens, 4)) ||
+      (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  const size_t need = da::decode_workspace_bytes(B, Lmax, n_signal, dv);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(DIFFATTN_ERR_WORKSPACE, "%s: need a 256-byte aligned workspace of %zu bytes", fn, need);
+  int rc = check_device();
+  if (rc) return rc;
+  da::DecodeArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.seqlens = seqlens;
+  a.out = out;
+  a.lambda = lambda;
+  a.lambda_init = lambda_init;
+  a.norm_w = norm_weight;
+  a.eps = eps;
+  a.flags = flags;
+  a.B = B;
+  a.Lmax = Lmax;
+  a.H = n_signal;
+  a.d = d;
+  a.dv = dv;
+  a.ws = static_cast<float*>(workspace);
+  a.noise_group = n_signal / n_noise;
+  cudaError_t e = da::launch_decode(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}

@@ -15,6 +15,9 @@
 // workspace.
 // Stage 2 (decode_combine_kernel, grid H x B): thread c merges the partials of channel c, forms
 // o1/l1 - lambda * o2/l2, and applies the per-head RMSNorm and the (1 - lambda_init) scale.
+// Grouped form (kGrouped; H signal heads sharing H / G noise heads, q [B, H + H/G, 128], K cache
+// [B, L, H + H/G, 128], V cache [B, L, H, 256]): lanes 0-15 read signal head h's K1 row, lanes
+// 16-31 noise head H + h/G's K2 row; the rest is unchanged.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -80,6 +83,7 @@ struct DecSplitParams {
   const int* block_table;  // paged: [B, max_pages]
   int page_size, max_pages, num_pages;
   uint32_t ps_magic, ps_shift;  // j / page_size = (umulhi(j, magic) + j) >> shift, j < 2^31
+  int group;                    // grouped form: signal heads per noise head
 };
 
 // Pool row of key j of sequence b in a paged cache [num_pages, page_size, heads, w]. A page id
@@ -108,19 +112,30 @@ __device__ __forceinline__ size_t cache_row(const DecSplitParams& p, int b, int 
     return static_cast<size_t>(b) * p.Lmax + j;
 }
 
-template <bool kPaged>
+// kGrouped is an instantiation of its own, so that the V1 variants keep their code.
+template <bool kPaged, bool kGrouped = false>
 __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecSplitParams p) {
-  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // grouped: grid (splits x G, noise heads, B), the G signal heads that read one noise head's
+  // rows of a split launched side by side so that the repeats of those rows hit L2
+  const int s = kGrouped ? blockIdx.x / p.group : blockIdx.x;
+  const int h = kGrouped ? blockIdx.y * p.group + blockIdx.x % p.group : blockIdx.y;
+  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int L = p.seqlens ? p.seqlens[b] : p.Lmax;
   L = L < 1 ? 1 : (L > p.Lmax ? p.Lmax : L);
   const int k0 = s * p.chunk;
   const int k1 = min(k0 + p.chunk, L);
 
+  // grouped: this lane's 8 q/k elements are column 8 (lane % 16) of head kh (q [B, heads, 128])
+  constexpr int kHalf = kDecWidth / 2;
+  const int heads = kGrouped ? p.H + p.H / p.group : p.H;
+  const int kh = kGrouped ? (lane < 16 ? h : p.H + h / p.group) : h;
   float qf[8];
   {
-    const uint4 qu = *reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(b) * p.H + h) *
-                                                              kDecWidth + 8 * lane);
+    const __nv_bfloat16* qp =
+        kGrouped ? p.q + (static_cast<size_t>(b) * heads + kh) * kHalf + 8 * (lane & 15)
+                 : p.q + (static_cast<size_t>(b) * p.H + h) * kDecWidth + 8 * lane;
+    const uint4 qu = *reinterpret_cast<const uint4*>(qp);
     bf16x8_to_f32(qu, qf);
 #pragma unroll
     for (int i = 0; i < 8; ++i) qf[i] *= p.scale_log2;
@@ -132,7 +147,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecSpli
   for (int i = 0; i < 8; ++i) o1[i] = o2[i] = 0.f;
 
   const size_t row_stride = static_cast<size_t>(p.H) * kDecWidth;  // elements between keys
-  const __nv_bfloat16* kbase = p.kc + static_cast<size_t>(h) * kDecWidth + 8 * lane;
+  const size_t k_stride = static_cast<size_t>(heads) * kHalf;       // grouped K rows
+  const __nv_bfloat16* kbase =
+      kGrouped ? p.kc + static_cast<size_t>(kh) * kHalf + 8 * (lane & 15)
+               : p.kc + static_cast<size_t>(h) * kDecWidth + 8 * lane;
   const __nv_bfloat16* vbase = p.vc + static_cast<size_t>(h) * kDecWidth + 8 * lane;
 
   for (int g0 = k0 + warp * kG; g0 < k1; g0 += kDecWarps * kG) {
@@ -140,9 +158,15 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecSpli
 #pragma unroll
     for (int e = 0; e < kG; ++e) {
       const int j = min(g0 + e, k1 - 1);  // clamp keeps the load in bounds; masked below
-      const size_t row = cache_row<kPaged>(p, b, j) * row_stride;
-      ku[e] = ldg_stream(kbase + row);
-      vu[e] = ldg_stream(vbase + row);
+      if constexpr (kGrouped) {
+        const size_t r = cache_row<kPaged>(p, b, j);
+        ku[e] = ldg_stream(kbase + r * k_stride);
+        vu[e] = ldg_stream(vbase + r * row_stride);
+      } else {
+        const size_t row = cache_row<kPaged>(p, b, j) * row_stride;
+        ku[e] = ldg_stream(kbase + row);
+        vu[e] = ldg_stream(vbase + row);
+      }
     }
     float sc[kG];
 #pragma unroll
@@ -323,7 +347,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   sp.num_pages = a.num_pages;
   sp.ps_magic = sp.ps_shift = 0;
   if (a.block_table) page_magic(a.page_size, &sp.ps_magic, &sp.ps_shift);
-  if (a.block_table)
+  sp.group = a.noise_group;
+  if (a.noise_group && a.block_table) return cudaErrorNotSupported;  // no paged grouped cache
+  if (a.noise_group)
+    decode_split_kernel<false, true>
+        <<<dim3(S * a.noise_group, a.H / a.noise_group, a.B), kDecThreads, 0, st>>>(sp);
+  else if (a.block_table)
     decode_split_kernel<true><<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
   else
     decode_split_kernel<false><<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
@@ -421,6 +450,7 @@ cudaError_t launch_decode_noalloc(const DecodeArgs& a, cudaStream_t st) {
   sp.chunk = chunk;
   sp.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.d));
   sp.block_table = nullptr;
+  sp.group = 0;
   decode_split_kernel<false><<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

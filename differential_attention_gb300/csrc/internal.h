@@ -7,27 +7,30 @@
 
 namespace da {
 
-enum Mode : int { MODE_V1 = 0, MODE_V2 = 1 };
+enum Mode : int { MODE_V1 = 0, MODE_V2 = 1, MODE_GDA = 2 };
 
 // One prefill problem, in the terms both prefill kernels (tensor-core and CUDA-core) use.
 // A "unit" is one differential head (V1) or one pair of query heads (V2); each unit has two maps
 // r = 0, 1 whose queries/keys are located by the helpers below.
 //   V1: q [B,N,H,2d], k [B,N,H,2d], v [B,N,H,dv]; map r uses columns [r*d, r*d + d) of head h.
 //   V2: q [B,N,Hq,d], k/v [B,N,Hkv,d]; map r uses query head 2p + r and KV head 2p / (Hq/Hkv).
+//   GDA (grouped: Hs signal heads, Hn noise heads): q, k [B,N,Hs+Hn,d], v [B,N,Hs,dv]; map 0
+//        uses head h of q and k, map 1 the noise head Hs + h / (Hs/Hn); V, lambda and the norm
+//        are those of signal head h, as in V1.
 struct Problem {
   const void* q;
   const void* k;
   const void* v;
   void* out;
   int B, N;
-  int units;        // V1: H;  V2: Hq / 2
+  int units;        // V1: H;  V2: Hq / 2;  GDA: Hs
   int dqk, dv;      // query/key width of one map, value width
   int mode;
-  int q_heads;      // heads in the q tensor (V1: H, V2: Hq)
-  int kv_heads;     // heads in the k/v tensors (V1: H, V2: Hkv)
-  int q_cols;       // elements per (token, head) row of q (V1: 2d, V2: d)
+  int q_heads;      // heads in the q tensor (V1: H, V2: Hq, GDA: Hs + Hn)
+  int kv_heads;     // heads in the k (and, but for GDA, v) tensors (V1: H, V2: Hkv, GDA: Hs + Hn)
+  int q_cols;       // elements per (token, head) row of q (V1: 2d, V2 and GDA: d)
   int k_cols;       // same for k
-  int group;        // V2: Hq / Hkv (query heads per KV head); V1: 1
+  int group;        // V2: Hq / Hkv (query heads per KV head); GDA: Hs / Hn; V1: 1
   const float* lambda;     // V1: [H]
   const float* lam_logit;  // V2: [B, N, Hq/2]
   const float* norm_w;     // [dv] or null (weight 1)
@@ -70,6 +73,11 @@ struct Problem {
   int page_size, max_pages, num_pages;
 };
 
+// heads in the v tensor (and the output's units are Problem::units)
+__host__ __device__ inline int v_heads(const Problem& p) {
+  return p.mode == MODE_GDA ? p.units : p.kv_heads;
+}
+
 __host__ inline void fill_dense_strides(Problem& p) {
   if (p.qs[2] != 0) return;
   auto dense = [&](long long (&s)[3], int heads, int cols) {
@@ -79,7 +87,7 @@ __host__ inline void fill_dense_strides(Problem& p) {
   };
   dense(p.qs, p.q_heads, p.q_cols);
   dense(p.ks, p.kv_heads, p.k_cols);
-  dense(p.vs, p.kv_heads, p.dv);
+  dense(p.vs, v_heads(p), p.dv);
   dense(p.os, p.units, p.dv);
 }
 __host__ inline bool dense_strides(const Problem& p) {
@@ -124,14 +132,23 @@ __device__ inline float lambda_from_vectors_warp(const Problem& p, int u) {
   return expf(d1) - expf(d2) + p.lambda_init;
 }
 
+// grouped form: the Q and K head of map r of signal head u (map 1 in noise head u / group)
+__host__ __device__ inline int grouped_head(const Problem& p, int u, int r) {
+  return r == 0 ? u : p.units + u / p.group;
+}
 __host__ __device__ inline int q_head_of(const Problem& p, int u, int r) {
-  return p.mode == MODE_V1 ? u : 2 * u + r;
+  return p.mode == MODE_V1 ? u : p.mode == MODE_V2 ? 2 * u + r : grouped_head(p, u, r);
 }
 __host__ __device__ inline int q_col_of(const Problem& p, int r) {
   return p.mode == MODE_V1 ? r * p.dqk : 0;
 }
+// the V head of unit u (and the K head of both maps in V1 and V2)
 __host__ __device__ inline int kv_head_of(const Problem& p, int u) {
-  return p.mode == MODE_V1 ? u : (2 * u) / p.group;
+  return p.mode == MODE_V2 ? (2 * u) / p.group : u;
+}
+// the K head of map r of unit u
+__host__ __device__ inline int k_head_of(const Problem& p, int u, int r) {
+  return p.mode == MODE_GDA ? grouped_head(p, u, r) : kv_head_of(p, u);
 }
 __host__ __device__ inline int k_col_of(const Problem& p, int r) {
   return p.mode == MODE_V1 ? r * p.dqk : 0;
@@ -166,6 +183,9 @@ struct DecodeArgs {
   // Lmax = max_pages * page_size
   const int* block_table;
   int page_size, max_pages, num_pages;
+  // grouped form: H signal heads, signal head h subtracting noise head H + h / noise_group of
+  // q [B, H + H/G, d] and the K cache [.., H + H/G, d]; 0: the V1 layout
+  int noise_group;
 };
 int decode_splits(int B, int Lmax, int H, int* chunk_out);
 size_t decode_workspace_bytes(int B, int Lmax, int H, int dv);

@@ -107,10 +107,11 @@ enum : int {
 };
 
 // SHARED_K: the V2 operator (both maps read one K tile); without it, V1 (launch_prefill_exact
-// picks the instantiation by mode). KMODE: where the keys are. The key modes are instantiations
-// of their own: their extra live values made the default variants spill at their 96-register
+// picks the instantiation by mode). KMODE: where the keys are. GROUPED: the grouped form (map 1's
+// Q and K in the unit's noise head). The key modes and the grouped form are instantiations of
+// their own: their extra live values made the default variants spill at their 96-register
 // budget.
-template <int DQK, int DV, bool SHARED_K, bool QK8, int KMODE>
+template <int DQK, int DV, bool SHARED_K, bool QK8, int KMODE, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_exact_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -239,12 +240,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ================================ TMA producer ================================
     if (lane == 0) {
-      const int kvh = kv_head_of(P, u);
+      const int kvh = kv_head_of(P, u);  // V (and the K of both maps but in the grouped form)
       mbar_arrive_expect_tx(bar(bars.q_full), C::kQBytes);
       for (int r = 0; r < 2; ++r)
         for (int c = 0; c < C::kQKBoxes; ++c)
           tma_load_4d(sQ + r * C::kQMapBytes + c * C::kChunk, &tm_q, bar(bars.q_full),
-                      q_col_of(P, r) + C::kQKBoxCols * c, q_head_of(P, u, r), seq0 + qt * BM, tb);
+                      q_col_of(P, r) + C::kQKBoxCols * c,
+                      GROUPED ? grouped_head(P, u, r) : (P.mode == MODE_V1 ? u : 2 * u + r),
+                      seq0 + qt * BM, tb);
       int issued = 0;  // loads issued into the ring
       auto acquire = [&](int idx, uint32_t bytes) -> int {
         const int slot = idx % NSLOT;
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int c = 0; c < C::kQKBoxes; ++c)
                 tma_load_4d(sSlot + ks * C::kSlot + (QK8 ? mp * C::kKMapBytes : 0) + c * C::kChunk,
                             &tm_k, bar(bars.slot_full[ks]), k_col_of(P, mp) + C::kQKBoxCols * c,
-                            kvh, krow, tb);
+                            GROUPED ? grouped_head(P, u, mp) : kvh, krow, tb);
             issued = k_load(t, r) + 1;
           }
         }
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bias[mp] = -(M + __log2f(L));
       }
-      if (P.mode == MODE_V1) {
+      if (GROUPED || P.mode == MODE_V1) {
         lam = P.lam_vec[0] ? lam_fused : P.lambda[u];
       } else if (row < (SHARED_K ? SN : P.N)) {
         // V2: the sigmoid of this token's logit for pair u (packed sequences: token seq0 + row;
@@ -656,7 +659,8 @@ static bool make_map(CUtensorMap* m, const void* base, int cols, int heads, int 
   return encode_tmap_4d(m, type, base, dims, strides, box, err, err_len);
 }
 
-template <int DQK, int DV, bool SHARED_K, bool QK8 = false, int KMODE = kKeysShared>
+template <int DQK, int DV, bool SHARED_K, bool QK8 = false, int KMODE = kKeysShared,
+          bool GROUPED = false>
 static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
   using C = Cfg<DQK, DV, SHARED_K, QK8>;
   CUtensorMap mq, mk, mv;
@@ -668,9 +672,9 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
                                          : mN;
   if (!make_map(&mq, p.q, p.q_cols, p.q_heads, mN, mB, p.qs, BM, err, err_len, C::kQKElt) ||
       !make_map(&mk, p.k, p.k_cols, p.kv_heads, mNk, mB, p.ks, BN, err, err_len, C::kQKElt) ||
-      !make_map(&mv, p.v, DV, p.kv_heads, mNk, mB, p.vs, BN / 2, err, err_len))
+      !make_map(&mv, p.v, DV, v_heads(p), mNk, mB, p.vs, BN / 2, err, err_len))
     return cudaErrorInvalidValue;
-  auto kern = prefill_exact_kernel<DQK, DV, SHARED_K, QK8, KMODE>;
+  auto kern = prefill_exact_kernel<DQK, DV, SHARED_K, QK8, KMODE, GROUPED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   KParams kp;
@@ -696,7 +700,13 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
 cudaError_t status_prefill_exact(int* v) { return read_clear_status(v); }
 
 cudaError_t launch_prefill_exact(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
-  if (p.mode == MODE_V1) {
+  if (p.mode == MODE_GDA) {  // grouped: batched, bf16 scores only
+    if (p.qk_fp8 || p.cu_seqlens) return cudaErrorNotSupported;
+    if (p.dqk == 128 && p.dv == 256)
+      return exact::launch_cfg<128, 256, false, false, exact::kKeysShared, true>(p, s, err, err_len);
+    if (p.dqk == 64 && p.dv == 128)
+      return exact::launch_cfg<64, 128, false, false, exact::kKeysShared, true>(p, s, err, err_len);
+  } else if (p.mode == MODE_V1) {
     if (p.qk_fp8) {
       if (p.dqk == 128 && p.dv == 256) return exact::launch_cfg<128, 256, false, true>(p, s, err, err_len);
       return cudaErrorNotSupported;

@@ -155,7 +155,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ================================ TMA producer ================================
     if (lane == 0) {
       const int qh = q_head_of(P, u, rank), qc = q_col_of(P, rank);
-      const int kvh = kv_head_of(P, u), kc = k_col_of(P, rank);
+      const int kvh = kv_head_of(P, u), kc = k_col_of(P, rank);  // V head; K column
+      const int kh = k_head_of(P, u, rank);                        // K head of this CTA's map
       mbar_arrive_expect_tx(bar(bars.q_full), C::kQBytes);
       for (int c = 0; c < DQK / 64; ++c)
         tma_load_4d(sQ + c * C::kChunkBytes, &tm_q, bar(bars.q_full), qc + 64 * c, qh, qt * BM, b);
@@ -167,7 +168,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(bar(bars.k_full[s]), C::kKBytes);
         for (int c = 0; c < DQK / 64; ++c)
           tma_load_4d(sK + s * C::kKBytes + c * C::kChunkBytes, &tm_k, bar(bars.k_full[s]),
-                      kc + 64 * c, kvh, j * BN, b);
+                      kc + 64 * c, kh, j * BN, b);
         if (!mbar_wait(bar(bars.v_empty[s]), ph ^ 1, abrt)) {
           issued = 2 * j + 1;
           break;
@@ -327,7 +328,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     // ------------------------------- epilogue -------------------------------------
     float f;
-    if (P.mode == MODE_V1) {
+    if (P.mode != MODE_V2) {
       f = (rank == 0 ? 1.f : P.lambda[u]) / l;
     } else {
       float lam = 0.f;
@@ -452,7 +453,7 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, p.q, p.q_cols, p.q_heads, p.N, p.B, err, err_len) ||
       !make_map(&mk, p.k, p.k_cols, p.kv_heads, p.N, p.B, err, err_len) ||
-      !make_map(&mv, p.v, DV, p.kv_heads, p.N, p.B, err, err_len))
+      !make_map(&mv, p.v, DV, v_heads(p), p.N, p.B, err, err_len))
     return cudaErrorInvalidValue;
   auto kern = prefill_tc_kernel<DQK, DV, NS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);

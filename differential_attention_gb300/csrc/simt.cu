@@ -170,10 +170,11 @@ __global__ void __launch_bounds__(kSimtRows * 32)
   }
   __syncwarp();
 
-  const int kvh = kv_head_of(p, u);
+  const int kvh = kv_head_of(p, u);  // V head
+  const int kh0 = k_head_of(p, u, 0), kh1 = k_head_of(p, u, 1);
   const int kend = (p.flags & 1) ? (i + 1) : p.N;
   auto krow = [&](int j, int r) {
-    return k + elem_off(p.ks, b, j, kvh) + k_col_of(p, r);
+    return k + elem_off(p.ks, b, j, r ? kh1 : kh0) + k_col_of(p, r);
   };
   auto score = [&](int j, int r) {
     const T* kr = krow(j, r);
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(kSimtRows * 32)
   }
 
   float lam;
-  if (p.mode == MODE_V1) {
+  if (p.mode != MODE_V2) {
     lam = p.lambda[u];
   } else {
     const float x = p.lam_logit[(static_cast<size_t>(b) * p.N + i) * p.units + u];

@@ -566,6 +566,49 @@ DIFFATTN_API int diffattn_bwd_varlen(const void* q, const void* k, const void* v
                                      int d, int dv_width, int flags, int dtype, void* workspace,
                                      size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Grouped differential attention (page "Differential Transformer: softmax can't say zero, so it
+ * subtracts", section "What other people found": the Grouped Differential Attention result, 3
+ * or 4 signal heads per noise head). n_signal heads keep their own Q1, K1, V, lambda and norm;
+ * they are split in n_noise contiguous groups of G = n_signal / n_noise, and signal head h
+ * subtracts the map of noise head h / G:
+ *   out_h = epilogue((softmax(Q1_h K1_h^T / sqrt d) - lambda[h] softmax(Q2_g K2_g^T / sqrt d)) V_h)
+ * with g = h / G and the epilogue of diffattn_fwd. n_noise = n_signal is diffattn_fwd with the
+ * halves of q and k stored as heads of their own.
+ *   q      : device [B, N, n_signal + n_noise, d]: heads 0 .. n_signal-1 hold Q1 of the signal
+ *            heads, heads n_signal .. n_signal+n_noise-1 Q2 of the noise heads
+ *   k      : device [B, N, n_signal + n_noise, d], the same split for K1 and K2
+ *   v, out : device [B, N, n_signal, dv]
+ *   lambda : device fp32 [n_signal]
+ *   lambda_init, norm_weight, eps, flags, dtype : as for diffattn_fwd
+ * Supported: d in {64, 128}, dv = 2d, n_signal a multiple of n_noise. Each signal head's CTA
+ * recomputes its group's noise map (two maps per head, as in diffattn_fwd); the noise heads'
+ * K is read from HBM once per group and from L2 by the group's other heads.
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_gda_fwd(const void* q, const void* k, const void* v, void* out,
+                                  const float* lambda, float lambda_init, const float* norm_weight,
+                                  float eps, int B, int N, int n_signal, int n_noise, int d, int dv,
+                                  int flags, int dtype, void* stream);
+
+/* Grouped decode: one query token per sequence over its cached keys 0 .. seqlens[b]-1, with the
+ * head split of diffattn_gda_fwd.
+ *   q       : device bf16 [B, n_signal + n_noise, d]
+ *   k_cache : device bf16 [B, Lmax, n_signal + n_noise, d]
+ *   v_cache : device bf16 [B, Lmax, n_signal, dv];  out : device bf16 [B, n_signal, dv]
+ *   seqlens, lambda ([n_signal]), lambda_init, norm_weight, eps, flags : as for diffattn_decode
+ *   workspace, ws_bytes : at least diffattn_decode_workspace_size(B, Lmax, n_signal, d, dv)
+ *                         bytes, 256-byte aligned
+ * Supported: d = 128, dv = 256, n_signal a multiple of n_noise. Every cached K1, K2 and V row is
+ * streamed once per head that reads it: a noise row serves the G heads of its group, the
+ * repeats mostly from L2.
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA. */
+DIFFATTN_API int diffattn_gda_decode(const void* q, const void* k_cache, const void* v_cache,
+                                     const int* seqlens, void* out, const float* lambda,
+                                     float lambda_init, const float* norm_weight, float eps, int B,
+                                     int Lmax, int n_signal, int n_noise, int d, int dv, int flags,
+                                     int dtype, void* workspace, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

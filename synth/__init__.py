@@ -9,6 +9,8 @@ from .workloads import (  # noqa: F401
     bf16_round,
     make_decode_inputs,
     make_dout,
+    make_gda_decode_inputs,
+    make_gda_inputs,
     make_lambda_vectors,
     make_prefill_inputs,
     make_tiny_inputs,

@@ -11,6 +11,9 @@ Tensor layouts (all row-major, last dimension contiguous):
   prefill   q [B, N, H, 2d] = [Q1 | Q2],  k [B, N, H, 2d] = [K1 | K2],  v [B, N, H, dv]
   decode    q [B, H, 2d],  k_cache [B, L, H, 2d],  v_cache [B, L, H, dv],  seqlens [B] int32
   V2        q [B, N, Hq, d] (pair p = heads 2p, 2p+1),  k, v [B, N, Hkv, d],  lam_logit [B, N, Hq/2]
+  grouped   q, k [B, N, Hs + Hn, d] (Hs signal heads' Q1/K1, then Hn noise heads' Q2/K2),
+            v [B, N, Hs, dv], lam [Hs]; decode q [B, Hs + Hn, d], caches [B, L, Hs + Hn, d] and
+            [B, L, Hs, dv]
 """
 from __future__ import annotations
 
@@ -28,6 +31,12 @@ WORKLOADS = {
     "decode_32k": dict(B=64, L=32768, H=12, d=128, dv=256, dtype="bf16", layer=12, norm=True),
     "v2_gqa": dict(B=2, N=8192, Hq=64, Hkv=8, d=128, causal=True, dtype="bf16"),
     "v2_decode_32k": dict(B=64, L=32768, Hq=64, Hkv=8, d=128, dtype="bf16"),
+    # grouped: the 12 heads of prefill_3b / decode_32k as signal heads over 3 noise heads (4 per
+    # noise head, the ratio "What other people found" reports for Grouped Differential Attention)
+    "gda_prefill_3b": dict(B=4, N=4096, Hs=12, Hn=3, d=128, dv=256, causal=True, dtype="bf16",
+                           layer=12, norm=True),
+    "gda_decode_32k": dict(B=64, L=32768, Hs=12, Hn=3, d=128, dv=256, dtype="bf16", layer=12,
+                           norm=True),
 }
 
 NORM_EPS = 1e-5
@@ -242,3 +251,60 @@ def to_fp8_e4m3(x: torch.Tensor):
     amax = float(x.float().abs().max())
     descale = amax / 448.0 if amax > 0 else 1.0
     return (x.float() / descale).to(torch.float8_e4m3fn), descale
+
+
+@dataclass
+class GroupedInputs:
+    q: torch.Tensor          # [B, N, Hs + Hn, d]
+    k: torch.Tensor          # [B, N, Hs + Hn, d]
+    v: torch.Tensor          # [B, N, Hs, dv]
+    lam: torch.Tensor        # [Hs] fp32
+    n_signal: int
+    layer: int = 12
+
+
+def make_gda_inputs(B: int, N: int, Hs: int, Hn: int, d: int, dv: int, seed: int, layer: int = 12,
+                    device="cpu", dtype=torch.bfloat16) -> GroupedInputs:
+    """Grouped prefill inputs: q, k, v ~ N(0, 1)/sqrt(d) as for the ungrouped prefill, with the
+    signal and noise heads along one head axis; lambda[h] ~ U[0.2, 0.8]."""
+    g = _gen(seed, device)
+    std = 1.0 / math.sqrt(d)
+    q = _randn((B, N, Hs + Hn, d), g, device, std).to(dtype)
+    k = _randn((B, N, Hs + Hn, d), g, device, std).to(dtype)
+    v = _randn((B, N, Hs, dv), g, device, std).to(dtype)
+    gh = _gen(seed + 1, "cpu")
+    lam = (0.2 + 0.6 * torch.rand((Hs,), generator=gh, dtype=torch.float32)).to(device)
+    return GroupedInputs(q=q, k=k, v=v, lam=lam, n_signal=Hs, layer=layer)
+
+
+@dataclass
+class GroupedDecodeInputs:
+    q: torch.Tensor          # [B, Hs + Hn, d]
+    k_cache: torch.Tensor    # [B, L, Hs + Hn, d]
+    v_cache: torch.Tensor    # [B, L, Hs, dv]
+    seqlens: torch.Tensor    # [B] int32
+    lam: torch.Tensor        # [Hs] fp32
+    n_signal: int
+    layer: int = 12
+
+
+def make_gda_decode_inputs(B: int, L: int, Hs: int, Hn: int, d: int, dv: int, seed: int,
+                           layer: int = 12, device="cpu", ragged: bool = False,
+                           dtype=torch.bfloat16) -> GroupedDecodeInputs:
+    """Grouped decode inputs, drawn as make_decode_inputs draws the ungrouped ones: cache
+    ~ N(0, 1) one batch row at a time, q ~ N(0, 1)/sqrt(d), lambda[h] ~ U[0.2, 0.8]."""
+    g = _gen(seed, device)
+    q = _randn((B, Hs + Hn, d), g, device, 1.0 / math.sqrt(d)).to(dtype)
+    k_cache = torch.empty((B, L, Hs + Hn, d), dtype=dtype, device=device)
+    v_cache = torch.empty((B, L, Hs, dv), dtype=dtype, device=device)
+    for b in range(B):
+        k_cache[b].copy_(_randn((L, Hs + Hn, d), g, device))
+        v_cache[b].copy_(_randn((L, Hs, dv), g, device))
+    gh = _gen(seed + 1, "cpu")
+    lam = (0.2 + 0.6 * torch.rand((Hs,), generator=gh, dtype=torch.float32)).to(device)
+    if ragged:
+        seqlens = torch.randint(1, L + 1, (B,), generator=gh, dtype=torch.int32)
+    else:
+        seqlens = torch.full((B,), L, dtype=torch.int32)
+    return GroupedDecodeInputs(q=q, k_cache=k_cache, v_cache=v_cache, seqlens=seqlens.to(device),
+                               lam=lam, n_signal=Hs, layer=layer)

@@ -312,3 +312,34 @@ def test_paged_and_host_validation(L):
     assert host(q=None) == -1
     assert host(layer=0) == -1
     assert host(ws_bytes=hneed - 1) == -8
+
+
+def test_gda_validation(L):
+    def fwd(ns=12, nn=3, d=128, dv=256, flags=7, dtype=0, q=FAKE, N=16):
+        return L.diffattn_gda_fwd(q, FAKE, FAKE, FAKE, FAKE, 0.5, None, 1e-5, 1, N, ns, nn, d, dv,
+                                  flags, dtype, None)
+
+    assert fwd(q=None) == -1
+    assert fwd(flags=64) == -1
+    assert fwd(dtype=7) == -3
+    assert fwd(N=0) == -2
+    assert fwd(nn=0) == -2
+    assert fwd(ns=12, nn=5) == -2          # not a whole number of signal heads per noise head
+    assert "multiple" in L.diffattn_last_error_string().decode()
+    assert fwd(d=96, dv=192) == -2
+    assert fwd(q=ODD) == -4
+
+    n = ctypes.c_size_t(0)
+    assert L.diffattn_decode_workspace_size(8, 4096, 12, 128, 256, ctypes.byref(n)) == 0
+    need = n.value
+
+    def dec(ns=12, nn=3, d=128, dv=256, dtype=0, ws=FAKE, ws_bytes=need, flags=6):
+        return L.diffattn_gda_decode(FAKE, FAKE, FAKE, None, FAKE, FAKE, 0.5, None, 1e-5, 8, 4096,
+                                     ns, nn, d, dv, flags, dtype, ws, ws_bytes, None)
+
+    assert dec(flags=16) == -1
+    assert dec(dtype=1) == -3
+    assert dec(ns=12, nn=8) == -2
+    assert dec(d=64, dv=128) == -2
+    assert dec(ws_bytes=need - 1) == -8
+    assert dec(ws=ctypes.c_void_p(0x10010)) == -8

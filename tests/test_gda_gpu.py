@@ -1,0 +1,183 @@
+"""GPU parity of grouped differential attention (several signal heads subtracting one shared
+noise head's map): prefill and decode, called through the C ABI, against the float64 oracle on
+identical seeded inputs; small cases on every output element, the full-size workloads on sampled
+rows (prefill) and sampled sequences (decode), in the launch configurations bench.py times."""
+import numpy as np
+import pytest
+import torch
+
+import differential_attention_gb300 as da
+from oracle import diffattn_ref as ref
+from synth import make_gda_decode_inputs, make_gda_inputs
+from tests.gpu_util import assert_bf16, assert_fp32
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    da.build()
+    da.lib()
+    yield
+    da.diffattn_device_status()
+    torch.cuda.empty_cache()
+
+
+def _w(dv):
+    return torch.linspace(0.5, 1.5, dv, dtype=torch.float32)
+
+
+# (B, N, Hs, Hn, d, causal): group sizes 1 (ungrouped), 2, 3, 4 and 12, ragged tails, one token
+GDA_CASES = [
+    (1, 1, 2, 1, 128, True),
+    (2, 77, 12, 3, 128, True),
+    (2, 300, 4, 1, 128, True),
+    (1, 645, 6, 2, 128, True),
+    (2, 129, 3, 3, 128, False),
+    (1, 384, 12, 4, 128, False),
+    (2, 200, 4, 2, 64, True),
+    (1, 333, 6, 3, 64, False),
+]
+
+
+@pytest.mark.parametrize("B,N,Hs,Hn,d,causal", GDA_CASES)
+def test_gda_fwd_small(B, N, Hs, Hn, d, causal):
+    inp = make_gda_inputs(B, N, Hs, Hn, d, 2 * d, seed=101 + N + Hs)
+    li = ref.lambda_init(inp.layer)
+    w = _w(2 * d)
+    got = da.diffattn_gda_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.lam.to(DEV), Hs,
+                              li, norm_weight=w.to(DEV), causal=causal)
+    want = ref.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, li, Hs, norm_weight=w, causal=causal)
+    assert_bf16(got, want)
+    da.diffattn_device_status()
+
+
+def test_gda_fwd_no_norm_no_scale():
+    inp = make_gda_inputs(1, 200, 6, 2, 128, 256, seed=7)
+    got = da.diffattn_gda_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.lam.to(DEV), 6,
+                              0.3, norm=False, scale=False)
+    want = ref.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, 0.3, 6, norm=False, apply_scale=False)
+    assert_bf16(got, want, abs_tol=3e-2)
+
+
+@pytest.mark.parametrize("dtype,cuda_cores", [("bf16", True), ("fp32", False)])
+def test_gda_fwd_cuda_core_path(dtype, cuda_cores):
+    inp = make_gda_inputs(2, 150, 4, 2, 64, 128, seed=9,
+                          dtype=torch.float32 if dtype == "fp32" else torch.bfloat16)
+    li = 0.45
+    got = da.diffattn_gda_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.lam.to(DEV), 4, li,
+                              cuda_cores=cuda_cores)
+    want = ref.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, li, 4)
+    (assert_fp32 if dtype == "fp32" else assert_bf16)(got, want)
+
+
+def test_gda_fwd_single_pass():
+    inp = make_gda_inputs(1, 300, 4, 2, 128, 256, seed=13)
+    lam = torch.full((4,), 0.5, dtype=torch.float32)
+    got = da.diffattn_gda_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), lam.to(DEV), 4, 0.6,
+                              single_pass=True)
+    want = ref.diffattn_gda_fwd(inp.q, inp.k, inp.v, lam, 0.6, 4)
+    assert_bf16(got, want)
+
+
+def test_gda_fwd_is_ungrouped_kernel_on_repeated_noise_heads():
+    """The grouped instantiation does the same arithmetic as the ungrouped one on a [Q1|Q2]
+    layout whose Q2/K2 repeat each noise head over its group: the outputs are bit-identical."""
+    B, N, Hs, Hn, d = 2, 260, 6, 2, 128
+    inp = make_gda_inputs(B, N, Hs, Hn, d, 2 * d, seed=17, device=DEV)
+    rep = torch.arange(Hs, Hs + Hn, device=DEV).repeat_interleave(Hs // Hn)
+    q1 = torch.cat([inp.q[:, :, :Hs], inp.q[:, :, rep]], dim=-1).contiguous()
+    k1 = torch.cat([inp.k[:, :, :Hs], inp.k[:, :, rep]], dim=-1).contiguous()
+    a = da.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, Hs, 0.7)
+    b = da.diffattn_fwd(q1, k1, inp.v, inp.lam, 0.7)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_gda_fwd_guard_band():
+    """Nothing is written outside the output tensor."""
+    inp = make_gda_inputs(1, 150, 4, 2, 128, 256, seed=19)
+    n = 150 * 4 * 256
+    buf = torch.full((n + 2 * 4096,), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = buf[4096:4096 + n].view(1, 150, 4, 256)
+    da.diffattn_gda_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.lam.to(DEV), 4, 0.5,
+                        out=out)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:4096] == 7.0) and torch.all(buf[4096 + n:] == 7.0)
+
+
+# (B, L, Hs, Hn, ragged)
+GDA_DECODE_CASES = [(2, 1, 2, 2, False), (3, 700, 4, 1, True), (2, 5000, 12, 3, False),
+                    (4, 3001, 6, 2, True)]
+
+
+@pytest.mark.parametrize("B,L,Hs,Hn,ragged", GDA_DECODE_CASES)
+def test_gda_decode_small(B, L, Hs, Hn, ragged):
+    inp = make_gda_decode_inputs(B, L, Hs, Hn, 128, 256, seed=23 + L, ragged=ragged)
+    li = ref.lambda_init(inp.layer)
+    w = torch.linspace(0.8, 1.2, 256, dtype=torch.float32)
+    got = da.diffattn_gda_decode(inp.q.to(DEV), inp.k_cache.to(DEV), inp.v_cache.to(DEV),
+                                 inp.lam.to(DEV), Hs, li, seqlens=inp.seqlens.to(DEV),
+                                 norm_weight=w.to(DEV))
+    want = ref.diffattn_gda_decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, inp.lam, li, Hs,
+                                   norm_weight=w)
+    assert_bf16(got, want)
+    da.diffattn_device_status()
+
+
+def test_gda_decode_matches_prefill_last_row():
+    inp = make_gda_inputs(1, 384, 6, 2, 128, 256, seed=29, device=DEV)
+    pre = da.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, 6, 0.5)
+    dec = da.diffattn_gda_decode(inp.q[:, -1].contiguous(), inp.k, inp.v, inp.lam, 6, 0.5)
+    got = dec.float().cpu().numpy()
+    want = pre[:, -1].float().cpu().numpy()
+    assert np.max(np.abs(got - want)) < 4e-2
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) < 2e-2
+
+
+def _rows(N, n_first, n_rand, seed):
+    rng = np.random.default_rng(seed)
+    rand = rng.choice(np.arange(n_first, N - 1), size=n_rand, replace=False)
+    return np.unique(np.concatenate([np.arange(n_first), [N - 1], rand]))
+
+
+def test_gda_prefill_3b_full():
+    """B4 N4096, 12 signal heads over 3 noise heads, causal, RMSNorm + scale: sampled rows of
+    every signal head."""
+    B, N, Hs, Hn = 4, 4096, 12, 3
+    inp = make_gda_inputs(B, N, Hs, Hn, 128, 256, seed=5000, device=DEV)
+    li = ref.lambda_init(inp.layer)
+    out = da.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, Hs, li)
+    da.diffattn_device_status()
+    rows = _rows(N, 64, 128, 5000)
+    lam = inp.lam.cpu().numpy()
+    got, want = [], []
+    for b in range(B):
+        for h in range(Hs):
+            g = Hs + ref.gda_noise_head(h, Hs, Hn)
+            sel = [h, g]
+            q = inp.q[b:b + 1, :, sel].cpu()
+            k = inp.k[b:b + 1, :, sel].cpu()
+            v = inp.v[b:b + 1, :, h:h + 1].cpu()
+            want.append(ref.diffattn_gda_fwd(q, k, v, lam[h:h + 1], li, 1, rows=rows)[0, :, 0])
+            got.append(out[b, torch.as_tensor(rows, device=DEV), h].float().cpu().numpy())
+    assert_bf16(np.stack(got), np.stack(want))
+
+
+def test_gda_decode_32k_full():
+    """B64, cache 32768, 12 signal heads over 3 noise heads: every head of 4 sampled sequences."""
+    inp = make_gda_decode_inputs(64, 32768, 12, 3, 128, 256, seed=5100, device=DEV)
+    li = ref.lambda_init(inp.layer)
+    out = da.diffattn_gda_decode(inp.q, inp.k_cache, inp.v_cache, inp.lam, 12, li)
+    da.diffattn_device_status()
+    sample = [0, 21, 50, 63]
+    want = ref.diffattn_gda_decode(inp.q[sample].cpu(), inp.k_cache[sample].cpu(),
+                                   inp.v_cache[sample].cpu(), inp.seqlens[sample].cpu(),
+                                   inp.lam.cpu(), li, 12)
+    assert_bf16(out[sample], want)
+    del inp
+    torch.cuda.empty_cache()
