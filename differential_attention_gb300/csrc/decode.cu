@@ -15,9 +15,9 @@
 // workspace.
 // Stage 2 (decode_combine_kernel, grid H x B): thread c merges the partials of channel c, forms
 // o1/l1 - lambda * o2/l2, and applies the per-head RMSNorm and the (1 - lambda_init) scale.
-// Grouped form (kGrouped; H signal heads sharing H / G noise heads, q [B, H + H/G, 128], K cache
-// [B, L, H + H/G, 128], V cache [B, L, H, 256]): lanes 0-15 read signal head h's K1 row, lanes
-// 16-31 noise head H + h/G's K2 row; the rest is unchanged.
+// Grouped form (decode_group_kernel; H signal heads sharing H / G noise heads, q [B, H + H/G, 128],
+// K cache [B, L, H + H/G, 128], V cache [B, L, H, 256]): lanes 0-15 read signal head h's K1 row,
+// lanes 16-31 noise head H + h/G's K2 row; a CTA covers several heads of one noise group.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -84,6 +84,7 @@ struct DecSplitParams {
   int page_size, max_pages, num_pages;
   uint32_t ps_magic, ps_shift;  // j / page_size = (umulhi(j, magic) + j) >> shift, j < 2^31
   int group;                    // grouped form: signal heads per noise head
+  int hpc;                      // grouped form: signal heads per CTA (a divisor of group)
 };
 
 // Pool row of key j of sequence b in a paged cache [num_pages, page_size, heads, w]. A page id
@@ -112,30 +113,19 @@ __device__ __forceinline__ size_t cache_row(const DecSplitParams& p, int b, int 
     return static_cast<size_t>(b) * p.Lmax + j;
 }
 
-// kGrouped is an instantiation of its own, so that the V1 variants keep their code.
-template <bool kPaged, bool kGrouped = false>
+template <bool kPaged>
 __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecSplitParams p) {
-  // grouped: grid (splits x G, noise heads, B), the G signal heads that read one noise head's
-  // rows of a split launched side by side so that the repeats of those rows hit L2
-  const int s = kGrouped ? blockIdx.x / p.group : blockIdx.x;
-  const int h = kGrouped ? blockIdx.y * p.group + blockIdx.x % p.group : blockIdx.y;
-  const int b = blockIdx.z;
+  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int L = p.seqlens ? p.seqlens[b] : p.Lmax;
   L = L < 1 ? 1 : (L > p.Lmax ? p.Lmax : L);
   const int k0 = s * p.chunk;
   const int k1 = min(k0 + p.chunk, L);
 
-  // grouped: this lane's 8 q/k elements are column 8 (lane % 16) of head kh (q [B, heads, 128])
-  constexpr int kHalf = kDecWidth / 2;
-  const int heads = kGrouped ? p.H + p.H / p.group : p.H;
-  const int kh = kGrouped ? (lane < 16 ? h : p.H + h / p.group) : h;
   float qf[8];
   {
-    const __nv_bfloat16* qp =
-        kGrouped ? p.q + (static_cast<size_t>(b) * heads + kh) * kHalf + 8 * (lane & 15)
-                 : p.q + (static_cast<size_t>(b) * p.H + h) * kDecWidth + 8 * lane;
-    const uint4 qu = *reinterpret_cast<const uint4*>(qp);
+    const uint4 qu = *reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(b) * p.H + h) *
+                                                              kDecWidth + 8 * lane);
     bf16x8_to_f32(qu, qf);
 #pragma unroll
     for (int i = 0; i < 8; ++i) qf[i] *= p.scale_log2;
@@ -147,10 +137,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecSpli
   for (int i = 0; i < 8; ++i) o1[i] = o2[i] = 0.f;
 
   const size_t row_stride = static_cast<size_t>(p.H) * kDecWidth;  // elements between keys
-  const size_t k_stride = static_cast<size_t>(heads) * kHalf;       // grouped K rows
-  const __nv_bfloat16* kbase =
-      kGrouped ? p.kc + static_cast<size_t>(kh) * kHalf + 8 * (lane & 15)
-               : p.kc + static_cast<size_t>(h) * kDecWidth + 8 * lane;
+  const __nv_bfloat16* kbase = p.kc + static_cast<size_t>(h) * kDecWidth + 8 * lane;
   const __nv_bfloat16* vbase = p.vc + static_cast<size_t>(h) * kDecWidth + 8 * lane;
 
   for (int g0 = k0 + warp * kG; g0 < k1; g0 += kDecWarps * kG) {
@@ -158,15 +145,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecSpli
 #pragma unroll
     for (int e = 0; e < kG; ++e) {
       const int j = min(g0 + e, k1 - 1);  // clamp keeps the load in bounds; masked below
-      if constexpr (kGrouped) {
-        const size_t r = cache_row<kPaged>(p, b, j);
-        ku[e] = ldg_stream(kbase + r * k_stride);
-        vu[e] = ldg_stream(vbase + r * row_stride);
-      } else {
-        const size_t row = cache_row<kPaged>(p, b, j) * row_stride;
-        ku[e] = ldg_stream(kbase + row);
-        vu[e] = ldg_stream(vbase + row);
-      }
+      const size_t row = cache_row<kPaged>(p, b, j) * row_stride;
+      ku[e] = ldg_stream(kbase + row);
+      vu[e] = ldg_stream(vbase + row);
     }
     float sc[kG];
 #pragma unroll
@@ -269,6 +250,168 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecSpli
   }
 }
 
+// Grouped decode: one CTA per (split, block of `hpc` signal heads of one noise group, sequence),
+// kGroupWarps warps per head splitting the keys. Lanes 0-15 stream the head's K1 half row past L1;
+// lanes 16-31 read the noise head's K2 half row through L1, where the block's other heads find it,
+// so a noise row enters the SM once per block instead of once per head. The math per warp is that
+// of decode_split_kernel; the partials go to the same records.
+constexpr int kGroupWarps = 2;
+
+__device__ __forceinline__ uint4 ldg_l1(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__global__ void __launch_bounds__(kDecThreads) decode_group_kernel(const DecSplitParams p) {
+  const int s = blockIdx.x, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = warp / kGroupWarps, wi = warp % kGroupWarps;
+  const int h = blockIdx.y * p.hpc + r;                    // this warp's signal head
+  const int heads = p.H + p.H / p.group;                   // heads of q and of the K cache
+  const int kh = lane < 16 ? h : p.H + h / p.group;        // K1 of h, or K2 of its noise head
+  constexpr int kHalf = kDecWidth / 2;
+  int L = p.seqlens ? p.seqlens[b] : p.Lmax;
+  L = L < 1 ? 1 : (L > p.Lmax ? p.Lmax : L);
+  const int k0 = s * p.chunk;
+  const int k1 = min(k0 + p.chunk, L);
+
+  float qf[8];
+  {
+    const uint4 qu = *reinterpret_cast<const uint4*>(
+        p.q + (static_cast<size_t>(b) * heads + kh) * kHalf + 8 * (lane & 15));
+    bf16x8_to_f32(qu, qf);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qf[i] *= p.scale_log2;
+  }
+
+  float m1 = -INFINITY, l1 = 0.f, m2 = -INFINITY, l2 = 0.f;
+  float o1[8], o2[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o1[i] = o2[i] = 0.f;
+
+  const size_t k_stride = static_cast<size_t>(heads) * kHalf;   // elements between keys
+  const size_t v_stride = static_cast<size_t>(p.H) * kDecWidth;
+  const __nv_bfloat16* kbase = p.kc + static_cast<size_t>(b) * p.Lmax * k_stride +
+                               static_cast<size_t>(kh) * kHalf + 8 * (lane & 15);
+  const __nv_bfloat16* vbase = p.vc + static_cast<size_t>(b) * p.Lmax * v_stride +
+                               static_cast<size_t>(h) * kDecWidth + 8 * lane;
+  const bool noise_lane = lane >= 16;
+
+  for (int g0 = k0 + wi * kG; g0 < k1; g0 += kGroupWarps * kG) {
+    uint4 ku[kG], vu[kG];
+#pragma unroll
+    for (int e = 0; e < kG; ++e) {
+      const size_t j = static_cast<size_t>(min(g0 + e, k1 - 1));  // clamped in bounds; masked below
+      ku[e] = noise_lane ? ldg_l1(kbase + j * k_stride) : ldg_stream(kbase + j * k_stride);
+      vu[e] = ldg_stream(vbase + j * v_stride);
+    }
+    float sc[kG];
+#pragma unroll
+    for (int e = 0; e < kG; ++e) {
+      float kf[8];
+      bf16x8_to_f32(ku[e], kf);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = fmaf(qf[i], kf[i], acc);
+      sc[e] = acc;
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+      for (int e = 0; e < kG; ++e) sc[e] += __shfl_xor_sync(0xffffffffu, sc[e], o);
+    }
+    float s1[kG], s2[kG];
+#pragma unroll
+    for (int e = 0; e < kG; ++e) {
+      const float other = __shfl_xor_sync(0xffffffffu, sc[e], 16);
+      const bool valid = (g0 + e) < k1;
+      s1[e] = valid ? (lane < 16 ? sc[e] : other) : -INFINITY;
+      s2[e] = valid ? (lane < 16 ? other : sc[e]) : -INFINITY;
+    }
+    float gm1 = s1[0], gm2 = s2[0];
+#pragma unroll
+    for (int e = 1; e < kG; ++e) {
+      gm1 = fmaxf(gm1, s1[e]);
+      gm2 = fmaxf(gm2, s2[e]);
+    }
+    const float n1 = fmaxf(m1, gm1), n2 = fmaxf(m2, gm2);  // finite: key g0 is valid
+    const float c1 = ex2_approx(m1 - n1), c2 = ex2_approx(m2 - n2);
+    l1 *= c1;
+    l2 *= c2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      o1[i] *= c1;
+      o2[i] *= c2;
+    }
+#pragma unroll
+    for (int e = 0; e < kG; ++e) {
+      const float p1 = ex2_approx(s1[e] - n1), p2 = ex2_approx(s2[e] - n2);
+      l1 += p1;
+      l2 += p2;
+      float vf[8];
+      bf16x8_to_f32(vu[e], vf);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        o1[i] = fmaf(p1, vf[i], o1[i]);
+        o2[i] = fmaf(p2, vf[i], o2[i]);
+      }
+    }
+    m1 = n1;
+    m2 = n2;
+  }
+
+  // merge each head's warps
+  __shared__ float s_o[kDecWarps][2][kDecWidth];
+  __shared__ float s_ml[kDecWarps][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    s_o[warp][0][8 * lane + i] = o1[i];
+    s_o[warp][1][8 * lane + i] = o2[i];
+  }
+  if (lane == 0) {
+    s_ml[warp][0] = m1;
+    s_ml[warp][1] = l1;
+    s_ml[warp][2] = m2;
+    s_ml[warp][3] = l2;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < p.hpc * kDecWidth; idx += blockDim.x) {
+    const int rr = idx / kDecWidth, c = idx % kDecWidth;
+    const int w0 = rr * kGroupWarps;
+    float* rec = p.ws + ((static_cast<size_t>(b) * p.H + blockIdx.y * p.hpc + rr) * p.splits + s) * kRec;
+    float M[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int w = 0; w < kGroupWarps; ++w) {
+      M[0] = fmaxf(M[0], s_ml[w0 + w][0]);
+      M[1] = fmaxf(M[1], s_ml[w0 + w][2]);
+    }
+    float oa[2] = {0.f, 0.f}, la[2] = {0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kGroupWarps; ++w) {
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const float mw = s_ml[w0 + w][2 * m];
+        if (mw != -INFINITY) {
+          const float f = ex2_approx(mw - M[m]);
+          la[m] = fmaf(s_ml[w0 + w][2 * m + 1], f, la[m]);
+          oa[m] = fmaf(s_o[w0 + w][m][c], f, oa[m]);
+        }
+      }
+    }
+    rec[4 + c] = oa[0];
+    rec[4 + kDecWidth + c] = oa[1];
+    if (c == 0) {
+      rec[0] = M[0];
+      rec[1] = la[0];
+      rec[2] = M[1];
+      rec[3] = la[1];
+    }
+  }
+}
+
 struct DecCombineParams {
   const float* ws;
   const float* lambda;
@@ -348,11 +491,15 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   sp.ps_magic = sp.ps_shift = 0;
   if (a.block_table) page_magic(a.page_size, &sp.ps_magic, &sp.ps_shift);
   sp.group = a.noise_group;
-  if (a.noise_group && a.block_table) return cudaErrorNotSupported;  // no paged grouped cache
-  if (a.noise_group)
-    decode_split_kernel<false, true>
-        <<<dim3(S * a.noise_group, a.H / a.noise_group, a.B), kDecThreads, 0, st>>>(sp);
-  else if (a.block_table)
+  sp.hpc = 1;
+  if (a.noise_group) {
+    if (a.block_table) return cudaErrorNotSupported;  // no paged grouped cache
+    // signal heads per CTA: the largest divisor of the group that fits the CTA's warps
+    const int max_hpc = kDecWarps / kGroupWarps;
+    for (int d = 1; d <= max_hpc; ++d)
+      if (a.noise_group % d == 0) sp.hpc = d;
+    decode_group_kernel<<<dim3(S, a.H / sp.hpc, a.B), kGroupWarps * 32 * sp.hpc, 0, st>>>(sp);
+  } else if (a.block_table)
     decode_split_kernel<true><<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
   else
     decode_split_kernel<false><<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
