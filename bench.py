@@ -979,6 +979,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         da.diffattn_device_status()
         gdms = statistics.mean(a.elapsed_time(b) for a, b in gd_ev)
         gdbytes = gda_decode_bytes(gd)
+        dsha_g = source_sha(["decode.cu", "ptx.cuh"])
         gdgbs = gdbytes / (gdms * 1e-3) / 1e9
         line["gda_decode"] = {
             "metric": "decode HBM GB/s", "value": world * gdgbs, "unit": "GB/s", "ms_per_call": gdms,
@@ -986,9 +987,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                         "signal heads over 3 noise heads, d128, dv256, bf16 (cache 20.9 GB at B64)",
             "roofline": {"bound": "hbm", "achieved": gdgbs, "peak": hbm, "unit": "GB/s",
                          "frac": gdgbs / hbm, "bytes_per_launch": gdbytes,
+                         "traffic": profiled_traffic("gda_decode_32k.md", dsha_g),
                          "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
-                         "timed": "diffattn_gda_decode call (split kernel + combine kernel); a "
-                                  "noise head's K rows serve its 4 signal heads, repeats from L2"},
+                         "timed": "diffattn_gda_decode call (group kernel + combine kernel); a "
+                                  "noise row serves the 4 signal heads of its group from L1"},
             "gpu_launches": 2 * gdsteps}
         del gdi, gws, gdout
         torch.cuda.empty_cache()
