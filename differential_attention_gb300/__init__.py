@@ -124,6 +124,9 @@ _SIGNATURES = {
                                + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_v2_decode_paged": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 9
                                  + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_v2_decode_fp8_paged": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_float] * 2
+                                     + [ctypes.c_int] * 8
+                                     + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_gda_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_float, ctypes.c_void_p,
                                                                  ctypes.c_float] + [ctypes.c_int] * 8
                          + [ctypes.c_void_p]),
@@ -1008,4 +1011,41 @@ def diffattn_gda_decode(q, k_cache, v_cache, lam, n_signal: int, lambda_init: fl
                                      float(eps), B, Lmax, int(n_signal), n_noise, d, dv, flags,
                                      DIFFATTN_BF16, _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def diffattn_v2_decode_fp8_paged(q8, k_pool8, v_pool, block_table, seqlens, lam_logit,
+                                 q_descale: float, k_descale: float, workspace=None, out=None,
+                                 stream=None):
+    """DIFF V2 decode with fp8 e4m3 q [B, Hq, d] and K pool [num_pages, page_size, Hkv, d] (real
+    values q8 * q_descale, k8 * k_descale), a bf16 V pool, block_table [B, max_pages] and seqlens
+    [B] int32; page_size a multiple of 128."""
+    _dev("q8", q8, torch.float8_e4m3fn)
+    B, Hq, d = q8.shape
+    _dev("k_pool8", k_pool8, torch.float8_e4m3fn)
+    _dev("v_pool", v_pool, torch.bfloat16)
+    num_pages, page_size, Hkv = k_pool8.shape[0], k_pool8.shape[1], k_pool8.shape[2]
+    if k_pool8.shape != (num_pages, page_size, Hkv, d) or v_pool.shape != k_pool8.shape:
+        raise ValueError("pools must both be [num_pages, page_size, Hkv, d]")
+    _dev("block_table", block_table, torch.int32)
+    _dev("seqlens", seqlens, torch.int32)
+    if block_table.dim() != 2 or block_table.shape[0] != B or seqlens.shape != (B,):
+        raise ValueError("block_table must be [B, max_pages] and seqlens [B]")
+    max_pages = block_table.shape[1]
+    _dev("lam_logit", lam_logit, torch.float32)
+    if lam_logit.shape != (B, Hq // 2):
+        raise ValueError("lam_logit must be [B, Hq/2]")
+    if workspace is None:
+        workspace = torch.empty(diffattn_v2_decode_workspace_size(B, max_pages * page_size, Hq,
+                                                                  Hkv, d),
+                                dtype=torch.uint8, device=q8.device)
+    _dev("workspace", workspace)
+    if out is None:
+        out = torch.empty((B, Hq // 2, d), dtype=torch.bfloat16, device=q8.device)
+    _dev("out", out, torch.bfloat16)
+    _check(lib().diffattn_v2_decode_fp8_paged(
+        _ptr(q8), _ptr(k_pool8), _ptr(v_pool), _ptr(block_table), _ptr(seqlens), _ptr(lam_logit),
+        _ptr(out), float(q_descale), float(k_descale), B, Hq, Hkv, d, num_pages, page_size,
+        max_pages, 0, _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
     return out

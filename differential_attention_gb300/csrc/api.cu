@@ -526,6 +526,63 @@ DIFFATTN_API int diffattn_v2_decode_fp8(const void* q8, const void* k_cache8, co
   return ok();
 }
 
+DIFFATTN_API int diffattn_v2_decode_fp8_paged(const void* q8, const void* k_pool8,
+                                              const void* v_pool, const int* block_table,
+                                              const int* seqlens, const float* lam_logit,
+                                              void* out, float q_descale, float k_descale, int B,
+                                              int Hq, int Hkv, int d, int num_pages, int page_size,
+                                              int max_pages, int flags, void* workspace,
+                                              size_t ws_bytes, void* stream) {
+  const char* fn = "diffattn_v2_decode_fp8_paged";
+  if (!q8 || !k_pool8 || !v_pool || !block_table || !seqlens || !lam_logit || !out)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (flags & ~DIFFATTN_CAUSAL) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if (!(q_descale > 0.f) || !(k_descale > 0.f) || !std::isfinite(q_descale * k_descale))
+    return fail(DIFFATTN_ERR_ARG, "%s: descales must be finite and > 0", fn);
+  if (num_pages < 1 || page_size < 1 || max_pages < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need num_pages, page_size, max_pages >= 1", fn);
+  if (page_size % 128 != 0)
+    return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: fp8 pages must hold a multiple of 128 tokens (got %d)", fn, page_size);
+  const long long lmax = static_cast<long long>(max_pages) * page_size;
+  if (lmax > (1LL << 30) || static_cast<long long>(num_pages) * page_size > 0x7fffffffLL)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need max_pages * page_size <= 2^30 and num_pages * page_size < 2^31", fn);
+  const int Lmax = static_cast<int>(lmax);
+  int rc = check_v2_decode_shape(fn, B, Lmax, Hq, Hkv, d);
+  if (rc) return rc;
+  if (!aligned(q8, 16) || !aligned(k_pool8, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(lam_logit, 4) || !aligned(seqlens, 4) || !aligned(block_table, 4))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  const size_t need = da::v2_decode_workspace_bytes(B, Lmax, Hq, Hkv);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(DIFFATTN_ERR_WORKSPACE, "%s: need a 256-byte aligned workspace of %zu bytes", fn, need);
+  rc = check_device();
+  if (rc) return rc;
+  da::V2DecodeArgs a{};
+  a.q = q8;
+  a.k_cache = k_pool8;
+  a.v_cache = v_pool;
+  a.seqlens = seqlens;
+  a.lam_logit = lam_logit;
+  a.out = out;
+  a.B = B;
+  a.Lmax = Lmax;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.ws = static_cast<float*>(workspace);
+  a.block_table = block_table;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.k8 = true;
+  a.qk_descale = q_descale * k_descale;
+  char err[256] = {0};
+  cudaError_t e = da::launch_v2_decode_tc(a, static_cast<cudaStream_t>(stream), err, sizeof(err));
+  if (e == cudaErrorNotSupported) return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: unsupported shape", fn);
+  if (e == cudaErrorInvalidValue && err[0]) return fail(DIFFATTN_ERR_CUDA, "%s: %s", fn, err);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
 namespace {
 int check_train_shape(const char* fn, int B, int N, int H, int d, int dv, int dtype) {
   if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);

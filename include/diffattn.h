@@ -278,6 +278,25 @@ DIFFATTN_API int diffattn_v2_decode_fp8(const void* q8, const void* k_cache8, co
                                         int Hkv, int d, int flags, void* workspace,
                                         size_t ws_bytes, void* stream);
 
+/* DIFF V2 decode with fp8 e4m3 q and K over a paged cache: the result of diffattn_v2_decode_fp8
+ * where key j of sequence b sits at row j % page_size of page block_table[b * max_pages +
+ * j / page_size], as in diffattn_v2_decode_paged.
+ *   q8 : device e4m3 [B, Hq, d];  k_pool8 : device e4m3 [num_pages, page_size, Hkv, d];
+ *   v_pool : device bf16 [num_pages, page_size, Hkv, d]
+ *   block_table, seqlens (required), workspace : as for diffattn_v2_decode_paged
+ *   q_descale, k_descale, lam_logit, out, flags : as for diffattn_v2_decode_fp8
+ * Supported: page_size a multiple of 128 (each 128-key tile is one TMA box of a page; other page
+ * sizes: ERR_UNSUPPORTED). A used block-table entry outside [0, num_pages) reads page 0 and makes
+ * the next diffattn_device_status() report DIFFATTN_ERR_INDEX.
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA. */
+DIFFATTN_API int diffattn_v2_decode_fp8_paged(const void* q8, const void* k_pool8,
+                                              const void* v_pool, const int* block_table,
+                                              const int* seqlens, const float* lam_logit,
+                                              void* out, float q_descale, float k_descale, int B,
+                                              int Hq, int Hkv, int d, int num_pages, int page_size,
+                                              int max_pages, int flags, void* workspace,
+                                              size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------------------------
  * DIFF V2 decode over a paged KV cache: the result of diffattn_v2_decode where key j of
  * sequence b sits at row j % page_size of page block_table[b * max_pages + j / page_size].

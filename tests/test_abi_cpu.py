@@ -343,3 +343,21 @@ def test_gda_validation(L):
     assert dec(d=64, dv=128) == -2
     assert dec(ws_bytes=need - 1) == -8
     assert dec(ws=ctypes.c_void_p(0x10010)) == -8
+
+
+def test_v2_decode_fp8_paged_validation(L):
+    n = ctypes.c_size_t(0)
+    assert L.diffattn_v2_decode_workspace_size(4, 4096, 16, 2, 128, ctypes.byref(n)) == 0
+    need = n.value
+
+    def dec(ps=128, mp=32, qd=1.0, flags=0, d=128, table=FAKE, ws_bytes=need):
+        return L.diffattn_v2_decode_fp8_paged(FAKE, FAKE, FAKE, table, FAKE, FAKE, FAKE, qd, 1.0,
+                                              4, 16, 2, d, 200, ps, mp, flags, FAKE, ws_bytes, None)
+
+    assert dec(table=None) == -1
+    assert dec(flags=16) == -1
+    assert dec(qd=0.0) == -1
+    assert dec(ps=64, mp=64) == -7          # fp8 pages must be whole 128-key tiles
+    assert "multiple of 128" in L.diffattn_last_error_string().decode()
+    assert dec(d=64) == -2
+    assert dec(ws_bytes=need - 1) == -8

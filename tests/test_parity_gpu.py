@@ -580,6 +580,28 @@ def test_v2_decode_fp8(B, L, Hq, Hkv, ragged):
     da.diffattn_device_status()
 
 
+@pytest.mark.parametrize("ps", [128, 256])
+def test_v2_decode_fp8_paged(ps):
+    """fp8 q and K over a shuffled page pool with spare pages: against the oracle on the
+    dequantized values, and bit-equal to the contiguous fp8 decode of the same cache."""
+    B, L, Hq, Hkv = 3, 768, 16, 2
+    inp = make_v2_decode_inputs(B, L, Hq, Hkv, 128, seed=271 + ps, ragged=True)
+    q8, qs = to_fp8_e4m3(inp.q)
+    k8, ks = to_fp8_e4m3(inp.k_cache)
+    # page the fp8 bytes (viewed as uint8) with the bf16 V cache, then view them back
+    kp, vp, table = page_cache(k8.view(torch.uint8), inp.v_cache, ps, seed=281 + ps, spare_pages=2)
+    kp8 = kp.view(torch.float8_e4m3fn)
+    got = da.diffattn_v2_decode_fp8_paged(q8.to(DEV), kp8.to(DEV), vp.to(DEV), table.to(DEV),
+                                          inp.seqlens.to(DEV), inp.lam_logit.to(DEV), qs, ks)
+    want = ref.diffattn_v2_decode_paged(q8.float() * qs, kp8.float() * ks, vp, table, inp.seqlens,
+                                        inp.lam_logit)
+    assert_bf16(got, want)
+    flat = da.diffattn_v2_decode_fp8(q8.to(DEV), k8.to(DEV), inp.v_cache.to(DEV),
+                                     inp.lam_logit.to(DEV), qs, ks, seqlens=inp.seqlens.to(DEV))
+    assert torch.equal(got, flat)
+    da.diffattn_device_status()
+
+
 def test_v2_decode_ignores_cache_past_seqlen():
     """Cache rows past seqlens[b] may hold anything (here NaN and Inf): the result must not see them."""
     inp = make_v2_decode_inputs(3, 520, 16, 2, 128, seed=131)
