@@ -28,6 +28,7 @@ DIFFATTN_NORM = 2
 DIFFATTN_SCALE = 4
 DIFFATTN_CUDA_CORES = 8
 DIFFATTN_SINGLE_PASS = 16
+DIFFATTN_EXACT = 32
 
 STATUS_NAMES = {0: "OK", -1: "ERR_ARG", -2: "ERR_SHAPE", -3: "ERR_DTYPE", -4: "ERR_ALIGN",
                 -5: "ERR_CUDA", -6: "ERR_TIMEOUT", -7: "ERR_UNSUPPORTED", -8: "ERR_WORKSPACE",
@@ -341,8 +342,12 @@ def diffattn_decode_noalloc(q, k_cache, v_cache, lam, lambda_init: float = 0.0, 
 
 
 def diffattn_v2_fwd(q, k, v, lam_logit, causal: bool = True, cuda_cores: bool = False,
-                    single_pass: bool = False, out=None, stream=None):
-    """DIFF V2 pair prefill: attn[2p] - sigmoid(lam_logit) * attn[2p+1] over shared GQA KV."""
+                    single_pass: bool = False, exact: bool = False, out=None, stream=None):
+    """DIFF V2 pair prefill: attn[2p] - sigmoid(lam_logit) * attn[2p+1] over shared GQA KV.
+
+    By default one flash pass per head (both heads of a pair in one CTA); `exact` takes the
+    two-pass kernel that rounds the difference of the maps once; `cuda_cores` the CUDA-core path.
+    `single_pass` names the default."""
     _dev("q", q)
     B, N, Hq, d = q.shape
     _dev("k", k, q.dtype)
@@ -357,7 +362,7 @@ def diffattn_v2_fwd(q, k, v, lam_logit, causal: bool = True, cuda_cores: bool = 
         out = torch.empty((B, N, Hq // 2, d), dtype=q.dtype, device=q.device)
     _dev("out", out, q.dtype)
     flags = ((DIFFATTN_CAUSAL if causal else 0) | (DIFFATTN_CUDA_CORES if cuda_cores else 0)
-             | (DIFFATTN_SINGLE_PASS if single_pass else 0))
+             | (DIFFATTN_SINGLE_PASS if single_pass else 0) | (DIFFATTN_EXACT if exact else 0))
     _check(lib().diffattn_v2_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_logit), _ptr(out), B, N, Hq,
                                  Hkv, d, flags, _code(q.dtype), _stream(stream)))
     return out

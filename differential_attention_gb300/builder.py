@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdiffattn.so")
-SOURCES = ["api.cu", "simt.cu", "decode.cu", "decode_v2_tc.cu", "backward.cu", "host_pipeline.cu", "tmap.cu", "prefill_tc.cu", "prefill_exact.cu"]
+SOURCES = ["api.cu", "simt.cu", "decode.cu", "decode_v2_tc.cu", "backward.cu", "host_pipeline.cu", "tmap.cu", "prefill_tc.cu", "prefill_exact.cu", "prefill_v2.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -69,6 +69,9 @@ DIFFATTN_API int diffattn_device_status(void* stream) {
   int v = 0, w = 0, x = 0, y = 0, z = 0;
   e = da::status_prefill_tc(&v);
   if (e == cudaSuccess) e = da::status_prefill_exact(&w);
+  int pv = 0;
+  if (e == cudaSuccess) e = da::status_prefill_v2(&pv);
+  w |= pv;
   if (e == cudaSuccess) e = da::status_simt(&x);
   if (e == cudaSuccess) e = da::status_v2_decode_tc(&y);
   if (e == cudaSuccess) e = da::status_backward(&z);
@@ -319,8 +322,11 @@ DIFFATTN_API int diffattn_v2_fwd(const void* q, const void* k, const void* v,
                                  const float* lam_logit, void* out, int B, int N, int Hq, int Hkv,
                                  int d, int flags, int dtype, void* stream) {
   if (!q || !k || !v || !lam_logit || !out) return fail(DIFFATTN_ERR_ARG, "diffattn_v2_fwd: null pointer");
-  constexpr int kV2Flags = DIFFATTN_CAUSAL | DIFFATTN_CUDA_CORES | DIFFATTN_SINGLE_PASS;
+  constexpr int kV2Flags =
+      DIFFATTN_CAUSAL | DIFFATTN_CUDA_CORES | DIFFATTN_SINGLE_PASS | DIFFATTN_EXACT;
   if (flags & ~kV2Flags) return fail(DIFFATTN_ERR_ARG, "diffattn_v2_fwd: unknown flag bits 0x%x", flags);
+  if ((flags & DIFFATTN_EXACT) && (flags & (DIFFATTN_CUDA_CORES | DIFFATTN_SINGLE_PASS)))
+    return fail(DIFFATTN_ERR_ARG, "diffattn_v2_fwd: DIFFATTN_EXACT excludes the other path flags");
   if (dtype != DIFFATTN_BF16 && dtype != DIFFATTN_FP32)
     return fail(DIFFATTN_ERR_DTYPE, "diffattn_v2_fwd: dtype must be DIFFATTN_BF16 or DIFFATTN_FP32");
   if (B < 1 || N < 1 || Hq < 2 || Hkv < 1)
@@ -359,8 +365,17 @@ DIFFATTN_API int diffattn_v2_fwd(const void* q, const void* k, const void* v,
   p.norm_w = nullptr;
   p.eps = 0.f;
   p.lambda_init = 0.f;
-  p.flags = flags & kV2Flags;
   p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  if (dtype == DIFFATTN_BF16 && !(flags & (DIFFATTN_CUDA_CORES | DIFFATTN_EXACT))) {
+    // one flash pass per head, both heads of a pair in one CTA
+    p.flags = flags & DIFFATTN_CAUSAL;
+    char err[256] = {0};
+    cudaError_t e = da::launch_prefill_v2(p, static_cast<cudaStream_t>(stream), err, sizeof(err));
+    if (err[0]) return fail(DIFFATTN_ERR_CUDA, "diffattn_v2_fwd: %s", err);
+    if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_fwd");
+    return ok();
+  }
+  p.flags = flags & (DIFFATTN_CAUSAL | DIFFATTN_CUDA_CORES);
   return run_prefill(p, dtype, "diffattn_v2_fwd", static_cast<cudaStream_t>(stream));
 }
 

@@ -164,6 +164,9 @@ cudaError_t launch_lambda_bwd(const float* lq1, const float* lk1, const float* l
 cudaError_t launch_prefill_simt(const Problem& p, bool is_bf16, cudaStream_t s);
 // Tensor-core prefill (bf16). Returns cudaErrorNotSupported for shapes it does not cover.
 cudaError_t launch_prefill_tc(const Problem& p, cudaStream_t s, char* err, size_t err_len);
+// DIFF V2 pair prefill, one flash pass per head, both heads of a pair in one CTA (dense bf16).
+cudaError_t launch_prefill_v2(const Problem& p, cudaStream_t s, char* err, size_t err_len);
+cudaError_t status_prefill_v2(int* v);
 
 struct DecodeArgs {
   const void* q;

@@ -62,7 +62,12 @@ typedef enum { DIFFATTN_BF16 = 0, DIFFATTN_FP32 = 1 } diffattn_dtype;
    map's probabilities rounded to bf16 before the product with V (the numerics of running a flash
    kernel once per map and subtracting). Fewer exponentials, but when the two maps are close its
    error relative to the output grows like 2^-9 / |1 - lambda|. The default tensor-core path finds
-   each map's exact row statistics first and rounds A1 - lambda A2 once, after the subtraction. */
+   each map's exact row statistics first and rounds A1 - lambda A2 once, after the subtraction.
+   For diffattn_v2_fwd, one pass per head is the default (see there). */
+#define DIFFATTN_EXACT 32 /* diffattn_v2_fwd only: find each head's exact row statistics first and
+   round attn[2p] - sigmoid(lam) * attn[2p+1] once, after the subtraction (the V1 default path),
+   instead of one flash pass per head. Also the numerics of diffattn_v2_fwd_varlen and
+   diffattn_v2_fwd_paged, which always take that path. */
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 DIFFATTN_API int diffattn_version(void);
@@ -205,7 +210,11 @@ DIFFATTN_API int diffattn_decode_noalloc(const void* q, const void* k_cache, con
  *               reads KV head floor(2p / (Hq / Hkv))
  *   lam_logit : device fp32 [B, N, Hq/2], the value before the sigmoid
  *   out       : device [B, N, Hq/2, d]
- *   flags     : DIFFATTN_CAUSAL or 0, optionally DIFFATTN_CUDA_CORES or DIFFATTN_SINGLE_PASS
+ *   flags     : DIFFATTN_CAUSAL or 0, optionally one of DIFFATTN_CUDA_CORES, DIFFATTN_EXACT
+ * Numerics: by default each head of a pair is one flash pass on the tensor cores, as the pages run
+ * it (two stock attention calls): its probabilities are rounded to bf16 before the product with V,
+ * the two normalised head outputs are subtracted in fp32. DIFFATTN_EXACT takes the two-pass kernel
+ * that rounds the difference of the maps once instead; DIFFATTN_SINGLE_PASS is the default here.
  * Supported: dtype DIFFATTN_BF16, d in {64, 128}, Hq even, Hq % Hkv == 0 and (Hq / Hkv) even (the
  * two heads of a pair must sit in one GQA group). The scale is 1/sqrt(d).
  * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_CUDA.

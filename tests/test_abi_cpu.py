@@ -104,6 +104,9 @@ def test_v2_validation(L):
 
     assert v2(q=None) == -1
     assert v2(flags=2) == -1
+    assert v2(flags=1 | 32 | 16) == -1  # DIFFATTN_EXACT with DIFFATTN_SINGLE_PASS
+    assert v2(flags=1 | 32 | 8) == -1   # DIFFATTN_EXACT with DIFFATTN_CUDA_CORES
+    assert v2(flags=64) == -1
     assert v2(Hq=63) == -2
     assert v2(Hq=64, Hkv=64) == -2   # Hq/Hkv = 1: a pair would straddle two GQA groups
     assert v2(Hq=48, Hkv=16) == -2   # Hq/Hkv = 3

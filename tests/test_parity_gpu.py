@@ -396,7 +396,7 @@ def test_v2_fwd_varlen(lens_q, lens_k, causal):
         a, b = int(cu_q[2]), int(cu_q[3])
         one = da.diffattn_v2_fwd(q[None, a:b].contiguous().to(DEV), k[None, a:b].contiguous().to(DEV),
                                  v[None, a:b].contiguous().to(DEV), lam[None, a:b].contiguous().to(DEV),
-                                 causal=causal)
+                                 causal=causal, exact=True)
         assert torch.equal(got[a:b], one[0])
     da.diffattn_device_status()
 
@@ -493,14 +493,49 @@ def test_decode_paged_bad_page_is_reported():
 # ------------------------------------------------------------------------------------------
 # V2
 # ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("exact", [False, True])
 @pytest.mark.parametrize("B,N,Hq,Hkv,d,causal", [(2, 300, 8, 2, 128, True), (1, 129, 4, 2, 128, False),
-                                                 (1, 200, 8, 4, 64, True), (1, 1, 2, 1, 128, True)])
-def test_v2_small(B, N, Hq, Hkv, d, causal):
+                                                 (1, 200, 8, 4, 64, True), (1, 1, 2, 1, 128, True),
+                                                 (3, 1000, 16, 2, 128, True), (1, 257, 4, 1, 64, False),
+                                                 (2, 640, 12, 2, 128, False)])
+def test_v2_small(B, N, Hq, Hkv, d, causal, exact):
+    """Both V2 prefill kernels against the oracle: one flash pass per head (the default, both
+    heads of a pair in one CTA) and the exact two-pass kernel; several key tiles, ragged tails,
+    one token, groups of 2, 4 and 8 query heads per KV head."""
     inp = make_v2_inputs(B, N, Hq, Hkv, d, seed=81 + N, causal=causal)
     got = da.diffattn_v2_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.lam_logit.to(DEV),
-                             causal=causal)
+                             causal=causal, exact=exact)
     want = ref.diffattn_v2_fwd(inp.q, inp.k, inp.v, inp.lam_logit, causal=causal)
     assert_bf16(got, want)
+    da.diffattn_device_status()
+
+
+def test_v2_identical_heads_give_one_minus_sigma_attention():
+    """q[2p] = q[2p+1]: the two heads of a pair compute the same map with the same arithmetic, so
+    the default kernel's output is (1 - sigmoid(lam)) times one head's attention, as the oracle's
+    pin states; the rounding of each map's probabilities cancels in the difference."""
+    inp = make_v2_inputs(2, 700, 8, 2, 128, seed=97)
+    q = inp.q.clone()
+    q[:, :, 1::2] = q[:, :, 0::2]
+    lam = inp.lam_logit * 3.0  # sigmoid up to ~1: the difference is far smaller than each head
+    got = da.diffattn_v2_fwd(q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), lam.to(DEV))
+    want = ref.diffattn_v2_fwd(q, inp.k, inp.v, lam)
+    assert_bf16(got, want)
+
+
+def test_v2_large_scores_rescale():
+    """Scores spread over tens of nats (q, k scaled up), so the running maximum grows by more than
+    2^8 inside a row and the default kernel rescales its output accumulators in tensor memory."""
+    inp = make_v2_inputs(1, 900, 8, 2, 128, seed=99)
+    # score std ~1.1 nats at key 0, growing linearly to ~11 nats at key 899: the maximum of a
+    # later key tile exceeds that of the earlier ones by far more than 2^8
+    grow = 1.0 + torch.arange(900, dtype=torch.float32) / 100.0
+    q = (inp.q.float() * 12.0).to(torch.bfloat16)
+    k = (inp.k.float() * 12.0 * grow[None, :, None, None]).to(torch.bfloat16)
+    got = da.diffattn_v2_fwd(q.to(DEV), k.to(DEV), inp.v.to(DEV), inp.lam_logit.to(DEV))
+    want = ref.diffattn_v2_fwd(q, k, inp.v, inp.lam_logit)
+    assert_bf16(got, want)
+    da.diffattn_device_status()
 
 
 def test_v2_cuda_core_path():
