@@ -518,14 +518,29 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         barrier()
         da.diffattn_device_status()
         vms = statistics.mean(a.elapsed_time(b) for a, b in v_ev)
+        # the exact two-pass path (DIFFATTN_EXACT) on the same inputs, for context
+        x_ev = [(ev(), ev()) for _ in range(5)]
+        for a, b_ in x_ev:
+            a.record(stream)
+            da.diffattn_v2_fwd(vinp.q, vinp.k, vinp.v, vinp.lam_logit, out=vout, exact=True)
+            b_.record(stream)
+        barrier()
+        da.diffattn_device_status()
+        xms = statistics.mean(a.elapsed_time(b_) for a, b_ in x_ev)
         vflops = float(vc["B"] * (vc["Hq"] // 2) * causal_pairs(vc["N"]) * V2_FLOPS_PER_PAIR)
         vtf = vflops / (vms * 1e-3) / 1e12
         line["v2"] = {"metric": "V2 fwd TFLOP/s", "value": world * vtf, "unit": "TFLOP/s",
                       "ms_per_call": vms,
                       "workload": "v2_gqa: B2 N8192 Hq64 (32 pairs) Hkv8 d128 causal",
+                      "kernel": "v2_pair_kernel<128,2> (both heads of a pair in one CTA, one "
+                                "flash pass per head)",
+                      "exact_two_pass_ms": xms,
                       "roofline": {"bound": "tensor", "achieved": vtf, "peak": peak_tf,
                                    "unit": "TFLOP/s", "frac": vtf / peak_tf,
-                                   "flops_per_launch": vflops}}
+                                   "flops_per_launch": vflops,
+                                   "traffic": profiled_traffic(
+                                       "v2_pair_gqa.md",
+                                       source_sha(["prefill_v2.cu", "ptx.cuh"]))}}
         del vinp, vout
         torch.cuda.empty_cache()
 
