@@ -586,28 +586,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (P.flags & 4) scale *= (1.f - P.lambda_init);
     if (ok) {
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P.out) +
-                           oaddr + c0;
+      // The warp's 32 rows x HC columns go through shared memory (the load ring, idle once the
+      // last product is done), so that each store instruction writes whole 128-byte row pieces
+      // instead of 32 scattered 16-byte ones.
+      constexpr int RB = HC * 2;          // bytes of one row's slice
+      constexpr int PIECES = RB / 16;     // 16-byte pieces per slice (8 at dv 256, 4 at dv 128)
+      constexpr int RPI = 32 / PIECES;    // rows per store instruction
+      static_assert(kSoftmaxThreads * RB <= C::NSLOT * C::kSlot, "staging fits in the ring");
+      uint8_t* stage = smem + C::kSlotOff + (warp - kSoftmaxWarp0) * 32 * RB;
+      const bool live = row < SN;
       const float* w = (P.flags & 2) && P.norm_w ? P.norm_w + c0 : nullptr;
 #pragma unroll 1
       for (int c = 0; c < HC / CW; ++c) {
         uint32_t o[CW];
         ld_o(c, o);
-        if (row < SN) {
 #pragma unroll
-          for (int g = 0; g < CW / 8; ++g) {
-            uint4 pkt;
-            uint32_t* pw = reinterpret_cast<uint32_t*>(&pkt);
+        for (int g = 0; g < CW / 8; ++g) {
+          uint4 pkt;
+          uint32_t* pw = reinterpret_cast<uint32_t*>(&pkt);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int e = 8 * g + 2 * i;
-              const float w0 = w ? w[CW * c + e] : 1.f;
-              const float w1 = w ? w[CW * c + e + 1] : 1.f;
-              pw[i] = pack_bf16x2(__uint_as_float(o[e]) * scale * w0,
-                                  __uint_as_float(o[e + 1]) * scale * w1);
-            }
-            *reinterpret_cast<uint4*>(out + CW * c + 8 * g) = pkt;
+          for (int i = 0; i < 4; ++i) {
+            const int e = 8 * g + 2 * i;
+            const float w0 = w ? w[CW * c + e] : 1.f;
+            const float w1 = w ? w[CW * c + e + 1] : 1.f;
+            pw[i] = pack_bf16x2(__uint_as_float(o[e]) * scale * w0,
+                                __uint_as_float(o[e + 1]) * scale * w1);
           }
+          const int piece = (CW * c + 8 * g) / 8;
+          *reinterpret_cast<uint4*>(stage + lane * RB + ((piece ^ (lane & (PIECES - 1))) * 16)) = pkt;
+        }
+        if (live) {
           if (P.o_pre) {  // training: the head output before the norm and scale
             __nv_bfloat16* op = static_cast<__nv_bfloat16*>(P.o_pre) +
                                 (orow * P.units + u) * DV + c0;
@@ -623,6 +631,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      }
+      __syncwarp();
+      __nv_bfloat16* out0 = static_cast<__nv_bfloat16*>(P.out) + c0;
+#pragma unroll
+      for (int it = 0; it < PIECES; ++it) {
+        const int rr = it * RPI + lane / PIECES;   // row (lane of the warp) this lane stores
+        const int pc = lane % PIECES;
+        const size_t addr = __shfl_sync(0xffffffffu, static_cast<unsigned long long>(oaddr), rr);
+        const bool rlive = __shfl_sync(0xffffffffu, live ? 1 : 0, rr) != 0;
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * RB + ((pc ^ (rr & (PIECES - 1))) * 16));
+        if (rlive) *reinterpret_cast<uint4*>(out0 + addr + pc * 8) = v;
       }
       if (P.stats && wg == 0 && row < P.N) {
         float* st = P.stats + (static_cast<size_t>(b) * P.units + u) * 2 * P.n_pad + row;

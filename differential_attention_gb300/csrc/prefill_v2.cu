@@ -362,33 +362,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     // `ok` is uniform per warp; the row test is not, so the tensor-memory loads (warp-wide
     // .sync.aligned instructions) stay outside it and only the stores are predicated.
     if (ok) {
+      // The warp's 32 rows x D/2 columns go through shared memory (the K ring, idle once the
+      // last score product is done), so that each store instruction writes whole 128-byte row
+      // pieces instead of 32 scattered 16-byte ones.
       constexpr int H2 = D / 2;
+      constexpr int RB = H2 * 2;          // bytes of one row's slice
+      constexpr int PIECES = RB / 16;     // 16-byte pieces per slice
+      constexpr int RPI = 32 / PIECES;    // rows per store instruction
+      static_assert(256 * RB <= NS * C::kKBytes, "staging fits in the K ring");
       const int col0 = h * H2;
+      uint8_t* stage = smem + C::kKOff + (warp - kSoftmaxWarp0) * 32 * RB;
       const bool live = row < P.N;
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P.out) +
-                           ((static_cast<size_t>(b) * P.N + (live ? row : 0)) * P.units + u) * D +
-                           col0;
 #pragma unroll 1
       for (int c = 0; c < H2; c += 32) {
         uint32_t oa[32], ob[32];
         tmem_ld32(tmem + tl + C::kOCol + col0 + c, oa);
         tmem_ld32(tmem + tl + C::kOCol + D + col0 + c, ob);
         tmem_wait_ld();
-        if (live) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 pkt;
-            uint32_t* pw = reinterpret_cast<uint32_t*>(&pkt);
+        for (int q = 0; q < 4; ++q) {
+          uint4 pkt;
+          uint32_t* pw = reinterpret_cast<uint32_t*>(&pkt);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int e = 8 * q + 2 * i;
-              pw[i] = pack_bf16x2(__uint_as_float(oa[e]) * fa - __uint_as_float(ob[e]) * fb,
-                                  __uint_as_float(oa[e + 1]) * fa - __uint_as_float(ob[e + 1]) * fb);
-            }
-            *reinterpret_cast<uint4*>(out + c + 8 * q) = pkt;
+          for (int i = 0; i < 4; ++i) {
+            const int e = 8 * q + 2 * i;
+            pw[i] = pack_bf16x2(__uint_as_float(oa[e]) * fa - __uint_as_float(ob[e]) * fb,
+                                __uint_as_float(oa[e + 1]) * fa - __uint_as_float(ob[e + 1]) * fb);
           }
+          const int piece = (c + 8 * q) / 8;
+          *reinterpret_cast<uint4*>(stage + lane * RB + ((piece ^ (lane & (PIECES - 1))) * 16)) = pkt;
         }
-        __syncwarp();
+      }
+      __syncwarp();
+      const size_t orow0 = (static_cast<size_t>(b) * P.N + qt * BM + 32 * (warp & 3)) * P.units + u;
+      __nv_bfloat16* out0 = static_cast<__nv_bfloat16*>(P.out) + col0;
+#pragma unroll
+      for (int it = 0; it < PIECES; ++it) {
+        const int rr = it * RPI + lane / PIECES;   // row (lane of the warp) this lane stores
+        const int pc = lane % PIECES;
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * RB + ((pc ^ (rr & (PIECES - 1))) * 16));
+        if (qt * BM + 32 * (warp & 3) + rr < P.N)
+          *reinterpret_cast<uint4*>(out0 + (orow0 + static_cast<size_t>(rr) * P.units) * D + pc * 8) = v;
       }
     }
   }
