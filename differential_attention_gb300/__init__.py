@@ -750,9 +750,11 @@ def diffattn_fwd_varlen_qk(q, k, v, cu_seqlens_q, cu_seqlens_k, lam, lambda_init
 
 
 def diffattn_v2_fwd_varlen(q, k, v, lam_logit, cu_seqlens_q, cu_seqlens_k=None, max_seqlen_q=None,
-                           max_seqlen_k=None, causal: bool = True, out=None, stream=None):
+                           max_seqlen_k=None, causal: bool = True, exact: bool = False, out=None,
+                           stream=None):
     """DIFF V2 over packed sequences: q [total_q, Hq, d], k, v [total_k, Hkv, d], lam_logit
-    [total_q, Hq/2]; cu_seqlens_k None means the keys share the queries' offsets."""
+    [total_q, Hq/2]; cu_seqlens_k None means the keys share the queries' offsets. `exact` as for
+    diffattn_v2_fwd."""
     _dev("q", q, torch.bfloat16)
     total_q, Hq, d = q.shape
     _dev("k", k, torch.bfloat16)
@@ -782,7 +784,8 @@ def diffattn_v2_fwd_varlen(q, k, v, lam_logit, cu_seqlens_q, cu_seqlens_k=None, 
                                         _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
                                         max(1, int(max_seqlen_q)), max(1, int(max_seqlen_k)),
                                         total_q, total_k, B, Hq, Hkv, d,
-                                        DIFFATTN_CAUSAL if causal else 0, DIFFATTN_BF16,
+                                        (DIFFATTN_CAUSAL if causal else 0) | (DIFFATTN_EXACT if exact else 0),
+                                        DIFFATTN_BF16,
                                         _stream(stream)))
     return out
 
@@ -835,7 +838,8 @@ def diffattn_fwd_paged(q, k_pool, v_pool, cu_seqlens_q, seqlens_k, block_table, 
 
 
 def diffattn_v2_fwd_paged(q, k_pool, v_pool, lam_logit, cu_seqlens_q, seqlens_k, block_table,
-                          max_seqlen_q=None, max_seqlen_k=None, causal: bool = True, out=None,
+                          max_seqlen_q=None, max_seqlen_k=None, causal: bool = True,
+                          exact: bool = False, out=None,
                           stream=None):
     """DIFF V2 with packed queries q [total_q, Hq, d] against keys in a page pool: k_pool,
     v_pool [num_pages, page_size, Hkv, d]; lam_logit [total_q, Hq/2]."""
@@ -856,7 +860,8 @@ def diffattn_v2_fwd_paged(q, k_pool, v_pool, lam_logit, cu_seqlens_q, seqlens_k,
                                        _ptr(out), _ptr(cu_seqlens_q), _ptr(seqlens_k),
                                        _ptr(block_table), mq, mk, total_q, num_pages, page_size,
                                        block_table.shape[1], B, Hq, Hkv, d,
-                                       DIFFATTN_CAUSAL if causal else 0, DIFFATTN_BF16,
+                                       (DIFFATTN_CAUSAL if causal else 0) | (DIFFATTN_EXACT if exact else 0),
+                                       DIFFATTN_BF16,
                                        _stream(stream)))
     return out
 

@@ -163,6 +163,17 @@ static int run_prefill(da::Problem& p, int dtype, const char* name, cudaStream_t
   return ok();
 }
 
+// V2 pair prefill: one flash pass per head, both heads of a pair in one CTA
+static int run_v2_pair(da::Problem& p, const char* name, cudaStream_t s) {
+  char err[256] = {0};
+  cudaError_t e = da::launch_prefill_v2(p, s, err, sizeof(err));
+  if (e == cudaErrorNotSupported)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: no V2 pair kernel for d=%d", name, p.dqk);
+  if (err[0]) return fail(DIFFATTN_ERR_CUDA, "%s: %s", name, err);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return ok();
+}
+
 DIFFATTN_API int diffattn_fwd(const void* q, const void* k, const void* v, void* out,
                               const float* lambda, float lambda_init, const float* norm_weight,
                               float eps, int B, int N, int H, int d, int dv, int flags, int dtype,
@@ -367,13 +378,8 @@ DIFFATTN_API int diffattn_v2_fwd(const void* q, const void* k, const void* v,
   p.lambda_init = 0.f;
   p.scale = 1.0f / std::sqrt(static_cast<float>(d));
   if (dtype == DIFFATTN_BF16 && !(flags & (DIFFATTN_CUDA_CORES | DIFFATTN_EXACT))) {
-    // one flash pass per head, both heads of a pair in one CTA
     p.flags = flags & DIFFATTN_CAUSAL;
-    char err[256] = {0};
-    cudaError_t e = da::launch_prefill_v2(p, static_cast<cudaStream_t>(stream), err, sizeof(err));
-    if (err[0]) return fail(DIFFATTN_ERR_CUDA, "diffattn_v2_fwd: %s", err);
-    if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_fwd");
-    return ok();
+    return run_v2_pair(p, "diffattn_v2_fwd", static_cast<cudaStream_t>(stream));
   }
   p.flags = flags & (DIFFATTN_CAUSAL | DIFFATTN_CUDA_CORES);
   return run_prefill(p, dtype, "diffattn_v2_fwd", static_cast<cudaStream_t>(stream));
@@ -1027,7 +1033,8 @@ DIFFATTN_API int diffattn_v2_fwd_varlen(const void* q, const void* k, const void
   const char* fn = "diffattn_v2_fwd_varlen";
   if (!q || !k || !v || !lam_logit || !out || !cu_seqlens_q)
     return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
-  if (flags & ~DIFFATTN_CAUSAL) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if (flags & ~(DIFFATTN_CAUSAL | DIFFATTN_EXACT))
+    return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
   if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);
   if (!cu_seqlens_k) {  // the keys share the query offsets
     max_seqlen_k = max_seqlen_q;
@@ -1066,13 +1073,14 @@ DIFFATTN_API int diffattn_v2_fwd_varlen(const void* q, const void* k, const void
   p.k_cols = d;
   p.group = Hq / Hkv;
   p.lam_logit = lam_logit;
-  p.flags = flags;
+  p.flags = flags & DIFFATTN_CAUSAL;
   p.scale = 1.0f / std::sqrt(static_cast<float>(d));
   p.cu_seqlens = cu_seqlens_q;
   p.total = total_q;
   p.cu_seqlens_k = cu_seqlens_k;
   p.total_k = total_k;
   p.max_seqlen_k = max_seqlen_k;
+  if (!(flags & DIFFATTN_EXACT)) return run_v2_pair(p, fn, static_cast<cudaStream_t>(stream));
   return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
 }
 
@@ -1168,7 +1176,8 @@ DIFFATTN_API int diffattn_v2_fwd_paged(const void* q, const void* k_pool, const 
   const char* fn = "diffattn_v2_fwd_paged";
   if (!q || !k_pool || !v_pool || !lam_logit || !out || !cu_seqlens_q || !seqlens_k || !block_table)
     return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
-  if (flags & ~DIFFATTN_CAUSAL) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if (flags & ~(DIFFATTN_CAUSAL | DIFFATTN_EXACT))
+    return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
   if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);
   int rc = check_paged_prefill(fn, B, max_seqlen_q, max_seqlen_k, total_q, num_pages, page_size,
                                max_pages);
@@ -1203,7 +1212,7 @@ DIFFATTN_API int diffattn_v2_fwd_paged(const void* q, const void* k_pool, const 
   p.k_cols = d;
   p.group = Hq / Hkv;
   p.lam_logit = lam_logit;
-  p.flags = flags;
+  p.flags = flags & DIFFATTN_CAUSAL;
   p.scale = 1.0f / std::sqrt(static_cast<float>(d));
   p.cu_seqlens = cu_seqlens_q;
   p.total = total_q;
@@ -1213,6 +1222,7 @@ DIFFATTN_API int diffattn_v2_fwd_paged(const void* q, const void* k_pool, const 
   p.page_size = page_size;
   p.max_pages = max_pages;
   p.num_pages = num_pages;
+  if (!(flags & DIFFATTN_EXACT)) return run_v2_pair(p, fn, static_cast<cudaStream_t>(stream));
   return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
 }
 

@@ -81,7 +81,14 @@ struct KParams {
   float scale_log2;  // log2(e) / sqrt(D)
 };
 
-template <int D, int NS>
+// Where the queries and keys are (KMODE): batched [B, N] (kDense); packed along the token axis
+// with cu_seqlens, keys at the queries' rows (kPacked) or with offsets of their own
+// (kKeysOffset); or packed queries against keys in a page pool through a block table
+// (kKeysPaged; page size a multiple of 128, so a key tile lies in one page). A compile-time
+// choice, so that the batched kernel carries none of the packed form's live values.
+enum : int { kDense = 0, kPacked = 1, kKeysOffset = 2, kKeysPaged = 3 };
+
+template <int D, int NS, int KMODE>
 __global__ void __launch_bounds__(kThreads, 1)
     v2_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const KParams kp) {
@@ -112,8 +119,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qt = causal ? (kp.n_qt - 1 - r_in / gsize) : (r_in / gsize);
   const int bu = g0 + r_in % gsize;
   const int b = bu / P.units, u = bu % P.units;
-  const int n_kv_all = (P.N + BN - 1) / BN;
-  const int n_kv = causal ? min(qt + 1, n_kv_all) : n_kv_all;
+  // this sequence's query rows: [seq0, seq0 + SN) of the (packed) token axis, TMA batch
+  // coordinate tb; its keys: SNk rows from kseq0 (or through the block table). With keys of
+  // their own the queries are the sequence's last SN positions: query i sees keys [0, qoff + i].
+  int seq0 = 0, SN = P.N, tb = b;
+  if constexpr (KMODE != kDense) {
+    seq0 = P.cu_seqlens[b];
+    SN = P.cu_seqlens[b + 1] - seq0;
+    tb = 0;
+    // offsets are device data: a sequence outside [0, total) or longer than the stated maximum
+    // is reported (DEV_BAD_INDEX) and skipped, so no store leaves the output
+    if (seq0 < 0 || SN < 0 || SN > P.N || seq0 > P.total - SN) {
+      if (threadIdx.x == 0 && qt == 0) flag_device_error(DEV_BAD_INDEX);
+      return;
+    }
+    if (qt * BM >= SN) return;  // a tile past this sequence's end: nothing to do (uniform)
+  }
+  int kseq0 = seq0, SNk = SN;
+  if constexpr (KMODE == kKeysOffset) {
+    kseq0 = P.cu_seqlens_k[b];
+    SNk = P.cu_seqlens_k[b + 1] - kseq0;
+    if (kseq0 < 0 || SNk < SN || kseq0 > P.total_k - SNk) {
+      if (threadIdx.x == 0 && qt == 0) flag_device_error(DEV_BAD_INDEX);
+      return;
+    }
+  } else if constexpr (KMODE == kKeysPaged) {
+    kseq0 = 0;
+    SNk = P.seqlens_k[b];
+    if (SNk < SN || SNk > P.max_pages * P.page_size) {
+      if (threadIdx.x == 0 && qt == 0) flag_device_error(DEV_BAD_INDEX);
+      return;
+    }
+  }
+  const int qoff = KMODE >= kKeysOffset ? SNk - SN : 0;
+  const int n_kv_all = (SNk + BN - 1) / BN;
+  // causal: the tile's last query row sees keys up to qoff + (qt + 1) BM - 1
+  const int n_kv = !causal ? n_kv_all
+                           : KMODE >= kKeysOffset ? min((qoff + (qt + 1) * BM + BN - 1) / BN, n_kv_all)
+                                                  : min(qt + 1, n_kv_all);  // BM == BN
+  // first output row of the tile on the (packed or batched) token axis
+  const size_t orow_tile =
+      (KMODE != kDense ? static_cast<size_t>(seq0) : static_cast<size_t>(b) * P.N) +
+      static_cast<size_t>(qt) * BM;
 
   auto bar = [](uint64_t& x) { return smem_u32(&x); };
 
@@ -159,16 +206,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < 2; ++h)
         for (int c = 0; c < D / 64; ++c)
           tma_load_4d(sQ + h * C::kQBytes + c * C::kChunkBytes, &tm_q, bar(bars.q_full), 64 * c,
-                      2 * u + h, qt * BM, b);
+                      2 * u + h, seq0 + qt * BM, tb);
+      // token-axis row of the sequence's key r: packed or batched rows, or (paged) the pool row
+      // through the block table. A page id outside the pool reads page 0 and, where the key is
+      // in use, flags DEV_BAD_INDEX.
+      auto key_row = [&](int r) -> int {
+        if constexpr (KMODE == kKeysPaged) {
+          const int pi = r / P.page_size;
+          int pg = 0;
+          if (pi < P.max_pages) {
+            pg = P.block_table[static_cast<size_t>(b) * P.max_pages + pi];
+            if (pg < 0 || pg >= P.num_pages) {
+              if (r < SNk) flag_device_error(DEV_BAD_INDEX);
+              pg = 0;
+            }
+          }
+          return pg * P.page_size + (r - pi * P.page_size);
+        } else {
+          return kseq0 + r;
+        }
+      };
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int s = j % NS;
         const uint32_t ph = (j / NS) & 1;
+        const int krow = key_row(j * BN);  // (paged: the table read overlaps the slot wait)
         if (!mbar_wait(bar(bars.k_empty[s]), ph ^ 1, abrt)) break;
         mbar_arrive_expect_tx(bar(bars.k_full[s]), C::kKBytes);
         for (int c = 0; c < D / 64; ++c)
           tma_load_4d(sK + s * C::kKBytes + c * C::kChunkBytes, &tm_k, bar(bars.k_full[s]),
-                      64 * c, kvh, j * BN, b);
+                      64 * c, kvh, krow, tb);
         if (!mbar_wait(bar(bars.v_empty[s]), ph ^ 1, abrt)) {
           issued = 2 * j + 1;
           break;
@@ -176,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(bar(bars.v_full[s]), C::kVBytes);
         for (int c = 0; c < D / 64; ++c)
           tma_load_4d(sV + s * C::kVBytes + c * C::kChunkBytes, &tm_v, bar(bars.v_full[s]),
-                      64 * c, kvh, j * BN, b);
+                      64 * c, kvh, krow, tb);
         issued = 2 * j + 2;
       }
       // Before leaving, make sure no copy of ours is still landing in shared memory.
@@ -253,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_s = tmem + tl + h * BN;
     const uint32_t t_o = tmem + tl + C::kOCol + h * D;
     const float sl2 = kp.scale_log2;
-    const int lim = causal ? min(row + 1, P.N) : P.N;  // keys [0, lim) are visible
+    const int lim = causal ? min(qoff + row + 1, SNk) : SNk;  // keys [0, lim) are visible
     float m = -INFINITY, l = 0.f;
     bool ok = true;
 
@@ -350,8 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       row_factor[0][r] = 1.f / l;
     } else {
       float lam = 0.f;
-      if (row < P.N) {
-        const float z = P.lam_logit[(static_cast<size_t>(b) * P.N + row) * P.units + u];
+      if (row < SN) {
+        const float z = P.lam_logit[(orow_tile + r) * P.units + u];
         lam = 1.f / (1.f + expf(-z));
       }
       row_factor[1][r] = lam / l;
@@ -372,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       static_assert(256 * RB <= NS * C::kKBytes, "staging fits in the K ring");
       const int col0 = h * H2;
       uint8_t* stage = smem + C::kKOff + (warp - kSoftmaxWarp0) * 32 * RB;
-      const bool live = row < P.N;
+      const bool live = row < SN;
 #pragma unroll 1
       for (int c = 0; c < H2; c += 32) {
         uint32_t oa[32], ob[32];
@@ -394,14 +461,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      const size_t orow0 = (static_cast<size_t>(b) * P.N + qt * BM + 32 * (warp & 3)) * P.units + u;
+      const size_t orow0 = (orow_tile + 32 * (warp & 3)) * P.units + u;
       __nv_bfloat16* out0 = static_cast<__nv_bfloat16*>(P.out) + col0;
 #pragma unroll
       for (int it = 0; it < PIECES; ++it) {
         const int rr = it * RPI + lane / PIECES;   // row (lane of the warp) this lane stores
         const int pc = lane % PIECES;
         const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * RB + ((pc ^ (rr & (PIECES - 1))) * 16));
-        if (qt * BM + 32 * (warp & 3) + rr < P.N)
+        if (qt * BM + 32 * (warp & 3) + rr < SN)
           *reinterpret_cast<uint4*>(out0 + (orow0 + static_cast<size_t>(rr) * P.units) * D + pc * 8) = v;
       }
     }
@@ -431,15 +498,21 @@ static bool make_map(CUtensorMap* m, const void* base, int cols, int heads, int 
   return encode_tmap_4d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, dims, strides, box, err, err_len);
 }
 
-template <int D, int NS>
+template <int D, int NS, int KMODE>
 static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
   using C = Cfg<D, NS>;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, D, p.q_heads, p.N, p.B, err, err_len) ||
-      !make_map(&mk, p.k, D, p.kv_heads, p.N, p.B, err, err_len) ||
-      !make_map(&mv, p.v, D, p.kv_heads, p.N, p.B, err, err_len))
+  // packed sequences: one batch row of `total` tokens; otherwise [B, N]
+  const int mN = KMODE != kDense ? p.total : p.N, mB = KMODE != kDense ? 1 : p.B;
+  // keys with offsets of their own, or the page pools as one [num_pages * page_size] axis
+  const int mNk = KMODE == kKeysPaged    ? p.num_pages * p.page_size
+                  : KMODE == kKeysOffset ? p.total_k
+                                         : mN;
+  if (!make_map(&mq, p.q, D, p.q_heads, mN, mB, err, err_len) ||
+      !make_map(&mk, p.k, D, p.kv_heads, mNk, mB, err, err_len) ||
+      !make_map(&mv, p.v, D, p.kv_heads, mNk, mB, err, err_len))
     return cudaErrorInvalidValue;
-  auto kern = v2_pair_kernel<D, NS>;
+  auto kern = v2_pair_kernel<D, NS, KMODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   KParams kp;
@@ -449,7 +522,8 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
   {
     // K/V bytes per (batch, pair) unit (the group / 2 pairs of a KV head share them); keep a
     // launch-order group's K/V within ~64 MB of L2
-    const double kv_bytes = static_cast<double>(p.N) * D * 2.0 * 2.0 / (p.group / 2);
+    const int nk = (p.cu_seqlens_k || p.block_table) ? p.max_seqlen_k : p.N;
+    const double kv_bytes = static_cast<double>(nk) * D * 2.0 * 2.0 / (p.group / 2);
     long long g = static_cast<long long>((64.0 * 1024 * 1024) / (kv_bytes > 1 ? kv_bytes : 1));
     const long long bu = static_cast<long long>(p.B) * p.units;
     kp.group = static_cast<int>(g < 1 ? 1 : (g > bu ? bu : g));
@@ -464,12 +538,32 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
 
 cudaError_t status_prefill_v2(int* v) { return read_clear_status(v); }
 
-// V2 pair prefill, dense bf16 tensors: q [B, N, Hq, D], k and v [B, N, Hkv, D], D = 64 or 128.
+// V2 pair prefill, bf16 tensors: q [B, N, Hq, D], k and v [B, N, Hkv, D] (or packed along the
+// token axis with cu_seqlens, keys with offsets of their own or in a page pool), D = 64 or 128.
 cudaError_t launch_prefill_v2(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
   if (p.mode != MODE_V2 || p.dqk != p.dv || p.group < 2 || p.group % 2 != 0)
     return cudaErrorNotSupported;
-  if (p.dqk == 128) return v2p::launch_cfg<128, 2>(p, s, err, err_len);
-  if (p.dqk == 64) return v2p::launch_cfg<64, 4>(p, s, err, err_len);
+  using namespace v2p;
+  const int mode = !p.cu_seqlens ? kDense
+                   : p.block_table ? kKeysPaged
+                   : p.cu_seqlens_k ? kKeysOffset
+                                    : kPacked;
+  if (p.dqk == 128) {
+    switch (mode) {
+      case kDense: return launch_cfg<128, 2, kDense>(p, s, err, err_len);
+      case kPacked: return launch_cfg<128, 2, kPacked>(p, s, err, err_len);
+      case kKeysOffset: return launch_cfg<128, 2, kKeysOffset>(p, s, err, err_len);
+      default: return launch_cfg<128, 2, kKeysPaged>(p, s, err, err_len);
+    }
+  }
+  if (p.dqk == 64) {
+    switch (mode) {
+      case kDense: return launch_cfg<64, 4, kDense>(p, s, err, err_len);
+      case kPacked: return launch_cfg<64, 4, kPacked>(p, s, err, err_len);
+      case kKeysOffset: return launch_cfg<64, 4, kKeysOffset>(p, s, err, err_len);
+      default: break;
+    }
+  }
   return cudaErrorNotSupported;
 }
 

@@ -64,10 +64,9 @@ typedef enum { DIFFATTN_BF16 = 0, DIFFATTN_FP32 = 1 } diffattn_dtype;
    error relative to the output grows like 2^-9 / |1 - lambda|. The default tensor-core path finds
    each map's exact row statistics first and rounds A1 - lambda A2 once, after the subtraction.
    For diffattn_v2_fwd, one pass per head is the default (see there). */
-#define DIFFATTN_EXACT 32 /* diffattn_v2_fwd only: find each head's exact row statistics first and
-   round attn[2p] - sigmoid(lam) * attn[2p+1] once, after the subtraction (the V1 default path),
-   instead of one flash pass per head. Also the numerics of diffattn_v2_fwd_varlen and
-   diffattn_v2_fwd_paged, which always take that path. */
+#define DIFFATTN_EXACT 32 /* V2 prefills (diffattn_v2_fwd, _varlen, _paged) only: find each head's
+   exact row statistics first and round attn[2p] - sigmoid(lam) * attn[2p+1] once, after the
+   subtraction (the V1 default path), instead of one flash pass per head. */
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 DIFFATTN_API int diffattn_version(void);
@@ -433,9 +432,10 @@ DIFFATTN_API int diffattn_fwd_varlen_qk(const void* q, const void* k, const void
  *   cu_seqlens_q : device int32 [B + 1];  cu_seqlens_k : device int32 [B + 1], or NULL for keys
  *            at the queries' offsets (max_seqlen_k and total_k are then ignored). Checked on the
  *            device as for diffattn_fwd_varlen_qk (DIFFATTN_ERR_INDEX).
- *   flags : DIFFATTN_CAUSAL or 0
- * Rows of `out` that belong to no sequence are not written. Supported: dtype DIFFATTN_BF16
- * (tensor-core exact path), d in {64, 128}, Hq/Hkv even.
+ *   flags : DIFFATTN_CAUSAL or 0, optionally DIFFATTN_EXACT (numerics as for diffattn_v2_fwd:
+ *            one flash pass per head by default)
+ * Rows of `out` that belong to no sequence are not written. Supported: dtype DIFFATTN_BF16,
+ * d in {64, 128}, Hq/Hkv even.
  * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_CUDA.
  * ------------------------------------------------------------------------------------------ */
 DIFFATTN_API int diffattn_v2_fwd_varlen(const void* q, const void* k, const void* v,
@@ -462,7 +462,8 @@ DIFFATTN_API int diffattn_v2_fwd_varlen(const void* q, const void* k, const void
  * Checked on the device: a sequence with Lk < Lq or Lk > max_pages * page_size is skipped, and a
  * used block-table entry outside [0, num_pages) reads page 0; both are reported by
  * diffattn_device_status() as DIFFATTN_ERR_INDEX. Entries past a sequence's keys are not read.
- * Other arguments as the packed calls. Supported: dtype DIFFATTN_BF16, d = 128 (V1: dv = 256).
+ * Other arguments (flags included: DIFFATTN_EXACT for V2) as the packed calls. Supported: dtype
+ * DIFFATTN_BF16, d = 128 (V1: dv = 256).
  * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_CUDA.
  * ------------------------------------------------------------------------------------------ */
 DIFFATTN_API int diffattn_fwd_paged(const void* q, const void* k_pool, const void* v_pool,

@@ -370,11 +370,14 @@ def test_fwd_varlen_qk_fewer_keys_than_queries_is_reported():
     assert_bf16(out[:100], want)
 
 
+@pytest.mark.parametrize("exact", [False, True])
 @pytest.mark.parametrize("lens_q,lens_k,causal", [([300, 1, 129, 0, 200], None, True),
                                                    ([100, 64], [700, 64], True),
                                                    ([50, 130], [50, 300], False)])
-def test_v2_fwd_varlen(lens_q, lens_k, causal):
-    """V2 over packed sequences (shared offsets, and keys of their own) against the oracle."""
+def test_v2_fwd_varlen(lens_q, lens_k, causal, exact):
+    """V2 over packed sequences (shared offsets, and keys of their own) against the oracle, on
+    the pair kernel (default) and the exact two-pass kernel; a sequence alone through the batched
+    V2 prefill on the same kernel gives the same numbers."""
     Hq, Hkv, d = 8, 2, 128
     tq = sum(lens_q) + 2
     tk = tq if lens_k is None else sum(lens_k) + 3
@@ -387,7 +390,8 @@ def test_v2_fwd_varlen(lens_q, lens_k, causal):
     cu_k = None if lens_k is None else torch.tensor(np.concatenate([[0], np.cumsum(lens_k)]),
                                                     dtype=torch.int32)
     got = da.diffattn_v2_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), lam.to(DEV), cu_q.to(DEV),
-                                    None if cu_k is None else cu_k.to(DEV), causal=causal)
+                                    None if cu_k is None else cu_k.to(DEV), causal=causal,
+                                    exact=exact)
     want = ref.diffattn_v2_fwd_varlen(q, k, v, lam, cu_q, cu_k, causal=causal)
     n = sum(lens_q)
     assert_bf16(got[:n], want[:n])
@@ -396,7 +400,7 @@ def test_v2_fwd_varlen(lens_q, lens_k, causal):
         a, b = int(cu_q[2]), int(cu_q[3])
         one = da.diffattn_v2_fwd(q[None, a:b].contiguous().to(DEV), k[None, a:b].contiguous().to(DEV),
                                  v[None, a:b].contiguous().to(DEV), lam[None, a:b].contiguous().to(DEV),
-                                 causal=causal, exact=True)
+                                 causal=causal, exact=exact)
         assert torch.equal(got[a:b], one[0])
     da.diffattn_device_status()
 
@@ -428,9 +432,12 @@ def test_fwd_paged(ps, lens_q, lens_k):
     da.diffattn_device_status()
 
 
-def test_v2_fwd_paged_and_bad_page():
-    """V2 against keys in pages, against the oracle; unused table entries (-1) are never read,
-    and a used entry outside the pool is reported as DIFFATTN_ERR_INDEX."""
+@pytest.mark.parametrize("exact", [False, True])
+def test_v2_fwd_paged_and_bad_page(exact):
+    """V2 against keys in pages, against the oracle, on the pair kernel (default) and the exact
+    two-pass kernel; the same numbers as the packed prefill over the keys laid out contiguously;
+    unused table entries (-1) are never read, and a used entry outside the pool is reported as
+    DIFFATTN_ERR_INDEX."""
     ps, Hq, Hkv = 128, 8, 2
     lens_q, lens_k = [200, 5], [600, 130]
     mp = 5
@@ -444,12 +451,19 @@ def test_v2_fwd_paged_and_bad_page():
     cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lens_q)]), dtype=torch.int32)
     sk = torch.tensor(lens_k, dtype=torch.int32)
     args = (q.to(DEV), k_pool.to(DEV), v_pool.to(DEV), lg.to(DEV), cu_q.to(DEV), sk.to(DEV))
-    got = da.diffattn_v2_fwd_paged(*args, table.to(DEV))
+    got = da.diffattn_v2_fwd_paged(*args, table.to(DEV), exact=exact)
     da.diffattn_device_status()  # OK: no used entry is bad
     want = ref.diffattn_v2_fwd_paged(q, k_pool, v_pool, lg, cu_q, sk, table)
     assert_bf16(got, want)
+    # the same keys packed contiguously: sequence b's rows are its cache rows 0 .. lens_k[b]-1
+    kf = torch.cat([kc[b, :lens_k[b]] for b in range(2)])
+    vf = torch.cat([vc[b, :lens_k[b]] for b in range(2)])
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lens_k)]), dtype=torch.int32)
+    flat = da.diffattn_v2_fwd_varlen(q.to(DEV), kf.to(DEV), vf.to(DEV), lg.to(DEV), cu_q.to(DEV),
+                                     cu_k.to(DEV), exact=exact)
+    assert torch.equal(got, flat)
     table[0, 3] = k_pool.shape[0] + 4
-    da.diffattn_v2_fwd_paged(*args, table.to(DEV))
+    da.diffattn_v2_fwd_paged(*args, table.to(DEV), exact=exact)
     with pytest.raises(da.DiffAttnError) as e:
         da.diffattn_device_status()
     assert e.value.status == -9  # DIFFATTN_ERR_INDEX
@@ -766,10 +780,13 @@ def test_cuda_graph_capture_and_replay():
     v2 = make_v2_decode_inputs(2, 500, 16, 2, 128, seed=243, ragged=True)
     v2q, v2k, v2v = v2.q.to(DEV), v2.k_cache.to(DEV), v2.v_cache.to(DEV)
     v2l, v2s = v2.lam_logit.to(DEV), v2.seqlens.to(DEV)
+    v2p = make_v2_inputs(2, 300, 8, 2, 128, seed=244)
+    pq, pk, pv, pl = v2p.q.to(DEV), v2p.k.to(DEV), v2p.v.to(DEV), v2p.lam_logit.to(DEV)
     li = da.diffattn_lambda_init(12)
     out_p = torch.empty((2, 300, 2, 256), dtype=torch.bfloat16, device=DEV)
     out_d = torch.empty((3, 2, 256), dtype=torch.bfloat16, device=DEV)
     out_v = torch.empty((2, 8, 128), dtype=torch.bfloat16, device=DEV)
+    out_2 = torch.empty((2, 300, 4, 128), dtype=torch.bfloat16, device=DEV)
     ws_d = torch.empty(da.diffattn_decode_workspace_size(3, 700, 2), dtype=torch.uint8, device=DEV)
     ws_v = torch.empty(da.diffattn_v2_decode_workspace_size(2, 500, 16, 2, 128), dtype=torch.uint8,
                        device=DEV)
@@ -779,11 +796,13 @@ def test_cuda_graph_capture_and_replay():
         da.diffattn_decode(dq, dk, dv, dl, li, seqlens=ds, workspace=ws_d, out=out_d, stream=stream)
         da.diffattn_v2_decode(v2q, v2k, v2v, v2l, seqlens=v2s, workspace=ws_v, out=out_v,
                               stream=stream)
+        da.diffattn_v2_fwd(pq, pk, pv, pl, out=out_2, stream=stream)
 
+    outs = (out_p, out_d, out_v, out_2)
     step()  # eager reference (also loads the kernels before capture)
     torch.cuda.synchronize()
-    want = [t.clone() for t in (out_p, out_d, out_v)]
-    for t in (out_p, out_d, out_v):
+    want = [t.clone() for t in outs]
+    for t in outs:
         t.zero_()
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
@@ -793,10 +812,10 @@ def test_cuda_graph_capture_and_replay():
             step(stream=s)
     torch.cuda.current_stream().wait_stream(s)
     for _ in range(2):
-        for t in (out_p, out_d, out_v):
+        for t in outs:
             t.zero_()
         g.replay()
         torch.cuda.synchronize()
-        for got, w in zip((out_p, out_d, out_v), want):
+        for got, w in zip(outs, want):
             assert torch.equal(got, w)
     da.diffattn_device_status()
