@@ -542,6 +542,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int uu = 0; uu < KW / 8; ++uu)
           st_shared_v4(d_row + (((u0 + uu) ^ (r & 7)) << 4), pk[4 * uu], pk[4 * uu + 1],
                        pk[4 * uu + 2], pk[4 * uu + 3]);
+        // Packed or paged keys: the tile's rows past the sequence's keys hold other data (the next
+        // sequence, padding, unused page rows) that may not be finite. Their D is 0, but 0 * NaN
+        // would still reach O, so those V rows are zeroed before D is released to the V product.
+        // Batched tiles past N are zero-filled by TMA.
+        const int vkey0 = jv * BN;
+        if ((KMODE != kKeysShared || P.cu_seqlens) && vkey0 + BN > SNk) {
+          for (int h = 0; h < 2 && ok; ++h) {
+            const int idx = v_load(jv, h);
+            ok = mbar_wait(bar(bars.slot_full[idx % NSLOT]), (idx / NSLOT) & 1, abrt);
+          }
+          if (__any_sync(0xffffffffu, !ok)) {
+            ok = false;
+            break;
+          }
+          // thread (wg, r): key r of the tile (V half r / 64, row r % 64), 64-column chunks
+          // wg, wg + 4, ... of that row
+          if (vkey0 + r >= SNk) {
+            const int vs = v_load(jv, r >> 6) % NSLOT;
+            for (int c = wg; c < DV / 64; c += kNumWG) {
+              const uint32_t vrow = sSlot + vs * C::kSlot + c * C::kVHalfChunk + (r & 63) * 128;
+#pragma unroll
+              for (int q = 0; q < 8; ++q) st_shared_v4(vrow + 16 * q, 0u, 0u, 0u, 0u);
+            }
+          }
+        }
         fence_proxy_async_smem();
         mbar_arrive(bar(bars.d_full));
       }

@@ -401,6 +401,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       float l0, l1;
       f2unpack(lsum, l0, l1);
       l += l0 + l1;
+      if constexpr (KMODE != kDense) {
+        // Packed or paged keys: the tile's rows past the sequence's keys hold other data (the next
+        // sequence, padding, unused page rows) that may not be finite. Their P is 0, but 0 * NaN
+        // would still reach O, so head a's threads zero those V rows before releasing P_a (both
+        // heads' products are issued after that). Batched tiles past N are zero-filled by TMA.
+        if (h == 0 && key0 + BN > SNk) {
+          const int s = j % NS;
+          ok = mbar_wait(bar(bars.v_full[s]), (j / NS) & 1, abrt);
+          if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+          if (key0 + r >= SNk) {
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+              const uint32_t vrow = sV + s * C::kVBytes + c * C::kChunkBytes + r * 128;
+#pragma unroll
+              for (int q = 0; q < 8; ++q) st_shared_v4(vrow + 16 * q, 0u, 0u, 0u, 0u);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(bars.p_full[h]));
