@@ -481,18 +481,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (!pass2) {
         // ---- pass 1: exact row max and row sum of each map (online over key tiles) ----
-#pragma unroll
-        for (int mp = 0; mp < 2; ++mp) {
-          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int i = 0; i < KW; i += 2)
-            mx[(i >> 1) & 3] = fmax3(mx[(i >> 1) & 3], __uint_as_float(sr[mp][i]),
-                                     __uint_as_float(sr[mp][i + 1]));
-          const float mt = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * sl2;
-          const float mn = fmaxf(m[mp], mt);
-          if (mn == -INFINITY) continue;  // every key of this tile is masked for this row
-          const float nb = -mn;
-          const uint64_t scale2 = f2pack(sl2, sl2), off2 = f2pack(nb, nb);
+        // The sum is taken against the running maximum m (any reference point gives the same
+        // statistics: b = m + log2 l); the tile's own maximum is found only on a row's first
+        // tile with a visible key, or when a score so far above m overflows the sum.
+        auto tile_sum = [&](int mp, float ref) -> float {
+          const uint64_t scale2 = f2pack(sl2, sl2), off2 = f2pack(-ref, -ref);
           uint64_t acc[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
           for (int i = 0; i < KW; i += 2) {
@@ -505,8 +498,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           float a0, a1, a2, a3;
           f2unpack(acc[0], a0, a1);
           f2unpack(acc[1], a2, a3);
-          l[mp] = l[mp] * ex2_approx(m[mp] + nb) + ((a0 + a1) + (a2 + a3));
-          m[mp] = mn;
+          return (a0 + a1) + (a2 + a3);
+        };
+        auto tile_max = [&](int mp) -> float {
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int i = 0; i < KW; i += 2)
+            mx[(i >> 1) & 3] = fmax3(mx[(i >> 1) & 3], __uint_as_float(sr[mp][i]),
+                                     __uint_as_float(sr[mp][i + 1]));
+          return fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * sl2;
+        };
+#pragma unroll
+        for (int mp = 0; mp < 2; ++mp) {
+          float sum = 0.f;
+          bool redo = m[mp] == -INFINITY;
+          if (!redo) {
+            sum = tile_sum(mp, m[mp]);
+            redo = sum > 0x1p64f;  // also true for +inf; a NaN score keeps its NaN
+          }
+          if (redo) {
+            const float mn = fmaxf(m[mp], tile_max(mp));
+            if (mn == -INFINITY) continue;  // every key so far is masked for this row
+            sum = tile_sum(mp, mn);
+            l[mp] = l[mp] * ex2_approx(m[mp] - mn);
+            m[mp] = mn;
+          }
+          l[mp] += sum;
         }
       } else {
         // ---- pass 2: D = A1 - lambda A2 in fp32, rounded once to bf16, into shared memory ----
