@@ -537,17 +537,39 @@ def test_v2_identical_heads_give_one_minus_sigma_attention():
     assert_bf16(got, want)
 
 
-def test_v2_large_scores_rescale():
-    """Scores spread over tens of nats (q, k scaled up), so the running maximum grows by more than
-    2^8 inside a row and the default kernel rescales its output accumulators in tensor memory."""
+def _growing_keys(k, n, rate):
+    """Scale key row j by (1 + j / rate): later key tiles reach far higher scores."""
+    grow = 1.0 + torch.arange(n, dtype=torch.float32) / rate
+    return (k.float() * 12.0 * grow[None, :, None, None]).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("rate", [100.0, 30.0])
+def test_v2_large_scores_rescale(rate):
+    """Scores spread over tens of nats (q, k scaled up, keys growing along the sequence): a later
+    key tile's maximum exceeds the first tile's by about 31 (rate 100) or 104 (rate 30) in log2
+    units, so the default kernel rescales its output accumulators in tensor memory."""
     inp = make_v2_inputs(1, 900, 8, 2, 128, seed=99)
-    # score std ~1.1 nats at key 0, growing linearly to ~11 nats at key 899: the maximum of a
-    # later key tile exceeds that of the earlier ones by far more than 2^8
-    grow = 1.0 + torch.arange(900, dtype=torch.float32) / 100.0
     q = (inp.q.float() * 12.0).to(torch.bfloat16)
-    k = (inp.k.float() * 12.0 * grow[None, :, None, None]).to(torch.bfloat16)
+    k = _growing_keys(inp.k, 900, rate)
     got = da.diffattn_v2_fwd(q.to(DEV), k.to(DEV), inp.v.to(DEV), inp.lam_logit.to(DEV))
     want = ref.diffattn_v2_fwd(q, k, inp.v, inp.lam_logit)
+    assert_bf16(got, want)
+    da.diffattn_device_status()
+
+
+@pytest.mark.parametrize("rate", [100.0, 30.0])
+def test_prefill_large_scores_move_the_reference(rate):
+    """The exact prefill's first pass takes row sums against a stale reference point; at rate 30
+    a later key tile's scores pass it by more than 64 (log2 units), so the sum is taken again
+    against the tile's maximum. Against the oracle, causal, with the norm."""
+    inp = make_prefill_inputs(1, 900, 2, 128, 256, seed=101, layer=12)
+    q = (inp.q.float() * 12.0).to(torch.bfloat16)
+    k = _growing_keys(inp.k, 900, rate)
+    lam = np.array([0.4, 0.8])
+    li = ref.lambda_init(12)
+    got = da.diffattn_fwd(q.to(DEV), k.to(DEV), inp.v.to(DEV),
+                          torch.tensor(lam, dtype=torch.float32, device=DEV), li)
+    want = ref.diffattn_fwd(q, k, inp.v, lam, li)
     assert_bf16(got, want)
     da.diffattn_device_status()
 
