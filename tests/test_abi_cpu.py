@@ -364,3 +364,19 @@ def test_v2_decode_fp8_paged_validation(L):
     assert "multiple of 128" in L.diffattn_last_error_string().decode()
     assert dec(d=64) == -2
     assert dec(ws_bytes=need - 1) == -8
+
+
+def test_binding_constants_match_the_header():
+    """Every flag, dtype and status value the binding passes or compares equals the header's."""
+    hdr = open(os.path.join(os.path.dirname(__file__), "..", "include", "diffattn.h")).read()
+    defines = {m.group(1): int(m.group(2))
+               for m in re.finditer(r"#define (DIFFATTN_[A-Z_0-9]+) (\d+)\b", hdr)}
+    enums = {m.group(1): int(m.group(2))
+             for m in re.finditer(r"\b(DIFFATTN_[A-Z_0-9]+) = (-?\d+)", hdr)}
+    for name in ("DIFFATTN_CAUSAL", "DIFFATTN_NORM", "DIFFATTN_SCALE", "DIFFATTN_CUDA_CORES",
+                 "DIFFATTN_SINGLE_PASS", "DIFFATTN_EXACT"):
+        assert getattr(da, name) == defines[name], name
+    for name in ("DIFFATTN_OK", "DIFFATTN_BF16", "DIFFATTN_FP32"):
+        assert getattr(da, name) == enums[name], name
+    flags = [defines[n] for n in defines if n not in ("DIFFATTN_H_",) and n in dir(da)]
+    assert len(set(flags)) == len(flags)  # distinct bits
