@@ -100,30 +100,38 @@ def pin_toy_needle_table():
     g = _golden("toy_needle_table.json")
     lam, gap, sigma, seeds = g["lam"], g["gap"], g["sigma"], g["seeds"]
 
-    def draws(n, rho):
-        z1 = np.empty((seeds, n)); z2 = np.empty((seeds, n))
-        for s in range(seeds):
+    def draws(n, rho, seed_ids):
+        z1 = np.empty((len(seed_ids), n)); z2 = np.empty((len(seed_ids), n))
+        for i, s in enumerate(seed_ids):
             c, e = np.random.default_rng(s).standard_normal((2, n))
-            z1[s] = sigma * c
-            z1[s, 0] += gap
-            z2[s] = sigma * (rho * c + math.sqrt(1 - rho * rho) * e)
+            z1[i] = sigma * c
+            z1[i, 0] += gap
+            z2[i] = sigma * (rho * c + math.sqrt(1 - rho * rho) * e)
         return z1, z2
 
-    def share(w):
-        return np.mean(np.abs(w[:, 0]) / np.abs(w).sum(axis=1))
+    def per_seed(n, rho):
+        """Needle share |w_0| / sum |w| and needle weight w_0 of each seed's row, without and with
+        the subtraction. Rows are independent, so they are drawn and weighted 50 seeds at a time:
+        the same values as one pass over all seeds, in a working set that stays in cache."""
+        out = {k: [] for k in ("share_single", "share_diff", "w_single", "w_diff")}
+        for s0 in range(0, seeds, 50):
+            z1, z2 = draws(n, rho, range(s0, min(seeds, s0 + 50)))
+            for tag, lam_ in (("single", 0.0), ("diff", lam)):
+                w = ref.diff_weights(z1, z2, lam_)
+                out["share_" + tag].append(np.abs(w[:, 0]) / np.abs(w).sum(axis=1))
+                out["w_" + tag].append(w[:, 0])
+        return {k: float(np.mean(np.concatenate(v))) for k, v in out.items()}
 
     for row in g["rho_sweep_n32"]:
-        z1, z2 = draws(32, row["rho"])
-        single = ref.diff_weights(z1, z2, 0.0)
-        diff = ref.diff_weights(z1, z2, lam)
-        assert round(share(single), 3) == pytest.approx(row["single"], abs=1e-9)
-        assert round(share(diff), 3) == pytest.approx(row["diff"], abs=1e-9)
-        assert round(np.mean(single[:, 0]), 3) == pytest.approx(row["w_single"], abs=1e-9)
-        assert round(np.mean(diff[:, 0]), 3) == pytest.approx(row["w_diff"], abs=1e-9)
+        m = per_seed(32, row["rho"])
+        assert round(m["share_single"], 3) == pytest.approx(row["single"], abs=1e-9)
+        assert round(m["share_diff"], 3) == pytest.approx(row["diff"], abs=1e-9)
+        assert round(m["w_single"], 3) == pytest.approx(row["w_single"], abs=1e-9)
+        assert round(m["w_diff"], 3) == pytest.approx(row["w_diff"], abs=1e-9)
     for row in g["n_sweep_rho09"]:
-        z1, z2 = draws(row["n"], 0.9)
-        assert round(share(ref.diff_weights(z1, z2, 0.0)), 3) == pytest.approx(row["single"], abs=1e-9)
-        assert round(share(ref.diff_weights(z1, z2, lam)), 3) == pytest.approx(row["diff"], abs=1e-9)
+        m = per_seed(row["n"], 0.9)
+        assert round(m["share_single"], 3) == pytest.approx(row["single"], abs=1e-9)
+        assert round(m["share_diff"], 3) == pytest.approx(row["diff"], abs=1e-9)
 
 
 def pin_worked_example():
@@ -658,15 +666,22 @@ def _mutants():
     }
 
 
+# The two statistical pins (thousands of draws) run last: a mistake is caught as soon as one pin
+# fails, so most mutants never reach them.
+_SLOW_PINS = (pin_toy_needle_table, pin_lambda_spread)
+PINS_CHEAP_FIRST = [p for p in PINS if p not in _SLOW_PINS] + list(_SLOW_PINS)
+
+
 @pytest.mark.parametrize("name", list(_mutants().keys()))
 def test_planted_mistakes_are_caught(name, monkeypatch):
     attr, fn = _mutants()[name]
     monkeypatch.setattr(ref, attr, fn)
-    failed = []
-    for pin in PINS:
+    caught_by = None
+    for pin in PINS_CHEAP_FIRST:
         try:
             with np.errstate(all="ignore"):
                 pin()
         except (AssertionError, FloatingPointError, ValueError, IndexError):
-            failed.append(pin.__name__)
-    assert failed, f"planted mistake '{name}' passed every pin"
+            caught_by = pin.__name__
+            break
+    assert caught_by, f"planted mistake '{name}' passed every pin"
