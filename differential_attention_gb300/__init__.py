@@ -64,6 +64,8 @@ _SIGNATURES = {
     "diffattn_decode_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 6
                                 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
                                 + [ctypes.c_int] * 7 + [ctypes.c_void_p]),
+    "diffattn_decode_split_count": (ctypes.c_int, [ctypes.c_int] * 4
+                                    + [ctypes.POINTER(ctypes.c_int)] * 2),
     "diffattn_v2_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 7
                         + [ctypes.c_void_p]),
     "diffattn_v2_decode_workspace_size": (ctypes.c_int, [ctypes.c_int] * 5
@@ -339,6 +341,15 @@ def diffattn_decode_noalloc(q, k_cache, v_cache, lam, lambda_init: float = 0.0, 
                                          _ptr(norm_weight), float(eps), B, Lmax, H, two_d // 2,
                                          dv, flags, DIFFATTN_BF16, _stream(stream)))
     return out
+
+
+def diffattn_decode_split_count(B: int, Lmax: int, H: int, noalloc: bool = False):
+    """(splits, keys per split) of diffattn_decode (noalloc False) or diffattn_decode_noalloc
+    (noalloc True) for B sequences x H heads over Lmax cached keys. Host arithmetic only."""
+    s, c = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().diffattn_decode_split_count(int(B), int(Lmax), int(H), int(bool(noalloc)),
+                                             ctypes.byref(s), ctypes.byref(c)))
+    return int(s.value), int(c.value)
 
 
 def diffattn_v2_fwd(q, k, v, lam_logit, causal: bool = True, cuda_cores: bool = False,

@@ -329,6 +329,25 @@ DIFFATTN_API int diffattn_decode_noalloc(const void* q, const void* k_cache, con
   return ok();
 }
 
+DIFFATTN_API int diffattn_decode_split_count(int B, int Lmax, int H, int noalloc, int* splits,
+                                             int* chunk_keys) {
+  if (!splits || !chunk_keys) return fail(DIFFATTN_ERR_ARG, "diffattn_decode_split_count: null pointer");
+  if (B < 1 || Lmax < 1 || H < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode_split_count: need B, Lmax, H >= 1");
+  int chunk = 0;
+  if (noalloc) {
+    if (static_cast<long long>(B) * H > da::decode_noalloc_max_units())
+      return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode_split_count: B*H = %lld exceeds the "
+                  "no-allocation scratch limit of %lld", static_cast<long long>(B) * H,
+                  da::decode_noalloc_max_units());
+    *splits = da::decode_noalloc_splits(B, Lmax, H, &chunk);
+  } else {
+    *splits = da::decode_splits(B, Lmax, H, &chunk);
+  }
+  *chunk_keys = chunk;
+  return ok();
+}
+
 DIFFATTN_API int diffattn_v2_fwd(const void* q, const void* k, const void* v,
                                  const float* lam_logit, void* out, int B, int N, int Hq, int Hkv,
                                  int d, int flags, int dtype, void* stream) {

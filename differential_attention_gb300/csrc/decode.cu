@@ -23,6 +23,9 @@
 #include <cmath>
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -532,19 +535,41 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
 // The array is shared by every call on a device and keeps the previous call's contents. Nothing
 // in it needs clearing: the split kernel writes every record (empty splits included) before the
 // combine kernel of the same call reads it. Two such calls that run at the same time on one
-// device (different streams, or graphs replayed concurrently) overwrite each other's partials:
-// the caller must keep them ordered.
+// device (on different streams, say) overwrite each other's partials: the caller must keep them
+// ordered.
 //
 // Host code may not use the array's name as a device address (on the host it names a host-side
-// stand-in). The device address is looked up once per device with cudaGetSymbolAddress, with that
-// device current, on the first call made on it; make that first call before any stream capture.
+// stand-in). The device address is looked up with cudaGetSymbolAddress, with that device current,
+// on the first call made on it (and again on the first call after its context was recreated);
+// make that first call before any stream capture.
 // ---------------------------------------------------------------------------------------------
 static __device__ __align__(256) float g_decode_scratch[kNoAllocScratchBytes / sizeof(float)];
 
 namespace {
 constexpr int kMaxDevices = 128;
 std::mutex g_scratch_mu;
-float* g_scratch_addr[kMaxDevices] = {};
+// The array's device address is a property of the context the module was loaded into, so the
+// cache remembers the context it was looked up in: after the primary context of a device is torn
+// down and recreated (cudaDeviceReset in this process), the next call looks it up again.
+struct ScratchSlot {
+  CUcontext ctx = nullptr;
+  float* addr = nullptr;
+};
+ScratchSlot g_scratch_slot[kMaxDevices];
+
+PFN_cuCtxGetCurrent_v4000 ctx_get_current_entry() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult res;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &res) ==
+            cudaSuccess &&
+        res == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  });
+  return fn;
+}
 }  // namespace
 
 cudaError_t decode_scratch_address(float** out) {
@@ -552,19 +577,50 @@ cudaError_t decode_scratch_address(float** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  auto get_ctx = ctx_get_current_entry();
+  if (!get_ctx) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (ctx == nullptr) {
+    // no context current on this thread yet: cudaSetDevice makes the device's primary one current
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return e;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  }
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchSlot& slot = g_scratch_slot[dev];
+  if (slot.addr == nullptr || slot.ctx != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = static_cast<float*>(p);
+    slot.ctx = ctx;
+    slot.addr = static_cast<float*>(p);
   }
-  *out = g_scratch_addr[dev];
+  *out = slot.addr;
   return cudaSuccess;
 }
 
 long long decode_noalloc_max_units() {
   return static_cast<long long>(kNoAllocScratchBytes / (kRec * sizeof(float)));
+}
+
+// The split count of diffattn_decode, lowered when B x H x splits records would not fit in the
+// scratch array: the chunk grows to ceil(Lmax / fit) keys, rounded up to whole CTA rounds, so
+// that splits = ceil(Lmax / chunk) <= fit. Requires B * H <= decode_noalloc_max_units().
+int decode_noalloc_splits(int B, int Lmax, int H, int* chunk_out) {
+  int chunk = 0;
+  int S = decode_splits(B, Lmax, H, &chunk);
+  const long long units = static_cast<long long>(B) * H;
+  const long long fit = decode_noalloc_max_units() / units;
+  if (S > fit) {
+    const int step = kDecWarps * kG;
+    long long c = (Lmax + fit - 1) / fit;
+    c = (c + step - 1) / step * step;
+    chunk = static_cast<int>(c);
+    S = static_cast<int>((Lmax + c - 1) / c);
+  }
+  if (chunk_out) *chunk_out = chunk;
+  return S;
 }
 
 // Same kernels as launch_decode, with the split count lowered (if needed) so that the partials
@@ -576,15 +632,7 @@ cudaError_t launch_decode_noalloc(const DecodeArgs& a, cudaStream_t st) {
   cudaError_t e = decode_scratch_address(&scratch);
   if (e != cudaSuccess) return e;
   int chunk = 0;
-  int S = decode_splits(a.B, a.Lmax, a.H, &chunk);
-  const long long fit = decode_noalloc_max_units() / units;
-  if (S > fit) {
-    const int step = kDecWarps * kG;
-    long long c = (a.Lmax + fit - 1) / fit;
-    c = (c + step - 1) / step * step;
-    chunk = static_cast<int>(c);
-    S = static_cast<int>((a.Lmax + c - 1) / c);
-  }
+  const int S = decode_noalloc_splits(a.B, a.Lmax, a.H, &chunk);
   DecSplitParams sp;
   sp.q = static_cast<const __nv_bfloat16*>(a.q);
   sp.kc = static_cast<const __nv_bfloat16*>(a.k_cache);

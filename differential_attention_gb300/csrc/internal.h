@@ -277,6 +277,7 @@ cudaError_t status_backward(int* v);
 // Decode whose split partials live in a fixed device array of this size (no workspace argument).
 constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(16) << 20;
 long long decode_noalloc_max_units();  // largest B * H whose partials fit (one split each)
+int decode_noalloc_splits(int B, int Lmax, int H, int* chunk_out);  // splits the no-alloc call runs
 cudaError_t launch_decode_noalloc(const DecodeArgs& a, cudaStream_t s);
 
 // Two-pass tensor-core prefill (A1 - lambda A2 formed in fp32 before rounding).

@@ -184,13 +184,17 @@ DIFFATTN_API int diffattn_decode(const void* q, const void* k_cache, const void*
  * partials go to a scratch array built into the library (DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES,
  * held on every GPU that loads the library until the process exits).
  *   Limit: B * H <= DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES / 2064 (= 8128); larger calls return
- *   DIFFATTN_ERR_SHAPE. The cache may be split into fewer slices than diffattn_decode uses, so
- *   results agree with diffattn_decode to rounding, not bit for bit.
+ *   DIFFATTN_ERR_SHAPE. Where B * H * (diffattn_decode's split count) records of 2064 bytes
+ *   would not fit, the cache is cut into fewer, longer slices (diffattn_decode_split_count
+ *   reports both counts); the result then agrees with diffattn_decode to rounding. Otherwise
+ *   both calls run the same kernels on the same slices and agree bit for bit.
  *   The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- *   with that device current); make that first call before any stream capture.
- *   All calls on a device share the array: calls that can run at the same time (other streams,
- *   concurrent replays) race on it, so keep them ordered. No call depends on what an earlier call
- *   left there. It calls no allocator (cudaMalloc, cudaFree or any library that allocates).
+ *   with that device current); make that first call before any stream capture. The address
+ *   belongs to the device's current context: a call made after that context was destroyed and
+ *   recreated in this process (cudaDeviceReset) looks it up again.
+ *   All calls on a device share the array: calls that can run at the same time (on other
+ *   streams) race on it, so keep them ordered. No call depends on what an earlier call left
+ *   there. It calls no allocator (cudaMalloc, cudaFree or any library that allocates).
  * ------------------------------------------------------------------------------------------ */
 #define DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
 DIFFATTN_API int diffattn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
@@ -198,6 +202,18 @@ DIFFATTN_API int diffattn_decode_noalloc(const void* q, const void* k_cache, con
                                          float lambda_init, const float* norm_weight, float eps,
                                          int B, int Lmax, int H, int d, int dv, int flags,
                                          int dtype, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * How many slices of the cache a decode of B sequences x H heads over Lmax keys is split into:
+ * by diffattn_decode (noalloc = 0) or by diffattn_decode_noalloc (noalloc = 1). Host-only
+ * arithmetic (no device is touched), so a caller can tell whether the two calls will agree bit
+ * for bit (equal counts) or to rounding (the no-allocation call lowered its count).
+ *   splits, chunk_keys : host int out-parameters: the slice count and keys per slice.
+ * Errors: ERR_ARG (null pointer), ERR_SHAPE (B, Lmax or H < 1, or noalloc = 1 with B * H above
+ * the no-allocation limit).
+ * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_decode_split_count(int B, int Lmax, int H, int noalloc, int* splits,
+                                             int* chunk_keys);
 
 /* ------------------------------------------------------------------------------------------
  * DIFF V2 prefill (page "Differential Transformer: softmax can't say zero, so it subtracts",

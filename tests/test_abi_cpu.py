@@ -98,6 +98,37 @@ def test_decode_validation(L):
     assert dec(ws=ctypes.c_void_p(0x10010)) == -8  # not 256-byte aligned
 
 
+def test_decode_split_counts(L):
+    """The split arithmetic of diffattn_decode and of its no-allocation variant (host only).
+    The no-allocation call keeps diffattn_decode's slices whenever B x H x splits partial
+    records (2064 bytes each) fit in its 16 MiB scratch, and otherwise cuts the cache into
+    fewer, longer slices of whole 32-key CTA rounds that still cover every key."""
+    max_units = (16 << 20) // 2064
+    assert max_units == 8128
+    # few (sequence, head) pairs: both calls split alike
+    assert da.diffattn_decode_split_count(3, 3001, 2) == da.diffattn_decode_split_count(3, 3001, 2, True)
+    # 768 pairs: 10 splits fit; the 3000-key cache and the 32K-token decode both need lowering
+    for lmax in (3000, 32768):
+        ws_s, _ = da.diffattn_decode_split_count(64, lmax, 12)
+        na_s, _ = da.diffattn_decode_split_count(64, lmax, 12, True)
+        assert ws_s > 10 and na_s <= 10 and na_s < ws_s, (lmax, ws_s, na_s)
+    for B, lmax, H in [(1, 1, 1), (1, 31, 1), (2, 257, 3), (3, 3001, 2), (16, 8192, 12),
+                       (64, 3000, 12), (64, 32768, 12), (8128, 100000, 1), (127, 65536, 64),
+                       (1000, 5, 8), (7, 1 << 20, 5)]:
+        ws_s, ws_c = da.diffattn_decode_split_count(B, lmax, H)
+        na_s, na_c = da.diffattn_decode_split_count(B, lmax, H, True)
+        for s, c in ((ws_s, ws_c), (na_s, na_c)):
+            assert c % 32 == 0 and s * c >= lmax and (s - 1) * c < lmax, (B, lmax, H, s, c)
+        assert na_s * B * H <= max_units and na_s <= ws_s
+        if ws_s * B * H <= max_units:
+            assert (na_s, na_c) == (ws_s, ws_c)
+    s, c = ctypes.c_int(0), ctypes.c_int(0)
+    assert L.diffattn_decode_split_count(8129, 16, 1, 1, ctypes.byref(s), ctypes.byref(c)) == -2
+    assert L.diffattn_decode_split_count(8129, 16, 1, 0, ctypes.byref(s), ctypes.byref(c)) == 0
+    assert L.diffattn_decode_split_count(0, 16, 1, 0, ctypes.byref(s), ctypes.byref(c)) == -2
+    assert L.diffattn_decode_split_count(1, 16, 1, 0, None, ctypes.byref(c)) == -1
+
+
 def test_v2_validation(L):
     def v2(Hq=64, Hkv=8, d=128, dtype=0, flags=1, q=FAKE):
         return L.diffattn_v2_fwd(q, FAKE, FAKE, FAKE, FAKE, 2, 64, Hq, Hkv, d, flags, dtype, None)
