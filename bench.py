@@ -3,13 +3,20 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step = one pass of the prefill hot path on the 3B-layer workload (B 4, N 4096, 12 heads,
-d 128, dv 256, causal, bf16): the lambda kernel (exp reparameterisation) followed by the fused
-DiffAttn prefill with RMSNorm and (1 - lambda_init) epilogue. `value` is TFLOP/s counted at 1536
-MMA flops per causal query-key pair (4d for the two score maps + 4dv for the two value products),
-summed over ranks (weak scaling: every rank runs its own batch). The same JSON line carries the
-decode workload (B 64, cache 32768, 12 heads: HBM GB/s) and the V2 GQA workload as secondary
-objects, the roofline of the dominant kernel, the clocks seen during the timed region, an
-end-to-end number through host buffers, and the float64 oracle timed on the host cores.
+d 128, dv 256, causal, bf16): lambda formed from its four vectors in the kernel's prologue, the
+fused DiffAttn prefill, RMSNorm and the (1 - lambda_init) scale. `value` is TFLOP/s counted at
+1536 MMA flops per causal query-key pair (4d for the two score maps + 4dv for the two value
+products), summed over ranks (weak scaling: every rank runs its own batch).
+
+The JSON line carries, in this order: the primary keys (with the roofline of the prefill kernel,
+the clocks of its timed loop and an end-to-end figure through host buffers beside the bare copy
+bound of the same bytes), one compact block per secondary workload, the float64 oracle timed on
+the host cores, a `headline` summary, and last the decode workload (B 64, cache 32768, 12 heads:
+HBM GB/s) with the clocks of its own timed loop.
+
+Roofline peaks: MEASURED_PEAKS.json's burst bf16 figure for a timed loop under a second, its
+sustained figure for longer loops, its copy bandwidth for HBM-bound kernels; the nominal dense
+figures of the part (2.25 PFLOP/s bf16, 8 TB/s) are reported beside them as `frac_nominal`.
 
 `--impl reference` times the float64 CPU oracle (the only reference implementation that exists
 for this method) on bounded samples of the same workload, on rank 0 only.
@@ -51,6 +58,10 @@ BWD_ISSUED_FLOPS_PER_PAIR = (2 * 128 + 2 * 256) + 2 * (2 * 128 + 2 * 256 + 2 * 1
     + (4 * 128 + 2 * 256)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal dense figures of the part, reported beside the measured fractions
+NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
+# a timed loop this long or longer is read against the sustained (power-capped) bf16 peak
+SUSTAINED_AFTER_MS = 1000.0
 
 
 def causal_pairs(N: int) -> int:
@@ -274,9 +285,93 @@ def run_reference(args, rank: int, world: int):
 # ---------------------------------------------------------------------------------------------
 # our path
 # ---------------------------------------------------------------------------------------------
+class Timer:
+    """Warm-up, then `n` calls of `fn` on the current stream, each bracketed by CUDA events.
+
+    Returns the mean per-call time (ms), the whole timed region (ms, from its own events) and,
+    when `clocks` is set, the clocks nvidia-smi saw while the loop ran."""
+
+    def __init__(self, torch, dev, barrier, warmup):
+        self.torch, self.dev, self.barrier, self.warmup = torch, dev, barrier, warmup
+        self.stream = torch.cuda.current_stream()
+
+    def ev(self):
+        return self.torch.cuda.Event(enable_timing=True)
+
+    def __call__(self, fn, n, clocks=False, status=None):
+        for _ in range(self.warmup):
+            fn()
+        if status:
+            status()
+        evs = [(self.ev(), self.ev()) for _ in range(n)]
+        t0, t1 = self.ev(), self.ev()
+
+        def loop():
+            self.barrier()
+            t0.record(self.stream)
+            for a, b in evs:
+                a.record(self.stream)
+                fn()
+                b.record(self.stream)
+            t1.record(self.stream)
+            self.barrier()
+
+        clk = None
+        if clocks:
+            with ClockSampler(self.dev.index) as sampler:
+                loop()
+            clk = sampler.summary()
+        else:
+            loop()
+        if status:
+            status()
+        return {"ms": statistics.mean(a.elapsed_time(b) for a, b in evs),
+                "total_ms": t0.elapsed_time(t1), "n": n, "clocks": clk}
+
+
+def tensor_peak(peaks, peak_src, total_ms, scale=1.0, what="bf16"):
+    """The measured bf16 peak that applies to a loop of `total_ms`: the burst figure for a loop
+    well under a second (the kernel does not reach the power cap), the sustained one otherwise."""
+    if total_ms < SUSTAINED_AFTER_MS:
+        key, kind = "bf16_tflops", "burst"
+    else:
+        key, kind = "bf16_tflops_sustained", "sustained"
+    p = peaks.get(key, FALLBACK_PEAKS[key]) * scale
+    src = f"{key} of {peak_src} ({kind}: the timed loop ran {total_ms:.0f} ms)"
+    if scale != 1.0:
+        src = f"{scale} x " + src + f"; {what}"
+    return p, src
+
+
+def tensor_roof(flops, t, peaks, peak_src, scale=1.0, what="bf16", nominal_scale=1.0):
+    achieved = flops / (t["ms"] * 1e-3) / 1e12
+    peak, src = tensor_peak(peaks, peak_src, t["total_ms"], scale, what)
+    nominal = NOMINAL["bf16_tflops"] * nominal_scale
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "peak_source": src,
+            "frac_nominal": achieved / nominal, "nominal_peak": nominal}
+
+
+def hbm_roof(nbytes, t, peaks, peak_src):
+    achieved = nbytes / (t["ms"] * 1e-3) / 1e9
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
+            "frac_nominal": achieved / NOMINAL["hbm_gbs"], "nominal_peak": NOMINAL["hbm_gbs"]}
+
+
+def compact(value, unit, t, roof, workload, world, **extra):
+    """A secondary workload's block: its figure, time, roofline fractions and a short name."""
+    blk = {"value": world * value, "unit": unit, "ms": round(t["ms"], 4), "calls": t["n"],
+           "frac": round(roof["frac"], 4), "frac_nominal": round(roof["frac_nominal"], 4),
+           "peak": f'{roof["peak"]:.1f} {roof["unit"]} ({roof["peak_source"].split(" (")[0]})',
+           "workload": workload}
+    blk.update(extra)
+    return blk
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     import torch
-    import torch.distributed as dist
     import differential_attention_gb300 as da
     from synth import (make_decode_inputs, make_dout, make_gda_decode_inputs, make_gda_inputs,
                        make_lambda_vectors, make_prefill_inputs, make_v2_decode_inputs,
@@ -287,8 +382,6 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     da.build()
     peaks, peak_src = load_peaks()
     stream = torch.cuda.current_stream()
-    peak_tf = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
 
     def barrier():
         dist_barrier()
@@ -296,16 +389,19 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     def max_over_ranks(x: float) -> float:
         return dist_max(x, dev)
 
-    def ev():
-        return torch.cuda.Event(enable_timing=True)
+    timer = Timer(torch, dev, barrier, args.warmup)
+    status = da.diffattn_device_status
+    want = lambda name: args.only in ("all", name)
 
     line = {"metric": "DiffAttn fwd TFLOP/s (% dense BF16 TC peak); decode HBM GB/s (% peak)",
             "value": None, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
+    extra = {}      # secondary workloads, printed after the primary keys
+    decode_blk = None
 
     # ======================= prefill: the step that `value` measures =======================
-    if args.only in ("all", "prefill"):
+    if want("prefill"):
         c = PREFILL
         inp = make_prefill_inputs(c["B"], c["N"], c["H"], c["d"], c["dv"], seed=1000 + rank,
                                   layer=c["layer"], device=dev)
@@ -313,30 +409,20 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         lv = tuple(t.to(dev).contiguous() for t in make_lambda_vectors(c["d"], seed=1001 + rank))
         out = torch.empty((c["B"], c["N"], c["H"], c["dv"]), dtype=torch.bfloat16, device=dev)
 
-        def step(q, k, v):
-            da.diffattn_fwd_fused_lambda(q, k, v, *lv, layer=c["layer"], out=out)
+        def step():
+            da.diffattn_fwd_fused_lambda(inp.q, inp.k, inp.v, *lv, layer=c["layer"], out=out)
 
-        for _ in range(args.warmup):
-            step(inp.q, inp.k, inp.v)
-        da.diffattn_device_status()
-        kev = [(ev(), ev()) for _ in range(args.steps)]
-        with ClockSampler(dev.index) as clk:
-            barrier()
-            t_start, t_end = ev(), ev()
-            t_start.record(stream)
-            for i in range(args.steps):
-                kev[i][0].record(stream)
-                step(inp.q, inp.k, inp.v)
-                kev[i][1].record(stream)
-            t_end.record(stream)
-            barrier()
-        da.diffattn_device_status()
-        total_ms = max_over_ranks(t_start.elapsed_time(t_end))
-        ms_per_step = total_ms / args.steps
-        kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+        t = timer(step, args.steps, clocks=True, status=status)
+        ms_per_step = max_over_ranks(t["total_ms"]) / args.steps
         flops = prefill_flops()
-        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        roof = tensor_roof(flops, t, peaks, peak_src)
         sha = source_sha(["prefill_exact.cu", "ptx.cuh"])
+        roof.update({"traffic": profiled_traffic("prefill_exact_3b.md", sha),
+                     "kernel": "prefill_exact_kernel<128,256,false> (lambda in the prologue)",
+                     "kernel_ms": t["ms"], "flops_per_launch": flops,
+                     "flops_per_pair": FLOPS_PER_PAIR,
+                     "definition_count_tflops":
+                         flops / FLOPS_PER_PAIR * FLOPS_PER_PAIR_DEF / (t["ms"] * 1e-3) / 1e12})
         line.update({
             "value": world * flops / (ms_per_step * 1e-3) / 1e12,
             "ms_per_step": ms_per_step,
@@ -345,21 +431,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        "parallelism": f"replicas x{world} (independent batches, no collective)",
                        "l2": "inputs larger than L2 (q, k, v = 302 MB per rank)",
                        "flops_per_pair": FLOPS_PER_PAIR},
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
-                         "unit": "TFLOP/s", "frac": achieved / peak_tf,
-                         "traffic": profiled_traffic("prefill_exact_3b.md", sha),
-                         "kernel": "prefill_exact_kernel<128,256,false>", "kernel_ms": kernel_ms,
-                         "flops_per_launch": flops,
-                         "peak_source": f"bf16_tflops_sustained of {peak_src} (kernel run back to back)",
-                         "definition_count_tflops":
-                             flops / FLOPS_PER_PAIR * FLOPS_PER_PAIR_DEF / (kernel_ms * 1e-3) / 1e12},
+            "roofline": roof,
             "gpu_launches": args.steps,
-            "clocks": clk.summary(),
+            "clocks": t["clocks"],
         })
 
         # ---------------- end to end through host buffers ----------------
         e2e_steps = max(3, min(20, args.steps))
-        hq, hk, hv = (t.cpu().pin_memory() for t in (inp.q, inp.k, inp.v))
+        hq, hk, hv = (x.cpu().pin_memory() for x in (inp.q, inp.k, inp.v))
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         hws = torch.empty(da.diffattn_fwd_host_workspace_size(c["B"], c["N"], c["H"], c["d"], c["dv"]),
                           dtype=torch.uint8, device=dev)
@@ -367,185 +446,103 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         def e2e_step():
             da.diffattn_fwd_host(hq, hk, hv, hout, *lv, layer=c["layer"], workspace=hws)
 
-        e2e_step()
-        barrier()
-        e0, e1 = ev(), ev()
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        barrier()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
+        te = timer(e2e_step, e2e_steps)
+        e2e_ms = max_over_ranks(te["total_ms"]) / e2e_steps
+
+        # the copy bound: the same pinned buffers moved with one plain cudaMemcpyAsync per tensor
+        # and no kernel; host-to-device on one stream, device-to-host on another, concurrently
+        # (the least any pipeline over this host link can take), and all four on one stream
+        dq, dk, dvv = (torch.empty_like(x) for x in (inp.q, inp.k, inp.v))
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+        def copies_overlapped():
+            s_in.wait_stream(stream)
+            s_out.wait_stream(stream)
+            with torch.cuda.stream(s_in):
+                for d_, h_ in ((dq, hq), (dk, hk), (dvv, hv)):
+                    d_.copy_(h_, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                hout.copy_(out, non_blocking=True)
+            stream.wait_stream(s_in)
+            stream.wait_stream(s_out)
+
+        def copies_serial():
+            for d_, h_ in ((dq, hq), (dk, hk), (dvv, hv)):
+                d_.copy_(h_, non_blocking=True)
+            hout.copy_(out, non_blocking=True)
+
+        tco = timer(copies_overlapped, e2e_steps)
+        tcs = timer(copies_serial, e2e_steps)
+        copy_ms = max_over_ranks(tco["total_ms"]) / e2e_steps
+        copy_serial_ms = max_over_ranks(tcs["total_ms"]) / e2e_steps
+        h2d, d2h = 3 * inp.q.numel() * 2, out.numel() * 2
         line["e2e"] = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                       "h2d_bytes_per_step": 3 * inp.q.numel() * 2,
-                       "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": e2e_ms,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e2e_ms,
+                       "copy_bound_ms": copy_ms, "copy_serial_ms": copy_serial_ms,
+                       "e2e_over_copy_bound": e2e_ms / copy_ms,
+                       "link_gbs": (h2d + d2h) / (copy_ms * 1e-3) / 1e9,
                        "via": "diffattn_fwd_host: pinned host q, k, v in and out, copies of "
-                              "each sequence overlapped with the prefill of the others"}
-        del inp, out, hq, hk, hv, hout, hws
-        torch.cuda.empty_cache()
+                              "each sequence overlapped with the prefill of the others; "
+                              "copy_bound_ms: the same bytes, plain copies only, H2D and D2H "
+                              "on two streams at once"}
+        del hq, hk, hv, hout, hws, dq, dk, dvv
 
-    # ======================= decode =======================
-    if args.only in ("all", "decode"):
-        dcfg = dict(DECODE, B=args.decode_batch)
-        dinp = make_decode_inputs(dcfg["B"], dcfg["L"], dcfg["H"], dcfg["d"], dcfg["dv"],
-                                  seed=2000 + rank, device=dev)
-        ws = torch.empty(da.diffattn_decode_workspace_size(dcfg["B"], dcfg["L"], dcfg["H"]),
-                         dtype=torch.uint8, device=dev)
-        dout = torch.empty((dcfg["B"], dcfg["H"], dcfg["dv"]), dtype=torch.bfloat16, device=dev)
-        li_dec = da.diffattn_lambda_init(dcfg["layer"])
-
-        def dec():
-            da.diffattn_decode(dinp.q, dinp.k_cache, dinp.v_cache, dinp.lam, li_dec, workspace=ws,
-                               out=dout)
-
-        for _ in range(args.warmup):
-            dec()
-        barrier()
-        dsteps = max(5, min(50, args.steps))
-        dev_ev = [(ev(), ev()) for _ in range(dsteps)]
-        for i in range(dsteps):
-            dev_ev[i][0].record(stream)
-            dec()
-            dev_ev[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        dms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
-        dbytes = decode_bytes(dcfg)
-        dgbs = dbytes / (dms * 1e-3) / 1e9
-        dsha = source_sha(["decode.cu", "ptx.cuh"])
-        line["decode"] = {
-            "metric": "decode HBM GB/s", "value": world * dgbs, "unit": "GB/s", "ms_per_call": dms,
-            "workload": f"decode_32k: B{dcfg['B']}, one query per sequence, cache 32768, H12, "
-                        "d128, dv256, bf16 (cache 25.8 GB at B64, larger than L2)",
-            "roofline": {"bound": "hbm", "achieved": dgbs, "peak": hbm, "unit": "GB/s",
-                         "frac": dgbs / hbm, "traffic": profiled_traffic("decode_32k.md", dsha),
-                         "bytes_per_launch": dbytes,
-                         "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
-                         "timed": "diffattn_decode call (split kernel + combine kernel)"},
-            "gpu_launches": 2 * dsteps}
-
-        # the same cache as a pool of 64-token pages, each sequence's pages scattered over it
-        ps = 64
-        mp = dcfg["L"] // ps
-        k_pool = dinp.k_cache.view(dcfg["B"] * mp, ps, dcfg["H"], 2 * dcfg["d"])
-        v_pool = dinp.v_cache.view(dcfg["B"] * mp, ps, dcfg["H"], dcfg["dv"])
-        gp = torch.Generator(device="cpu")
-        gp.manual_seed(2100 + rank)
-        table = torch.randperm(dcfg["B"] * mp, generator=gp).to(torch.int32).view(dcfg["B"], mp).to(dev)
-
-        def dec_paged():
-            da.diffattn_decode_paged(dinp.q, k_pool, v_pool, table, dinp.seqlens, dinp.lam, li_dec,
-                                     workspace=ws, out=dout)
-
-        for _ in range(args.warmup):
-            dec_paged()
-        barrier()
-        pev = [(ev(), ev()) for _ in range(dsteps)]
-        for i in range(dsteps):
-            pev[i][0].record(stream)
-            dec_paged()
-            pev[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        pms = statistics.mean(a.elapsed_time(b) for a, b in pev)
-        pgbs = dbytes / (pms * 1e-3) / 1e9
-        line["decode_paged"] = {
-            "metric": "decode HBM GB/s", "value": world * pgbs, "unit": "GB/s", "ms_per_call": pms,
-            "workload": f"decode_32k over a paged cache: B{dcfg['B']}, cache 32768 in 64-token pages "
-                        "placed in a random order in the pool, H12, d128, dv256, bf16",
-            "roofline": {"bound": "hbm", "achieved": pgbs, "peak": hbm, "unit": "GB/s",
-                         "frac": pgbs / hbm, "bytes_per_launch": dbytes,
-                         "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
-                         "timed": "diffattn_decode_paged call (split kernel + combine kernel)"},
-            "gpu_launches": 2 * dsteps}
-        del dinp, ws, dout, k_pool, v_pool, table
+        # the single-pass kernel (one flash pass per map on a 2-CTA cluster, opt-in), same inputs
+        lam_h = da.diffattn_lambda(*(x.expand(c["H"], -1).contiguous() for x in lv), layer=c["layer"])
+        li = da.diffattn_lambda_init(c["layer"])
+        ts = timer(lambda: da.diffattn_fwd(inp.q, inp.k, inp.v, lam_h, li, single_pass=True,
+                                           out=out), max(5, min(50, args.steps)), status=status)
+        td = timer(lambda: da.diffattn_fwd(inp.q, inp.k, inp.v, lam_h, li, out=out),
+                   max(5, min(50, args.steps)), status=status)
+        rs, rd = tensor_roof(flops, ts, peaks, peak_src), tensor_roof(flops, td, peaks, peak_src)
+        extra["prefill_single_pass"] = compact(
+            rs["achieved"], "TFLOP/s", ts, rs,
+            "prefill_3b, DIFFATTN_SINGLE_PASS: prefill_tc_kernel (a flash pass per map, 2-CTA "
+            "cluster)", world, default_two_pass_ms=round(td["ms"], 4))
+        del inp, out
         torch.cuda.empty_cache()
 
     # ======================= long-context prefill =======================
-    if args.only in ("all", "long"):
+    if want("long"):
         c = LONG
         inp = make_prefill_inputs(c["B"], c["N"], c["H"], c["d"], c["dv"], seed=4000 + rank,
                                   layer=c["layer"], device=dev, needle=True)
-        lv = tuple(t.to(dev).contiguous() for t in make_lambda_vectors(c["d"], seed=4001 + rank))
+        lv = tuple(x.to(dev).contiguous() for x in make_lambda_vectors(c["d"], seed=4001 + rank))
         out = torch.empty((c["B"], c["N"], c["H"], c["dv"]), dtype=torch.bfloat16, device=dev)
-
-        def lstep():
-            da.diffattn_fwd_fused_lambda(inp.q, inp.k, inp.v, *lv, layer=c["layer"], out=out)
-
-        for _ in range(args.warmup):
-            lstep()
-        barrier()
-        lsteps = max(3, min(10, args.steps))
-        l_ev = [(ev(), ev()) for _ in range(lsteps)]
-        for i in range(lsteps):
-            l_ev[i][0].record(stream)
-            lstep()
-            l_ev[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        lms = statistics.mean(a.elapsed_time(b) for a, b in l_ev)
+        t = timer(lambda: da.diffattn_fwd_fused_lambda(inp.q, inp.k, inp.v, *lv, layer=c["layer"],
+                                                       out=out),
+                  max(3, min(10, args.steps)), status=status)
         lflops = prefill_flops(c)
-        ltf = lflops / (lms * 1e-3) / 1e12
-        line["prefill_64k"] = {
-            "metric": "DiffAttn fwd TFLOP/s", "value": world * ltf, "unit": "TFLOP/s",
-            "ms_per_call": lms,
-            "workload": "prefill_64k: B1 N65536 H12 d128 dv256 causal, layer 24, one needle key per head",
-            "roofline": {"bound": "tensor", "achieved": ltf, "peak": peak_tf, "unit": "TFLOP/s",
-                         "frac": ltf / peak_tf, "flops_per_launch": lflops}}
+        r = tensor_roof(lflops, t, peaks, peak_src)
+        extra["prefill_64k"] = compact(r["achieved"], "TFLOP/s", t, r,
+                                       "B1 N65536 H12 causal, layer 24, one needle key per head", world)
         del inp, out
         torch.cuda.empty_cache()
 
     # ======================= V2 =======================
-    if args.only in ("all", "v2"):
+    if want("v2"):
         vc = V2
         vinp = make_v2_inputs(vc["B"], vc["N"], vc["Hq"], vc["Hkv"], vc["d"], seed=3000 + rank,
                               device=dev)
         vout = torch.empty((vc["B"], vc["N"], vc["Hq"] // 2, vc["d"]), dtype=torch.bfloat16,
                            device=dev)
-
-        def v2():
-            da.diffattn_v2_fwd(vinp.q, vinp.k, vinp.v, vinp.lam_logit, out=vout)
-
-        for _ in range(args.warmup):
-            v2()
-        barrier()
-        vsteps = max(5, min(30, args.steps))
-        v_ev = [(ev(), ev()) for _ in range(vsteps)]
-        for i in range(vsteps):
-            v_ev[i][0].record(stream)
-            v2()
-            v_ev[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        vms = statistics.mean(a.elapsed_time(b) for a, b in v_ev)
-        # the exact two-pass path (DIFFATTN_EXACT) on the same inputs, for context
-        x_ev = [(ev(), ev()) for _ in range(5)]
-        for a, b_ in x_ev:
-            a.record(stream)
-            da.diffattn_v2_fwd(vinp.q, vinp.k, vinp.v, vinp.lam_logit, out=vout, exact=True)
-            b_.record(stream)
-        barrier()
-        da.diffattn_device_status()
-        xms = statistics.mean(a.elapsed_time(b_) for a, b_ in x_ev)
+        t = timer(lambda: da.diffattn_v2_fwd(vinp.q, vinp.k, vinp.v, vinp.lam_logit, out=vout),
+                  max(5, min(30, args.steps)), status=status)
+        tx = timer(lambda: da.diffattn_v2_fwd(vinp.q, vinp.k, vinp.v, vinp.lam_logit, out=vout,
+                                              exact=True), 5, status=status)
         vflops = float(vc["B"] * (vc["Hq"] // 2) * causal_pairs(vc["N"]) * V2_FLOPS_PER_PAIR)
-        vtf = vflops / (vms * 1e-3) / 1e12
-        line["v2"] = {"metric": "V2 fwd TFLOP/s", "value": world * vtf, "unit": "TFLOP/s",
-                      "ms_per_call": vms,
-                      "workload": "v2_gqa: B2 N8192 Hq64 (32 pairs) Hkv8 d128 causal",
-                      "kernel": "v2_pair_kernel<128,2> (both heads of a pair in one CTA, one "
-                                "flash pass per head)",
-                      "exact_two_pass_ms": xms,
-                      "roofline": {"bound": "tensor", "achieved": vtf, "peak": peak_tf,
-                                   "unit": "TFLOP/s", "frac": vtf / peak_tf,
-                                   "flops_per_launch": vflops,
-                                   "traffic": profiled_traffic(
-                                       "v2_pair_gqa.md",
-                                       source_sha(["prefill_v2.cu", "ptx.cuh"]))}}
+        r = tensor_roof(vflops, t, peaks, peak_src)
+        extra["v2"] = compact(r["achieved"], "TFLOP/s", t, r,
+                              "B2 N8192 Hq64 (32 pairs) Hkv8 d128 causal, v2_pair_kernel", world,
+                              exact_two_pass_ms=round(tx["ms"], 4),
+                              traffic=profiled_traffic("v2_pair_gqa.md",
+                                                       source_sha(["prefill_v2.cu", "ptx.cuh"])))
         del vinp, vout
         torch.cuda.empty_cache()
 
     # ======================= prefill with fp8 scores =======================
-    if args.only in ("all", "fp8"):
+    if want("fp8"):
         c = PREFILL
         inp = make_prefill_inputs(c["B"], c["N"], c["H"], c["d"], c["dv"], seed=9000 + rank,
                                   layer=c["layer"], device=dev)
@@ -554,42 +551,21 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         lam = torch.full((c["H"],), 0.6, dtype=torch.float32, device=dev)
         li = da.diffattn_lambda_init(c["layer"])
         out = torch.empty((c["B"], c["N"], c["H"], c["dv"]), dtype=torch.bfloat16, device=dev)
-
-        def f8step():
-            da.diffattn_fwd_fp8(q8, k8, inp.v, lam, qs, ks, li, out=out)
-
-        for _ in range(args.warmup):
-            f8step()
-        barrier()
-        n_steps = max(5, min(200, args.steps))
-        evs = [(ev(), ev()) for _ in range(n_steps)]
-        for i in range(n_steps):
-            evs[i][0].record(stream)
-            f8step()
-            evs[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-        f8flops = prefill_flops()
-        f8tf = f8flops / (ms * 1e-3) / 1e12
-        # 1024 of the 1536 flops per pair are score products on the fp8 tensor cores (twice the
-        # bf16 rate by the nominal ratio), 512 the bf16 product with V: blended peak 1.5x bf16
-        blend = 1.5 * peak_tf
-        line["prefill_fp8"] = {
-            "metric": "DiffAttn fwd TFLOP/s", "value": world * f8tf, "unit": "TFLOP/s",
-            "ms_per_call": ms,
-            "workload": "prefill_3b (B4 N4096 H12 d128 dv256 causal) with fp8 e4m3 q and k "
-                        "(per-tensor absmax scale), bf16 v and output",
-            "roofline": {"bound": "tensor", "achieved": f8tf, "peak": blend, "unit": "TFLOP/s",
-                         "frac": f8tf / blend, "flops_per_launch": f8flops,
-                         "peak_source": "1.5 x bf16_tflops_sustained: scores at the fp8 rate "
-                                        "(2x bf16, nominal ratio), the V product at the bf16 rate"},
-            "gpu_launches": n_steps}
+        t = timer(lambda: da.diffattn_fwd_fp8(q8, k8, inp.v, lam, qs, ks, li, out=out),
+                  max(5, min(200, args.steps)), status=status)
+        # 1024 of the 1536 flops per pair are score products at the fp8 rate (2x bf16 by the
+        # nominal ratio), 512 the bf16 product with V: blended peak 1.5x bf16
+        r = tensor_roof(prefill_flops(), t, peaks, peak_src, scale=1.5,
+                        what="scores at the fp8 rate (2x bf16, nominal ratio), V product at bf16",
+                        nominal_scale=1.5)
+        extra["prefill_fp8"] = compact(r["achieved"], "TFLOP/s", t, r,
+                                       "prefill_3b with fp8 e4m3 q, k (per-tensor scales)", world,
+                                       peak_note="blended: 1.5 x bf16")
         del inp, q8, k8, out
         torch.cuda.empty_cache()
 
     # ======================= variable-length prefill (packed sequences) =======================
-    if args.only in ("all", "varlen"):
+    if want("varlen"):
         c = PREFILL
         lens = varlen_lengths()
         total = int(sum(lens))
@@ -600,37 +576,18 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         li = da.diffattn_lambda_init(c["layer"])
         out = torch.empty((total, c["H"], c["dv"]), dtype=torch.bfloat16, device=dev)
         q, k, v = inp.q[0], inp.k[0], inp.v[0]
-
-        def vstep():
-            da.diffattn_fwd_varlen(q, k, v, cu, lam, li, max_seqlen=max(lens), out=out)
-
-        for _ in range(args.warmup):
-            vstep()
-        barrier()
         n_steps = max(5, min(50, args.steps))
-        evs = [(ev(), ev()) for _ in range(n_steps)]
-        for i in range(n_steps):
-            evs[i][0].record(stream)
-            vstep()
-            evs[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        t = timer(lambda: da.diffattn_fwd_varlen(q, k, v, cu, lam, li, max_seqlen=max(lens),
+                                                 out=out), n_steps, status=status)
         vflops = float(sum(c["H"] * causal_pairs(n) * FLOPS_PER_PAIR for n in lens))
-        vtf = vflops / (ms * 1e-3) / 1e12
-        line["varlen"] = {
-            "metric": "DiffAttn fwd TFLOP/s", "value": world * vtf, "unit": "TFLOP/s",
-            "ms_per_call": ms,
-            "workload": f"prefill_3b shapes over {len(lens)} packed sequences of mixed length "
-                        f"(seeded, {min(lens)}..{max(lens)} tokens, {total} in total), causal, H12",
-            "roofline": {"bound": "tensor", "achieved": vtf, "peak": peak_tf, "unit": "TFLOP/s",
-                         "frac": vtf / peak_tf, "flops_per_launch": vflops},
-            "gpu_launches": n_steps}
+        r = tensor_roof(vflops, t, peaks, peak_src)
+        extra["varlen"] = compact(r["achieved"], "TFLOP/s", t, r,
+                                  f"{len(lens)} packed sequences, {min(lens)}..{max(lens)} tokens "
+                                  f"({total}), causal, H12", world)
         del inp, out, q, k, v
         torch.cuda.empty_cache()
 
-        # the last 1024-token chunk of each prefill_3b prompt against its 4096 keys (queries and
-        # keys with offsets of their own)
+        # the last 1024-token chunk of each prefill_3b prompt against its 4096 keys
         Lq, Lk = 1024, c["N"]
         kin = make_prefill_inputs(c["B"], Lk, c["H"], c["d"], c["dv"], seed=8100 + rank,
                                   layer=c["layer"], device=dev)
@@ -639,33 +596,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         cu_q = torch.arange(c["B"] + 1, dtype=torch.int32, device=dev) * Lq
         cu_k = torch.arange(c["B"] + 1, dtype=torch.int32, device=dev) * Lk
         out = torch.empty((c["B"] * Lq, c["H"], c["dv"]), dtype=torch.bfloat16, device=dev)
-
-        def cstep():
-            da.diffattn_fwd_varlen_qk(q, k, v, cu_q, cu_k, lam, li, max_seqlen_q=Lq,
-                                      max_seqlen_k=Lk, out=out)
-
-        for _ in range(args.warmup):
-            cstep()
-        barrier()
-        evs = [(ev(), ev()) for _ in range(n_steps)]
-        for i in range(n_steps):
-            evs[i][0].record(stream)
-            cstep()
-            evs[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        t = timer(lambda: da.diffattn_fwd_varlen_qk(q, k, v, cu_q, cu_k, lam, li, max_seqlen_q=Lq,
+                                                    max_seqlen_k=Lk, out=out),
+                  n_steps, status=status)
         pairs = Lq * (Lk - Lq) + Lq * (Lq + 1) // 2  # query at position p sees p + 1 keys
         cflops = float(c["B"] * c["H"] * pairs * FLOPS_PER_PAIR)
-        ctf = cflops / (ms * 1e-3) / 1e12
-        line["varlen_qk"] = {
-            "metric": "DiffAttn fwd TFLOP/s", "value": world * ctf, "unit": "TFLOP/s",
-            "ms_per_call": ms,
-            "workload": f"prefill_3b prompts computed as a last chunk: B{c['B']}, {Lq} queries "
-                        f"against {Lk} keys each, causal, H12, d128, dv256",
-            "roofline": {"bound": "tensor", "achieved": ctf, "peak": peak_tf, "unit": "TFLOP/s",
-                         "frac": ctf / peak_tf, "flops_per_launch": cflops},
-            "gpu_launches": n_steps}
+        r = tensor_roof(cflops, t, peaks, peak_src)
+        extra["varlen_qk"] = compact(r["achieved"], "TFLOP/s", t, r,
+                                     f"last {Lq}-query chunk of B{c['B']} prompts over {Lk} keys",
+                                     world)
 
         # the same chunk with the prompts' keys in a pool of 256-token pages in a random order
         ps = 256
@@ -679,36 +618,18 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         k_pool = k_pool[torch.argsort(table.flatten())].contiguous()
         v_pool = v_pool[torch.argsort(table.flatten())].contiguous()
         sk = torch.full((c["B"],), Lk, dtype=torch.int32, device=dev)
-
-        def pstep():
-            da.diffattn_fwd_paged(q, k_pool, v_pool, cu_q, sk, table, lam, li, max_seqlen_q=Lq,
-                                  max_seqlen_k=Lk, out=out)
-
-        for _ in range(args.warmup):
-            pstep()
-        barrier()
-        evs = [(ev(), ev()) for _ in range(n_steps)]
-        for i in range(n_steps):
-            evs[i][0].record(stream)
-            pstep()
-            evs[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-        ptf = cflops / (ms * 1e-3) / 1e12
-        line["paged_prefill"] = {
-            "metric": "DiffAttn fwd TFLOP/s", "value": world * ptf, "unit": "TFLOP/s",
-            "ms_per_call": ms,
-            "workload": f"the varlen_qk chunk with the keys in {ps}-token pages placed in a random "
-                        "order in the pool",
-            "roofline": {"bound": "tensor", "achieved": ptf, "peak": peak_tf, "unit": "TFLOP/s",
-                         "frac": ptf / peak_tf, "flops_per_launch": cflops},
-            "gpu_launches": n_steps}
+        t = timer(lambda: da.diffattn_fwd_paged(q, k_pool, v_pool, cu_q, sk, table, lam, li,
+                                                max_seqlen_q=Lq, max_seqlen_k=Lk, out=out),
+                  n_steps, status=status)
+        r = tensor_roof(cflops, t, peaks, peak_src)
+        extra["paged_prefill"] = compact(r["achieved"], "TFLOP/s", t, r,
+                                         f"the varlen_qk chunk, keys in shuffled {ps}-token pages",
+                                         world)
         del kin, out, q, k, v, k_pool, v_pool, table
         torch.cuda.empty_cache()
 
     # ======================= training step: forward (saving statistics) + backward ==========
-    if args.only in ("all", "backward"):
+    if want("backward"):
         c = PREFILL
         inp = make_prefill_inputs(c["B"], c["N"], c["H"], c["d"], c["dv"], seed=7000 + rank,
                                   layer=c["layer"], device=dev)
@@ -732,40 +653,17 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             da.diffattn_bwd(inp.q, inp.k, inp.v, saved["o_pre"], saved["stats"], dy, lam, li,
                             norm_weight=w, workspace=ws, grads=grads)
 
-        for _ in range(args.warmup):
-            fwd()
-            bwd()
-        barrier()
         n_steps = max(3, min(20, args.steps))
-        ev_f = [(ev(), ev()) for _ in range(n_steps)]
-        ev_b = [(ev(), ev()) for _ in range(n_steps)]
-        for i in range(n_steps):
-            ev_f[i][0].record(stream)
-            fwd()
-            ev_f[i][1].record(stream)
-            ev_b[i][0].record(stream)
-            bwd()
-            ev_b[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        fms = statistics.mean(a.elapsed_time(b) for a, b in ev_f)
-        bms = statistics.mean(a.elapsed_time(b) for a, b in ev_b)
+        tf_ = timer(fwd, n_steps, status=status)
+        tb = timer(bwd, n_steps, status=status)
         pairs = c["B"] * c["H"] * causal_pairs(c["N"])
         bflops = float(pairs * BWD_FLOPS_PER_PAIR)
-        btf = bflops / (bms * 1e-3) / 1e12
-        line["backward"] = {
-            "metric": "DiffAttn bwd TFLOP/s", "value": world * btf, "unit": "TFLOP/s",
-            "ms_per_call": bms, "fwd_train_ms": fms,
-            "workload": "prefill_3b training step: B4 N4096 H12 d128 dv256 causal, norm + scale; "
-                        "forward with saved statistics, then every gradient",
-            "roofline": {"bound": "tensor", "achieved": btf, "peak": peak_tf, "unit": "TFLOP/s",
-                         "frac": btf / peak_tf, "flops_per_launch": bflops,
-                         "flops_per_pair": BWD_FLOPS_PER_PAIR,
-                         "issued_flops_per_pair": BWD_ISSUED_FLOPS_PER_PAIR,
-                         "traffic": profiled_traffic("backward_dkdq_3b.md",
-                                                     source_sha(["backward.cu", "ptx.cuh"])),
-                         "traffic_kernel": "bwd_dkdq_kernel (the largest of the five)"},
-            "gpu_launches": 5 * n_steps}
+        r = tensor_roof(bflops, tb, peaks, peak_src)
+        extra["backward"] = compact(
+            r["achieved"], "TFLOP/s", tb, r,
+            "prefill_3b training: every gradient (2560 flops per causal pair)", world,
+            fwd_train_ms=round(tf_["ms"], 4),
+            traffic=profiled_traffic("backward_dkdq_3b.md", source_sha(["backward.cu", "ptx.cuh"])))
         del inp, dy, saved, grads, ws
         torch.cuda.empty_cache()
 
@@ -786,187 +684,37 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                      dlam=torch.empty(c["H"], dtype=torch.float32, device=dev),
                      dw=torch.empty(c["dv"], dtype=torch.float32, device=dev))
-
-        def bwd_packed():
-            da.diffattn_bwd_varlen(q, k, v, o_pre, stats, dyp, cu, lam, li, max_seqlen=mx,
-                                   norm_weight=w, workspace=ws, grads=grads)
-
-        for _ in range(args.warmup):
-            bwd_packed()
-        barrier()
-        evs = [(ev(), ev()) for _ in range(n_steps)]
-        for i in range(n_steps):
-            evs[i][0].record(stream)
-            bwd_packed()
-            evs[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        t = timer(lambda: da.diffattn_bwd_varlen(q, k, v, o_pre, stats, dyp, cu, lam, li,
+                                                 max_seqlen=mx, norm_weight=w, workspace=ws,
+                                                 grads=grads), n_steps, status=status)
         vflops = float(sum(c["H"] * causal_pairs(n) * BWD_FLOPS_PER_PAIR for n in lens))
-        vtf = vflops / (ms * 1e-3) / 1e12
-        line["backward_varlen"] = {
-            "metric": "DiffAttn bwd TFLOP/s", "value": world * vtf, "unit": "TFLOP/s",
-            "ms_per_call": ms,
-            "workload": f"backward over {len(lens)} packed sequences of mixed length ({min(lens)}.."
-                        f"{max(lens)} tokens, {total} in total), causal, H12, norm + scale",
-            "roofline": {"bound": "tensor", "achieved": vtf, "peak": peak_tf, "unit": "TFLOP/s",
-                         "frac": vtf / peak_tf, "flops_per_launch": vflops},
-            "gpu_launches": 5 * n_steps}
+        r = tensor_roof(vflops, t, peaks, peak_src)
+        extra["backward_varlen"] = compact(r["achieved"], "TFLOP/s", t, r,
+                                           f"backward over the {len(lens)} packed sequences", world)
         del pin, q, k, v, dyp, o_pre, stats, ws, grads
         torch.cuda.empty_cache()
 
-    # ======================= V2 decode =======================
-    if args.only in ("all", "v2_decode"):
-        c = dict(V2_DECODE, B=args.decode_batch)
-        vd = make_v2_decode_inputs(c["B"], c["L"], c["Hq"], c["Hkv"], c["d"], seed=5000 + rank,
-                                   device=dev)
-        ws = torch.empty(da.diffattn_v2_decode_workspace_size(c["B"], c["L"], c["Hq"], c["Hkv"],
-                                                              c["d"]), dtype=torch.uint8, device=dev)
-        vdout = torch.empty((c["B"], c["Hq"] // 2, c["d"]), dtype=torch.bfloat16, device=dev)
-
-        def v2dec():
-            da.diffattn_v2_decode(vd.q, vd.k_cache, vd.v_cache, vd.lam_logit, workspace=ws,
-                                  out=vdout)
-
-        for _ in range(args.warmup):
-            v2dec()
-        barrier()
-        n_steps = max(5, min(50, args.steps))
-        evs = [(ev(), ev()) for _ in range(n_steps)]
-        for i in range(n_steps):
-            evs[i][0].record(stream)
-            v2dec()
-            evs[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-        nbytes = v2_decode_bytes(c)
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        line["v2_decode"] = {
-            "metric": "V2 decode HBM GB/s", "value": world * gbs, "unit": "GB/s", "ms_per_call": ms,
-            "workload": f"v2_decode_32k: B{c['B']}, one query per sequence, cache 32768, Hq64 "
-                        "(32 pairs) over Hkv8, d128, bf16 (cache 8.6 GB at B64, larger than L2)",
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                         "frac": gbs / hbm,
-                         "traffic": profiled_traffic("v2_decode_32k.md",
-                                                     source_sha(["decode_v2_tc.cu", "ptx.cuh"])),
-                         "bytes_per_launch": nbytes,
-                         "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
-                         "timed": "diffattn_v2_decode call (split kernel + combine kernel)"},
-            "gpu_launches": 2 * n_steps}
-
-        # fp8 e4m3 q and K cache (per-tensor scales), V bf16: 3/4 of the bytes for every key
-        q8, qds = to_fp8_e4m3(vd.q)
-        k8, kds = to_fp8_e4m3(vd.k_cache)
-
-        def v2dec8():
-            da.diffattn_v2_decode_fp8(q8, k8, vd.v_cache, vd.lam_logit, qds, kds, workspace=ws,
-                                      out=vdout)
-
-        for _ in range(args.warmup):
-            v2dec8()
-        barrier()
-        evs = [(ev(), ev()) for _ in range(n_steps)]
-        for i in range(n_steps):
-            evs[i][0].record(stream)
-            v2dec8()
-            evs[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        ms8 = statistics.mean(a.elapsed_time(b) for a, b in evs)
-        nbytes8 = nbytes * 3 / 4
-        gbs8 = nbytes8 / (ms8 * 1e-3) / 1e9
-        line["v2_decode_fp8"] = {
-            "metric": "V2 decode HBM GB/s", "value": world * gbs8, "unit": "GB/s",
-            "ms_per_call": ms8, "speedup_vs_bf16_cache": ms / ms8,
-            "workload": f"v2_decode_32k with fp8 e4m3 q and K cache (per-tensor scales), bf16 V",
-            "roofline": {"bound": "hbm", "achieved": gbs8, "peak": hbm, "unit": "GB/s",
-                         "frac": gbs8 / hbm, "bytes_per_launch": nbytes8,
-                         "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
-                         "timed": "diffattn_v2_decode_fp8 call (split kernel + combine kernel)"},
-            "gpu_launches": 2 * n_steps}
-        del q8, k8
-
-        # the same cache as pools of pages placed in a random order: 64-token pages (one TMA box
-        # per 64 keys) and 16-token pages (the smallest box the tensor-core kernel takes)
-        paged = {}
-        for ps in (64, 16):
-            mp = c["L"] // ps
-            k_pool = vd.k_cache.view(c["B"] * mp, ps, c["Hkv"], c["d"])
-            v_pool = vd.v_cache.view(c["B"] * mp, ps, c["Hkv"], c["d"])
-            gp = torch.Generator(device="cpu")
-            gp.manual_seed(5100 + ps + rank)
-            table = torch.randperm(c["B"] * mp, generator=gp).to(torch.int32).view(c["B"], mp).to(dev)
-
-            def v2dec_paged():
-                da.diffattn_v2_decode_paged(vd.q, k_pool, v_pool, table, vd.seqlens, vd.lam_logit,
-                                            workspace=ws, out=vdout)
-
-            for _ in range(args.warmup):
-                v2dec_paged()
-            barrier()
-            evs = [(ev(), ev()) for _ in range(n_steps)]
-            for i in range(n_steps):
-                evs[i][0].record(stream)
-                v2dec_paged()
-                evs[i][1].record(stream)
-            barrier()
-            da.diffattn_device_status()
-            pms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-            pgbs = nbytes / (pms * 1e-3) / 1e9
-            paged[f"page_{ps}"] = {"value": world * pgbs, "ms_per_call": pms, "frac": pgbs / hbm}
-            del k_pool, v_pool, table
-        line["v2_decode_paged"] = {
-            "metric": "V2 decode HBM GB/s", "unit": "GB/s",
-            "value": paged["page_64"]["value"], "ms_per_call": paged["page_64"]["ms_per_call"],
-            "workload": f"v2_decode_32k over a paged cache: B{c['B']}, cache 32768 in pages placed "
-                        "in a random order in the pool, Hq64 over Hkv8, d128, bf16",
-            "page_sizes": paged,
-            "roofline": {"bound": "hbm", "achieved": paged["page_64"]["value"] / world, "peak": hbm,
-                         "unit": "GB/s", "frac": paged["page_64"]["frac"],
-                         "bytes_per_launch": nbytes,
-                         "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
-                         "timed": "diffattn_v2_decode_paged call, 64-token pages (split kernel + "
-                                  "combine kernel)"},
-            "gpu_launches": 2 * n_steps * len(paged)}
-        del vd, ws, vdout
-        torch.cuda.empty_cache()
-
     # ======================= grouped: signal heads sharing noise heads =======================
-    if args.only in ("all", "gda"):
+    if want("gda"):
         gc = GDA
         ginp = make_gda_inputs(gc["B"], gc["N"], gc["Hs"], gc["Hn"], gc["d"], gc["dv"],
                                seed=5000 + rank, device=dev)
         gout = torch.empty((gc["B"], gc["N"], gc["Hs"], gc["dv"]), dtype=torch.bfloat16, device=dev)
         li_g = da.diffattn_lambda_init(gc["layer"])
-
-        def gda():
-            da.diffattn_gda_fwd(ginp.q, ginp.k, ginp.v, ginp.lam, gc["Hs"], li_g, out=gout)
-
-        for _ in range(args.warmup):
-            gda()
-        barrier()
-        gsteps = max(5, min(50, args.steps))
-        g_ev = [(ev(), ev()) for _ in range(gsteps)]
-        for i in range(gsteps):
-            g_ev[i][0].record(stream)
-            gda()
-            g_ev[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        gms = statistics.mean(a.elapsed_time(b) for a, b in g_ev)
-        gflops = float(gc["B"] * gc["Hs"] * causal_pairs(gc["N"]) * FLOPS_PER_PAIR)
-        gtf = gflops / (gms * 1e-3) / 1e12
-        line["gda_prefill"] = {
-            "metric": "DiffAttn fwd TFLOP/s", "value": world * gtf, "unit": "TFLOP/s",
-            "ms_per_call": gms,
-            "workload": "gda_prefill_3b: B4 N4096, 12 signal heads over 3 noise heads (4 per noise "
-                        "head), d128 dv256 causal, RMSNorm + scale",
-            "roofline": {"bound": "tensor", "achieved": gtf, "peak": peak_tf, "unit": "TFLOP/s",
-                         "frac": gtf / peak_tf, "flops_per_launch": gflops,
-                         "flops_per_pair": FLOPS_PER_PAIR,
-                         "note": "MMA flops issued: each signal head's CTA recomputes its noise map"},
-            "gpu_launches": gsteps}
+        t = timer(lambda: da.diffattn_gda_fwd(ginp.q, ginp.k, ginp.v, ginp.lam, gc["Hs"], li_g,
+                                              out=gout), max(5, min(50, args.steps)), status=status)
+        pairs = float(gc["B"] * gc["Hs"] * causal_pairs(gc["N"]))
+        G = gc["Hs"] // gc["Hn"]
+        # the method's own MMA work per (signal head, causal pair): its map's scores (2d), the
+        # noise map's scores once per group (2d / G) and both maps' products with V (4dv)
+        method_per_pair = 2 * gc["d"] + 2 * gc["d"] / G + 4 * gc["dv"]
+        r = tensor_roof(pairs * method_per_pair, t, peaks, peak_src)
+        issued = pairs * FLOPS_PER_PAIR / (t["ms"] * 1e-3) / 1e12
+        extra["gda_prefill"] = compact(r["achieved"], "TFLOP/s", t, r,
+                                       "prefill_3b with 12 signal heads over 3 noise heads", world,
+                                       flops_per_pair=method_per_pair,
+                                       issued_tflops=round(issued, 1),
+                                       issued_flops_per_pair=FLOPS_PER_PAIR)
         del ginp, gout
         torch.cuda.empty_cache()
 
@@ -976,46 +724,134 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         gws = torch.empty(da.diffattn_decode_workspace_size(gd["B"], gd["L"], gd["Hs"]),
                           dtype=torch.uint8, device=dev)
         gdout = torch.empty((gd["B"], gd["Hs"], gd["dv"]), dtype=torch.bfloat16, device=dev)
-
-        def gdec():
-            da.diffattn_gda_decode(gdi.q, gdi.k_cache, gdi.v_cache, gdi.lam, gd["Hs"], li_g,
-                                   workspace=gws, out=gdout)
-
-        for _ in range(args.warmup):
-            gdec()
-        barrier()
-        gdsteps = max(5, min(50, args.steps))
-        gd_ev = [(ev(), ev()) for _ in range(gdsteps)]
-        for i in range(gdsteps):
-            gd_ev[i][0].record(stream)
-            gdec()
-            gd_ev[i][1].record(stream)
-        barrier()
-        da.diffattn_device_status()
-        gdms = statistics.mean(a.elapsed_time(b) for a, b in gd_ev)
+        t = timer(lambda: da.diffattn_gda_decode(gdi.q, gdi.k_cache, gdi.v_cache, gdi.lam,
+                                                 gd["Hs"], li_g, workspace=gws, out=gdout),
+                  max(5, min(50, args.steps)), status=status)
         gdbytes = gda_decode_bytes(gd)
-        dsha_g = source_sha(["decode.cu", "ptx.cuh"])
-        gdgbs = gdbytes / (gdms * 1e-3) / 1e9
-        line["gda_decode"] = {
-            "metric": "decode HBM GB/s", "value": world * gdgbs, "unit": "GB/s", "ms_per_call": gdms,
-            "workload": f"gda_decode_32k: B{gd['B']}, one query per sequence, cache 32768, 12 "
-                        "signal heads over 3 noise heads, d128, dv256, bf16 (cache 20.9 GB at B64)",
-            "roofline": {"bound": "hbm", "achieved": gdgbs, "peak": hbm, "unit": "GB/s",
-                         "frac": gdgbs / hbm, "bytes_per_launch": gdbytes,
-                         "traffic": profiled_traffic("gda_decode_32k.md", dsha_g),
-                         "peak_source": f"hbm_gbs of {peak_src} (copy, read+write)",
-                         "timed": "diffattn_gda_decode call (group kernel + combine kernel); a "
-                                  "noise row serves the 4 signal heads of its group from L1"},
-            "gpu_launches": 2 * gdsteps}
+        r = hbm_roof(gdbytes, t, peaks, peak_src)
+        extra["gda_decode"] = compact(r["achieved"], "GB/s", t, r,
+                                      f"decode_32k with 12 signal heads over 3 noise heads, B{gd['B']}",
+                                      world, traffic=profiled_traffic(
+                                          "gda_decode_32k.md", source_sha(["decode.cu", "ptx.cuh"])))
         del gdi, gws, gdout
         torch.cuda.empty_cache()
 
+    # ======================= V2 decode =======================
+    if want("v2_decode"):
+        c = dict(V2_DECODE, B=args.decode_batch)
+        vd = make_v2_decode_inputs(c["B"], c["L"], c["Hq"], c["Hkv"], c["d"], seed=5000 + rank,
+                                   device=dev)
+        ws = torch.empty(da.diffattn_v2_decode_workspace_size(c["B"], c["L"], c["Hq"], c["Hkv"],
+                                                              c["d"]), dtype=torch.uint8, device=dev)
+        vdout = torch.empty((c["B"], c["Hq"] // 2, c["d"]), dtype=torch.bfloat16, device=dev)
+        n_steps = max(5, min(50, args.steps))
+        t = timer(lambda: da.diffattn_v2_decode(vd.q, vd.k_cache, vd.v_cache, vd.lam_logit,
+                                                workspace=ws, out=vdout), n_steps, status=status)
+        nbytes = v2_decode_bytes(c)
+        r = hbm_roof(nbytes, t, peaks, peak_src)
+        extra["v2_decode"] = compact(r["achieved"], "GB/s", t, r,
+                                     f"B{c['B']} cache 32768, Hq64 over Hkv8, d128", world,
+                                     traffic=profiled_traffic(
+                                         "v2_decode_32k.md", source_sha(["decode_v2_tc.cu", "ptx.cuh"])))
+
+        # fp8 e4m3 q and K cache (per-tensor scales), V bf16: 3/4 of the bytes for every key
+        q8, qds = to_fp8_e4m3(vd.q)
+        k8, kds = to_fp8_e4m3(vd.k_cache)
+        t8 = timer(lambda: da.diffattn_v2_decode_fp8(q8, k8, vd.v_cache, vd.lam_logit, qds, kds,
+                                                     workspace=ws, out=vdout), n_steps, status=status)
+        r8 = hbm_roof(nbytes * 3 / 4, t8, peaks, peak_src)
+        extra["v2_decode_fp8"] = compact(r8["achieved"], "GB/s", t8, r8,
+                                         "v2_decode_32k, fp8 e4m3 q and K cache, bf16 V", world,
+                                         speedup_vs_bf16_cache=round(t["ms"] / t8["ms"], 3))
+        del q8, k8
+
+        # the same cache as pools of pages placed in a random order
+        for ps in (64, 16):
+            mp = c["L"] // ps
+            k_pool = vd.k_cache.view(c["B"] * mp, ps, c["Hkv"], c["d"])
+            v_pool = vd.v_cache.view(c["B"] * mp, ps, c["Hkv"], c["d"])
+            gp = torch.Generator(device="cpu")
+            gp.manual_seed(5100 + ps + rank)
+            table = torch.randperm(c["B"] * mp, generator=gp).to(torch.int32).view(c["B"], mp).to(dev)
+            tp = timer(lambda: da.diffattn_v2_decode_paged(vd.q, k_pool, v_pool, table, vd.seqlens,
+                                                           vd.lam_logit, workspace=ws, out=vdout),
+                       n_steps, status=status)
+            rp = hbm_roof(nbytes, tp, peaks, peak_src)
+            extra[f"v2_decode_paged_{ps}"] = compact(rp["achieved"], "GB/s", tp, rp,
+                                                     f"v2_decode_32k in shuffled {ps}-token pages",
+                                                     world)
+            del k_pool, v_pool, table
+        del vd, ws, vdout
+        torch.cuda.empty_cache()
+
+    # ======================= decode (config of the metric's second half) =======================
+    if want("decode"):
+        dcfg = dict(DECODE, B=args.decode_batch)
+        dinp = make_decode_inputs(dcfg["B"], dcfg["L"], dcfg["H"], dcfg["d"], dcfg["dv"],
+                                  seed=2000 + rank, device=dev)
+        ws = torch.empty(da.diffattn_decode_workspace_size(dcfg["B"], dcfg["L"], dcfg["H"]),
+                         dtype=torch.uint8, device=dev)
+        dout = torch.empty((dcfg["B"], dcfg["H"], dcfg["dv"]), dtype=torch.bfloat16, device=dev)
+        li_dec = da.diffattn_lambda_init(dcfg["layer"])
+        dbytes = decode_bytes(dcfg)
+
+        # the same cache as a pool of 64-token pages, each sequence's pages scattered over it
+        ps = 64
+        mp = dcfg["L"] // ps
+        k_pool = dinp.k_cache.view(dcfg["B"] * mp, ps, dcfg["H"], 2 * dcfg["d"])
+        v_pool = dinp.v_cache.view(dcfg["B"] * mp, ps, dcfg["H"], dcfg["dv"])
+        gp = torch.Generator(device="cpu")
+        gp.manual_seed(2100 + rank)
+        table = torch.randperm(dcfg["B"] * mp, generator=gp).to(torch.int32).view(dcfg["B"], mp).to(dev)
+        tp = timer(lambda: da.diffattn_decode_paged(dinp.q, k_pool, v_pool, table, dinp.seqlens,
+                                                    dinp.lam, li_dec, workspace=ws, out=dout),
+                   max(5, min(50, args.steps)), status=status)
+        rp = hbm_roof(dbytes, tp, peaks, peak_src)
+        extra["decode_paged"] = compact(rp["achieved"], "GB/s", tp, rp,
+                                        "decode_32k in shuffled 64-token pages", world)
+
+        # the headline decode loop: long enough (>= ~0.7 s) for its own clock record; the 25.8 GB
+        # cache is 200x the L2, so every call streams it from HBM
+        n_dec = max(5, min(200, 10 * args.steps))
+        t = timer(lambda: da.diffattn_decode(dinp.q, dinp.k_cache, dinp.v_cache, dinp.lam, li_dec,
+                                             workspace=ws, out=dout), n_dec, clocks=True,
+                  status=status)
+        dms = max_over_ranks(t["ms"])
+        t["ms"] = dms
+        r = hbm_roof(dbytes, t, peaks, peak_src)
+        r.update({"traffic": profiled_traffic("decode_32k.md", source_sha(["decode.cu", "ptx.cuh"])),
+                  "bytes_per_launch": dbytes})
+        decode_blk = {
+            "metric": "decode HBM GB/s", "value": world * r["achieved"], "unit": "GB/s",
+            "ms_per_call": dms, "calls": n_dec,
+            "workload": f"decode_32k: B{dcfg['B']} x 1 query, cache 32768, H12, d128, dv256, bf16 "
+                        "(25.8 GB, read once per call)",
+            "frac": r["frac"], "frac_nominal": r["frac_nominal"],
+            "roofline": r, "clocks": t["clocks"], "gpu_launches": 2 * n_dec}
+        del dinp, ws, dout, k_pool, v_pool, table
+        torch.cuda.empty_cache()
+
     # ======================= CPU baseline (rank 0, N = 1 only) =======================
-    line["cpu_baseline"] = None
+    cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":
         v, cores, desc, _, _ = oracle_sample(args.cpu_seconds)
-        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                                "sample": desc}
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    # the secondary workloads first, then the CPU baseline, the headline figures, and the
+    # decode block last (the end of the line is what a truncated log keeps)
+    line.update(extra)
+    line["cpu_baseline"] = cpu
+    head = {}
+    if line.get("roofline"):
+        head.update({"prefill_3b_tflops": round(line["roofline"]["achieved"], 1),
+                     "prefill_frac": round(line["roofline"]["frac"], 4),
+                     "prefill_frac_nominal": round(line["roofline"]["frac_nominal"], 4)})
+    if decode_blk:
+        head.update({"decode_32k_gbs": round(decode_blk["value"], 1),
+                     "decode_frac": round(decode_blk["frac"], 4),
+                     "decode_frac_nominal": round(decode_blk["frac_nominal"], 4)})
+    line["headline"] = head
+    line["decode"] = decode_blk
     if rank == 0:
         print(json.dumps(line), flush=True)
 
