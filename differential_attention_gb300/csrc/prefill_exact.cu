@@ -185,21 +185,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = !causal ? n_kv_all
                         : KMODE != kKeysShared ? min((qoff + (qt + 1) * BM + BN - 1) / BN, n_kv_all)
                                : min(qt + 1, n_kv_all);  // BM == BN
-  const int T = 2 * n;  // tiles over both passes
+  // W1: pass 1 runs over 256-key tiles (one N = 256 score MMA per map and k-step instead of two
+  // N = 128 ones: a tcgen05.mma's cost grows far less than its N). Only S1 and S2 live in pass 1,
+  // so each map's 256 score columns take half of tensor memory, single-buffered. The shared-K
+  // (V2), fp8 and d = 64 forms keep 128-key tiles in both passes (a 256-row chunk of K is one
+  // 32 KB ring slot at d = 128).
+  constexpr bool W1 = !SHARED_K && !QK8 && DQK == 128;
+  static_assert(!W1 || C::kSlot >= 2 * C::kChunk, "a 256-row K chunk fills one ring slot");
+  const int n1 = W1 ? (n + 1) / 2 : n;  // pass-1 tiles (the last one 128 keys wide when n is odd)
+  const int T = n1 + n;                 // tiles over both passes
 
-  // Ring order of the loads = the order in which the MMA issuer consumes them. Iteration t of
-  // the issuer uses the K loads of tile t (one per map, or one shared K) and then, for t > n,
-  // the two V halves of pass-2 tile jv = t - 1 - n. base(t) = index of iteration t's first load.
+  // Ring order of the loads = the order in which the MMA issuer consumes them. Iteration t < n1
+  // of the issuer uses the K loads of pass-1 tile t: with W1 one per map and 64-column chunk
+  // (each a slot of 256 key rows), else one per map (or one shared K). Iteration t >= n1 uses
+  // the K loads of pass-2 tile t - n1 (one per map, both chunks of 128 rows), then for t > n1
+  // the two V halves of pass-2 tile jv = t - 1 - n1. base(t) = index of iteration t's first load.
   constexpr int KL = C::kKLoads;
-  auto base = [n](int t) { return t * KL + 2 * max(0, t - n - 1); };
+  constexpr int KL1 = W1 ? 4 : KL;
+  auto base = [n1](int t) {
+    return t <= n1 ? KL1 * t : KL1 * n1 + KL + (KL + 2) * (t - n1 - 1);
+  };
   auto k_load = [&](int t, int r) { return base(t) + r; };
   auto v_load = [&](int jv, int h) {
-    const int t = n + 1 + jv;
+    const int t = n1 + 1 + jv;
     return base(t) + (t < T ? KL : 0) + h;
   };
-  // TMEM score buffer of tile t and its use count on that buffer (barrier phase index).
-  auto sbuf = [n](int t) { return t < n ? (t & 1) : 0; };
-  auto suse = [n](int t) { return t < n ? (t >> 1) : ((n + 1) >> 1) + (t - n); };
+  // TMEM score buffer of tile t and its use count on that buffer (barrier phase index). With W1
+  // buffer 0 holds map 1's scores (pass 1) and both maps' (pass 2), buffer 1 map 2's (pass 1):
+  // each is used once per tile, so the use count of either is t.
+  auto sbuf = [n1](int t) { return (!W1 && t < n1) ? (t & 1) : 0; };
+  auto suse = [n1](int t) { return W1 ? t : t < n1 ? (t >> 1) : ((n1 + 1) >> 1) + (t - n1); };
 
   auto bar = [](uint64_t& x) { return smem_u32(&x); };
 
@@ -276,8 +291,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       bool ok = true;
       for (int t = 0; t <= T && ok; ++t) {
-        if (t < T) {
-          const int j = t < n ? t : t - n;
+        if (W1 && t < n1) {
+          // pass-1 tile t: keys [256 t, 256 t + 256), one slot per map and 64-column chunk,
+          // holding its 256 rows as two 128-row boxes (one when the tile is 128 keys wide)
+          const int halves = 2 * t + 1 < n ? 2 : 1;
+          const int krow0 = key_row(2 * t * BN);
+          const int krow1 = halves == 2 ? key_row((2 * t + 1) * BN) : 0;
+          for (int q = 0; q < 4 && ok; ++q) {
+            const int mp = q >> 1, c = q & 1;
+            const int ks = acquire(k_load(t, q), halves * C::kChunk);
+            if (ks < 0) {
+              ok = false;
+              break;
+            }
+            for (int hh = 0; hh < halves; ++hh)
+              tma_load_4d(sSlot + ks * C::kSlot + hh * C::kChunk, &tm_k, bar(bars.slot_full[ks]),
+                          k_col_of(P, mp) + C::kQKBoxCols * c, GROUPED ? grouped_head(P, u, mp) : kvh,
+                          hh ? krow1 : krow0, tb);
+            issued = k_load(t, q) + 1;
+          }
+        } else if (t < T) {
+          const int j = t < n1 ? t : t - n1;
           const int krow = key_row(j * BN);  // (paged: the table read overlaps the slot wait)
           for (int r = 0; r < KL && ok; ++r) {
             const int ks = acquire(k_load(t, r), C::kKLoadBytes);
@@ -293,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             issued = k_load(t, r) + 1;
           }
         }
-        if (ok && t >= n + 1) {
-          const int jv = t - n - 1;
+        if (ok && t >= n1 + 1) {
+          const int jv = t - n1 - 1;
           for (int h = 0; h < 2 && ok; ++h) {
             const int vrow = key_row(jv * BN + 64 * h);
             const int vs = acquire(v_load(jv, h), C::kVHalfBytes);
@@ -327,11 +361,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(bar(bars.q_full), 0, abrt);
       tc_fence_after();
       for (int t = 0; ok && t <= T; ++t) {
-        if (t < T) {
+        if (W1 && t < n1) {
+          // pass-1 tile t: S_r (128 x 256, or 128 x 128 for a last tile of 128 keys) into
+          // columns 256 r; each 64-column chunk's slot is released as soon as its four k-steps
+          // are done, so the next tile's load overlaps the rest of this tile's products
+          constexpr uint32_t idesc_w = umma_idesc_bf16(BM, 2 * BN, 0, 0);
+          const uint32_t idesc = 2 * t + 1 < n ? idesc_w : idesc_s;
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            if (t > 0 && !(ok = mbar_wait(bar(bars.s_free[r]), (t - 1) & 1, abrt))) break;
+            const uint64_t qd = desc_add(dq0, r * C::kQMapBytes);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int ki = k_load(t, 2 * r + c), s = ki % NSLOT;
+              if (!(ok = mbar_wait(bar(bars.slot_full[s]), (ki / NSLOT) & 1, abrt))) break;
+              tc_fence_after();
+              const uint64_t kd = desc_add(dslot0, s * C::kSlot);
+#pragma unroll
+              for (int k4 = 0; k4 < 4; ++k4)
+                mma_bf16_ss(tmem + r * 256, desc_add(qd, c * C::kChunk + k4 * 32),
+                            desc_add(kd, k4 * 32), idesc, (c > 0 || k4 > 0) ? 1u : 0u);
+              tc_commit(bar(bars.slot_empty[s]));
+            }
+            if (!ok) break;
+            tc_commit(bar(bars.s_full[r]));
+          }
+          if (!ok) break;
+        } else if (t < T) {
           const int buf = sbuf(t);
           // The buffer's previous scores must have been read by both warpgroups: tile t-2 in
-          // pass 1 (two buffers), tile t-1 in pass 2 (one buffer; reading t-1 implies t-2).
-          const int prev = t < n ? t - 2 : t - 1;
+          // pass 1 (two buffers), tile t-1 in pass 2 (one buffer; reading t-1 implies t-2; with
+          // W1 the last pass-1 tile's map-1 scores, which held these columns).
+          const int prev = t < n1 ? t - 2 : t - 1;
           if (prev >= 0 &&
               !(ok = mbar_wait(bar(bars.s_free[sbuf(prev)]), suse(prev) & 1, abrt)))
             break;
@@ -359,8 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(bar(bars.s_full[buf]));
         }
         const int tp = t - 1;
-        if (tp >= n) {
-          const int jv = tp - n;
+        if (tp >= n1) {
+          const int jv = tp - n1;
+          // O's columns held map 2's scores in the last pass-1 tile (W1): read by now
+          if (W1 && jv == 0 && !(ok = mbar_wait(bar(bars.s_free[1]), (n1 - 1) & 1, abrt))) break;
           if (!(ok = mbar_wait(bar(bars.d_full), jv & 1, abrt))) break;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -452,11 +515,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t d_row = sD + (wg >> 1) * C::kChunk + r * 128;
     const int u0 = (wg & 1) * 4;
 
+    // Pass-1 statistics over 32 scores v of one map: their sum of 2^(s c - ref), and their
+    // maximum (times c).
+    auto sum32 = [&](const uint32_t (&v)[KW], float ref) -> float {
+      const uint64_t scale2 = f2pack(sl2, sl2), off2 = f2pack(-ref, -ref);
+      uint64_t acc[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+#pragma unroll
+      for (int i = 0; i < KW; i += 2) {
+        float x0, x1;
+        f2unpack(f2fma(f2pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), scale2, off2),
+                 x0, x1);
+        acc[(i >> 1) & 1] = f2add(acc[(i >> 1) & 1], f2pack(ex2_approx(x0), ex2_approx(x1)));
+      }
+      float a0, a1, a2, a3;
+      f2unpack(acc[0], a0, a1);
+      f2unpack(acc[1], a2, a3);
+      return (a0 + a1) + (a2 + a3);
+    };
+    auto max32 = [&](const uint32_t (&v)[KW]) -> float {
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < KW; i += 2)
+        mx[(i >> 1) & 3] = fmax3(mx[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+      return fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * sl2;
+    };
+
     for (int t = 0; t < T; ++t) {
-      const bool pass2 = t >= n;
+      if (W1 && t < n1) {
+        // ---- pass 1 over 256-key tile t: keys [64 wg, 64 wg + 64) of each map, map by map ----
+        // (statistics as in the 128-key form below: a sum against the reference point m, the
+        // maximum only on a row's first tile with a visible key or when the sum passes 2^64)
+        const int wkey0 = 2 * t * BN + 2 * KW * wg;
+#pragma unroll
+        for (int mp = 0; mp < 2; ++mp) {
+          ok = mbar_wait(bar(bars.s_full[mp]), t & 1, abrt);
+          if (__any_sync(0xffffffffu, !ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t sw[2][KW];
+          const uint32_t sb = tmem + tl + mp * 256 + 2 * KW * wg;
+          tmem_ld32(sb, sw[0]);
+          tmem_ld32(sb + KW, sw[1]);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(bar(bars.s_free[mp]));  // this map's scores are in registers
+          if (wkey0 + 2 * KW > lim) {
+#pragma unroll
+            for (int i = 0; i < KW; ++i) {
+              if (wkey0 + i >= lim) sw[0][i] = __float_as_uint(-INFINITY);
+              if (wkey0 + KW + i >= lim) sw[1][i] = __float_as_uint(-INFINITY);
+            }
+          }
+          __syncwarp();
+          float sum = 0.f;
+          bool redo = m[mp] == -INFINITY;
+          if (!redo) {
+            sum = sum32(sw[0], m[mp]) + sum32(sw[1], m[mp]);
+            redo = sum > 0x1p64f;  // also true for +inf; a NaN score keeps its NaN
+          }
+          if (redo) {
+            const float mn = fmaxf(m[mp], fmaxf(max32(sw[0]), max32(sw[1])));
+            if (mn == -INFINITY) continue;  // every key so far is masked for this row
+            sum = sum32(sw[0], mn) + sum32(sw[1], mn);
+            l[mp] = l[mp] * ex2_approx(m[mp] - mn);
+            m[mp] = mn;
+          }
+          l[mp] += sum;
+        }
+        if (!ok) break;
+        continue;
+      }
+      const bool pass2 = t >= n1;
       if (pass2 && !merged) merge();
       const int buf = sbuf(t);
-      const int key0 = (pass2 ? t - n : t) * BN + KW * wg;
+      const int key0 = (pass2 ? t - n1 : t) * BN + KW * wg;
       ok = mbar_wait(bar(bars.s_full[buf]), suse(t) & 1, abrt);
       if (__any_sync(0xffffffffu, !ok)) {
         ok = false;
@@ -484,30 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The sum is taken against the running maximum m (any reference point gives the same
         // statistics: b = m + log2 l); the tile's own maximum is found only on a row's first
         // tile with a visible key, or when a score so far above m overflows the sum.
-        auto tile_sum = [&](int mp, float ref) -> float {
-          const uint64_t scale2 = f2pack(sl2, sl2), off2 = f2pack(-ref, -ref);
-          uint64_t acc[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
-#pragma unroll
-          for (int i = 0; i < KW; i += 2) {
-            float x0, x1;
-            f2unpack(f2fma(f2pack(__uint_as_float(sr[mp][i]), __uint_as_float(sr[mp][i + 1])),
-                           scale2, off2),
-                     x0, x1);
-            acc[(i >> 1) & 1] = f2add(acc[(i >> 1) & 1], f2pack(ex2_approx(x0), ex2_approx(x1)));
-          }
-          float a0, a1, a2, a3;
-          f2unpack(acc[0], a0, a1);
-          f2unpack(acc[1], a2, a3);
-          return (a0 + a1) + (a2 + a3);
-        };
-        auto tile_max = [&](int mp) -> float {
-          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int i = 0; i < KW; i += 2)
-            mx[(i >> 1) & 3] = fmax3(mx[(i >> 1) & 3], __uint_as_float(sr[mp][i]),
-                                     __uint_as_float(sr[mp][i + 1]));
-          return fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * sl2;
-        };
+        auto tile_sum = [&](int mp, float ref) -> float { return sum32(sr[mp], ref); };
+        auto tile_max = [&](int mp) -> float { return max32(sr[mp]); };
 #pragma unroll
         for (int mp = 0; mp < 2; ++mp) {
           float sum = 0.f;
@@ -527,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // ---- pass 2: D = A1 - lambda A2 in fp32, rounded once to bf16, into shared memory ----
-        const int jv = t - n;
+        const int jv = t - n1;
         const uint64_t scale2 = f2pack(sl2, sl2), bias2 = f2pack(bias[0], bias[1]);
         const uint64_t nlam2 = f2pack(-lam, -lam);
         uint32_t pk[KW / 2];
@@ -743,10 +855,12 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
   kp.n_qt = (p.N + BM - 1) / BM;
   kp.scale_log2 = kLog2e * p.scale;
   {
-    // K/V bytes one (batch, unit) pair streams; keep a group's K/V within ~64 MB of L2
+    // K/V bytes one (batch, unit) pair streams; keep a group's K/V within 32 MB of L2. Measured
+    // at the 3B-layer shape: with 32 MB DRAM reads equal q + k + v (303 MB), with 64 MB the
+    // streamed queries and outputs evict K/V tiles that later query tiles read again (408 MB)
     const int nk = (p.cu_seqlens_k || p.block_table) ? p.max_seqlen_k : p.N;
     const double kv_bytes = static_cast<double>(nk) * (p.k_cols * C::kQKElt + DV * 2.0);
-    long long g = static_cast<long long>((64.0 * 1024 * 1024) / (kv_bytes > 1 ? kv_bytes : 1));
+    long long g = static_cast<long long>((32.0 * 1024 * 1024) / (kv_bytes > 1 ? kv_bytes : 1));
     const long long bu = static_cast<long long>(p.B) * p.units;
     kp.group = static_cast<int>(g < 1 ? 1 : (g > bu ? bu : g));
   }
