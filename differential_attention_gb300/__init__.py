@@ -18,7 +18,11 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libdiffattn.so")
+# DIFFATTN_DEBUG_BUILD=1 selects the bounds-checking debug build of the same library
+# (libdiffattn_debug.so: every kernel checks its tile coordinates and row indices and reports a
+# failure through diffattn_device_status); the default is the release build.
+DEBUG_BUILD = os.environ.get("DIFFATTN_DEBUG_BUILD", "0") == "1"
+LIB_PATH = os.path.join(_PKG, "libdiffattn_debug.so" if DEBUG_BUILD else "libdiffattn.so")
 
 DIFFATTN_OK = 0
 DIFFATTN_BF16 = 0
@@ -156,9 +160,10 @@ def lib() -> ctypes.CDLL:
 
 
 def build(force: bool = False) -> str:
-    """Compile libdiffattn.so for sm_103a if it is missing or stale (see builder.py)."""
+    """Compile libdiffattn.so (libdiffattn_debug.so with DIFFATTN_DEBUG_BUILD=1) for sm_103a if it
+    is missing or stale (see builder.py)."""
     from .builder import build_library
-    return build_library(force=force)
+    return build_library(force=force, debug=DEBUG_BUILD)
 
 
 def _check(rc: int):

@@ -56,6 +56,7 @@ constexpr int kPrefillFlags =
 }  // namespace
 
 constexpr int DEV_BAD_INDEX_BIT = 2;  // the kernels' DEV_BAD_INDEX status bit
+constexpr int DEV_BOUNDS_BIT = 4;     // DEV_BOUNDS: a debug-build bounds check failed
 
 extern "C" {
 
@@ -79,6 +80,10 @@ DIFFATTN_API int diffattn_device_status(void* stream) {
   if (e == cudaSuccess) e = da::status_decode(&dd);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
   v |= w | x | y | z | dd;
+  if (v & DEV_BOUNDS_BIT)
+    return fail(DIFFATTN_ERR_INDEX,
+                "a debug-build bounds check failed: a tile coordinate or row index was outside "
+                "its tensor (status %d)", v);
   if (v & DEV_BAD_INDEX_BIT)
     return fail(DIFFATTN_ERR_INDEX, "a block-table entry was outside [0, num_pages) (status %d)", v);
   if (v != 0) return fail(DIFFATTN_ERR_TIMEOUT, "a bounded wait inside a kernel ran out (status %d)", v);

@@ -51,6 +51,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
+// bulk_load of n floats at element offset `off` of an fp32 array of `total` elements. Debug
+// builds check the range; a failed check loads from offset 0, so the barrier still completes.
+__device__ __forceinline__ void bulk_load_f32(uint32_t dst, const float* base, size_t off,
+                                              size_t total, uint32_t n, uint32_t bar) {
+  if constexpr (kDebugChecks) {
+    if (off + n > total) {
+      flag_device_error(DEV_BOUNDS);
+      off = 0;
+    }
+  }
+  bulk_load(dst, base + off, n * 4, bar);
+}
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
                "f"(c), "f"(d)
@@ -165,6 +177,12 @@ __device__ __forceinline__ bool seq_rows(const Args& a, int b, SeqRows& s) {
   s.trow = s.s0;
   s.tb = 0;
   return s.s0 >= 0 && s.len >= 0 && s.len <= a.N && s.s0 <= a.total - s.len;
+}
+
+// Extent of the tensor maps over [B, N, H, cols] (packed: one batch row of `total` tokens), for
+// the debug-build checks of tile coordinates.
+__device__ __forceinline__ Ext4 map_ext(const Args& a, int cols, int elt) {
+  return Ext4{cols, a.H, a.cu ? a.total : a.N, a.cu ? 1 : a.B, elt};
 }
 
 // =============================================================================================
@@ -354,8 +372,8 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
       prefetch_tmap(&tm_vh);
       mbar_arrive_expect_tx(bar(cs.q_full), 2 * kBox);
       for (int c = 0; c < 2; ++c)
-        tma_load_4d(sQ + c * kBox, &tm_q, bar(cs.q_full), kD + 64 * c, h, sq.trow + qt * kT,
-                    sq.tb);
+        tma_load_4d_chk(sQ + c * kBox, &tm_q, bar(cs.q_full), kD + 64 * c, h, sq.trow + qt * kT,
+                    sq.tb, map_ext(a, 2 * kD, 2));
       int issued = 0;
       bool ok = true;
       auto acquire = [&](int idx, uint32_t bytes) -> int {
@@ -370,8 +388,8 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
           const int s = acquire(idx, 2 * kBox);
           if (s < 0) { ok = false; break; }
           for (int c = 0; c < 2; ++c)
-            tma_load_4d(sRing + s * kSlot + c * kBox, &tm_k, bar(cs.slot_full[s]), kD + 64 * c, h,
-                        sq.trow + t * kT, sq.tb);
+            tma_load_4d_chk(sRing + s * kSlot + c * kBox, &tm_k, bar(cs.slot_full[s]), kD + 64 * c, h,
+                        sq.trow + t * kT, sq.tb, map_ext(a, 2 * kD, 2));
           issued = ++idx;
         }
         if (t >= 1) {
@@ -379,8 +397,8 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
             const int s = acquire(idx, 4 * kVHalfBox);
             if (s < 0) { ok = false; break; }
             for (int c = 0; c < 4; ++c)
-              tma_load_4d(sRing + s * kSlot + c * kVHalfBox, &tm_vh, bar(cs.slot_full[s]), 64 * c,
-                          h, sq.trow + (t - 1) * kT + 64 * hf, sq.tb);
+              tma_load_4d_chk(sRing + s * kSlot + c * kVHalfBox, &tm_vh, bar(cs.slot_full[s]), 64 * c,
+                          h, sq.trow + (t - 1) * kT + 64 * hf, sq.tb, map_ext(a, kDV, 2));
             issued = ++idx;
           }
         }
@@ -637,10 +655,10 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       prefetch_tmap(&tm_do);
       mbar_arrive_expect_tx(bar(cs.kv_full), 6 * kBox);
       for (int c = 0; c < 2; ++c)
-        tma_load_4d(sK + c * kBox, &tm_k, bar(cs.kv_full), m * kD + 64 * c, h, sq.trow + j * kT,
-                    sq.tb);
+        tma_load_4d_chk(sK + c * kBox, &tm_k, bar(cs.kv_full), m * kD + 64 * c, h, sq.trow + j * kT,
+                    sq.tb, map_ext(a, 2 * kD, 2));
       for (int c = 0; c < 4; ++c)
-        tma_load_4d(sV + c * kBox, &tm_v, bar(cs.kv_full), 64 * c, h, sq.trow + j * kT, sq.tb);
+        tma_load_4d_chk(sV + c * kBox, &tm_v, bar(cs.kv_full), 64 * c, h, sq.trow + j * kT, sq.tb, map_ext(a, kDV, 2));
       bool ok = true;
       int t = 0;
       for (; t < T && ok; ++t) {
@@ -648,15 +666,16 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
         if (!(ok = mbar_wait(bar(cs.do_empty), (t & 1) ^ 1, abrt))) break;
         mbar_arrive_expect_tx(bar(cs.do_full), 4 * kBox);
         for (int c = 0; c < 4; ++c)
-          tma_load_4d(sDO + c * kBox, &tm_do, bar(cs.do_full), 64 * c, h, sq.trow + i * kT, sq.tb);
+          tma_load_4d_chk(sDO + c * kBox, &tm_do, bar(cs.do_full), 64 * c, h, sq.trow + i * kT, sq.tb, map_ext(a, kDV, 2));
         if (!(ok = mbar_wait(bar(cs.q_empty), (t & 1) ^ 1, abrt))) break;
         mbar_arrive_expect_tx(bar(cs.q_full), 2 * kBox + 2 * kT * 4);
         for (int c = 0; c < 2; ++c)
-          tma_load_4d(sQ + c * kBox, &tm_q, bar(cs.q_full), m * kD + 64 * c, h, sq.trow + i * kT,
-                      sq.tb);
-        bulk_load(sBD, a.stats + st_base + static_cast<size_t>(i) * kT, kT * 4, bar(cs.q_full));
-        bulk_load(sBD + kT * 4, a.delta + st_base + static_cast<size_t>(i) * kT, kT * 4,
-                  bar(cs.q_full));
+          tma_load_4d_chk(sQ + c * kBox, &tm_q, bar(cs.q_full), m * kD + 64 * c, h, sq.trow + i * kT,
+                      sq.tb, map_ext(a, 2 * kD, 2));
+        const size_t nst = static_cast<size_t>(a.B) * a.H * 2 * a.Npad;
+        bulk_load_f32(sBD, a.stats, st_base + static_cast<size_t>(i) * kT, nst, kT, bar(cs.q_full));
+        bulk_load_f32(sBD + kT * 4, a.delta, st_base + static_cast<size_t>(i) * kT, nst, kT,
+                      bar(cs.q_full));
       }
       // nothing of ours may still be landing at exit
       mbar_wait(bar(cs.kv_full), 0, nullptr);
@@ -851,9 +870,13 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       if (!(ok = bar_and(2, 128, true))) break;
       if (r == 0) {
         const int i = i0 + t;
+        const Ext4 eacc = map_ext(a, 2 * kD, 4);
         for (int c = 0; c < 4; ++c)
-          tma_reduce_add_4d(&tm_dqacc, sDO + c * kBox, m * kD + 32 * c, h, sq.trow + i * kT,
-                            sq.tb);
+          if (!kDebugChecks ||
+              (dbg_index_ok(sq.trow + i * kT, eacc.z) && dbg_index_ok(sq.tb, eacc.w) &&
+               dbg_index_ok(h, eacc.y) && dbg_index_ok(m * kD + 32 * c, eacc.x)))
+            tma_reduce_add_4d(&tm_dqacc, sDO + c * kBox, m * kD + 32 * c, h, sq.trow + i * kT,
+                              sq.tb);
         bulk_commit();
         bulk_wait_read();
         mbar_arrive(bar(cs.do_empty));  // the slot may take the next dO tile
@@ -964,7 +987,7 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
       prefetch_tmap(&tm_do);
       mbar_arrive_expect_tx(bar(cs.kv_full), 4 * kBox);
       for (int c = 0; c < 4; ++c)
-        tma_load_4d(sK + c * kBox, &tm_k, bar(cs.kv_full), 64 * c, h, sq.trow + j * kT, sq.tb);
+        tma_load_4d_chk(sK + c * kBox, &tm_k, bar(cs.kv_full), 64 * c, h, sq.trow + j * kT, sq.tb, map_ext(a, 2 * kD, 2));
       bool ok = true;
       int t = 0;
       for (; t < T && ok; ++t) {
@@ -973,15 +996,16 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
         if (!(ok = mbar_wait(bar(cs.b_empty[t & 1]), ((t >> 1) & 1) ^ 1, abrt))) break;
         mbar_arrive_expect_tx(bar(cs.q_full), 4 * kBox + 2 * kT * 4);
         for (int c = 0; c < 4; ++c)
-          tma_load_4d(sQ + c * kBox, &tm_q, bar(cs.q_full), 64 * c, h, sq.trow + i * kT, sq.tb);
+          tma_load_4d_chk(sQ + c * kBox, &tm_q, bar(cs.q_full), 64 * c, h, sq.trow + i * kT, sq.tb, map_ext(a, 2 * kD, 2));
         const uint32_t sb = sB + (t & 1) * 2 * kT * 4;
-        bulk_load(sb, a.stats + st_base + static_cast<size_t>(i) * kT, kT * 4, bar(cs.q_full));
-        bulk_load(sb + kT * 4, a.stats + st_base + a.Npad + static_cast<size_t>(i) * kT, kT * 4,
-                  bar(cs.q_full));
+        const size_t nst = static_cast<size_t>(a.B) * a.H * 2 * a.Npad;
+        bulk_load_f32(sb, a.stats, st_base + static_cast<size_t>(i) * kT, nst, kT, bar(cs.q_full));
+        bulk_load_f32(sb + kT * 4, a.stats, st_base + a.Npad + static_cast<size_t>(i) * kT, nst, kT,
+                      bar(cs.q_full));
         if (!(ok = mbar_wait(bar(cs.do_empty), (t & 1) ^ 1, abrt))) break;
         mbar_arrive_expect_tx(bar(cs.do_full), 4 * kBox);
         for (int c = 0; c < 4; ++c)
-          tma_load_4d(sDO + c * kBox, &tm_do, bar(cs.do_full), 64 * c, h, sq.trow + i * kT, sq.tb);
+          tma_load_4d_chk(sDO + c * kBox, &tm_do, bar(cs.do_full), 64 * c, h, sq.trow + i * kT, sq.tb, map_ext(a, kDV, 2));
       }
       mbar_wait(bar(cs.kv_full), 0, nullptr);
       if (t > 0) {

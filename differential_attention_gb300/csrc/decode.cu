@@ -109,11 +109,17 @@ __device__ __forceinline__ size_t paged_row(const int* table, int max_pages, int
 // Row (key j of sequence b) of a contiguous [B, Lmax, H, w] cache, or of a paged pool.
 template <bool kPaged>
 __device__ __forceinline__ size_t cache_row(const DecSplitParams& p, int b, int j) {
+  size_t r;
   if constexpr (kPaged)
-    return paged_row(p.block_table, p.max_pages, p.page_size, p.num_pages, p.ps_magic, p.ps_shift,
-                     b, j);
+    r = paged_row(p.block_table, p.max_pages, p.page_size, p.num_pages, p.ps_magic, p.ps_shift, b,
+                  j);
   else
-    return static_cast<size_t>(b) * p.Lmax + j;
+    r = static_cast<size_t>(b) * p.Lmax + j;
+  // debug builds: the row inside the cache (the grid's z extent is the batch)
+  if (!dbg_index_ok(static_cast<long long>(r),
+                    kPaged ? 1LL * p.num_pages * p.page_size : 1LL * gridDim.z * p.Lmax))
+    r = 0;
+  return r;
 }
 
 template <bool kPaged>
@@ -307,7 +313,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_group_kernel(const DecSpli
     uint4 ku[kG], vu[kG];
 #pragma unroll
     for (int e = 0; e < kG; ++e) {
-      const size_t j = static_cast<size_t>(min(g0 + e, k1 - 1));  // clamped in bounds; masked below
+      size_t j = static_cast<size_t>(min(g0 + e, k1 - 1));  // clamped in bounds; masked below
+      if (!dbg_index_ok(static_cast<long long>(j), p.Lmax)) j = 0;
       ku[e] = noise_lane ? ldg_l1(kbase + j * k_stride) : ldg_stream(kbase + j * k_stride);
       vu[e] = ldg_stream(vbase + j * v_stride);
     }
@@ -758,11 +765,17 @@ __global__ void __launch_bounds__(kV2Warps * 32) v2dec_split_kernel(const V2DecP
   const __nv_bfloat16* kb = p.kc + static_cast<size_t>(g) * kV2D + 8 * hl;
   const __nv_bfloat16* vb = p.vc + static_cast<size_t>(g) * kV2D + 8 * hl;
   auto rowof = [&](int j) -> size_t {
+    size_t r;
     if constexpr (kPaged)
-      return paged_row(p.block_table, p.max_pages, p.page_size, p.num_pages, p.ps_magic,
-                       p.ps_shift, b, j);
+      r = paged_row(p.block_table, p.max_pages, p.page_size, p.num_pages, p.ps_magic, p.ps_shift,
+                    b, j);
     else
-      return static_cast<size_t>(b) * p.Lmax + j;
+      r = static_cast<size_t>(b) * p.Lmax + j;
+    // debug builds: the row inside the cache (the grid's z extent is the batch)
+    if (!dbg_index_ok(static_cast<long long>(r),
+                      kPaged ? 1LL * p.num_pages * p.page_size : 1LL * gridDim.z * p.Lmax))
+      r = 0;
+    return r;
   };
   constexpr int kStride = kV2Warps * 2 * kV2Keys;  // keys per CTA step
   // The loop bound is warp-uniform so that every shuffle below has all 32 lanes; a half-warp

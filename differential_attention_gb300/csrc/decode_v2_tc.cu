@@ -86,6 +86,14 @@ struct Params {
   uint32_t ps_magic, ps_shift;      // j / page_size = (umulhi(j, magic) + j) >> shift
 };
 
+// Extents of the q, K and V tensor maps (the host builds them with these dimensions), for the
+// debug-build checks of tile coordinates: q [B][Hq][128]; caches [B or 1][rows][Hkv][128].
+__device__ __forceinline__ Ext4 q_ext(const Params& p, int elt) { return Ext4{kD, p.Hq, p.B, 1, elt}; }
+__device__ __forceinline__ Ext4 kv_ext(const Params& p, int elt) {
+  const bool paged = p.block_table != nullptr;
+  return Ext4{kD, p.Hkv, paged ? p.num_pages * p.page_size : p.Lmax, paged ? 1 : p.B, elt};
+}
+
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
@@ -226,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(bars.q_empty[qs]), ((qi >> 1) & 1) ^ 1, abrt)) break;
         mbar_arrive_expect_tx(bar(bars.q_full[qs]), (K8 ? 1 : 2) * G * 128);
         for (int c = 0; c < (K8 ? 1 : 2); ++c)
-          tma_load_4d(sQ + qs * kQSlot + c * (kN * 128), &tm_q, bar(bars.q_full[qs]), 64 * c,
-                      it.g * G, it.b, 0);
+          tma_load_4d_chk(sQ + qs * kQSlot + c * (kN * 128), &tm_q, bar(bars.q_full[qs]), 64 * c,
+                      it.g * G, it.b, 0, q_ext(p, K8 ? 1 : 2));
         ++qi;
       }
       for (int j = max(0, qi - 2); j < qi; ++j)
@@ -256,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < it.nt; ++t, ++n) {
           if (n % kGatherTeams != team) continue;  // the other team's tile
           const int st = n % kStages;
-          const int row = page_row(p, it, it.k0 + t * kTile + 32 * gw + lane);
+          int row = page_row(p, it, it.k0 + t * kTile + 32 * gw + lane);
+          if (!dbg_index_ok(row, 1LL * p.num_pages * p.page_size)) row = 0;
           // every lane waits: with lane 0 waiting alone and the others parked at a shuffle, the
           // warp resumed late enough to halve the throughput
           const bool w = mbar_wait(bar(bars.kv_empty[st]), ((n / kStages) & 1) ^ 1, abrt);
@@ -301,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(bar(bars.q_empty[qs]), ((qi >> 1) & 1) ^ 1, abrt))) break;
         mbar_arrive_expect_tx(bar(bars.q_full[qs]), (K8 ? 1 : 2) * G * 128);
         for (int c = 0; c < (K8 ? 1 : 2); ++c)
-          tma_load_4d(sQ + qs * kQSlot + c * (kN * 128), &tm_q, bar(bars.q_full[qs]), 64 * c,
-                      it.g * G, it.b, 0);
+          tma_load_4d_chk(sQ + qs * kQSlot + c * (kN * 128), &tm_q, bar(bars.q_full[qs]), 64 * c,
+                      it.g * G, it.b, 0, q_ext(p, K8 ? 1 : 2));
         ++qi;
         for (int t = 0; t < it.nt; ++t, ++n) {
           const int st = n % kStages;
@@ -313,20 +322,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(bars.k_full[st]), K8 ? kChunk : kKV);
           if (p.block_table) {
             for (int c = 0; c < (K8 ? 1 : 2); ++c)
-              tma_load_4d(sK + st * kKV + c * kChunk, &tm_k, bar(bars.k_full[st]), 64 * c, it.g,
-                          row0, 0);
+              tma_load_4d_chk(sK + st * kKV + c * kChunk, &tm_k, bar(bars.k_full[st]), 64 * c, it.g,
+                          row0, 0, kv_ext(p, K8 ? 1 : 2));
             mbar_arrive_expect_tx(bar(bars.v_full[st]), kKV);
             for (int c = 0; c < 2; ++c)
-              tma_load_4d(sV + st * kKV + c * kChunk, &tm_v, bar(bars.v_full[st]), 64 * c, it.g,
-                          row0, 0);
+              tma_load_4d_chk(sV + st * kKV + c * kChunk, &tm_v, bar(bars.v_full[st]), 64 * c, it.g,
+                          row0, 0, kv_ext(p, 2));
           } else {
             for (int c = 0; c < (K8 ? 1 : 2); ++c)
-              tma_load_4d(sK + st * kKV + c * kChunk, &tm_k, bar(bars.k_full[st]), 64 * c, it.g,
-                          key, it.b);
+              tma_load_4d_chk(sK + st * kKV + c * kChunk, &tm_k, bar(bars.k_full[st]), 64 * c, it.g,
+                          key, it.b, kv_ext(p, K8 ? 1 : 2));
             mbar_arrive_expect_tx(bar(bars.v_full[st]), kKV);
             for (int c = 0; c < 2; ++c)
-              tma_load_4d(sV + st * kKV + c * kChunk, &tm_v, bar(bars.v_full[st]), 64 * c, it.g,
-                          key, it.b);
+              tma_load_4d_chk(sV + st * kKV + c * kChunk, &tm_v, bar(bars.v_full[st]), 64 * c, it.g,
+                          key, it.b, kv_ext(p, 2));
           }
         }
       }

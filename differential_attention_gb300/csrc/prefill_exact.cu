@@ -256,13 +256,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================ TMA producer ================================
     if (lane == 0) {
       const int kvh = kv_head_of(P, u);  // V (and the K of both maps but in the grouped form)
+      // extents of the three tensor maps (the host builds them with these dimensions)
+      const int mN = P.cu_seqlens ? P.total : P.N, mB = P.cu_seqlens ? 1 : P.B;
+      const int mNk = KMODE == kKeysPaged    ? P.num_pages * P.page_size
+                      : KMODE == kKeysOffset ? P.total_k
+                                             : mN;
+      const Ext4 eq{P.q_cols, P.q_heads, mN, mB, C::kQKElt};
+      const Ext4 ek{P.k_cols, P.kv_heads, mNk, mB, C::kQKElt};
+      const Ext4 ev{DV, v_heads(P), mNk, mB, 2};
       mbar_arrive_expect_tx(bar(bars.q_full), C::kQBytes);
       for (int r = 0; r < 2; ++r)
         for (int c = 0; c < C::kQKBoxes; ++c)
-          tma_load_4d(sQ + r * C::kQMapBytes + c * C::kChunk, &tm_q, bar(bars.q_full),
-                      q_col_of(P, r) + C::kQKBoxCols * c,
-                      GROUPED ? grouped_head(P, u, r) : (P.mode == MODE_V1 ? u : 2 * u + r),
-                      seq0 + qt * BM, tb);
+          tma_load_4d_chk(sQ + r * C::kQMapBytes + c * C::kChunk, &tm_q, bar(bars.q_full),
+                          q_col_of(P, r) + C::kQKBoxCols * c,
+                          GROUPED ? grouped_head(P, u, r) : (P.mode == MODE_V1 ? u : 2 * u + r),
+                          seq0 + qt * BM, tb, eq);
       int issued = 0;  // loads issued into the ring
       auto acquire = [&](int idx, uint32_t bytes) -> int {
         const int slot = idx % NSLOT;
@@ -305,9 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             for (int hh = 0; hh < halves; ++hh)
-              tma_load_4d(sSlot + ks * C::kSlot + hh * C::kChunk, &tm_k, bar(bars.slot_full[ks]),
-                          k_col_of(P, mp) + C::kQKBoxCols * c, GROUPED ? grouped_head(P, u, mp) : kvh,
-                          hh ? krow1 : krow0, tb);
+              tma_load_4d_chk(sSlot + ks * C::kSlot + hh * C::kChunk, &tm_k,
+                              bar(bars.slot_full[ks]), k_col_of(P, mp) + C::kQKBoxCols * c,
+                              GROUPED ? grouped_head(P, u, mp) : kvh, hh ? krow1 : krow0, tb, ek);
             issued = k_load(t, q) + 1;
           }
         } else if (t < T) {
@@ -321,9 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int mp = QK8 ? 0 : r; mp <= (QK8 ? 1 : r); ++mp)  // maps in this load
               for (int c = 0; c < C::kQKBoxes; ++c)
-                tma_load_4d(sSlot + ks * C::kSlot + (QK8 ? mp * C::kKMapBytes : 0) + c * C::kChunk,
-                            &tm_k, bar(bars.slot_full[ks]), k_col_of(P, mp) + C::kQKBoxCols * c,
-                            GROUPED ? grouped_head(P, u, mp) : kvh, krow, tb);
+                tma_load_4d_chk(
+                    sSlot + ks * C::kSlot + (QK8 ? mp * C::kKMapBytes : 0) + c * C::kChunk, &tm_k,
+                    bar(bars.slot_full[ks]), k_col_of(P, mp) + C::kQKBoxCols * c,
+                    GROUPED ? grouped_head(P, u, mp) : kvh, krow, tb, ek);
             issued = k_load(t, r) + 1;
           }
         }
@@ -337,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             for (int c = 0; c < DV / 64; ++c)
-              tma_load_4d(sSlot + vs * C::kSlot + c * C::kVHalfChunk, &tm_v,
-                          bar(bars.slot_full[vs]), 64 * c, kvh, vrow, tb);
+              tma_load_4d_chk(sSlot + vs * C::kSlot + c * C::kVHalfChunk, &tm_v,
+                              bar(bars.slot_full[vs]), 64 * c, kvh, vrow, tb, ev);
             issued = v_load(jv, h) + 1;
           }
         }
@@ -769,7 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int piece = (CW * c + 8 * g) / 8;
           *reinterpret_cast<uint4*>(stage + lane * RB + ((piece ^ (lane & (PIECES - 1))) * 16)) = pkt;
         }
-        if (live) {
+        if (live && dbg_index_ok(static_cast<long long>(orow),
+                                 P.cu_seqlens ? P.total : 1LL * P.B * P.N)) {
           if (P.o_pre) {  // training: the head output before the norm and scale
             __nv_bfloat16* op = static_cast<__nv_bfloat16*>(P.o_pre) +
                                 (orow * P.units + u) * DV + c0;
@@ -793,7 +803,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rr = it * RPI + lane / PIECES;   // row (lane of the warp) this lane stores
         const int pc = lane % PIECES;
         const size_t addr = __shfl_sync(0xffffffffu, static_cast<unsigned long long>(oaddr), rr);
-        const bool rlive = __shfl_sync(0xffffffffu, live ? 1 : 0, rr) != 0;
+        bool rlive = __shfl_sync(0xffffffffu, live ? 1 : 0, rr) != 0;
+        if constexpr (kDebugChecks) {  // (every lane takes the shuffle)
+          const long long rrow = static_cast<long long>(
+              __shfl_sync(0xffffffffu, static_cast<unsigned long long>(orow), rr));
+          if (rlive) rlive = dbg_index_ok(rrow, P.cu_seqlens ? P.total : 1LL * P.B * P.N);
+        }
         const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * RB + ((pc ^ (rr & (PIECES - 1))) * 16));
         if (rlive) *reinterpret_cast<uint4*>(out0 + addr + pc * 8) = v;
       }

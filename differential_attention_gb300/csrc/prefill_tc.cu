@@ -157,9 +157,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int qh = q_head_of(P, u, rank), qc = q_col_of(P, rank);
       const int kvh = kv_head_of(P, u), kc = k_col_of(P, rank);  // V head; K column
       const int kh = k_head_of(P, u, rank);                        // K head of this CTA's map
+      // extents of the three tensor maps (the host builds them with these dimensions)
+      const Ext4 eq{P.q_cols, P.q_heads, P.N, P.B, 2}, ek{P.k_cols, P.kv_heads, P.N, P.B, 2};
+      const Ext4 ev{DV, v_heads(P), P.N, P.B, 2};
       mbar_arrive_expect_tx(bar(bars.q_full), C::kQBytes);
       for (int c = 0; c < DQK / 64; ++c)
-        tma_load_4d(sQ + c * C::kChunkBytes, &tm_q, bar(bars.q_full), qc + 64 * c, qh, qt * BM, b);
+        tma_load_4d_chk(sQ + c * C::kChunkBytes, &tm_q, bar(bars.q_full), qc + 64 * c, qh, qt * BM,
+                        b, eq);
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int s = j % NS;
@@ -167,16 +171,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(bars.k_empty[s]), ph ^ 1, abrt)) break;
         mbar_arrive_expect_tx(bar(bars.k_full[s]), C::kKBytes);
         for (int c = 0; c < DQK / 64; ++c)
-          tma_load_4d(sK + s * C::kKBytes + c * C::kChunkBytes, &tm_k, bar(bars.k_full[s]),
-                      kc + 64 * c, kh, j * BN, b);
+          tma_load_4d_chk(sK + s * C::kKBytes + c * C::kChunkBytes, &tm_k, bar(bars.k_full[s]),
+                          kc + 64 * c, kh, j * BN, b, ek);
         if (!mbar_wait(bar(bars.v_empty[s]), ph ^ 1, abrt)) {
           issued = 2 * j + 1;
           break;
         }
         mbar_arrive_expect_tx(bar(bars.v_full[s]), C::kVBytes);
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_4d(sV + s * C::kVBytes + c * C::kChunkBytes, &tm_v, bar(bars.v_full[s]),
-                      64 * c, kvh, j * BN, b);
+          tma_load_4d_chk(sV + s * C::kVBytes + c * C::kChunkBytes, &tm_v, bar(bars.v_full[s]),
+                          64 * c, kvh, j * BN, b, ev);
         issued = 2 * j + 2;
       }
       // Before leaving, make sure no copy of ours is still landing in shared memory.

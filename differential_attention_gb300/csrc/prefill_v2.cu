@@ -202,11 +202,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================ TMA producer ================================
     if (lane == 0) {
       const int kvh = kv_head_of(P, u);
+      // extents of the three tensor maps (the host builds them with these dimensions)
+      const int mN = KMODE != kDense ? P.total : P.N, mB = KMODE != kDense ? 1 : P.B;
+      const int mNk = KMODE == kKeysPaged    ? P.num_pages * P.page_size
+                      : KMODE == kKeysOffset ? P.total_k
+                                             : mN;
+      const Ext4 eq{D, P.q_heads, mN, mB, 2}, ekv{D, P.kv_heads, mNk, mB, 2};
       mbar_arrive_expect_tx(bar(bars.q_full), 2 * C::kQBytes);
       for (int h = 0; h < 2; ++h)
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sQ + h * C::kQBytes + c * C::kChunkBytes, &tm_q, bar(bars.q_full), 64 * c,
-                      2 * u + h, seq0 + qt * BM, tb);
+          tma_load_4d_chk(sQ + h * C::kQBytes + c * C::kChunkBytes, &tm_q, bar(bars.q_full),
+                          64 * c, 2 * u + h, seq0 + qt * BM, tb, eq);
       // token-axis row of the sequence's key r: packed or batched rows, or (paged) the pool row
       // through the block table. A page id outside the pool reads page 0 and, where the key is
       // in use, flags DEV_BAD_INDEX.
@@ -234,16 +240,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(bars.k_empty[s]), ph ^ 1, abrt)) break;
         mbar_arrive_expect_tx(bar(bars.k_full[s]), C::kKBytes);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sK + s * C::kKBytes + c * C::kChunkBytes, &tm_k, bar(bars.k_full[s]),
-                      64 * c, kvh, krow, tb);
+          tma_load_4d_chk(sK + s * C::kKBytes + c * C::kChunkBytes, &tm_k, bar(bars.k_full[s]),
+                          64 * c, kvh, krow, tb, ekv);
         if (!mbar_wait(bar(bars.v_empty[s]), ph ^ 1, abrt)) {
           issued = 2 * j + 1;
           break;
         }
         mbar_arrive_expect_tx(bar(bars.v_full[s]), C::kVBytes);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sV + s * C::kVBytes + c * C::kChunkBytes, &tm_v, bar(bars.v_full[s]),
-                      64 * c, kvh, krow, tb);
+          tma_load_4d_chk(sV + s * C::kVBytes + c * C::kChunkBytes, &tm_v, bar(bars.v_full[s]),
+                          64 * c, kvh, krow, tb, ekv);
         issued = 2 * j + 2;
       }
       // Before leaving, make sure no copy of ours is still landing in shared memory.
@@ -488,7 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rr = it * RPI + lane / PIECES;   // row (lane of the warp) this lane stores
         const int pc = lane % PIECES;
         const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * RB + ((pc ^ (rr & (PIECES - 1))) * 16));
-        if (qt * BM + 32 * (warp & 3) + rr < SN)
+        if (qt * BM + 32 * (warp & 3) + rr < SN &&
+            dbg_index_ok(static_cast<long long>(orow_tile) + 32 * (warp & 3) + rr,
+                         KMODE != kDense ? P.total : 1LL * P.B * P.N))
           *reinterpret_cast<uint4*>(out0 + (orow0 + static_cast<size_t>(rr) * P.units) * D + pc * 8) = v;
       }
     }

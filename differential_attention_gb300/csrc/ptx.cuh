@@ -8,8 +8,19 @@
 
 namespace da {
 
-// Error codes a kernel can leave in the device status word.
-enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
+// Error codes a kernel can leave in the device status word. DEV_BOUNDS only in debug builds.
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2, DEV_BOUNDS = 4 };
+
+// Debug builds (-DDIFFATTN_DEBUG; libdiffattn_debug.so, `builder.py --debug`) check every tile
+// coordinate of a TMA copy and every gathered or stored row index against the extent of its
+// tensor. A failed check records DEV_BOUNDS in the device status word and the access is clamped
+// into the tensor (a copy must still complete its barrier) or skipped (plain loads and stores);
+// it never traps. Release builds compile the checks out.
+#ifdef DIFFATTN_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
 
 // Device status word of this translation unit: a kernel whose bounded wait ran out ORs an
 // error code into it; the host reads and clears it (read_clear_status). Internal linkage keeps
@@ -37,6 +48,22 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 __device__ __forceinline__ void flag_device_error(int code) { atomicOr(&g_device_status, code); }
+
+// Debug builds: false (and DEV_BOUNDS recorded) when an index is outside [0, n). Release: true.
+__device__ __forceinline__ bool dbg_index_ok(long long i, long long n) {
+  if constexpr (kDebugChecks) {
+    if (i < 0 || i >= n) {
+      flag_device_error(DEV_BOUNDS);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Extent of a 4-D tensor map: x = element columns (innermost), y, z, w; elt = bytes per element.
+struct Ext4 {
+  int x, y, z, w, elt;
+};
 
 // ---------------------------------------------------------------------------------------------
 // mbarrier
@@ -158,6 +185,27 @@ __device__ __forceinline__ void tma_load_4d(uint32_t smem_dst, const void* tmap,
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
+}
+// tma_load_4d with the debug-build check of its coordinates against the tensor's extent: x a
+// multiple of 16 bytes inside the row, the head and batch inside their dimensions, and the row
+// non-negative and less than one 128-row tile past the last row (the tail tiles of a sequence
+// run past its end, which TMA fills with zeros). A failed check loads from coordinate 0 of the
+// offending dimensions instead.
+__device__ __forceinline__ void tma_load_4d_chk(uint32_t smem_dst, const void* tmap, uint32_t bar,
+                                                int c0, int c1, int c2, int c3, const Ext4& e) {
+  if constexpr (kDebugChecks) {
+    const bool x_ok = c0 >= 0 && c0 < e.x && (c0 * e.elt) % 16 == 0;
+    const bool y_ok = c1 >= 0 && c1 < e.y, z_ok = c2 >= 0 && c2 < e.z + 128;
+    const bool w_ok = c3 >= 0 && c3 < e.w;
+    if (!(x_ok && y_ok && z_ok && w_ok)) {
+      flag_device_error(DEV_BOUNDS);
+      if (!x_ok) c0 = 0;
+      if (!y_ok) c1 = 0;
+      if (!z_ok) c2 = 0;
+      if (!w_ok) c3 = 0;
+    }
+  }
+  tma_load_4d(smem_dst, tmap, bar, c0, c1, c2, c3);
 }
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

@@ -79,7 +79,12 @@ DIFFATTN_API const char* diffattn_last_error_string(void);
  * Returns DIFFATTN_OK, DIFFATTN_ERR_TIMEOUT (a bounded wait ran out since the last call),
  * DIFFATTN_ERR_INDEX (device-side offsets were out of range: a paged decode met a block-table
  * entry outside [0, num_pages), and read page 0 instead; or a varlen prefill met a sequence
- * outside [0, total), and skipped it; that call's output is invalid), or DIFFATTN_ERR_CUDA. */
+ * outside [0, total), and skipped it; that call's output is invalid), or DIFFATTN_ERR_CUDA.
+ * In the debug build of the library (libdiffattn_debug.so, compiled with -DDIFFATTN_DEBUG) every
+ * kernel also checks each tile coordinate of its TMA copies and each row it gathers or stores
+ * against the extent of its tensor; a failed check clamps the copy into the tensor (or skips the
+ * load or store) and is reported here as DIFFATTN_ERR_INDEX. The release library has no such
+ * checks. */
 DIFFATTN_API int diffattn_device_status(void* stream);
 
 /* Diagnostics (not part of the method): launch one kernel whose bounded wait is certain to run
