@@ -1389,6 +1389,45 @@ cudaError_t host_chunk_prefill(const da::HostPipeArgs& a, const void* q, const v
   char* err = static_cast<char*>(ctx);
   return da::launch_prefill_exact(p, s, err, 256);
 }
+
+// one piece of diffattn_fwd_host: `rows` queries at the end of `keys` keys of one sequence (the
+// key-offset form of the exact prefill, lambda formed in the kernel)
+cudaError_t host_piece_prefill(const da::HostPipeArgs& a, const void* q, const void* k,
+                               const void* v, void* out, int rows, int keys, const int* cu_q,
+                               const int* cu_k, cudaStream_t s, void* ctx) {
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = 1;
+  p.N = rows;
+  p.units = a.H;
+  p.dqk = a.d;
+  p.dv = a.dv;
+  p.mode = da::MODE_V1;
+  p.q_heads = a.H;
+  p.kv_heads = a.H;
+  p.q_cols = 2 * a.d;
+  p.k_cols = 2 * a.d;
+  p.group = 1;
+  p.norm_w = a.norm_w;
+  p.eps = a.eps;
+  p.lambda_init = diffattn_lambda_init(a.layer);
+  p.flags = a.flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(a.d));
+  for (int i = 0; i < 4; ++i) p.lam_vec[i] = a.lam_vec[i];
+  p.lam_dim = a.lam_dim;
+  p.lam_sets = a.lam_sets;
+  p.cu_seqlens = cu_q;
+  p.total = rows;
+  p.cu_seqlens_k = cu_k;
+  p.total_k = keys;
+  p.max_seqlen_k = keys;
+  da::fill_dense_strides(p);
+  char* err = static_cast<char*>(ctx);
+  return da::launch_prefill_exact(p, s, err, 256);
+}
 }  // namespace
 
 DIFFATTN_API int diffattn_fwd_host_workspace_size(int B, int N, int H, int d, int dv, size_t* bytes) {
@@ -1449,7 +1488,8 @@ DIFFATTN_API int diffattn_fwd_host(const void* q_host, const void* k_host, const
   a.eps = eps;
   a.flags = flags;
   char err[256] = {0};
-  cudaError_t e = da::launch_host_pipeline(a, static_cast<cudaStream_t>(stream), host_chunk_prefill, err);
+  cudaError_t e = da::launch_host_pipeline(a, static_cast<cudaStream_t>(stream), host_chunk_prefill,
+                                           host_piece_prefill, err);
   if (err[0]) return fail(DIFFATTN_ERR_CUDA, "diffattn_fwd_host: %s", err);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_fwd_host");
   return ok();

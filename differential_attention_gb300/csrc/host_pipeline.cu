@@ -8,6 +8,13 @@
 // so chunk c + 1 is copied in while chunk c computes and chunk c - 1 is copied out. The caller's
 // stream finally waits for the last copy out, so the call is asynchronous on that stream like
 // every other entry point. Streams and events are created once per device and reused.
+//
+// Causal prefills of long sequences end finer: the last sequence streams in as pieces of rows,
+// and piece p is computed as soon as it has landed -- its queries against the keys received so
+// far (queries at the end of their keys: the same rows as the whole sequence's prefill, bit for
+// bit) -- and copied back at once, so that only one piece's compute and copy-out remain after
+// the last input has arrived instead of a whole sequence's. (The earlier sequences stay whole:
+// pieces throughout made the host-to-device copies, which bound the call, slower.)
 #include <mutex>
 
 #include "internal.h"
@@ -15,10 +22,14 @@
 namespace da {
 namespace {
 
+constexpr int kMaxPieces = 32;
+
 struct DevicePipe {
   bool ready = false;
   cudaStream_t in = nullptr, out = nullptr;
   cudaEvent_t copied[2], computed[2], drained[2], done;
+  cudaEvent_t piece_in[kMaxPieces], piece_done[kMaxPieces];
+  int offsets[4 * kMaxPieces];  // per piece: {0, its rows}, {0, keys received}: staged to device
 };
 
 constexpr int kMaxDevices = 64;
@@ -41,6 +52,10 @@ cudaError_t get_pipe(DevicePipe** out) {
       if ((e = cudaEventCreateWithFlags(&p.drained[i], cudaEventDisableTiming)) != cudaSuccess) return e;
     }
     if ((e = cudaEventCreateWithFlags(&p.done, cudaEventDisableTiming)) != cudaSuccess) return e;
+    for (int i = 0; i < kMaxPieces; ++i) {
+      if ((e = cudaEventCreateWithFlags(&p.piece_in[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+      if ((e = cudaEventCreateWithFlags(&p.piece_done[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
     p.ready = true;
   }
   *out = &p;
@@ -48,6 +63,16 @@ cudaError_t get_pipe(DevicePipe** out) {
 }
 
 }  // namespace
+
+// Rows per piece of the last sequence, or 0 for whole-sequence chunks throughout: causal
+// sequences of at least 2048 rows end in pieces of 1024 rows (a multiple of the 128-row tile; at
+// most kMaxPieces - 1 pieces, larger pieces beyond that).
+int host_piece_rows(int N, int flags) {
+  if (!(flags & 1) || N < 2048) return 0;
+  int P = 1024;
+  while ((N + P - 1) / P > kMaxPieces - 1) P += 128;
+  return P;
+}
 
 int host_chunk_sequences(int B, int N, int H) {
   // smallest chunk that still fills every SM about twice with CTAs (128-row tiles x heads)
@@ -58,17 +83,28 @@ int host_chunk_sequences(int B, int N, int H) {
   return static_cast<int>(cb);
 }
 
-size_t host_workspace_bytes(int B, int N, int H, int d, int dv) {
+// Two slots of cb sequences' q, k, v and out (bf16), then 512 bytes for the pieces' offsets.
+static size_t slot_bytes_of(int B, int N, int H, int d, int dv) {
   const int cb = host_chunk_sequences(B, N, H);
   const size_t rows = static_cast<size_t>(cb) * N * H;
-  const size_t slot = rows * (2 * d + 2 * d + dv + dv) * 2;  // q, k, v, out (bf16)
-  return 2 * ((slot + 255) & ~static_cast<size_t>(255));
+  const size_t slot = rows * (2 * d + 2 * d + dv + dv) * 2;
+  return (slot + 255) & ~static_cast<size_t>(255);
 }
 
-// `run` launches the prefill of one chunk (B = cb sequences) on `stream` with device pointers.
+size_t host_workspace_bytes(int B, int N, int H, int d, int dv) {
+  return 2 * slot_bytes_of(B, N, H, d, dv) + 4 * kMaxPieces * sizeof(int);
+}
+
+// `run` launches the prefill of one chunk (B = cb sequences) on `stream` with device pointers;
+// `run_piece` that of one piece: `rows` queries (q, out) at the end of `keys` keys (k, v) of one
+// sequence, with the device offset arrays {0, rows} and {0, keys}.
 cudaError_t launch_host_pipeline(const HostPipeArgs& a, cudaStream_t stream,
                                  cudaError_t (*run)(const HostPipeArgs&, const void*, const void*,
                                                     const void*, void*, int, cudaStream_t, void*),
+                                 cudaError_t (*run_piece)(const HostPipeArgs&, const void*,
+                                                          const void*, const void*, void*, int,
+                                                          int, const int*, const int*,
+                                                          cudaStream_t, void*),
                                  void* ctx) {
   DevicePipe* pp = nullptr;
   cudaError_t e = get_pipe(&pp);
@@ -79,7 +115,7 @@ cudaError_t launch_host_pipeline(const HostPipeArgs& a, cudaStream_t stream,
   const int cb = host_chunk_sequences(a.B, a.N, a.H);
   const size_t seq_q = static_cast<size_t>(a.N) * a.H * 2 * a.d * 2;  // bytes of one sequence
   const size_t seq_v = static_cast<size_t>(a.N) * a.H * a.dv * 2;
-  const size_t slot_bytes = host_workspace_bytes(a.B, a.N, a.H, a.d, a.dv) / 2;
+  const size_t slot_bytes = slot_bytes_of(a.B, a.N, a.H, a.d, a.dv);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   const char* qh = static_cast<const char*>(a.q);
   const char* kh = static_cast<const char*>(a.k);
@@ -92,7 +128,64 @@ cudaError_t launch_host_pipeline(const HostPipeArgs& a, cudaStream_t stream,
   if ((e = cudaStreamWaitEvent(p.in, p.done, 0)) != cudaSuccess) return e;
   if ((e = cudaStreamWaitEvent(p.out, p.done, 0)) != cudaSuccess) return e;
 
-  const int chunks = (a.B + cb - 1) / cb;
+  const int P = host_piece_rows(a.N, a.flags);
+  if (P > 0) {
+    // one sequence per slot: the earlier ones as one piece of N rows (offset entry 0), the last
+    // one as np pieces of P rows (entries 1 .. np; the last piece shorter)
+    const int np = (a.N + P - 1) / P;
+    const size_t row_q = static_cast<size_t>(a.H) * 2 * a.d * 2, row_v = static_cast<size_t>(a.H) * a.dv * 2;
+    int* offs = reinterpret_cast<int*>(ws + 2 * slot_bytes);
+    p.offsets[0] = 0;
+    p.offsets[1] = a.N;
+    p.offsets[2] = 0;
+    p.offsets[3] = a.N;
+    for (int i = 0; i < np; ++i) {
+      const int end = (i + 1) * P < a.N ? (i + 1) * P : a.N;
+      p.offsets[4 * (i + 1) + 0] = 0;
+      p.offsets[4 * (i + 1) + 1] = end - i * P;
+      p.offsets[4 * (i + 1) + 2] = 0;
+      p.offsets[4 * (i + 1) + 3] = end;
+    }
+    // (from pageable memory: the call returns once the host array has been read)
+    if ((e = cudaMemcpyAsync(offs, p.offsets, 4 * (np + 1) * sizeof(int), cudaMemcpyHostToDevice,
+                             stream)) != cudaSuccess)
+      return e;
+    for (int b = 0; b < a.B; ++b) {
+      const int s = b & 1;
+      uint8_t* dq = ws + s * slot_bytes;
+      uint8_t* dk = dq + seq_q;
+      uint8_t* dvv = dk + seq_q;
+      uint8_t* dout = dvv + seq_v;
+      // inputs of sequence b may overwrite the slot once sequence b - 2 has been computed
+      if (b >= 2 && (e = cudaStreamWaitEvent(p.in, p.computed[s], 0)) != cudaSuccess) return e;
+      const bool last = b == a.B - 1;
+      for (int i = 0; i < (last ? np : 1); ++i) {
+        const int e0 = last ? 4 * (i + 1) : 0;  // this piece's offset entry
+        const int r0 = last ? i * P : 0, rows = p.offsets[e0 + 1];
+        const size_t oq = b * seq_q + r0 * row_q, ov = b * seq_v + r0 * row_v;
+        if ((e = cudaMemcpyAsync(dq + r0 * row_q, qh + oq, rows * row_q, cudaMemcpyHostToDevice, p.in)) != cudaSuccess) return e;
+        if ((e = cudaMemcpyAsync(dk + r0 * row_q, kh + oq, rows * row_q, cudaMemcpyHostToDevice, p.in)) != cudaSuccess) return e;
+        if ((e = cudaMemcpyAsync(dvv + r0 * row_v, vh + ov, rows * row_v, cudaMemcpyHostToDevice, p.in)) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(p.piece_in[i], p.in)) != cudaSuccess) return e;
+        // compute the piece: its rows are in, and (first piece) the slot's output was drained
+        if ((e = cudaStreamWaitEvent(stream, p.piece_in[i], 0)) != cudaSuccess) return e;
+        if (i == 0 && b >= 2 && (e = cudaStreamWaitEvent(stream, p.drained[s], 0)) != cudaSuccess) return e;
+        // (a whole sequence through the batched kernel, a piece through the key-offset form)
+        e = last ? run_piece(a, dq + r0 * row_q, dk, dvv, dout + r0 * row_v, rows, r0 + rows,
+                             offs + e0, offs + e0 + 2, stream, ctx)
+                 : run(a, dq, dk, dvv, dout, 1, stream, ctx);
+        if (e != cudaSuccess) return e;
+        if ((e = cudaEventRecord(p.piece_done[i], stream)) != cudaSuccess) return e;
+        // copy the piece's output back
+        if ((e = cudaStreamWaitEvent(p.out, p.piece_done[i], 0)) != cudaSuccess) return e;
+        if ((e = cudaMemcpyAsync(oh + ov, dout + r0 * row_v, rows * row_v, cudaMemcpyDeviceToHost, p.out)) != cudaSuccess) return e;
+      }
+      if ((e = cudaEventRecord(p.computed[s], stream)) != cudaSuccess) return e;
+      if ((e = cudaEventRecord(p.drained[s], p.out)) != cudaSuccess) return e;
+    }
+  }
+
+  const int chunks = P > 0 ? 0 : (a.B + cb - 1) / cb;
   for (int c = 0; c < chunks; ++c) {
     const int s = c & 1;
     const int b0 = c * cb, nb = (a.B - b0) < cb ? (a.B - b0) : cb;

@@ -239,10 +239,15 @@ struct HostPipeArgs {
   int flags;
 };
 int host_chunk_sequences(int B, int N, int H);
+int host_piece_rows(int N, int flags);  // rows per piece of the piecewise pipeline, 0: chunks
 size_t host_workspace_bytes(int B, int N, int H, int d, int dv);
 cudaError_t launch_host_pipeline(const HostPipeArgs& a, cudaStream_t stream,
                                  cudaError_t (*run)(const HostPipeArgs&, const void*, const void*,
                                                     const void*, void*, int, cudaStream_t, void*),
+                                 cudaError_t (*run_piece)(const HostPipeArgs&, const void*,
+                                                          const void*, const void*, void*, int,
+                                                          int, const int*, const int*,
+                                                          cudaStream_t, void*),
                                  void* ctx);
 
 // Backward of the V1 prefill (d = 128, dv = 256, bf16).

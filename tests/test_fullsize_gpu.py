@@ -103,6 +103,24 @@ def test_prefill_64k_full_with_needle():
     assert_bf16(got, want)
 
 
+def test_fwd_host_3b_bit_equal():
+    """The end-to-end entry point at the 3B-layer shape (pinned host buffers, each sequence in
+    1024-row pieces computed as they land): bit-equal to the device-side fused-lambda prefill,
+    which the full check above ties to the oracle."""
+    B, N, H, layer = 4, 4096, 12, 12
+    inp = make_prefill_inputs(B, N, H, 128, 256, seed=1100, layer=layer, device=DEV)
+    lv = tuple(t.to(DEV).contiguous() for t in make_lambda_vectors(128, seed=1101))
+    want = da.diffattn_fwd_fused_lambda(inp.q, inp.k, inp.v, *lv, layer=layer).cpu()
+    hq, hk, hv = (t.cpu().pin_memory() for t in (inp.q, inp.k, inp.v))
+    hout = torch.zeros((B, N, H, 256), dtype=torch.bfloat16).pin_memory()
+    da.diffattn_fwd_host(hq, hk, hv, hout, *lv, layer=layer)
+    torch.cuda.synchronize()
+    da.diffattn_device_status()
+    assert torch.equal(hout, want)
+    del inp
+    torch.cuda.empty_cache()
+
+
 def test_decode_32k_full():
     """B64, cache 32768, H12: all 64 sequences (every head) against the oracle, one sequence's
     cache (0.4 GB of bf16) at a time, each (sequence, head) within the bf16 bar."""

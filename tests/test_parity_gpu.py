@@ -196,10 +196,12 @@ def test_decode_matches_prefill_last_row():
 # ------------------------------------------------------------------------------------------
 # prefill from host buffers (pipelined copies)
 # ------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("B,N,H", [(5, 300, 2), (1, 129, 1)])
+@pytest.mark.parametrize("B,N,H", [(5, 300, 2), (1, 129, 1), (3, 2500, 1)])
 def test_fwd_host(B, N, H):
     """Host q, k, v, out through the pipelined entry point: the same numbers as the device-side
-    fused-lambda prefill (bit for bit: the same kernel per sequence), checked against the oracle."""
+    fused-lambda prefill (bit for bit: each row sees the same keys in the same tiles), checked
+    against the oracle. Sequences of 2500 tokens take the piecewise path (pieces of 1024, 1024
+    and 452 rows, each computed against the keys received so far; three sequences reuse a slot)."""
     inp = make_prefill_inputs(B, N, H, 128, 256, seed=231 + B)
     vecs = [t.to(DEV).contiguous() for t in inp.lam_vectors]
     hq, hk, hv = (t.contiguous().pin_memory() for t in (inp.q, inp.k, inp.v))
