@@ -134,9 +134,11 @@ _SIGNATURES = {
     "diffattn_v2_decode_fp8_paged": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_float] * 2
                                      + [ctypes.c_int] * 8
                                      + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_gda_fwd_workspace_size": (ctypes.c_int, [ctypes.c_int] * 6
+                                        + [ctypes.POINTER(ctypes.c_size_t)]),
     "diffattn_gda_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_float, ctypes.c_void_p,
                                                                  ctypes.c_float] + [ctypes.c_int] * 8
-                         + [ctypes.c_void_p]),
+                         + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_gda_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.c_void_p,
                                                                     ctypes.c_float]
                             + [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_size_t,
@@ -973,12 +975,22 @@ def diffattn_fwd_host(q, k, v, out, lq1, lk1, lq2, lk2, layer: int, norm_weight=
     return out
 
 
+def diffattn_gda_fwd_workspace_size(B: int, N: int, n_signal: int, n_noise: int, d: int = 128,
+                                    dv: int = 256) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().diffattn_gda_fwd_workspace_size(B, N, n_signal, n_noise, d, dv, ctypes.byref(n)))
+    return int(n.value)
+
+
 def diffattn_gda_fwd(q, k, v, lam, n_signal: int, lambda_init: float = 0.0, norm_weight=None,
                      eps: float = 1e-5, causal: bool = True, norm: bool = True, scale: bool = True,
-                     cuda_cores: bool = False, single_pass: bool = False, out=None, stream=None):
+                     cuda_cores: bool = False, single_pass: bool = False, noise_pass: bool = True,
+                     workspace=None, out=None, stream=None):
     """Grouped differential-attention prefill: q, k [B, N, n_signal + n_noise, d] (signal heads'
     Q1/K1 first, then the noise heads' Q2/K2), v [B, N, n_signal, dv], lam [n_signal]; signal
-    head h subtracts noise head h // (n_signal / n_noise). See include/diffattn.h."""
+    head h subtracts noise head h // (n_signal / n_noise). With `noise_pass` (the default) the
+    noise maps' row statistics are computed once per noise head into `workspace` (allocated here
+    if not given); without it each signal head recomputes them. See include/diffattn.h."""
     _dev("q", q)
     B, N, heads, d = q.shape
     n_noise = heads - int(n_signal)
@@ -998,10 +1010,20 @@ def diffattn_gda_fwd(q, k, v, lam, n_signal: int, lambda_init: float = 0.0, norm
     flags = ((DIFFATTN_CAUSAL if causal else 0) | (DIFFATTN_NORM if norm else 0)
              | (DIFFATTN_SCALE if scale else 0) | (DIFFATTN_CUDA_CORES if cuda_cores else 0)
              | (DIFFATTN_SINGLE_PASS if single_pass else 0))
+    ws_bytes = 0
+    if noise_pass:
+        need = diffattn_gda_fwd_workspace_size(B, N, int(n_signal), n_noise, d, dv)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if workspace is not None:
+            _dev("workspace", workspace)
+            ws_bytes = workspace.numel() * workspace.element_size()
+    else:
+        workspace = None
     _check(lib().diffattn_gda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lam),
                                   float(lambda_init), _ptr(norm_weight), float(eps), B, N,
                                   int(n_signal), n_noise, d, dv, flags, _code(q.dtype),
-                                  _stream(stream)))
+                                  _ptr(workspace), ws_bytes, _stream(stream)))
     return out
 
 

@@ -1506,10 +1506,26 @@ static int check_groups(const char* fn, int n_signal, int n_noise) {
   return 0;
 }
 
+DIFFATTN_API int diffattn_gda_fwd_workspace_size(int B, int N, int n_signal, int n_noise, int d,
+                                                 int dv, size_t* bytes) {
+  const char* fn = "diffattn_gda_fwd_workspace_size";
+  if (!bytes) return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (B < 1 || N < 1) return fail(DIFFATTN_ERR_SHAPE, "%s: B, N must be >= 1", fn);
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  if (!(d == 64 || d == 128) || dv != 2 * d)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need d in {64, 128} and dv = 2d", fn);
+  // one fp32 row statistic per (sequence, noise head, row padded to the 128-row tile); d = 64
+  // runs in one launch and needs none
+  *bytes = d == 128 ? static_cast<size_t>(B) * n_noise * ((N + 127) / 128 * 128) * sizeof(float)
+                    : 0;
+  return ok();
+}
+
 DIFFATTN_API int diffattn_gda_fwd(const void* q, const void* k, const void* v, void* out,
                                   const float* lambda, float lambda_init, const float* norm_weight,
                                   float eps, int B, int N, int n_signal, int n_noise, int d, int dv,
-                                  int flags, int dtype, void* stream) {
+                                  int flags, int dtype, void* workspace, size_t ws_bytes,
+                                  void* stream) {
   const char* fn = "diffattn_gda_fwd";
   if (!q || !k || !v || !out || !lambda) return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
   if (flags & ~kPrefillFlags) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
@@ -1528,6 +1544,16 @@ DIFFATTN_API int diffattn_gda_fwd(const void* q, const void* k, const void* v, v
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
       !aligned(lambda, 4) || (norm_weight && !aligned(norm_weight, 16)))
     return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  // a workspace selects the two-launch form (tensor-core path, d = 128)
+  const bool simt = (flags & DIFFATTN_CUDA_CORES) || dtype == DIFFATTN_FP32;
+  const bool two_launch = workspace && d == 128 && !simt && !(flags & DIFFATTN_SINGLE_PASS);
+  if (two_launch) {
+    size_t need = 0;
+    diffattn_gda_fwd_workspace_size(B, N, n_signal, n_noise, d, dv, &need);
+    if (ws_bytes < need || !aligned(workspace, 256))
+      return fail(DIFFATTN_ERR_WORKSPACE, "%s: need a 256-byte aligned workspace of %zu bytes", fn,
+                  need);
+  }
   int rc = check_device();
   if (rc) return rc;
   da::Problem p{};
@@ -1553,6 +1579,7 @@ DIFFATTN_API int diffattn_gda_fwd(const void* q, const void* k, const void* v, v
   p.lambda_init = lambda_init;
   p.flags = flags;
   p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  if (two_launch) p.gda_noise = static_cast<float*>(workspace);
   return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
 }
 

@@ -71,6 +71,13 @@ struct Problem {
   const int* seqlens_k;
   const int* block_table;
   int page_size, max_pages, num_pages;
+  // grouped form in two launches (exact path, d = 128): phase 1 computes each noise map's row
+  // statistic (base-2 log-sum-exp of the scaled scores) once per noise head into gda_noise
+  // [B, Hn, n_pad]; phase 2 runs the signal heads, whose first pass covers their own map only and
+  // reads the noise map's statistic from gda_noise. Phase 0: one launch, each signal head's CTA
+  // recomputing its noise map's statistics.
+  int gda_phase;
+  float* gda_noise;
 };
 
 // heads in the v tensor (and the output's units are Problem::units)

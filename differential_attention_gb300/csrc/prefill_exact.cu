@@ -136,7 +136,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Launch order: (batch, unit) pairs are taken in groups whose K/V fit in L2 together; inside a
   // group the query tiles go longest-first (causal) across the group's pairs.
-  const int BU = P.B * P.units;
+  // grouped form in two launches: phase 1 runs one CTA per (noise head, query tile) -- unit u is
+  // then the first signal head of the noise head's group -- and phase 2 the signal heads
+  const int gphase = GROUPED ? P.gda_phase : 0;
+  const int gunits = gphase == 1 ? P.units / P.group : P.units;
+  const int BU = P.B * gunits;
   const bool causal = (P.flags & 1) != 0;
   const int item = blockIdx.x;
   const int g0 = (item / (kp.group * kp.n_qt)) * kp.group;
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r_in = item - g0 * kp.n_qt;
   const int qt = causal ? (kp.n_qt - 1 - r_in / gsize) : (r_in / gsize);
   const int bu = g0 + r_in % gsize;
-  const int b = bu / P.units, u = bu % P.units;
+  const int b = bu / gunits, u = gphase == 1 ? (bu % gunits) * P.group : bu % gunits;
   // this sequence's query rows: [seq0, seq0 + SN) of the (packed) token axis, its key rows
   // [kseq0, kseq0 + SNk); TMA batch coordinate tb. With keys of their own (cu_seqlens_k) the
   // queries are the sequence's last SN positions: query row i sees keys [0, qoff + i], with
@@ -193,7 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool W1 = !SHARED_K && !QK8 && DQK == 128;
   static_assert(!W1 || C::kSlot >= 2 * C::kChunk, "a 256-row K chunk fills one ring slot");
   const int n1 = W1 ? (n + 1) / 2 : n;  // pass-1 tiles (the last one 128 keys wide when n is odd)
-  const int T = n1 + n;                 // tiles over both passes
+  const int T = gphase == 1 ? n1 : n1 + n;  // tiles over both passes (phase 1: pass 1 only)
+  // maps in pass 1: both, or (grouped phases, W1 only) map 2 alone (phase 1) or map 1 alone
+  // (phase 2)
+  const int p1maps = gphase ? 1 : 2, p1map0 = gphase == 1 ? 1 : 0;
 
   // Ring order of the loads = the order in which the MMA issuer consumes them. Iteration t < n1
   // of the issuer uses the K loads of pass-1 tile t: with W1 one per map and 64-column chunk
@@ -201,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the K loads of pass-2 tile t - n1 (one per map, both chunks of 128 rows), then for t > n1
   // the two V halves of pass-2 tile jv = t - 1 - n1. base(t) = index of iteration t's first load.
   constexpr int KL = C::kKLoads;
-  constexpr int KL1 = W1 ? 4 : KL;
-  auto base = [n1](int t) {
+  const int KL1 = W1 ? 2 * p1maps : KL;
+  auto base = [n1, KL1](int t) {
     return t <= n1 ? KL1 * t : KL1 * n1 + KL + (KL + 2) * (t - n1 - 1);
   };
   auto k_load = [&](int t, int r) { return base(t) + r; };
@@ -305,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int halves = 2 * t + 1 < n ? 2 : 1;
           const int krow0 = key_row(2 * t * BN);
           const int krow1 = halves == 2 ? key_row((2 * t + 1) * BN) : 0;
-          for (int q = 0; q < 4 && ok; ++q) {
-            const int mp = q >> 1, c = q & 1;
+          for (int q = 0; q < KL1 && ok; ++q) {
+            const int mp = p1maps == 2 ? (q >> 1) : p1map0, c = q & 1;
             const int ks = acquire(k_load(t, q), halves * C::kChunk);
             if (ks < 0) {
               ok = false;
@@ -378,11 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t idesc = 2 * t + 1 < n ? idesc_w : idesc_s;
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
+            if (p1maps == 1 && r != p1map0) continue;
             if (t > 0 && !(ok = mbar_wait(bar(bars.s_free[r]), (t - 1) & 1, abrt))) break;
             const uint64_t qd = desc_add(dq0, r * C::kQMapBytes);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-              const int ki = k_load(t, 2 * r + c), s = ki % NSLOT;
+              const int ki = k_load(t, (p1maps == 2 ? 2 * r : 0) + c), s = ki % NSLOT;
               if (!(ok = mbar_wait(bar(bars.slot_full[s]), (ki / NSLOT) & 1, abrt))) break;
               tc_fence_after();
               const uint64_t kd = desc_add(dslot0, s * C::kSlot);
@@ -432,7 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tp >= n1) {
           const int jv = tp - n1;
           // O's columns held map 2's scores in the last pass-1 tile (W1): read by now
-          if (W1 && jv == 0 && !(ok = mbar_wait(bar(bars.s_free[1]), (n1 - 1) & 1, abrt))) break;
+          if (W1 && jv == 0 && p1maps == 2 &&
+              !(ok = mbar_wait(bar(bars.s_free[1]), (n1 - 1) & 1, abrt)))
+            break;
           if (!(ok = mbar_wait(bar(bars.d_full), jv & 1, abrt))) break;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -502,6 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bias[mp] = -(M + __log2f(L));
       }
+      // grouped, phase 2: the noise map's statistic comes from phase 1 (rows past N: unused)
+      if (gphase == 2)
+        bias[1] = -P.gda_noise[(static_cast<size_t>(b) * (P.units / P.group) + u / P.group) *
+                                   P.n_pad + row];
       if (GROUPED || P.mode == MODE_V1) {
         lam = P.lam_vec[0] ? lam_fused : P.lambda[u];
       } else if (row < (SHARED_K ? SN : P.N)) {
@@ -557,6 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wkey0 = 2 * t * BN + 2 * KW * wg;
 #pragma unroll
         for (int mp = 0; mp < 2; ++mp) {
+          if (p1maps == 1 && mp != p1map0) continue;
           ok = mbar_wait(bar(bars.s_full[mp]), t & 1, abrt);
           if (__any_sync(0xffffffffu, !ok)) {
             ok = false;
@@ -710,6 +725,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!merged) merge();
+    if (gphase == 1) {
+      // grouped, phase 1: the noise map's row statistic is this launch's only output
+      if (ok && wg == 0 && row < P.N)
+        P.gda_noise[(static_cast<size_t>(b) * (P.units / P.group) + u / P.group) * P.n_pad + row] =
+            -bias[1];
+      ok = false;  // no epilogue
+    }
     if (ok) {
       ok = mbar_wait(bar(bars.o_full), 0, abrt);
       ok = !__any_sync(0xffffffffu, !ok);
@@ -879,7 +901,9 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
     const long long bu = static_cast<long long>(p.B) * p.units;
     kp.group = static_cast<int>(g < 1 ? 1 : (g > bu ? bu : g));
   }
-  const long long items = static_cast<long long>(kp.n_qt) * p.B * p.units;
+  // grouped phase 1: one CTA per (noise head, query tile)
+  const int gunits = (GROUPED && p.gda_phase == 1) ? p.units / p.group : p.units;
+  const long long items = static_cast<long long>(kp.n_qt) * p.B * gunits;
   if (items == 0) return cudaSuccess;
   kern<<<dim3(static_cast<unsigned>(items)), kThreads, C::kDynSmem, s>>>(mq, mk, mv, kp);
   return cudaGetLastError();
@@ -892,10 +916,26 @@ cudaError_t status_prefill_exact(int* v) { return read_clear_status(v); }
 cudaError_t launch_prefill_exact(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
   if (p.mode == MODE_GDA) {  // grouped: batched, bf16 scores only
     if (p.qk_fp8 || p.cu_seqlens) return cudaErrorNotSupported;
-    if (p.dqk == 128 && p.dv == 256)
-      return exact::launch_cfg<128, 256, false, false, exact::kKeysShared, true>(p, s, err, err_len);
-    if (p.dqk == 64 && p.dv == 128)
-      return exact::launch_cfg<64, 128, false, false, exact::kKeysShared, true>(p, s, err, err_len);
+    if (p.dqk == 128 && p.dv == 256) {
+      if (!p.gda_noise) {
+        Problem q = p;
+        q.gda_phase = 0;
+        return exact::launch_cfg<128, 256, false, false, exact::kKeysShared, true>(q, s, err, err_len);
+      }
+      // two launches: the noise maps' statistics once per noise head, then the signal heads
+      Problem q = p;
+      q.n_pad = (p.N + exact::BM - 1) / exact::BM * exact::BM;
+      q.gda_phase = 1;
+      cudaError_t e = exact::launch_cfg<128, 256, false, false, exact::kKeysShared, true>(q, s, err, err_len);
+      if (e != cudaSuccess) return e;
+      q.gda_phase = 2;
+      return exact::launch_cfg<128, 256, false, false, exact::kKeysShared, true>(q, s, err, err_len);
+    }
+    if (p.dqk == 64 && p.dv == 128) {  // (one launch: the two-launch form needs d = 128)
+      Problem q = p;
+      q.gda_phase = 0;
+      return exact::launch_cfg<64, 128, false, false, exact::kKeysShared, true>(q, s, err, err_len);
+    }
   } else if (p.mode == MODE_V1) {
     if (p.qk_fp8) {
       if (p.dqk == 128 && p.dv == 256) return exact::launch_cfg<128, 256, false, true>(p, s, err, err_len);

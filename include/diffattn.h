@@ -631,15 +631,25 @@ DIFFATTN_API int diffattn_bwd_varlen(const void* q, const void* k, const void* v
  *   v, out : device [B, N, n_signal, dv]
  *   lambda : device fp32 [n_signal]
  *   lambda_init, norm_weight, eps, flags, dtype : as for diffattn_fwd
- * Supported: d in {64, 128}, dv = 2d, n_signal a multiple of n_noise. Each signal head's CTA
- * recomputes its group's noise map (two maps per head, as in diffattn_fwd); the noise heads'
- * K is read from HBM once per group and from L2 by the group's other heads.
- * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_CUDA.
+ *   workspace, ws_bytes : device scratch of diffattn_gda_fwd_workspace_size() bytes, 256-byte
+ *            aligned, contents need not be initialised; or NULL. With a workspace (tensor-core
+ *            path, d = 128) the call runs two launches: the first computes each noise map's row
+ *            statistic (its exact softmax normaliser) once per noise head into the workspace;
+ *            the second runs the signal heads, whose first pass then covers their own map only.
+ *            With NULL each signal head's CTA recomputes its group's noise map statistics (two
+ *            maps per head, as in diffattn_fwd); the result is the same up to rounding. The
+ *            workspace must not be shared with a call that can run at the same time.
+ * Supported: d in {64, 128}, dv = 2d, n_signal a multiple of n_noise. The noise heads' K is read
+ * from HBM once per group and from L2 by the group's other heads.
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA.
  * ------------------------------------------------------------------------------------------ */
+DIFFATTN_API int diffattn_gda_fwd_workspace_size(int B, int N, int n_signal, int n_noise, int d,
+                                                 int dv, size_t* bytes);
 DIFFATTN_API int diffattn_gda_fwd(const void* q, const void* k, const void* v, void* out,
                                   const float* lambda, float lambda_init, const float* norm_weight,
                                   float eps, int B, int N, int n_signal, int n_noise, int d, int dv,
-                                  int flags, int dtype, void* stream);
+                                  int flags, int dtype, void* workspace, size_t ws_bytes,
+                                  void* stream);
 
 /* Grouped decode: one query token per sequence over its cached keys 0 .. seqlens[b]-1, with the
  * head split of diffattn_gda_fwd.

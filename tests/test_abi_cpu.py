@@ -349,9 +349,20 @@ def test_paged_and_host_validation(L):
 
 
 def test_gda_validation(L):
-    def fwd(ns=12, nn=3, d=128, dv=256, flags=7, dtype=0, q=FAKE, N=16):
+    def fwd(ns=12, nn=3, d=128, dv=256, flags=7, dtype=0, q=FAKE, N=16, ws=None, ws_bytes=0):
         return L.diffattn_gda_fwd(q, FAKE, FAKE, FAKE, FAKE, 0.5, None, 1e-5, 1, N, ns, nn, d, dv,
-                                  flags, dtype, None)
+                                  flags, dtype, ws, ws_bytes, None)
+
+    n = ctypes.c_size_t(0)
+    assert L.diffattn_gda_fwd_workspace_size(4, 4096, 12, 3, 128, 256, ctypes.byref(n)) == 0
+    assert n.value == 4 * 3 * 4096 * 4                   # one fp32 statistic per noise row
+    assert L.diffattn_gda_fwd_workspace_size(1, 130, 12, 3, 128, 256, ctypes.byref(n)) == 0
+    assert n.value == 3 * 256 * 4                         # rows padded to the 128-row tile
+    assert L.diffattn_gda_fwd_workspace_size(1, 130, 12, 3, 64, 128, ctypes.byref(n)) == 0
+    assert n.value == 0                                   # d = 64: one launch, no workspace
+    assert L.diffattn_gda_fwd_workspace_size(1, 130, 12, 5, 128, 256, ctypes.byref(n)) == -2
+    assert fwd(ws=ctypes.c_void_p(0x10000), ws_bytes=3 * 128 * 4 - 4) == -8
+    assert fwd(ws=ctypes.c_void_p(0x10010), ws_bytes=1 << 20) == -8   # not 256-byte aligned
 
     assert fwd(q=None) == -1
     assert fwd(flags=64) == -1

@@ -44,16 +44,33 @@ GDA_CASES = [
 ]
 
 
+@pytest.mark.parametrize("noise_pass", [True, False])
 @pytest.mark.parametrize("B,N,Hs,Hn,d,causal", GDA_CASES)
-def test_gda_fwd_small(B, N, Hs, Hn, d, causal):
+def test_gda_fwd_small(B, N, Hs, Hn, d, causal, noise_pass):
+    """Both forms against the oracle: the noise maps' statistics computed once per noise head
+    (two launches, d = 128) or by every signal head (one launch)."""
     inp = make_gda_inputs(B, N, Hs, Hn, d, 2 * d, seed=101 + N + Hs)
     li = ref.lambda_init(inp.layer)
     w = _w(2 * d)
     got = da.diffattn_gda_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.lam.to(DEV), Hs,
-                              li, norm_weight=w.to(DEV), causal=causal)
+                              li, norm_weight=w.to(DEV), causal=causal, noise_pass=noise_pass)
     want = ref.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, li, Hs, norm_weight=w, causal=causal)
     assert_bf16(got, want)
     da.diffattn_device_status()
+
+
+def test_gda_noise_pass_is_bit_equal_to_one_launch():
+    """A noise map's row statistic is computed with the same arithmetic, in the same order,
+    whether its own launch forms it once per noise head or every signal head forms it again: the
+    two forms give bit-identical outputs (ragged tail, 3 signal heads per noise head)."""
+    inp = make_gda_inputs(2, 700, 6, 2, 128, 256, seed=23, device=DEV)
+    ws = torch.full((da.diffattn_gda_fwd_workspace_size(2, 700, 6, 2),), 255, dtype=torch.uint8,
+                    device=DEV)  # stale contents must not matter
+    a = da.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, 6, 0.7, workspace=ws)
+    b = da.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, 6, 0.7, noise_pass=False)
+    torch.cuda.synchronize()
+    da.diffattn_device_status()
+    assert torch.equal(a, b)
 
 
 def test_gda_fwd_no_norm_no_scale():
@@ -92,7 +109,7 @@ def test_gda_fwd_is_ungrouped_kernel_on_repeated_noise_heads():
     rep = torch.arange(Hs, Hs + Hn, device=DEV).repeat_interleave(Hs // Hn)
     q1 = torch.cat([inp.q[:, :, :Hs], inp.q[:, :, rep]], dim=-1).contiguous()
     k1 = torch.cat([inp.k[:, :, :Hs], inp.k[:, :, rep]], dim=-1).contiguous()
-    a = da.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, Hs, 0.7)
+    a = da.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, Hs, 0.7, noise_pass=False)
     b = da.diffattn_fwd(q1, k1, inp.v, inp.lam, 0.7)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
