@@ -1161,38 +1161,67 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
 }
 
 // =============================================================================================
-// bwd_finish_kernel: blocks [0, nq) convert dQ (8 elements per thread); block nq sums dlam and
-// the norm-weight partials in a fixed order.
+// bwd_finish_kernel: blocks [0, nq) convert dQ (two 8-element groups per thread and step, both
+// groups' loads issued first); block nq sums dlam; blocks nq + 1 .. nq + 8 sum the norm-weight
+// partials, 32 channels each: warp w adds partials w, w + 8, ... (lane = channel), then the eight
+// warp sums are added in warp order. Every sum has a fixed order: the result is deterministic.
 // =============================================================================================
+constexpr int kFinishSumBlocks = kDV / 32;
+
 __global__ void __launch_bounds__(256) bwd_finish_kernel(const Args a, long long n8, int nq) {
   if (static_cast<int>(blockIdx.x) < nq) {
     // packed: rows past the last sequence belong to none and are not written
     if (a.cu) n8 = min(n8, static_cast<long long>(min(max(a.cu[a.B], 0), a.total)) * a.H * 2 * kD / 8);
+    const long long stride = static_cast<long long>(nq) * 256;
+    const float4* src = reinterpret_cast<const float4*>(a.dqacc);
     for (long long e = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; e < n8;
-         e += static_cast<long long>(nq) * 256) {
-      const float4* src = reinterpret_cast<const float4*>(a.dqacc) + 2 * e;
-      const float4 x = src[0], y = src[1];
+         e += 2 * stride) {
+      const long long e2 = e + stride;
+      const bool two = e2 < n8;
+      const float4 x = src[2 * e], y = src[2 * e + 1];
+      float4 x2 = x, y2 = y;
+      if (two) {
+        x2 = src[2 * e2];
+        y2 = src[2 * e2 + 1];
+      }
       uint4 pk;
       pk.x = pack_bf16x2(x.x, x.y);
       pk.y = pack_bf16x2(x.z, x.w);
       pk.z = pack_bf16x2(y.x, y.y);
       pk.w = pack_bf16x2(y.z, y.w);
       reinterpret_cast<uint4*>(a.dq)[e] = pk;
+      if (two) {
+        pk.x = pack_bf16x2(x2.x, x2.y);
+        pk.y = pack_bf16x2(x2.z, x2.w);
+        pk.z = pack_bf16x2(y2.x, y2.y);
+        pk.w = pack_bf16x2(y2.z, y2.w);
+        reinterpret_cast<uint4*>(a.dq)[e2] = pk;
+      }
     }
     return;
   }
-  for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
-    float s = 0.f;
-    for (int b = 0; b < a.B; ++b)
-      for (int t = 0; t < a.n_t; ++t) s += a.dl_part[(static_cast<size_t>(b) * a.H + h) * a.n_t + t];
-    a.dlambda[h] = s;
-  }
-  if (a.dnorm_w) {
-    for (int c = threadIdx.x; c < kDV; c += blockDim.x) {
+  if (static_cast<int>(blockIdx.x) == nq) {
+    for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
       float s = 0.f;
-      for (int k = 0; k < a.pre_blocks; ++k) s += a.dw_part[static_cast<size_t>(k) * kDV + c];
-      a.dnorm_w[c] = a.norm ? s : 0.f;
+      for (int b = 0; b < a.B; ++b)
+        for (int t = 0; t < a.n_t; ++t) s += a.dl_part[(static_cast<size_t>(b) * a.H + h) * a.n_t + t];
+      a.dlambda[h] = s;
     }
+    return;
+  }
+  if (!a.dnorm_w) return;
+  __shared__ float part[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = (static_cast<int>(blockIdx.x) - nq - 1) * 32 + lane;
+  float s = 0.f;
+  for (int k = warp; k < a.pre_blocks; k += 8) s += a.dw_part[static_cast<size_t>(k) * kDV + c];
+  part[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += part[w][lane];
+    a.dnorm_w[c] = a.norm ? t : 0.f;
   }
 }
 
@@ -1343,8 +1372,9 @@ cudaError_t launch_backward(const BackwardArgs& x, cudaStream_t st, char* err, s
 
   const long long n8 = tokens * x.H * 2 * kD / 8;
   long long nq = (n8 + 255) / 256;
-  if (nq > 4 * 152) nq = 4 * 152;
-  bwd_finish_kernel<<<static_cast<int>(nq) + 1, 256, 0, st>>>(a, n8, static_cast<int>(nq));
+  if (nq > 8 * 152) nq = 8 * 152;  // eight 256-thread blocks per SM: a full SM of threads
+  bwd_finish_kernel<<<static_cast<int>(nq) + 1 + kFinishSumBlocks, 256, 0, st>>>(
+      a, n8, static_cast<int>(nq));
   return cudaGetLastError();
 }
 

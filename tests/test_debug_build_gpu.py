@@ -4,9 +4,11 @@ libdiffattn_debug.so is the same source compiled with -DDIFFATTN_DEBUG: every ke
 tile coordinates of its TMA copies and every row it gathers or stores against the extent of its
 tensor, and reports a failed check through diffattn_device_status (DIFFATTN_ERR_INDEX) instead of
 touching memory outside the tensor. It stands in for a memory sanitizer. This test builds it and
-runs tests/test_parity_gpu.py (every entry point on small, ragged and edge-case shapes, each
-checked against the float64 oracle, each calling diffattn_device_status) in a child process that
-loads the debug build; the suite must pass, with no check failing.
+runs the small-case GPU suites -- every entry point on small, ragged and edge-case shapes
+(test_parity_gpu.py), the backward (test_backward_gpu.py), the grouped form (test_gda_gpu.py),
+non-finite inputs and guard bands around every output and workspace -- in a child process that
+loads the debug build; each test checks against the float64 oracle and calls
+diffattn_device_status, and all must pass with no check failing.
 """
 import os
 import subprocess
@@ -29,12 +31,14 @@ def test_parity_suite_under_the_debug_build():
                            timeout=1200)
     assert build.returncode == 0, build.stdout[-2000:] + build.stderr[-4000:]
     assert build.stdout.strip().endswith("libdiffattn_debug.so")
-    run = subprocess.run([sys.executable, "-m", "pytest", "tests/test_parity_gpu.py", "-m", "gpu",
-                          "-x", "-q", "-p", "no:cacheprovider"], cwd=ROOT, env=env,
-                         capture_output=True, text=True, timeout=1800)
+    suites = ["tests/test_parity_gpu.py", "tests/test_backward_gpu.py", "tests/test_gda_gpu.py",
+              "tests/test_nonfinite_gpu.py", "tests/test_guard_gpu.py"]
+    run = subprocess.run([sys.executable, "-m", "pytest", *suites, "-m", "gpu", "-x", "-q", "-p",
+                          "no:cacheprovider"], cwd=ROOT, env=env, capture_output=True, text=True,
+                         timeout=1800)
     assert run.returncode == 0, run.stdout[-4000:] + run.stderr[-2000:]
     summary = [ln for ln in run.stdout.splitlines() if " passed" in ln]
     assert summary, run.stdout[-2000:]
     print("debug build:", build.stdout.strip(), "|", summary[-1])
     n_passed = int(summary[-1].split(" passed")[0].split()[-1])
-    assert n_passed >= 100, summary[-1]
+    assert n_passed >= 150, summary[-1]
