@@ -729,6 +729,30 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del ginp, gout
         torch.cuda.empty_cache()
 
+        # the same heads over the packed sequences of the varlen line
+        lens = varlen_lengths()
+        total = int(sum(lens))
+        vin = make_gda_inputs(1, total, gc["Hs"], gc["Hn"], gc["d"], gc["dv"], seed=5100 + rank,
+                              device=dev)
+        cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=dev)
+        vout = torch.empty((total, gc["Hs"], gc["dv"]), dtype=torch.bfloat16, device=dev)
+        vws = torch.empty(da.diffattn_gda_fwd_workspace_size(len(lens), max(lens), gc["Hs"],
+                                                             gc["Hn"]),
+                          dtype=torch.uint8, device=dev)
+        q, k, v = vin.q[0], vin.k[0], vin.v[0]
+        t = timer(lambda: da.diffattn_gda_fwd_varlen(q, k, v, cu, vin.lam, gc["Hs"], li_g,
+                                                     max_seqlen=max(lens), workspace=vws,
+                                                     out=vout),
+                  max(5, min(50, args.steps)), status=status)
+        vpairs = float(sum(gc["Hs"] * causal_pairs(n) for n in lens))
+        r = tensor_roof(vpairs * method_per_pair, t, peaks, peak_src)
+        extra["gda_varlen"] = compact(r["achieved"], "TFLOP/s", t, r,
+                                      f"{len(lens)} packed sequences ({total} tokens), 12 signal "
+                                      f"heads over 3 noise heads", world,
+                                      flops_per_pair=method_per_pair)
+        del vin, vout, vws, q, k, v
+        torch.cuda.empty_cache()
+
         gd = dict(GDA_DECODE, B=args.decode_batch)
         gdi = make_gda_decode_inputs(gd["B"], gd["L"], gd["Hs"], gd["Hn"], gd["d"], gd["dv"],
                                      seed=5100 + rank, device=dev)

@@ -139,6 +139,10 @@ _SIGNATURES = {
     "diffattn_gda_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_float, ctypes.c_void_p,
                                                                  ctypes.c_float] + [ctypes.c_int] * 8
                          + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_gda_fwd_varlen": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 2
+                                + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                                   ctypes.c_float] + [ctypes.c_int] * 7
+                                + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_gda_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.c_void_p,
                                                                     ctypes.c_float]
                             + [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_size_t,
@@ -1024,6 +1028,53 @@ def diffattn_gda_fwd(q, k, v, lam, n_signal: int, lambda_init: float = 0.0, norm
                                   float(lambda_init), _ptr(norm_weight), float(eps), B, N,
                                   int(n_signal), n_noise, d, dv, flags, _code(q.dtype),
                                   _ptr(workspace), ws_bytes, _stream(stream)))
+    return out
+
+
+def diffattn_gda_fwd_varlen(q, k, v, cu_seqlens, lam, n_signal: int, lambda_init: float = 0.0,
+                            max_seqlen=None, norm_weight=None, eps: float = 1e-5,
+                            causal: bool = True, norm: bool = True, scale: bool = True,
+                            noise_pass: bool = True, workspace=None, out=None, stream=None):
+    """Grouped prefill over packed sequences: q, k [total, n_signal + n_noise, d], v
+    [total, n_signal, dv], cu_seqlens int32 [B + 1] on the device. `max_seqlen` is read from
+    cu_seqlens if not given (one device-to-host copy); the workspace is sized for B sequences of
+    max_seqlen rows."""
+    _dev("q", q, torch.bfloat16)
+    total, heads, d = q.shape
+    n_noise = heads - int(n_signal)
+    dv = v.shape[-1]
+    _dev("k", k, torch.bfloat16)
+    _dev("v", v, torch.bfloat16)
+    if k.shape != q.shape or v.shape[:2] != (total, n_signal):
+        raise ValueError("k must match q, and v must be [total, n_signal, dv]")
+    _dev("cu_seqlens", cu_seqlens, torch.int32)
+    B = cu_seqlens.numel() - 1
+    if max_seqlen is None:
+        max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if B > 0 else 1
+    max_seqlen = max(1, int(max_seqlen))
+    _dev("lam", lam, torch.float32)
+    if lam.numel() != n_signal:
+        raise ValueError("lam must hold one value per signal head")
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if out is None:
+        out = torch.zeros((total, n_signal, dv), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    ws_bytes = 0
+    if noise_pass:
+        need = diffattn_gda_fwd_workspace_size(max(1, B), max_seqlen, int(n_signal), n_noise, d, dv)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if workspace is not None:
+            _dev("workspace", workspace)
+            ws_bytes = workspace.numel() * workspace.element_size()
+    else:
+        workspace = None
+    _check(lib().diffattn_gda_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(cu_seqlens),
+                                         max_seqlen, total, _ptr(lam), float(lambda_init),
+                                         _ptr(norm_weight), float(eps), B, int(n_signal), n_noise,
+                                         d, dv, _train_flags(causal, norm, scale), DIFFATTN_BF16,
+                                         _ptr(workspace), ws_bytes, _stream(stream)))
     return out
 
 

@@ -1583,6 +1583,72 @@ DIFFATTN_API int diffattn_gda_fwd(const void* q, const void* k, const void* v, v
   return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
 }
 
+DIFFATTN_API int diffattn_gda_fwd_varlen(const void* q, const void* k, const void* v, void* out,
+                                         const int* cu_seqlens, int max_seqlen, int total,
+                                         const float* lambda, float lambda_init,
+                                         const float* norm_weight, float eps, int B, int n_signal,
+                                         int n_noise, int d, int dv, int flags, int dtype,
+                                         void* workspace, size_t ws_bytes, void* stream) {
+  const char* fn = "diffattn_gda_fwd_varlen";
+  if (!q || !k || !v || !out || !cu_seqlens || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  constexpr int kVarFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kVarFlags) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "%s: eps must be > 0 with DIFFATTN_NORM", fn);
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);
+  if (B < 1 || max_seqlen < 1 || total < 1 || max_seqlen > total)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need B >= 1 and 1 <= max_seqlen <= total", fn);
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  if (!(d == 64 || d == 128) || dv != 2 * d)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need d in {64, 128} and dv = 2d (got d=%d dv=%d)", fn, d, dv);
+  const int heads = n_signal + n_noise;
+  const long long tiles = (static_cast<long long>(max_seqlen) + 127) / 128 * B * n_signal;
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(total) * heads > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: problem too large for one launch", fn);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || !aligned(cu_seqlens, 4) || (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  // the workspace holds the statistics of B sequences of up to max_seqlen rows
+  const bool two_launch = workspace && d == 128;
+  if (two_launch) {
+    size_t need = 0;
+    diffattn_gda_fwd_workspace_size(B, max_seqlen, n_signal, n_noise, d, dv, &need);
+    if (ws_bytes < need || !aligned(workspace, 256))
+      return fail(DIFFATTN_ERR_WORKSPACE, "%s: need a 256-byte aligned workspace of %zu bytes", fn,
+                  need);
+  }
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = max_seqlen;
+  p.units = n_signal;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_GDA;
+  p.q_heads = heads;
+  p.kv_heads = heads;
+  p.q_cols = d;
+  p.k_cols = d;
+  p.group = n_signal / n_noise;
+  p.lambda = lambda;
+  p.lam_logit = nullptr;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  p.cu_seqlens = cu_seqlens;
+  p.total = total;
+  if (two_launch) p.gda_noise = static_cast<float*>(workspace);
+  return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
+}
+
 DIFFATTN_API int diffattn_gda_decode(const void* q, const void* k_cache, const void* v_cache,
                                      const int* seqlens, void* out, const float* lambda,
                                      float lambda_init, const float* norm_weight, float eps, int B,

@@ -914,8 +914,8 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
 cudaError_t status_prefill_exact(int* v) { return read_clear_status(v); }
 
 cudaError_t launch_prefill_exact(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
-  if (p.mode == MODE_GDA) {  // grouped: batched, bf16 scores only
-    if (p.qk_fp8 || p.cu_seqlens) return cudaErrorNotSupported;
+  if (p.mode == MODE_GDA) {  // grouped: batched or packed, bf16 scores only
+    if (p.qk_fp8 || p.cu_seqlens_k || p.block_table) return cudaErrorNotSupported;
     if (p.dqk == 128 && p.dv == 256) {
       if (!p.gda_noise) {
         Problem q = p;

@@ -651,6 +651,26 @@ DIFFATTN_API int diffattn_gda_fwd(const void* q, const void* k, const void* v, v
                                   int flags, int dtype, void* workspace, size_t ws_bytes,
                                   void* stream);
 
+/* Grouped prefill over packed sequences: diffattn_gda_fwd on sequences of different lengths
+ * packed along the token axis (no padding), each attending only to itself, as
+ * diffattn_fwd_varlen does for the ungrouped operator.
+ *   q, k   : device [total, n_signal + n_noise, d] (the head split of diffattn_gda_fwd)
+ *   v, out : device [total, n_signal, dv]
+ *   cu_seqlens, max_seqlen, total : as diffattn_fwd_varlen (offsets checked on the device)
+ *   workspace, ws_bytes : as diffattn_gda_fwd, of diffattn_gda_fwd_workspace_size(B,
+ *            max_seqlen, ...) bytes (entry (b, g, i): row i of sequence b's noise map g), or NULL
+ * Rows of `out` that belong to no sequence are not written.
+ * Supported: dtype DIFFATTN_BF16 (tensor-core exact path), flags CAUSAL | NORM | SCALE, d in
+ * {64, 128}, dv = 2d, n_signal a multiple of n_noise.
+ * Errors: as diffattn_gda_fwd.
+ */
+DIFFATTN_API int diffattn_gda_fwd_varlen(const void* q, const void* k, const void* v, void* out,
+                                         const int* cu_seqlens, int max_seqlen, int total,
+                                         const float* lambda, float lambda_init,
+                                         const float* norm_weight, float eps, int B, int n_signal,
+                                         int n_noise, int d, int dv, int flags, int dtype,
+                                         void* workspace, size_t ws_bytes, void* stream);
+
 /* Grouped decode: one query token per sequence over its cached keys 0 .. seqlens[b]-1, with the
  * head split of diffattn_gda_fwd.
  *   q       : device bf16 [B, n_signal + n_noise, d]

@@ -592,6 +592,22 @@ def diffattn_gda_fwd(q, k, v, lam, lam_init: float, n_signal: int, norm_weight=N
     return out
 
 
+def diffattn_gda_fwd_varlen(q, k, v, cu_seqlens, lam, lam_init: float, n_signal: int,
+                            norm_weight=None, eps: float = 1e-5, norm: bool = True,
+                            apply_scale: bool = True, causal: bool = True):
+    """`diffattn_gda_fwd` applied to each sequence of a packed batch on its own: q, k
+    [total, Hs + Hn, d], v [total, Hs, dv]; sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1.
+    Returns float64 [total, Hs, dv]; rows in no sequence are 0."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    out = np.zeros((q.shape[0], n_signal, v.shape[-1]))
+    for s0, s1 in varlen_segments(cu_seqlens):
+        if s1 > s0:
+            out[s0:s1] = diffattn_gda_fwd(q[None, s0:s1], k[None, s0:s1], v[None, s0:s1], lam,
+                                          lam_init, n_signal, norm_weight, eps, norm, apply_scale,
+                                          causal)[0]
+    return out
+
+
 def diffattn_gda_decode(q, k_cache, v_cache, seqlens, lam, lam_init: float, n_signal: int,
                         norm_weight=None, eps: float = 1e-5, norm: bool = True,
                         apply_scale: bool = True):

@@ -374,6 +374,23 @@ def test_gda_validation(L):
     assert fwd(d=96, dv=192) == -2
     assert fwd(q=ODD) == -4
 
+    def fwd_var(ns=12, nn=3, d=128, flags=7, dtype=0, cu=FAKE, maxlen=300, total=1000, ws=None,
+                ws_bytes=0):
+        return L.diffattn_gda_fwd_varlen(FAKE, FAKE, FAKE, FAKE, cu, maxlen, total, FAKE, 0.5,
+                                         None, 1e-5, 4, ns, nn, d, 2 * d, flags, dtype, ws,
+                                         ws_bytes, None)
+
+    assert fwd_var(cu=None) == -1
+    assert fwd_var(flags=7 | 8) == -1          # the CUDA-core and single-pass forms: batched only
+    assert fwd_var(dtype=1) == -3
+    assert fwd_var(maxlen=2000) == -2          # longer than the packed axis
+    assert fwd_var(ns=12, nn=5) == -2
+    assert fwd_var(d=96) == -2
+    assert fwd_var(cu=ctypes.c_void_p(0x10002)) == -4
+    # the workspace holds B sequences of max_seqlen rows: 4 * 3 * 384 fp32 here
+    assert fwd_var(ws=ctypes.c_void_p(0x10000), ws_bytes=4 * 3 * 384 * 4 - 4) == -8
+    assert fwd_var(ws=ctypes.c_void_p(0x10010), ws_bytes=1 << 20) == -8
+
     n = ctypes.c_size_t(0)
     assert L.diffattn_decode_workspace_size(8, 4096, 12, 128, 256, ctypes.byref(n)) == 0
     need = n.value

@@ -73,6 +73,62 @@ def test_gda_noise_pass_is_bit_equal_to_one_launch():
     assert torch.equal(a, b)
 
 
+# (sequence lengths, Hs, Hn, d, causal): empty and one-token sequences, ragged tails, several tiles
+GDA_VARLEN_CASES = [
+    ([300, 1, 129, 0, 640], 6, 2, 128, True),
+    ([128, 256], 4, 1, 128, False),
+    ([5, 77, 200], 12, 3, 128, True),
+    ([200, 0, 331], 6, 3, 64, True),
+]
+
+
+@pytest.mark.parametrize("noise_pass", [True, False])
+@pytest.mark.parametrize("lens,Hs,Hn,d,causal", GDA_VARLEN_CASES)
+def test_gda_fwd_varlen(lens, Hs, Hn, d, causal, noise_pass):
+    """Packed grouped prefill against the oracle; rows in no sequence untouched; one sequence
+    bit-equal to the batched grouped prefill of that sequence alone (same form)."""
+    total = sum(lens) + 3
+    inp = make_gda_inputs(1, total, Hs, Hn, d, 2 * d, seed=211 + len(lens) + Hs)
+    q, k, v = inp.q[0], inp.k[0], inp.v[0]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    li = ref.lambda_init(inp.layer)
+    w = _w(2 * d)
+    ws = None
+    if noise_pass:  # stale workspace contents must not matter
+        ws = torch.full((max(1, da.diffattn_gda_fwd_workspace_size(len(lens), max(lens), Hs, Hn,
+                                                                   d, 2 * d)),),
+                        255, dtype=torch.uint8, device=DEV)
+    got = da.diffattn_gda_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cu.to(DEV), inp.lam.to(DEV),
+                                     Hs, li, norm_weight=w.to(DEV), causal=causal,
+                                     noise_pass=noise_pass, workspace=ws)
+    want = ref.diffattn_gda_fwd_varlen(q, k, v, cu, inp.lam, li, Hs, norm_weight=w, causal=causal)
+    n_in = sum(lens)
+    assert_bf16(got[:n_in], want[:n_in])
+    assert torch.count_nonzero(got[n_in:]) == 0
+    i = min(2, len(lens) - 1)
+    s0, n = int(cu[i]), lens[i]
+    one = da.diffattn_gda_fwd(q[None, s0:s0 + n].contiguous().to(DEV),
+                              k[None, s0:s0 + n].contiguous().to(DEV),
+                              v[None, s0:s0 + n].contiguous().to(DEV), inp.lam.to(DEV), Hs, li,
+                              norm_weight=w.to(DEV), causal=causal, noise_pass=noise_pass)
+    torch.cuda.synchronize()
+    da.diffattn_device_status()
+    assert torch.equal(got[s0:s0 + n], one[0])
+
+
+def test_gda_fwd_varlen_bad_offsets_are_reported():
+    """A sequence past the packed length is skipped by the kernels' own check (both launches of
+    the two-launch form) and reported as DIFFATTN_ERR_INDEX."""
+    inp = make_gda_inputs(1, 256, 4, 2, 128, 256, seed=227)
+    cu = torch.tensor([0, 128, 400], dtype=torch.int32, device=DEV)  # 400 > total
+    da.diffattn_gda_fwd_varlen(inp.q[0].to(DEV), inp.k[0].to(DEV), inp.v[0].to(DEV), cu,
+                               inp.lam.to(DEV), 4, 0.5, max_seqlen=256)
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_device_status()
+    assert e.value.status == -9  # DIFFATTN_ERR_INDEX
+    da.diffattn_device_status()
+
+
 def test_gda_fwd_no_norm_no_scale():
     inp = make_gda_inputs(1, 200, 6, 2, 128, 256, seed=7)
     got = da.diffattn_gda_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.lam.to(DEV), 6,

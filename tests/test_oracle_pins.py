@@ -573,6 +573,36 @@ def pin_gda():
             assert same.tolist() == [h // G != 1 for h in range(Hs)]
 
 
+def pin_gda_varlen():
+    """Packed grouped prefill: with equal lengths it is the batched grouped prefill; with one noise
+    head per signal head it is the ungrouped packed prefill on the halves stored as heads; each
+    sequence sees only itself."""
+    rng = np.random.default_rng(23)
+    B, N, Hs, Hn, d, dv = 2, 6, 4, 2, 4, 8
+    q = rng.standard_normal((B, N, Hs + Hn, d)); k = rng.standard_normal((B, N, Hs + Hn, d))
+    v = rng.standard_normal((B, N, Hs, dv)); lam = np.array([0.1, 0.5, 0.9, 0.3])
+    cu = np.arange(B + 1) * N
+    got = ref.diffattn_gda_fwd_varlen(q.reshape(B * N, Hs + Hn, d), k.reshape(B * N, Hs + Hn, d),
+                                      v.reshape(B * N, Hs, dv), cu, lam, 0.2, Hs)
+    want = ref.diffattn_gda_fwd(q, k, v, lam, 0.2, Hs).reshape(B * N, Hs, dv)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    # n_noise = n_signal on packed rows: the ungrouped packed operator with [Q1 | Q2] halves
+    cu2 = np.array([0, 3, 3, 9, 10]); T = 11; H = 3
+    q1, q2, k1, k2 = (rng.standard_normal((T, H, d)) for _ in range(4))
+    vv = rng.standard_normal((T, H, dv)); lam3 = np.array([0.7, 0.2, 0.4])
+    g = ref.diffattn_gda_fwd_varlen(np.concatenate([q1, q2], 1), np.concatenate([k1, k2], 1), vv,
+                                    cu2, lam3, 0.3, H)
+    u = ref.diffattn_fwd_varlen(np.concatenate([q1, q2], 2), np.concatenate([k1, k2], 2), vv, cu2,
+                                lam3, 0.3)
+    assert np.allclose(g, u, rtol=1e-12, atol=1e-12) and np.all(g[10] == 0)
+    # independence: another sequence's noise keys do not reach this one
+    qq = np.concatenate([q1, q2], 1)[:, :H + 1]; kk = np.concatenate([k1, k2], 1)[:, :H + 1]
+    a = ref.diffattn_gda_fwd_varlen(qq, kk, vv, cu2, lam3, 0.3, H)
+    kk2 = kk.copy(); kk2[3:9, H] += rng.standard_normal((6, d))  # (a shared shift would cancel)
+    b = ref.diffattn_gda_fwd_varlen(qq, kk2, vv, cu2, lam3, 0.3, H)
+    assert np.allclose(a[:3], b[:3]) and np.allclose(a[9], b[9]) and not np.allclose(a[3:9], b[3:9])
+
+
 def pin_gda_decode_is_last_prefill_row():
     """Grouped decode equals the last row of a causal grouped prefill over the same keys."""
     rng = np.random.default_rng(47)
@@ -592,7 +622,7 @@ PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, p
         pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
         pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen, pin_varlen_qk,
-        pin_v2_varlen, pin_paged_prefill, pin_bwd_varlen, pin_gda,
+        pin_v2_varlen, pin_paged_prefill, pin_bwd_varlen, pin_gda, pin_gda_varlen,
         pin_gda_decode_is_last_prefill_row]
 
 
