@@ -482,10 +482,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        "copy_bound_ms": copy_ms, "copy_serial_ms": copy_serial_ms,
                        "e2e_over_copy_bound": e2e_ms / copy_ms,
                        "link_gbs": (h2d + d2h) / (copy_ms * 1e-3) / 1e9,
-                       "via": "diffattn_fwd_host: pinned host q, k, v in and out, copies of "
-                              "each sequence overlapped with the prefill of the others; "
-                              "copy_bound_ms: the same bytes, plain copies only, H2D and D2H "
-                              "on two streams at once"}
+                       "via": "diffattn_fwd_host: pinned host q, k, v copied in, each "
+                              "sequence's copies overlapped with the prefill of the others; the "
+                              "prefill stores its output rows into the pinned host out over the "
+                              "link (d2h bytes); copy_bound_ms: the same bytes, plain copies "
+                              "only, H2D and D2H on two streams at once"}
         del hq, hk, hv, hout, hws, dq, dk, dvv
 
         # the single-pass kernel (one flash pass per map on a 2-CTA cluster, opt-in), same inputs

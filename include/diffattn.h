@@ -357,13 +357,17 @@ DIFFATTN_API int diffattn_v2_decode_paged(const void* q, const void* k_pool, con
  * next chunk, which runs on `stream`.
  *   q_host, k_host : host [B, N, H, 2d] bf16;  v_host, out_host : host [B, N, H, dv] bf16.
  *                    Page-locked (cudaHostAlloc / cudaHostRegister) memory is needed for the
- *                    copies to overlap; all four must stay valid until `stream` completes.
+ *                    copies to overlap; all four must stay valid until `stream` completes. A
+ *                    page-locked out_host that is mapped into the device's address space (the
+ *                    default for cudaHostAlloc on unified-address systems) is written by the
+ *                    prefill's own stores over the host link, with no output copy; any other
+ *                    out_host is filled by copies from the workspace.
  *   lq1 .. lk2, lambda_dim, lambda_sets, layer, norm_weight, eps, flags :
  *                    device data and meaning as diffattn_fwd_fused_lambda
  *   workspace, ws_bytes : device, >= diffattn_fwd_host_workspace_size(), 256-byte aligned, not
  *                    shared with a call that can run at the same time
  * The call returns once everything is enqueued; `stream` then completes after the last output
- * copy. Calls on one device serialise on the library's copy streams.
+ * row has been written. Calls on one device serialise on the library's copy streams.
  * Supported: d in {64, 128}, dv = 2d. Errors: as diffattn_fwd_fused_lambda, plus ERR_WORKSPACE.
  * ------------------------------------------------------------------------------------------ */
 DIFFATTN_API int diffattn_fwd_host_workspace_size(int B, int N, int H, int d, int dv,

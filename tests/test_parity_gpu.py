@@ -196,18 +196,22 @@ def test_decode_matches_prefill_last_row():
 # ------------------------------------------------------------------------------------------
 # prefill from host buffers (pipelined copies)
 # ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("pinned_out", [True, False])
 @pytest.mark.parametrize("B,N,H,d", [(5, 300, 2, 128), (1, 129, 1, 128), (3, 2500, 1, 128),
                                      (2, 2100, 2, 64)])
-def test_fwd_host(B, N, H, d):
+def test_fwd_host(B, N, H, d, pinned_out):
     """Host q, k, v, out through the pipelined entry point: the same numbers as the device-side
     fused-lambda prefill (bit for bit: each row sees the same keys in the same tiles), checked
     against the oracle. Causal sequences of 2048 tokens or more end in the piecewise path: the
     last sequence as pieces of 1024 rows (1024, 1024 and 452 rows at 2500 tokens; 1024, 1024 and
-    52 at 2100, d = 64), each computed against the keys received so far."""
+    52 at 2100, d = 64), each computed against the keys received so far. A page-locked `out` is
+    written by the kernels themselves; a pageable one through device slots and copies back."""
     inp = make_prefill_inputs(B, N, H, d, 2 * d, seed=231 + B)
     vecs = [t.to(DEV).contiguous() for t in inp.lam_vectors]
     hq, hk, hv = (t.contiguous().pin_memory() for t in (inp.q, inp.k, inp.v))
-    hout = torch.zeros((B, N, H, 2 * d), dtype=torch.bfloat16).pin_memory()
+    hout = torch.zeros((B, N, H, 2 * d), dtype=torch.bfloat16)
+    if pinned_out:
+        hout = hout.pin_memory()
     da.diffattn_fwd_host(hq, hk, hv, hout, *vecs, layer=12)
     torch.cuda.synchronize()
     dev_out = da.diffattn_fwd_fused_lambda(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), *vecs, layer=12)
