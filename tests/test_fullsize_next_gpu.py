@@ -1,5 +1,6 @@
 """GPU parity at full size for the bench lines beyond the five base workloads: fp8 scores, the
-packed, chunked and paged prefills, the paged and fp8 decodes and the packed backward. Each runs
+packed, chunked and paged prefills, the grouped packed prefill, the paged and fp8 decodes and the
+packed backward. Each runs
 in the launch configuration bench.py times. Inputs are drawn on the device; the float64 oracle
 recomputes sampled outputs. Where two entry points run the same arithmetic on the same data
 (paged against contiguous caches) the outputs must also be bit-identical."""
@@ -10,8 +11,8 @@ import torch
 import differential_attention_gb300 as da
 from bench import varlen_lengths
 from oracle import diffattn_ref as ref
-from synth import (make_decode_inputs, make_dout, make_prefill_inputs, make_v2_decode_inputs,
-                   to_fp8_e4m3)
+from synth import (make_decode_inputs, make_dout, make_gda_inputs, make_prefill_inputs,
+                   make_v2_decode_inputs, to_fp8_e4m3)
 from tests.gpu_util import assert_bf16, assert_grad
 
 pytestmark = pytest.mark.gpu
@@ -94,6 +95,35 @@ def test_varlen_full():
         sl = lambda t: t[:, s0:s0 + n].cpu()
         w = ref.diffattn_fwd(sl(inp.q), sl(inp.k), sl(inp.v), [0.6] * H, ref.lambda_init(12),
                              rows=rows)[0]
+        want.append(w.reshape(-1, 256))
+        got.append(out[torch.as_tensor(s0 + rows, device=DEV)].float().cpu().numpy().reshape(-1, 256))
+    assert_bf16(np.concatenate(got), np.concatenate(want))
+
+
+def test_gda_varlen_full():
+    """The bench's grouped packed line: the 16 packed sequences with 12 signal heads over 3 noise
+    heads, both launches (noise statistics once per noise head, into a workspace). Sampled rows of
+    every signal head of five sequences against each sequence's own grouped prefill in the
+    oracle."""
+    Hs, Hn = 12, 3
+    lens = varlen_lengths()
+    total = int(sum(lens))
+    inp = make_gda_inputs(1, total, Hs, Hn, 128, 256, seed=5100, device=DEV)
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=DEV)
+    li = da.diffattn_lambda_init(12)
+    ws = torch.empty(da.diffattn_gda_fwd_workspace_size(len(lens), max(lens), Hs, Hn),
+                     dtype=torch.uint8, device=DEV)
+    out = da.diffattn_gda_fwd_varlen(inp.q[0], inp.k[0], inp.v[0], cu, inp.lam, Hs, li,
+                                     max_seqlen=max(lens), workspace=ws)
+    da.diffattn_device_status()
+    offs = np.concatenate([[0], np.cumsum(lens)])
+    lam = inp.lam.cpu().numpy()
+    got, want = [], []
+    for s in (0, 1, 5, 9, 15):
+        s0, n = int(offs[s]), int(lens[s])
+        rows = _rows(n, 16, 32, 5100 + s)
+        sl = lambda t: t[:, s0:s0 + n].cpu()
+        w = ref.diffattn_gda_fwd(sl(inp.q), sl(inp.k), sl(inp.v), lam, li, Hs, rows=rows)[0]
         want.append(w.reshape(-1, 256))
         got.append(out[torch.as_tensor(s0 + rows, device=DEV)].float().cpu().numpy().reshape(-1, 256))
     assert_bf16(np.concatenate(got), np.concatenate(want))
