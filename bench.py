@@ -770,7 +770,23 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                       f"decode_32k with 12 signal heads over 3 noise heads, B{gd['B']}",
                                       world, traffic=profiled_traffic(
                                           "gda_decode_32k.md", source_sha(["decode.cu", "ptx.cuh"])))
-        del gdi, gws, gdout
+
+        # the same cache as pools of 64-token pages, each sequence's pages scattered over them
+        gps = 64
+        gmp = gd["L"] // gps
+        gk_pool = gdi.k_cache.view(gd["B"] * gmp, gps, gd["Hs"] + gd["Hn"], gd["d"])
+        gv_pool = gdi.v_cache.view(gd["B"] * gmp, gps, gd["Hs"], gd["dv"])
+        ggp = torch.Generator(device="cpu")
+        ggp.manual_seed(5200 + rank)
+        gtable = torch.randperm(gd["B"] * gmp, generator=ggp).to(torch.int32).view(gd["B"], gmp).to(dev)
+        t = timer(lambda: da.diffattn_gda_decode_paged(gdi.q, gk_pool, gv_pool, gtable, gdi.seqlens,
+                                                       gdi.lam, gd["Hs"], li_g, workspace=gws,
+                                                       out=gdout),
+                  max(5, min(50, args.steps)), status=status)
+        r = hbm_roof(gdbytes, t, peaks, peak_src)
+        extra["gda_decode_paged"] = compact(r["achieved"], "GB/s", t, r,
+                                            f"gda_decode_32k in shuffled {gps}-token pages", world)
+        del gdi, gws, gdout, gk_pool, gv_pool, gtable
         torch.cuda.empty_cache()
 
     # ======================= V2 decode =======================

@@ -143,6 +143,10 @@ _SIGNATURES = {
                                 + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
                                    ctypes.c_float] + [ctypes.c_int] * 7
                                 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_gda_decode_paged": (ctypes.c_int, [ctypes.c_void_p] * 7
+                                  + [ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
+                                  + [ctypes.c_int] * 10
+                                  + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_gda_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.c_void_p,
                                                                     ctypes.c_float]
                             + [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_size_t,
@@ -1110,6 +1114,48 @@ def diffattn_gda_decode(q, k_cache, v_cache, lam, n_signal: int, lambda_init: fl
                                      float(eps), B, Lmax, int(n_signal), n_noise, d, dv, flags,
                                      DIFFATTN_BF16, _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def diffattn_gda_decode_paged(q, k_pool, v_pool, block_table, seqlens, lam, n_signal: int,
+                              lambda_init: float = 0.0, norm_weight=None, eps: float = 1e-5,
+                              norm: bool = True, scale: bool = True, workspace=None, out=None,
+                              stream=None):
+    """Grouped decode over a paged cache: q [B, n_signal + n_noise, d], pools
+    [num_pages, page_size, n_signal + n_noise, d] and [num_pages, page_size, n_signal, dv],
+    block_table [B, max_pages] int32, seqlens [B] int32; returns [B, n_signal, dv]."""
+    _dev("q", q, torch.bfloat16)
+    B, heads, d = q.shape
+    n_noise = heads - int(n_signal)
+    _dev("k_pool", k_pool, torch.bfloat16)
+    _dev("v_pool", v_pool, torch.bfloat16)
+    num_pages, page_size = k_pool.shape[0], k_pool.shape[1]
+    dv = v_pool.shape[-1]
+    if (k_pool.shape != (num_pages, page_size, heads, d)
+            or v_pool.shape[:3] != (num_pages, page_size, n_signal)):
+        raise ValueError("pools must be [num_pages, page_size, n_signal + n_noise, d] and "
+                         "[num_pages, page_size, n_signal, dv]")
+    _dev("block_table", block_table, torch.int32)
+    _dev("seqlens", seqlens, torch.int32)
+    max_pages = block_table.shape[1]
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if workspace is None:
+        workspace = torch.empty(diffattn_decode_workspace_size(B, max_pages * page_size,
+                                                               int(n_signal), d, dv),
+                                dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, int(n_signal), dv), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    flags = (DIFFATTN_NORM if norm else 0) | (DIFFATTN_SCALE if scale else 0)
+    _check(lib().diffattn_gda_decode_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                           _ptr(seqlens), _ptr(out), _ptr(lam), float(lambda_init),
+                                           _ptr(norm_weight), float(eps), B, int(n_signal), n_noise,
+                                           d, dv, num_pages, page_size, max_pages, flags,
+                                           DIFFATTN_BF16, _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(),
+                                           _stream(stream)))
     return out
 
 

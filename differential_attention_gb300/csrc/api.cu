@@ -1697,3 +1697,63 @@ DIFFATTN_API int diffattn_gda_decode(const void* q, const void* k_cache, const v
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return ok();
 }
+
+DIFFATTN_API int diffattn_gda_decode_paged(const void* q, const void* k_pool, const void* v_pool,
+                                           const int* block_table, const int* seqlens, void* out,
+                                           const float* lambda, float lambda_init,
+                                           const float* norm_weight, float eps, int B,
+                                           int n_signal, int n_noise, int d, int dv, int num_pages,
+                                           int page_size, int max_pages, int flags, int dtype,
+                                           void* workspace, size_t ws_bytes, void* stream) {
+  const char* fn = "diffattn_gda_decode_paged";
+  if (!q || !k_pool || !v_pool || !block_table || !seqlens || !out || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (flags & ~(DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE))
+    return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "%s: eps must be > 0 with DIFFATTN_NORM", fn);
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);
+  if (B < 1 || B > 65535 || num_pages < 1 || page_size < 1 || max_pages < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need 1 <= B <= 65535 and num_pages, page_size, max_pages >= 1", fn);
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  const long long lmax = static_cast<long long>(max_pages) * page_size;
+  if (lmax > 0x7fffffffLL || static_cast<long long>(num_pages) * page_size > (1LL << 40))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: max_pages * page_size too large", fn);
+  if (d != 128 || dv != 256)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need d = 128 and dv = 256 (got d=%d dv=%d)", fn, d, dv);
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || !aligned(seqlens, 4) || !aligned(block_table, 4) ||
+      (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  const int Lmax = static_cast<int>(lmax);
+  const size_t need = da::decode_workspace_bytes(B, Lmax, n_signal, dv);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(DIFFATTN_ERR_WORKSPACE, "%s: need a 256-byte aligned workspace of %zu bytes", fn, need);
+  int rc = check_device();
+  if (rc) return rc;
+  da::DecodeArgs a{};
+  a.q = q;
+  a.k_cache = k_pool;
+  a.v_cache = v_pool;
+  a.seqlens = seqlens;
+  a.out = out;
+  a.lambda = lambda;
+  a.lambda_init = lambda_init;
+  a.norm_w = norm_weight;
+  a.eps = eps;
+  a.flags = flags;
+  a.B = B;
+  a.Lmax = Lmax;
+  a.H = n_signal;
+  a.d = d;
+  a.dv = dv;
+  a.ws = static_cast<float*>(workspace);
+  a.noise_group = n_signal / n_noise;
+  a.block_table = block_table;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  cudaError_t e = da::launch_decode(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}

@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecSpli
 // kGroupWarps warps per head splitting the keys. Lanes 0-15 stream the head's K1 half row past L1;
 // lanes 16-31 read the noise head's K2 half row through L1, where the block's other heads find it,
 // so a noise row enters the SM once per block instead of once per head. The math per warp is that
-// of decode_split_kernel; the partials go to the same records.
+// of decode_split_kernel; the partials go to the same records. kPaged: the caches are page pools
+// [num_pages, page_size, heads, w] addressed through the block table, key by key.
 constexpr int kGroupWarps = 2;
 
 __device__ __forceinline__ uint4 ldg_l1(const void* p) {
@@ -274,7 +275,8 @@ __device__ __forceinline__ uint4 ldg_l1(const void* p) {
   return r;
 }
 
-__global__ void __launch_bounds__(kDecThreads) decode_group_kernel(const DecSplitParams p) {
+template <bool kPaged>
+__device__ __forceinline__ void decode_group_body(const DecSplitParams& p) {
   const int s = blockIdx.x, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = warp / kGroupWarps, wi = warp % kGroupWarps;
@@ -303,18 +305,43 @@ __global__ void __launch_bounds__(kDecThreads) decode_group_kernel(const DecSpli
 
   const size_t k_stride = static_cast<size_t>(heads) * kHalf;   // elements between keys
   const size_t v_stride = static_cast<size_t>(p.H) * kDecWidth;
-  const __nv_bfloat16* kbase = p.kc + static_cast<size_t>(b) * p.Lmax * k_stride +
-                               static_cast<size_t>(kh) * kHalf + 8 * (lane & 15);
-  const __nv_bfloat16* vbase = p.vc + static_cast<size_t>(b) * p.Lmax * v_stride +
-                               static_cast<size_t>(h) * kDecWidth + 8 * lane;
+  // contiguous caches: sequence b's rows start at b * Lmax; page pools: rows come from the table
+  const size_t row0 = kPaged ? 0 : static_cast<size_t>(b) * p.Lmax;
+  const __nv_bfloat16* kbase = p.kc + row0 * k_stride + static_cast<size_t>(kh) * kHalf +
+                               8 * (lane & 15);
+  const __nv_bfloat16* vbase = p.vc + row0 * v_stride + static_cast<size_t>(h) * kDecWidth + 8 * lane;
   const bool noise_lane = lane >= 16;
 
   for (int g0 = k0 + wi * kG; g0 < k1; g0 += kGroupWarps * kG) {
     uint4 ku[kG], vu[kG];
+    // paged: the pool row of key g0 from one table lookup; the group's other keys follow it in
+    // the same page unless the group crosses a page boundary (then each key looks its page up)
+    size_t prow0 = 0;
+    bool one_page = false;
+    if constexpr (kPaged) {
+      const uint32_t uj = static_cast<uint32_t>(g0);
+      const uint32_t pi = (__umulhi(uj, p.ps_magic) + uj) >> p.ps_shift;  // g0 / page_size
+      const uint32_t off = uj - pi * static_cast<uint32_t>(p.page_size);
+      one_page = off + kG <= static_cast<uint32_t>(p.page_size);
+      if (one_page) {
+        int pg = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + pi);
+        if (pg < 0 || pg >= p.num_pages) {
+          flag_device_error(DEV_BAD_INDEX);
+          pg = 0;
+        }
+        prow0 = static_cast<size_t>(pg) * p.page_size + off;
+      }
+    }
 #pragma unroll
     for (int e = 0; e < kG; ++e) {
       size_t j = static_cast<size_t>(min(g0 + e, k1 - 1));  // clamped in bounds; masked below
-      if (!dbg_index_ok(static_cast<long long>(j), p.Lmax)) j = 0;
+      if constexpr (kPaged) {
+        // the key's row in the pool (j - g0 < kG stays inside g0's page on the one-page path)
+        j = one_page ? prow0 + (j - static_cast<size_t>(g0)) : cache_row<true>(p, b, static_cast<int>(j));
+        if (!dbg_index_ok(static_cast<long long>(j), 1LL * p.num_pages * p.page_size)) j = 0;
+      } else {
+        if (!dbg_index_ok(static_cast<long long>(j), p.Lmax)) j = 0;
+      }
       ku[e] = noise_lane ? ldg_l1(kbase + j * k_stride) : ldg_stream(kbase + j * k_stride);
       vu[e] = ldg_stream(vbase + j * v_stride);
     }
@@ -422,6 +449,15 @@ __global__ void __launch_bounds__(kDecThreads) decode_group_kernel(const DecSpli
   }
 }
 
+// The contiguous form keeps the register budget the compiler picks for it (80); the paged form,
+// with its table lookups, is held to three CTAs per SM.
+__global__ void __launch_bounds__(kDecThreads) decode_group_kernel(const DecSplitParams p) {
+  decode_group_body<false>(p);
+}
+__global__ void __launch_bounds__(kDecThreads, 3) decode_group_paged_kernel(const DecSplitParams p) {
+  decode_group_body<true>(p);
+}
+
 struct DecCombineParams {
   const float* ws;
   const float* lambda;
@@ -503,12 +539,15 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   sp.group = a.noise_group;
   sp.hpc = 1;
   if (a.noise_group) {
-    if (a.block_table) return cudaErrorNotSupported;  // no paged grouped cache
     // signal heads per CTA: the largest divisor of the group that fits the CTA's warps
     const int max_hpc = kDecWarps / kGroupWarps;
     for (int d = 1; d <= max_hpc; ++d)
       if (a.noise_group % d == 0) sp.hpc = d;
-    decode_group_kernel<<<dim3(S, a.H / sp.hpc, a.B), kGroupWarps * 32 * sp.hpc, 0, st>>>(sp);
+    const dim3 grid(S, a.H / sp.hpc, a.B);
+    if (a.block_table)
+      decode_group_paged_kernel<<<grid, kGroupWarps * 32 * sp.hpc, 0, st>>>(sp);
+    else
+      decode_group_kernel<<<grid, kGroupWarps * 32 * sp.hpc, 0, st>>>(sp);
   } else if (a.block_table)
     decode_split_kernel<true><<<dim3(S, a.H, a.B), kDecThreads, 0, st>>>(sp);
   else

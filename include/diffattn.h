@@ -693,6 +693,27 @@ DIFFATTN_API int diffattn_gda_decode(const void* q, const void* k_cache, const v
                                      int Lmax, int n_signal, int n_noise, int d, int dv, int flags,
                                      int dtype, void* workspace, size_t ws_bytes, void* stream);
 
+/* Grouped decode over a paged KV cache: diffattn_gda_decode with the caches held in fixed-size
+ * pages of shared pools, addressed as in diffattn_decode_paged (key j of sequence b is row
+ * j % page_size of page block_table[b][j / page_size]).
+ *   k_pool : device bf16 [num_pages, page_size, n_signal + n_noise, d] (the head split of
+ *            diffattn_gda_fwd)
+ *   v_pool : device bf16 [num_pages, page_size, n_signal, dv]
+ *   block_table, seqlens, num_pages, page_size, max_pages : as for diffattn_decode_paged (any
+ *            page size; a used table entry outside [0, num_pages) reads page 0 instead and is
+ *            reported by diffattn_device_status() as DIFFATTN_ERR_INDEX)
+ *   other arguments as diffattn_gda_decode; workspace of at least
+ *   diffattn_decode_workspace_size(B, max_pages * page_size, n_signal, d, dv) bytes
+ * Supported: d = 128, dv = 256, n_signal a multiple of n_noise.
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA. */
+DIFFATTN_API int diffattn_gda_decode_paged(const void* q, const void* k_pool, const void* v_pool,
+                                           const int* block_table, const int* seqlens, void* out,
+                                           const float* lambda, float lambda_init,
+                                           const float* norm_weight, float eps, int B,
+                                           int n_signal, int n_noise, int d, int dv, int num_pages,
+                                           int page_size, int max_pages, int flags, int dtype,
+                                           void* workspace, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -408,6 +408,28 @@ def diffattn_v2_decode_paged(q, k_pool, v_pool, block_table, seqlens, lam_logit)
     return diffattn_v2_decode(q, kc, vc, sl, lam_logit)
 
 
+def diffattn_gda_decode_paged(q, k_pool, v_pool, block_table, seqlens, lam, lam_init: float,
+                              n_signal: int, norm_weight=None, eps: float = 1e-5,
+                              norm: bool = True, apply_scale: bool = True):
+    """`diffattn_gda_decode` over a cache held in pages: k_pool [num_pages, page_size, Hs + Hn, d],
+    v_pool [num_pages, page_size, Hs, dv], block_table [B, max_pages], seqlens [B]. Each
+    sequence's keys are gathered from the pool in order, then decoded as a contiguous cache."""
+    num_pages, page_size, heads, w = k_pool.shape
+    kp = _f64(k_pool).reshape(num_pages * page_size, heads, w)
+    vp = _f64(v_pool).reshape(num_pages * page_size, v_pool.shape[2], v_pool.shape[-1])
+    B = q.shape[0]
+    sl = np.asarray(_f64(seqlens)).astype(np.int64)
+    L = int(sl.max())
+    kc = np.zeros((B, L, heads, w))
+    vc = np.zeros((B, L, vp.shape[1], vp.shape[-1]))
+    for b in range(B):
+        rows = paged_rows(block_table, seqlens, page_size, b)
+        kc[b, :rows.size] = kp[rows]
+        vc[b, :rows.size] = vp[rows]
+    return diffattn_gda_decode(q, kc, vc, sl, lam, lam_init, n_signal, norm_weight, eps, norm,
+                               apply_scale)
+
+
 # --------------------------------------------------------------------------------------------
 # variable-length prefill (packed sequences; the operator per sequence is unchanged)
 # --------------------------------------------------------------------------------------------

@@ -406,6 +406,21 @@ def test_gda_validation(L):
     assert dec(ws_bytes=need - 1) == -8
     assert dec(ws=ctypes.c_void_p(0x10010)) == -8
 
+    # paged: the workspace is sized for max_pages * page_size keys (32 pages of 128 here)
+    def decp(ns=12, nn=3, d=128, ps=128, mp=32, table=FAKE, seqlens=FAKE, ws_bytes=need, flags=6):
+        return L.diffattn_gda_decode_paged(FAKE, FAKE, FAKE, table, seqlens, FAKE, FAKE, 0.5, None,
+                                           1e-5, 8, ns, nn, d, 2 * d, 500, ps, mp, flags, 0, FAKE,
+                                           ws_bytes, None)
+
+    assert decp(table=None) == -1
+    assert decp(seqlens=None) == -1
+    assert decp(flags=16) == -1
+    assert decp(ns=12, nn=5) == -2
+    assert decp(d=64) == -2
+    assert decp(ps=0) == -2
+    assert decp(table=ctypes.c_void_p(0x10002)) == -4
+    assert decp(ws_bytes=need - 1) == -8
+
 
 def test_v2_decode_fp8_paged_validation(L):
     n = ctypes.c_size_t(0)

@@ -202,6 +202,74 @@ def test_gda_decode_small(B, L, Hs, Hn, ragged):
     da.diffattn_device_status()
 
 
+def _paged(k_cache, v_cache, ps, seed):
+    """The caches cut into pages of ps tokens (the last page padded), the pages moved to a seeded
+    random order in the pools, and the block table that finds them there."""
+    B, L = k_cache.shape[:2]
+    mp = (L + ps - 1) // ps
+    pad = mp * ps - L
+    if pad:
+        k_cache = torch.cat([k_cache, torch.zeros_like(k_cache[:, :pad])], 1)
+        v_cache = torch.cat([v_cache, torch.zeros_like(v_cache[:, :pad])], 1)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    table = torch.randperm(B * mp, generator=g).to(torch.int32).view(B, mp)
+    order = torch.argsort(table.flatten())
+    k_pool = k_cache.reshape(B * mp, ps, *k_cache.shape[2:])[order].contiguous()
+    v_pool = v_cache.reshape(B * mp, ps, *v_cache.shape[2:])[order].contiguous()
+    return k_pool, v_pool, table
+
+
+# (B, L, Hs, Hn, page size, ragged): pages of 16 to 256 tokens, group sizes 1 to 4, a last page
+# partly used, one-key sequences
+GDA_DECODE_PAGED_CASES = [(2, 300, 4, 1, 16, True), (3, 1000, 12, 3, 64, True),
+                          (2, 777, 6, 2, 256, False), (4, 129, 3, 3, 128, True)]
+
+
+@pytest.mark.parametrize("B,L,Hs,Hn,ps,ragged", GDA_DECODE_PAGED_CASES)
+def test_gda_decode_paged(B, L, Hs, Hn, ps, ragged):
+    """Grouped decode over shuffled pages: against the oracle's paged composition, and bit-equal
+    to the contiguous grouped decode on the same keys."""
+    inp = make_gda_decode_inputs(B, L, Hs, Hn, 128, 256, seed=41 + L, ragged=ragged)
+    li = ref.lambda_init(inp.layer)
+    w = torch.linspace(0.8, 1.2, 256, dtype=torch.float32)
+    k_pool, v_pool, table = _paged(inp.k_cache, inp.v_cache, ps, seed=43 + ps)
+    got = da.diffattn_gda_decode_paged(inp.q.to(DEV), k_pool.to(DEV), v_pool.to(DEV),
+                                       table.to(DEV), inp.seqlens.to(DEV), inp.lam.to(DEV), Hs,
+                                       li, norm_weight=w.to(DEV))
+    want = ref.diffattn_gda_decode_paged(inp.q, k_pool, v_pool, table, inp.seqlens, inp.lam, li,
+                                         Hs, norm_weight=w)
+    assert_bf16(got, want)
+    contiguous = da.diffattn_gda_decode(inp.q.to(DEV), inp.k_cache.to(DEV), inp.v_cache.to(DEV),
+                                        inp.lam.to(DEV), Hs, li, seqlens=inp.seqlens.to(DEV),
+                                        norm_weight=w.to(DEV))
+    torch.cuda.synchronize()
+    da.diffattn_device_status()
+    assert torch.equal(got, contiguous)
+
+
+def test_gda_decode_paged_bad_page_is_reported():
+    """A used block-table entry outside the pool reads page 0 instead (nothing faults) and the host
+    sees DIFFATTN_ERR_INDEX; entries past a sequence's keys are not read."""
+    inp = make_gda_decode_inputs(2, 256, 4, 2, 128, 256, seed=47)
+    k_pool, v_pool, table = _paged(inp.k_cache, inp.v_cache, 64, seed=48)
+    seqlens = torch.tensor([256, 60], dtype=torch.int32)
+    ok_table = table.clone()
+    ok_table[1, 1:] = 10_000  # past sequence 1's 60 keys: never read
+    da.diffattn_gda_decode_paged(inp.q.to(DEV), k_pool.to(DEV), v_pool.to(DEV), ok_table.to(DEV),
+                                 seqlens.to(DEV), inp.lam.to(DEV), 4, 0.5)
+    torch.cuda.synchronize()
+    da.diffattn_device_status()  # nothing flagged
+    bad = table.clone()
+    bad[0, 2] = 10_000  # keys 128..191 of sequence 0
+    da.diffattn_gda_decode_paged(inp.q.to(DEV), k_pool.to(DEV), v_pool.to(DEV), bad.to(DEV),
+                                 seqlens.to(DEV), inp.lam.to(DEV), 4, 0.5)
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_device_status()
+    assert e.value.status == -9  # DIFFATTN_ERR_INDEX
+    da.diffattn_device_status()
+
+
 def test_gda_decode_matches_prefill_last_row():
     inp = make_gda_inputs(1, 384, 6, 2, 128, 256, seed=29, device=DEV)
     pre = da.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, 6, 0.5)
@@ -253,4 +321,33 @@ def test_gda_decode_32k_full():
                                    inp.lam.cpu(), li, 12)
     assert_bf16(out[sample], want)
     del inp
+    torch.cuda.empty_cache()
+
+
+def test_gda_decode_paged_32k_full():
+    """The same grouped decode over shuffled 64-token pages (the bench's paged layout): bit-equal
+    to the contiguous call for every sequence and head, and 2 sampled sequences against the
+    oracle's paged composition."""
+    inp = make_gda_decode_inputs(64, 32768, 12, 3, 128, 256, seed=5300, device=DEV, ragged=True)
+    li = ref.lambda_init(inp.layer)
+    flat = da.diffattn_gda_decode(inp.q, inp.k_cache, inp.v_cache, inp.lam, 12, li,
+                                  seqlens=inp.seqlens)
+    k_pool, v_pool, table = _paged(inp.k_cache, inp.v_cache, 64, seed=5301)
+    del inp.k_cache, inp.v_cache
+    torch.cuda.empty_cache()
+    table = table.to(DEV)
+    paged = da.diffattn_gda_decode_paged(inp.q, k_pool, v_pool, table, inp.seqlens, inp.lam, 12, li)
+    torch.cuda.synchronize()
+    da.diffattn_device_status()
+    assert torch.equal(flat, paged)
+    sample = [5, 44]
+    pages = sorted({int(x) for s_ in sample for x in table[s_].cpu().tolist()})
+    remap = {pg: i for i, pg in enumerate(pages)}
+    sub_table = torch.tensor([[remap[int(x)] for x in table[s_].cpu().tolist()] for s_ in sample],
+                             dtype=torch.int32)
+    idx = torch.tensor(pages, device=DEV)
+    want = ref.diffattn_gda_decode_paged(inp.q[sample].cpu(), k_pool[idx].cpu(), v_pool[idx].cpu(),
+                                         sub_table, inp.seqlens[sample].cpu(), inp.lam.cpu(), li, 12)
+    assert_bf16(paged[sample], want)
+    del k_pool, v_pool
     torch.cuda.empty_cache()

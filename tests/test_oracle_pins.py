@@ -603,6 +603,38 @@ def pin_gda_varlen():
     assert np.allclose(a[:3], b[:3]) and np.allclose(a[9], b[9]) and not np.allclose(a[3:9], b[3:9])
 
 
+def pin_gda_decode_paged():
+    """Paged grouped decode equals the contiguous grouped decode over the same keys: identity
+    table, then the pool's pages shuffled with the table following; ragged lengths."""
+    rng = np.random.default_rng(29)
+    B, L, Hs, Hn, d, dv, ps = 3, 17, 4, 2, 4, 8, 5
+    max_pages = (L + ps - 1) // ps
+    q = rng.standard_normal((B, Hs + Hn, d))
+    kc = rng.standard_normal((B, max_pages * ps, Hs + Hn, d))
+    vc = rng.standard_normal((B, max_pages * ps, Hs, dv))
+    seqlens = np.array([17, 1, 9])
+    lam = np.array([0.2, 0.5, 0.7, 0.9])
+    want = ref.diffattn_gda_decode(q, kc, vc, seqlens, lam, 0.4, Hs)
+    k_pool = kc.reshape(B * max_pages, ps, Hs + Hn, d)
+    v_pool = vc.reshape(B * max_pages, ps, Hs, dv)
+    table = np.arange(B * max_pages).reshape(B, max_pages)
+    got = ref.diffattn_gda_decode_paged(q, k_pool, v_pool, table, seqlens, lam, 0.4, Hs)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    perm = rng.permutation(B * max_pages)
+    k_sh = np.empty_like(k_pool); v_sh = np.empty_like(v_pool)
+    k_sh[perm], v_sh[perm] = k_pool, v_pool
+    got2 = ref.diffattn_gda_decode_paged(q, k_sh, v_sh, perm[table], seqlens, lam, 0.4, Hs)
+    assert np.allclose(got2, want, rtol=1e-12, atol=1e-12)
+    # keys past a sequence's length (rows 1.. of the one-key sequence's page) do not reach it;
+    # a key inside it (row 0 of sequence 0's first page) does
+    k_sh2 = k_sh.copy(); k_sh2[perm[table[1, 0]], 1:] += rng.standard_normal((ps - 1, Hs + Hn, d))
+    got3 = ref.diffattn_gda_decode_paged(q, k_sh2, v_sh, perm[table], seqlens, lam, 0.4, Hs)
+    assert np.allclose(got3, want, rtol=1e-12, atol=1e-12)
+    k_sh3 = k_sh.copy(); k_sh3[perm[table[0, 0]], 0] += rng.standard_normal((Hs + Hn, d))
+    got4 = ref.diffattn_gda_decode_paged(q, k_sh3, v_sh, perm[table], seqlens, lam, 0.4, Hs)
+    assert not np.allclose(got4[0], want[0]) and np.allclose(got4[1:], want[1:])
+
+
 def pin_gda_decode_is_last_prefill_row():
     """Grouped decode equals the last row of a causal grouped prefill over the same keys."""
     rng = np.random.default_rng(47)
@@ -623,7 +655,7 @@ PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, p
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
         pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen, pin_varlen_qk,
         pin_v2_varlen, pin_paged_prefill, pin_bwd_varlen, pin_gda, pin_gda_varlen,
-        pin_gda_decode_is_last_prefill_row]
+        pin_gda_decode_paged, pin_gda_decode_is_last_prefill_row]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
