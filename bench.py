@@ -731,6 +731,49 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del ginp, gout
         torch.cuda.empty_cache()
 
+        # the last 1024-token chunk of each prompt against its 4096 keys, keys packed with offsets
+        # of their own, then in a pool of shuffled 256-token pages
+        Lq, Lk = 1024, gc["N"]
+        cin = make_gda_inputs(gc["B"], Lk, gc["Hs"], gc["Hn"], gc["d"], gc["dv"], seed=5050 + rank,
+                              device=dev)
+        heads = gc["Hs"] + gc["Hn"]
+        ck, cv = cin.k.reshape(-1, heads, gc["d"]), cin.v.reshape(-1, gc["Hs"], gc["dv"])
+        cq = cin.q[:, Lk - Lq:].reshape(-1, heads, gc["d"]).contiguous()
+        ccu_q = torch.arange(gc["B"] + 1, dtype=torch.int32, device=dev) * Lq
+        ccu_k = torch.arange(gc["B"] + 1, dtype=torch.int32, device=dev) * Lk
+        cout = torch.empty((gc["B"] * Lq, gc["Hs"], gc["dv"]), dtype=torch.bfloat16, device=dev)
+        cws = torch.empty(da.diffattn_gda_fwd_workspace_size(gc["B"], Lq, gc["Hs"], gc["Hn"]),
+                          dtype=torch.uint8, device=dev)
+        t = timer(lambda: da.diffattn_gda_fwd_varlen_qk(cq, ck, cv, ccu_q, ccu_k, cin.lam, gc["Hs"],
+                                                        li_g, max_seqlen_q=Lq, max_seqlen_k=Lk,
+                                                        workspace=cws, out=cout),
+                  max(5, min(50, args.steps)), status=status)
+        cpairs = float(gc["B"] * gc["Hs"] * (Lq * (Lk - Lq) + Lq * (Lq + 1) // 2))
+        r = tensor_roof(cpairs * method_per_pair, t, peaks, peak_src)
+        extra["gda_chunk"] = compact(r["achieved"], "TFLOP/s", t, r,
+                                     f"last {Lq}-query chunk of B{gc['B']} prompts over {Lk} keys, "
+                                     f"12 signal heads over 3 noise heads", world,
+                                     flops_per_pair=method_per_pair)
+        cps = 256
+        cmp_ = Lk // cps
+        cgp = torch.Generator(device="cpu")
+        cgp.manual_seed(5060 + rank)
+        ctable = torch.randperm(gc["B"] * cmp_, generator=cgp).to(torch.int32).view(gc["B"], cmp_).to(dev)
+        corder = torch.argsort(ctable.flatten())
+        ck_pool = cin.k.reshape(gc["B"] * cmp_, cps, heads, gc["d"])[corder].contiguous()
+        cv_pool = cin.v.reshape(gc["B"] * cmp_, cps, gc["Hs"], gc["dv"])[corder].contiguous()
+        csk = torch.full((gc["B"],), Lk, dtype=torch.int32, device=dev)
+        t = timer(lambda: da.diffattn_gda_fwd_paged(cq, ck_pool, cv_pool, ccu_q, csk, ctable,
+                                                    cin.lam, gc["Hs"], li_g, max_seqlen_q=Lq,
+                                                    max_seqlen_k=Lk, workspace=cws, out=cout),
+                  max(5, min(50, args.steps)), status=status)
+        r = tensor_roof(cpairs * method_per_pair, t, peaks, peak_src)
+        extra["gda_chunk_paged"] = compact(r["achieved"], "TFLOP/s", t, r,
+                                           f"the gda_chunk line, keys in shuffled {cps}-token pages",
+                                           world, flops_per_pair=method_per_pair)
+        del cin, ck, cv, cq, cout, cws, ck_pool, cv_pool, ctable
+        torch.cuda.empty_cache()
+
         # the same heads over the packed sequences of the varlen line
         lens = varlen_lengths()
         total = int(sum(lens))

@@ -147,6 +147,14 @@ _SIGNATURES = {
                                   + [ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
                                   + [ctypes.c_int] * 10
                                   + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_gda_fwd_varlen_qk": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int] * 4
+                                   + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                                      ctypes.c_float] + [ctypes.c_int] * 7
+                                   + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_gda_fwd_paged": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 6
+                               + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
+                               + [ctypes.c_int] * 7
+                               + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_gda_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.c_void_p,
                                                                     ctypes.c_float]
                             + [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_size_t,
@@ -1079,6 +1087,96 @@ def diffattn_gda_fwd_varlen(q, k, v, cu_seqlens, lam, n_signal: int, lambda_init
                                          _ptr(norm_weight), float(eps), B, int(n_signal), n_noise,
                                          d, dv, _train_flags(causal, norm, scale), DIFFATTN_BF16,
                                          _ptr(workspace), ws_bytes, _stream(stream)))
+    return out
+
+
+def _gda_ws(noise_pass, workspace, B, max_seqlen, n_signal, n_noise, d, dv, device):
+    """The two-launch form's workspace (allocated here if not given), or none."""
+    if not noise_pass:
+        return None, 0
+    need = diffattn_gda_fwd_workspace_size(max(1, B), max_seqlen, int(n_signal), n_noise, d, dv)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if workspace is None:
+        return None, 0
+    _dev("workspace", workspace)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def diffattn_gda_fwd_varlen_qk(q, k, v, cu_seqlens_q, cu_seqlens_k, lam, n_signal: int,
+                               lambda_init: float = 0.0, max_seqlen_q=None, max_seqlen_k=None,
+                               norm_weight=None, eps: float = 1e-5, causal: bool = True,
+                               norm: bool = True, scale: bool = True, noise_pass: bool = True,
+                               workspace=None, out=None, stream=None):
+    """Grouped prefill with each sequence's queries at the end of its keys: q [total_q,
+    n_signal + n_noise, d], k [total_k, n_signal + n_noise, d], v [total_k, n_signal, dv],
+    cu_seqlens_q / cu_seqlens_k int32 [B + 1] on the device."""
+    _dev("q", q, torch.bfloat16)
+    total_q, heads, d = q.shape
+    n_noise = heads - int(n_signal)
+    _dev("k", k, torch.bfloat16)
+    _dev("v", v, torch.bfloat16)
+    total_k, dv = k.shape[0], v.shape[-1]
+    if k.shape != (total_k, heads, d) or v.shape[:2] != (total_k, n_signal):
+        raise ValueError("k must be [total_k, n_signal + n_noise, d] and v [total_k, n_signal, dv]")
+    _dev("cu_seqlens_q", cu_seqlens_q, torch.int32)
+    _dev("cu_seqlens_k", cu_seqlens_k, torch.int32)
+    B = cu_seqlens_q.numel() - 1
+    if max_seqlen_q is None:
+        max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B > 0 else 1
+    if max_seqlen_k is None:
+        max_seqlen_k = int((cu_seqlens_k[1:] - cu_seqlens_k[:-1]).max().item()) if B > 0 else 1
+    mq, mk = max(1, int(max_seqlen_q)), max(1, int(max_seqlen_k))
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if out is None:
+        out = torch.zeros((total_q, int(n_signal), dv), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    workspace, ws_bytes = _gda_ws(noise_pass, workspace, B, mq, n_signal, n_noise, d, dv, q.device)
+    _check(lib().diffattn_gda_fwd_varlen_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                            _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk,
+                                            total_q, total_k, _ptr(lam), float(lambda_init),
+                                            _ptr(norm_weight), float(eps), B, int(n_signal),
+                                            n_noise, d, dv, _train_flags(causal, norm, scale),
+                                            DIFFATTN_BF16, _ptr(workspace), ws_bytes,
+                                            _stream(stream)))
+    return out
+
+
+def diffattn_gda_fwd_paged(q, k_pool, v_pool, cu_seqlens_q, seqlens_k, block_table, lam,
+                           n_signal: int, lambda_init: float = 0.0, max_seqlen_q=None,
+                           max_seqlen_k=None, norm_weight=None, eps: float = 1e-5,
+                           causal: bool = True, norm: bool = True, scale: bool = True,
+                           noise_pass: bool = True, workspace=None, out=None, stream=None):
+    """Grouped prefill of packed queries q [total_q, n_signal + n_noise, d] against keys in page
+    pools k_pool [num_pages, page_size, n_signal + n_noise, d], v_pool [.., n_signal, dv];
+    sequence b has seqlens_k[b] keys through block_table[b] and its queries are the last of those
+    positions."""
+    _dev("q", q, torch.bfloat16)
+    total_q, heads, d = q.shape
+    n_noise = heads - int(n_signal)
+    B, mq, mk = _paged_args(q, k_pool, v_pool, cu_seqlens_q, seqlens_k, block_table,
+                            max_seqlen_q, max_seqlen_k)
+    num_pages, page_size, dv = k_pool.shape[0], k_pool.shape[1], v_pool.shape[-1]
+    if (k_pool.shape != (num_pages, page_size, heads, d)
+            or v_pool.shape[:3] != (num_pages, page_size, n_signal)):
+        raise ValueError("pools must be [num_pages, page_size, n_signal + n_noise, d] and "
+                         "[num_pages, page_size, n_signal, dv]")
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if out is None:
+        out = torch.zeros((total_q, int(n_signal), dv), dtype=torch.bfloat16, device=q.device)
+    _dev("out", out, torch.bfloat16)
+    workspace, ws_bytes = _gda_ws(noise_pass, workspace, B, mq, n_signal, n_noise, d, dv, q.device)
+    _check(lib().diffattn_gda_fwd_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(out),
+                                        _ptr(cu_seqlens_q), _ptr(seqlens_k), _ptr(block_table), mq,
+                                        mk, total_q, num_pages, page_size, block_table.shape[1],
+                                        _ptr(lam), float(lambda_init), _ptr(norm_weight),
+                                        float(eps), B, int(n_signal), n_noise, d, dv,
+                                        _train_flags(causal, norm, scale), DIFFATTN_BF16,
+                                        _ptr(workspace), ws_bytes, _stream(stream)))
     return out
 
 

@@ -1649,6 +1649,124 @@ DIFFATTN_API int diffattn_gda_fwd_varlen(const void* q, const void* k, const voi
   return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
 }
 
+// grouped prefill with queries at the end of their keys: the keys packed with offsets of their
+// own (koff) or in page pools (paged); the remaining arguments as diffattn_gda_fwd_varlen
+static int gda_prefill_qk(const char* fn, const void* q, const void* k, const void* v, void* out,
+                          const int* cu_q, const int* cu_k, const int* seqlens_k,
+                          const int* block_table, int max_q, int max_k, int total_q, int total_k,
+                          int num_pages, int page_size, int max_pages, const float* lambda,
+                          float lambda_init, const float* norm_weight, float eps, int B,
+                          int n_signal, int n_noise, int d, int dv, int flags, int dtype,
+                          void* workspace, size_t ws_bytes, void* stream) {
+  constexpr int kFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kFlags) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "%s: eps must be > 0 with DIFFATTN_NORM", fn);
+  if (dtype != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: dtype must be DIFFATTN_BF16", fn);
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  if (d != 128 || dv != 256)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need d = 128 and dv = 256 (got d=%d dv=%d)", fn, d, dv);
+  const int heads = n_signal + n_noise;
+  const long long tiles = (static_cast<long long>(max_q) + 127) / 128 * B * n_signal;
+  const long long krows = block_table ? static_cast<long long>(num_pages) * page_size : total_k;
+  if (tiles * 2 > 0x7fffffffLL || krows * heads > (1LL << 34) ||
+      static_cast<long long>(total_q) * heads > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: problem too large for one launch", fn);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || !aligned(cu_q, 4) || (cu_k && !aligned(cu_k, 4)) ||
+      (seqlens_k && !aligned(seqlens_k, 4)) || (block_table && !aligned(block_table, 4)) ||
+      (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  if (workspace) {  // the two-launch form: statistics of B sequences of up to max_q query rows
+    size_t need = 0;
+    diffattn_gda_fwd_workspace_size(B, max_q, n_signal, n_noise, d, dv, &need);
+    if (ws_bytes < need || !aligned(workspace, 256))
+      return fail(DIFFATTN_ERR_WORKSPACE, "%s: need a 256-byte aligned workspace of %zu bytes", fn,
+                  need);
+  }
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = max_q;
+  p.units = n_signal;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_GDA;
+  p.q_heads = heads;
+  p.kv_heads = heads;
+  p.q_cols = d;
+  p.k_cols = d;
+  p.group = n_signal / n_noise;
+  p.lambda = lambda;
+  p.lam_logit = nullptr;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  p.cu_seqlens = cu_q;
+  p.total = total_q;
+  p.max_seqlen_k = max_k;
+  if (block_table) {
+    p.seqlens_k = seqlens_k;
+    p.block_table = block_table;
+    p.page_size = page_size;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+  } else {
+    p.cu_seqlens_k = cu_k;
+    p.total_k = total_k;
+  }
+  if (workspace) p.gda_noise = static_cast<float*>(workspace);
+  return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
+}
+
+DIFFATTN_API int diffattn_gda_fwd_varlen_qk(const void* q, const void* k, const void* v, void* out,
+                                            const int* cu_seqlens_q, const int* cu_seqlens_k,
+                                            int max_seqlen_q, int max_seqlen_k, int total_q,
+                                            int total_k, const float* lambda, float lambda_init,
+                                            const float* norm_weight, float eps, int B,
+                                            int n_signal, int n_noise, int d, int dv, int flags,
+                                            int dtype, void* workspace, size_t ws_bytes,
+                                            void* stream) {
+  const char* fn = "diffattn_gda_fwd_varlen_qk";
+  if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (B < 1 || max_seqlen_q < 1 || total_q < 1 || max_seqlen_q > total_q ||
+      max_seqlen_k < max_seqlen_q || max_seqlen_k > total_k)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need B >= 1, 1 <= max_seqlen_q <= total_q and "
+                "max_seqlen_q <= max_seqlen_k <= total_k", fn);
+  return gda_prefill_qk(fn, q, k, v, out, cu_seqlens_q, cu_seqlens_k, nullptr, nullptr,
+                        max_seqlen_q, max_seqlen_k, total_q, total_k, 0, 0, 0, lambda, lambda_init,
+                        norm_weight, eps, B, n_signal, n_noise, d, dv, flags, dtype, workspace,
+                        ws_bytes, stream);
+}
+
+DIFFATTN_API int diffattn_gda_fwd_paged(const void* q, const void* k_pool, const void* v_pool,
+                                        void* out, const int* cu_seqlens_q, const int* seqlens_k,
+                                        const int* block_table, int max_seqlen_q, int max_seqlen_k,
+                                        int total_q, int num_pages, int page_size, int max_pages,
+                                        const float* lambda, float lambda_init,
+                                        const float* norm_weight, float eps, int B, int n_signal,
+                                        int n_noise, int d, int dv, int flags, int dtype,
+                                        void* workspace, size_t ws_bytes, void* stream) {
+  const char* fn = "diffattn_gda_fwd_paged";
+  if (!q || !k_pool || !v_pool || !out || !cu_seqlens_q || !seqlens_k || !block_table || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (int rc = check_paged_prefill(fn, B, max_seqlen_q, max_seqlen_k, total_q, num_pages,
+                                   page_size, max_pages))
+    return rc;
+  return gda_prefill_qk(fn, q, k_pool, v_pool, out, cu_seqlens_q, nullptr, seqlens_k,
+                        block_table, max_seqlen_q, max_seqlen_k, total_q, 0, num_pages, page_size,
+                        max_pages, lambda, lambda_init, norm_weight, eps, B, n_signal, n_noise, d,
+                        dv, flags, dtype, workspace, ws_bytes, stream);
+}
+
 DIFFATTN_API int diffattn_gda_decode(const void* q, const void* k_cache, const void* v_cache,
                                      const int* seqlens, void* out, const float* lambda,
                                      float lambda_init, const float* norm_weight, float eps, int B,

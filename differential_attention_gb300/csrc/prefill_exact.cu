@@ -914,23 +914,31 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
 cudaError_t status_prefill_exact(int* v) { return read_clear_status(v); }
 
 cudaError_t launch_prefill_exact(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
-  if (p.mode == MODE_GDA) {  // grouped: batched or packed, bf16 scores only
-    if (p.qk_fp8 || p.cu_seqlens_k || p.block_table) return cudaErrorNotSupported;
+  if (p.mode == MODE_GDA) {  // grouped: batched, packed, keys of their own or paged; bf16 scores
+    if (p.qk_fp8) return cudaErrorNotSupported;
+    const bool koff = p.cu_seqlens && p.cu_seqlens_k;
+    const bool paged = p.cu_seqlens && p.block_table;
     if (p.dqk == 128 && p.dv == 256) {
+      auto launch = [&](const Problem& q) {
+        return paged  ? exact::launch_cfg<128, 256, false, false, exact::kKeysPaged, true>(q, s, err, err_len)
+               : koff ? exact::launch_cfg<128, 256, false, false, exact::kKeysOffset, true>(q, s, err, err_len)
+                      : exact::launch_cfg<128, 256, false, false, exact::kKeysShared, true>(q, s, err, err_len);
+      };
       if (!p.gda_noise) {
         Problem q = p;
         q.gda_phase = 0;
-        return exact::launch_cfg<128, 256, false, false, exact::kKeysShared, true>(q, s, err, err_len);
+        return launch(q);
       }
       // two launches: the noise maps' statistics once per noise head, then the signal heads
       Problem q = p;
       q.n_pad = (p.N + exact::BM - 1) / exact::BM * exact::BM;
       q.gda_phase = 1;
-      cudaError_t e = exact::launch_cfg<128, 256, false, false, exact::kKeysShared, true>(q, s, err, err_len);
+      cudaError_t e = launch(q);
       if (e != cudaSuccess) return e;
       q.gda_phase = 2;
-      return exact::launch_cfg<128, 256, false, false, exact::kKeysShared, true>(q, s, err, err_len);
+      return launch(q);
     }
+    if (koff || paged) return cudaErrorNotSupported;
     if (p.dqk == 64 && p.dv == 128) {  // (one launch: the two-launch form needs d = 128)
       Problem q = p;
       q.gda_phase = 0;

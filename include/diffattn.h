@@ -675,6 +675,41 @@ DIFFATTN_API int diffattn_gda_fwd_varlen(const void* q, const void* k, const voi
                                          int n_noise, int d, int dv, int flags, int dtype,
                                          void* workspace, size_t ws_bytes, void* stream);
 
+/* Grouped prefill with each sequence's queries at the end of its keys (chunked prompts, new tokens
+ * over a cache): diffattn_gda_fwd's operator with the key layout of diffattn_fwd_varlen_qk
+ * (keys packed with offsets of their own) or of diffattn_fwd_paged (keys in page pools).
+ *   q, out : device [total_q, n_signal + n_noise, d] and [total_q, n_signal, dv], packed by
+ *            cu_seqlens_q as in diffattn_gda_fwd_varlen
+ *   k, v   : device [total_k, n_signal + n_noise, d] and [total_k, n_signal, dv] with
+ *            cu_seqlens_k (varlen_qk); or pools k_pool [num_pages, page_size, n_signal + n_noise, d]
+ *            and v_pool [num_pages, page_size, n_signal, dv] with seqlens_k and block_table
+ *            (paged; page_size a multiple of 128)
+ *   the offsets, lengths and table are checked on the device as for the ungrouped forms
+ *   workspace, ws_bytes : as diffattn_gda_fwd, of diffattn_gda_fwd_workspace_size(B,
+ *            max_seqlen_q, ...) bytes, or NULL (each signal head then forms its noise map's
+ *            statistics itself)
+ * Rows of `out` that belong to no sequence are not written.
+ * Supported: dtype DIFFATTN_BF16, flags CAUSAL | NORM | SCALE, d = 128, dv = 256, n_signal a
+ * multiple of n_noise.
+ * Errors: as diffattn_gda_fwd; ERR_SHAPE as diffattn_fwd_varlen_qk / diffattn_fwd_paged.
+ */
+DIFFATTN_API int diffattn_gda_fwd_varlen_qk(const void* q, const void* k, const void* v, void* out,
+                                            const int* cu_seqlens_q, const int* cu_seqlens_k,
+                                            int max_seqlen_q, int max_seqlen_k, int total_q,
+                                            int total_k, const float* lambda, float lambda_init,
+                                            const float* norm_weight, float eps, int B,
+                                            int n_signal, int n_noise, int d, int dv, int flags,
+                                            int dtype, void* workspace, size_t ws_bytes,
+                                            void* stream);
+DIFFATTN_API int diffattn_gda_fwd_paged(const void* q, const void* k_pool, const void* v_pool,
+                                        void* out, const int* cu_seqlens_q, const int* seqlens_k,
+                                        const int* block_table, int max_seqlen_q, int max_seqlen_k,
+                                        int total_q, int num_pages, int page_size, int max_pages,
+                                        const float* lambda, float lambda_init,
+                                        const float* norm_weight, float eps, int B, int n_signal,
+                                        int n_noise, int d, int dv, int flags, int dtype,
+                                        void* workspace, size_t ws_bytes, void* stream);
+
 /* Grouped decode: one query token per sequence over its cached keys 0 .. seqlens[b]-1, with the
  * head split of diffattn_gda_fwd.
  *   q       : device bf16 [B, n_signal + n_noise, d]

@@ -630,6 +630,39 @@ def diffattn_gda_fwd_varlen(q, k, v, cu_seqlens, lam, lam_init: float, n_signal:
     return out
 
 
+def diffattn_gda_fwd_varlen_qk(q, k, v, cu_seqlens_q, cu_seqlens_k, lam, lam_init: float,
+                               n_signal: int, norm_weight=None, eps: float = 1e-5,
+                               norm: bool = True, apply_scale: bool = True, causal: bool = True):
+    """`diffattn_gda_fwd` where sequence b has keys k, v rows cu_seqlens_k[b] .. and queries q
+    rows cu_seqlens_q[b] .., its last Lq positions (as in `diffattn_fwd_varlen_qk`). q, k
+    [*, Hs + Hn, d], v [*, Hs, dv]. Each sequence's queries are placed at their positions among
+    Lk and the grouped prefill is taken on those rows only. Returns float64 [total_q, Hs, dv];
+    rows in no sequence are 0."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    out = np.zeros((q.shape[0], n_signal, v.shape[-1]))
+    for (q0, q1), (k0, k1) in zip(varlen_segments(cu_seqlens_q), varlen_segments(cu_seqlens_k)):
+        if q1 == q0:
+            continue
+        pos = query_positions(q1 - q0, k1 - k0)
+        q_full = np.zeros((1, k1 - k0) + q.shape[1:])
+        q_full[0, pos] = q[q0:q1]
+        out[q0:q1] = diffattn_gda_fwd(q_full, k[None, k0:k1], v[None, k0:k1], lam, lam_init,
+                                      n_signal, norm_weight, eps, norm, apply_scale, causal,
+                                      rows=pos)[0]
+    return out
+
+
+def diffattn_gda_fwd_paged(q, k_pool, v_pool, cu_seqlens_q, seqlens_k, block_table, lam,
+                           lam_init: float, n_signal: int, norm_weight=None, eps: float = 1e-5,
+                           norm: bool = True, apply_scale: bool = True, causal: bool = True):
+    """`diffattn_gda_fwd_varlen_qk` with each sequence's keys read from page pools k_pool
+    [num_pages, page_size, Hs + Hn, d], v_pool [.., Hs, dv] through block_table [B, max_pages]."""
+    k, cu_k = gather_pages(k_pool, block_table, seqlens_k)
+    v, _ = gather_pages(v_pool, block_table, seqlens_k)
+    return diffattn_gda_fwd_varlen_qk(q, k, v, cu_seqlens_q, cu_k, lam, lam_init, n_signal,
+                                      norm_weight, eps, norm, apply_scale, causal)
+
+
 def diffattn_gda_decode(q, k_cache, v_cache, seqlens, lam, lam_init: float, n_signal: int,
                         norm_weight=None, eps: float = 1e-5, norm: bool = True,
                         apply_scale: bool = True):

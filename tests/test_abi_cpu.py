@@ -391,6 +391,27 @@ def test_gda_validation(L):
     assert fwd_var(ws=ctypes.c_void_p(0x10000), ws_bytes=4 * 3 * 384 * 4 - 4) == -8
     assert fwd_var(ws=ctypes.c_void_p(0x10010), ws_bytes=1 << 20) == -8
 
+    def fwd_qk(mq=16, mk=32, tq=32, tk=64, cu=FAKE, d=128, ws=None, ws_bytes=0):
+        return L.diffattn_gda_fwd_varlen_qk(FAKE, FAKE, FAKE, FAKE, cu, FAKE, mq, mk, tq, tk, FAKE,
+                                            0.5, None, 1e-5, 2, 12, 3, d, 2 * d, 7, 0, ws,
+                                            ws_bytes, None)
+
+    assert fwd_qk(cu=None) == -1
+    assert fwd_qk(mq=64, mk=32) == -2          # more queries than keys
+    assert fwd_qk(mk=128, tk=64) == -2
+    assert fwd_qk(d=64) == -2                  # d = 128 only
+    assert fwd_qk(cu=ctypes.c_void_p(0x10002)) == -4
+    assert fwd_qk(ws=ctypes.c_void_p(0x10000), ws_bytes=4) == -8
+
+    def fwd_pg(ps=128, mq=16, mk=300, tq=32, pages=8, maxp=4, table=FAKE):
+        return L.diffattn_gda_fwd_paged(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, table, mq, mk, tq,
+                                        pages, ps, maxp, FAKE, 0.5, None, 1e-5, 2, 12, 3, 128, 256,
+                                        7, 0, None, 0, None)
+
+    assert fwd_pg(table=None) == -1
+    assert fwd_pg(ps=64) == -2                 # a tile of 128 keys must lie in one page
+    assert fwd_pg(mk=600) == -2                # more keys than max_pages * page_size
+
     n = ctypes.c_size_t(0)
     assert L.diffattn_decode_workspace_size(8, 4096, 12, 128, 256, ctypes.byref(n)) == 0
     need = n.value

@@ -129,6 +129,43 @@ def test_gda_varlen_full():
     assert_bf16(np.concatenate(got), np.concatenate(want))
 
 
+def test_gda_chunk_and_paged_full():
+    """The bench's grouped chunk lines: the last 1024 rows of four 4096-token prompts (12 signal
+    over 3 noise heads) against all their keys, keys packed and in shuffled 256-token pages:
+    bit-identical to each other and to those rows of the whole prompts' grouped prefill; sampled
+    rows against the oracle."""
+    B, Lq, Lk, Hs, Hn = 4, 1024, 4096, 12, 3
+    cin = make_gda_inputs(B, Lk, Hs, Hn, 128, 256, seed=5050, device=DEV)
+    li = da.diffattn_lambda_init(12)
+    heads = Hs + Hn
+    k, v = cin.k.reshape(-1, heads, 128), cin.v.reshape(-1, Hs, 256)
+    q = cin.q[:, Lk - Lq:].reshape(-1, heads, 128).contiguous()
+    cu_q = torch.arange(B + 1, dtype=torch.int32, device=DEV) * Lq
+    cu_k = torch.arange(B + 1, dtype=torch.int32, device=DEV) * Lk
+    out = da.diffattn_gda_fwd_varlen_qk(q, k, v, cu_q, cu_k, cin.lam, Hs, li, max_seqlen_q=Lq,
+                                        max_seqlen_k=Lk)
+    k_pool, v_pool, table = _shuffled_pages(cin.k, cin.v, 256, 5060)
+    sk = torch.full((B,), Lk, dtype=torch.int32, device=DEV)
+    pout = da.diffattn_gda_fwd_paged(q, k_pool, v_pool, cu_q, sk, table, cin.lam, Hs, li,
+                                     max_seqlen_q=Lq, max_seqlen_k=Lk)
+    whole = da.diffattn_gda_fwd(cin.q, cin.k, cin.v, cin.lam, Hs, li)
+    da.diffattn_device_status()
+    assert torch.equal(out, pout)
+    assert torch.equal(out, whole[:, Lk - Lq:].reshape(-1, Hs, 256))
+    rows = _rows(Lq, 16, 32, 5050)
+    lam = cin.lam.cpu().numpy()
+    got, want = [], []
+    for b in (0, 3):
+        sl = lambda t: t[b:b + 1].cpu()
+        w = ref.diffattn_gda_fwd(sl(cin.q), sl(cin.k), sl(cin.v), lam, ref.lambda_init(12), Hs,
+                                 rows=Lk - Lq + rows)[0]
+        want.append(w.reshape(-1, 256))
+        got.append(out[torch.as_tensor(b * Lq + rows, device=DEV)].float().cpu().numpy().reshape(-1, 256))
+    assert_bf16(np.concatenate(got), np.concatenate(want))
+    del cin, k_pool, v_pool, whole
+    torch.cuda.empty_cache()
+
+
 def test_varlen_qk_and_paged_full():
     """The last 1024 rows of four 4096-token prompts against all their keys (queries at the end of
     their keys), contiguous and in shuffled 256-token pages: the two are bit-identical, and

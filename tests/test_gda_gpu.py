@@ -129,6 +129,83 @@ def test_gda_fwd_varlen_bad_offsets_are_reported():
     da.diffattn_device_status()
 
 
+# (query lengths, key lengths, Hs, Hn, causal): a chunk far into a long prefix, decode-like one-row
+# chunks, an empty sequence, whole prompts (Lq = Lk)
+GDA_QK_CASES = [([300, 1, 100, 0, 640], [300, 700, 357, 90, 640], 6, 2, True),
+                ([128, 77], [1000, 77], 12, 3, True),
+                ([50, 200], [260, 200], 4, 1, False)]
+
+
+def _gda_qk_inputs(lq, lk, Hs, Hn, seed):
+    g = torch.Generator().manual_seed(seed)
+    tq, tk = sum(lq), sum(lk)
+    q = (torch.randn((tq, Hs + Hn, 128), generator=g) / 128 ** 0.5).to(torch.bfloat16)
+    k = (torch.randn((tk, Hs + Hn, 128), generator=g) / 128 ** 0.5).to(torch.bfloat16)
+    v = (torch.randn((tk, Hs, 256), generator=g) / 128 ** 0.5).to(torch.bfloat16)
+    lam = 0.2 + 0.6 * torch.rand((Hs,), generator=g)
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lq)]), dtype=torch.int32)
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lk)]), dtype=torch.int32)
+    return q, k, v, lam, cu_q, cu_k
+
+
+def _pool(k, v, lk, ps, seed):
+    """Each sequence's keys cut into pages of ps tokens, the pages shuffled in pools."""
+    B = len(lk)
+    mp = max(1, max((n + ps - 1) // ps for n in lk))
+    g = torch.Generator().manual_seed(seed)
+    table = torch.randperm(B * mp, generator=g).to(torch.int32).view(B, mp)
+    kp = torch.zeros((B * mp, ps) + tuple(k.shape[1:]), dtype=k.dtype)
+    vp = torch.zeros((B * mp, ps) + tuple(v.shape[1:]), dtype=v.dtype)
+    off = 0
+    for b, n in enumerate(lk):
+        for j0 in range(0, n, ps):
+            j1 = min(n, j0 + ps)
+            kp[table[b, j0 // ps], :j1 - j0] = k[off + j0:off + j1]
+            vp[table[b, j0 // ps], :j1 - j0] = v[off + j0:off + j1]
+        off += n
+    return kp, vp, table
+
+
+@pytest.mark.parametrize("noise_pass", [True, False])
+@pytest.mark.parametrize("lq,lk,Hs,Hn,causal", GDA_QK_CASES)
+def test_gda_fwd_varlen_qk_and_paged(lq, lk, Hs, Hn, causal, noise_pass):
+    """Grouped prefill with queries at the end of their keys against the oracle, keys packed with
+    offsets of their own and in shuffled 128-token pages: the two bit-equal."""
+    q, k, v, lam, cu_q, cu_k = _gda_qk_inputs(lq, lk, Hs, Hn, seed=53 + sum(lq))
+    w = _w(256)
+    li = 0.6
+    got = da.diffattn_gda_fwd_varlen_qk(q.to(DEV), k.to(DEV), v.to(DEV), cu_q.to(DEV),
+                                        cu_k.to(DEV), lam.to(DEV), Hs, li, norm_weight=w.to(DEV),
+                                        causal=causal, noise_pass=noise_pass)
+    want = ref.diffattn_gda_fwd_varlen_qk(q, k, v, cu_q, cu_k, lam, li, Hs, norm_weight=w,
+                                          causal=causal)
+    assert_bf16(got, want)
+    kp, vp, table = _pool(k, v, lk, 128, seed=59 + sum(lk))
+    paged = da.diffattn_gda_fwd_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), cu_q.to(DEV),
+                                      torch.tensor(lk, dtype=torch.int32, device=DEV),
+                                      table.to(DEV), lam.to(DEV), Hs, li, norm_weight=w.to(DEV),
+                                      causal=causal, noise_pass=noise_pass)
+    torch.cuda.synchronize()
+    da.diffattn_device_status()
+    assert torch.equal(got, paged)
+
+
+def test_gda_fwd_varlen_qk_chunk_equals_whole_prompt_rows():
+    """The last 388 rows of two 900-token prompts (from row 512: the chunk's query tiles then
+    fall on the whole prompt's tile boundaries) as a chunk over all 900 keys: bit-equal to those
+    rows of the grouped prefill of the whole prompts (same tiles, same arithmetic)."""
+    inp = make_gda_inputs(2, 900, 6, 2, 128, 256, seed=61, device=DEV)
+    whole = da.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, 6, 0.5)
+    q = inp.q[:, 512:].reshape(-1, 8, 128).contiguous()
+    k, v = inp.k.reshape(-1, 8, 128), inp.v.reshape(-1, 6, 256)
+    cu_q = torch.tensor([0, 388, 776], dtype=torch.int32, device=DEV)
+    cu_k = torch.tensor([0, 900, 1800], dtype=torch.int32, device=DEV)
+    chunk = da.diffattn_gda_fwd_varlen_qk(q, k, v, cu_q, cu_k, inp.lam, 6, 0.5)
+    torch.cuda.synchronize()
+    da.diffattn_device_status()
+    assert torch.equal(chunk, whole[:, 512:].reshape(-1, 6, 256))
+
+
 def test_gda_fwd_no_norm_no_scale():
     inp = make_gda_inputs(1, 200, 6, 2, 128, 256, seed=7)
     got = da.diffattn_gda_fwd(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.lam.to(DEV), 6,

@@ -603,6 +603,51 @@ def pin_gda_varlen():
     assert np.allclose(a[:3], b[:3]) and np.allclose(a[9], b[9]) and not np.allclose(a[3:9], b[3:9])
 
 
+def pin_gda_varlen_qk_and_paged():
+    """Grouped prefill with queries at the end of their keys: with Lq = Lk it is the packed grouped
+    prefill; each query row equals that row of the whole sequence's grouped prefill; with one noise
+    head per signal head it is the ungrouped form on the halves stored as heads; paged keys
+    through any table give the same result."""
+    rng = np.random.default_rng(31)
+    Hs, Hn, d, dv = 4, 2, 4, 8
+    lam = np.array([0.3, 0.5, 0.7, 0.9])
+    lk = [9, 1, 6]; lq = [3, 1, 6]
+    cu_k = np.concatenate([[0], np.cumsum(lk)]); cu_q = np.concatenate([[0], np.cumsum(lq)])
+    k = rng.standard_normal((cu_k[-1], Hs + Hn, d)); v = rng.standard_normal((cu_k[-1], Hs, dv))
+    qk = rng.standard_normal((cu_k[-1], Hs + Hn, d))   # queries at every key position
+    q = np.concatenate([qk[cu_k[b + 1] - lq[b]:cu_k[b + 1]] for b in range(3)])
+    for causal in (True, False):
+        got = ref.diffattn_gda_fwd_varlen_qk(q, k, v, cu_q, cu_k, lam, 0.4, Hs, causal=causal)
+        whole = ref.diffattn_gda_fwd_varlen(qk, k, v, cu_k, lam, 0.4, Hs, causal=causal)
+        want = np.concatenate([whole[cu_k[b + 1] - lq[b]:cu_k[b + 1]] for b in range(3)])
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    same = ref.diffattn_gda_fwd_varlen_qk(qk, k, v, cu_k, cu_k, lam, 0.4, Hs)
+    assert np.allclose(same, ref.diffattn_gda_fwd_varlen(qk, k, v, cu_k, lam, 0.4, Hs),
+                       rtol=1e-12, atol=1e-12)
+    # one noise head per signal head: the ungrouped chunked form on [Q1 | Q2] halves
+    H = 3
+    q1, q2 = rng.standard_normal((cu_q[-1], H, d)), rng.standard_normal((cu_q[-1], H, d))
+    k1, k2 = rng.standard_normal((cu_k[-1], H, d)), rng.standard_normal((cu_k[-1], H, d))
+    vv = rng.standard_normal((cu_k[-1], H, dv)); lam3 = np.array([0.2, 0.6, 0.8])
+    g = ref.diffattn_gda_fwd_varlen_qk(np.concatenate([q1, q2], 1), np.concatenate([k1, k2], 1),
+                                       vv, cu_q, cu_k, lam3, 0.3, H)
+    u = ref.diffattn_fwd_varlen_qk(np.concatenate([q1, q2], 2), np.concatenate([k1, k2], 2), vv,
+                                   cu_q, cu_k, lam3, 0.3)
+    assert np.allclose(g, u, rtol=1e-12, atol=1e-12)
+    # paged: pages of 4 keys, shuffled in the pool
+    ps = 4
+    mp = max((n + ps - 1) // ps for n in lk)
+    pool_k = np.zeros((3 * mp, ps, Hs + Hn, d)); pool_v = np.zeros((3 * mp, ps, Hs, dv))
+    perm = rng.permutation(3 * mp); table = perm.reshape(3, mp)
+    for b in range(3):
+        for j in range(lk[b]):
+            pool_k[table[b, j // ps], j % ps] = k[cu_k[b] + j]
+            pool_v[table[b, j // ps], j % ps] = v[cu_k[b] + j]
+    paged = ref.diffattn_gda_fwd_paged(q, pool_k, pool_v, cu_q, np.array(lk), table, lam, 0.4, Hs)
+    assert np.allclose(paged, ref.diffattn_gda_fwd_varlen_qk(q, k, v, cu_q, cu_k, lam, 0.4, Hs),
+                       rtol=1e-12, atol=1e-12)
+
+
 def pin_gda_decode_paged():
     """Paged grouped decode equals the contiguous grouped decode over the same keys: identity
     table, then the pool's pages shuffled with the table following; ragged lengths."""
@@ -655,7 +700,7 @@ PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, p
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
         pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen, pin_varlen_qk,
         pin_v2_varlen, pin_paged_prefill, pin_bwd_varlen, pin_gda, pin_gda_varlen,
-        pin_gda_decode_paged, pin_gda_decode_is_last_prefill_row]
+        pin_gda_varlen_qk_and_paged, pin_gda_decode_paged, pin_gda_decode_is_last_prefill_row]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
