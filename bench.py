@@ -832,6 +832,45 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del gdi, gws, gdout, gk_pool, gv_pool, gtable
         torch.cuda.empty_cache()
 
+        # training on the grouped prefill: forward saving statistics, then every gradient
+        ginp = make_gda_inputs(gc["B"], gc["N"], gc["Hs"], gc["Hn"], gc["d"], gc["dv"],
+                               seed=5000 + rank, device=dev)
+        gws = torch.empty(da.diffattn_gda_fwd_workspace_size(gc["B"], gc["N"], gc["Hs"], gc["Hn"]),
+                          dtype=torch.uint8, device=dev)
+        gdy = make_dout(gc["B"], gc["N"], gc["Hs"], gc["dv"], seed=5300 + rank, device=dev)
+        gw = torch.ones(gc["dv"], dtype=torch.float32, device=dev)
+        gbws = torch.empty(da.diffattn_gda_bwd_workspace_size(gc["B"], gc["N"], gc["Hs"], gc["Hn"]),
+                           dtype=torch.uint8, device=dev)
+        ggrads = dict(dq=torch.empty_like(ginp.q), dk=torch.empty_like(ginp.k),
+                      dv=torch.empty_like(ginp.v),
+                      dlam=torch.empty(gc["Hs"], dtype=torch.float32, device=dev),
+                      dw=torch.empty(gc["dv"], dtype=torch.float32, device=dev))
+        gsaved = {}
+
+        def gfwd():
+            gsaved["out"], gsaved["o_pre"], gsaved["stats"] = da.diffattn_gda_fwd_train(
+                ginp.q, ginp.k, ginp.v, ginp.lam, gc["Hs"], li_g, norm_weight=gw, workspace=gws)
+
+        def gbwd():
+            da.diffattn_gda_bwd(ginp.q, ginp.k, ginp.v, gsaved["o_pre"], gsaved["stats"], gdy,
+                                ginp.lam, gc["Hs"], li_g, norm_weight=gw, workspace=gbws,
+                                grads=ggrads)
+
+        n_steps = max(3, min(20, args.steps))
+        tf_ = timer(gfwd, n_steps, status=status)
+        tb = timer(gbwd, n_steps, status=status)
+        # per (signal head, causal pair): the V1 count with the noise map's scores formed once per
+        # group (2d / G instead of 2d)
+        gbwd_per_pair = BWD_FLOPS_PER_PAIR - 2 * gc["d"] + 2 * gc["d"] / G
+        gpairs = float(gc["B"] * gc["Hs"] * causal_pairs(gc["N"]))
+        r = tensor_roof(gpairs * gbwd_per_pair, tb, peaks, peak_src)
+        extra["gda_backward"] = compact(r["achieved"], "TFLOP/s", tb, r,
+                                        "gda_prefill training: every gradient", world,
+                                        flops_per_pair=gbwd_per_pair,
+                                        fwd_train_ms=round(tf_["ms"], 4))
+        del ginp, gws, gdy, gw, gbws, ggrads, gsaved
+        torch.cuda.empty_cache()
+
     # ======================= V2 decode =======================
     if want("v2_decode"):
         c = dict(V2_DECODE, B=args.decode_batch)

@@ -155,6 +155,16 @@ _SIGNATURES = {
                                + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
                                + [ctypes.c_int] * 7
                                + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_gda_fwd_train": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_float, ctypes.c_void_p,
+                                                                       ctypes.c_float]
+                               + [ctypes.c_int] * 8
+                               + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_gda_bwd_workspace_size": (ctypes.c_int, [ctypes.c_int] * 6
+                                        + [ctypes.POINTER(ctypes.c_size_t)]),
+    "diffattn_gda_bwd": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_float, ctypes.c_void_p,
+                                                                 ctypes.c_float]
+                         + [ctypes.c_void_p] * 5 + [ctypes.c_int] * 8
+                         + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_gda_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.c_void_p,
                                                                     ctypes.c_float]
                             + [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_size_t,
@@ -1178,6 +1188,74 @@ def diffattn_gda_fwd_paged(q, k_pool, v_pool, cu_seqlens_q, seqlens_k, block_tab
                                         _train_flags(causal, norm, scale), DIFFATTN_BF16,
                                         _ptr(workspace), ws_bytes, _stream(stream)))
     return out
+
+
+def diffattn_gda_fwd_train(q, k, v, lam, n_signal: int, lambda_init: float = 0.0,
+                           norm_weight=None, eps: float = 1e-5, causal: bool = True,
+                           norm: bool = True, scale: bool = True, noise_pass: bool = True,
+                           workspace=None, stream=None):
+    """Grouped forward for training: returns (out, o_pre, stats); o_pre [B, N, n_signal, dv] is
+    each signal head's output before the norm and scale, stats [B, n_signal, 2, Npad] the per-row
+    base-2 log-sum-exp of each map."""
+    _dev("q", q, torch.bfloat16)
+    B, N, heads, d = q.shape
+    n_noise = heads - int(n_signal)
+    _dev("k", k, torch.bfloat16)
+    _dev("v", v, torch.bfloat16)
+    dv = v.shape[-1]
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    out = torch.empty((B, N, int(n_signal), dv), dtype=torch.bfloat16, device=q.device)
+    o_pre = torch.empty_like(out)
+    npad = (N + 127) // 128 * 128
+    stats = torch.empty((B, int(n_signal), 2, npad), dtype=torch.float32, device=q.device)
+    workspace, ws_bytes = _gda_ws(noise_pass, workspace, B, N, n_signal, n_noise, d, dv, q.device)
+    _check(lib().diffattn_gda_fwd_train(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(o_pre),
+                                        _ptr(stats), _ptr(lam), float(lambda_init),
+                                        _ptr(norm_weight), float(eps), B, N, int(n_signal),
+                                        n_noise, d, dv, _train_flags(causal, norm, scale),
+                                        DIFFATTN_BF16, _ptr(workspace), ws_bytes, _stream(stream)))
+    return out, o_pre, stats
+
+
+def diffattn_gda_bwd_workspace_size(B: int, N: int, n_signal: int, n_noise: int, d: int = 128,
+                                    dv: int = 256) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().diffattn_gda_bwd_workspace_size(B, N, n_signal, n_noise, d, dv, ctypes.byref(n)))
+    return n.value
+
+
+def diffattn_gda_bwd(q, k, v, o_pre, stats, dout, lam, n_signal: int, lambda_init: float = 0.0,
+                     norm_weight=None, eps: float = 1e-5, causal: bool = True, norm: bool = True,
+                     scale: bool = True, workspace=None, grads=None, stream=None):
+    """Backward of the grouped prefill. Returns dict(dq, dk [B, N, n_signal + n_noise, d], dv,
+    dlam [n_signal], dw)."""
+    _dev("q", q, torch.bfloat16)
+    B, N, heads, d = q.shape
+    n_noise = heads - int(n_signal)
+    dv = v.shape[-1]
+    for name, t in (("k", k), ("v", v), ("o_pre", o_pre), ("dout", dout)):
+        _dev(name, t, torch.bfloat16)
+    _dev("stats", stats, torch.float32)
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if workspace is None:
+        workspace = torch.empty(diffattn_gda_bwd_workspace_size(B, N, int(n_signal), n_noise, d, dv),
+                                dtype=torch.uint8, device=q.device)
+    if grads is None:
+        grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                     dlam=torch.empty((int(n_signal),), dtype=torch.float32, device=q.device),
+                     dw=torch.empty((dv,), dtype=torch.float32, device=q.device))
+    _check(lib().diffattn_gda_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o_pre), _ptr(stats), _ptr(dout),
+                                  _ptr(lam), float(lambda_init), _ptr(norm_weight), float(eps),
+                                  _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]),
+                                  _ptr(grads["dlam"]), _ptr(grads.get("dw")), B, N, int(n_signal),
+                                  n_noise, d, dv, _train_flags(causal, norm, scale), DIFFATTN_BF16,
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
+    return grads
 
 
 def diffattn_gda_decode(q, k_cache, v_cache, lam, n_signal: int, lambda_init: float = 0.0,

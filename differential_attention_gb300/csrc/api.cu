@@ -730,7 +730,8 @@ int bwd_impl(const char* fn, const void* q, const void* k, const void* v, const 
              const float* stats, const void* dout, const float* lambda, float lambda_init,
              const float* norm_weight, float eps, void* dq, void* dk, void* dv, float* dlambda,
              float* dnorm_weight, int B, int N, int H, int d, int dv_width, int flags, int dtype,
-             const int* cu, int total, void* workspace, size_t ws_bytes, void* stream) {
+             const int* cu, int total, void* workspace, size_t ws_bytes, void* stream,
+             int n_noise = 0) {
   if (!q || !k || !v || !o_pre || !stats || !dout || !lambda || !dq || !dk || !dv || !dlambda)
     return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
   constexpr int kTrainFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
@@ -748,7 +749,7 @@ int bwd_impl(const char* fn, const void* q, const void* k, const void* v, const 
       (cu && !aligned(cu, 4)))
     return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
   const long long rows = cu ? total : static_cast<long long>(B) * N;
-  const size_t need = da::backward_workspace_bytes(B, N, H, rows);
+  const size_t need = da::backward_workspace_bytes(B, N, H, rows, n_noise > 0);
   if (!workspace || ws_bytes < need || !aligned(workspace, 256))
     return fail(DIFFATTN_ERR_WORKSPACE, "%s: need a 256-byte aligned workspace of %zu bytes", fn, need);
   rc = check_device();
@@ -776,6 +777,7 @@ int bwd_impl(const char* fn, const void* q, const void* k, const void* v, const 
   a.workspace = workspace;
   a.cu_seqlens = cu;
   a.total = total;
+  a.n_noise = n_noise;
   char err[256] = {0};
   cudaError_t e = da::launch_backward(a, static_cast<cudaStream_t>(stream), err, sizeof(err));
   if (err[0]) return fail(DIFFATTN_ERR_CUDA, "%s: %s", fn, err);
@@ -1581,6 +1583,88 @@ DIFFATTN_API int diffattn_gda_fwd(const void* q, const void* k, const void* v, v
   p.scale = 1.0f / std::sqrt(static_cast<float>(d));
   if (two_launch) p.gda_noise = static_cast<float*>(workspace);
   return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
+}
+
+DIFFATTN_API int diffattn_gda_fwd_train(const void* q, const void* k, const void* v, void* out,
+                                        void* o_pre, float* stats, const float* lambda,
+                                        float lambda_init, const float* norm_weight, float eps,
+                                        int B, int N, int n_signal, int n_noise, int d, int dv,
+                                        int flags, int dtype, void* workspace, size_t ws_bytes,
+                                        void* stream) {
+  const char* fn = "diffattn_gda_fwd_train";
+  if (!q || !k || !v || !out || !o_pre || !stats || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  constexpr int kTrainFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kTrainFlags) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "%s: eps must be > 0 with DIFFATTN_NORM", fn);
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  if (int rc = check_train_shape(fn, B, N, n_signal + n_noise, d, dv, dtype)) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(o_pre, 16) || !aligned(stats, 16) || !aligned(lambda, 4) ||
+      (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  if (workspace) {
+    size_t need = 0;
+    diffattn_gda_fwd_workspace_size(B, N, n_signal, n_noise, d, dv, &need);
+    if (ws_bytes < need || !aligned(workspace, 256))
+      return fail(DIFFATTN_ERR_WORKSPACE, "%s: need a 256-byte aligned workspace of %zu bytes", fn,
+                  need);
+  }
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = N;
+  p.units = n_signal;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_GDA;
+  p.q_heads = n_signal + n_noise;
+  p.kv_heads = n_signal + n_noise;
+  p.q_cols = d;
+  p.k_cols = d;
+  p.group = n_signal / n_noise;
+  p.lambda = lambda;
+  p.lam_logit = nullptr;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  p.stats = stats;
+  p.o_pre = o_pre;
+  p.n_pad = (N + 127) / 128 * 128;
+  if (workspace) p.gda_noise = static_cast<float*>(workspace);
+  return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
+}
+
+DIFFATTN_API int diffattn_gda_bwd_workspace_size(int B, int N, int n_signal, int n_noise, int d,
+                                                 int dv, size_t* bytes) {
+  const char* fn = "diffattn_gda_bwd_workspace_size";
+  if (!bytes) return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  if (int rc = check_train_shape(fn, B, N, n_signal + n_noise, d, dv, DIFFATTN_BF16)) return rc;
+  *bytes = da::backward_workspace_bytes(B, N, n_signal, static_cast<long long>(B) * N, true);
+  return ok();
+}
+
+DIFFATTN_API int diffattn_gda_bwd(const void* q, const void* k, const void* v, const void* o_pre,
+                                  const float* stats, const void* dout, const float* lambda,
+                                  float lambda_init, const float* norm_weight, float eps, void* dq,
+                                  void* dk, void* dv, float* dlambda, float* dnorm_weight, int B,
+                                  int N, int n_signal, int n_noise, int d, int dv_width, int flags,
+                                  int dtype, void* workspace, size_t ws_bytes, void* stream) {
+  const char* fn = "diffattn_gda_bwd";
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  if (int rc = check_train_shape(fn, B, N, n_signal + n_noise, d, dv_width, dtype)) return rc;
+  return bwd_impl(fn, q, k, v, o_pre, stats, dout, lambda, lambda_init, norm_weight, eps, dq, dk,
+                  dv, dlambda, dnorm_weight, B, N, n_signal, d, dv_width, flags, dtype, nullptr, 0,
+                  workspace, ws_bytes, stream, n_noise);
 }
 
 DIFFATTN_API int diffattn_gda_fwd_varlen(const void* q, const void* k, const void* v, void* out,

@@ -27,6 +27,13 @@
 //   dv: S1^T, S2^T (2 x 128) + dV (256).
 // Every wait is bounded (2 s); a timeout flags DEV_TIMEOUT in this file's status word and the
 // roles unwind without hanging.
+//
+// Grouped form (GR instantiations, page "Differential Transformer: softmax can't say zero, so it
+// subtracts", section "What other people found"): q, k are [B, N, Hs + Hn, d] with map 2 of
+// signal head h in noise head Hs + h / G; the tile kernels read map 2's Q and K there. dQ goes to
+// an fp32 accumulator of q's layout as before; a noise head's dK2 collects the contributions of
+// the G signal heads of its group through fp32 reductions into dkacc [tokens, Hn, d], converted
+// by bwd_gda_dk_kernel.
 #include <cuda.h>
 
 #include <cstdio>
@@ -154,7 +161,23 @@ struct Args {
   // N is then the longest sequence, and stats, delta, dl_part keep their per-sequence layout
   const int* cu;
   int total;
+  // grouped form: G signal heads per noise head (0: the ungrouped layout), heads of q and k
+  // (Hs + Hn), and the noise heads' fp32 dK accumulator [tokens, Hn, d]
+  int group, hqk;
+  float* dkacc;
 };
+
+// Head and first column of map m's Q or K for unit h: [Q1 | Q2] of head h, or (grouped) head h
+// for map 1 and noise head H + h / G for map 2, each d wide.
+template <bool GR>
+__device__ __forceinline__ int qk_head(const Args& a, int h, int m) {
+  if constexpr (GR) return m ? a.H + h / a.group : h;
+  else return h;
+}
+template <bool GR>
+__device__ __forceinline__ int qk_col(int m) {
+  return GR ? 0 : m * kD;
+}
 
 // Rows of sequence b: [s0, s0 + len) of the token axis (batched: b N .. b N + N - 1), and the
 // TMA coordinates (row, batch) of its first row. False for offsets outside the packed tensor
@@ -183,6 +206,11 @@ __device__ __forceinline__ bool seq_rows(const Args& a, int b, SeqRows& s) {
 // the debug-build checks of tile coordinates.
 __device__ __forceinline__ Ext4 map_ext(const Args& a, int cols, int elt) {
   return Ext4{cols, a.H, a.cu ? a.total : a.N, a.cu ? 1 : a.B, elt};
+}
+// Extent of the q and k maps (and of the dQ accumulator, elt 4)
+template <bool GR>
+__device__ __forceinline__ Ext4 qk_ext(const Args& a, int elt) {
+  return GR ? Ext4{kD, a.hqk, a.cu ? a.total : a.N, a.cu ? 1 : a.B, elt} : map_ext(a, 2 * kD, elt);
 }
 
 // =============================================================================================
@@ -266,6 +294,11 @@ __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(const Args a) {
     float4* zq = reinterpret_cast<float4*>(a.dqacc + static_cast<size_t>(r) * (2 * kD) + 8 * lane);
     zq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     zq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // grouped: the noise heads' dK accumulator, d floats per row (its rows [tokens, Hn] lie
+    // inside the tokens x Hs rows zeroed here)
+    if (a.dkacc)
+      reinterpret_cast<float4*>(a.dkacc + static_cast<size_t>(r) * kD)[lane] =
+          make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) sdw[warp][8 * lane + i] = dwl[i];
@@ -304,6 +337,7 @@ struct Ctrl {
 constexpr int kDynSmem = kCtrlOff + static_cast<int>(sizeof(Ctrl));
 }  // namespace dl
 
+template <bool GR>
 __global__ void __launch_bounds__(dl::kThreads, 1)
     bwd_delta_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -372,8 +406,8 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
       prefetch_tmap(&tm_vh);
       mbar_arrive_expect_tx(bar(cs.q_full), 2 * kBox);
       for (int c = 0; c < 2; ++c)
-        tma_load_4d_chk(sQ + c * kBox, &tm_q, bar(cs.q_full), kD + 64 * c, h, sq.trow + qt * kT,
-                    sq.tb, map_ext(a, 2 * kD, 2));
+        tma_load_4d_chk(sQ + c * kBox, &tm_q, bar(cs.q_full), qk_col<GR>(1) + 64 * c,
+                        qk_head<GR>(a, h, 1), sq.trow + qt * kT, sq.tb, qk_ext<GR>(a, 2));
       int issued = 0;
       bool ok = true;
       auto acquire = [&](int idx, uint32_t bytes) -> int {
@@ -388,8 +422,9 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
           const int s = acquire(idx, 2 * kBox);
           if (s < 0) { ok = false; break; }
           for (int c = 0; c < 2; ++c)
-            tma_load_4d_chk(sRing + s * kSlot + c * kBox, &tm_k, bar(cs.slot_full[s]), kD + 64 * c, h,
-                        sq.trow + t * kT, sq.tb, map_ext(a, 2 * kD, 2));
+            tma_load_4d_chk(sRing + s * kSlot + c * kBox, &tm_k, bar(cs.slot_full[s]),
+                            qk_col<GR>(1) + 64 * c, qk_head<GR>(a, h, 1), sq.trow + t * kT, sq.tb,
+                            qk_ext<GR>(a, 2));
           issued = ++idx;
         }
         if (t >= 1) {
@@ -584,6 +619,7 @@ struct Ctrl {
 constexpr int kDynSmem = kCtrlOff + static_cast<int>(sizeof(Ctrl));
 }  // namespace kq
 
+template <bool GR>
 __global__ void __launch_bounds__(kq::kThreads, 1)
     bwd_dkdq_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -655,8 +691,8 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       prefetch_tmap(&tm_do);
       mbar_arrive_expect_tx(bar(cs.kv_full), 6 * kBox);
       for (int c = 0; c < 2; ++c)
-        tma_load_4d_chk(sK + c * kBox, &tm_k, bar(cs.kv_full), m * kD + 64 * c, h, sq.trow + j * kT,
-                    sq.tb, map_ext(a, 2 * kD, 2));
+        tma_load_4d_chk(sK + c * kBox, &tm_k, bar(cs.kv_full), qk_col<GR>(m) + 64 * c,
+                        qk_head<GR>(a, h, m), sq.trow + j * kT, sq.tb, qk_ext<GR>(a, 2));
       for (int c = 0; c < 4; ++c)
         tma_load_4d_chk(sV + c * kBox, &tm_v, bar(cs.kv_full), 64 * c, h, sq.trow + j * kT, sq.tb, map_ext(a, kDV, 2));
       bool ok = true;
@@ -670,8 +706,8 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
         if (!(ok = mbar_wait(bar(cs.q_empty), (t & 1) ^ 1, abrt))) break;
         mbar_arrive_expect_tx(bar(cs.q_full), 2 * kBox + 2 * kT * 4);
         for (int c = 0; c < 2; ++c)
-          tma_load_4d_chk(sQ + c * kBox, &tm_q, bar(cs.q_full), m * kD + 64 * c, h, sq.trow + i * kT,
-                      sq.tb, map_ext(a, 2 * kD, 2));
+          tma_load_4d_chk(sQ + c * kBox, &tm_q, bar(cs.q_full), qk_col<GR>(m) + 64 * c,
+                          qk_head<GR>(a, h, m), sq.trow + i * kT, sq.tb, qk_ext<GR>(a, 2));
         const size_t nst = static_cast<size_t>(a.B) * a.H * 2 * a.Npad;
         bulk_load_f32(sBD, a.stats, st_base + static_cast<size_t>(i) * kT, nst, kT, bar(cs.q_full));
         bulk_load_f32(sBD + kT * 4, a.delta, st_base + static_cast<size_t>(i) * kT, nst, kT,
@@ -818,9 +854,26 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       tmem_ld32(tmem + tl + 2 * kT + 64 * wg, o[0]);
       tmem_ld32(tmem + tl + 2 * kT + 64 * wg + 32, o[1]);
       tmem_wait_ld();
-      if (key < sq.len) {
-        __nv_bfloat16* dst = a.dk + ((static_cast<size_t>(sq.s0) + key) * a.H + h) * (2 * kD) +
-                             m * kD + 64 * wg;
+      if (GR && m == 1 && key < sq.len) {
+        // grouped, map 2: this signal head's share of its noise head's dK2, added in fp32
+        float* dst = a.dkacc +
+                     ((static_cast<size_t>(sq.s0) + key) * (a.hqk - a.H) + h / a.group) * kD +
+                     64 * wg;
+        if (dbg_index_ok(static_cast<long long>((static_cast<size_t>(sq.s0) + key) *
+                                                    (a.hqk - a.H) + h / a.group),
+                         (a.cu ? 1LL * a.total : 1LL * a.B * a.N) * (a.hqk - a.H))) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              red_add_v4(dst + 32 * hh + 4 * g, __uint_as_float(o[hh][4 * g]),
+                         __uint_as_float(o[hh][4 * g + 1]), __uint_as_float(o[hh][4 * g + 2]),
+                         __uint_as_float(o[hh][4 * g + 3]));
+        }
+      } else if (key < sq.len) {
+        __nv_bfloat16* dst = a.dk + ((static_cast<size_t>(sq.s0) + key) * (GR ? a.hqk : a.H) +
+                                     qk_head<GR>(a, h, m)) * (GR ? kD : 2 * kD) +
+                             qk_col<GR>(m) + 64 * wg;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
@@ -870,12 +923,13 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       if (!(ok = bar_and(2, 128, true))) break;
       if (r == 0) {
         const int i = i0 + t;
-        const Ext4 eacc = map_ext(a, 2 * kD, 4);
+        const Ext4 eacc = qk_ext<GR>(a, 4);
+        const int qh = qk_head<GR>(a, h, m), qc = qk_col<GR>(m);
         for (int c = 0; c < 4; ++c)
           if (!kDebugChecks ||
               (dbg_index_ok(sq.trow + i * kT, eacc.z) && dbg_index_ok(sq.tb, eacc.w) &&
-               dbg_index_ok(h, eacc.y) && dbg_index_ok(m * kD + 32 * c, eacc.x)))
-            tma_reduce_add_4d(&tm_dqacc, sDO + c * kBox, m * kD + 32 * c, h, sq.trow + i * kT,
+               dbg_index_ok(qh, eacc.y) && dbg_index_ok(qc + 32 * c, eacc.x)))
+            tma_reduce_add_4d(&tm_dqacc, sDO + c * kBox, qc + 32 * c, qh, sq.trow + i * kT,
                               sq.tb);
         bulk_commit();
         bulk_wait_read();
@@ -923,6 +977,7 @@ struct Ctrl {
 constexpr int kDynSmem = kCtrlOff + static_cast<int>(sizeof(Ctrl));
 }  // namespace vv
 
+template <bool GR>
 __global__ void __launch_bounds__(vv::kThreads, 1)
     bwd_dv_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
@@ -994,7 +1049,8 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
       prefetch_tmap(&tm_do);
       mbar_arrive_expect_tx(bar(cs.kv_full), 4 * kBox);
       for (int c = 0; c < 4; ++c)
-        tma_load_4d_chk(sK + c * kBox, &tm_k, bar(cs.kv_full), 64 * c, h, sq.trow + j * kT, sq.tb, map_ext(a, 2 * kD, 2));
+        tma_load_4d_chk(sK + c * kBox, &tm_k, bar(cs.kv_full), qk_col<GR>(c >> 1) + 64 * (c & 1),
+                        qk_head<GR>(a, h, c >> 1), sq.trow + j * kT, sq.tb, qk_ext<GR>(a, 2));
       // Q of inner tile t: map mp's half once S_mp of tile t - 1 has read it; b1, b2 (the
       // softmax's row statistics) into buffer t & 1 once the softmax has read tile t - 2's, on a
       // barrier of that buffer's own (the Q barriers run up to two tiles ahead of the softmax,
@@ -1006,8 +1062,9 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
           if (!mbar_wait(bar(cs.q_empty[mp]), (t & 1) ^ 1, abrt)) return false;
           mbar_arrive_expect_tx(bar(cs.q_full[mp]), 2 * kBox);
           for (int c = 0; c < 2; ++c)
-            tma_load_4d_chk(sQ + (2 * mp + c) * kBox, &tm_q, bar(cs.q_full[mp]), kD * mp + 64 * c,
-                            h, sq.trow + i * kT, sq.tb, map_ext(a, 2 * kD, 2));
+            tma_load_4d_chk(sQ + (2 * mp + c) * kBox, &tm_q, bar(cs.q_full[mp]),
+                            qk_col<GR>(mp) + 64 * c, qk_head<GR>(a, h, mp), sq.trow + i * kT,
+                            sq.tb, qk_ext<GR>(a, 2));
           ++nq[mp];
         }
         if (!mbar_wait(bar(cs.b_empty[t & 1]), ((t >> 1) & 1) ^ 1, abrt)) return false;
@@ -1196,10 +1253,34 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
 // =============================================================================================
 constexpr int kFinishSumBlocks = kDV / 32;
 
+// Grouped form: the noise heads' dK (fp32 sums over each group's signal heads) to bf16 at heads
+// Hs .. Hs + Hn - 1 of dk [tokens, Hs + Hn, d]; one thread per 8 channels.
+__global__ void __launch_bounds__(256) bwd_gda_dk_kernel(const Args a, long long tokens) {
+  const int hn = a.hqk - a.H;
+  const long long n8 = tokens * hn * (kD / 8);
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n8;
+       e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = e / (kD / 8);             // token * Hn + g
+    const int c8 = static_cast<int>(e % (kD / 8));
+    const long long t = row / hn;
+    const int g = static_cast<int>(row % hn);
+    const float4 x = reinterpret_cast<const float4*>(a.dkacc)[2 * e];
+    const float4 y = reinterpret_cast<const float4*>(a.dkacc)[2 * e + 1];
+    uint4 pk;
+    pk.x = pack_bf16x2(x.x, x.y);
+    pk.y = pack_bf16x2(x.z, x.w);
+    pk.z = pack_bf16x2(y.x, y.y);
+    pk.w = pack_bf16x2(y.z, y.w);
+    reinterpret_cast<uint4*>(a.dk + (static_cast<size_t>(t) * a.hqk + a.H + g) * kD)[c8] = pk;
+  }
+}
+
 __global__ void __launch_bounds__(256) bwd_finish_kernel(const Args a, long long n8, int nq) {
   if (static_cast<int>(blockIdx.x) < nq) {
     // packed: rows past the last sequence belong to none and are not written
-    if (a.cu) n8 = min(n8, static_cast<long long>(min(max(a.cu[a.B], 0), a.total)) * a.H * 2 * kD / 8);
+    if (a.cu)
+      n8 = min(n8, static_cast<long long>(min(max(a.cu[a.B], 0), a.total)) *
+                       (a.group ? a.hqk * kD : a.H * 2 * kD) / 8);
     const long long stride = static_cast<long long>(nq) * 256;
     const float4* src = reinterpret_cast<const float4*>(a.dqacc);
     for (long long e = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; e < n8;
@@ -1280,11 +1361,12 @@ static bool make_map_f32(CUtensorMap* m, void* base, int cols, int H, int N, int
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-  size_t dO, delta, dqacc, dw_part, dl_part, total;
+  size_t dO, delta, dqacc, dw_part, dl_part, dkacc, total;
   int pre_blocks;
 };
-// tokens: B N (batched) or the packed length
-static WsLayout ws_layout(int B, int N, int H, long long tokens) {
+// tokens: B N (batched) or the packed length; grouped: plus the noise heads' dK accumulator
+// (sized for tokens x H rows of d floats, H the signal heads: Hn <= H)
+static WsLayout ws_layout(int B, int N, int H, long long tokens, bool grouped = false) {
   WsLayout w;
   const int Npad = (N + kT - 1) / kT * kT;
   const int n_t = Npad / kT;
@@ -1302,14 +1384,16 @@ static WsLayout ws_layout(int B, int N, int H, long long tokens) {
   off = align256(off + static_cast<size_t>(w.pre_blocks) * kDV * 4);
   w.dl_part = off;
   off = align256(off + static_cast<size_t>(B) * H * n_t * 4);
+  w.dkacc = off;
+  if (grouped) off = align256(off + static_cast<size_t>(rows) * kD * 4);
   w.total = off;
   return w;
 }
 
 }  // namespace bwd
 
-size_t backward_workspace_bytes(int B, int N, int H, long long rows) {
-  return bwd::ws_layout(B, N, H, rows).total;
+size_t backward_workspace_bytes(int B, int N, int H, long long rows, bool grouped) {
+  return bwd::ws_layout(B, N, H, rows, grouped).total;
 }
 
 cudaError_t status_backward(int* v) { return read_clear_status(v); }
@@ -1318,7 +1402,8 @@ cudaError_t launch_backward(const BackwardArgs& x, cudaStream_t st, char* err, s
   using namespace bwd;
   const bool packed = x.cu_seqlens != nullptr;
   const long long tokens = packed ? x.total : static_cast<long long>(x.B) * x.N;
-  const WsLayout L = ws_layout(x.B, x.N, x.H, tokens);
+  const bool grouped = x.n_noise > 0;
+  const WsLayout L = ws_layout(x.B, x.N, x.H, tokens, grouped);
   uint8_t* ws = static_cast<uint8_t*>(x.workspace);
   Args a{};
   a.q = static_cast<const __nv_bfloat16*>(x.q);
@@ -1353,6 +1438,9 @@ cudaError_t launch_backward(const BackwardArgs& x, cudaStream_t st, char* err, s
   a.c_log2 = kLog2e * a.c;
   a.cu = x.cu_seqlens;
   a.total = x.total;
+  a.group = grouped ? x.H / x.n_noise : 0;
+  a.hqk = grouped ? x.H + x.n_noise : x.H;
+  a.dkacc = grouped ? reinterpret_cast<float*>(ws + L.dkacc) : nullptr;
   {
     // bytes each unit keeps re-reading (or, for dQ, accumulating) while its tiles run; a group
     // keeps about 48 MB of them in the 126 MB L2
@@ -1370,9 +1458,11 @@ cudaError_t launch_backward(const BackwardArgs& x, cudaStream_t st, char* err, s
   // packed: the token axis as one batch row of `total`
   const int mN = packed ? x.total : x.N, mB = packed ? 1 : x.B;
   CUtensorMap mq, mk, mv, mvh, mdo, mdq;
-  if (!make_map_f32(&mdq, a.dqacc, 2 * kD, x.H, mN, mB, err, err_len) ||
-      !make_map(&mq, x.q, 2 * kD, x.H, mN, mB, kT, err, err_len) ||
-      !make_map(&mk, x.k, 2 * kD, x.H, mN, mB, kT, err, err_len) ||
+  // q, k (and the dQ accumulator): [Q1 | Q2] per head, or (grouped) d-wide heads Hs + Hn
+  const int qk_cols = grouped ? kD : 2 * kD;
+  if (!make_map_f32(&mdq, a.dqacc, qk_cols, a.hqk, mN, mB, err, err_len) ||
+      !make_map(&mq, x.q, qk_cols, a.hqk, mN, mB, kT, err, err_len) ||
+      !make_map(&mk, x.k, qk_cols, a.hqk, mN, mB, kT, err, err_len) ||
       !make_map(&mv, x.v, kDV, x.H, mN, mB, kT, err, err_len) ||
       !make_map(&mvh, x.v, kDV, x.H, mN, mB, kT / 2, err, err_len) ||
       !make_map(&mdo, a.dO, kDV, x.H, mN, mB, kT, err, err_len))
@@ -1383,22 +1473,30 @@ cudaError_t launch_backward(const BackwardArgs& x, cudaStream_t st, char* err, s
   if (e != cudaSuccess) return e;
 
   const int items = a.n_t * x.B * x.H;
-  e = cudaFuncSetAttribute(bwd_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dl::kDynSmem);
+  auto delta_k = grouped ? bwd_delta_kernel<true> : bwd_delta_kernel<false>;
+  auto dkdq_k = grouped ? bwd_dkdq_kernel<true> : bwd_dkdq_kernel<false>;
+  auto dv_k = grouped ? bwd_dv_kernel<true> : bwd_dv_kernel<false>;
+  e = cudaFuncSetAttribute(delta_k, cudaFuncAttributeMaxDynamicSharedMemorySize, dl::kDynSmem);
   if (e != cudaSuccess) return e;
-  bwd_delta_kernel<<<items, dl::kThreads, dl::kDynSmem, st>>>(mq, mk, mvh, a);
+  delta_k<<<items, dl::kThreads, dl::kDynSmem, st>>>(mq, mk, mvh, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  e = cudaFuncSetAttribute(bwd_dkdq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kq::kDynSmem);
+  e = cudaFuncSetAttribute(dkdq_k, cudaFuncAttributeMaxDynamicSharedMemorySize, kq::kDynSmem);
   if (e != cudaSuccess) return e;
-  bwd_dkdq_kernel<<<2 * items, kq::kThreads, kq::kDynSmem, st>>>(mq, mk, mv, mdo, mdq, a);
+  dkdq_k<<<2 * items, kq::kThreads, kq::kDynSmem, st>>>(mq, mk, mv, mdo, mdq, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  e = cudaFuncSetAttribute(bwd_dv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, vv::kDynSmem);
+  e = cudaFuncSetAttribute(dv_k, cudaFuncAttributeMaxDynamicSharedMemorySize, vv::kDynSmem);
   if (e != cudaSuccess) return e;
-  bwd_dv_kernel<<<items, vv::kThreads, vv::kDynSmem, st>>>(mq, mk, mdo, a);
+  dv_k<<<items, vv::kThreads, vv::kDynSmem, st>>>(mq, mk, mdo, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  const long long n8 = tokens * x.H * 2 * kD / 8;
+  if (grouped) {  // the noise heads' dK from their fp32 sums
+    bwd_gda_dk_kernel<<<8 * 152, 256, 0, st>>>(a, tokens);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+
+  const long long n8 = tokens * a.hqk * qk_cols / 8;
   long long nq = (n8 + 255) / 256;
   if (nq > 8 * 152) nq = 8 * 152;  // eight 256-thread blocks per SM: a full SM of threads
   bwd_finish_kernel<<<static_cast<int>(nq) + 1 + kFinishSumBlocks, 256, 0, st>>>(

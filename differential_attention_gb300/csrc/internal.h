@@ -280,9 +280,13 @@ struct BackwardArgs {
   // [total, H, *]; N is then the longest sequence
   const int* cu_seqlens;
   int total;
+  // grouped form (0: ungrouped): H is then the number of signal heads, q and k are
+  // [B, N, H + n_noise, d] and v, out [B, N, H, dv]
+  int n_noise;
 };
-// rows: B N (batched) or `total` (packed); N the (longest) sequence length
-size_t backward_workspace_bytes(int B, int N, int H, long long rows);
+// rows: B N (batched) or `total` (packed); N the (longest) sequence length; grouped: with room
+// for the noise heads' dK accumulator
+size_t backward_workspace_bytes(int B, int N, int H, long long rows, bool grouped = false);
 cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s, char* err, size_t err_len);
 cudaError_t status_backward(int* v);
 

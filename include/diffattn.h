@@ -675,6 +675,41 @@ DIFFATTN_API int diffattn_gda_fwd_varlen(const void* q, const void* k, const voi
                                          int n_noise, int d, int dv, int flags, int dtype,
                                          void* workspace, size_t ws_bytes, void* stream);
 
+/* Grouped training: the forward saving what the backward needs, and the backward (gradients of
+ * every input of diffattn_gda_fwd, the chain rule of its operator: signal head h's gradients are
+ * those of the ungrouped operator with map 2 taken from noise head n_signal + h / G, and a
+ * noise head's dQ2 and dK2 sum the contributions of the G signal heads of its group).
+ *   diffattn_gda_fwd_train: diffattn_gda_fwd plus
+ *     o_pre : device bf16 [B, N, n_signal, dv], each signal head's output before the norm
+ *     stats : device fp32 [B, n_signal, 2, Npad] (Npad = N rounded up to 128): per row and map the
+ *             base-2 log-sum-exp of the scaled scores (map 2's is its noise head's)
+ *     workspace, ws_bytes : as diffattn_gda_fwd (NULL: one launch)
+ *   diffattn_gda_bwd: dout [B, N, n_signal, dv] the gradient of out; writes
+ *     dq, dk : device bf16 [B, N, n_signal + n_noise, d] (q's layout)
+ *     dv     : device bf16 [B, N, n_signal, dv]
+ *     dlambda : device fp32 [n_signal];  dnorm_weight : device fp32 [dv] or NULL
+ *     workspace, ws_bytes : at least diffattn_gda_bwd_workspace_size() bytes, 256-byte aligned
+ *   The noise heads' dK2 is summed in fp32 through atomic additions, so its last bits can
+ *   differ from run to run; every other output is deterministic.
+ * Supported: batched, d = 128, dv = 256, dtype DIFFATTN_BF16, flags CAUSAL | NORM | SCALE,
+ * n_signal a multiple of n_noise.
+ * Errors: ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA.
+ */
+DIFFATTN_API int diffattn_gda_fwd_train(const void* q, const void* k, const void* v, void* out,
+                                        void* o_pre, float* stats, const float* lambda,
+                                        float lambda_init, const float* norm_weight, float eps,
+                                        int B, int N, int n_signal, int n_noise, int d, int dv,
+                                        int flags, int dtype, void* workspace, size_t ws_bytes,
+                                        void* stream);
+DIFFATTN_API int diffattn_gda_bwd_workspace_size(int B, int N, int n_signal, int n_noise, int d,
+                                                 int dv, size_t* bytes);
+DIFFATTN_API int diffattn_gda_bwd(const void* q, const void* k, const void* v, const void* o_pre,
+                                  const float* stats, const void* dout, const float* lambda,
+                                  float lambda_init, const float* norm_weight, float eps, void* dq,
+                                  void* dk, void* dv, float* dlambda, float* dnorm_weight, int B,
+                                  int N, int n_signal, int n_noise, int d, int dv_width, int flags,
+                                  int dtype, void* workspace, size_t ws_bytes, void* stream);
+
 /* Grouped prefill with each sequence's queries at the end of its keys (chunked prompts, new tokens
  * over a cache): diffattn_gda_fwd's operator with the key layout of diffattn_fwd_varlen_qk
  * (keys packed with offsets of their own) or of diffattn_fwd_paged (keys in page pools).

@@ -663,6 +663,46 @@ def diffattn_gda_fwd_paged(q, k_pool, v_pool, cu_seqlens_q, seqlens_k, block_tab
                                       norm_weight, eps, norm, apply_scale, causal)
 
 
+def diffattn_gda_bwd(q, k, v, lam, lam_init: float, n_signal: int, dy, norm_weight=None,
+                     eps: float = 1e-5, norm: bool = True, apply_scale: bool = True,
+                     causal: bool = True):
+    """Backward of `diffattn_gda_fwd` for the upstream gradient dy [B, N, Hs, dv]. Signal head h's
+    operator is the ungrouped one with map 2 taken from noise head g = Hs + gda_noise_head(h), so
+    its gradients are those of `diff_attn_head_bwd`; a noise head's dQ2 and dK2 are the sums of
+    the contributions of the signal heads of its group.
+
+    Returns dict(dq [B,N,Hs+Hn,d], dk [B,N,Hs+Hn,d], dv [B,N,Hs,dv], dlam [Hs], dw [dv]) in
+    float64 (dw: the norm weight's gradient, zeros without the norm)."""
+    q, k, v, dy = _f64(q), _f64(k), _f64(v), _f64(dy)
+    B, N, heads, d = q.shape
+    Hs = n_signal
+    Hn = heads - Hs
+    lam = np.broadcast_to(_f64(lam), (Hs,))
+    s = (1.0 - lam_init) if apply_scale else 1.0
+    out = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v),
+               dlam=np.zeros(Hs), dw=np.zeros(v.shape[-1]))
+    for b in range(B):
+        for h in range(Hs):
+            g = Hs + gda_noise_head(h, Hs, Hn)
+            q1, k1, q2, k2 = q[b, :, h], k[b, :, h], q[b, :, g], k[b, :, g]
+            O = diff_attn_head(q1, k1, q2, k2, v[b, :, h], float(lam[h]), causal)
+            dYs = dy[b, :, h] * s
+            if norm:
+                dO, dwh = subln_bwd(O, norm_weight, eps, dYs)
+                out["dw"] += dwh
+            else:
+                dO = dYs
+            dq1, dk1, dq2, dk2, dvh, dl = diff_attn_head_bwd(q1, k1, q2, k2, v[b, :, h],
+                                                              float(lam[h]), causal, dO)
+            out["dq"][b, :, h] += dq1
+            out["dk"][b, :, h] += dk1
+            out["dq"][b, :, g] += dq2
+            out["dk"][b, :, g] += dk2
+            out["dv"][b, :, h] = dvh
+            out["dlam"][h] += dl
+    return out
+
+
 def diffattn_gda_decode(q, k_cache, v_cache, seqlens, lam, lam_init: float, n_signal: int,
                         norm_weight=None, eps: float = 1e-5, norm: bool = True,
                         apply_scale: bool = True):

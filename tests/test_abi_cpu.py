@@ -443,6 +443,43 @@ def test_gda_validation(L):
     assert decp(ws_bytes=need - 1) == -8
 
 
+def test_gda_training_validation(L):
+    def train(q=FAKE, stats=FAKE, ns=12, nn=3, d=128, dv=256, flags=7, dtype=0, ws=None,
+              ws_bytes=0):
+        return L.diffattn_gda_fwd_train(q, FAKE, FAKE, FAKE, FAKE, stats, FAKE, 0.5, None, 1e-5, 1,
+                                        300, ns, nn, d, dv, flags, dtype, ws, ws_bytes, None)
+
+    assert train(q=None) == -1
+    assert train(stats=None) == -1
+    assert train(flags=8) == -1              # DIFFATTN_CUDA_CORES has no training path
+    assert train(ns=12, nn=5) == -2          # not a whole number of signal heads per noise head
+    assert train(d=64, dv=128) == -2
+    assert train(dtype=1) == -3
+    assert train(stats=ODD) == -4
+    assert train(ws=ctypes.c_void_p(0x10000), ws_bytes=3 * 384 * 4 - 4) == -8
+    n = ctypes.c_size_t(0)
+    assert L.diffattn_gda_bwd_workspace_size(4, 4096, 12, 3, 128, 256, ctypes.byref(n)) == 0
+    need = n.value
+    m = ctypes.c_size_t(0)
+    assert L.diffattn_bwd_workspace_size(4, 4096, 12, 128, 256, ctypes.byref(m)) == 0
+    # the ungrouped backward's workspace for the signal heads, plus the noise heads' fp32 dK sums
+    assert need >= m.value + 4 * 4096 * 3 * 128 * 4
+    assert L.diffattn_gda_bwd_workspace_size(4, 4096, 12, 5, 128, 256, ctypes.byref(n)) == -2
+
+    def bwd(q=FAKE, dk=FAKE, ns=12, nn=3, ws=FAKE, ws_bytes=need, N=4096, dtype=0):
+        return L.diffattn_gda_bwd(q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.5, None, 1e-5, FAKE, dk,
+                                  FAKE, FAKE, None, 4, N, ns, nn, 128, 256, 7, dtype, ws, ws_bytes,
+                                  None)
+
+    assert bwd(q=None) == -1
+    assert bwd(dk=None) == -1
+    assert bwd(N=0) == -2
+    assert bwd(ns=12, nn=0) == -2
+    assert bwd(dtype=1) == -3
+    assert bwd(q=ODD) == -4
+    assert bwd(ws_bytes=need - 1) == -8
+
+
 def test_v2_decode_fp8_paged_validation(L):
     n = ctypes.c_size_t(0)
     assert L.diffattn_v2_decode_workspace_size(4, 4096, 16, 2, 128, ctypes.byref(n)) == 0

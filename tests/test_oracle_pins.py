@@ -573,6 +573,49 @@ def pin_gda():
             assert same.tolist() == [h // G != 1 for h in range(Hs)]
 
 
+def pin_gda_bwd():
+    """Grouped backward: with one noise head per signal head it is the ungrouped backward on the
+    halves stored as heads; every gradient matches central differences of the grouped forward's
+    loss <dy, Y> (a noise head's gradient collects its whole group)."""
+    rng = np.random.default_rng(37)
+    B, N, H, d, dv = 1, 5, 2, 3, 4
+    q1, q2, k1, k2 = (rng.standard_normal((B, N, H, d)) for _ in range(4))
+    v = rng.standard_normal((B, N, H, dv)); dy = rng.standard_normal((B, N, H, dv))
+    lam = np.array([0.3, 0.8]); w = np.linspace(0.5, 1.5, dv)
+    g = ref.diffattn_gda_bwd(np.concatenate([q1, q2], 2), np.concatenate([k1, k2], 2), v, lam,
+                             0.4, H, dy, norm_weight=w)
+    u = ref.diffattn_bwd(np.concatenate([q1, q2], 3), np.concatenate([k1, k2], 3), v, lam, 0.4, dy,
+                         norm_weight=w)
+    assert np.allclose(g["dq"][:, :, :H], u["dq"][..., :d]) and np.allclose(g["dq"][:, :, H:], u["dq"][..., d:])
+    assert np.allclose(g["dk"][:, :, :H], u["dk"][..., :d]) and np.allclose(g["dk"][:, :, H:], u["dk"][..., d:])
+    assert np.allclose(g["dv"], u["dv"]) and np.allclose(g["dlam"], u["dlam"]) and np.allclose(g["dw"], u["dw"])
+    # grouped: 3 signal heads over 1 noise head, central differences
+    Hs, Hn = 3, 1
+    q = rng.standard_normal((1, 4, Hs + Hn, d)); k = rng.standard_normal((1, 4, Hs + Hn, d))
+    v = rng.standard_normal((1, 4, Hs, dv)); dy = rng.standard_normal((1, 4, Hs, dv))
+    lam = np.array([0.2, 0.5, 0.9])
+    grads = ref.diffattn_gda_bwd(q, k, v, lam, 0.4, Hs, dy, norm_weight=w)
+    loss = lambda q_, k_, v_, lam_, w_: float(np.sum(dy * ref.diffattn_gda_fwd(
+        q_, k_, v_, lam_, 0.4, Hs, norm_weight=w_)))
+    h = 1e-6
+    for name, x in (("dq", q), ("dk", k), ("dv", v)):
+        for idx in [(0, 3, Hs, 1), (0, 2, 0, 2), (0, 1, 2, 0)] if name != "dv" else [(0, 3, 1, 2), (0, 0, 2, 3)]:
+            xp = x.copy(); xm = x.copy(); xp[idx] += h; xm[idx] -= h
+            args_p = [q, k, v]; args_m = [q, k, v]
+            pos = ("dq", "dk", "dv").index(name)
+            args_p[pos] = xp; args_m[pos] = xm
+            fd = (loss(*args_p, lam, w) - loss(*args_m, lam, w)) / (2 * h)
+            assert abs(fd - grads[name][idx]) < 1e-6 * max(1.0, abs(fd)), (name, idx)
+    for i in range(Hs):
+        lp = lam.copy(); lm = lam.copy(); lp[i] += h; lm[i] -= h
+        fd = (loss(q, k, v, lp, w) - loss(q, k, v, lm, w)) / (2 * h)
+        assert abs(fd - grads["dlam"][i]) < 1e-6 * max(1.0, abs(fd))
+    for c in (0, 3):
+        wp = w.copy(); wm = w.copy(); wp[c] += h; wm[c] -= h
+        fd = (loss(q, k, v, lam, wp) - loss(q, k, v, lam, wm)) / (2 * h)
+        assert abs(fd - grads["dw"][c]) < 1e-6 * max(1.0, abs(fd))
+
+
 def pin_gda_varlen():
     """Packed grouped prefill: with equal lengths it is the batched grouped prefill; with one noise
     head per signal head it is the ungrouped packed prefill on the halves stored as heads; each
@@ -699,7 +742,7 @@ PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, p
         pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
         pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen, pin_varlen_qk,
-        pin_v2_varlen, pin_paged_prefill, pin_bwd_varlen, pin_gda, pin_gda_varlen,
+        pin_v2_varlen, pin_paged_prefill, pin_bwd_varlen, pin_gda, pin_gda_bwd, pin_gda_varlen,
         pin_gda_varlen_qk_and_paged, pin_gda_decode_paged, pin_gda_decode_is_last_prefill_row]
 
 
