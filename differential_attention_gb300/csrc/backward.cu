@@ -88,6 +88,9 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+__device__ __forceinline__ void bulk_wait_read_le1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred) {
   uint32_t r;
@@ -593,30 +596,40 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
 // inner tile is computed query-major: S = Q K^T and dW = dO V^T have the 128 queries on the TMEM
 // lanes, so a query's b and delta are per-thread constants. Warps 0 (TMA), 1 (MMA, TMEM),
 // 2-9: two warpgroups, thread r = query row r, key columns [64 w, 64 w + 64); 10-13: the dQ
-// warpgroup (thread r = query row r, all 128 d-columns), which stages each tile's dQ in the dO
-// slot and adds it into the fp32 accumulator with TMA tensor reductions.
-// TMEM: S cols 0-127, dW 128-255, dK 256-383, dQ partial 384-511.
-// Shared memory: K_m,j (32 KB) and V_j (64 KB) stay; Q_m,i (32 KB + its b and delta rows) and
-// dO_i (64 KB) have one slot each; the dS tile (32 KB, [query][key]) is read MN-major as dS^T
-// for dK and K-major for dQ. MMA issue order per inner tile t (keeps the Q slot, freed by dK_t,
-// off the critical path): dK_t | dW_{t+1} | S_{t+1} | dQ_t.
+// warpgroup (thread r = query row r, all 128 d-columns), which moves each tile's dQ partial
+// through a staging ring of two 32-column boxes and adds it into the fp32 accumulator with TMA
+// tensor reductions, off the path of every operand.
+// TMEM: S cols 0-127, dK 256-383, and two buffers P0 (128-255) and P1 (384-511): tile t's dW
+// goes to P(t & 1), and once the dS warps have read it, tile t's dQ partial overwrites it; so
+// dW_{t+1} needs only dQ_{t-1} drained and runs while the dS warps work on tile t.
+// Shared memory: K_m,j (32 KB) stays; V_j has one half-slot (32 KB: dv columns [0, 128) or
+// [128, 256)), refilled once per inner tile: tile t's dW runs over the half left in the slot
+// by tile t - 1 first, then over the other half (so halves alternate 0,1 | 1,0 | 0,1 ...).
+// Q_m,i (32 KB + its b and delta rows) and dO_i (64 KB) have one slot each; the dS tile (32 KB,
+// [query][key]) is read MN-major as dS^T for dK and K-major for dQ; the dQ staging ring (32 KB).
+// MMA issue order per inner tile t: dW_{t+1} (both V halves) | dK_t | dQ_t | S_{t+1}: dW_{t+1}
+// runs while the dS warps work on tile t, and the next Q load runs under dK_t and dQ_t.
 // =============================================================================================
 namespace kq {
 constexpr int kThreads = 448;  // TMA, MMA, 8 dS warps, 4 dQ warps
 constexpr int kKOff = 0;
 constexpr int kVOff = kKOff + 2 * kBox;
-constexpr int kQOff = kVOff + 4 * kBox;
+constexpr int kQOff = kVOff + 2 * kBox;
 constexpr int kDOOff = kQOff + 2 * kBox;
 constexpr int kDSOff = kDOOff + 4 * kBox;
-constexpr int kBDOff = kDSOff + 2 * kBox;   // b[128], delta[128]
+constexpr int kSTOff = kDSOff + 2 * kBox;   // dQ staging: two boxes of 32 fp32 columns
+constexpr int kBDOff = kSTOff + 2 * kBox;   // b[128], delta[128]
 constexpr int kCtrlOff = kBDOff + 2 * kT * 4;
 struct Ctrl {
-  uint64_t kv_full, q_full, q_empty, do_full, do_empty, s_full, s_free, ds_full, ds_empty,
-      dq_full, dq_free, dk_full, teardown;
+  uint64_t k_full, v_full, v_empty, q_full, q_empty, do_full, do_empty, s_full, s_free, ds_full,
+      ds_empty, dq_full, dq_free, dk_full, teardown;
   uint32_t tmem_slot;
   int abort_flag;
 };
 constexpr int kDynSmem = kCtrlOff + static_cast<int>(sizeof(Ctrl));
+static_assert(kDynSmem <= 232448, "dK/dQ kernel exceeds 227 KB of shared memory");
+// TMEM column of buffer P(t & 1), which holds dW_t and then the dQ partial of tile t
+__device__ __forceinline__ uint32_t pbuf(int t) { return static_cast<uint32_t>(kT + 2 * kT * (t & 1)); }
 }  // namespace kq
 
 template <bool GR>
@@ -632,7 +645,8 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sK = smem_u32(smem + kKOff), sV = smem_u32(smem + kVOff);
   const uint32_t sQ = smem_u32(smem + kQOff), sDO = smem_u32(smem + kDOOff);
-  const uint32_t sDS = smem_u32(smem + kDSOff), sBD = smem_u32(smem + kBDOff);
+  const uint32_t sDS = smem_u32(smem + kDSOff), sST = smem_u32(smem + kSTOff);
+  const uint32_t sBD = smem_u32(smem + kBDOff);
   const float* bd = reinterpret_cast<const float*>(smem + kBDOff);
   auto bar = [](uint64_t& x) { return smem_u32(&x); };
   if ((smem_u32(smem) & 1023u) != 0) {
@@ -655,7 +669,9 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
   const int T = nts - i0;  // inner (query) tiles
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(cs.kv_full), 1);
+    mbar_init(bar(cs.k_full), 1);
+    mbar_init(bar(cs.v_full), 1);
+    mbar_init(bar(cs.v_empty), 1);
     mbar_init(bar(cs.q_full), 1);
     mbar_init(bar(cs.q_empty), 1);
     mbar_init(bar(cs.do_full), 1);
@@ -689,21 +705,34 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_do);
-      mbar_arrive_expect_tx(bar(cs.kv_full), 6 * kBox);
+      // V half-load n carries dv columns [128 (n & 1), +128): load 0 with K, then load t + 1
+      // (tile t's second half) once tile t's first half has been read
+      auto load_v = [&](int n) {
+        mbar_arrive_expect_tx(bar(cs.v_full), 2 * kBox);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d_chk(sV + c * kBox, &tm_v, bar(cs.v_full), 128 * (n & 1) + 64 * c, h,
+                          sq.trow + j * kT, sq.tb, map_ext(a, kDV, 2));
+      };
+      mbar_arrive_expect_tx(bar(cs.k_full), 2 * kBox);
       for (int c = 0; c < 2; ++c)
-        tma_load_4d_chk(sK + c * kBox, &tm_k, bar(cs.kv_full), qk_col<GR>(m) + 64 * c,
+        tma_load_4d_chk(sK + c * kBox, &tm_k, bar(cs.k_full), qk_col<GR>(m) + 64 * c,
                         qk_head<GR>(a, h, m), sq.trow + j * kT, sq.tb, qk_ext<GR>(a, 2));
-      for (int c = 0; c < 4; ++c)
-        tma_load_4d_chk(sV + c * kBox, &tm_v, bar(cs.kv_full), 64 * c, h, sq.trow + j * kT, sq.tb, map_ext(a, kDV, 2));
+      load_v(0);
       bool ok = true;
-      int t = 0;
-      for (; t < T && ok; ++t) {
+      int nv = 1, ndo = 0, nq = 0;  // loads issued: V halves, dO tiles, Q tiles
+      for (int t = 0; t < T && ok; ++t) {
         const int i = i0 + t;
         if (!(ok = mbar_wait(bar(cs.do_empty), (t & 1) ^ 1, abrt))) break;
+        ++ndo;
         mbar_arrive_expect_tx(bar(cs.do_full), 4 * kBox);
         for (int c = 0; c < 4; ++c)
           tma_load_4d_chk(sDO + c * kBox, &tm_do, bar(cs.do_full), 64 * c, h, sq.trow + i * kT, sq.tb, map_ext(a, kDV, 2));
+        // in the order the MMA issuer frees the slots: tile t's first dW half frees the V slot
+        // before dK_{t-1} frees the Q slot
+        if (!(ok = mbar_wait(bar(cs.v_empty), (nv & 1) ^ 1, abrt))) break;
+        load_v(nv++);
         if (!(ok = mbar_wait(bar(cs.q_empty), (t & 1) ^ 1, abrt))) break;
+        ++nq;
         mbar_arrive_expect_tx(bar(cs.q_full), 2 * kBox + 2 * kT * 4);
         for (int c = 0; c < 2; ++c)
           tma_load_4d_chk(sQ + c * kBox, &tm_q, bar(cs.q_full), qk_col<GR>(m) + 64 * c,
@@ -714,11 +743,10 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
                       bar(cs.q_full));
       }
       // nothing of ours may still be landing at exit
-      mbar_wait(bar(cs.kv_full), 0, nullptr);
-      if (t > 0) {
-        mbar_wait(bar(cs.do_full), (t - 1) & 1, nullptr);
-        mbar_wait(bar(cs.q_full), (t - 1) & 1, nullptr);
-      }
+      mbar_wait(bar(cs.k_full), 0, nullptr);
+      mbar_wait(bar(cs.v_full), (nv - 1) & 1, nullptr);
+      if (ndo > 0) mbar_wait(bar(cs.do_full), (ndo - 1) & 1, nullptr);
+      if (nq > 0) mbar_wait(bar(cs.q_full), (nq - 1) & 1, nullptr);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -733,17 +761,40 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       const uint64_t dDO0 = umma_smem_desc(sDO, 16, 1024);
       const uint64_t dDS0 = umma_smem_desc(sDS, 16, 1024);
       const uint64_t dDSmn = umma_smem_desc(sDS, kBox, 1024);
-      auto issue_dw_s = [&](int t) -> bool {
-        if (!mbar_wait(bar(cs.do_full), t & 1, abrt)) return false;
-        if (t > 0 && !mbar_wait(bar(cs.s_free), (t - 1) & 1, abrt)) return false;
-        tc_fence_after();
+      int nv = 0;  // V half-loads waited for
+      // dW_t goes to TMEM buffer P(t & 1) (columns 128 + 256 (t & 1)), over the V half in the
+      // slot (dv columns [128 hf, +128)): 8 K-steps from dO's boxes 2 hf, 2 hf + 1
+      auto dw_half = [&](int t, int hf) {
 #pragma unroll
-        for (int kk = 0; kk < kDV / 16; ++kk) {
+        for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kT, desc_add(dDO0, off), desc_add(dV0, off), idesc_kk, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + pbuf(t), desc_add(dDO0, 2 * hf * kBox + off), desc_add(dV0, off),
+                      idesc_kk, (hf == (t & 1) && kk == 0) ? 0u : 1u);
         }
-        // the dO slot next holds the staged dQ of tile t - 1; for t = 0 it is free right away
-        if (t == 0) tc_commit(bar(cs.do_empty));
+      };
+      auto wait_v = [&]() -> bool {
+        const bool r = mbar_wait(bar(cs.v_full), nv & 1, abrt);
+        ++nv;
+        tc_fence_after();
+        return r;
+      };
+      // dW_t: first over the V half left in the slot (hf = t & 1), then over the other half once
+      // it has loaded. P(t & 1) last held dQ_{t-2}, which the dQ warps must have read.
+      auto issue_dw = [&](int t) -> bool {
+        if (!mbar_wait(bar(cs.do_full), t & 1, abrt)) return false;
+        if (t >= 2 && !mbar_wait(bar(cs.dq_free), t & 1, abrt)) return false;
+        if (t == 0 && !wait_v()) return false;
+        tc_fence_after();
+        dw_half(t, t & 1);
+        tc_commit(bar(cs.v_empty));  // the slot may take the other half
+        if (!wait_v()) return false;
+        dw_half(t, (t & 1) ^ 1);
+        tc_commit(bar(cs.do_empty));  // dO_t read: the slot may take dO_{t+1}
+        return true;
+      };
+      // S_t (columns 0-127, free once the dS warps hold S_{t-1}); its commit also covers dW_t
+      auto issue_s = [&](int t) -> bool {
+        if (t > 0 && !mbar_wait(bar(cs.s_free), (t - 1) & 1, abrt)) return false;
         if (!mbar_wait(bar(cs.q_full), t & 1, abrt)) return false;
         tc_fence_after();
 #pragma unroll
@@ -751,13 +802,16 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
           mma_bf16_ss(tmem, desc_add(dQ0, off), desc_add(dK0, off), idesc_kk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(bar(cs.s_full));
+        tc_commit(bar(cs.s_full));  // S_t and dW_t
         return true;
       };
-      bool ok = mbar_wait(bar(cs.kv_full), 0, abrt);
+      bool ok = mbar_wait(bar(cs.k_full), 0, abrt);
       tc_fence_after();
-      if (ok && T > 0) ok = issue_dw_s(0);
+      if (ok && T > 0) ok = issue_dw(0) && issue_s(0);
       for (int t = 0; ok && t < T; ++t) {
+        const bool nxt = t + 1 < T;
+        // dW_{t+1} runs while the dS warps work on tile t
+        if (nxt && !(ok = issue_dw(t + 1))) break;
         if (!(ok = mbar_wait(bar(cs.ds_full), t & 1, abrt))) break;
         tc_fence_after();
 #pragma unroll
@@ -765,15 +819,13 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
           mma_bf16_ss(tmem + 2 * kT, desc_add(dDSmn, kk * 2048), desc_add(dQmn, kk * 2048),
                       idesc_dk, (t > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bar(cs.q_empty));
-        if (t + 1 < T && !(ok = issue_dw_s(t + 1))) break;
-        if (t > 0 && !(ok = mbar_wait(bar(cs.dq_free), (t - 1) & 1, abrt))) break;
-        tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)  // dQ partial = dS K  (K = keys)
-          mma_bf16_ss(tmem + 3 * kT, desc_add(dDS0, (kk >> 2) * kBox + (kk & 3) * 32),
+        for (int kk = 0; kk < kT / 16; ++kk)  // dQ partial = dS K into P(t & 1)  (K = keys)
+          mma_bf16_ss(tmem + pbuf(t), desc_add(dDS0, (kk >> 2) * kBox + (kk & 3) * 32),
                       desc_add(dKmn, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
         tc_commit(bar(cs.dq_full));
         tc_commit(bar(cs.ds_empty));
+        if (nxt && !(ok = issue_s(t + 1))) break;
       }
       tc_commit(bar(cs.dk_full));
       tc_commit(bar(cs.teardown));
@@ -809,11 +861,11 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t sv[32], wv[32];
         tmem_ld32(tmem + tl + 64 * wg + 32 * hh, sv);
-        tmem_ld32(tmem + tl + kT + 64 * wg + 32 * hh, wv);
+        tmem_ld32(tmem + tl + pbuf(t) + 64 * wg + 32 * hh, wv);
         tmem_wait_ld();
         if (hh == 1) {
           tc_fence_before();
-          mbar_arrive(bar(cs.s_free));  // S and dW are in registers
+          mbar_arrive(bar(cs.s_free));  // S is in registers
         }
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -842,6 +894,7 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
         st_shared_v4(ds_row + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
                      pk[4 * u + 3]);
       fence_proxy_async_smem();
+      tc_fence_before();  // dW_t has been read: dQ_t may overwrite P(t & 1)
       mbar_arrive(bar(cs.ds_full));
     }
     if (ok) {
@@ -888,52 +941,59 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       }
     }
   } else {
-    // ---- dQ warpgroup: thread r = query row r of the inner tile. Each tile's dQ partial goes
-    // from TMEM to the dO slot (free once the next tile's dW has read it), four 32-column
-    // 128B-swizzled boxes, and is added into the fp32 accumulator by TMA tensor reductions. The
-    // slot is handed back to the producer (do_empty) once the reductions have read it. ----
+    // ---- dQ warpgroup: thread r = query row r of the inner tile. Each tile's dQ partial
+    // (TMEM buffer P(t & 1)) is read two 32-column boxes at a time into registers, so the buffer
+    // is free for dW_{t+2} after two loads; each pair goes into a staging ring of two 128B-swizzled
+    // boxes and is added into the fp32 accumulator by TMA tensor reductions. Thread 0 issues the
+    // reductions and waits until they have read the ring before it is restaged. ----
     const int q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+    const Ext4 eacc = qk_ext<GR>(a, 4);
+    const int qh = qk_head<GR>(a, h, m), qc = qk_col<GR>(m);
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       bool g = ok && mbar_wait(bar(cs.dq_full), t & 1, abrt);
       g = __all_sync(0xffffffffu, g);
-      // thread 0 reaches this barrier only after the previous tile's reductions have read the
-      // slot (for the last tile nothing else orders the staging after them)
       if (!(ok = bar_and(2, 128, g))) break;
-      {
-        tc_fence_after();
+      tc_fence_after();
+      const int i = i0 + t;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + tl + 3 * kT + 32 * c, o);
-          tmem_wait_ld();
-          if (c == 3) {
-            tc_fence_before();
-            mbar_arrive(bar(cs.dq_free));
-          }
-          const uint32_t row = sDO + c * kBox + r * 128;
+      for (int pr = 0; pr < 2; ++pr) {
+        uint32_t o[2][32];
+        tmem_ld32(tmem + tl + pbuf(t) + 64 * pr, o[0]);
+        tmem_ld32(tmem + tl + pbuf(t) + 64 * pr + 32, o[1]);
+        tmem_wait_ld();
+        if (pr == 1) {
+          tc_fence_before();
+          mbar_arrive(bar(cs.dq_free));
+          // the ring: thread 0 waits for the first pair's reductions to have read it
+          if (r == 0) bulk_wait_read();
+          named_barrier_sync(2, 128);
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const uint32_t row = sST + x * kBox + r * 128;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            st_shared_v4(row + ((u ^ (r & 7)) << 4), o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+            st_shared_v4(row + ((u ^ (r & 7)) << 4), o[x][4 * u], o[x][4 * u + 1], o[x][4 * u + 2],
+                         o[x][4 * u + 3]);
         }
         fence_proxy_async_smem();
-      }
-      if (!(ok = bar_and(2, 128, true))) break;
-      if (r == 0) {
-        const int i = i0 + t;
-        const Ext4 eacc = qk_ext<GR>(a, 4);
-        const int qh = qk_head<GR>(a, h, m), qc = qk_col<GR>(m);
-        for (int c = 0; c < 4; ++c)
-          if (!kDebugChecks ||
-              (dbg_index_ok(sq.trow + i * kT, eacc.z) && dbg_index_ok(sq.tb, eacc.w) &&
-               dbg_index_ok(qh, eacc.y) && dbg_index_ok(qc + 32 * c, eacc.x)))
-            tma_reduce_add_4d(&tm_dqacc, sDO + c * kBox, qc + 32 * c, qh, sq.trow + i * kT,
-                              sq.tb);
-        bulk_commit();
-        bulk_wait_read();
-        mbar_arrive(bar(cs.do_empty));  // the slot may take the next dO tile
+        named_barrier_sync(2, 128);
+        if (r == 0) {
+          for (int x = 0; x < 2; ++x) {
+            const int c = 2 * pr + x;
+            if (!kDebugChecks ||
+                (dbg_index_ok(sq.trow + i * kT, eacc.z) && dbg_index_ok(sq.tb, eacc.w) &&
+                 dbg_index_ok(qh, eacc.y) && dbg_index_ok(qc + 32 * c, eacc.x)))
+              tma_reduce_add_4d(&tm_dqacc, sST + x * kBox, qc + 32 * c, qh, sq.trow + i * kT,
+                                sq.tb);
+          }
+          bulk_commit();
+          // before the next tile restages the ring (ordered by the barrier that opens it)
+          if (pr == 1) bulk_wait_read();
+        }
       }
     }
     if (r == 0) bulk_wait_all();
