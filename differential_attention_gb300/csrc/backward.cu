@@ -607,8 +607,9 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
 // by tile t - 1 first, then over the other half (so halves alternate 0,1 | 1,0 | 0,1 ...).
 // Q_m,i (32 KB + its b and delta rows) and dO_i (64 KB) have one slot each; the dS tile (32 KB,
 // [query][key]) is read MN-major as dS^T for dK and K-major for dQ; the dQ staging ring (32 KB).
-// MMA issue order per inner tile t: dW_{t+1} (both V halves) | dK_t | dQ_t | S_{t+1}: dW_{t+1}
-// runs while the dS warps work on tile t, and the next Q load runs under dK_t and dQ_t.
+// MMA issue order per inner tile t: dW_{t+1} over the resident V half | dK_t | dW_{t+1} over the
+// other half | dQ_t | S_{t+1}: the first half runs while the dS warps work on tile t, the V
+// half-load runs under dK_t, and the next Q load under the second half and dQ_t.
 // =============================================================================================
 namespace kq {
 constexpr int kThreads = 448;  // TMA, MMA, 8 dS warps, 4 dQ warps
@@ -780,13 +781,16 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       };
       // dW_t: first over the V half left in the slot (hf = t & 1), then over the other half once
       // it has loaded. P(t & 1) last held dQ_{t-2}, which the dQ warps must have read.
-      auto issue_dw = [&](int t) -> bool {
+      auto dw_first = [&](int t) -> bool {
         if (!mbar_wait(bar(cs.do_full), t & 1, abrt)) return false;
         if (t >= 2 && !mbar_wait(bar(cs.dq_free), t & 1, abrt)) return false;
         if (t == 0 && !wait_v()) return false;
         tc_fence_after();
         dw_half(t, t & 1);
         tc_commit(bar(cs.v_empty));  // the slot may take the other half
+        return true;
+      };
+      auto dw_second = [&](int t) -> bool {
         if (!wait_v()) return false;
         dw_half(t, (t & 1) ^ 1);
         tc_commit(bar(cs.do_empty));  // dO_t read: the slot may take dO_{t+1}
@@ -807,11 +811,12 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
       };
       bool ok = mbar_wait(bar(cs.k_full), 0, abrt);
       tc_fence_after();
-      if (ok && T > 0) ok = issue_dw(0) && issue_s(0);
+      if (ok && T > 0) ok = dw_first(0) && dw_second(0) && issue_s(0);
       for (int t = 0; ok && t < T; ++t) {
         const bool nxt = t + 1 < T;
-        // dW_{t+1} runs while the dS warps work on tile t
-        if (nxt && !(ok = issue_dw(t + 1))) break;
+        // dW_{t+1}'s first half runs while the dS warps work on tile t; its second half waits
+        // for the other V half, whose load runs under dK_t
+        if (nxt && !(ok = dw_first(t + 1))) break;
         if (!(ok = mbar_wait(bar(cs.ds_full), t & 1, abrt))) break;
         tc_fence_after();
 #pragma unroll
@@ -819,6 +824,7 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
           mma_bf16_ss(tmem + 2 * kT, desc_add(dDSmn, kk * 2048), desc_add(dQmn, kk * 2048),
                       idesc_dk, (t > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bar(cs.q_empty));
+        if (nxt && !(ok = dw_second(t + 1))) break;
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)  // dQ partial = dS K into P(t & 1)  (K = keys)
           mma_bf16_ss(tmem + pbuf(t), desc_add(dDS0, (kk >> 2) * kBox + (kk & 3) * 32),
@@ -867,21 +873,31 @@ __global__ void __launch_bounds__(kq::kThreads, 1)
           tc_fence_before();
           mbar_arrive(bar(cs.s_free));  // S is in registers
         }
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
+        // dS for a pair of keys; the mask is tested outside the unrolled loops (only tiles that
+        // reach past N or cross the diagonal take the masked copy)
+        auto ds_pair = [&](int e, float& y0, float& y1) {
           float x0, x1;
           f2unpack(f2fma(f2pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nb2), x0, x1);
           const uint64_t g = f2fma(f2pack(__uint_as_float(wv[e]), __uint_as_float(wv[e + 1])), coef2, nd2);
-          float y0, y1;
           f2unpack(f2mul(f2pack(ex2_approx(x0), ex2_approx(x1)), g), y0, y1);
-          if (edge) {
+        };
+        if (!edge) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float y0, y1;
+            ds_pair(e, y0, y1);
+            pk[16 * hh + (e >> 1)] = pack_bf16x2(y0, y1);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float y0, y1;
+            ds_pair(e, y0, y1);
             const int kk0 = j * kT + 64 * wg + 32 * hh + e;
             const bool v0 = kk0 < sq.len && qq < sq.len && (!a.causal || qq >= kk0);
             const bool v1 = kk0 + 1 < sq.len && qq < sq.len && (!a.causal || qq >= kk0 + 1);
-            y0 = v0 ? y0 : 0.f;
-            y1 = v1 ? y1 : 0.f;
+            pk[16 * hh + (e >> 1)] = pack_bf16x2(v0 ? y0 : 0.f, v1 ? y1 : 0.f);
           }
-          pk[16 * hh + (e >> 1)] = pack_bf16x2(y0, y1);
         }
       }
       if (t > 0) {
