@@ -523,13 +523,24 @@ __global__ void __launch_bounds__(dl::kThreads, 1)
       mbar_arrive(bar(cs.s_free[buf]));
       const int key0 = t * kT;
       uint32_t pk[kT / 2];
+      // the mask is tested outside the unrolled loops: only the tile that reaches the row's
+      // last visible key takes the masked copy
+      if (key0 + kT <= lim) {
 #pragma unroll
-      for (int i = 0; i < kT / 2; ++i) {
-        const float x0 = fmaf(__uint_as_float(sr[i >> 4][(2 * i) & 31]), a.c_log2, -b2);
-        const float x1 = fmaf(__uint_as_float(sr[i >> 4][(2 * i + 1) & 31]), a.c_log2, -b2);
-        const float p0 = (key0 + 2 * i < lim) ? ex2_approx(x0) : 0.f;
-        const float p1 = (key0 + 2 * i + 1 < lim) ? ex2_approx(x1) : 0.f;
-        pk[i] = pack_bf16x2(p0, p1);
+        for (int i = 0; i < kT / 2; ++i) {
+          const float x0 = fmaf(__uint_as_float(sr[i >> 4][(2 * i) & 31]), a.c_log2, -b2);
+          const float x1 = fmaf(__uint_as_float(sr[i >> 4][(2 * i + 1) & 31]), a.c_log2, -b2);
+          pk[i] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kT / 2; ++i) {
+          const float x0 = fmaf(__uint_as_float(sr[i >> 4][(2 * i) & 31]), a.c_log2, -b2);
+          const float x1 = fmaf(__uint_as_float(sr[i >> 4][(2 * i + 1) & 31]), a.c_log2, -b2);
+          const float p0 = (key0 + 2 * i < lim) ? ex2_approx(x0) : 0.f;
+          const float p1 = (key0 + 2 * i + 1 < lim) ? ex2_approx(x1) : 0.f;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
       }
       if (t > 0) {
         ok = mbar_wait(bar(cs.p_empty), (t - 1) & 1, abrt);
@@ -1253,23 +1264,33 @@ __global__ void __launch_bounds__(vv::kThreads, 1)
           tc_fence_before();
           mbar_arrive(bar(cs.s_free));  // both score tiles are in registers
         }
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
+        // W for a pair of keys; the mask is tested outside the unrolled loops (only tiles that
+        // reach past N or cross the diagonal take the masked copy)
+        auto w_pair = [&](int e, float& w0, float& w1) {
           float x0, x1, y0, y1;
           f2unpack(f2fma(f2pack(__uint_as_float(s1[e]), __uint_as_float(s1[e + 1])), c2, nb1_2), x0, x1);
           f2unpack(f2fma(f2pack(__uint_as_float(s2[e]), __uint_as_float(s2[e + 1])), c2, nb2_2), y0, y1);
-          float w0, w1;
           f2unpack(f2fma(f2pack(ex2_approx(y0), ex2_approx(y1)), nlam2,
                          f2pack(ex2_approx(x0), ex2_approx(x1))),
                    w0, w1);
-          if (edge) {
+        };
+        if (!edge) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float w0, w1;
+            w_pair(e, w0, w1);
+            pk[16 * hh + (e >> 1)] = pack_bf16x2(w0, w1);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float w0, w1;
+            w_pair(e, w0, w1);
             const int kk0 = j * kT + 64 * wg + 32 * hh + e;
             const bool v0 = kk0 < sq.len && qq < sq.len && (!a.causal || qq >= kk0);
             const bool v1 = kk0 + 1 < sq.len && qq < sq.len && (!a.causal || qq >= kk0 + 1);
-            w0 = v0 ? w0 : 0.f;
-            w1 = v1 ? w1 : 0.f;
+            pk[16 * hh + (e >> 1)] = pack_bf16x2(v0 ? w0 : 0.f, v1 ? w1 : 0.f);
           }
-          pk[16 * hh + (e >> 1)] = pack_bf16x2(w0, w1);
         }
       }
       if (t > 0) {
