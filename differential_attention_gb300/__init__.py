@@ -165,6 +165,16 @@ _SIGNATURES = {
                                                                  ctypes.c_float]
                          + [ctypes.c_void_p] * 5 + [ctypes.c_int] * 8
                          + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_gda_fwd_train_varlen": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 2
+                                      + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                                         ctypes.c_float] + [ctypes.c_int] * 7
+                                      + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_gda_bwd_varlen_workspace_size": (ctypes.c_int, [ctypes.c_int] * 7
+                                               + [ctypes.POINTER(ctypes.c_size_t)]),
+    "diffattn_gda_bwd_varlen": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 2
+                                + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                                   ctypes.c_float] + [ctypes.c_void_p] * 5 + [ctypes.c_int] * 7
+                                + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "diffattn_gda_decode": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.c_void_p,
                                                                     ctypes.c_float]
                             + [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_size_t,
@@ -1255,6 +1265,85 @@ def diffattn_gda_bwd(q, k, v, o_pre, stats, dout, lam, n_signal: int, lambda_ini
                                   n_noise, d, dv, _train_flags(causal, norm, scale), DIFFATTN_BF16,
                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _stream(stream)))
+    return grads
+
+
+def diffattn_gda_fwd_train_varlen(q, k, v, cu_seqlens, lam, n_signal: int, lambda_init: float = 0.0,
+                                  max_seqlen=None, norm_weight=None, eps: float = 1e-5,
+                                  causal: bool = True, norm: bool = True, scale: bool = True,
+                                  noise_pass: bool = True, workspace=None, stream=None):
+    """Grouped training forward over packed sequences (q, k [total, n_signal + n_noise, d],
+    v [total, n_signal, dv]): returns (out, o_pre, stats) with stats [B, n_signal, 2, Npad],
+    Npad the longest sequence rounded up to 128."""
+    _dev("q", q, torch.bfloat16)
+    total, heads, d = q.shape
+    n_noise = heads - int(n_signal)
+    _dev("k", k, torch.bfloat16)
+    _dev("v", v, torch.bfloat16)
+    dv = v.shape[-1]
+    _dev("cu_seqlens", cu_seqlens, torch.int32)
+    B, N = _max_seqlen(cu_seqlens, max_seqlen)
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    out = torch.zeros((total, int(n_signal), dv), dtype=torch.bfloat16, device=q.device)
+    o_pre = torch.zeros_like(out)
+    stats = torch.zeros((B, int(n_signal), 2, (N + 127) // 128 * 128), dtype=torch.float32,
+                        device=q.device)
+    workspace, ws_bytes = _gda_ws(noise_pass, workspace, B, N, n_signal, n_noise, d, dv, q.device)
+    _check(lib().diffattn_gda_fwd_train_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(o_pre),
+                                               _ptr(stats), _ptr(cu_seqlens), N, total, _ptr(lam),
+                                               float(lambda_init), _ptr(norm_weight), float(eps), B,
+                                               int(n_signal), n_noise, d, dv,
+                                               _train_flags(causal, norm, scale), DIFFATTN_BF16,
+                                               _ptr(workspace), ws_bytes, _stream(stream)))
+    return out, o_pre, stats
+
+
+def diffattn_gda_bwd_varlen_workspace_size(B: int, max_seqlen: int, total: int, n_signal: int,
+                                           n_noise: int, d: int = 128, dv: int = 256) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().diffattn_gda_bwd_varlen_workspace_size(B, max_seqlen, total, n_signal, n_noise,
+                                                        d, dv, ctypes.byref(n)))
+    return n.value
+
+
+def diffattn_gda_bwd_varlen(q, k, v, o_pre, stats, dout, cu_seqlens, lam, n_signal: int,
+                            lambda_init: float = 0.0, max_seqlen=None, norm_weight=None,
+                            eps: float = 1e-5, causal: bool = True, norm: bool = True,
+                            scale: bool = True, workspace=None, grads=None, stream=None):
+    """Grouped backward over packed sequences, from the tensors of diffattn_gda_fwd_train_varlen.
+    Returns dict(dq, dk [total, n_signal + n_noise, d], dv, dlam [n_signal], dw); rows in no
+    sequence stay zero in the returned tensors."""
+    _dev("q", q, torch.bfloat16)
+    total, heads, d = q.shape
+    n_noise = heads - int(n_signal)
+    dv = v.shape[-1]
+    for name, t in (("k", k), ("v", v), ("o_pre", o_pre), ("dout", dout)):
+        _dev(name, t, torch.bfloat16)
+    _dev("stats", stats, torch.float32)
+    _dev("cu_seqlens", cu_seqlens, torch.int32)
+    B, N = _max_seqlen(cu_seqlens, max_seqlen)
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if workspace is None:
+        workspace = torch.empty(diffattn_gda_bwd_varlen_workspace_size(B, N, total, int(n_signal),
+                                                                       n_noise, d, dv),
+                                dtype=torch.uint8, device=q.device)
+    if grads is None:
+        grads = dict(dq=torch.zeros_like(q), dk=torch.zeros_like(k), dv=torch.zeros_like(v),
+                     dlam=torch.empty((int(n_signal),), dtype=torch.float32, device=q.device),
+                     dw=torch.empty((dv,), dtype=torch.float32, device=q.device))
+    _check(lib().diffattn_gda_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o_pre), _ptr(stats),
+                                         _ptr(dout), _ptr(cu_seqlens), N, total, _ptr(lam),
+                                         float(lambda_init), _ptr(norm_weight), float(eps),
+                                         _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]),
+                                         _ptr(grads["dlam"]), _ptr(grads.get("dw")), B,
+                                         int(n_signal), n_noise, d, dv,
+                                         _train_flags(causal, norm, scale), DIFFATTN_BF16,
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream)))
     return grads
 
 

@@ -1667,6 +1667,105 @@ DIFFATTN_API int diffattn_gda_bwd(const void* q, const void* k, const void* v, c
                   workspace, ws_bytes, stream, n_noise);
 }
 
+DIFFATTN_API int diffattn_gda_fwd_train_varlen(const void* q, const void* k, const void* v,
+                                               void* out, void* o_pre, float* stats,
+                                               const int* cu_seqlens, int max_seqlen, int total,
+                                               const float* lambda, float lambda_init,
+                                               const float* norm_weight, float eps, int B,
+                                               int n_signal, int n_noise, int d, int dv, int flags,
+                                               int dtype, void* workspace, size_t ws_bytes,
+                                               void* stream) {
+  const char* fn = "diffattn_gda_fwd_train_varlen";
+  if (!q || !k || !v || !out || !o_pre || !stats || !cu_seqlens || !lambda)
+    return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  constexpr int kTrainFlags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kTrainFlags) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "%s: eps must be > 0 with DIFFATTN_NORM", fn);
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  const int heads = n_signal + n_noise;
+  if (int rc = check_train_shape(fn, B, max_seqlen, heads, d, dv, dtype)) return rc;
+  if (total < max_seqlen || static_cast<long long>(total) * heads > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need max_seqlen <= total and total * heads <= 2^30", fn);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(o_pre, 16) || !aligned(stats, 16) || !aligned(lambda, 4) ||
+      !aligned(cu_seqlens, 4) || (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  if (workspace) {  // the noise maps' statistics of B sequences of up to max_seqlen rows
+    size_t need = 0;
+    diffattn_gda_fwd_workspace_size(B, max_seqlen, n_signal, n_noise, d, dv, &need);
+    if (ws_bytes < need || !aligned(workspace, 256))
+      return fail(DIFFATTN_ERR_WORKSPACE, "%s: need a 256-byte aligned workspace of %zu bytes", fn,
+                  need);
+  }
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = max_seqlen;
+  p.units = n_signal;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_GDA;
+  p.q_heads = heads;
+  p.kv_heads = heads;
+  p.q_cols = d;
+  p.k_cols = d;
+  p.group = n_signal / n_noise;
+  p.lambda = lambda;
+  p.lam_logit = nullptr;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  p.stats = stats;
+  p.o_pre = o_pre;
+  p.n_pad = (max_seqlen + 127) / 128 * 128;
+  p.cu_seqlens = cu_seqlens;
+  p.total = total;
+  if (workspace) p.gda_noise = static_cast<float*>(workspace);
+  return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
+}
+
+DIFFATTN_API int diffattn_gda_bwd_varlen_workspace_size(int B, int max_seqlen, int total,
+                                                        int n_signal, int n_noise, int d, int dv,
+                                                        size_t* bytes) {
+  const char* fn = "diffattn_gda_bwd_varlen_workspace_size";
+  if (!bytes) return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  if (int rc = check_train_shape(fn, B, max_seqlen, n_signal + n_noise, d, dv, DIFFATTN_BF16))
+    return rc;
+  if (total < max_seqlen) return fail(DIFFATTN_ERR_SHAPE, "%s: need max_seqlen <= total", fn);
+  *bytes = da::backward_workspace_bytes(B, max_seqlen, n_signal, total, true);
+  return ok();
+}
+
+DIFFATTN_API int diffattn_gda_bwd_varlen(const void* q, const void* k, const void* v,
+                                         const void* o_pre, const float* stats, const void* dout,
+                                         const int* cu_seqlens, int max_seqlen, int total,
+                                         const float* lambda, float lambda_init,
+                                         const float* norm_weight, float eps, void* dq, void* dk,
+                                         void* dv, float* dlambda, float* dnorm_weight, int B,
+                                         int n_signal, int n_noise, int d, int dv_width, int flags,
+                                         int dtype, void* workspace, size_t ws_bytes,
+                                         void* stream) {
+  const char* fn = "diffattn_gda_bwd_varlen";
+  if (!cu_seqlens) return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  const int heads = n_signal + n_noise;
+  if (int rc = check_train_shape(fn, B, max_seqlen, heads, d, dv_width, dtype)) return rc;
+  if (total < max_seqlen || static_cast<long long>(total) * heads > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need max_seqlen <= total and total * heads <= 2^30", fn);
+  return bwd_impl(fn, q, k, v, o_pre, stats, dout, lambda, lambda_init, norm_weight, eps, dq, dk,
+                  dv, dlambda, dnorm_weight, B, max_seqlen, n_signal, d, dv_width, flags, dtype,
+                  cu_seqlens, total, workspace, ws_bytes, stream, n_noise);
+}
+
 DIFFATTN_API int diffattn_gda_fwd_varlen(const void* q, const void* k, const void* v, void* out,
                                          const int* cu_seqlens, int max_seqlen, int total,
                                          const float* lambda, float lambda_init,

@@ -1353,6 +1353,8 @@ constexpr int kFinishSumBlocks = kDV / 32;
 // Grouped form: the noise heads' dK (fp32 sums over each group's signal heads) to bf16 at heads
 // Hs .. Hs + Hn - 1 of dk [tokens, Hs + Hn, d]; one thread per 8 channels.
 __global__ void __launch_bounds__(256) bwd_gda_dk_kernel(const Args a, long long tokens) {
+  // packed: rows past the last sequence belong to none and are not written
+  if (a.cu) tokens = min(tokens, static_cast<long long>(min(max(a.cu[a.B], 0), a.total)));
   const int hn = a.hqk - a.H;
   const long long n8 = tokens * hn * (kD / 8);
   for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n8;

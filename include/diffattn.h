@@ -710,6 +710,46 @@ DIFFATTN_API int diffattn_gda_bwd(const void* q, const void* k, const void* v, c
                                   int N, int n_signal, int n_noise, int d, int dv_width, int flags,
                                   int dtype, void* workspace, size_t ws_bytes, void* stream);
 
+/* Grouped training over packed sequences: diffattn_gda_fwd_train and diffattn_gda_bwd with the
+ * packed layout of diffattn_gda_fwd_varlen (page "Differential Transformer: softmax can't say
+ * zero, so it subtracts", section "What other people found", with the batching of
+ * diffattn_fwd_train_varlen / diffattn_bwd_varlen). Each sequence's gradients are those of its
+ * own grouped forward; dlambda and dnorm_weight sum over the sequences.
+ *   q, k, dq, dk : device bf16 [total, n_signal + n_noise, d]; v, dv, out, o_pre, dout : device
+ *                  bf16 [total, n_signal, dv]; sequence b is rows cu_seqlens[b] ..
+ *                  cu_seqlens[b+1] - 1 (device int32 [B + 1], non-decreasing, cu[B] <= total,
+ *                  checked on the device)
+ *   stats        : device fp32 [B, n_signal, 2, Npad], Npad = max_seqlen rounded up to 128
+ *   max_seqlen   : the longest sequence (an upper bound)
+ *   workspace    : forward, as diffattn_gda_fwd_varlen (or NULL); backward, at least
+ *                  diffattn_gda_bwd_varlen_workspace_size(B, max_seqlen, total, ...) bytes,
+ *                  256-byte aligned
+ * Rows of out, o_pre, dq, dk and dv that belong to no sequence are not written.
+ * Supported: dtype DIFFATTN_BF16, flags CAUSAL | NORM | SCALE, d = 128, dv = 256, n_signal a
+ * multiple of n_noise.
+ * Errors: as diffattn_gda_fwd_train / diffattn_gda_bwd; ERR_SHAPE if max_seqlen > total or total *
+ * (n_signal + n_noise) > 2^30; bad offsets are reported through diffattn_device_status. */
+DIFFATTN_API int diffattn_gda_fwd_train_varlen(const void* q, const void* k, const void* v,
+                                               void* out, void* o_pre, float* stats,
+                                               const int* cu_seqlens, int max_seqlen, int total,
+                                               const float* lambda, float lambda_init,
+                                               const float* norm_weight, float eps, int B,
+                                               int n_signal, int n_noise, int d, int dv, int flags,
+                                               int dtype, void* workspace, size_t ws_bytes,
+                                               void* stream);
+DIFFATTN_API int diffattn_gda_bwd_varlen_workspace_size(int B, int max_seqlen, int total,
+                                                        int n_signal, int n_noise, int d, int dv,
+                                                        size_t* bytes);
+DIFFATTN_API int diffattn_gda_bwd_varlen(const void* q, const void* k, const void* v,
+                                         const void* o_pre, const float* stats, const void* dout,
+                                         const int* cu_seqlens, int max_seqlen, int total,
+                                         const float* lambda, float lambda_init,
+                                         const float* norm_weight, float eps, void* dq, void* dk,
+                                         void* dv, float* dlambda, float* dnorm_weight, int B,
+                                         int n_signal, int n_noise, int d, int dv_width, int flags,
+                                         int dtype, void* workspace, size_t ws_bytes,
+                                         void* stream);
+
 /* Grouped prefill with each sequence's queries at the end of its keys (chunked prompts, new tokens
  * over a cache): diffattn_gda_fwd's operator with the key layout of diffattn_fwd_varlen_qk
  * (keys packed with offsets of their own) or of diffattn_fwd_paged (keys in page pools).

@@ -703,6 +703,28 @@ def diffattn_gda_bwd(q, k, v, lam, lam_init: float, n_signal: int, dy, norm_weig
     return out
 
 
+def diffattn_gda_bwd_varlen(q, k, v, cu_seqlens, lam, lam_init: float, n_signal: int, dy,
+                            norm_weight=None, eps: float = 1e-5, norm: bool = True,
+                            apply_scale: bool = True, causal: bool = True):
+    """`diffattn_gda_bwd` over packed sequences (q, k [total, Hs + Hn, d], v, dy [total, Hs, dv]):
+    each sequence's gradients are those of its own grouped forward; dlam and dw sum over the
+    sequences. Rows in no sequence get zero gradients."""
+    q, k, v, dy = _f64(q), _f64(k), _f64(v), _f64(dy)
+    out = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v),
+               dlam=np.zeros(n_signal), dw=np.zeros(v.shape[-1]))
+    for s0, s1 in varlen_segments(cu_seqlens):
+        if s1 == s0:
+            continue
+        g = diffattn_gda_bwd(q[None, s0:s1], k[None, s0:s1], v[None, s0:s1], lam, lam_init,
+                             n_signal, dy[None, s0:s1], norm_weight, eps, norm, apply_scale,
+                             causal)
+        for name in ("dq", "dk", "dv"):
+            out[name][s0:s1] = g[name][0]
+        out["dlam"] += g["dlam"]
+        out["dw"] += g["dw"]
+    return out
+
+
 def diffattn_gda_decode(q, k_cache, v_cache, seqlens, lam, lam_init: float, n_signal: int,
                         norm_weight=None, eps: float = 1e-5, norm: bool = True,
                         apply_scale: bool = True):

@@ -479,6 +479,34 @@ def test_gda_training_validation(L):
     assert bwd(q=ODD) == -4
     assert bwd(ws_bytes=need - 1) == -8
 
+    # packed sequences
+    def train_v(cu=FAKE, stats=FAKE, ns=12, nn=3, mx=300, total=1000, dtype=0):
+        return L.diffattn_gda_fwd_train_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, stats, cu, mx, total,
+                                               FAKE, 0.5, None, 1e-5, 4, ns, nn, 128, 256, 7,
+                                               dtype, None, 0, None)
+
+    assert train_v(cu=None) == -1
+    assert train_v(stats=None) == -1
+    assert train_v(ns=12, nn=5) == -2
+    assert train_v(mx=2000) == -2            # longer than the packed axis
+    assert train_v(dtype=1) == -3
+    assert train_v(cu=ctypes.c_void_p(0x10002)) == -4
+    assert L.diffattn_gda_bwd_varlen_workspace_size(4, 300, 1000, 12, 3, 128, 256,
+                                                    ctypes.byref(n)) == 0
+    need_v = n.value
+    assert L.diffattn_gda_bwd_varlen_workspace_size(4, 300, 200, 12, 3, 128, 256,
+                                                    ctypes.byref(n)) == -2
+
+    def bwd_v(cu=FAKE, ns=12, nn=3, ws_bytes=need_v, total=1000):
+        return L.diffattn_gda_bwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, cu, 300, total, FAKE,
+                                         0.5, None, 1e-5, FAKE, FAKE, FAKE, FAKE, None, 4, ns, nn,
+                                         128, 256, 7, 0, FAKE, ws_bytes, None)
+
+    assert bwd_v(cu=None) == -1
+    assert bwd_v(ns=12, nn=5) == -2
+    assert bwd_v(total=200) == -2
+    assert bwd_v(ws_bytes=need_v - 1) == -8
+
 
 def test_v2_decode_fp8_paged_validation(L):
     n = ctypes.c_size_t(0)

@@ -150,3 +150,96 @@ def test_gda_bwd_is_ungrouped_with_one_signal_head_per_noise_head():
         else:
             ulp = 2.0 ** -7 * dq_u.abs() + 1e-3 * dq_u.abs().max()
             assert bool(((dq - dq_u).abs() <= ulp).all())
+
+
+# packed sequences: (lengths, n_signal, n_noise, causal, norm); empty and one-token sequences,
+# ragged and multi-tile ones, and three rows after the last sequence that belong to none
+GDA_VARLEN_CASES = [([300, 0, 129, 5, 640], 4, 2, True, True), ([128, 257], 3, 3, False, True),
+                    ([200, 1, 77], 6, 2, True, False)]
+
+
+@pytest.mark.parametrize("lens,Hs,Hn,causal,norm", GDA_VARLEN_CASES)
+def test_gda_train_varlen(lens, Hs, Hn, causal, norm):
+    """Grouped training over packed sequences: the forward equals the packed grouped prefill
+    (bit-equal) and every gradient matches the oracle's per-sequence grouped backward; rows in no
+    sequence stay zero."""
+    n = sum(lens)
+    total = n + 3
+    inp = make_gda_inputs(1, total, Hs, Hn, 128, 256, seed=91 + len(lens) + Hs)
+    dy = make_dout(1, total, Hs, 256, seed=97 + len(lens))
+    q, k, v, dyp = inp.q[0], inp.k[0], inp.v[0], dy[0]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    li = ref.lambda_init(inp.layer)
+    w = _w()
+    wd = w.to(DEV) if norm else None
+    qd, kd, vd, cud, lam = q.to(DEV), k.to(DEV), v.to(DEV), cu.to(DEV), inp.lam.to(DEV)
+    out, o_pre, stats = da.diffattn_gda_fwd_train_varlen(qd, kd, vd, cud, lam, Hs, li,
+                                                         norm_weight=wd, causal=causal, norm=norm)
+    plain = da.diffattn_gda_fwd_varlen(qd, kd, vd, cud, lam, Hs, li, norm_weight=wd,
+                                       causal=causal, norm=norm)
+    assert torch.equal(out[:n], plain[:n])
+    g = da.diffattn_gda_bwd_varlen(qd, kd, vd, o_pre, stats, dyp.to(DEV), cud, lam, Hs, li,
+                                   norm_weight=wd, causal=causal, norm=norm)
+    torch.cuda.synchronize()
+    da.diffattn_device_status()
+    want = ref.diffattn_gda_bwd_varlen(q, k, v, cu, inp.lam, li, Hs, dyp,
+                                       norm_weight=w if norm else None, norm=norm, causal=causal)
+    for name in ("dq", "dk", "dv"):
+        assert_grad(g[name][:n], want[name][:n], name=name)
+        assert torch.count_nonzero(g[name][n:]) == 0
+    terms = np.zeros(Hs)
+    for s0, s1 in zip(cu[:-1].tolist(), cu[1:].tolist()):
+        if s1 > s0:
+            one = type(inp)(**{**inp.__dict__, "q": inp.q[:, s0:s1], "k": inp.k[:, s0:s1],
+                               "v": inp.v[:, s0:s1]})
+            terms += _dlam_term_scale(one, dy[:, s0:s1], li, w if norm else None, norm, True,
+                                      causal)
+    gl = g["dlam"].double().cpu().numpy()
+    assert np.all(np.abs(gl - want["dlam"]) <= 1e-2 * np.abs(want["dlam"]) + 2.0 ** -8 * terms)
+    if norm:
+        assert_grad(g["dw"], want["dw"], rel_tol=1e-2, name="dw")
+
+
+def test_gda_bwd_varlen_one_sequence_is_the_batched_backward():
+    """One packed sequence filling the batch: the signal heads' dK, dV, dlambda and the norm
+    weight's gradient are bit-equal to the batched grouped backward's (fixed-order sums); dQ and
+    the noise heads' dK agree to the last bf16 bit (their fp32 sums, over key tiles and over the
+    group's signal heads, land in any order)."""
+    N, Hs, Hn = 384, 6, 2
+    inp = make_gda_inputs(1, N, Hs, Hn, 128, 256, seed=103, device=DEV)
+    dy = make_dout(1, N, Hs, 256, seed=107).to(DEV)
+    w = _w().to(DEV)
+    cu = torch.tensor([0, N], dtype=torch.int32, device=DEV)
+    _, o_pre, stats = da.diffattn_gda_fwd_train(inp.q, inp.k, inp.v, inp.lam, Hs, 0.4, norm_weight=w)
+    g = da.diffattn_gda_bwd(inp.q, inp.k, inp.v, o_pre, stats, dy, inp.lam, Hs, 0.4, norm_weight=w)
+    _, o_pre_p, stats_p = da.diffattn_gda_fwd_train_varlen(inp.q[0], inp.k[0], inp.v[0], cu,
+                                                           inp.lam, Hs, 0.4, norm_weight=w)
+    p = da.diffattn_gda_bwd_varlen(inp.q[0], inp.k[0], inp.v[0], o_pre_p, stats_p, dy[0], cu,
+                                   inp.lam, Hs, 0.4, norm_weight=w)
+    torch.cuda.synchronize()
+    da.diffattn_device_status()
+    assert torch.equal(o_pre[0], o_pre_p) and torch.equal(stats, stats_p)
+    assert torch.equal(g["dk"][0, :, :Hs], p["dk"][:, :Hs]) and torch.equal(g["dv"][0], p["dv"])
+    assert torch.equal(g["dlam"], p["dlam"]) and torch.equal(g["dw"], p["dw"])
+    for a, b in ((g["dq"][0], p["dq"]), (g["dk"][0, :, Hs:], p["dk"][:, Hs:])):
+        a, b = a.float(), b.float()
+        assert bool(((a - b).abs() <= 2.0 ** -7 * b.abs() + 1e-3 * b.abs().max()).all())
+
+
+def test_gda_train_varlen_bad_offsets_are_reported():
+    """A sequence running past the packed length is skipped by the grouped training forward and
+    every backward kernel, and reported."""
+    inp = make_gda_inputs(1, 256, 4, 2, 128, 256, seed=109, device=DEV)
+    dy = make_dout(1, 256, 4, 256, seed=113).to(DEV)
+    cu = torch.tensor([0, 128, 400], dtype=torch.int32, device=DEV)  # 400 > total
+    q, k, v = inp.q[0], inp.k[0], inp.v[0]
+    out, o_pre, stats = da.diffattn_gda_fwd_train_varlen(q, k, v, cu, inp.lam, 4, 0.5,
+                                                         max_seqlen=256)
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_device_status()
+    assert e.value.status == -9
+    da.diffattn_gda_bwd_varlen(q, k, v, o_pre, stats, dy[0], cu, inp.lam, 4, 0.5, max_seqlen=256)
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_device_status()
+    assert e.value.status == -9
+    da.diffattn_device_status()

@@ -646,6 +646,44 @@ def pin_gda_varlen():
     assert np.allclose(a[:3], b[:3]) and np.allclose(a[9], b[9]) and not np.allclose(a[3:9], b[3:9])
 
 
+def pin_gda_bwd_varlen():
+    """Packed grouped backward: with equal lengths it is the batched grouped backward; with one
+    noise head per signal head it is the ungrouped packed backward on the halves stored as heads;
+    rows in no sequence get zero gradients and a sequence's gradients see only itself."""
+    rng = np.random.default_rng(47)
+    B, N, Hs, Hn, d, dv = 2, 5, 4, 2, 3, 4
+    q = rng.standard_normal((B, N, Hs + Hn, d)); k = rng.standard_normal((B, N, Hs + Hn, d))
+    v = rng.standard_normal((B, N, Hs, dv)); dy = rng.standard_normal((B, N, Hs, dv))
+    lam = np.array([0.2, 0.6, 0.9, 0.4]); w = rng.uniform(0.5, 1.5, dv)
+    want = ref.diffattn_gda_bwd(q, k, v, lam, 0.3, Hs, dy, norm_weight=w)
+    got = ref.diffattn_gda_bwd_varlen(q.reshape(B * N, Hs + Hn, d), k.reshape(B * N, Hs + Hn, d),
+                                      v.reshape(B * N, Hs, dv), np.arange(B + 1) * N, lam, 0.3, Hs,
+                                      dy.reshape(B * N, Hs, dv), norm_weight=w)
+    for name in ("dq", "dk", "dv"):
+        assert np.allclose(got[name], want[name].reshape(B * N, *want[name].shape[2:]), rtol=1e-12,
+                           atol=1e-12), name
+    assert np.allclose(got["dlam"], want["dlam"]) and np.allclose(got["dw"], want["dw"])
+    # n_noise = n_signal: the ungrouped packed backward on [Q1 | Q2], an empty sequence, a tail
+    cu = np.array([0, 3, 3, 8]); T, H = 9, 2
+    q1, q2, k1, k2 = (rng.standard_normal((T, H, d)) for _ in range(4))
+    vv = rng.standard_normal((T, H, dv)); dd = rng.standard_normal((T, H, dv))
+    lam2 = np.array([0.5, 0.8])
+    g = ref.diffattn_gda_bwd_varlen(np.concatenate([q1, q2], 1), np.concatenate([k1, k2], 1), vv,
+                                    cu, lam2, 0.3, H, dd, norm_weight=w)
+    u = ref.diffattn_bwd_varlen(np.concatenate([q1, q2], 2), np.concatenate([k1, k2], 2), vv, cu,
+                                lam2, 0.3, dd, norm_weight=w)
+    assert np.allclose(g["dq"][:, :H], u["dq"][..., :d]) and np.allclose(g["dq"][:, H:], u["dq"][..., d:])
+    assert np.allclose(g["dk"][:, :H], u["dk"][..., :d]) and np.allclose(g["dk"][:, H:], u["dk"][..., d:])
+    assert np.allclose(g["dv"], u["dv"]) and np.allclose(g["dlam"], u["dlam"]) and np.allclose(g["dw"], u["dw"])
+    assert not g["dq"][8].any() and not g["dk"][8].any() and not g["dv"][8].any()
+    # a sequence's gradients do not depend on another sequence's rows
+    k3 = np.concatenate([k1, k2], 1).copy(); k3[3:8] += rng.standard_normal((5, 2 * H, d))
+    g3 = ref.diffattn_gda_bwd_varlen(np.concatenate([q1, q2], 1), k3, vv, cu, lam2, 0.3, H, dd,
+                                     norm_weight=w)
+    assert np.allclose(g3["dq"][:3], g["dq"][:3]) and np.allclose(g3["dk"][:3], g["dk"][:3])
+    assert not np.allclose(g3["dq"][3:8], g["dq"][3:8])
+
+
 def pin_gda_varlen_qk_and_paged():
     """Grouped prefill with queries at the end of their keys: with Lq = Lk it is the packed grouped
     prefill; each query row equals that row of the whole sequence's grouped prefill; with one noise
@@ -742,7 +780,7 @@ PINS = [pin_lambda_init_table, pin_lambda_init_shape, pin_lambda_closed_forms, p
         pin_norm_and_scale, pin_fwd_layout, pin_decode_is_last_prefill_row, pin_v2,
         pin_v2_decode_is_last_prefill_row, pin_bwd_finite_differences, pin_bwd_autograd,
         pin_lambda_bwd, pin_paged_decode, pin_v2_paged_decode, pin_varlen, pin_varlen_qk,
-        pin_v2_varlen, pin_paged_prefill, pin_bwd_varlen, pin_gda, pin_gda_bwd, pin_gda_varlen,
+        pin_v2_varlen, pin_paged_prefill, pin_bwd_varlen, pin_gda, pin_gda_bwd, pin_gda_bwd_varlen, pin_gda_varlen,
         pin_gda_varlen_qk_and_paged, pin_gda_decode_paged, pin_gda_decode_is_last_prefill_row]
 
 
