@@ -868,7 +868,35 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                         "gda_prefill training: every gradient", world,
                                         flops_per_pair=gbwd_per_pair,
                                         fwd_train_ms=round(tf_["ms"], 4))
-        del ginp, gws, gdy, gw, gbws, ggrads, gsaved
+        del ginp, gws, gdy, gbws, ggrads, gsaved
+        torch.cuda.empty_cache()
+
+        # the grouped backward over the packed sequences of the varlen line
+        lens = varlen_lengths()
+        total, mx = int(sum(lens)), max(lens)
+        vin = make_gda_inputs(1, total, gc["Hs"], gc["Hn"], gc["d"], gc["dv"], seed=5400 + rank,
+                              device=dev)
+        q, k, v = vin.q[0], vin.k[0], vin.v[0]
+        vdy = make_dout(1, total, gc["Hs"], gc["dv"], seed=5407 + rank, device=dev)[0]
+        cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=dev)
+        _, o_pre, stats = da.diffattn_gda_fwd_train_varlen(q, k, v, cu, vin.lam, gc["Hs"], li_g,
+                                                           max_seqlen=mx, norm_weight=gw)
+        vbws = torch.empty(da.diffattn_gda_bwd_varlen_workspace_size(len(lens), mx, total,
+                                                                     gc["Hs"], gc["Hn"]),
+                           dtype=torch.uint8, device=dev)
+        vgrads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                      dlam=torch.empty(gc["Hs"], dtype=torch.float32, device=dev),
+                      dw=torch.empty(gc["dv"], dtype=torch.float32, device=dev))
+        t = timer(lambda: da.diffattn_gda_bwd_varlen(q, k, v, o_pre, stats, vdy, cu, vin.lam,
+                                                     gc["Hs"], li_g, max_seqlen=mx,
+                                                     norm_weight=gw, workspace=vbws,
+                                                     grads=vgrads), n_steps, status=status)
+        vpairs = float(sum(gc["Hs"] * causal_pairs(n) for n in lens))
+        r = tensor_roof(vpairs * gbwd_per_pair, t, peaks, peak_src)
+        extra["gda_backward_varlen"] = compact(r["achieved"], "TFLOP/s", t, r,
+                                               f"grouped backward over the {len(lens)} packed "
+                                               f"sequences", world, flops_per_pair=gbwd_per_pair)
+        del vin, q, k, v, vdy, o_pre, stats, vbws, vgrads, gw
         torch.cuda.empty_cache()
 
     # ======================= V2 decode =======================
