@@ -1,6 +1,6 @@
 """GPU parity at full size for the bench lines beyond the five base workloads: fp8 scores, the
-packed, chunked and paged prefills, the grouped packed prefill, the paged and fp8 decodes and the
-packed backward. Each runs
+packed, chunked and paged prefills, the grouped packed prefill, the paged and fp8 decodes, the
+packed backward and the grouped backward (batched and packed). Each runs
 in the launch configuration bench.py times. Inputs are drawn on the device; the float64 oracle
 recomputes sampled outputs. Where two entry points run the same arithmetic on the same data
 (paged against contiguous caches) the outputs must also be bit-identical."""
@@ -285,5 +285,77 @@ def test_bwd_varlen_full():
             for name in ("dq", "dk", "dv"):
                 assert_grad(g[name][None, s0:s0 + n, h:h + 1], want[name],
                             name=f"{name} seq{s} h{h}")
+    del inp, dy, o_pre, stats, g
+    torch.cuda.empty_cache()
+
+
+def _group_heads(grp, Hs, G):
+    """Signal heads of noise group grp, and those heads followed by its noise head."""
+    sig = list(range(grp * G, grp * G + G))
+    return sig, sig + [Hs + grp]
+
+
+def test_gda_bwd_3b_full():
+    """The bench's grouped training line (B4 N4096, 12 signal heads over 3 noise heads, noise
+    statistics through the workspace): every gradient of one group (signal heads 4-7 and noise
+    head 13) in sequence 2 against the oracle's grouped backward."""
+    B, N, Hs, Hn = 4, 4096, 12, 3
+    G = Hs // Hn
+    inp = make_gda_inputs(B, N, Hs, Hn, 128, 256, seed=5000, device=DEV)
+    dy = make_dout(B, N, Hs, 256, seed=5300, device=DEV)
+    li = da.diffattn_lambda_init(12)
+    w = torch.ones(256, dtype=torch.float32, device=DEV)
+    ws = torch.empty(da.diffattn_gda_fwd_workspace_size(B, N, Hs, Hn), dtype=torch.uint8,
+                     device=DEV)
+    _, o_pre, stats = da.diffattn_gda_fwd_train(inp.q, inp.k, inp.v, inp.lam, Hs, li,
+                                                norm_weight=w, workspace=ws)
+    g = da.diffattn_gda_bwd(inp.q, inp.k, inp.v, o_pre, stats, dy, inp.lam, Hs, li, norm_weight=w)
+    da.diffattn_device_status()
+    b = 2
+    sig, heads = _group_heads(1, Hs, G)
+    sl = lambda t, hs: t[b:b + 1][:, :, hs].cpu()
+    want = ref.diffattn_gda_bwd(sl(inp.q, heads), sl(inp.k, heads), sl(inp.v, sig),
+                                inp.lam.cpu().numpy()[sig], li, G, sl(dy, sig),
+                                norm_weight=np.ones(256))
+    for name, hs in (("dq", heads), ("dk", heads), ("dv", sig)):
+        for j, h in enumerate(hs):
+            assert_grad(g[name][b:b + 1, :, h:h + 1], want[name][:, :, j:j + 1],
+                        name=f"{name} b{b} h{h}")
+    del inp, dy, ws, o_pre, stats, g
+    torch.cuda.empty_cache()
+
+
+def test_gda_bwd_varlen_full():
+    """The bench's grouped packed backward (the 16 packed sequences, 12 signal heads over 3 noise
+    heads): every gradient of one group in a 2497-token sequence and of every group in the
+    shortest multi-token sequence against the oracle's grouped backward of that sequence."""
+    Hs, Hn = 12, 3
+    G = Hs // Hn
+    lens = varlen_lengths()
+    total = int(sum(lens))
+    inp = make_gda_inputs(1, total, Hs, Hn, 128, 256, seed=5400, device=DEV)
+    q, k, v = inp.q[0], inp.k[0], inp.v[0]
+    dy = make_dout(1, total, Hs, 256, seed=5407, device=DEV)[0]
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=DEV)
+    li = da.diffattn_lambda_init(12)
+    mx = max(lens)
+    _, o_pre, stats = da.diffattn_gda_fwd_train_varlen(q, k, v, cu, inp.lam, Hs, li, max_seqlen=mx)
+    g = da.diffattn_gda_bwd_varlen(q, k, v, o_pre, stats, dy, cu, inp.lam, Hs, li, max_seqlen=mx)
+    da.diffattn_device_status()
+    offs = np.concatenate([[0], np.cumsum(lens)])
+    lam = inp.lam.cpu().numpy()
+    long_s = lens.index(2497)
+    short = min((n, s) for s, n in enumerate(lens) if n >= 2)[1]
+    for s, groups in ((long_s, [2]), (short, range(Hn))):
+        s0, n = int(offs[s]), int(lens[s])
+        for grp in groups:
+            sig, heads = _group_heads(grp, Hs, G)
+            sl = lambda t, hs: t[None, s0:s0 + n][:, :, hs].cpu()
+            want = ref.diffattn_gda_bwd(sl(q, heads), sl(k, heads), sl(v, sig), lam[sig], li, G,
+                                        sl(dy, sig))
+            for name, hs in (("dq", heads), ("dk", heads), ("dv", sig)):
+                for j, h in enumerate(hs):
+                    assert_grad(g[name][None, s0:s0 + n, h:h + 1], want[name][:, :, j:j + 1],
+                                name=f"{name} seq{s} h{h}")
     del inp, dy, o_pre, stats, g
     torch.cuda.empty_cache()
