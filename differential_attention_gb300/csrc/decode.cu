@@ -123,7 +123,7 @@ __device__ __forceinline__ size_t cache_row(const DecSplitParams& p, int b, int 
 }
 
 template <bool kPaged>
-__global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecSplitParams p) {
+__global__ void __launch_bounds__(kDecThreads, kPaged ? 3 : 4) decode_split_kernel(const DecSplitParams p) {
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int L = p.seqlens ? p.seqlens[b] : p.Lmax;
