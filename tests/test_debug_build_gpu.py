@@ -5,8 +5,8 @@ tile coordinates of its TMA copies and every row it gathers or stores against th
 tensor, and reports a failed check through diffattn_device_status (DIFFATTN_ERR_INDEX) instead of
 touching memory outside the tensor. It stands in for a memory sanitizer. This test builds it and
 runs the small-case GPU suites -- every entry point on small, ragged and edge-case shapes
-(test_parity_gpu.py), the backward (test_backward_gpu.py), the grouped form (test_gda_gpu.py),
-non-finite inputs and guard bands around every output and workspace -- in a child process that
+(test_parity_gpu.py), the backward (test_backward_gpu.py), the grouped form and its training
+path (test_gda_gpu.py, test_gda_train_gpu.py), non-finite inputs and guard bands around every output and workspace -- in a child process that
 loads the debug build; each test checks against the float64 oracle and calls
 diffattn_device_status, and all must pass with no check failing.
 """
@@ -32,7 +32,8 @@ def test_parity_suite_under_the_debug_build():
     assert build.returncode == 0, build.stdout[-2000:] + build.stderr[-4000:]
     assert build.stdout.strip().endswith("libdiffattn_debug.so")
     suites = ["tests/test_parity_gpu.py", "tests/test_backward_gpu.py", "tests/test_gda_gpu.py",
-              "tests/test_nonfinite_gpu.py", "tests/test_guard_gpu.py"]
+              "tests/test_gda_train_gpu.py", "tests/test_nonfinite_gpu.py",
+              "tests/test_guard_gpu.py"]
     run = subprocess.run([sys.executable, "-m", "pytest", *suites, "-m", "gpu", "-x", "-q", "-p",
                           "no:cacheprovider"], cwd=ROOT, env=env, capture_output=True, text=True,
                          timeout=1800)
