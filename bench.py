@@ -728,7 +728,22 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                        issued_tflops=round(issued, 1),
                                        issued_flops_per_pair=issued_per_pair,
                                        one_launch_ms=round(t1["ms"], 4))
-        del ginp, gout
+
+        # the same heads with fp8 e4m3 q and k (one launch: each signal head forms its noise map)
+        q8, qs = to_fp8_e4m3(ginp.q)
+        k8, ks = to_fp8_e4m3(ginp.k)
+        t8 = timer(lambda: da.diffattn_gda_fwd_fp8(q8, k8, ginp.v, ginp.lam, gc["Hs"], qs, ks, li_g,
+                                                   out=gout),
+                   max(5, min(50, args.steps)), status=status)
+        # issued per (signal head, pair), as on the prefill_fp8 line: both maps' scores in both
+        # passes at the fp8 rate, the product with V at bf16 (1536 flops, blended peak 1.5x bf16)
+        r = tensor_roof(pairs * FLOPS_PER_PAIR, t8, peaks, peak_src, scale=1.5,
+                        what="scores at the fp8 rate (2x bf16, nominal ratio), V product at bf16",
+                        nominal_scale=1.5)
+        extra["gda_prefill_fp8"] = compact(r["achieved"], "TFLOP/s", t8, r,
+                                           "gda_prefill with fp8 e4m3 q and k (one launch)", world,
+                                           flops_per_pair=FLOPS_PER_PAIR)
+        del ginp, gout, q8, k8
         torch.cuda.empty_cache()
 
         # the last 1024-token chunk of each prompt against its 4096 keys, keys packed with offsets

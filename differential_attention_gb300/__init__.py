@@ -139,6 +139,9 @@ _SIGNATURES = {
     "diffattn_gda_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_float, ctypes.c_void_p,
                                                                  ctypes.c_float] + [ctypes.c_int] * 8
                          + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "diffattn_gda_fwd_fp8": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_float] * 2
+                             + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_float]
+                             + [ctypes.c_int] * 7 + [ctypes.c_void_p]),
     "diffattn_gda_fwd_varlen": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 2
                                 + [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
                                    ctypes.c_float] + [ctypes.c_int] * 7
@@ -1016,6 +1019,34 @@ def diffattn_gda_fwd_workspace_size(B: int, N: int, n_signal: int, n_noise: int,
     n = ctypes.c_size_t(0)
     _check(lib().diffattn_gda_fwd_workspace_size(B, N, n_signal, n_noise, d, dv, ctypes.byref(n)))
     return int(n.value)
+
+
+def diffattn_gda_fwd_fp8(q8, k8, v, lam, n_signal: int, q_descale: float, k_descale: float,
+                         lambda_init: float = 0.0, norm_weight=None, eps: float = 1e-5,
+                         causal: bool = True, norm: bool = True, scale: bool = True, out=None,
+                         stream=None):
+    """Grouped prefill with fp8 e4m3 q and k (real values q8 * q_descale, k8 * k_descale; the head
+    split of diffattn_gda_fwd) and bf16 v [B, N, n_signal, dv]: the score products run on the fp8
+    tensor cores."""
+    _dev("q8", q8, torch.float8_e4m3fn)
+    B, N, heads, d = q8.shape
+    n_noise = heads - int(n_signal)
+    _dev("k8", k8, torch.float8_e4m3fn)
+    _dev("v", v, torch.bfloat16)
+    if k8.shape != q8.shape or v.shape[:3] != (B, N, n_signal):
+        raise ValueError("k8 must match q8, and v must be [B, N, n_signal, dv]")
+    dv = v.shape[-1]
+    _dev("lam", lam, torch.float32)
+    if norm_weight is not None:
+        _dev("norm_weight", norm_weight, torch.float32)
+    if out is None:
+        out = torch.empty((B, N, int(n_signal), dv), dtype=torch.bfloat16, device=v.device)
+    _dev("out", out, torch.bfloat16)
+    _check(lib().diffattn_gda_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v), _ptr(out), float(q_descale),
+                                      float(k_descale), _ptr(lam), float(lambda_init),
+                                      _ptr(norm_weight), float(eps), B, N, int(n_signal), n_noise,
+                                      d, dv, _train_flags(causal, norm, scale), _stream(stream)))
+    return out
 
 
 def diffattn_gda_fwd(q, k, v, lam, n_signal: int, lambda_init: float = 0.0, norm_weight=None,

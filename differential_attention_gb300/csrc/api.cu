@@ -1585,6 +1585,60 @@ DIFFATTN_API int diffattn_gda_fwd(const void* q, const void* k, const void* v, v
   return run_prefill(p, dtype, fn, static_cast<cudaStream_t>(stream));
 }
 
+DIFFATTN_API int diffattn_gda_fwd_fp8(const void* q, const void* k, const void* v, void* out,
+                                      float q_descale, float k_descale, const float* lambda,
+                                      float lambda_init, const float* norm_weight, float eps,
+                                      int B, int N, int n_signal, int n_noise, int d, int dv,
+                                      int flags, void* stream) {
+  const char* fn = "diffattn_gda_fwd_fp8";
+  if (!q || !k || !v || !out || !lambda) return fail(DIFFATTN_ERR_ARG, "%s: null pointer", fn);
+  constexpr int kF8Flags = DIFFATTN_CAUSAL | DIFFATTN_NORM | DIFFATTN_SCALE;
+  if (flags & ~kF8Flags) return fail(DIFFATTN_ERR_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+  if ((flags & DIFFATTN_NORM) && !(eps > 0.f))
+    return fail(DIFFATTN_ERR_ARG, "%s: eps must be > 0 with DIFFATTN_NORM", fn);
+  if (!(q_descale > 0.f) || !(k_descale > 0.f) || !std::isfinite(q_descale) ||
+      !std::isfinite(k_descale))
+    return fail(DIFFATTN_ERR_ARG, "%s: descale factors must be finite and > 0", fn);
+  if (B < 1 || N < 1) return fail(DIFFATTN_ERR_SHAPE, "%s: B, N must be >= 1", fn);
+  if (int rc = check_groups(fn, n_signal, n_noise)) return rc;
+  if (d != 128 || dv != 256)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need d = 128 and dv = 256 (got d=%d dv=%d)", fn, d, dv);
+  const int heads = n_signal + n_noise;
+  const long long tiles = (static_cast<long long>(N) + 127) / 128 * B * n_signal;
+  if (tiles * 2 > 0x7fffffffLL || static_cast<long long>(N) * heads > (1LL << 30))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: problem too large for one launch", fn);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lambda, 4) || (norm_weight && !aligned(norm_weight, 16)))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  int rc = check_device();
+  if (rc) return rc;
+  da::Problem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.N = N;
+  p.units = n_signal;
+  p.dqk = d;
+  p.dv = dv;
+  p.mode = da::MODE_GDA;
+  p.q_heads = heads;
+  p.kv_heads = heads;
+  p.q_cols = d;
+  p.k_cols = d;
+  p.group = n_signal / n_noise;
+  p.lambda = lambda;
+  p.lam_logit = nullptr;
+  p.norm_w = norm_weight;
+  p.eps = eps;
+  p.lambda_init = lambda_init;
+  p.flags = flags;
+  p.scale = q_descale * k_descale / std::sqrt(static_cast<float>(d));
+  p.qk_fp8 = true;
+  return run_prefill(p, DIFFATTN_BF16, fn, static_cast<cudaStream_t>(stream));
+}
+
 DIFFATTN_API int diffattn_gda_fwd_train(const void* q, const void* k, const void* v, void* out,
                                         void* o_pre, float* stats, const float* lambda,
                                         float lambda_init, const float* norm_weight, float eps,

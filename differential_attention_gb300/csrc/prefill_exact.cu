@@ -914,8 +914,13 @@ static cudaError_t launch_cfg(const Problem& p, cudaStream_t s, char* err, size_
 cudaError_t status_prefill_exact(int* v) { return read_clear_status(v); }
 
 cudaError_t launch_prefill_exact(const Problem& p, cudaStream_t s, char* err, size_t err_len) {
-  if (p.mode == MODE_GDA) {  // grouped: batched, packed, keys of their own or paged; bf16 scores
-    if (p.qk_fp8) return cudaErrorNotSupported;
+  if (p.mode == MODE_GDA) {  // grouped: batched, packed, keys of their own or paged
+    if (p.qk_fp8) {  // fp8 scores: batched, one launch (each signal head forms its noise map)
+      if (p.dqk != 128 || p.dv != 256 || p.cu_seqlens) return cudaErrorNotSupported;
+      Problem q = p;
+      q.gda_phase = 0;
+      return exact::launch_cfg<128, 256, false, true, exact::kKeysShared, true>(q, s, err, err_len);
+    }
     const bool koff = p.cu_seqlens && p.cu_seqlens_k;
     const bool paged = p.cu_seqlens && p.block_table;
     if (p.dqk == 128 && p.dv == 256) {

@@ -655,6 +655,29 @@ DIFFATTN_API int diffattn_gda_fwd(const void* q, const void* k, const void* v, v
                                   int flags, int dtype, void* workspace, size_t ws_bytes,
                                   void* stream);
 
+/* Grouped prefill with fp8 scores: diffattn_gda_fwd where q and k hold fp8 e4m3 values with one
+ * dequantisation factor each (page "Differential Transformer: softmax can't say zero, so it
+ * subtracts": section "What other people found" for the grouped form, and its note on attention
+ * logits quantized to low bit widths for the fp8 score products).
+ *   q, k   : device fp8 e4m3 [B, N, n_signal + n_noise, d], the head split of diffattn_gda_fwd;
+ *            the real values are q * q_descale and k * k_descale (per tensor, finite, > 0)
+ *   v, out : device bf16 [B, N, n_signal, dv]
+ *   lambda, lambda_init, norm_weight, eps : as for diffattn_gda_fwd
+ * The score products run on the fp8 tensor cores (tcgen05 kind::f8f6f4, fp32 accumulation); the
+ * softmaxes, the subtraction, the product with V (bf16), the norm and the scale are those of
+ * diffattn_gda_fwd. One launch: each signal head's CTA forms its noise map's statistics itself.
+ * n_noise = n_signal is diffattn_fwd_fp8 with the halves of q and k stored as heads of their own.
+ * Supported: d = 128, dv = 256, n_signal a multiple of n_noise; flags DIFFATTN_CAUSAL |
+ * DIFFATTN_NORM | DIFFATTN_SCALE.
+ * Errors: ERR_ARG (null pointer, unknown flag, eps, descale factors), ERR_SHAPE, ERR_ALIGN,
+ * ERR_CUDA.
+ */
+DIFFATTN_API int diffattn_gda_fwd_fp8(const void* q, const void* k, const void* v, void* out,
+                                      float q_descale, float k_descale, const float* lambda,
+                                      float lambda_init, const float* norm_weight, float eps,
+                                      int B, int N, int n_signal, int n_noise, int d, int dv,
+                                      int flags, void* stream);
+
 /* Grouped prefill over packed sequences: diffattn_gda_fwd on sequences of different lengths
  * packed along the token axis (no padding), each attending only to itself, as
  * diffattn_fwd_varlen does for the ungrouped operator.

@@ -311,6 +311,18 @@ def test_fused_lambda_varlen_fp8_strided_validation(L):
     assert fp8(qd=float("inf")) == -1
     assert fp8(d=64) == -2
 
+    def gda_fp8(qd=1.0, d=128, ns=12, nn=3, flags=7, lam=FAKE, v=FAKE):
+        return L.diffattn_gda_fwd_fp8(FAKE, FAKE, v, FAKE, qd, 1.0, lam, 0.5, None, 1e-5, 2, 16,
+                                      ns, nn, d, 2 * d, flags, None)
+
+    assert gda_fp8(lam=None) == -1
+    assert gda_fp8(qd=-1.0) == -1
+    assert gda_fp8(qd=float("nan")) == -1
+    assert gda_fp8(flags=7 | 16) == -1       # only CAUSAL | NORM | SCALE
+    assert gda_fp8(d=64) == -2
+    assert gda_fp8(ns=12, nn=5) == -2        # signal heads not a multiple of noise heads
+    assert gda_fp8(v=ctypes.c_void_p(0x10008)) == -4
+
     def strided(st):
         arr = (ctypes.c_longlong * 12)(*st)
         return L.diffattn_fwd_strided(FAKE, FAKE, FAKE, FAKE, arr, FAKE, 0.5, None, 1e-5, 1, 16, 1,

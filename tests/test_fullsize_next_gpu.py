@@ -1,7 +1,7 @@
 """GPU parity at full size for the bench lines beyond the five base workloads: fp8 scores, the
-packed, chunked and paged prefills, the grouped packed prefill, the paged and fp8 decodes, the
-packed backward and the grouped backward (batched and packed). Each runs
-in the launch configuration bench.py times. Inputs are drawn on the device; the float64 oracle
+packed, chunked and paged prefills, the grouped packed and fp8 prefills, the paged and fp8
+decodes, the packed backward and the grouped backward (batched and packed). Each runs in the
+launch configuration bench.py times. Inputs are drawn on the device; the float64 oracle
 recomputes sampled outputs. Where two entry points run the same arithmetic on the same data
 (paged against contiguous caches) the outputs must also be bit-identical."""
 import numpy as np
@@ -127,6 +127,33 @@ def test_gda_varlen_full():
         want.append(w.reshape(-1, 256))
         got.append(out[torch.as_tensor(s0 + rows, device=DEV)].float().cpu().numpy().reshape(-1, 256))
     assert_bf16(np.concatenate(got), np.concatenate(want))
+
+
+def test_gda_fp8_full():
+    """The bench's grouped fp8 line (B4 N4096, 12 signal heads over 3 noise heads, fp8 e4m3 q and
+    k with per-tensor scales): sampled rows of every signal head of two sequences against the
+    oracle's grouped prefill on the dequantized values."""
+    B, N, Hs, Hn = 4, 4096, 12, 3
+    inp = make_gda_inputs(B, N, Hs, Hn, 128, 256, seed=5000, device=DEV)
+    q8, qs = to_fp8_e4m3(inp.q)
+    k8, ks = to_fp8_e4m3(inp.k)
+    li = da.diffattn_lambda_init(12)
+    out = da.diffattn_gda_fwd_fp8(q8, k8, inp.v, inp.lam, Hs, qs, ks, li)
+    da.diffattn_device_status()
+    rows = _rows(N, 32, 64, 5001)
+    lam = inp.lam.cpu().numpy()
+    got, want = [], []
+    for b in (1, 2):
+        for h in range(Hs):
+            sel = [h, Hs + h // (Hs // Hn)]
+            q = q8[b:b + 1, :, sel].cpu().double() * qs
+            k = k8[b:b + 1, :, sel].cpu().double() * ks
+            v = inp.v[b:b + 1, :, h:h + 1].cpu()
+            want.append(ref.diffattn_gda_fwd(q, k, v, lam[h:h + 1], li, 1, rows=rows)[0, :, 0])
+            got.append(out[b, torch.as_tensor(rows, device=DEV), h].float().cpu().numpy())
+    assert_bf16(np.stack(got), np.stack(want))
+    del inp, q8, k8, out
+    torch.cuda.empty_cache()
 
 
 def test_gda_chunk_and_paged_full():

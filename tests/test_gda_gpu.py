@@ -8,7 +8,7 @@ import torch
 
 import differential_attention_gb300 as da
 from oracle import diffattn_ref as ref
-from synth import make_gda_decode_inputs, make_gda_inputs
+from synth import make_gda_decode_inputs, make_gda_inputs, to_fp8_e4m3
 from tests.gpu_util import assert_bf16, assert_fp32
 
 pytestmark = pytest.mark.gpu
@@ -245,6 +245,48 @@ def test_gda_fwd_is_ungrouped_kernel_on_repeated_noise_heads():
     a = da.diffattn_gda_fwd(inp.q, inp.k, inp.v, inp.lam, Hs, 0.7, noise_pass=False)
     b = da.diffattn_fwd(q1, k1, inp.v, inp.lam, 0.7)
     torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# fp8 scores: (B, N, Hs, Hn, causal): one token, group sizes 1 to 4, ragged tails, full attention
+GDA_FP8_CASES = [(1, 1, 2, 1, True), (2, 300, 12, 3, True), (1, 645, 6, 2, True),
+                 (2, 129, 4, 4, False)]
+
+
+@pytest.mark.parametrize("B,N,Hs,Hn,causal", GDA_FP8_CASES)
+def test_gda_fwd_fp8(B, N, Hs, Hn, causal):
+    """fp8 e4m3 q and k with per-tensor descale factors: the oracle runs the grouped prefill on
+    exactly the dequantised fp8 values, so the bar is the bf16 prefill's."""
+    inp = make_gda_inputs(B, N, Hs, Hn, 128, 256, seed=401 + N + Hs)
+    q8, qs = to_fp8_e4m3(inp.q)
+    k8, ks = to_fp8_e4m3(inp.k)
+    li = ref.lambda_init(inp.layer)
+    w = _w(256)
+    got = da.diffattn_gda_fwd_fp8(q8.to(DEV), k8.to(DEV), inp.v.to(DEV), inp.lam.to(DEV), Hs, qs,
+                                  ks, li, norm_weight=w.to(DEV), causal=causal)
+    want = ref.diffattn_gda_fwd(q8.float() * qs, k8.float() * ks, inp.v, inp.lam, li, Hs,
+                                norm_weight=w, causal=causal)
+    assert_bf16(got, want)
+    da.diffattn_device_status()
+
+
+def test_gda_fwd_fp8_is_ungrouped_fp8_on_repeated_noise_heads():
+    """The grouped fp8 instantiation does the ungrouped fp8 prefill's arithmetic on a [Q1|Q2]
+    layout whose Q2/K2 repeat each noise head over its group: the outputs are bit-identical."""
+    B, N, Hs, Hn = 2, 260, 6, 2
+    inp = make_gda_inputs(B, N, Hs, Hn, 128, 256, seed=19, device=DEV)
+    q8, qs = to_fp8_e4m3(inp.q)
+    k8, ks = to_fp8_e4m3(inp.k)
+    rep = torch.arange(Hs, Hs + Hn, device=DEV).repeat_interleave(Hs // Hn)
+
+    def halves(t8):  # [Q1 of head h | Q2 of its noise head] per signal head, through byte views
+        u = t8.view(torch.uint8)
+        return torch.cat([u[:, :, :Hs], u[:, :, rep]], dim=-1).contiguous().view(torch.float8_e4m3fn)
+
+    a = da.diffattn_gda_fwd_fp8(q8, k8, inp.v, inp.lam, Hs, qs, ks, 0.7)
+    b = da.diffattn_fwd_fp8(halves(q8), halves(k8), inp.v, inp.lam, qs, ks, 0.7)
+    torch.cuda.synchronize()
+    da.diffattn_device_status()
     assert torch.equal(a, b)
 
 
